@@ -1,0 +1,216 @@
+"""Seeded synthetic inputs for the scan, shared by the tests and the benchmark.
+
+This module draws random numbers and lays them out; it holds none of the scan's
+arithmetic. Everything is generated on the CPU with a seeded
+``torch.Generator`` (one generator per call, tensors drawn in a fixed order), so
+the CUDA path and the oracle see bit-identical inputs.
+
+The named workloads follow the scalar benchmark shape of the
+"associative_scan_triton" README (performance: B=8, C=1536, seqlen from 128 to
+65536) and the block-matrix shape family of "Triton scan kernels" (Kernel
+design: one (b, n) lane per state block, (k, v) blocks):
+
+* ``single_sequence``  B=1, C=4, T=128, cu_seqlens=[0, 128], h0 = 0,
+  a ~ U(0,1), x ~ N(0,1), dh ~ N(0,1)
+* ``dense_4k``         [8, 1536, 4096] fp32, a ~ U(0,1), x ~ N(0,1),
+  h0 ~ N(0,1), dh ~ N(0,1)
+* ``dense_64k``        [8, 1536, 65536] fp32, a = sigmoid(z), z ~ N(2,1),
+  x ~ N(0,1), h0 = 0, dh ~ N(0,1)
+* ``packed_bidir``     C=2048, 64 sequences of length ~ U{512..8192} packed
+  with int32 cu_seqlens, bf16 a ~ U(0,1) and x ~ N(0,1) per branch, resets
+  (a = 0 at a packed position, all channels, both branches) with probability
+  1e-3, fp32 dh ~ N(0,1) per branch
+* ``affine_4x4``       B=8, T=4096, N=256, k=v=4, A = Q s with Q the
+  orthogonal factor of a 4x4 N(0,1) matrix and s ~ U(0.9, 1.0) per matrix,
+  B ~ N(0,1), h0 = 0, dH ~ N(0,1)
+* ``log_4k``           [8, 1536, 4096] fp32, log a = logsigmoid(z),
+  z ~ N(0,1), log x ~ N(0,1), no initial state, dh ~ N(0,1)
+
+Every generator takes a ``scale`` that shrinks the sizes for quick tests while
+keeping the distributions.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+@dataclass
+class ScalarWorkload:
+    """Inputs of one scalar scan problem (dense [B,C,T] or packed [C,T])."""
+
+    name: str
+    a: torch.Tensor
+    x: torch.Tensor
+    dh: torch.Tensor
+    h0: Optional[torch.Tensor] = None
+    cu_seqlens: Optional[torch.Tensor] = None
+    reverse: bool = False
+
+    @property
+    def n_elem(self) -> int:
+        return self.a.numel()
+
+
+@dataclass
+class BidirWorkload:
+    """Two independent branches over the same packed layout."""
+
+    name: str
+    af: torch.Tensor
+    xf: torch.Tensor
+    ar: torch.Tensor
+    xr: torch.Tensor
+    dhf: torch.Tensor
+    dhr: torch.Tensor
+    cu_seqlens: torch.Tensor
+    resets: torch.Tensor = field(default=None)
+    h0f: Optional[torch.Tensor] = None
+    h0r: Optional[torch.Tensor] = None
+
+    @property
+    def n_elem(self) -> int:
+        return self.af.numel() * 2
+
+
+@dataclass
+class AffineWorkload:
+    name: str
+    A: torch.Tensor
+    Bm: torch.Tensor
+    dH: torch.Tensor
+    h0: Optional[torch.Tensor] = None
+
+    @property
+    def n_blocks(self) -> int:
+        return self.A.shape[0] * self.A.shape[1] * self.A.shape[2]
+
+
+@dataclass
+class LogWorkload:
+    name: str
+    log_a: torch.Tensor
+    log_x: torch.Tensor
+    dh: torch.Tensor
+    log_h0: Optional[torch.Tensor] = None
+    cu_seqlens: Optional[torch.Tensor] = None
+
+    @property
+    def n_elem(self) -> int:
+        return self.log_a.numel()
+
+
+def scalar_dense(B: int, C: int, T: int, seed: int = 0, *, gate: str = "uniform",
+                 h0: bool = True, dtype=torch.float32, name: str = "dense") -> ScalarWorkload:
+    """Dense [B,C,T] inputs. gate: 'uniform' a~U(0,1); 'sigmoid2' a=sigmoid(N(2,1))."""
+    g = _gen(seed)
+    if gate == "uniform":
+        a = torch.rand((B, C, T), generator=g)
+    elif gate == "sigmoid2":
+        a = torch.sigmoid(torch.randn((B, C, T), generator=g) + 2.0)
+    else:
+        raise ValueError(gate)
+    x = torch.randn((B, C, T), generator=g)
+    h0t = torch.randn((B, C), generator=g) if h0 else None
+    dh = torch.randn((B, C, T), generator=g)
+    return ScalarWorkload(name, a.to(dtype), x.to(dtype), dh, h0t)
+
+
+def single_sequence(seed: int = 0) -> ScalarWorkload:
+    g = _gen(seed)
+    C, T = 4, 128
+    a = torch.rand((C, T), generator=g)
+    x = torch.randn((C, T), generator=g)
+    dh = torch.randn((C, T), generator=g)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    return ScalarWorkload("single_sequence", a, x, dh, None, cu)
+
+
+def dense_4k(seed: int = 0, scale: int = 1) -> ScalarWorkload:
+    return scalar_dense(8, 1536 // scale, 4096, seed, gate="uniform", h0=True, name="dense_4k")
+
+
+def dense_64k(seed: int = 0, scale: int = 1) -> ScalarWorkload:
+    return scalar_dense(8, 1536 // scale, 65536, seed, gate="sigmoid2", h0=False, name="dense_64k")
+
+
+def packed_lengths(n_seqs: int, lo: int, hi: int, g: torch.Generator) -> torch.Tensor:
+    """Integer lengths ~ U{lo..hi} (inclusive) and their exclusive cumsum."""
+    lens = torch.randint(lo, hi + 1, (n_seqs,), generator=g, dtype=torch.int64)
+    cu = torch.zeros(n_seqs + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(lens, 0)
+    return cu.to(torch.int32)
+
+
+def packed_bidir(seed: int = 0, C: int = 2048, n_seqs: int = 64, lo: int = 512, hi: int = 8192,
+                 p_reset: float = 1e-3, dtype=torch.bfloat16, h0: bool = False,
+                 name: str = "packed_bidir") -> BidirWorkload:
+    g = _gen(seed)
+    cu = packed_lengths(n_seqs, lo, hi, g)
+    T = int(cu[-1])
+    resets = torch.rand((T,), generator=g) < p_reset
+    keep = (~resets).to(torch.float32)
+
+    def gate():
+        return (torch.rand((C, T), generator=g) * keep).to(dtype)
+
+    af = gate()
+    xf = torch.randn((C, T), generator=g).to(dtype)
+    ar = gate()
+    xr = torch.randn((C, T), generator=g).to(dtype)
+    dhf = torch.randn((C, T), generator=g)
+    dhr = torch.randn((C, T), generator=g)
+    h0f = torch.randn((n_seqs, C), generator=g) if h0 else None
+    h0r = torch.randn((n_seqs, C), generator=g) if h0 else None
+    return BidirWorkload(name, af, xf, ar, xr, dhf, dhr, cu, resets, h0f, h0r)
+
+
+def _orthogonal_4x4(n: int, k: int, g: torch.Generator) -> torch.Tensor:
+    """Orthogonal factors of n random N(0,1) k x k matrices (Gram-Schmidt on columns)."""
+    M = torch.randn((n, k, k), generator=g, dtype=torch.float64)
+    Q = torch.empty_like(M)
+    for j in range(k):
+        v = M[:, :, j].clone()
+        for i in range(j):
+            v -= (Q[:, :, i] * M[:, :, j]).sum(-1, keepdim=True) * Q[:, :, i]
+        Q[:, :, j] = v / v.norm(dim=-1, keepdim=True)
+    return Q
+
+
+def affine(B: int, T: int, N: int, k: int, v: int, seed: int = 0, *, h0: bool = False,
+           name: str = "affine") -> AffineWorkload:
+    g = _gen(seed)
+    Q = _orthogonal_4x4(B * T * N, k, g)
+    s = torch.rand((B * T * N, 1, 1), generator=g, dtype=torch.float64) * 0.1 + 0.9
+    A = (Q * s).to(torch.float32).reshape(B, T, N, k, k)
+    Bm = torch.randn((B, T, N, k, v), generator=g)
+    dH = torch.randn((B, T, N, k, v), generator=g)
+    h0t = torch.randn((B, N, k, v), generator=g) if h0 else None
+    return AffineWorkload(name, A, Bm, dH, h0t)
+
+
+def affine_4x4(seed: int = 0, scale: int = 1) -> AffineWorkload:
+    return affine(8, 4096 // scale, 256, 4, 4, seed, name="affine_4x4")
+
+
+def log_dense(B: int, C: int, T: int, seed: int = 0, *, h0: bool = False,
+              name: str = "log") -> LogWorkload:
+    g = _gen(seed)
+    log_a = torch.nn.functional.logsigmoid(torch.randn((B, C, T), generator=g))
+    log_x = torch.randn((B, C, T), generator=g)
+    dh = torch.randn((B, C, T), generator=g)
+    lh0 = torch.randn((B, C), generator=g) if h0 else None
+    return LogWorkload(name, log_a, log_x, dh, lh0)
+
+
+def log_4k(seed: int = 0, scale: int = 1) -> LogWorkload:
+    return log_dense(8, 1536 // scale, 4096, seed, name="log_4k")

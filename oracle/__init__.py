@@ -1,0 +1,215 @@
+"""Sequential fp64 CPU oracle for the associative affine scan.
+
+TEST INFRASTRUCTURE ONLY. The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the CUDA library and
+its Python binding never do. It shares no code with the CUDA path: the
+arithmetic lives in ``oracle.c`` (plain C, double precision, one left-to-right
+loop per row, segment or lane), and this module only marshals numpy arrays.
+
+What each routine follows (page titles and sections of the source pages):
+
+* ``scan_fwd`` / ``scan_bwd``: "associative_scan_triton" README, quick start
+  (h[t] = g[t] * h[t-1] + x[t], cu_seqlens packing, bidirectional branches) and
+  how it works (reverse scan on shifted gates, d_gates = shifted_states *
+  d_tokens).
+* ``scan_log_fwd`` / ``scan_log_bwd``: "Triton scan kernels", One
+  associative-scan family (the same recurrence carried in log space).
+* ``affine_fwd`` / ``affine_bwd``: "Triton scan kernels", One associative-scan
+  family, Kernel design, and Autograd integration and the reversed-scan
+  backward (reverse scan with A_{t+1}^T).
+* ``chunk_summary`` / ``compose``: "Our RG-LRU GPU audit", Exact real chunk
+  algebra.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int32)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain cc, no CUDA)."""
+    stale = (not os.path.exists(_LIB) or
+             os.path.getmtime(_LIB) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["cc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            sig = {
+                "oracle_scan_fwd": [_dp, _dp, _dp, _ip, ctypes.c_int, _dp, _i64, _i64, _i64, ctypes.c_int],
+                "oracle_scan_bwd": [_dp, _dp, _dp, _ip, ctypes.c_int, _dp, _dp, _dp, _dp,
+                                    _i64, _i64, _i64, ctypes.c_int],
+                "oracle_scan_log_fwd": [_dp, _dp, _dp, _ip, ctypes.c_int, _dp, _i64, _i64, _i64,
+                                        ctypes.c_int],
+                "oracle_scan_log_bwd": [_dp, _dp, _dp, _ip, ctypes.c_int, _dp, _dp, _dp, _dp,
+                                        _i64, _i64, _i64, ctypes.c_int],
+                "oracle_affine_fwd": [_dp, _dp, _dp, _dp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int],
+                "oracle_affine_bwd": [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                      ctypes.c_int, ctypes.c_int],
+            }
+            for name, args in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            lib.oracle_chunk_summary.argtypes = [_dp, _dp, _i64, _dp, _dp]
+            lib.oracle_chunk_summary.restype = None
+            lib.oracle_compose.argtypes = [ctypes.c_double] * 4 + [_dp, _dp]
+            lib.oracle_compose.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f64(arr):
+    if arr is None:
+        return None
+    if hasattr(arr, "detach"):  # torch tensor -> numpy, values converted exactly
+        arr = arr.detach().cpu().double().numpy()
+    return np.ascontiguousarray(arr, dtype=np.float64)
+
+
+def _ptr(arr, typ=_dp):
+    return None if arr is None else arr.ctypes.data_as(typ)
+
+
+def _cu(cu_seqlens):
+    if cu_seqlens is None:
+        return None, 0
+    if hasattr(cu_seqlens, "detach"):
+        cu_seqlens = cu_seqlens.detach().cpu().numpy()
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    return cu, int(cu.shape[0]) - 1
+
+
+def _scalar_dims(a, cu):
+    if cu is None:
+        if a.ndim != 3:
+            raise ValueError("dense scalar scan expects [B, C, T]")
+        return a.shape
+    if a.ndim != 2:
+        raise ValueError("packed scalar scan expects [C, T]")
+    return (1,) + a.shape
+
+
+def scan_fwd(a, x, h0=None, cu_seqlens=None, reverse=False):
+    """h_t = a_t h_{t-1} + x_t (reverse: h_t = a_t h_{t+1} + x_t), fp64."""
+    a, x, h0 = _f64(a), _f64(x), _f64(h0)
+    cu, n = _cu(cu_seqlens)
+    B, C, T = _scalar_dims(a, cu)
+    h = np.empty_like(a)
+    rc = _load().oracle_scan_fwd(_ptr(a), _ptr(x), _ptr(h0), _ptr(cu, _ip), n, _ptr(h),
+                                 B, C, T, int(bool(reverse)))
+    if rc:
+        raise ValueError("oracle_scan_fwd: malformed arguments")
+    return h
+
+
+def scan_bwd(a, x, dh, h0=None, cu_seqlens=None, reverse=False):
+    """Returns (da, dx, dh0) of L = sum dh * h; dh0 has h0's layout."""
+    a, x, dh, h0 = _f64(a), _f64(x), _f64(dh), _f64(h0)
+    cu, n = _cu(cu_seqlens)
+    B, C, T = _scalar_dims(a, cu)
+    da = np.empty_like(a)
+    dx = np.empty_like(a)
+    dh0 = np.empty((n, C) if cu is not None else (B, C), dtype=np.float64)
+    rc = _load().oracle_scan_bwd(_ptr(a), _ptr(x), _ptr(h0), _ptr(cu, _ip), n, _ptr(dh),
+                                 _ptr(da), _ptr(dx), _ptr(dh0), B, C, T, int(bool(reverse)))
+    if rc:
+        raise ValueError("oracle_scan_bwd: malformed arguments")
+    return da, dx, dh0
+
+
+def scan_log_fwd(log_a, log_x, log_h0=None, cu_seqlens=None, reverse=False):
+    """h_t = exp(l_t), l_t = logaddexp(l_{t-1} + log_a_t, log_x_t), fp64."""
+    la, lx, lh0 = _f64(log_a), _f64(log_x), _f64(log_h0)
+    cu, n = _cu(cu_seqlens)
+    B, C, T = _scalar_dims(la, cu)
+    h = np.empty_like(la)
+    rc = _load().oracle_scan_log_fwd(_ptr(la), _ptr(lx), _ptr(lh0), _ptr(cu, _ip), n, _ptr(h),
+                                     B, C, T, int(bool(reverse)))
+    if rc:
+        raise ValueError("oracle_scan_log_fwd: malformed arguments")
+    return h
+
+
+def scan_log_bwd(log_a, log_x, dh, log_h0=None, cu_seqlens=None, reverse=False):
+    """Returns (dlog_a, dlog_x, dlog_h0) of L = sum dh * h for the log-space scan."""
+    la, lx, dh, lh0 = _f64(log_a), _f64(log_x), _f64(dh), _f64(log_h0)
+    cu, n = _cu(cu_seqlens)
+    B, C, T = _scalar_dims(la, cu)
+    dla = np.empty_like(la)
+    dlx = np.empty_like(la)
+    dlh0 = np.empty((n, C) if cu is not None else (B, C), dtype=np.float64)
+    rc = _load().oracle_scan_log_bwd(_ptr(la), _ptr(lx), _ptr(lh0), _ptr(cu, _ip), n, _ptr(dh),
+                                     _ptr(dla), _ptr(dlx), _ptr(dlh0), B, C, T,
+                                     int(bool(reverse)))
+    if rc:
+        raise ValueError("oracle_scan_log_bwd: malformed arguments")
+    return dla, dlx, dlh0
+
+
+def affine_fwd(A, Bm, h0=None):
+    """H_t = A_t H_{t-1} + B_t; A [B,T,N,k,k], Bm [B,T,N,k,v], h0 [B,N,k,v]."""
+    A, Bm, h0 = _f64(A), _f64(Bm), _f64(h0)
+    B, T, N, k, _ = A.shape
+    v = Bm.shape[-1]
+    H = np.empty_like(Bm)
+    rc = _load().oracle_affine_fwd(_ptr(A), _ptr(Bm), _ptr(h0), _ptr(H), B, T, N, k, v)
+    if rc:
+        raise ValueError("oracle_affine_fwd: malformed arguments")
+    return H
+
+
+def affine_bwd(A, Bm, dH, h0=None):
+    """Returns (dA, dB, dh0) of L = sum <dH_t, H_t>."""
+    A, Bm, dH, h0 = _f64(A), _f64(Bm), _f64(dH), _f64(h0)
+    B, T, N, k, _ = A.shape
+    v = Bm.shape[-1]
+    dA = np.empty_like(A)
+    dB = np.empty_like(Bm)
+    dh0 = np.empty((B, N, k, v), dtype=np.float64)
+    rc = _load().oracle_affine_bwd(_ptr(A), _ptr(Bm), _ptr(h0), _ptr(dH), _ptr(dA), _ptr(dB),
+                                   _ptr(dh0), B, T, N, k, v)
+    if rc:
+        raise ValueError("oracle_affine_bwd: malformed arguments")
+    return dA, dB, dh0
+
+
+def chunk_summary(a, x):
+    """(P, Q) of a run of scalar steps, built left to right."""
+    a, x = _f64(a), _f64(x)
+    P, Q = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_chunk_summary(_ptr(a), _ptr(x), a.shape[0], ctypes.byref(P), ctypes.byref(Q))
+    return P.value, Q.value
+
+
+def compose(s1, s2):
+    """Summary of "apply s1 then s2" for scalar summaries (P, Q)."""
+    P, Q = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_compose(s1[0], s1[1], s2[0], s2[1], ctypes.byref(P), ctypes.byref(Q))
+    return P.value, Q.value

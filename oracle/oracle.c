@@ -1,0 +1,381 @@
+/*
+ * oracle.c -- sequential fp64 CPU oracle for the associative affine scan.
+ *
+ * TEST INFRASTRUCTURE ONLY (see oracle.h): loaded by the tests, the package
+ * smoke check and the benchmark's CPU-baseline leg; never by the library.
+ * Parity with it is pinned, independently of this file, by closed forms,
+ * brute force on tiny inputs and invariants in tests/test_oracle_pins.py.
+ *
+ * Build: cc -O2 -ffp-contract=off -shared -fPIC oracle.c -lm
+ * (-ffp-contract=off keeps a*b + c as two rounded operations on every host,
+ * so x86-64 and aarch64 give the same bits.)
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* cu_seqlens follows the flash-attn convention named in the
+ * "associative_scan_triton" README ("how it works"): non-decreasing offsets
+ * from 0 to the packed length. Empty segments are allowed. */
+static int check_segments(const int32_t* cu, int n_seqs, int64_t B, int64_t T) {
+  if (!cu) return 0;
+  if (B != 1 || n_seqs < 1) return -1;
+  if (cu[0] != 0 || (int64_t)cu[n_seqs] != T) return -1;
+  for (int i = 0; i < n_seqs; ++i)
+    if (cu[i + 1] < cu[i]) return -1;
+  return 0;
+}
+
+/* Segment s of a row: [beg, end). Dense rows are one segment [0, T). */
+static void segment_bounds(const int32_t* cu, int s, int64_t T, int64_t* beg,
+                           int64_t* end) {
+  if (cu) {
+    *beg = cu[s];
+    *end = cu[s + 1];
+  } else {
+    *beg = 0;
+    *end = T;
+  }
+}
+
+/* Index of the initial state of segment s of row r: [B, C] dense, [n_seqs, C]
+ * packed (B == 1 there, so the row is the channel). */
+static int64_t h0_index(const int32_t* cu, int s, int64_t r, int64_t C) {
+  return cu ? (int64_t)s * C + r : r;
+}
+
+/* "associative_scan_triton" README, quick start: h[t] = g[t] * h[t-1] + x[t],
+ * each packed sequence scanned on its own; the reverse branch of
+ * scan_bidirectional_branched runs the same recurrence from the segment end. */
+int oracle_scan_fwd(const double* a, const double* x, const double* h0,
+                    const int32_t* cu, int n_seqs, double* h, int64_t B,
+                    int64_t C, int64_t T, int reverse) {
+  if (!a || !x || !h || B < 0 || C < 0 || T < 0) return -1;
+  if (check_segments(cu, n_seqs, B, T)) return -1;
+  const int64_t rows = B * C;
+  const int nseg = cu ? n_seqs : 1;
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* ar = a + r * T;
+    const double* xr = x + r * T;
+    double* hr = h + r * T;
+    for (int s = 0; s < nseg; ++s) {
+      int64_t beg, end;
+      segment_bounds(cu, s, T, &beg, &end);
+      double state = h0 ? h0[h0_index(cu, s, r, C)] : 0.0;
+      if (!reverse) {
+        for (int64_t t = beg; t < end; ++t) {
+          state = ar[t] * state + xr[t];
+          hr[t] = state;
+        }
+      } else {
+        for (int64_t t = end - 1; t >= beg; --t) {
+          state = ar[t] * state + xr[t];
+          hr[t] = state;
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+/* "associative_scan_triton" README, how it works: the backward computes
+ * d_tokens by a reverse scan on shifted gates and d_gates = shifted_states *
+ * d_tokens. For the causal branch the shifted gate of step t is a_{t+1} (zero
+ * past the segment end, so no gradient leaks between packed sequences) and the
+ * shifted state is h_{t-1} (h0 at the segment start); the reverse branch mirrors
+ * both shifts. The initial-state gradient ("Our RG-LRU GPU audit", fused path:
+ * "nonzero initial state and its gradient") is a_first * d_tokens_first. */
+int oracle_scan_bwd(const double* a, const double* x, const double* h0,
+                    const int32_t* cu, int n_seqs, const double* dh, double* da,
+                    double* dx, double* dh0, int64_t B, int64_t C, int64_t T,
+                    int reverse) {
+  if (!a || !x || !dh || !da || !dx || B < 0 || C < 0 || T < 0) return -1;
+  if (check_segments(cu, n_seqs, B, T)) return -1;
+  const int64_t rows = B * C;
+  const int nseg = cu ? n_seqs : 1;
+  double* hs = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+  if (!hs) return -1;
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* ar = a + r * T;
+    const double* xr = x + r * T;
+    const double* dhr = dh + r * T;
+    double* dar = da + r * T;
+    double* dxr = dx + r * T;
+    for (int s = 0; s < nseg; ++s) {
+      int64_t beg, end;
+      segment_bounds(cu, s, T, &beg, &end);
+      const double init = h0 ? h0[h0_index(cu, s, r, C)] : 0.0;
+      double d_init = 0.0;
+      if (!reverse) {
+        double state = init;
+        for (int64_t t = beg; t < end; ++t) {
+          state = ar[t] * state + xr[t];
+          hs[t] = state;
+        }
+        double g = 0.0;
+        for (int64_t t = end - 1; t >= beg; --t) {
+          const double shifted_gate = (t + 1 < end) ? ar[t + 1] : 0.0;
+          g = dhr[t] + shifted_gate * g;
+          dxr[t] = g;
+          const double shifted_state = (t > beg) ? hs[t - 1] : init;
+          dar[t] = shifted_state * g;
+        }
+        if (end > beg) d_init = ar[beg] * dxr[beg];
+      } else {
+        double state = init;
+        for (int64_t t = end - 1; t >= beg; --t) {
+          state = ar[t] * state + xr[t];
+          hs[t] = state;
+        }
+        double g = 0.0;
+        for (int64_t t = beg; t < end; ++t) {
+          const double shifted_gate = (t - 1 >= beg) ? ar[t - 1] : 0.0;
+          g = dhr[t] + shifted_gate * g;
+          dxr[t] = g;
+          const double shifted_state = (t + 1 < end) ? hs[t + 1] : init;
+          dar[t] = shifted_state * g;
+        }
+        if (end > beg) d_init = ar[end - 1] * dxr[end - 1];
+      }
+      if (dh0) dh0[h0_index(cu, s, r, C)] = d_init;
+    }
+  }
+  free(hs);
+  return 0;
+}
+
+/* log(exp(u) + exp(w)) with the larger term factored out; -inf is the
+ * additive identity (a zero term). */
+static double log_add_exp(double u, double w) {
+  if (u == -INFINITY) return w;
+  if (w == -INFINITY) return u;
+  const double m = u > w ? u : w;
+  return m + log1p(exp(-fabs(u - w)));
+}
+
+/* "Triton scan kernels", One associative-scan family: parallel_scan_log is the
+ * same recurrence carried in log space, writing h = exp(.) directly. Step by
+ * step, h_t = a_t h_{t-1} + x_t with a_t = exp(log_a_t), x_t = exp(log_x_t)
+ * reads l_t = log(exp(l_{t-1} + log_a_t) + exp(log_x_t)). */
+int oracle_scan_log_fwd(const double* log_a, const double* log_x,
+                        const double* log_h0, const int32_t* cu, int n_seqs,
+                        double* h, int64_t B, int64_t C, int64_t T,
+                        int reverse) {
+  if (!log_a || !log_x || !h || B < 0 || C < 0 || T < 0) return -1;
+  if (check_segments(cu, n_seqs, B, T)) return -1;
+  const int64_t rows = B * C;
+  const int nseg = cu ? n_seqs : 1;
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* la = log_a + r * T;
+    const double* lx = log_x + r * T;
+    double* hr = h + r * T;
+    for (int s = 0; s < nseg; ++s) {
+      int64_t beg, end;
+      segment_bounds(cu, s, T, &beg, &end);
+      double l = log_h0 ? log_h0[h0_index(cu, s, r, C)] : -INFINITY;
+      if (!reverse) {
+        for (int64_t t = beg; t < end; ++t) {
+          l = log_add_exp(l + la[t], lx[t]);
+          hr[t] = exp(l);
+        }
+      } else {
+        for (int64_t t = end - 1; t >= beg; --t) {
+          l = log_add_exp(l + la[t], lx[t]);
+          hr[t] = exp(l);
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+/* Gradient of the log-space scan by the chain rule through the linear adjoint:
+ * d log_a_t = da_t a_t, d log_x_t = dx_t x_t, d log_h0 = dh0 h0. */
+int oracle_scan_log_bwd(const double* log_a, const double* log_x,
+                        const double* log_h0, const int32_t* cu, int n_seqs,
+                        const double* dh, double* dlog_a, double* dlog_x,
+                        double* dlog_h0, int64_t B, int64_t C, int64_t T,
+                        int reverse) {
+  if (!log_a || !log_x || !dh || !dlog_a || !dlog_x || B < 0 || C < 0 || T < 0)
+    return -1;
+  if (check_segments(cu, n_seqs, B, T)) return -1;
+  const int64_t n = B * C * T;
+  const int64_t nh0 = cu ? (int64_t)n_seqs * C : B * C;
+  double* a = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double* x = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double* h0 = log_h0 ? (double*)malloc(sizeof(double) * (size_t)(nh0 > 0 ? nh0 : 1)) : NULL;
+  double* dh0 = (double*)malloc(sizeof(double) * (size_t)(nh0 > 0 ? nh0 : 1));
+  int rc = -1;
+  if (!a || !x || !dh0 || (log_h0 && !h0)) goto done;
+  for (int64_t i = 0; i < n; ++i) {
+    a[i] = exp(log_a[i]);
+    x[i] = exp(log_x[i]);
+  }
+  if (h0)
+    for (int64_t i = 0; i < nh0; ++i) h0[i] = exp(log_h0[i]);
+  rc = oracle_scan_bwd(a, x, h0, cu, n_seqs, dh, dlog_a, dlog_x, dh0, B, C, T,
+                       reverse);
+  if (rc) goto done;
+  for (int64_t i = 0; i < n; ++i) {
+    dlog_a[i] *= a[i];
+    dlog_x[i] *= x[i];
+  }
+  if (dlog_h0)
+    for (int64_t i = 0; i < nh0; ++i) dlog_h0[i] = h0 ? dh0[i] * h0[i] : 0.0;
+done:
+  free(a);
+  free(x);
+  free(h0);
+  free(dh0);
+  return rc;
+}
+
+/* "Triton scan kernels", One associative-scan family and Kernel design:
+ * h_t = A_t h_{t-1} + B_t with A_t a k x k matrix and B_t a k x v injection,
+ * one (b, n) lane walking T in order. Row-major matrices. */
+int oracle_affine_fwd(const double* A, const double* Bm, const double* h0,
+                      double* H, int64_t B, int64_t T, int64_t N, int k, int v) {
+  if (!A || !Bm || !H || B < 0 || T < 0 || N < 0 || k < 1 || v < 1 || k > 64 ||
+      v > 64)
+    return -1;
+  const int64_t kk = (int64_t)k * k, kv = (int64_t)k * v;
+  double* state = (double*)malloc(sizeof(double) * (size_t)kv);
+  double* next = (double*)malloc(sizeof(double) * (size_t)kv);
+  if (!state || !next) {
+    free(state);
+    free(next);
+    return -1;
+  }
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t n = 0; n < N; ++n) {
+      for (int64_t e = 0; e < kv; ++e)
+        state[e] = h0 ? h0[(b * N + n) * kv + e] : 0.0;
+      for (int64_t t = 0; t < T; ++t) {
+        const int64_t blk = (b * T + t) * N + n;
+        const double* At = A + blk * kk;
+        const double* Bt = Bm + blk * kv;
+        for (int i = 0; i < k; ++i) {
+          for (int j = 0; j < v; ++j) {
+            double acc = 0.0;
+            for (int l = 0; l < k; ++l) acc += At[i * k + l] * state[l * v + j];
+            next[i * v + j] = acc + Bt[i * v + j];
+          }
+        }
+        memcpy(state, next, sizeof(double) * (size_t)kv);
+        memcpy(H + blk * kv, state, sizeof(double) * (size_t)kv);
+      }
+    }
+  }
+  free(state);
+  free(next);
+  return 0;
+}
+
+/* "Triton scan kernels", Autograd integration and the reversed-scan backward:
+ * reverse-scan the output gradients with A_{t+1}^T (G_t = dH_t + A_{t+1}^T
+ * G_{t+1}), then dL/dB_t = G_t and dL/dA_t = G_t H_{t-1}^T from the forward
+ * states (H_{-1} = h0); dL/dh0 = A_0^T G_0. */
+int oracle_affine_bwd(const double* A, const double* Bm, const double* h0,
+                      const double* dH, double* dA, double* dB, double* dh0,
+                      int64_t B, int64_t T, int64_t N, int k, int v) {
+  if (!A || !Bm || !dH || !dA || !dB || B < 0 || T < 0 || N < 0 || k < 1 ||
+      v < 1 || k > 64 || v > 64)
+    return -1;
+  const int64_t kk = (int64_t)k * k, kv = (int64_t)k * v;
+  double* hs = (double*)malloc(sizeof(double) * (size_t)((T > 0 ? T : 1) * kv));
+  double* g = (double*)malloc(sizeof(double) * (size_t)kv);
+  double* gnew = (double*)malloc(sizeof(double) * (size_t)kv);
+  double* init = (double*)malloc(sizeof(double) * (size_t)kv);
+  if (!hs || !g || !gnew || !init) {
+    free(hs);
+    free(g);
+    free(gnew);
+    free(init);
+    return -1;
+  }
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t n = 0; n < N; ++n) {
+      for (int64_t e = 0; e < kv; ++e)
+        init[e] = h0 ? h0[(b * N + n) * kv + e] : 0.0;
+      /* forward states of this lane */
+      for (int64_t t = 0; t < T; ++t) {
+        const int64_t blk = (b * T + t) * N + n;
+        const double* At = A + blk * kk;
+        const double* Bt = Bm + blk * kv;
+        const double* prev = t > 0 ? hs + (t - 1) * kv : init;
+        for (int i = 0; i < k; ++i)
+          for (int j = 0; j < v; ++j) {
+            double acc = 0.0;
+            for (int l = 0; l < k; ++l) acc += At[i * k + l] * prev[l * v + j];
+            hs[t * kv + i * v + j] = acc + Bt[i * v + j];
+          }
+      }
+      /* reverse adjoint scan */
+      for (int64_t e = 0; e < kv; ++e) g[e] = 0.0;
+      for (int64_t t = T - 1; t >= 0; --t) {
+        const int64_t blk = (b * T + t) * N + n;
+        const double* dHt = dH + blk * kv;
+        for (int i = 0; i < k; ++i)
+          for (int j = 0; j < v; ++j) {
+            double acc = 0.0;
+            if (t + 1 < T) {
+              const double* An = A + ((b * T + t + 1) * N + n) * kk;
+              for (int l = 0; l < k; ++l) acc += An[l * k + i] * g[l * v + j];
+            }
+            gnew[i * v + j] = dHt[i * v + j] + acc;
+          }
+        memcpy(g, gnew, sizeof(double) * (size_t)kv);
+        memcpy(dB + blk * kv, g, sizeof(double) * (size_t)kv);
+        const double* prev = t > 0 ? hs + (t - 1) * kv : init;
+        double* dAt = dA + blk * kk;
+        for (int i = 0; i < k; ++i)
+          for (int l = 0; l < k; ++l) {
+            double acc = 0.0;
+            for (int j = 0; j < v; ++j) acc += g[i * v + j] * prev[l * v + j];
+            dAt[i * k + l] = acc;
+          }
+      }
+      if (dh0) {
+        double* d = dh0 + (b * N + n) * kv;
+        for (int i = 0; i < k; ++i)
+          for (int j = 0; j < v; ++j) {
+            double acc = 0.0;
+            if (T > 0) {
+              const double* A0 = A + ((b * T) * N + n) * kk;
+              for (int l = 0; l < k; ++l) acc += A0[l * k + i] * g[l * v + j];
+            }
+            d[i * v + j] = acc;
+          }
+      }
+    }
+  }
+  free(hs);
+  free(g);
+  free(gnew);
+  free(init);
+  return 0;
+}
+
+/* "Our RG-LRU GPU audit", Exact real chunk algebra: the summary of a chunk is
+ * h_out = P h_in + Q, updated left to right by P <- a_t P, Q <- a_t Q + b_t. */
+void oracle_chunk_summary(const double* a, const double* x, int64_t n,
+                          double* P, double* Q) {
+  double p = 1.0, q = 0.0;
+  for (int64_t t = 0; t < n; ++t) {
+    p = a[t] * p;
+    q = a[t] * q + x[t];
+  }
+  *P = p;
+  *Q = q;
+}
+
+/* "Triton scan kernels", One associative-scan family: "apply (A1, B1) then
+ * (A2, B2)" is the affine map h -> A2 (A1 h + B1) + B2 = (A2 A1) h + (A2 B1 + B2),
+ * a monoid with identity (I, 0). Scalar case. */
+void oracle_compose(double P1, double Q1, double P2, double Q2, double* P,
+                    double* Q) {
+  *P = P2 * P1;
+  *Q = P2 * Q1 + Q2;
+}

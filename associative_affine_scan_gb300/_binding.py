@@ -1,0 +1,440 @@
+"""ctypes binding of libscan (include/libscan.h).
+
+Argument marshalling only: every function checks shapes and dtypes of torch
+CUDA tensors, allocates the outputs with torch, passes raw device pointers and
+the current stream to the C entry point of the same name, and raises
+``ScanError`` on a non-zero status. All arithmetic runs in libscan's kernels.
+There is no fallback: if libscan.so is missing or no GPU is present, the call
+fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libscan.so")
+
+SCAN_OK = 0
+SCAN_ERR_INVALID_ARG = 1
+SCAN_ERR_UNSUPPORTED = 2
+SCAN_ERR_ALIGNMENT = 3
+SCAN_ERR_WORKSPACE = 4
+SCAN_ERR_CUDA = 5
+SCAN_ERR_TIMEOUT = 6
+SCAN_ERR_SEQLENS = 7
+
+SCAN_F32 = 0
+SCAN_BF16 = 1
+
+SCAN_VARIANT_AUTO = 0
+SCAN_VARIANT_STATIONARY = 1
+SCAN_VARIANT_LOOKBACK = 2
+
+SCAN_OP_FWD = 0
+SCAN_OP_BWD = 1
+SCAN_OP_BIDIR_FWD = 2
+SCAN_OP_BIDIR_BWD = 3
+SCAN_OP_LOG_FWD = 4
+SCAN_OP_AFFINE_FWD = 5
+SCAN_OP_AFFINE_BWD = 6
+
+EXPORTED = (
+    "scan_status_string", "scan_version", "scan_workspace_bytes", "scan_workspace_init",
+    "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
+    "scan_log_fwd", "affine_scan_fwd", "affine_scan_bwd",
+)
+
+
+class ScanError(RuntimeError):
+    """A libscan entry point returned a non-zero scan_status."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+class ScanOpts(ctypes.Structure):
+    _fields_ = [
+        ("variant", ctypes.c_int32),
+        ("chunk", ctypes.c_int32),
+        ("rows_per_cta", ctypes.c_int32),
+        ("test_stall", ctypes.c_int32),
+        ("wait_limit_s", ctypes.c_double),
+        ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_sz = ctypes.c_size_t
+_opt = ctypes.POINTER(ScanOpts)
+
+_SIGS = {
+    "scan_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "scan_version": ([], ctypes.c_int32),
+    "scan_workspace_bytes": ([ctypes.c_int, _i64, _i64, _i64, _i32, _i32, _opt], _sz),
+    "scan_workspace_init": ([_vp, _sz, _vp], ctypes.c_int),
+    "scan_get_device_status": ([_vp, _vp], ctypes.c_int),
+    "scan_fwd": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, ctypes.c_int, _i32, _opt,
+                  _vp, _sz, _vp], ctypes.c_int),
+    "scan_bwd": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int,
+                  _i32, _opt, _vp, _sz, _vp], ctypes.c_int),
+    "scan_bidir_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i64, _i64, _i64,
+                        ctypes.c_int, _opt, _vp, _sz, _vp], ctypes.c_int),
+    "scan_bidir_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
+                        _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _opt, _vp, _sz, _vp],
+                       ctypes.c_int),
+    "scan_log_fwd": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, _i32, _opt, _vp, _sz,
+                      _vp], ctypes.c_int),
+    "affine_scan_fwd": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _opt, _vp, _sz, _vp],
+                        ctypes.c_int),
+    "affine_scan_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _opt,
+                         _vp, _sz, _vp], ctypes.c_int),
+}
+
+_lock = threading.Lock()
+_lib_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libscan.so (raises if it has not been built)."""
+    global _lib_handle
+    if _lib_handle is None:
+        with _lock:
+            if _lib_handle is None:
+                if not os.path.exists(LIB_PATH):
+                    raise ImportError(
+                        f"{LIB_PATH} is missing: build it with "
+                        "`python -c 'import __graft_entry__ as g; g.build()'`")
+                h = ctypes.CDLL(LIB_PATH)
+                for name, (args, res) in _SIGS.items():
+                    fn = getattr(h, name)
+                    fn.argtypes = args
+                    fn.restype = res
+                _lib_handle = h
+    return _lib_handle
+
+
+def status_string(status: int) -> str:
+    return lib().scan_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != SCAN_OK:
+        raise ScanError(status, where)
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _opts(opts) -> Optional[ScanOpts]:
+    if opts is None:
+        return None
+    if isinstance(opts, ScanOpts):
+        return opts
+    o = ScanOpts()
+    for k, v in dict(opts).items():
+        if k == "cu_seqlens_host":
+            arr = (ctypes.c_int32 * len(v))(*[int(e) for e in v])
+            o._keep = arr  # keep the host copy alive for the call
+            o.cu_seqlens_host = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
+        else:
+            setattr(o, k, v)
+    return o
+
+
+def _optref(o: Optional[ScanOpts]):
+    return None if o is None else ctypes.byref(o)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SCAN_F32
+    if t.dtype == torch.bfloat16:
+        return SCAN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: fp32 or bf16 expected")
+
+
+def _need(t: Optional[torch.Tensor], name: str, *, dtype=None, shape=None, device=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _scalar_dims(a: torch.Tensor, cu_seqlens):
+    if cu_seqlens is None:
+        if a.dim() != 3:
+            raise ValueError("dense scan expects [B, C, T]")
+        return a.shape[0], a.shape[1], a.shape[2], 0
+    if a.dim() != 2:
+        raise ValueError("packed scan expects [C, T] with cu_seqlens")
+    _need(cu_seqlens, "cu_seqlens", dtype=torch.int32, device=a.device)
+    return 1, a.shape[0], a.shape[1], cu_seqlens.numel() - 1
+
+
+class _Workspaces:
+    """One zeroed workspace per (device, stream), grown on demand."""
+
+    def __init__(self):
+        self._buf = {}
+        self._lk = threading.Lock()
+
+    def get(self, nbytes: int, device: torch.device, stream: ctypes.c_void_p) -> torch.Tensor:
+        key = (device.index, stream.value)
+        with self._lk:
+            buf = self._buf.get(key)
+            if buf is None or buf.numel() < nbytes:
+                size = max(nbytes, 4096)
+                buf = torch.empty(size, dtype=torch.uint8, device=device)
+                _check(lib().scan_workspace_init(_ptr(buf), size, stream), "scan_workspace_init")
+                self._buf[key] = buf
+            return buf
+
+    def current(self, device, stream):
+        return self._buf.get((device.index, stream.value))
+
+
+_ws = _Workspaces()
+
+
+def workspace_for(op: int, B: int, C: int, T: int, k: int, v: int, opts, device, stream):
+    o = _opts(opts)
+    n = lib().scan_workspace_bytes(op, B, C, T, k, v, _optref(o))
+    if n == 0:
+        raise ScanError(SCAN_ERR_INVALID_ARG, "scan_workspace_bytes")
+    return _ws.get(n, device, stream), n, o
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def scan_version() -> int:
+    return int(lib().scan_version())
+
+
+def scan_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def scan_workspace_bytes(op: int, B: int, C: int, T: int, k: int = 0, v: int = 0, opts=None) -> int:
+    return int(lib().scan_workspace_bytes(op, B, C, T, k, v, _optref(_opts(opts))))
+
+
+def scan_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    """Zero a caller-owned workspace (a CUDA uint8 tensor) on `stream`."""
+    _need(workspace, "workspace")
+    _check(lib().scan_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream, workspace.device)), "scan_workspace_init")
+
+
+def scan_get_device_status(device=None, stream=None) -> int:
+    """Sticky device status of the workspace used on (device, stream); resets it."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    s = _stream(stream, device)
+    buf = _ws.current(device, s)
+    if buf is None:
+        return SCAN_OK
+    return int(lib().scan_get_device_status(_ptr(buf), s))
+
+
+def scan_fwd(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None, opts=None, stream=None):
+    """h_t = a_t h_{t-1} + x_t (reverse: h_t = a_t h_{t+1} + x_t). Returns h (fp32)."""
+    _need(a, "a")
+    dev = a.device
+    dt = _dtype_code(a)
+    B, C, T, n = _scalar_dims(a, cu_seqlens)
+    _need(x, "x", dtype=a.dtype, shape=a.shape, device=dev)
+    _need(h0, "h0", dtype=torch.float32, shape=(n, C) if cu_seqlens is not None else (B, C),
+          device=dev)
+    h = out if out is not None else torch.empty(a.shape, dtype=torch.float32, device=dev)
+    _need(h, "out", dtype=torch.float32, shape=a.shape, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_FWD, B, C, T, 0, 0, opts, dev, s)
+    st = lib().scan_fwd(_ptr(a), _ptr(x), _ptr(h0), _ptr(cu_seqlens), n, _ptr(h), B, C, T, dt,
+                        int(bool(reverse)), _optref(o), _ptr(ws), ws.numel(), s)
+    _check(st, "scan_fwd")
+    return h
+
+
+def scan_bwd(a, h, dh, h0=None, cu_seqlens=None, reverse=False, *, out=None, opts=None,
+             stream=None, need_dh0=True):
+    """Backward of L = sum dh * h. Returns (da, dx, dh0) with da, dx in a's dtype."""
+    _need(a, "a")
+    dev = a.device
+    dt = _dtype_code(a)
+    B, C, T, n = _scalar_dims(a, cu_seqlens)
+    _need(h, "h", dtype=torch.float32, shape=a.shape, device=dev)
+    _need(dh, "dh", dtype=torch.float32, shape=a.shape, device=dev)
+    h0_shape = (n, C) if cu_seqlens is not None else (B, C)
+    _need(h0, "h0", dtype=torch.float32, shape=h0_shape, device=dev)
+    if out is not None:
+        da, dx, dh0 = out
+    else:
+        da = torch.empty_like(a)
+        dx = torch.empty_like(a)
+        dh0 = torch.empty(h0_shape, dtype=torch.float32, device=dev) if need_dh0 else None
+    _need(da, "da", dtype=a.dtype, shape=a.shape, device=dev)
+    _need(dx, "dx", dtype=a.dtype, shape=a.shape, device=dev)
+    _need(dh0, "dh0", dtype=torch.float32, shape=h0_shape, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_BWD, B, C, T, 0, 0, opts, dev, s)
+    st = lib().scan_bwd(_ptr(a), _ptr(h), _ptr(dh), _ptr(h0), _ptr(cu_seqlens), n, _ptr(da),
+                        _ptr(dx), _ptr(dh0), B, C, T, dt, int(bool(reverse)), _optref(o),
+                        _ptr(ws), ws.numel(), s)
+    _check(st, "scan_bwd")
+    return da, dx, dh0
+
+
+def scan_bidir_fwd(af, xf, ar, xr, h0f=None, h0r=None, cu_seqlens=None, *, out=None, opts=None,
+                   stream=None):
+    """Causal branch over (af, xf) and reverse branch over (ar, xr). Returns (hf, hr)."""
+    _need(af, "af")
+    dev = af.device
+    dt = _dtype_code(af)
+    B, C, T, n = _scalar_dims(af, cu_seqlens)
+    for t, nm in ((xf, "xf"), (ar, "ar"), (xr, "xr")):
+        _need(t, nm, dtype=af.dtype, shape=af.shape, device=dev)
+    h0_shape = (n, C) if cu_seqlens is not None else (B, C)
+    _need(h0f, "h0f", dtype=torch.float32, shape=h0_shape, device=dev)
+    _need(h0r, "h0r", dtype=torch.float32, shape=h0_shape, device=dev)
+    if out is not None:
+        hf, hr = out
+    else:
+        hf = torch.empty(af.shape, dtype=torch.float32, device=dev)
+        hr = torch.empty(af.shape, dtype=torch.float32, device=dev)
+    _need(hf, "hf", dtype=torch.float32, shape=af.shape, device=dev)
+    _need(hr, "hr", dtype=torch.float32, shape=af.shape, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_BIDIR_FWD, B, C, T, 0, 0, opts, dev, s)
+    st = lib().scan_bidir_fwd(_ptr(af), _ptr(xf), _ptr(ar), _ptr(xr), _ptr(h0f), _ptr(h0r),
+                              _ptr(cu_seqlens), n, _ptr(hf), _ptr(hr), B, C, T, dt, _optref(o),
+                              _ptr(ws), ws.numel(), s)
+    _check(st, "scan_bidir_fwd")
+    return hf, hr
+
+
+def scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, h0f=None, h0r=None, cu_seqlens=None, *, out=None,
+                   opts=None, stream=None):
+    """Backward of both branches. Returns (daf, dxf, dh0f, dar, dxr, dh0r)."""
+    _need(af, "af")
+    dev = af.device
+    dt = _dtype_code(af)
+    B, C, T, n = _scalar_dims(af, cu_seqlens)
+    _need(ar, "ar", dtype=af.dtype, shape=af.shape, device=dev)
+    for t, nm in ((hf, "hf"), (dhf, "dhf"), (hr, "hr"), (dhr, "dhr")):
+        _need(t, nm, dtype=torch.float32, shape=af.shape, device=dev)
+    h0_shape = (n, C) if cu_seqlens is not None else (B, C)
+    _need(h0f, "h0f", dtype=torch.float32, shape=h0_shape, device=dev)
+    _need(h0r, "h0r", dtype=torch.float32, shape=h0_shape, device=dev)
+    if out is not None:
+        daf, dxf, dh0f, dar, dxr, dh0r = out
+    else:
+        daf, dxf, dar, dxr = (torch.empty_like(af) for _ in range(4))
+        dh0f = torch.empty(h0_shape, dtype=torch.float32, device=dev)
+        dh0r = torch.empty(h0_shape, dtype=torch.float32, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_BIDIR_BWD, B, C, T, 0, 0, opts, dev, s)
+    st = lib().scan_bidir_bwd(_ptr(af), _ptr(hf), _ptr(dhf), _ptr(h0f), _ptr(ar), _ptr(hr),
+                              _ptr(dhr), _ptr(h0r), _ptr(cu_seqlens), n, _ptr(daf), _ptr(dxf),
+                              _ptr(dh0f), _ptr(dar), _ptr(dxr), _ptr(dh0r), B, C, T, dt,
+                              _optref(o), _ptr(ws), ws.numel(), s)
+    _check(st, "scan_bidir_bwd")
+    return daf, dxf, dh0f, dar, dxr, dh0r
+
+
+def scan_log_fwd(log_a, log_x, log_h0=None, cu_seqlens=None, reverse=False, *, out=None, opts=None,
+                 stream=None):
+    """h_t = exp(l_t), l_t = log(exp(l_{t-1} + log_a_t) + exp(log_x_t)). Returns h (fp32)."""
+    _need(log_a, "log_a", dtype=torch.float32)
+    dev = log_a.device
+    B, C, T, n = _scalar_dims(log_a, cu_seqlens)
+    _need(log_x, "log_x", dtype=torch.float32, shape=log_a.shape, device=dev)
+    _need(log_h0, "log_h0", dtype=torch.float32,
+          shape=(n, C) if cu_seqlens is not None else (B, C), device=dev)
+    h = out if out is not None else torch.empty(log_a.shape, dtype=torch.float32, device=dev)
+    _need(h, "out", dtype=torch.float32, shape=log_a.shape, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_LOG_FWD, B, C, T, 0, 0, opts, dev, s)
+    st = lib().scan_log_fwd(_ptr(log_a), _ptr(log_x), _ptr(log_h0), _ptr(cu_seqlens), n, _ptr(h),
+                            B, C, T, int(bool(reverse)), _optref(o), _ptr(ws), ws.numel(), s)
+    _check(st, "scan_log_fwd")
+    return h
+
+
+def _affine_dims(A, Bm):
+    if A.dim() != 5 or Bm.dim() != 5:
+        raise ValueError("affine scan expects A [B,T,N,k,k] and Bm [B,T,N,k,v]")
+    B, T, N, k, k2 = A.shape
+    if k2 != k or tuple(Bm.shape[:4]) != (B, T, N, k):
+        raise ValueError("affine scan: A [B,T,N,k,k] and Bm [B,T,N,k,v] disagree")
+    return B, T, N, k, Bm.shape[4]
+
+
+def affine_scan_fwd(A, Bm, h0=None, *, out=None, opts=None, stream=None):
+    """H_t = A_t H_{t-1} + B_t. Returns H [B,T,N,k,v] (fp32)."""
+    _need(A, "A", dtype=torch.float32)
+    dev = A.device
+    _need(Bm, "Bm", dtype=torch.float32, device=dev)
+    B, T, N, k, v = _affine_dims(A, Bm)
+    _need(h0, "h0", dtype=torch.float32, shape=(B, N, k, v), device=dev)
+    H = out if out is not None else torch.empty(Bm.shape, dtype=torch.float32, device=dev)
+    _need(H, "out", dtype=torch.float32, shape=Bm.shape, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_AFFINE_FWD, B, N, T, k, v, opts, dev, s)
+    st = lib().affine_scan_fwd(_ptr(A), _ptr(Bm), _ptr(h0), _ptr(H), B, T, N, k, v, _optref(o),
+                               _ptr(ws), ws.numel(), s)
+    _check(st, "affine_scan_fwd")
+    return H
+
+
+def affine_scan_bwd(A, H, dH, h0=None, *, out=None, opts=None, stream=None):
+    """Backward of L = sum <dH_t, H_t>. Returns (dA, dB, dh0)."""
+    _need(A, "A", dtype=torch.float32)
+    dev = A.device
+    _need(H, "H", dtype=torch.float32, device=dev)
+    B, T, N, k, v = _affine_dims(A, H)
+    _need(dH, "dH", dtype=torch.float32, shape=H.shape, device=dev)
+    _need(h0, "h0", dtype=torch.float32, shape=(B, N, k, v), device=dev)
+    if out is not None:
+        dA, dB, dh0 = out
+    else:
+        dA = torch.empty_like(A)
+        dB = torch.empty_like(H)
+        dh0 = torch.empty((B, N, k, v), dtype=torch.float32, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_AFFINE_BWD, B, N, T, k, v, opts, dev, s)
+    st = lib().affine_scan_bwd(_ptr(A), _ptr(H), _ptr(dH), _ptr(h0), _ptr(dA), _ptr(dB),
+                               _ptr(dh0), B, T, N, k, v, _optref(o), _ptr(ws), ws.numel(), s)
+    _check(st, "affine_scan_bwd")
+    return dA, dB, dh0

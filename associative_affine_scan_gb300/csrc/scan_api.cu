@@ -1,0 +1,375 @@
+// scan_api.cu -- the C ABI of libscan: argument checks, the per-shape planner,
+// workspace sizing and kernel launches. See include/libscan.h for the contract.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/libscan.h"
+#include "scan_internal.h"
+
+using namespace scan;
+
+namespace {
+
+constexpr int64_t kMaxGrid = 0x7fffffffLL;
+
+__global__ void fill_zero_kernel(float* p, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0.f;
+}
+
+bool aligned(const void* p, size_t a) { return p == nullptr || ((uintptr_t)p % a) == 0; }
+
+scan_opts defaults(const scan_opts* o) {
+  scan_opts d;
+  std::memset(&d, 0, sizeof(d));
+  if (o) d = *o;
+  return d;
+}
+
+unsigned long long wait_ns(const scan_opts& o) {
+  const double s = o.wait_limit_s > 0 ? o.wait_limit_s : 1.0;
+  const double ns = s * 1e9;
+  return ns > 1.8e19 ? 18000000000000000000ULL : (unsigned long long)ns;
+}
+
+int chunk_to_j(int chunk) {
+  switch (chunk) {
+    case 128: return 1;
+    case 256: return 2;
+    case 512: return 4;
+    case 1024: return 8;
+    default: return 0;
+  }
+}
+
+// Per-shape plan for the scalar and log forms. rows = B*C (dense) or C (packed);
+// nbr = number of branches launched together.
+scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const scan_opts& o,
+                        ScalarPlan* pl) {
+  if (rows < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
+  int J;
+  if (o.chunk) {
+    J = chunk_to_j(o.chunk);
+    if (!J) return SCAN_ERR_INVALID_ARG;
+  } else {
+    J = T <= 128 ? 1 : (T <= 256 ? 2 : 4);
+  }
+  int R = o.rows_per_cta;
+  if (R < 0 || R > 8) return SCAN_ERR_INVALID_ARG;
+  if (R == 0) R = rows < 8 ? (int)(rows > 0 ? rows : 1) : 8;
+  const int64_t L = 128LL * J;
+  // the vectorised path shifts each row by up to 3 elements
+  const int64_t span = T + ((T % 4) ? 3 : 0);
+  const int64_t M = T > 0 ? (span + L - 1) / L : 0;
+  const int64_t G = (rows + R - 1) / R;
+  int variant = o.variant;
+  if (variant < 0 || variant > 2) return SCAN_ERR_INVALID_ARG;
+  if (variant == SCAN_VARIANT_AUTO) variant = VAR_LOOKBACK;
+  const int64_t tiles = M * G * nbr;
+  if (M > kMaxGrid || G > kMaxGrid || tiles > kMaxGrid || rows * M * nbr > (1LL << 40))
+    return SCAN_ERR_UNSUPPORTED;
+  pl->variant = variant;
+  pl->J = J;
+  pl->R = R;
+  pl->M = (int)M;
+  pl->G = (int)G;
+  pl->vec = true;
+  pl->ws_bytes = kWsHeaderBytes +
+                 (variant == VAR_LOOKBACK ? (size_t)(nbr * rows * M) * 16u : (size_t)0);
+  if (varlen) {
+    const int WL = (int)L + 8;
+    const int nwords = (WL + 31) / 32;
+    pl->smem = 4u * (size_t)((nwords + 3) & ~3) + 8u * (size_t)WL;
+  } else {
+    pl->smem = 0;
+  }
+  return SCAN_OK;
+}
+
+scan_status check_host_cu(const int32_t* cu, int32_t n, int64_t T) {
+  if (!cu) return SCAN_OK;
+  if (cu[0] != 0 || (int64_t)cu[n] != T) return SCAN_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i)
+    if (cu[i + 1] < cu[i]) return SCAN_ERR_INVALID_ARG;
+  return SCAN_OK;
+}
+
+// Shared front end of the scalar/log entry points: shape checks, plan,
+// workspace check, base parameters.
+scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t n_seqs, int nbr,
+                    const scan_opts& o, void* ws, size_t ws_bytes, ScalarParams* p,
+                    ScalarPlan* pl) {
+  if (B < 0 || C < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
+  if (cu) {
+    if (B != 1 || n_seqs < 1 || T > 0x7fffffffLL) return SCAN_ERR_INVALID_ARG;
+    if (o.cu_seqlens_host) {
+      const scan_status st = check_host_cu(o.cu_seqlens_host, n_seqs, T);
+      if (st != SCAN_OK) return st;
+    }
+  }
+  const int64_t rows = B * C;
+  scan_status st = plan_scalar(rows, T, nbr, cu != nullptr, o, pl);
+  if (st != SCAN_OK) return st;
+  if (!ws) return SCAN_ERR_WORKSPACE;
+  if (ws_bytes < pl->ws_bytes || !aligned(ws, 16)) return SCAN_ERR_WORKSPACE;
+  std::memset(p, 0, sizeof(*p));
+  p->cu = cu;
+  p->n_seqs = cu ? n_seqs : 1;
+  p->nbr = nbr;
+  p->rows = rows;
+  p->T = T;
+  p->M = pl->M;
+  p->G = pl->G;
+  p->R = pl->R;
+  p->ntiles = (int64_t)pl->M * pl->G * nbr;
+  p->hdr = static_cast<WsHeader*>(ws);
+  p->recs = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(ws) +
+                                                  kWsHeaderBytes);
+  p->wait_limit_ns = wait_ns(o);
+  p->test_stall = o.test_stall;
+  return SCAN_OK;
+}
+
+scan_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA; }
+
+// dh0 when there is nothing to scan: every initial-state gradient is 0.
+scan_status zero_dh0(float* dh0, int64_t n, cudaStream_t s) {
+  if (!dh0 || n <= 0) return SCAN_OK;
+  return from_cuda(launch_fill_zero(dh0, n, s));
+}
+
+size_t elt(scan_dtype dt) { return dt == SCAN_BF16 ? 2 : 4; }
+
+}  // namespace
+
+namespace scan {
+cudaError_t launch_fill_zero(float* p, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+  fill_zero_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, n);
+  return cudaGetLastError();
+}
+}  // namespace scan
+
+extern "C" {
+
+const char* scan_status_string(scan_status s) {
+  switch (s) {
+    case SCAN_OK: return "SCAN_OK";
+    case SCAN_ERR_INVALID_ARG: return "SCAN_ERR_INVALID_ARG: malformed argument";
+    case SCAN_ERR_UNSUPPORTED: return "SCAN_ERR_UNSUPPORTED: outside the supported envelope";
+    case SCAN_ERR_ALIGNMENT: return "SCAN_ERR_ALIGNMENT: misaligned pointer";
+    case SCAN_ERR_WORKSPACE: return "SCAN_ERR_WORKSPACE: workspace missing or too small";
+    case SCAN_ERR_CUDA: return "SCAN_ERR_CUDA: CUDA runtime error";
+    case SCAN_ERR_TIMEOUT: return "SCAN_ERR_TIMEOUT: a look-back wait expired on the device";
+    case SCAN_ERR_SEQLENS: return "SCAN_ERR_SEQLENS: cu_seqlens is not 0 <= ... <= T";
+    default: return "unknown scan_status";
+  }
+}
+
+int32_t scan_version(void) { return LIBSCAN_VERSION; }
+
+size_t scan_workspace_bytes(scan_op op, int64_t B, int64_t C, int64_t T, int32_t k, int32_t v,
+                            const scan_opts* opts) {
+  const scan_opts o = defaults(opts);
+  if (B < 0 || C < 0 || T < 0) return 0;
+  ScalarPlan pl;
+  switch (op) {
+    case SCAN_OP_FWD:
+    case SCAN_OP_BWD:
+    case SCAN_OP_LOG_FWD:
+      return plan_scalar(B * C, T, 1, false, o, &pl) == SCAN_OK ? pl.ws_bytes : 0;
+    case SCAN_OP_BIDIR_FWD:
+    case SCAN_OP_BIDIR_BWD:
+      return plan_scalar(B * C, T, 2, false, o, &pl) == SCAN_OK ? pl.ws_bytes : 0;
+    case SCAN_OP_AFFINE_FWD:
+    case SCAN_OP_AFFINE_BWD:
+      (void)k;
+      (void)v;
+      return kWsHeaderBytes;
+    default:
+      return 0;
+  }
+}
+
+scan_status scan_workspace_init(void* ws, size_t bytes, cudaStream_t stream) {
+  if (!ws || bytes < kWsHeaderBytes) return SCAN_ERR_WORKSPACE;
+  return from_cuda(cudaMemsetAsync(ws, 0, bytes, stream));
+}
+
+scan_status scan_get_device_status(void* ws, cudaStream_t stream) {
+  if (!ws) return SCAN_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SCAN_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SCAN_ERR_CUDA;
+  if (h.status != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(static_cast<unsigned char*>(ws) + offsetof(WsHeader, status), &zero,
+                   sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return SCAN_ERR_CUDA;
+  }
+  return (scan_status)h.status;
+}
+
+scan_status scan_fwd(const void* a, const void* x, const float* h0, const int32_t* cu,
+                     int32_t n_seqs, float* h, int64_t B, int64_t C, int64_t T, scan_dtype dt,
+                     int32_t reverse, const scan_opts* opts, void* ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+  if (dt != SCAN_F32 && dt != SCAN_BF16) return SCAN_ERR_INVALID_ARG;
+  const scan_opts o = defaults(opts);
+  ScalarParams p;
+  ScalarPlan pl;
+  scan_status st = prepare(B, C, T, cu, n_seqs, 1, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  if (p.rows * T == 0) return SCAN_OK;
+  if (!a || !x || !h) return SCAN_ERR_INVALID_ARG;
+  pl.vec = aligned(a, 4 * elt(dt)) && aligned(x, 4 * elt(dt)) && aligned(h, 16);
+  p.br[0].a = a;
+  p.br[0].x = x;
+  p.br[0].h0 = h0;
+  p.br[0].out_h = h;
+  p.br[0].dir = reverse ? -1 : 1;
+  return from_cuda(dt == SCAN_F32 ? launch_scalar_fwd_f32(p, pl, stream)
+                                  : launch_scalar_fwd_bf16(p, pl, stream));
+}
+
+scan_status scan_bwd(const void* a, const float* h, const float* dh, const float* h0,
+                     const int32_t* cu, int32_t n_seqs, void* da, void* dx, float* dh0,
+                     int64_t B, int64_t C, int64_t T, scan_dtype dt, int32_t reverse,
+                     const scan_opts* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (dt != SCAN_F32 && dt != SCAN_BF16) return SCAN_ERR_INVALID_ARG;
+  const scan_opts o = defaults(opts);
+  ScalarParams p;
+  ScalarPlan pl;
+  scan_status st = prepare(B, C, T, cu, n_seqs, 1, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  const int64_t n_h0 = cu ? (int64_t)n_seqs * C : B * C;
+  if (p.rows * T == 0) return zero_dh0(dh0, n_h0, stream);
+  if (!a || !h || !dh || !da || !dx) return SCAN_ERR_INVALID_ARG;
+  pl.vec = aligned(a, 4 * elt(dt)) && aligned(da, 4 * elt(dt)) && aligned(dx, 4 * elt(dt)) &&
+           aligned(h, 16) && aligned(dh, 16);
+  p.br[0].a = a;
+  p.br[0].h = h;
+  p.br[0].dh = dh;
+  p.br[0].h0 = h0;
+  p.br[0].da = da;
+  p.br[0].dx = dx;
+  p.br[0].dh0 = dh0;
+  p.br[0].dir = reverse ? -1 : 1;
+  return from_cuda(dt == SCAN_F32 ? launch_scalar_bwd_f32(p, pl, stream)
+                                  : launch_scalar_bwd_bf16(p, pl, stream));
+}
+
+scan_status scan_bidir_fwd(const void* af, const void* xf, const void* ar, const void* xr,
+                           const float* h0f, const float* h0r, const int32_t* cu, int32_t n_seqs,
+                           float* hf, float* hr, int64_t B, int64_t C, int64_t T, scan_dtype dt,
+                           const scan_opts* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (dt != SCAN_F32 && dt != SCAN_BF16) return SCAN_ERR_INVALID_ARG;
+  const scan_opts o = defaults(opts);
+  ScalarParams p;
+  ScalarPlan pl;
+  scan_status st = prepare(B, C, T, cu, n_seqs, 2, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  if (p.rows * T == 0) return SCAN_OK;
+  if (!af || !xf || !ar || !xr || !hf || !hr) return SCAN_ERR_INVALID_ARG;
+  const size_t va = 4 * elt(dt);
+  pl.vec = aligned(af, va) && aligned(xf, va) && aligned(ar, va) && aligned(xr, va) &&
+           aligned(hf, 16) && aligned(hr, 16);
+  p.br[0].a = af;
+  p.br[0].x = xf;
+  p.br[0].h0 = h0f;
+  p.br[0].out_h = hf;
+  p.br[0].dir = 1;
+  p.br[1].a = ar;
+  p.br[1].x = xr;
+  p.br[1].h0 = h0r;
+  p.br[1].out_h = hr;
+  p.br[1].dir = -1;
+  return from_cuda(dt == SCAN_F32 ? launch_scalar_fwd_f32(p, pl, stream)
+                                  : launch_scalar_fwd_bf16(p, pl, stream));
+}
+
+scan_status scan_bidir_bwd(const void* af, const float* hf, const float* dhf, const float* h0f,
+                           const void* ar, const float* hr, const float* dhr, const float* h0r,
+                           const int32_t* cu, int32_t n_seqs, void* daf, void* dxf, float* dh0f,
+                           void* dar, void* dxr, float* dh0r, int64_t B, int64_t C, int64_t T,
+                           scan_dtype dt, const scan_opts* opts, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  if (dt != SCAN_F32 && dt != SCAN_BF16) return SCAN_ERR_INVALID_ARG;
+  const scan_opts o = defaults(opts);
+  ScalarParams p;
+  ScalarPlan pl;
+  scan_status st = prepare(B, C, T, cu, n_seqs, 2, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  const int64_t n_h0 = cu ? (int64_t)n_seqs * C : B * C;
+  if (p.rows * T == 0) {
+    st = zero_dh0(dh0f, n_h0, stream);
+    return st != SCAN_OK ? st : zero_dh0(dh0r, n_h0, stream);
+  }
+  if (!af || !hf || !dhf || !ar || !hr || !dhr || !daf || !dxf || !dar || !dxr)
+    return SCAN_ERR_INVALID_ARG;
+  const size_t va = 4 * elt(dt);
+  pl.vec = aligned(af, va) && aligned(ar, va) && aligned(daf, va) && aligned(dxf, va) &&
+           aligned(dar, va) && aligned(dxr, va) && aligned(hf, 16) && aligned(dhf, 16) &&
+           aligned(hr, 16) && aligned(dhr, 16);
+  p.br[0].a = af;
+  p.br[0].h = hf;
+  p.br[0].dh = dhf;
+  p.br[0].h0 = h0f;
+  p.br[0].da = daf;
+  p.br[0].dx = dxf;
+  p.br[0].dh0 = dh0f;
+  p.br[0].dir = 1;
+  p.br[1].a = ar;
+  p.br[1].h = hr;
+  p.br[1].dh = dhr;
+  p.br[1].h0 = h0r;
+  p.br[1].da = dar;
+  p.br[1].dx = dxr;
+  p.br[1].dh0 = dh0r;
+  p.br[1].dir = -1;
+  return from_cuda(dt == SCAN_F32 ? launch_scalar_bwd_f32(p, pl, stream)
+                                  : launch_scalar_bwd_bf16(p, pl, stream));
+}
+
+scan_status scan_log_fwd(const float* log_a, const float* log_x, const float* log_h0,
+                         const int32_t* cu, int32_t n_seqs, float* h, int64_t B, int64_t C,
+                         int64_t T, int32_t reverse, const scan_opts* opts, void* ws,
+                         size_t ws_bytes, cudaStream_t stream) {
+  const scan_opts o = defaults(opts);
+  ScalarParams p;
+  ScalarPlan pl;
+  scan_status st = prepare(B, C, T, cu, n_seqs, 1, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  if (p.rows * T == 0) return SCAN_OK;
+  if (!log_a || !log_x || !h) return SCAN_ERR_INVALID_ARG;
+  pl.vec = aligned(log_a, 16) && aligned(log_x, 16) && aligned(h, 16);
+  p.br[0].a = log_a;
+  p.br[0].x = log_x;
+  p.br[0].h0 = log_h0;
+  p.br[0].out_h = h;
+  p.br[0].dir = reverse ? -1 : 1;
+  return from_cuda(launch_log_fwd(p, pl, stream));
+}
+
+scan_status affine_scan_fwd(const float* A, const float* Bm, const float* h0, float* H, int64_t B,
+                            int64_t T, int64_t N, int32_t k, int32_t v, const scan_opts* opts,
+                            void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)A; (void)Bm; (void)h0; (void)H; (void)B; (void)T; (void)N; (void)k; (void)v;
+  (void)opts; (void)ws; (void)ws_bytes; (void)stream;
+  return SCAN_ERR_UNSUPPORTED;
+}
+
+scan_status affine_scan_bwd(const float* A, const float* H, const float* dH, const float* h0,
+                            float* dA, float* dB, float* dh0, int64_t B, int64_t T, int64_t N,
+                            int32_t k, int32_t v, const scan_opts* opts, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  (void)A; (void)H; (void)dH; (void)h0; (void)dA; (void)dB; (void)dh0; (void)B; (void)T;
+  (void)N; (void)k; (void)v; (void)opts; (void)ws; (void)ws_bytes; (void)stream;
+  return SCAN_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// scan_internal.h -- structures shared by libscan's translation units.
+//
+// Host planner (scan_api.cu) and kernels (scan_scalar_*.cu, scan_affine.cu)
+// agree on these layouts; nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace scan {
+
+enum Mode { MODE_FWD = 0, MODE_BWD = 1 };
+enum Variant { VAR_STATIONARY = 1, VAR_LOOKBACK = 2 };
+
+// Workspace header, at offset 0 of every workspace. The look-back kernels take
+// a tile ticket from `ticket_epoch` (low 32 bits) and read the launch epoch
+// from its high 32 bits in the same atomic; the last block of a launch resets
+// the ticket, advances the epoch and clears `done`, so no per-call memset is
+// needed. `status` is the sticky device error (a scan_status value).
+struct alignas(64) WsHeader {
+  unsigned long long ticket_epoch;
+  unsigned int done;
+  unsigned int status;
+  unsigned int info[4];  // where a wait expired: tile ticket, branch, row, scan index
+};
+
+constexpr size_t kWsHeaderBytes = 256;  // records start here
+
+// One branch of a scalar scan launch.
+struct BranchArgs {
+  const void* a;     // gate a (dtype dt); forward and backward
+  const void* x;     // forward: x (dtype dt)
+  const float* h;    // backward: forward output h
+  const float* dh;   // backward: upstream gradient
+  const float* h0;   // nullable initial state ([B,C] dense, [n_seqs,C] packed)
+  float* out_h;      // forward output
+  void* dx;          // backward outputs (dtype dt)
+  void* da;
+  float* dh0;        // nullable
+  int dir;           // direction of the forward recurrence: +1 causal, -1 reverse
+};
+
+struct ScalarParams {
+  BranchArgs br[2];
+  const int32_t* cu;  // nullable packed offsets
+  int n_seqs;
+  int nbr;            // branches in this launch (1 or 2)
+  int64_t rows;       // B*C dense, C packed
+  int64_t T;          // row length
+  int M;              // chunks per row along T
+  int G;              // row groups (blocks along rows)
+  int R;              // rows (warps) per block
+  int64_t ntiles;     // M * G * nbr
+  unsigned long long* recs;  // look-back records: [nbr][rows][M] x 16 bytes
+  WsHeader* hdr;
+  unsigned long long wait_limit_ns;
+  int test_stall;
+};
+
+struct ScalarPlan {
+  int variant;  // VAR_*
+  int J;        // 128-element blocks per chunk (chunk = 128 J)
+  int R;
+  int M;
+  int G;
+  bool vec;     // vectorised loads/stores
+  size_t ws_bytes;
+  size_t smem;
+};
+
+// Launchers (one translation unit per mode/dtype family).
+cudaError_t launch_scalar_fwd_f32(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
+cudaError_t launch_scalar_fwd_bf16(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
+cudaError_t launch_scalar_bwd_f32(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
+cudaError_t launch_scalar_bwd_bf16(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
+cudaError_t launch_log_fwd(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
+
+// Block-matrix affine scan.
+struct AffineParams {
+  const float* A;
+  const float* Bm;
+  const float* H;    // backward: forward output
+  const float* dH;   // backward
+  const float* h0;
+  float* out_H;      // forward output
+  float* dA;
+  float* dB;
+  float* dh0;
+  int64_t B, T, N;
+  int k, v;
+  int Lc;            // time steps per chunk
+  int M;             // chunks along T
+  int NL;            // lanes (state blocks) per block
+  int G;             // lane groups = B * ceil(N / NL)
+  int64_t ntiles;
+  unsigned char* recs;
+  WsHeader* hdr;
+  unsigned long long wait_limit_ns;
+  int test_stall;
+};
+
+struct AffinePlan {
+  int Lc;
+  int NL;
+  int M;
+  int G;
+  size_t ws_bytes;
+  size_t smem;
+  int threads;
+};
+
+cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);
+cudaError_t launch_affine_bwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);
+
+// Writes zeros to n floats (empty-input edge cases).
+cudaError_t launch_fill_zero(float* p, int64_t n, cudaStream_t s);
+
+}  // namespace scan

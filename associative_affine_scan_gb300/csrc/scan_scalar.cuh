@@ -1,0 +1,827 @@
+// scan_scalar.cuh -- chunked scan kernels for the scalar and log-space forms.
+//
+// The recurrence h_t = a_t h_{t-1} + x_t ("associative_scan_triton" README,
+// quick start) is an affine map per step; a run of steps composes to one map
+// h_out = P h_in + Q ("Our RG-LRU GPU audit", Exact real chunk algebra), and
+// "apply (P1, Q1) then (P2, Q2)" = (P2 P1, P2 Q1 + Q2) is associative
+// ("Triton scan kernels", One associative-scan family). The log-space form
+// carries l = log h with the same algebra in (log-coefficient sum, shifted
+// log-sum-exp) form.
+//
+// Work decomposition (one thread block = R rows x one chunk of L = 128 J
+// time steps; one warp per row):
+//   * each lane holds 4 consecutive steps per 128-step block, loaded with one
+//     128-bit (fp32) or 64-bit (bf16) coalesced access per block;
+//   * lane-serial composition of its 4 steps, a warp-shuffle inclusive scan of
+//     the lanes' (P, Q) pairs and a serial carry across the J blocks give every
+//     step its chunk-local map (P_t, Q_t) in fp32 registers;
+//   * the chunk's carry-in comes either from the registers of the same block
+//     (STATIONARY: the block walks its row group's chunks in order) or from a
+//     decoupled look-back over the published summaries of earlier chunks
+//     (LOOKBACK: chunks are independent blocks taken in ticket order, chunk
+//     index major, so earlier chunks always belong to running or finished
+//     blocks);
+//   * h_t = P_t h_in + Q_t is stored with 128-bit streaming stores.
+//
+// Packed sequences (cu_seqlens) never cut the tiling: the first step of every
+// sequence (in scan direction) becomes the constant map (0, a h0 + x), which
+// erases everything before it exactly, so nothing leaks across sequences
+// ("associative_scan_triton" README, how it works). Steps outside [0, T) are
+// the identity map and are not written ("Our RG-LRU GPU audit", partial final
+// chunks).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "scan_internal.h"
+
+namespace scan {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kStatusTimeout = 6u;  // scan_status values
+constexpr unsigned kStatusSeqlens = 7u;
+constexpr unsigned kStatusWorkspace = 4u;
+
+// ---------------------------------------------------------------------------
+// memory access helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned long long pack_rec(uint32_t tag, float v) {
+  return ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v);
+}
+
+__device__ __forceinline__ void set_status(WsHeader* hdr, unsigned code) {
+  atomicCAS(&hdr->status, 0u, code);
+}
+
+template <typename TA>
+struct IO;
+
+template <>
+struct IO<float> {
+  static __device__ __forceinline__ void ld4(const float* p, float v[4]) {
+    const float4 q = __ldcs(reinterpret_cast<const float4*>(p));
+    v[0] = q.x;
+    v[1] = q.y;
+    v[2] = q.z;
+    v[3] = q.w;
+  }
+  static __device__ __forceinline__ float ld1(const float* p) { return __ldcs(p); }
+  static __device__ __forceinline__ void st4(float* p, const float v[4]) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+  }
+  static __device__ __forceinline__ void st1(float* p, float v) { __stcs(p, v); }
+};
+
+template <>
+struct IO<__nv_bfloat16> {
+  static __device__ __forceinline__ void ld4(const __nv_bfloat16* p, float v[4]) {
+    const uint2 q = __ldcs(reinterpret_cast<const uint2*>(p));
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xffff0000u);
+  }
+  static __device__ __forceinline__ float ld1(const __nv_bfloat16* p) {
+    const unsigned short u = __ldcs(reinterpret_cast<const unsigned short*>(p));
+    return __uint_as_float(((unsigned)u) << 16);
+  }
+  static __device__ __forceinline__ unsigned pack2(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const unsigned*>(&b);
+  }
+  static __device__ __forceinline__ void st4(__nv_bfloat16* p, const float v[4]) {
+    __stcs(reinterpret_cast<uint2*>(p), make_uint2(pack2(v[0], v[1]), pack2(v[2], v[3])));
+  }
+  static __device__ __forceinline__ void st1(__nv_bfloat16* p, float v) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    __stcs(reinterpret_cast<unsigned short*>(p), *reinterpret_cast<const unsigned short*>(&b));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// the two monoids
+// ---------------------------------------------------------------------------
+
+// Linear space: E = the map h -> p h + q.
+struct LinOp {
+  struct E {
+    float p, q;
+  };
+  static __device__ __forceinline__ E identity() { return {1.f, 0.f}; }
+  static __device__ __forceinline__ E make(float a, float x) { return {a, x}; }
+  // first step of a sequence: the constant map h -> a h0 + x
+  static __device__ __forceinline__ E make_first(float a, float x, const float* h0, int64_t i) {
+    return {0.f, fmaf(a, h0 ? h0[i] : 0.f, x)};
+  }
+  // "apply e1 then e2"
+  static __device__ __forceinline__ E compose(const E& e1, const E& e2) {
+    return {e2.p * e1.p, fmaf(e2.p, e1.q, e2.q)};
+  }
+  static __device__ __forceinline__ float initial_carry() { return 0.f; }
+  static __device__ __forceinline__ float value(const E& e, float c) { return fmaf(e.p, c, e.q); }
+  static __device__ __forceinline__ float carry_after(const E& e, float c) { return fmaf(e.p, c, e.q); }
+  static __device__ __forceinline__ bool is_const(const E& e) { return e.p == 0.f; }
+  static __device__ __forceinline__ float const_carry(const E& e) { return e.q; }
+  static __device__ __forceinline__ E from_inc(float c) { return {0.f, c}; }
+  static __device__ __forceinline__ E from_agg(float u, float w) { return {u, w}; }
+  static __device__ __forceinline__ void to_agg(const E& e, float& u, float& w) {
+    u = e.p;
+    w = e.q;
+  }
+  static __device__ __forceinline__ E shfl(const E& e, int src) {
+    return {__shfl_sync(kFull, e.p, src), __shfl_sync(kFull, e.q, src)};
+  }
+  static __device__ __forceinline__ E shfl_up(const E& e, int d) {
+    return {__shfl_up_sync(kFull, e.p, d), __shfl_up_sync(kFull, e.q, d)};
+  }
+  static __device__ __forceinline__ E shfl_down(const E& e, int d) {
+    return {__shfl_down_sync(kFull, e.p, d), __shfl_down_sync(kFull, e.q, d)};
+  }
+  static __device__ __forceinline__ E shfl_xor(const E& e, int d) {
+    return {__shfl_xor_sync(kFull, e.p, d), __shfl_xor_sync(kFull, e.q, d)};
+  }
+};
+
+// log(exp(u) + exp(w)); -inf is the zero term.
+__device__ __forceinline__ float log_add_exp(float u, float w) {
+  const float m = fmaxf(u, w);
+  if (m == -CUDART_INF_F) return -CUDART_INF_F;
+  return m + __logf(1.f + __expf(-fabsf(u - w)));
+}
+
+// Log space: E = the map l -> log(exp(l + a) + s exp(m)): a is the running
+// log-coefficient sum, (m, s) a max-shifted log-sum-exp accumulator ("Triton
+// scan kernels", One associative-scan family, parallel_scan_log).
+struct LogOp {
+  struct E {
+    float a, m, s;
+  };
+  static __device__ __forceinline__ E identity() { return {0.f, -CUDART_INF_F, 0.f}; }
+  static __device__ __forceinline__ E make(float la, float lx) { return {la, lx, 1.f}; }
+  static __device__ __forceinline__ E make_first(float la, float lx, const float* lh0, int64_t i) {
+    if (!lh0) return {-CUDART_INF_F, lx, 1.f};
+    const float u = lh0[i] + la;
+    const float m = fmaxf(u, lx);
+    if (m == -CUDART_INF_F) return {-CUDART_INF_F, -CUDART_INF_F, 0.f};
+    return {-CUDART_INF_F, m, __expf(u - m) + __expf(lx - m)};
+  }
+  static __device__ __forceinline__ E compose(const E& e1, const E& e2) {
+    const float u = e1.m + e2.a;  // e1's accumulated mass carried through e2
+    const float d = u - e2.m;     // NaN only when both are -inf
+    const bool up = u > e2.m;
+    float ex = __expf(-fabsf(d));
+    if (d != d) ex = 0.f;
+    E r;
+    r.a = e1.a + e2.a;
+    r.m = up ? u : e2.m;
+    r.s = up ? fmaf(e2.s, ex, e1.s) : fmaf(e1.s, ex, e2.s);
+    return r;
+  }
+  static __device__ __forceinline__ float initial_carry() { return -CUDART_INF_F; }
+  // linear-space output exp(l_t) for the carry-in log state c
+  static __device__ __forceinline__ float value(const E& e, float c) {
+    return __expf(c + e.a) + e.s * __expf(e.m);
+  }
+  static __device__ __forceinline__ float carry_after(const E& e, float c) {
+    return log_add_exp(c + e.a, e.m + __logf(e.s));
+  }
+  static __device__ __forceinline__ bool is_const(const E& e) { return e.a == -CUDART_INF_F; }
+  static __device__ __forceinline__ float const_carry(const E& e) { return e.m + __logf(e.s); }
+  static __device__ __forceinline__ E from_inc(float c) { return {-CUDART_INF_F, c, 1.f}; }
+  static __device__ __forceinline__ E from_agg(float u, float w) { return {u, w, 1.f}; }
+  static __device__ __forceinline__ void to_agg(const E& e, float& u, float& w) {
+    u = e.a;
+    w = e.m + __logf(e.s);
+  }
+  static __device__ __forceinline__ E shfl(const E& e, int src) {
+    return {__shfl_sync(kFull, e.a, src), __shfl_sync(kFull, e.m, src), __shfl_sync(kFull, e.s, src)};
+  }
+  static __device__ __forceinline__ E shfl_up(const E& e, int d) {
+    return {__shfl_up_sync(kFull, e.a, d), __shfl_up_sync(kFull, e.m, d),
+            __shfl_up_sync(kFull, e.s, d)};
+  }
+  static __device__ __forceinline__ E shfl_down(const E& e, int d) {
+    return {__shfl_down_sync(kFull, e.a, d), __shfl_down_sync(kFull, e.m, d),
+            __shfl_down_sync(kFull, e.s, d)};
+  }
+  static __device__ __forceinline__ E shfl_xor(const E& e, int d) {
+    return {__shfl_xor_sync(kFull, e.a, d), __shfl_xor_sync(kFull, e.m, d),
+            __shfl_xor_sync(kFull, e.s, d)};
+  }
+};
+
+// ---------------------------------------------------------------------------
+// packed-sequence window: which positions start a non-empty sequence
+// ---------------------------------------------------------------------------
+
+// Positions [W0, W0 + WL) around a chunk. bit(p) is set when a non-empty
+// sequence starts at p or ends just before p (so bit(T) is always set);
+// sstart[p - W0] names the sequence starting at p, send[p - W0] the one
+// ending at p - 1.
+struct SegWin {
+  uint32_t* bits;
+  int* sstart;
+  int* send;
+  int64_t W0;
+  int WL;
+};
+
+__device__ __forceinline__ bool win_bit(const SegWin& w, int64_t p) {
+  const int i = (int)(p - w.W0);
+  return (w.bits[i >> 5] >> (i & 31)) & 1u;
+}
+
+// Called by every thread of the block. cu is sorted (checked separately);
+// with a malformed cu every index still stays inside [0, n].
+__device__ inline void build_window(SegWin& w, const int32_t* cu, int n, int warp, int lane) {
+  const int nwords = (w.WL + 31) >> 5;
+  __syncthreads();  // the previous chunk's readers are done
+  for (int i = threadIdx.x; i < nwords; i += blockDim.x) w.bits[i] = 0u;
+  __syncthreads();
+  if (warp == 0) {
+    // lb = number of offsets cu[i] (0 <= i <= n) below W0, by a 32-way search
+    int lo = 0, hi = n + 1;
+    while (hi - lo > 32) {
+      const int step = (hi - lo + 31) >> 5;
+      const int idx = lo + lane * step;
+      const bool pr = idx < hi && (int64_t)cu[idx] < w.W0;
+      const int c = __popc(__ballot_sync(kFull, pr));
+      const int nlo = c > 0 ? lo + (c - 1) * step + 1 : lo;
+      const int nhi = min(hi, lo + c * step);
+      lo = nlo;
+      hi = max(nhi, nlo);
+    }
+    {
+      const int idx = lo + lane;
+      const bool pr = idx < hi && (int64_t)cu[idx] < w.W0;
+      lo += __popc(__ballot_sync(kFull, pr));
+    }
+    const int first = max(lo - 1, 0);
+    for (int base = first;; base += 32) {
+      const int i = base + lane;
+      const bool in = i < n;
+      int s = 0, e = 0;
+      if (in) {
+        s = cu[i];
+        e = cu[i + 1];
+      }
+      const bool before_end = in && (int64_t)s < w.W0 + w.WL;
+      if (before_end && e > s) {
+        const int64_t ps = (int64_t)s - w.W0;
+        if (ps >= 0 && ps < w.WL) {
+          atomicOr(&w.bits[ps >> 5], 1u << (ps & 31));
+          w.sstart[ps] = i;
+        }
+        const int64_t pe = (int64_t)e - w.W0;
+        if (pe >= 0 && pe < w.WL) {
+          atomicOr(&w.bits[pe >> 5], 1u << (pe & 31));
+          w.send[pe] = i;
+        }
+      }
+      if (!__all_sync(kFull, before_end)) break;
+    }
+  }
+  __syncthreads();
+}
+
+// Checks 0 = cu[0] <= ... <= cu[n] = T and writes dh0 = 0 for empty sequences.
+// Called by every thread of one block.
+template <int MODE>
+__device__ inline void check_segments(const ScalarParams& p) {
+  const int n = p.n_seqs;
+  int bad = 0;
+  for (int i = threadIdx.x; i <= n; i += blockDim.x) {
+    const int64_t c = p.cu[i];
+    if (i == 0 && c != 0) bad = 1;
+    if (i == n && c != p.T) bad = 1;
+    if (i < n && (int64_t)p.cu[i + 1] < c) bad = 1;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.hdr, kStatusSeqlens);
+  if (MODE == MODE_BWD) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int b = 0; b < p.nbr; ++b) {
+      float* dh0 = p.br[b].dh0;
+      if (!dh0) continue;
+      for (int i = warp; i < n; i += nw) {
+        if (p.cu[i] != p.cu[i + 1]) continue;
+        for (int64_t c = lane; c < p.rows; c += 32) dh0[(int64_t)i * p.rows + c] = 0.f;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// decoupled look-back
+// ---------------------------------------------------------------------------
+
+// Composition in lane order where a higher lane is earlier in scan order.
+template <class Op>
+__device__ __forceinline__ typename Op::E warp_reduce_ordered(typename Op::E v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const typename Op::E o = Op::shfl_xor(v, off);
+    v = (lane & off) ? Op::compose(v, o) : Op::compose(o, v);
+  }
+  return v;
+}
+
+// Carry-in of chunk k of one row: walks the records of chunks k-1, k-2, ...
+// 32 at a time until a terminal one (an inclusive state, or a summary that
+// is a constant map) and composes everything after it. Every wait is bounded
+// by p.wait_limit_ns; on expiry the sticky status becomes SCAN_ERR_TIMEOUT
+// and the initial carry is returned, so the kernel always completes.
+template <class Op>
+__device__ float lookback(const ScalarParams& p, const unsigned long long* recs_row, int k,
+                          uint32_t epoch, int lane, unsigned ticket, int brn, int64_t row) {
+  uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
+  if (p.test_stall && brn == 0 && row == 0 && k == 1) tag_agg = tag_inc = 0xffffffffu;
+  typename Op::E acc = Op::identity();
+  int pos = k - 1;
+  const unsigned long long t_begin = global_ns();
+  unsigned backoff = 32;
+  while (true) {
+    const int idx = pos - lane;
+    typename Op::E e = Op::identity();
+    int st;  // 0 not ready, 1 summary, 2 terminal
+    if (idx >= 0) {
+      const unsigned long long w1 = ld_relaxed(recs_row + 2 * idx + 1);
+      const uint32_t tg = (uint32_t)(w1 >> 32);
+      if (tg == tag_inc) {
+        e = Op::from_inc(__uint_as_float((uint32_t)w1));
+        st = 2;
+      } else if (tg == tag_agg) {
+        const unsigned long long w0 = ld_relaxed(recs_row + 2 * idx);
+        if ((uint32_t)(w0 >> 32) == tag_agg) {
+          e = Op::from_agg(__uint_as_float((uint32_t)w0), __uint_as_float((uint32_t)w1));
+          st = Op::is_const(e) ? 2 : 1;
+        } else {
+          st = 0;
+        }
+      } else {
+        st = 0;
+      }
+    } else {
+      e = Op::from_inc(Op::initial_carry());
+      st = 2;
+    }
+    const unsigned term = __ballot_sync(kFull, st == 2);
+    const unsigned wait = __ballot_sync(kFull, st == 0);
+    const int f = term ? __ffs(term) - 1 : 32;
+    const unsigned below = f >= 32 ? kFull : ((1u << f) - 1u);
+    if (wait & below) {
+      if (__any_sync(kFull, global_ns() - t_begin > p.wait_limit_ns)) {
+        if (lane == 0) {
+          set_status(p.hdr, kStatusTimeout);
+          p.hdr->info[0] = ticket;
+          p.hdr->info[1] = (unsigned)brn;
+          p.hdr->info[2] = (unsigned)row;
+          p.hdr->info[3] = (unsigned)k;
+        }
+        return Op::initial_carry();
+      }
+      __nanosleep(backoff);
+      backoff = backoff < 1024 ? backoff * 2 : 1024;
+      continue;
+    }
+    if (lane > f) e = Op::identity();
+    const typename Op::E win = warp_reduce_ordered<Op>(e, lane);
+    acc = Op::compose(win, acc);
+    if (f < 32) break;
+    pos -= 32;
+  }
+  return Op::const_carry(acc);
+}
+
+// ---------------------------------------------------------------------------
+// neighbours across lanes (backward needs a_{t+-1} and h_{t-+1})
+// ---------------------------------------------------------------------------
+
+// value at memory position (group start + 4): the next lane's first element,
+// the next block's lane 0, or the halo after the chunk
+template <int J>
+__device__ __forceinline__ float next_in_memory(const float (&V)[J][4], int j, float halo, int lane) {
+  float v = __shfl_down_sync(kFull, V[j][0], 1);
+  const float vb = (j + 1 < J) ? __shfl_sync(kFull, V[j + 1 < J ? j + 1 : j][0], 0) : halo;
+  return lane == 31 ? vb : v;
+}
+
+// value at memory position (group start - 1)
+template <int J>
+__device__ __forceinline__ float prev_in_memory(const float (&V)[J][4], int j, float halo, int lane) {
+  float v = __shfl_up_sync(kFull, V[j][3], 1);
+  const float vb = (j > 0) ? __shfl_sync(kFull, V[j > 0 ? j - 1 : 0][3], 31) : halo;
+  return lane == 0 ? vb : v;
+}
+
+// ---------------------------------------------------------------------------
+// one chunk of one row group
+// ---------------------------------------------------------------------------
+
+// S is the scan direction: +1 walks t upwards, -1 downwards. A forward call
+// scans in the recurrence's direction; a backward call scans against it.
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S>
+__device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int k, bool stationary,
+                                      uint32_t epoch, unsigned ticket, SegWin& win, float& carry) {
+  using E = typename Op::E;
+  constexpr int L = 128 * J;
+  const BranchArgs& br = p.br[brn];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)g * p.R + warp;
+  const bool active = row < p.rows;
+  const int64_t T = p.T;
+  const int m = (S > 0) ? k : (p.M - 1 - k);
+  // rows are cut so that every 4-step group starts on a 4-element boundary of
+  // memory (16 bytes fp32, 8 bytes bf16) whatever T is
+  const int shift = VEC ? (int)((row * T) & 3) : 0;
+  const int64_t t0 = (int64_t)m * L - shift;
+  const int64_t roff = row * T;
+  const int64_t tl = t0 + 4 * lane;
+
+  float A[J][4], X[J][4], H[J][4];
+  float halo_a = 0.f, halo_h = 0.f;
+  if (active) {
+    const TA* a = static_cast<const TA*>(br.a) + roff;
+    if (MODE == MODE_FWD) {
+      const TA* x = static_cast<const TA*>(br.x) + roff;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int64_t t = tl + 128 * j;
+        if (VEC && t >= 0 && t + 4 <= T) {
+          IO<TA>::ld4(a + t, A[j]);
+          IO<TA>::ld4(x + t, X[j]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t tt = t + e;
+            const bool v = tt >= 0 && tt < T;
+            A[j][e] = v ? IO<TA>::ld1(a + tt) : 0.f;
+            X[j][e] = v ? IO<TA>::ld1(x + tt) : 0.f;
+          }
+        }
+      }
+    } else {
+      const float* h = br.h + roff;
+      const float* dh = br.dh + roff;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int64_t t = tl + 128 * j;
+        if (VEC && t >= 0 && t + 4 <= T) {
+          IO<TA>::ld4(a + t, A[j]);
+          IO<float>::ld4(h + t, H[j]);
+          IO<float>::ld4(dh + t, X[j]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t tt = t + e;
+            const bool v = tt >= 0 && tt < T;
+            A[j][e] = v ? IO<TA>::ld1(a + tt) : 0.f;
+            H[j][e] = v ? IO<float>::ld1(h + tt) : 0.f;
+            X[j][e] = v ? IO<float>::ld1(dh + tt) : 0.f;
+          }
+        }
+      }
+      // halos: the gate one step after (S = -1) or before (S = +1) the chunk,
+      // the state one step before (S = -1) or after (S = +1)
+      if (lane == 0) {
+        const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
+        const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
+        if (pa >= 0 && pa < T) halo_a = IO<TA>::ld1(a + pa);
+        if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(h + ph);
+      }
+      halo_a = __shfl_sync(kFull, halo_a, 0);
+      halo_h = __shfl_sync(kFull, halo_h, 0);
+    }
+  }
+
+  if (VARLEN) {
+    win.W0 = (int64_t)m * L - 4;
+    build_window(win, p.cu, p.n_seqs, warp, lane);
+  }
+  if (!active) return;
+
+  // boundary tests in memory order
+  auto is_start = [&](int64_t t) -> bool {  // t is the first step of a sequence
+    if (VARLEN) return win_bit(win, t);
+    return t == 0;
+  };
+  auto is_end = [&](int64_t t) -> bool {  // t is the last step of a sequence
+    if (VARLEN) return win_bit(win, t + 1);
+    return t == T - 1;
+  };
+  // sequence index -> row of h0/dh0; clamped so that even a malformed
+  // cu_seqlens (reported through the status word) cannot address outside h0
+  auto seq_row = [&](int s) -> int64_t {
+    s = s < 0 ? 0 : (s >= p.n_seqs ? p.n_seqs - 1 : s);
+    return (int64_t)s * p.rows + row;
+  };
+  auto h0_index_start = [&](int64_t t) -> int64_t {
+    if (VARLEN) return seq_row(win.sstart[t - win.W0]);
+    return row;
+  };
+  auto h0_index_end = [&](int64_t t) -> int64_t {
+    if (VARLEN) return seq_row(win.send[t + 1 - win.W0]);
+    return row;
+  };
+
+  // ---- elements ----
+  E el[J][4];
+  float HN[J];  // backward: cross-lane neighbour state of each group's edge step
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int64_t t = tl + 128 * j;
+    if (MODE == MODE_FWD) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t tt = t + e;
+        E v = Op::identity();
+        if (tt >= 0 && tt < T) {
+          v = Op::make(A[j][e], X[j][e]);
+          if (S > 0) {
+            if (is_start(tt)) v = Op::make_first(A[j][e], X[j][e], br.h0, h0_index_start(tt));
+          } else {
+            if (is_end(tt)) v = Op::make_first(A[j][e], X[j][e], br.h0, h0_index_end(tt));
+          }
+        }
+        el[j][e] = v;
+      }
+    } else {
+      float gate[4];
+      if (S < 0) {  // causal recurrence: gate a_{t+1}, state h_{t-1}
+        gate[0] = A[j][1];
+        gate[1] = A[j][2];
+        gate[2] = A[j][3];
+        gate[3] = next_in_memory<J>(A, j, halo_a, lane);
+        HN[j] = prev_in_memory<J>(H, j, halo_h, lane);
+      } else {  // reverse recurrence: gate a_{t-1}, state h_{t+1}
+        gate[0] = prev_in_memory<J>(A, j, halo_a, lane);
+        gate[1] = A[j][0];
+        gate[2] = A[j][1];
+        gate[3] = A[j][2];
+        HN[j] = next_in_memory<J>(H, j, halo_h, lane);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t tt = t + e;
+        E v = Op::identity();
+        if (tt >= 0 && tt < T) {
+          // the shifted gate is 0 past the end of the sequence (scan-first step)
+          const bool cut = (S < 0) ? is_end(tt) : is_start(tt);
+          v = Op::make(cut ? 0.f : gate[e], X[j][e]);
+        }
+        el[j][e] = v;
+      }
+    }
+  }
+
+  // ---- chunk-local inclusive scan in scan order ----
+  E blk = Op::identity();
+#pragma unroll
+  for (int jj = 0; jj < J; ++jj) {
+    const int j = (S > 0) ? jj : (J - 1 - jj);
+    E lane_tot;
+    if (S > 0) {
+#pragma unroll
+      for (int e = 1; e < 4; ++e) el[j][e] = Op::compose(el[j][e - 1], el[j][e]);
+      lane_tot = el[j][3];
+    } else {
+#pragma unroll
+      for (int e = 2; e >= 0; --e) el[j][e] = Op::compose(el[j][e + 1], el[j][e]);
+      lane_tot = el[j][0];
+    }
+    E inc = lane_tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const E o = (S > 0) ? Op::shfl_up(inc, off) : Op::shfl_down(inc, off);
+      const bool has = (S > 0) ? (lane >= off) : (lane + off < 32);
+      if (has) inc = Op::compose(o, inc);
+    }
+    E ex = (S > 0) ? Op::shfl_up(inc, 1) : Op::shfl_down(inc, 1);
+    if (lane == ((S > 0) ? 0 : 31)) ex = Op::identity();
+    const E pre = Op::compose(blk, ex);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) el[j][e] = Op::compose(pre, el[j][e]);
+    blk = Op::compose(blk, Op::shfl(inc, (S > 0) ? 31 : 0));
+  }
+
+  // ---- carry-in ----
+  float c;
+  if (stationary) {
+    c = carry;
+    carry = Op::carry_after(blk, c);
+  } else {
+    unsigned long long* recs_row = p.recs + ((int64_t)brn * p.rows + row) * (int64_t)p.M * 2;
+    unsigned long long* rec = recs_row + 2 * (int64_t)k;
+    const uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
+    if (k == 0) {
+      c = Op::initial_carry();
+      if (lane == 0) st_relaxed(rec + 1, pack_rec(tag_inc, Op::carry_after(blk, c)));
+    } else {
+      const bool cst = Op::is_const(blk);
+      if (lane == 0) {
+        if (cst) {
+          st_relaxed(rec + 1, pack_rec(tag_inc, Op::const_carry(blk)));
+        } else {
+          float u, w;
+          Op::to_agg(blk, u, w);
+          st_relaxed(rec, pack_rec(tag_agg, u));
+          st_relaxed(rec + 1, pack_rec(tag_agg, w));
+        }
+      }
+      c = lookback<Op>(p, recs_row, k, epoch, lane, ticket, brn, row);
+      if (!cst && lane == 0) st_relaxed(rec + 1, pack_rec(tag_inc, Op::carry_after(blk, c)));
+    }
+  }
+
+  // ---- outputs ----
+  if (MODE == MODE_FWD) {
+    float* h = br.out_h + roff;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int64_t t = tl + 128 * j;
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = Op::value(el[j][e], c);
+      if (VEC && t >= 0 && t + 4 <= T) {
+        IO<float>::st4(h + t, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (t + e >= 0 && t + e < T) IO<float>::st1(h + t + e, v[e]);
+      }
+    }
+  } else {
+    TA* dx = static_cast<TA*>(br.dx) + roff;
+    TA* da = static_cast<TA*>(br.da) + roff;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int64_t t = tl + 128 * j;
+      float gx[4], ga[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t tt = t + e;
+        const float gv = Op::value(el[j][e], c);
+        float hn;
+        if (S < 0) hn = (e > 0) ? H[j][e - 1] : HN[j];
+        else hn = (e < 3) ? H[j][e + 1] : HN[j];
+        if (tt >= 0 && tt < T) {
+          // the step that starts the forward recurrence reads h0 and feeds dh0
+          const bool first_fwd = (S < 0) ? is_start(tt) : is_end(tt);
+          if (first_fwd) {
+            const int64_t hi = (S < 0) ? h0_index_start(tt) : h0_index_end(tt);
+            hn = br.h0 ? br.h0[hi] : 0.f;
+            if (br.dh0) br.dh0[hi] = A[j][e] * gv;
+          }
+        }
+        gx[e] = gv;
+        ga[e] = gv * hn;
+      }
+      if (VEC && t >= 0 && t + 4 <= T) {
+        IO<TA>::st4(dx + t, gx);
+        IO<TA>::st4(da + t, ga);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (t + e >= 0 && t + e < T) {
+            IO<TA>::st1(dx + t + e, gx[e]);
+            IO<TA>::st1(da + t + e, ga[e]);
+          }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------
+
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
+__global__ void __launch_bounds__(256) scalar_scan_kernel(const __grid_constant__ ScalarParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int L = 128 * J;
+  SegWin win;
+  if (VARLEN) {
+    win.WL = L + 8;
+    const int nwords = (win.WL + 31) >> 5;
+    win.bits = reinterpret_cast<uint32_t*>(smem);
+    win.sstart = reinterpret_cast<int*>(smem + 4 * ((nwords + 3) & ~3));
+    win.send = win.sstart + win.WL;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  (void)warp;
+  (void)lane;
+
+  if (VARIANT == VAR_LOOKBACK) {
+    __shared__ unsigned s_ticket, s_epoch;
+    if (threadIdx.x == 0) {
+      const unsigned long long te = atomicAdd(&p.hdr->ticket_epoch, 1ull);
+      s_ticket = (unsigned)te;
+      s_epoch = (unsigned)(te >> 32);
+    }
+    __syncthreads();
+    const unsigned ticket = s_ticket;
+    const uint32_t epoch = s_epoch;
+    if ((int64_t)ticket < p.ntiles) {
+      const int per_k = p.G * p.nbr;
+      const int k = (int)(ticket / (unsigned)per_k);
+      const int rem = (int)(ticket % (unsigned)per_k);
+      const int g = rem / p.nbr;
+      const int brn = rem % p.nbr;
+      if (VARLEN && ticket == 0) check_segments<MODE>(p);
+      float carry = 0.f;
+      const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
+      if (S > 0)
+        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, false, epoch, ticket, win, carry);
+      else
+        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, false, epoch, ticket, win, carry);
+    } else if (threadIdx.x == 0) {
+      set_status(p.hdr, kStatusWorkspace);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned d = atomicAdd(&p.hdr->done, 1u);
+      if (d == gridDim.x - 1) {
+        p.hdr->done = 0u;
+        atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
+        __threadfence();
+      }
+    }
+  } else {
+    const int g = blockIdx.x / p.nbr;
+    const int brn = blockIdx.x % p.nbr;
+    if (VARLEN && blockIdx.x == 0) check_segments<MODE>(p);
+    float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
+    const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
+    for (int k = 0; k < p.M; ++k) {
+      if (S > 0)
+        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, true, 0u, 0u, win, carry);
+      else
+        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, true, 0u, 0u, win, carry);
+    }
+  }
+}
+
+// Host-side dispatch over the compile-time choices.
+template <class Op, int MODE, typename TA, int VARIANT, bool VARLEN, bool VEC, int J>
+cudaError_t launch_one(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
+  auto kern = scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+  if (pl.smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)pl.smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t grid = (VARIANT == VAR_LOOKBACK) ? p.ntiles : (int64_t)p.G * p.nbr;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, 32 * p.R, pl.smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <class Op, int MODE, typename TA, int VARIANT, bool VARLEN, bool VEC>
+cudaError_t launch_pick_j(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
+  switch (pl.J) {
+    case 1: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 1>(p, pl, s);
+    case 2: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 2>(p, pl, s);
+    case 4: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 4>(p, pl, s);
+    case 8: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 8>(p, pl, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class Op, int MODE, typename TA>
+cudaError_t launch_scalar(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
+  const bool varlen = p.cu != nullptr;
+  if (pl.variant == VAR_LOOKBACK) {
+    if (varlen)
+      return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, true, true>(p, pl, s)
+                    : launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, true, false>(p, pl, s);
+    return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, false, true>(p, pl, s)
+                  : launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, false, false>(p, pl, s);
+  }
+  if (varlen)
+    return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_STATIONARY, true, true>(p, pl, s)
+                  : launch_pick_j<Op, MODE, TA, VAR_STATIONARY, true, false>(p, pl, s);
+  return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_STATIONARY, false, true>(p, pl, s)
+                : launch_pick_j<Op, MODE, TA, VAR_STATIONARY, false, false>(p, pl, s);
+}
+
+}  // namespace scan

@@ -1,0 +1,447 @@
+"""Benchmark of libscan's hot path: one step = scan_fwd + scan_bwd of the scalar
+scan on the dense [B=8, C=1536, T=4096] fp32 workload (synthetic, seeded).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dense_4k|dense_64k] [--all-rows]
+
+Prints one JSON line (rank 0). `value` is whole-job scan elements/s of the
+fwd+bwd step with inputs resident in HBM (CUDA events on the launching stream,
+L2 flushed between steps); `e2e` is the same metric through the same C ABI
+calls with pinned host buffers, host<->device copies inside the timed region.
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+Under torchrun (N > 1) every rank scans its own copy of the workload (weak
+scaling, no collective on the data path); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "scan elements/s and achieved HBM GB/s (fwd, fwd+bwd) at B=8 C=1536 T=4K–64K"
+UNIT = "elem/s"
+# fp32 algorithmic bytes per element: fwd reads a, x and writes h; bwd reads a,
+# h, dh and writes da, dx (h0 / dh0 are per row, < 0.1 %)
+FWD_BYTES = 12
+BWD_BYTES = 20
+# the pages' figure for this workload: "associative_scan_triton" README,
+# kernel-level Fwd+Bwd table, seqlen 4096: 0.602 ms on an H100 (fp32 inferred)
+PAGES_FWD_BWD_MS = {"dense_4k": 0.602, "dense_64k": 9.212}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward
+# kernel on this workload, from the ncu capture summarised in profiles/
+# (None until a capture of the current kernel exists)
+BWD_TRAFFIC_BYTES = None
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def __enter__(self):
+        sel = []
+        try:
+            uuid = torch.cuda.get_device_properties(self.dev).uuid
+            sel = ["-i", f"GPU-{uuid}"]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for line in (getattr(self, "out", "") or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_workload(name: str, rank: int):
+    from associative_affine_scan_gb300 import workloads
+    if name == "dense_4k":
+        return workloads.dense_4k(seed=rank)
+    if name == "dense_64k":
+        return workloads.dense_64k(seed=rank)
+    raise ValueError(name)
+
+
+def run_ours(args, world, rank, local):
+    import associative_affine_scan_gb300 as scan
+    if not os.path.exists(scan.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    w = make_workload(args.workload, rank)
+    B, C, T = w.a.shape
+    n = B * C * T
+    a, x, dh = (t.to(dev) for t in (w.a, w.x, w.dh))
+    h0 = w.h0.to(dev) if w.h0 is not None else None
+    h = torch.empty_like(a)
+    da, dx = torch.empty_like(a), torch.empty_like(a)
+    dh0 = torch.empty(B, C, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        scan.scan_fwd(a, x, h0, out=h)
+        scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if scan.scan_get_device_status(dev) != scan.SCAN_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps, outside the event pair
+            ev[i][0].record(stream)
+            scan.scan_fwd(a, x, h0, out=h)
+            ev[i][1].record(stream)
+            scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    status = scan.scan_get_device_status(dev)
+    if status != scan.SCAN_OK:
+        raise RuntimeError(f"device status {scan.scan_status_string(status)}")
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [f + b for f, b in zip(fwd_ms, bwd_ms)]
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms_local, world, dev)
+    fwd_avg = max_over_ranks(sum(fwd_ms) / len(fwd_ms), world, dev)
+    bwd_avg = max_over_ranks(sum(bwd_ms) / len(bwd_ms), world, dev)
+    clocks = clk.summary()
+
+    # ---- end to end through the same calls with pinned host buffers ----
+    ha, hx, hdh = (t.pin_memory() for t in (w.a, w.x, w.dh))
+    hh0 = w.h0.pin_memory() if w.h0 is not None else None
+    out_h = torch.empty(a.shape, dtype=torch.float32).pin_memory()
+    out_da, out_dx = (torch.empty(a.shape, dtype=torch.float32).pin_memory() for _ in range(2))
+    out_dh0 = torch.empty(B, C, dtype=torch.float32).pin_memory()
+    bytes_in = sum(t.numel() * t.element_size() for t in (ha, hx, hdh) + ((hh0,) if hh0 is not None else ()))
+    bytes_out = sum(t.numel() * t.element_size() for t in (out_h, out_da, out_dx, out_dh0))
+
+    def e2e_step():
+        a.copy_(ha, non_blocking=True)
+        x.copy_(hx, non_blocking=True)
+        dh.copy_(hdh, non_blocking=True)
+        if hh0 is not None:
+            h0.copy_(hh0, non_blocking=True)
+        scan.scan_fwd(a, x, h0, out=h)
+        scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
+        out_h.copy_(h, non_blocking=True)
+        out_da.copy_(da, non_blocking=True)
+        out_dx.copy_(dx, non_blocking=True)
+        out_dh0.copy_(dh0, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    extra = {}
+    if args.all_rows:
+        extra = measure_rows(args, dev, scan)
+
+    return dict(n=n, B=B, C=C, T=T, ms=ms, fwd_ms=fwd_avg, bwd_ms=bwd_avg, wall=wall,
+                clocks=clocks, e2e_ms=e2e_ms, bytes_in=bytes_in, bytes_out=bytes_out,
+                w=w, extra=extra)
+
+
+def time_calls(fn, steps, warmup, flush, stream):
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        total += s.elapsed_time(e)
+    return total / steps
+
+
+def measure_rows(args, dev, scan):
+    """Per-row throughput of the other forms (packed bidirectional, affine, log)."""
+    from associative_affine_scan_gb300 import workloads
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps, warm = max(3, min(args.steps, 10)), 3
+    out = {}
+    peak, _ = measured_peaks()
+
+    w = workloads.packed_bidir(seed=0)
+    af, xf, ar, xr, cu, dhf, dhr = (t.to(dev) for t in (w.af, w.xf, w.ar, w.xr, w.cu_seqlens,
+                                                         w.dhf, w.dhr))
+    hf, hr = scan.scan_bidir_fwd(af, xf, ar, xr, None, None, cu)
+    n = 2 * af.numel()
+    f_ms = time_calls(lambda: scan.scan_bidir_fwd(af, xf, ar, xr, None, None, cu, out=(hf, hr)),
+                      steps, warm, flush, stream)
+    g = scan.scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, None, None, cu)
+    b_ms = time_calls(lambda: scan.scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, None, None, cu, out=g),
+                      steps, warm, flush, stream)
+    out["packed_bidir"] = {"elems": n, "fwd_ms": f_ms, "bwd_ms": b_ms,
+                           "fwd_gbs": n * 8 / f_ms / 1e6, "bwd_gbs": n * 14 / b_ms / 1e6,
+                           "fwd_bwd_elem_per_s": n / (f_ms + b_ms) * 1e3}
+    del af, xf, ar, xr, dhf, dhr, hf, hr, g
+
+    w = workloads.log_4k(seed=0)
+    la, lx = w.log_a.to(dev), w.log_x.to(dev)
+    hl = scan.scan_log_fwd(la, lx)
+    n = la.numel()
+    l_ms = time_calls(lambda: scan.scan_log_fwd(la, lx, out=hl), steps, warm, flush, stream)
+    out["log_4k"] = {"elems": n, "fwd_ms": l_ms, "fwd_gbs": n * 12 / l_ms / 1e6,
+                     "frac": n * 12 / l_ms / 1e6 / peak}
+    del la, lx, hl
+
+    try:
+        w = workloads.affine_4x4(seed=0)
+        A, Bm, dH = w.A.to(dev), w.Bm.to(dev), w.dH.to(dev)
+        H = scan.affine_scan_fwd(A, Bm)
+        nb = w.n_blocks
+        f_ms = time_calls(lambda: scan.affine_scan_fwd(A, Bm, out=H), steps, warm, flush, stream)
+        g = scan.affine_scan_bwd(A, H, dH)
+        b_ms = time_calls(lambda: scan.affine_scan_bwd(A, H, dH, out=g), steps, warm, flush,
+                          stream)
+        out["affine_4x4"] = {"blocks": nb, "fwd_ms": f_ms, "bwd_ms": b_ms,
+                             "fwd_gbs": nb * 192 / f_ms / 1e6, "bwd_gbs": nb * 320 / b_ms / 1e6}
+    except Exception as e:  # not built yet
+        out["affine_4x4"] = {"error": str(e)}
+    return out
+
+
+def oracle_fwd_bwd(w, rows):
+    """The fp64 oracle on `rows` rows of the workload (fwd then bwd)."""
+    import oracle
+    B, C, T = w.a.shape
+    a = w.a.reshape(B * C, T)[:rows].double().numpy()[None]
+    x = w.x.reshape(B * C, T)[:rows].double().numpy()[None]
+    dh = w.dh.reshape(B * C, T)[:rows].double().numpy()[None]
+    h0 = w.h0.reshape(B * C)[:rows].double().numpy()[None] if w.h0 is not None else None
+    t0 = time.perf_counter()
+    oracle.scan_fwd(a, x, h0)
+    oracle.scan_bwd(a, x, dh, h0)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget_s: float = 10.0):
+    """Oracle elements/s on a bounded sample: whole rows of the workload, as many
+    as fit in about `budget_s` seconds of single-thread CPU work."""
+    B, C, T = w.a.shape
+    rows = B * C
+    probe = min(rows, 64)
+    dt = oracle_fwd_bwd(w, probe)
+    per_row = dt / probe
+    take = int(max(1, min(rows, budget_s / max(per_row, 1e-9))))
+    dt = oracle_fwd_bwd(w, take)
+    return {"value": take * T / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{take} of {rows} rows x T={T} (fwd+bwd, fp64, single thread), {dt:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return None
+    w = make_workload(args.workload, 0)
+    B, C, T = w.a.shape
+    rows = B * C
+    probe = min(rows, 32)
+    per_row = oracle_fwd_bwd(w, probe) / probe
+    # each step: as many rows as fit in ~4 s, so the whole run ends in minutes
+    take = int(max(1, min(rows, 4.0 / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_fwd_bwd(w, max(1, take // 8))
+    times = [oracle_fwd_bwd(w, take) for _ in range(args.steps)]
+    dt = sum(times) / len(times)
+    value = take * T / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "C": C, "T": T,
+                   "step": "oracle scan fwd + bwd on a bounded row sample"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{take} of {rows} rows x T={T} per step (fwd+bwd, fp64)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dense_4k", choices=["dense_4k", "dense_64k"])
+    ap.add_argument("--all-rows", action="store_true",
+                    help="also time the packed bidirectional, log and affine forms")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, world, rank, local)
+    if rank != 0:
+        barrier(world)
+        return
+    peak, peak_kind = measured_peaks()
+    n_total = r["n"] * world
+    value = n_total / (r["ms"] * 1e-3)
+    bwd_gbs = r["n"] * BWD_BYTES / (r["bwd_ms"] * 1e-3) / 1e9
+    fwd_gbs = r["n"] * FWD_BYTES / (r["fwd_ms"] * 1e-3) / 1e9
+    step_gbs = r["n"] * (FWD_BYTES + BWD_BYTES) / (r["ms"] * 1e-3) / 1e9
+    pages_ms = PAGES_FWD_BWD_MS.get(args.workload)
+    vs = value / (r["n"] / (pages_ms * 1e-3)) if pages_ms else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": vs, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": r["B"], "C": r["C"], "T": r["T"],
+                   "step": "scan_fwd + scan_bwd (fp32)", "l2": "flushed (256 MB write) between "
+                   "timed steps; per-step working set 1.2 GB > L2"},
+        "gbs": step_gbs,
+        "fwd": {"ms": r["fwd_ms"], "elem_per_s": r["n"] / (r["fwd_ms"] * 1e-3), "gbs": fwd_gbs,
+                "frac": fwd_gbs / peak},
+        "bwd": {"ms": r["bwd_ms"], "elem_per_s": r["n"] / (r["bwd_ms"] * 1e-3), "gbs": bwd_gbs,
+                "frac": bwd_gbs / peak},
+        "roofline": {"bound": "hbm", "kernel": "scalar_scan_kernel (backward)",
+                     "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
+                     "peak_source": peak_kind,
+                     "traffic": BWD_TRAFFIC_BYTES},
+        "e2e": {"value": n_total / (r["e2e_ms"] * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": r["bytes_in"], "d2h_bytes_per_step": r["bytes_out"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": r["clocks"],
+        "wall_s": r["wall"],
+        "baseline_context": {"ms": pages_ms, "hardware": "H100 80GB",
+                             "source": "associative_scan_triton README, kernel-level Fwd+Bwd"},
+    }
+    if r["extra"]:
+        line["rows"] = r["extra"]
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(r["w"])
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,233 @@
+/*
+ * libscan.h -- C ABI of libscan, the GB300 (sm_103a) associative affine scan.
+ *
+ * The library computes the first-order affine recurrence
+ *
+ *     h_t = A_t h_{t-1} + B_t
+ *
+ * forward and backward on one GPU, in three forms:
+ *   - scalar, channel-wise: h[t] = a[t] * h[t-1] + x[t] over [B, C, T], with
+ *     packed variable-length sequences (cu_seqlens), resets (a_t = 0), a
+ *     nonzero initial state and two opposite-direction branches;
+ *   - block matrix: A_t is k x k and B_t, h_t are k x v;
+ *   - log space: the scalar recurrence carried as l_t = log h_t.
+ *
+ * Sources (page titles and sections of the pages that define the operation):
+ *   [TSK]  "Triton scan kernels" (minGRU docs): One associative-scan family
+ *          (the recurrence, its monoid and the four scan ops), Kernel design
+ *          ((b, n) lanes, channel tiles, (k, v) blocks), The TF32 / IEEE
+ *          precision guard (envelope k, v in {1, 2, 4, 8, 16}), Autograd
+ *          integration and the reversed-scan backward.
+ *   [AST]  "associative_scan_triton" README: quick start (scan_causal,
+ *          scan_bidirectional_branched, cu_seqlens), how it works (chunked
+ *          scan, no cross-document leakage, backward by a reverse scan on
+ *          shifted gates with d_gates = shifted_states * d_tokens).
+ *   [RGA]  "Our RG-LRU GPU audit": Strengthened fused path (resets, nonzero
+ *          initial state and its gradient, partial final chunks), Exact real
+ *          chunk algebra (h_out = P h_in + Q).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers to contiguous row-major arrays;
+ *     scalars are passed by value. The caller owns every buffer. The library
+ *     never allocates device memory and never synchronises the stream except
+ *     in scan_get_device_status().
+ *   - Every call is asynchronous on `stream`; it returns after validating its
+ *     arguments on the host and enqueueing its kernel(s). No exception crosses
+ *     the ABI and there is no fallback: an input outside what the kernels
+ *     support returns an error status and computes nothing.
+ *   - Time index t is 0-based and h_{-1} = h0 (zero when h0 is NULL).
+ *   - Accumulation is always fp32. `a`, `x`, `da`, `dx` may be fp32 or bf16
+ *     (scan_dtype); h, h0, dh, dh0 are always fp32 ([TSK] Kernel design:
+ *     "Accumulation is fp32 regardless of input dtype").
+ *   - Dense layout: a, x, h, dh, da, dx are [B, C, T]; h0, dh0 are [B, C].
+ *     Packed layout (cu_seqlens != NULL): B must be 1, tensors are [C, T]
+ *     with T the total packed length, cu_seqlens is a device int32 array of
+ *     n_seqs + 1 non-decreasing offsets from 0 to T ([AST] quick start,
+ *     flash-attn convention), h0/dh0 are [n_seqs, C]. Empty sequences are
+ *     allowed; their dh0 rows are written as 0.
+ *   - A reset is simply a_t = 0: it erases the prefix ([RGA] Exact real chunk
+ *     algebra). No separate reset mask exists.
+ *   - Workspace: a device buffer of scan_workspace_bytes() bytes that the
+ *     caller allocates once and zeroes once with scan_workspace_init(). After
+ *     that it may be reused by any number of calls on one stream without
+ *     clearing; calls that run concurrently on the GPU need separate
+ *     workspaces. It also holds the sticky device status word read by
+ *     scan_get_device_status().
+ *   - Any base pointer may be unaligned; 16-byte aligned fp32 tensors and
+ *     8-byte aligned bf16 tensors (torch allocations are) take the
+ *     vectorised path.
+ */
+#ifndef LIBSCAN_H
+#define LIBSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LIBSCAN_VERSION 1
+
+typedef enum scan_status {
+  SCAN_OK = 0,
+  SCAN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, malformed host cu_seqlens */
+  SCAN_ERR_UNSUPPORTED = 2, /* outside the kernels' envelope (e.g. k, v not in {1,2,4,8,16}) */
+  SCAN_ERR_ALIGNMENT = 3,   /* reserved: no current entry point requires alignment */
+  SCAN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than scan_workspace_bytes() */
+  SCAN_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+  SCAN_ERR_TIMEOUT = 6,     /* device: a look-back wait ran past opts.wait_limit_s */
+  SCAN_ERR_SEQLENS = 7      /* device: cu_seqlens not 0 = cu[0] <= ... <= cu[n] = T */
+} scan_status;
+
+typedef enum scan_dtype {
+  SCAN_F32 = 0,
+  SCAN_BF16 = 1
+} scan_dtype;
+
+/* How T is split across thread blocks. STATIONARY: one block walks the whole
+ * row group in order with the running state in registers ([TSK] Kernel design;
+ * [RGA] state-stationary serial path). LOOKBACK: T is cut into chunks handled
+ * by independent blocks; each block publishes its chunk summary (P, Q)
+ * ([RGA] Exact real chunk algebra) and reads its predecessors' summaries
+ * (decoupled look-back). AUTO picks per shape. */
+typedef enum scan_variant {
+  SCAN_VARIANT_AUTO = 0,
+  SCAN_VARIANT_STATIONARY = 1,
+  SCAN_VARIANT_LOOKBACK = 2
+} scan_variant;
+
+typedef enum scan_op {
+  SCAN_OP_FWD = 0,
+  SCAN_OP_BWD = 1,
+  SCAN_OP_BIDIR_FWD = 2,
+  SCAN_OP_BIDIR_BWD = 3,
+  SCAN_OP_LOG_FWD = 4,
+  SCAN_OP_AFFINE_FWD = 5,
+  SCAN_OP_AFFINE_BWD = 6
+} scan_op;
+
+/* Optional tuning and test controls; pass NULL for the defaults (all zero). */
+typedef struct scan_opts {
+  int32_t variant;       /* scan_variant; 0 = AUTO */
+  int32_t chunk;         /* scalar/log: elements of T per block row, one of 128, 256, 512,
+                            1024; affine: time steps per block, one of 16, 32, 64; 0 = planner */
+  int32_t rows_per_cta;  /* scalar/log: rows (channels) per block, 1..16; 0 = planner */
+  int32_t test_stall;    /* test hook: 1 makes one look-back wait on a summary that is
+                            never published, so the wait limit expires (SCAN_ERR_TIMEOUT) */
+  double wait_limit_s;   /* bound on every look-back wait; <= 0 means 1.0 second */
+  const int32_t* cu_seqlens_host; /* optional host copy of cu_seqlens, validated before launch */
+} scan_opts;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* scan_status_string(scan_status status);
+
+/* LIBSCAN_VERSION of the loaded library. */
+int32_t scan_version(void);
+
+/* Bytes of workspace a call of `op` with these sizes needs under `opts`
+ * (NULL = defaults). Scalar/log ops: (B, C, T) as in the call, k = v = 0.
+ * Affine ops: B = batch, C = N (state blocks), T = time, and k, v.
+ * Returns 0 for arguments the call itself would reject. */
+size_t scan_workspace_bytes(scan_op op, int64_t B, int64_t C, int64_t T,
+                            int32_t k, int32_t v, const scan_opts* opts);
+
+/* Zero a freshly allocated workspace (asynchronous on `stream`). */
+scan_status scan_workspace_init(void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/* Synchronise `stream`, read the workspace's sticky device status
+ * (SCAN_ERR_TIMEOUT, SCAN_ERR_SEQLENS or SCAN_OK), reset it to SCAN_OK and
+ * return it. */
+scan_status scan_get_device_status(void* workspace, cudaStream_t stream);
+
+/* Scalar forward ([AST] quick start, scan_causal; [TSK] linear_scan):
+ *   reverse == 0: h_t = a_t h_{t-1} + x_t, h_{-1} = h0;
+ *   reverse != 0: h_t = a_t h_{t+1} + x_t, h_T = h0 (per row or sequence).
+ * a, x: [B,C,T] or packed [C,T] of `dt`; h0: nullable fp32 [B,C] or
+ * [n_seqs,C]; h: fp32 output. */
+scan_status scan_fwd(const void* a, const void* x, const float* h0,
+                     const int32_t* cu_seqlens, int32_t n_seqs, float* h,
+                     int64_t B, int64_t C, int64_t T, scan_dtype dt,
+                     int32_t reverse, const scan_opts* opts, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Scalar backward of L = sum_t <dh_t, h_t> ([AST] how it works: d_tokens by a
+ * reverse scan on shifted gates, d_gates = shifted_states * d_tokens):
+ *   g_t = dh_t + a_{t+1} g_{t+1} (a_{t+1} = 0 past the sequence end),
+ *   dx_t = g_t, da_t = g_t h_{t-1} (h_{-1} = h0), dh0 = a_0 g_0
+ * (mirrored when reverse != 0). `h` is the forward output, used as the
+ * shifted state so no forward state is recomputed or stored ([TSK]
+ * Autograd integration: the backward reads only the forward's inputs and
+ * outputs). h0 is needed for da at a sequence start (nullable = 0). da, dx
+ * have dtype `dt`; dh0 is a nullable fp32 output. */
+scan_status scan_bwd(const void* a, const float* h, const float* dh,
+                     const float* h0, const int32_t* cu_seqlens, int32_t n_seqs,
+                     void* da, void* dx, float* dh0, int64_t B, int64_t C,
+                     int64_t T, scan_dtype dt, int32_t reverse,
+                     const scan_opts* opts, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Two independent branches in one launch ([AST] quick start,
+ * scan_bidirectional_branched): branch f is causal over (af, xf), branch r
+ * runs from each sequence's end over (ar, xr). Same result as scan_fwd with
+ * reverse = 0 and reverse = 1; the outputs are separate, not summed. */
+scan_status scan_bidir_fwd(const void* af, const void* xf, const void* ar,
+                           const void* xr, const float* h0f, const float* h0r,
+                           const int32_t* cu_seqlens, int32_t n_seqs,
+                           float* hf, float* hr, int64_t B, int64_t C,
+                           int64_t T, scan_dtype dt, const scan_opts* opts,
+                           void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/* Backward of both branches in one launch; equal to scan_bwd with
+ * reverse = 0 on branch f and reverse = 1 on branch r. */
+scan_status scan_bidir_bwd(const void* af, const float* hf, const float* dhf,
+                           const float* h0f, const void* ar, const float* hr,
+                           const float* dhr, const float* h0r,
+                           const int32_t* cu_seqlens, int32_t n_seqs,
+                           void* daf, void* dxf, float* dh0f, void* dar,
+                           void* dxr, float* dh0r, int64_t B, int64_t C,
+                           int64_t T, scan_dtype dt, const scan_opts* opts,
+                           void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/* Log-space forward ([TSK] One associative-scan family, parallel_scan_log):
+ *   l_t = log(exp(l_{t-1} + log_a_t) + exp(log_x_t)), l_{-1} = log_h0
+ *   (-inf when log_h0 is NULL), output h_t = exp(l_t) in linear space.
+ * log_a may be -inf (a reset). All fp32; layouts as scan_fwd. */
+scan_status scan_log_fwd(const float* log_a, const float* log_x,
+                         const float* log_h0, const int32_t* cu_seqlens,
+                         int32_t n_seqs, float* h, int64_t B, int64_t C,
+                         int64_t T, int32_t reverse, const scan_opts* opts,
+                         void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* Block-matrix forward ([TSK] One associative-scan family, matrix_affine_scan;
+ * Kernel design): H_t = A_t H_{t-1} + B_t per (b, n) lane, H_{-1} = h0.
+ * A: [B,T,N,k,k], Bm and H: [B,T,N,k,v], h0: nullable [B,N,k,v]; row-major
+ * matrices; fp32. Supported (k, v): k = v = 4 and k = 1 with v = 1;
+ * others return SCAN_ERR_UNSUPPORTED. */
+scan_status affine_scan_fwd(const float* A, const float* Bm, const float* h0,
+                            float* H, int64_t B, int64_t T, int64_t N,
+                            int32_t k, int32_t v, const scan_opts* opts,
+                            void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/* Block-matrix backward of L = sum_t <dH_t, H_t> ([TSK] Autograd integration
+ * and the reversed-scan backward): G_t = dH_t + A_{t+1}^T G_{t+1},
+ * dB_t = G_t, dA_t = G_t H_{t-1}^T (H_{-1} = h0), dh0 = A_0^T G_0.
+ * H is the forward output; dh0 is nullable. Same envelope as the forward. */
+scan_status affine_scan_bwd(const float* A, const float* H, const float* dH,
+                            const float* h0, float* dA, float* dB, float* dh0,
+                            int64_t B, int64_t T, int64_t N, int32_t k,
+                            int32_t v, const scan_opts* opts, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSCAN_H */

@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: the library builds, loads and exports every entry
+point that include/libscan.h declares, and host-side argument checks reject bad
+input before anything is launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    from associative_affine_scan_gb300 import build_lib
+    path = build_lib.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "libscan.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd", "scan_log_fwd",
+               "affine_scan_fwd", "affine_scan_bwd", "scan_workspace_bytes",
+               "scan_workspace_init", "scan_get_device_status", "scan_status_string"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(built):
+    for name in declared_functions():
+        assert hasattr(built, name), name
+
+
+def test_binding_names_match_the_header():
+    import associative_affine_scan_gb300 as scan
+    for name in declared_functions():
+        assert name in scan.EXPORTED
+        assert callable(getattr(scan, name))
+
+
+def test_status_strings_and_version():
+    import associative_affine_scan_gb300 as scan
+    assert scan.scan_version() == 1
+    for code in range(8):
+        assert scan.scan_status_string(code).startswith("SCAN_")
+
+
+def test_workspace_sizes():
+    import associative_affine_scan_gb300 as scan
+    # look-back: header + 16 bytes per (branch, row, chunk of 512)
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096) == 256 + 12288 * 8 * 16
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_BIDIR_FWD, 1, 2048, 1000) == \
+        256 + 2 * 2048 * 2 * 16
+    # stationary needs only the header
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096,
+                                     opts={"variant": scan.SCAN_VARIANT_STATIONARY}) == 256
+    # rejected arguments size to 0
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, -1, 4, 4) == 0
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 100}) == 0
+
+
+def _raw(name):
+    import associative_affine_scan_gb300 as scan
+    return getattr(scan.lib(), name)
+
+
+def test_host_side_checks_need_no_gpu():
+    import associative_affine_scan_gb300 as scan
+    f = _raw("scan_fwd")
+    fake = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x100000)
+    # bad dtype
+    assert f(fake, fake, None, None, 0, fake, 1, 1, 4, 7, 0, None, ws, 4096, None) == \
+        scan.SCAN_ERR_INVALID_ARG
+    # negative size
+    assert f(fake, fake, None, None, 0, fake, 1, -1, 4, 0, 0, None, ws, 4096, None) == \
+        scan.SCAN_ERR_INVALID_ARG
+    # packed layout requires B == 1
+    assert f(fake, fake, None, fake, 1, fake, 2, 1, 4, 0, 0, None, ws, 4096, None) == \
+        scan.SCAN_ERR_INVALID_ARG
+    # missing / short workspace
+    assert f(fake, fake, None, None, 0, fake, 1, 4, 4096, 0, 0, None, None, 0, None) == \
+        scan.SCAN_ERR_WORKSPACE
+    assert f(fake, fake, None, None, 0, fake, 1, 4, 4096, 0, 0, None, ws, 300, None) == \
+        scan.SCAN_ERR_WORKSPACE
+    # malformed host copy of cu_seqlens
+    opts = scan.ScanOpts()
+    bad = (ctypes.c_int32 * 3)(0, 7, 5)
+    opts.cu_seqlens_host = ctypes.cast(bad, ctypes.POINTER(ctypes.c_int32))
+    assert f(fake, fake, None, fake, 2, fake, 1, 4, 5, 0, 0, ctypes.byref(opts), ws, 1 << 20,
+             None) == scan.SCAN_ERR_INVALID_ARG
+    # bad option values
+    opts = scan.ScanOpts()
+    opts.rows_per_cta = 99
+    assert f(fake, fake, None, None, 0, fake, 1, 4, 64, 0, 0, ctypes.byref(opts), ws, 1 << 20,
+             None) == scan.SCAN_ERR_INVALID_ARG
+    # empty problem: nothing to launch, OK
+    assert f(None, None, None, None, 0, None, 1, 0, 64, 0, 0, None, ws, 4096, None) == scan.SCAN_OK
+
+
+def test_affine_envelope_rejected_on_host():
+    import associative_affine_scan_gb300 as scan
+    f = _raw("affine_scan_fwd")
+    fake = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x100000)
+    assert f(fake, fake, None, fake, 1, 8, 4, 3, 4, None, ws, 1 << 20, None) == \
+        scan.SCAN_ERR_UNSUPPORTED

@@ -230,8 +230,9 @@ _ws = _Workspaces()
 def workspace_for(op: int, B: int, C: int, T: int, k: int, v: int, opts, device, stream):
     o = _opts(opts)
     n = lib().scan_workspace_bytes(op, B, C, T, k, v, _optref(o))
-    if n == 0:
-        raise ScanError(SCAN_ERR_INVALID_ARG, "scan_workspace_bytes")
+    # 0 means the call itself will reject its arguments; give it a header-sized
+    # workspace so that it reports its own, more precise status
+    n = max(int(n), 4096)
     return _ws.get(n, device, stream), n, o
 
 

@@ -1,0 +1,482 @@
+// scan_affine.cu -- block-matrix affine scan H_t = A_t H_{t-1} + B_t.
+//
+// "Triton scan kernels", One associative-scan family: A_t is k x k, B_t and
+// H_t are k x v, and "apply (A1, B1) then (A2, B2)" = (A2 A1, A2 B1 + B2)
+// is associative but not commutative, so every composition below keeps the
+// time order. The backward ("Autograd integration and the reversed-scan
+// backward") is the same scan run from the end over (A_{t+1}^T, dH_t):
+// G_t = A_{t+1}^T G_{t+1} + dH_t, dB_t = G_t, dA_t = G_t H_{t-1}^T,
+// dh0 = A_0^T G_0, reading only the forward's inputs and output.
+//
+// Work decomposition: one (b, n) lane is a state block walking T. A block of
+// 128 threads takes 32 consecutive lanes (one per thread of a warp, so each
+// warp step reads 32 adjacent k x k blocks = one contiguous run of memory) and
+// one chunk of 4 * LS steps, split into 4 sub-chunks (one per warp):
+//   pass 1: each thread composes its sub-chunk into a summary (P, Q) in fp32
+//           registers (time order kept);
+//   warp 0: composes the 4 sub-chunk summaries into the chunk summary,
+//           publishes it, obtains the chunk's carry-in by a decoupled
+//           look-back over earlier chunks' published summaries (bounded
+//           waits), publishes the chunk's inclusive state and hands each
+//           sub-chunk its own carry-in through shared memory;
+//   pass 3: each thread replays its sub-chunk from its carry-in (the chunk's
+//           inputs were read microseconds earlier and are served from L2) and
+//           writes the outputs.
+// Chunks are taken in ticket order, chunk index major, so the chunks a block
+// waits for belong to blocks that are already running or finished.
+#include <cuda_runtime.h>
+
+#include "scan_scalar.cuh"
+
+namespace scan {
+namespace {
+
+constexpr int kSub = 4;     // sub-chunks (warps) per block
+constexpr int kLanes = 32;  // state-block lanes per block
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// n floats (n % 4 == 0, 16-byte aligned). keep: leave the lines in L2 for a
+// second read; otherwise stream (evict first).
+template <int N>
+__device__ __forceinline__ void ldv(const float* p, float (&r)[N], bool keep) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 q = keep ? __ldg(reinterpret_cast<const float4*>(p + i))
+                          : __ldcs(reinterpret_cast<const float4*>(p + i));
+    r[i] = q.x;
+    r[i + 1] = q.y;
+    r[i + 2] = q.z;
+    r[i + 3] = q.w;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void ldv_cg(const float* p, float (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 q = __ldcg(reinterpret_cast<const float4*>(p + i));
+    r[i] = q.x;
+    r[i + 1] = q.y;
+    r[i + 2] = q.z;
+    r[i + 3] = q.w;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void stv(float* p, const float (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4)
+    __stcs(reinterpret_cast<float4*>(p + i), make_float4(r[i], r[i + 1], r[i + 2], r[i + 3]));
+}
+
+template <int N>
+__device__ __forceinline__ void stv_cg(float* p, const float (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4)
+    __stcg(reinterpret_cast<float4*>(p + i), make_float4(r[i], r[i + 1], r[i + 2], r[i + 3]));
+}
+
+template <int N>
+__device__ __forceinline__ void fill(float (&r)[N], float v) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) r[i] = v;
+}
+
+template <int K>
+__device__ __forceinline__ void set_identity(float (&r)[K * K]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i)
+#pragma unroll
+    for (int j = 0; j < K; ++j) r[i * K + j] = (i == j) ? 1.f : 0.f;
+}
+
+// Y = M X (M k x k row-major, X k x w); Y must not alias X.
+template <int K, int W>
+__device__ __forceinline__ void mul(const float (&M)[K * K], const float (&X)[K * W],
+                                    float (&Y)[K * W]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i)
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      float acc = M[i * K] * X[j];
+#pragma unroll
+      for (int l = 1; l < K; ++l) acc = fmaf(M[i * K + l], X[l * W + j], acc);
+      Y[i * W + j] = acc;
+    }
+}
+
+// Y = M^T X
+template <int K, int W>
+__device__ __forceinline__ void mul_t(const float (&M)[K * K], const float (&X)[K * W],
+                                      float (&Y)[K * W]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i)
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      float acc = M[i] * X[j];
+#pragma unroll
+      for (int l = 1; l < K; ++l) acc = fmaf(M[l * K + i], X[l * W + j], acc);
+      Y[i * W + j] = acc;
+    }
+}
+
+// Y = M X + D
+template <int K, int W>
+__device__ __forceinline__ void mul_add(const float (&M)[K * K], const float (&X)[K * W],
+                                        const float (&D)[K * W], float (&Y)[K * W]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i)
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      float acc = D[i * W + j];
+#pragma unroll
+      for (int l = 0; l < K; ++l) acc = fmaf(M[i * K + l], X[l * W + j], acc);
+      Y[i * W + j] = acc;
+    }
+}
+
+// Y = M^T X + D
+template <int K, int W>
+__device__ __forceinline__ void mul_t_add(const float (&M)[K * K], const float (&X)[K * W],
+                                          const float (&D)[K * W], float (&Y)[K * W]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i)
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      float acc = D[i * W + j];
+#pragma unroll
+      for (int l = 0; l < K; ++l) acc = fmaf(M[l * K + i], X[l * W + j], acc);
+      Y[i * W + j] = acc;
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void copy(const float (&s)[N], float (&d)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) d[i] = s[i];
+}
+
+// Record of one (lane, chunk) in the workspace: P (k x k), Q (k x v), the
+// inclusive state (k x v), then two epoch-tagged flags (summary, inclusive).
+template <int K, int V>
+struct RecLayout {
+  static constexpr int kP = 0;
+  static constexpr int kQ = K * K;
+  static constexpr int kH = K * K + K * V;
+  static constexpr int kFlags = K * K + 2 * K * V;
+  static constexpr int kFloats = ((kFlags + 2) + 3) & ~3;
+};
+
+// Carry-in of chunk k of one lane: walk back over the lane's earlier chunks,
+// composing their summaries (later ones applied last) until one publishes
+// its inclusive state. Bounded by p.wait_limit_ns.
+template <int K, int V>
+__device__ void lookback(const AffineParams& p, const float* lane_recs, int k, uint32_t epoch,
+                         bool stalled, unsigned ticket, int64_t lane_id, float (&carry)[K * V]) {
+  using RL = RecLayout<K, V>;
+  uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
+  if (stalled) tag_agg = tag_inc = 0xffffffffu;
+  float Pacc[K * K], Qacc[K * V];
+  set_identity<K>(Pacc);
+  fill(Qacc, 0.f);
+  int pos = k - 1;
+  const unsigned long long t_begin = global_ns();
+  unsigned backoff = 32;
+  while (pos >= 0) {
+    const float* r = lane_recs + (int64_t)pos * RL::kFloats;
+    const unsigned* flags = reinterpret_cast<const unsigned*>(r + RL::kFlags);
+    if (ld_acquire_u32(flags + 1) == tag_inc) {
+      float Hc[K * V], tmp[K * V];
+      ldv_cg(r + RL::kH, Hc);
+      mul_add<K, V>(Pacc, Hc, Qacc, tmp);
+      copy(tmp, carry);
+      return;
+    }
+    if (ld_acquire_u32(flags) == tag_agg) {
+      float Pp[K * K], Qp[K * V], tq[K * V], tp[K * K];
+      ldv_cg(r + RL::kP, Pp);
+      ldv_cg(r + RL::kQ, Qp);
+      mul_add<K, V>(Pacc, Qp, Qacc, tq);  // earlier chunk applied first
+      mul<K, K>(Pacc, Pp, tp);
+      copy(tq, Qacc);
+      copy(tp, Pacc);
+      --pos;
+      backoff = 32;
+      continue;
+    }
+    if (global_ns() - t_begin > p.wait_limit_ns) {
+      set_status(p.hdr, kStatusTimeout);
+      p.hdr->info[0] = ticket;
+      p.hdr->info[1] = 0;
+      p.hdr->info[2] = (unsigned)lane_id;
+      p.hdr->info[3] = (unsigned)k;
+      break;
+    }
+    __nanosleep(backoff);
+    backoff = backoff < 1024 ? backoff * 2 : 1024;
+  }
+  // chunk 0 always publishes its inclusive state, so this is reached only
+  // after a timeout: continue from a zero state
+  copy(Qacc, carry);
+}
+
+template <int K, int V, int LS, int MODE>
+__global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ AffineParams p) {
+  constexpr int KK = K * K, KV = K * V;
+  using RL = RecLayout<K, V>;
+  __shared__ float s_sum[kSub][kLanes][KK + KV];
+  __shared__ float s_in[kSub][kLanes][KV];
+  __shared__ unsigned s_ticket, s_epoch;
+
+  if (threadIdx.x == 0) {
+    const unsigned long long te = atomicAdd(&p.hdr->ticket_epoch, 1ull);
+    s_ticket = (unsigned)te;
+    s_epoch = (unsigned)(te >> 32);
+  }
+  __syncthreads();
+  const unsigned ticket = s_ticket;
+  const uint32_t epoch = s_epoch;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if ((int64_t)ticket < p.ntiles) {
+    const int k = (int)(ticket / (unsigned)p.G);
+    const int g = (int)(ticket % (unsigned)p.G);
+    const int64_t groups_n = (p.N + kLanes - 1) / kLanes;
+    const int64_t b = g / groups_n;
+    const int64_t n = (g % groups_n) * kLanes + lane;
+    const bool active = n < p.N;
+    const int m = (MODE == MODE_FWD) ? k : (p.M - 1 - k);
+    const int64_t T = p.T;
+    const int64_t t_lo = (int64_t)m * (kSub * LS) + (int64_t)warp * LS;
+    const int64_t t_hi = t_lo + LS < T ? t_lo + LS : T;
+    const int64_t lane_id = b * p.N + (active ? n : 0);
+    const int64_t NN = p.N;
+    auto blk = [&](int64_t t) -> int64_t { return (b * T + t) * NN + n; };
+
+    // ---- pass 1: sub-chunk summary ----
+    float P[KK], Q[KV];
+    set_identity<K>(P);
+    fill(Q, 0.f);
+    if (active && t_lo < t_hi) {
+      if (MODE == MODE_FWD) {
+        float An[KK], Bn[KV];
+        ldv(p.A + blk(t_lo) * KK, An, true);
+        ldv(p.Bm + blk(t_lo) * KV, Bn, true);
+        for (int64_t t = t_lo; t < t_hi; ++t) {
+          float Ac[KK], Bc[KV], tq[KV], tp[KK];
+          copy(An, Ac);
+          copy(Bn, Bc);
+          if (t + 1 < t_hi) {
+            ldv(p.A + blk(t + 1) * KK, An, true);
+            ldv(p.Bm + blk(t + 1) * KV, Bn, true);
+          }
+          mul_add<K, V>(Ac, Q, Bc, tq);
+          mul<K, K>(Ac, P, tp);
+          copy(tq, Q);
+          copy(tp, P);
+        }
+      } else {
+        // G_t = A_{t+1}^T G_{t+1} + dH_t, walking t downwards
+        float An[KK], Dn[KV];
+        {
+          const int64_t t = t_hi - 1;
+          if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, An, true);
+          else fill(An, 0.f);
+          ldv(p.dH + blk(t) * KV, Dn, true);
+        }
+        for (int64_t t = t_hi - 1; t >= t_lo; --t) {
+          float Ac[KK], Dc[KV], tq[KV], tp[KK];
+          copy(An, Ac);
+          copy(Dn, Dc);
+          if (t - 1 >= t_lo) {
+            ldv(p.A + blk(t) * KK, An, true);
+            ldv(p.dH + blk(t - 1) * KV, Dn, true);
+          }
+          mul_t_add<K, V>(Ac, Q, Dc, tq);
+          mul_t<K, K>(Ac, P, tp);
+          copy(tq, Q);
+          copy(tp, P);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < KK; ++i) s_sum[warp][lane][i] = P[i];
+#pragma unroll
+    for (int i = 0; i < KV; ++i) s_sum[warp][lane][KK + i] = Q[i];
+    __syncthreads();
+
+    // ---- chunk summary, look-back, carry-ins (warp 0, one thread per lane) ----
+    if (warp == 0 && active) {
+      float Pt[KK], Qt[KV];
+      set_identity<K>(Pt);
+      fill(Qt, 0.f);
+#pragma unroll
+      for (int q = 0; q < kSub; ++q) {
+        const int s = (MODE == MODE_FWD) ? q : kSub - 1 - q;
+        float Ps[KK], Qs[KV], tq[KV], tp[KK];
+#pragma unroll
+        for (int i = 0; i < KK; ++i) Ps[i] = s_sum[s][lane][i];
+#pragma unroll
+        for (int i = 0; i < KV; ++i) Qs[i] = s_sum[s][lane][KK + i];
+        mul_add<K, V>(Ps, Qt, Qs, tq);  // sub-chunk s applied after the earlier ones
+        mul<K, K>(Ps, Pt, tp);
+        copy(tq, Qt);
+        copy(tp, Pt);
+      }
+      float* lane_recs = p.recs + lane_id * (int64_t)p.M * RL::kFloats;
+      float* rec = lane_recs + (int64_t)k * RL::kFloats;
+      unsigned* flags = reinterpret_cast<unsigned*>(rec + RL::kFlags);
+      const uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
+      float carry[KV];
+      if (k == 0) {
+        if (MODE == MODE_FWD && p.h0) ldv(p.h0 + lane_id * KV, carry, false);
+        else fill(carry, 0.f);
+      } else {
+        stv_cg(rec + RL::kP, Pt);
+        stv_cg(rec + RL::kQ, Qt);
+        __threadfence();
+        st_release_u32(flags, tag_agg);
+        const bool stalled = p.test_stall && lane_id == 0 && k == 1;
+        lookback<K, V>(p, lane_recs, k, epoch, stalled, ticket, lane_id, carry);
+      }
+      {
+        float Hout[KV];
+        mul_add<K, V>(Pt, carry, Qt, Hout);
+        stv_cg(rec + RL::kH, Hout);
+        __threadfence();
+        st_release_u32(flags + 1, tag_inc);
+      }
+#pragma unroll
+      for (int q = 0; q < kSub; ++q) {
+        const int s = (MODE == MODE_FWD) ? q : kSub - 1 - q;
+#pragma unroll
+        for (int i = 0; i < KV; ++i) s_in[s][lane][i] = carry[i];
+        float Ps[KK], Qs[KV], tq[KV];
+#pragma unroll
+        for (int i = 0; i < KK; ++i) Ps[i] = s_sum[s][lane][i];
+#pragma unroll
+        for (int i = 0; i < KV; ++i) Qs[i] = s_sum[s][lane][KK + i];
+        mul_add<K, V>(Ps, carry, Qs, tq);
+        copy(tq, carry);
+      }
+    }
+    __syncthreads();
+
+    // ---- pass 3: replay the sub-chunk from its carry-in ----
+    if (active && t_lo < t_hi) {
+      float c[KV];
+#pragma unroll
+      for (int i = 0; i < KV; ++i) c[i] = s_in[warp][lane][i];
+      if (MODE == MODE_FWD) {
+        float An[KK], Bn[KV];
+        ldv(p.A + blk(t_lo) * KK, An, false);
+        ldv(p.Bm + blk(t_lo) * KV, Bn, false);
+        for (int64_t t = t_lo; t < t_hi; ++t) {
+          float Ac[KK], Bc[KV], h[KV];
+          copy(An, Ac);
+          copy(Bn, Bc);
+          if (t + 1 < t_hi) {
+            ldv(p.A + blk(t + 1) * KK, An, false);
+            ldv(p.Bm + blk(t + 1) * KV, Bn, false);
+          }
+          mul_add<K, V>(Ac, c, Bc, h);
+          stv(p.out_H + blk(t) * KV, h);
+          copy(h, c);
+        }
+      } else {
+        for (int64_t t = t_hi - 1; t >= t_lo; --t) {
+          float An[KK], Dn[KV], Hp[KV], gnew[KV], dA[KK];
+          if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, An, false);
+          else fill(An, 0.f);
+          ldv(p.dH + blk(t) * KV, Dn, false);
+          if (t >= 1) ldv(p.H + blk(t - 1) * KV, Hp, false);
+          else if (p.h0) ldv(p.h0 + lane_id * KV, Hp, false);
+          else fill(Hp, 0.f);
+          mul_t_add<K, V>(An, c, Dn, gnew);
+          copy(gnew, c);
+          stv(p.dB + blk(t) * KV, c);
+          // dA_t = G_t H_{t-1}^T
+#pragma unroll
+          for (int i = 0; i < K; ++i)
+#pragma unroll
+            for (int l = 0; l < K; ++l) {
+              float acc = c[i * V] * Hp[l * V];
+#pragma unroll
+              for (int j = 1; j < V; ++j) acc = fmaf(c[i * V + j], Hp[l * V + j], acc);
+              dA[i * K + l] = acc;
+            }
+          stv(p.dA + blk(t) * KK, dA);
+          if (t == 0 && p.dh0) {
+            float A0[KK], d0[KV];
+            ldv(p.A + blk(0) * KK, A0, false);
+            mul_t<K, V>(A0, c, d0);
+            stv(p.dh0 + lane_id * KV, d0);
+          }
+        }
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    set_status(p.hdr, kStatusWorkspace);
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned d = atomicAdd(&p.hdr->done, 1u);
+    if (d == gridDim.x - 1) {
+      p.hdr->done = 0u;
+      atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
+      __threadfence();
+    }
+  }
+}
+
+template <int K, int V, int MODE>
+cudaError_t launch_kv(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
+  if (p.ntiles <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)p.ntiles;
+  switch (pl.Lc / kSub) {
+    case 16: affine_kernel<K, V, 16, MODE><<<grid, 128, 0, s>>>(p); break;
+    case 32: affine_kernel<K, V, 32, MODE><<<grid, 128, 0, s>>>(p); break;
+    case 64: affine_kernel<K, V, 64, MODE><<<grid, 128, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_affine(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
+  if (p.k == 4 && p.v == 4) return launch_kv<4, 4, MODE>(p, pl, s);
+  if (p.k == 2 && p.v == 2) return launch_kv<2, 2, MODE>(p, pl, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int affine_record_floats(int k, int v) {
+  if (k == 4 && v == 4) return RecLayout<4, 4>::kFloats;
+  if (k == 2 && v == 2) return RecLayout<2, 2>::kFloats;
+  return 0;
+}
+
+int affine_sub_chunks() { return kSub; }
+int affine_lanes_per_block() { return kLanes; }
+
+cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
+  return launch_affine<MODE_FWD>(p, pl, s);
+}
+
+cudaError_t launch_affine_bwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
+  return launch_affine<MODE_BWD>(p, pl, s);
+}
+
+}  // namespace scan

@@ -13,6 +13,8 @@ using namespace scan;
 namespace {
 
 constexpr int64_t kMaxGrid = 0x7fffffffLL;
+constexpr int64_t kStationaryMinRows = 152 * 16;
+constexpr int kCuSmemEntries = 4096;  // packed offsets staged in shared memory
 
 __global__ void fill_zero_kernel(float* p, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -59,7 +61,7 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   }
   int R = o.rows_per_cta;
   if (R < 0 || R > 8) return SCAN_ERR_INVALID_ARG;
-  if (R == 0) R = rows < 8 ? (int)(rows > 0 ? rows : 1) : 8;
+  if (R == 0) R = rows < 4 ? (int)(rows > 0 ? rows : 1) : 4;
   const int64_t L = 128LL * J;
   // the vectorised path shifts each row by up to 3 elements
   const int64_t span = T + ((T % 4) ? 3 : 0);
@@ -67,7 +69,12 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   const int64_t G = (rows + R - 1) / R;
   int variant = o.variant;
   if (variant < 0 || variant > 2) return SCAN_ERR_INVALID_ARG;
-  if (variant == SCAN_VARIANT_AUTO) variant = VAR_LOOKBACK;
+  // Stationary blocks walk T in order with the carry in registers and no
+  // inter-block traffic; that needs enough rows to occupy every SM (one warp
+  // per row, about 16 resident warps per SM on 152 SMs). Fewer rows split T
+  // across blocks and use the look-back.
+  if (variant == SCAN_VARIANT_AUTO)
+    variant = rows * nbr >= kStationaryMinRows ? VAR_STATIONARY : VAR_LOOKBACK;
   const int64_t tiles = M * G * nbr;
   if (M > kMaxGrid || G > kMaxGrid || tiles > kMaxGrid || rows * M * nbr > (1LL << 40))
     return SCAN_ERR_UNSUPPORTED;
@@ -79,13 +86,28 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   pl->vec = true;
   pl->ws_bytes = kWsHeaderBytes +
                  (variant == VAR_LOOKBACK ? (size_t)(nbr * rows * M) * 16u : (size_t)0);
-  if (varlen) {
-    const int WL = (int)L + 8;
-    const int nwords = (WL + 31) / 32;
-    pl->smem = 4u * (size_t)((nwords + 3) & ~3) + 8u * (size_t)WL;
-  } else {
-    pl->smem = 0;
-  }
+  (void)varlen;
+  pl->smem = 0;
+  return SCAN_OK;
+}
+
+// Per-shape plan for the block-matrix form: a block covers 32 lanes and one
+// chunk of Lc steps (4 sub-chunks of Lc / 4).
+scan_status plan_affine(int64_t B, int64_t T, int64_t N, int k, int v, const scan_opts& o,
+                        AffinePlan* pl) {
+  if (B < 0 || T < 0 || N < 0) return SCAN_ERR_INVALID_ARG;
+  const int rec = affine_record_floats(k, v);
+  if (rec == 0) return SCAN_ERR_UNSUPPORTED;
+  int Lc = o.chunk ? o.chunk : 128;
+  if (Lc != 64 && Lc != 128 && Lc != 256) return SCAN_ERR_INVALID_ARG;
+  const int64_t lanes = affine_lanes_per_block();
+  const int64_t M = T > 0 ? (T + Lc - 1) / Lc : 0;
+  const int64_t G = B * ((N + lanes - 1) / lanes);
+  if (M * G > kMaxGrid) return SCAN_ERR_UNSUPPORTED;
+  pl->Lc = Lc;
+  pl->M = (int)M;
+  pl->G = (int)G;
+  pl->ws_bytes = kWsHeaderBytes + (size_t)(B * N * M) * (size_t)rec * sizeof(float);
   return SCAN_OK;
 }
 
@@ -115,6 +137,7 @@ scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t 
   if (st != SCAN_OK) return st;
   if (!ws) return SCAN_ERR_WORKSPACE;
   if (ws_bytes < pl->ws_bytes || !aligned(ws, 16)) return SCAN_ERR_WORKSPACE;
+  if (cu) pl->smem = 4u * (size_t)(n_seqs + 1 <= kCuSmemEntries ? n_seqs + 1 : kCuSmemEntries);
   std::memset(p, 0, sizeof(*p));
   p->cu = cu;
   p->n_seqs = cu ? n_seqs : 1;
@@ -186,10 +209,10 @@ size_t scan_workspace_bytes(scan_op op, int64_t B, int64_t C, int64_t T, int32_t
     case SCAN_OP_BIDIR_BWD:
       return plan_scalar(B * C, T, 2, false, o, &pl) == SCAN_OK ? pl.ws_bytes : 0;
     case SCAN_OP_AFFINE_FWD:
-    case SCAN_OP_AFFINE_BWD:
-      (void)k;
-      (void)v;
-      return kWsHeaderBytes;
+    case SCAN_OP_AFFINE_BWD: {
+      AffinePlan ap;
+      return plan_affine(B, T, C, k, v, o, &ap) == SCAN_OK ? ap.ws_bytes : 0;
+    }
     default:
       return 0;
   }
@@ -355,21 +378,79 @@ scan_status scan_log_fwd(const float* log_a, const float* log_x, const float* lo
   return from_cuda(launch_log_fwd(p, pl, stream));
 }
 
+}  // extern "C"
+
+namespace {
+
+scan_status prepare_affine(int64_t B, int64_t T, int64_t N, int32_t k, int32_t v,
+                           const scan_opts& o, void* ws, size_t ws_bytes, AffineParams* p,
+                           AffinePlan* pl) {
+  scan_status st = plan_affine(B, T, N, k, v, o, pl);
+  if (st != SCAN_OK) return st;
+  if (!ws || ws_bytes < pl->ws_bytes || !aligned(ws, 16)) return SCAN_ERR_WORKSPACE;
+  std::memset(p, 0, sizeof(*p));
+  p->B = B;
+  p->T = T;
+  p->N = N;
+  p->k = k;
+  p->v = v;
+  p->Lc = pl->Lc;
+  p->M = pl->M;
+  p->G = pl->G;
+  p->ntiles = (int64_t)pl->M * pl->G;
+  p->hdr = static_cast<WsHeader*>(ws);
+  p->recs = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeaderBytes);
+  p->wait_limit_ns = wait_ns(o);
+  p->test_stall = o.test_stall;
+  return SCAN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 scan_status affine_scan_fwd(const float* A, const float* Bm, const float* h0, float* H, int64_t B,
                             int64_t T, int64_t N, int32_t k, int32_t v, const scan_opts* opts,
                             void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)A; (void)Bm; (void)h0; (void)H; (void)B; (void)T; (void)N; (void)k; (void)v;
-  (void)opts; (void)ws; (void)ws_bytes; (void)stream;
-  return SCAN_ERR_UNSUPPORTED;
+  const scan_opts o = defaults(opts);
+  AffineParams p;
+  AffinePlan pl;
+  scan_status st = prepare_affine(B, T, N, k, v, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  if (B * T * N == 0) return SCAN_OK;
+  if (!A || !Bm || !H) return SCAN_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(Bm, 16) || !aligned(H, 16) || !aligned(h0, 16))
+    return SCAN_ERR_ALIGNMENT;
+  p.A = A;
+  p.Bm = Bm;
+  p.h0 = h0;
+  p.out_H = H;
+  return from_cuda(launch_affine_fwd(p, pl, stream));
 }
 
 scan_status affine_scan_bwd(const float* A, const float* H, const float* dH, const float* h0,
                             float* dA, float* dB, float* dh0, int64_t B, int64_t T, int64_t N,
                             int32_t k, int32_t v, const scan_opts* opts, void* ws,
                             size_t ws_bytes, cudaStream_t stream) {
-  (void)A; (void)H; (void)dH; (void)h0; (void)dA; (void)dB; (void)dh0; (void)B; (void)T;
-  (void)N; (void)k; (void)v; (void)opts; (void)ws; (void)ws_bytes; (void)stream;
-  return SCAN_ERR_UNSUPPORTED;
+  const scan_opts o = defaults(opts);
+  AffineParams p;
+  AffinePlan pl;
+  scan_status st = prepare_affine(B, T, N, k, v, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  if (B * N == 0) return SCAN_OK;
+  if (T == 0) return zero_dh0(dh0, B * N * (int64_t)k * v, stream);
+  if (!A || !H || !dH || !dA || !dB) return SCAN_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(H, 16) || !aligned(dH, 16) || !aligned(dA, 16) ||
+      !aligned(dB, 16) || !aligned(h0, 16) || !aligned(dh0, 16))
+    return SCAN_ERR_ALIGNMENT;
+  p.A = A;
+  p.H = H;
+  p.dH = dH;
+  p.h0 = h0;
+  p.dA = dA;
+  p.dB = dB;
+  p.dh0 = dh0;
+  return from_cuda(launch_affine_bwd(p, pl, stream));
 }
 
 }  // extern "C"

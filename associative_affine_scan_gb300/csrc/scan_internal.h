@@ -90,10 +90,9 @@ struct AffineParams {
   int k, v;
   int Lc;            // time steps per chunk
   int M;             // chunks along T
-  int NL;            // lanes (state blocks) per block
-  int G;             // lane groups = B * ceil(N / NL)
+  int G;             // lane groups = B * ceil(N / 32)
   int64_t ntiles;
-  unsigned char* recs;
+  float* recs;       // look-back records: [B*N][M] x record floats
   WsHeader* hdr;
   unsigned long long wait_limit_ns;
   int test_stall;
@@ -101,13 +100,15 @@ struct AffineParams {
 
 struct AffinePlan {
   int Lc;
-  int NL;
   int M;
   int G;
   size_t ws_bytes;
-  size_t smem;
-  int threads;
 };
+
+// Floats per (lane, chunk) record for block shape (k, v); 0 if unsupported.
+int affine_record_floats(int k, int v);
+int affine_sub_chunks();
+int affine_lanes_per_block();
 
 cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);
 cudaError_t launch_affine_bwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);

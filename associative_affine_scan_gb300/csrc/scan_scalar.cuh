@@ -234,74 +234,33 @@ struct LogOp {
 // packed-sequence window: which positions start a non-empty sequence
 // ---------------------------------------------------------------------------
 
-// Positions [W0, W0 + WL) around a chunk. bit(p) is set when a non-empty
-// sequence starts at p or ends just before p (so bit(T) is always set);
-// sstart[p - W0] names the sequence starting at p, send[p - W0] the one
-// ending at p - 1.
+// Packed-sequence lookup: the n + 1 offsets of cu_seqlens, staged once per
+// block in shared memory when they fit (otherwise read through the
+// read-only cache).
+constexpr int kCuSmem = 4096;
+
 struct SegWin {
-  uint32_t* bits;
-  int* sstart;
-  int* send;
-  int64_t W0;
-  int WL;
+  const int32_t* cu;
+  int n;
 };
 
-__device__ __forceinline__ bool win_bit(const SegWin& w, int64_t p) {
-  const int i = (int)(p - w.W0);
-  return (w.bits[i >> 5] >> (i & 31)) & 1u;
+// Largest i in [0, n-1] with cu[i] <= t: the non-empty sequence holding step
+// t (empty sequences share their offset with the next one, which wins). Every
+// probe stays inside [0, n-1], whatever cu holds.
+__device__ __forceinline__ int seg_find(const SegWin& w, int64_t t) {
+  int lo = 0, hi = w.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)w.cu[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
-// Called by every thread of the block. cu is sorted (checked separately);
-// with a malformed cu every index still stays inside [0, n].
-__device__ inline void build_window(SegWin& w, const int32_t* cu, int n, int warp, int lane) {
-  const int nwords = (w.WL + 31) >> 5;
-  __syncthreads();  // the previous chunk's readers are done
-  for (int i = threadIdx.x; i < nwords; i += blockDim.x) w.bits[i] = 0u;
-  __syncthreads();
-  if (warp == 0) {
-    // lb = number of offsets cu[i] (0 <= i <= n) below W0, by a 32-way search
-    int lo = 0, hi = n + 1;
-    while (hi - lo > 32) {
-      const int step = (hi - lo + 31) >> 5;
-      const int idx = lo + lane * step;
-      const bool pr = idx < hi && (int64_t)cu[idx] < w.W0;
-      const int c = __popc(__ballot_sync(kFull, pr));
-      const int nlo = c > 0 ? lo + (c - 1) * step + 1 : lo;
-      const int nhi = min(hi, lo + c * step);
-      lo = nlo;
-      hi = max(nhi, nlo);
-    }
-    {
-      const int idx = lo + lane;
-      const bool pr = idx < hi && (int64_t)cu[idx] < w.W0;
-      lo += __popc(__ballot_sync(kFull, pr));
-    }
-    const int first = max(lo - 1, 0);
-    for (int base = first;; base += 32) {
-      const int i = base + lane;
-      const bool in = i < n;
-      int s = 0, e = 0;
-      if (in) {
-        s = cu[i];
-        e = cu[i + 1];
-      }
-      const bool before_end = in && (int64_t)s < w.W0 + w.WL;
-      if (before_end && e > s) {
-        const int64_t ps = (int64_t)s - w.W0;
-        if (ps >= 0 && ps < w.WL) {
-          atomicOr(&w.bits[ps >> 5], 1u << (ps & 31));
-          w.sstart[ps] = i;
-        }
-        const int64_t pe = (int64_t)e - w.W0;
-        if (pe >= 0 && pe < w.WL) {
-          atomicOr(&w.bits[pe >> 5], 1u << (pe & 31));
-          w.send[pe] = i;
-        }
-      }
-      if (!__all_sync(kFull, before_end)) break;
-    }
-  }
-  __syncthreads();
+// Moves s forward to the sequence holding t (t at or after sequence s).
+__device__ __forceinline__ int seg_advance(const SegWin& w, int s, int64_t t) {
+  while (s + 1 < w.n && (int64_t)w.cu[s + 1] <= t) ++s;
+  return s;
 }
 
 // Checks 0 = cu[0] <= ... <= cu[n] = T and writes dh0 = 0 for empty sequences.
@@ -441,7 +400,7 @@ __device__ __forceinline__ float prev_in_memory(const float (&V)[J][4], int j, f
 // scans in the recurrence's direction; a backward call scans against it.
 template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S>
 __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int k, bool stationary,
-                                      uint32_t epoch, unsigned ticket, SegWin& win, float& carry) {
+                                      uint32_t epoch, unsigned ticket, const SegWin& win, float& carry) {
   using E = typename Op::E;
   constexpr int L = 128 * J;
   const BranchArgs& br = p.br[brn];
@@ -513,34 +472,37 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
     }
   }
 
-  if (VARLEN) {
-    win.W0 = (int64_t)m * L - 4;
-    build_window(win, p.cu, p.n_seqs, warp, lane);
-  }
   if (!active) return;
 
-  // boundary tests in memory order
-  auto is_start = [&](int64_t t) -> bool {  // t is the first step of a sequence
-    if (VARLEN) return win_bit(win, t);
-    return t == 0;
+  // packed sequences: the sequence holding each group's first step
+  int gseg[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    gseg[j] = 0;
+    if (VARLEN) {
+      const int64_t t = tl + 128 * j;
+      gseg[j] = seg_find(win, t < 0 ? 0 : (t < T ? t : T - 1));
+    }
+  }
+  // Boundary facts of step tt (valid, in group j): does a sequence start or
+  // end there, and which row of h0/dh0 belongs to its sequence.
+  struct Bound {
+    bool start, end;
+    int64_t h0row;
   };
-  auto is_end = [&](int64_t t) -> bool {  // t is the last step of a sequence
-    if (VARLEN) return win_bit(win, t + 1);
-    return t == T - 1;
-  };
-  // sequence index -> row of h0/dh0; clamped so that even a malformed
-  // cu_seqlens (reported through the status word) cannot address outside h0
-  auto seq_row = [&](int s) -> int64_t {
-    s = s < 0 ? 0 : (s >= p.n_seqs ? p.n_seqs - 1 : s);
-    return (int64_t)s * p.rows + row;
-  };
-  auto h0_index_start = [&](int64_t t) -> int64_t {
-    if (VARLEN) return seq_row(win.sstart[t - win.W0]);
-    return row;
-  };
-  auto h0_index_end = [&](int64_t t) -> int64_t {
-    if (VARLEN) return seq_row(win.send[t + 1 - win.W0]);
-    return row;
+  auto bound = [&](int j, int64_t tt) -> Bound {
+    Bound b;
+    if (VARLEN) {
+      const int s = seg_advance(win, gseg[j], tt);
+      b.start = (int64_t)win.cu[s] == tt;
+      b.end = (int64_t)win.cu[s + 1] == tt + 1;
+      b.h0row = (int64_t)s * p.rows + row;
+    } else {
+      b.start = tt == 0;
+      b.end = tt == T - 1;
+      b.h0row = row;
+    }
+    return b;
   };
 
   // ---- elements ----
@@ -556,11 +518,8 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
         E v = Op::identity();
         if (tt >= 0 && tt < T) {
           v = Op::make(A[j][e], X[j][e]);
-          if (S > 0) {
-            if (is_start(tt)) v = Op::make_first(A[j][e], X[j][e], br.h0, h0_index_start(tt));
-          } else {
-            if (is_end(tt)) v = Op::make_first(A[j][e], X[j][e], br.h0, h0_index_end(tt));
-          }
+          const Bound bd = bound(j, tt);
+          if ((S > 0) ? bd.start : bd.end) v = Op::make_first(A[j][e], X[j][e], br.h0, bd.h0row);
         }
         el[j][e] = v;
       }
@@ -585,7 +544,8 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
         E v = Op::identity();
         if (tt >= 0 && tt < T) {
           // the shifted gate is 0 past the end of the sequence (scan-first step)
-          const bool cut = (S < 0) ? is_end(tt) : is_start(tt);
+          const Bound bd = bound(j, tt);
+          const bool cut = (S < 0) ? bd.end : bd.start;
           v = Op::make(cut ? 0.f : gate[e], X[j][e]);
         }
         el[j][e] = v;
@@ -685,11 +645,10 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
         else hn = (e < 3) ? H[j][e + 1] : HN[j];
         if (tt >= 0 && tt < T) {
           // the step that starts the forward recurrence reads h0 and feeds dh0
-          const bool first_fwd = (S < 0) ? is_start(tt) : is_end(tt);
-          if (first_fwd) {
-            const int64_t hi = (S < 0) ? h0_index_start(tt) : h0_index_end(tt);
-            hn = br.h0 ? br.h0[hi] : 0.f;
-            if (br.dh0) br.dh0[hi] = A[j][e] * gv;
+          const Bound bd = bound(j, tt);
+          if ((S < 0) ? bd.start : bd.end) {
+            hn = br.h0 ? br.h0[bd.h0row] : 0.f;
+            if (br.dh0) br.dh0[bd.h0row] = A[j][e] * gv;
           }
         }
         gx[e] = gv;
@@ -717,14 +676,14 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
 template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
 __global__ void __launch_bounds__(256) scalar_scan_kernel(const __grid_constant__ ScalarParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int L = 128 * J;
   SegWin win;
-  if (VARLEN) {
-    win.WL = L + 8;
-    const int nwords = (win.WL + 31) >> 5;
-    win.bits = reinterpret_cast<uint32_t*>(smem);
-    win.sstart = reinterpret_cast<int*>(smem + 4 * ((nwords + 3) & ~3));
-    win.send = win.sstart + win.WL;
+  win.cu = p.cu;
+  win.n = p.n_seqs;
+  if (VARLEN && p.n_seqs + 1 <= kCuSmem) {
+    int32_t* s_cu = reinterpret_cast<int32_t*>(smem);
+    for (int i = threadIdx.x; i <= p.n_seqs; i += blockDim.x) s_cu[i] = __ldg(p.cu + i);
+    __syncthreads();
+    win.cu = s_cu;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   (void)warp;

@@ -53,9 +53,9 @@
  *     clearing; calls that run concurrently on the GPU need separate
  *     workspaces. It also holds the sticky device status word read by
  *     scan_get_device_status().
- *   - Any base pointer may be unaligned; 16-byte aligned fp32 tensors and
- *     8-byte aligned bf16 tensors (torch allocations are) take the
- *     vectorised path.
+ *   - Scalar and log forms accept any base pointer; 16-byte aligned fp32
+ *     tensors and 8-byte aligned bf16 tensors (torch allocations are) take
+ *     the vectorised path. The block form needs 16-byte aligned tensors.
  */
 #ifndef LIBSCAN_H
 #define LIBSCAN_H
@@ -75,7 +75,7 @@ typedef enum scan_status {
   SCAN_OK = 0,
   SCAN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, malformed host cu_seqlens */
   SCAN_ERR_UNSUPPORTED = 2, /* outside the kernels' envelope (e.g. k, v not in {1,2,4,8,16}) */
-  SCAN_ERR_ALIGNMENT = 3,   /* reserved: no current entry point requires alignment */
+  SCAN_ERR_ALIGNMENT = 3,   /* affine tensors must be 16-byte aligned */
   SCAN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than scan_workspace_bytes() */
   SCAN_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
   SCAN_ERR_TIMEOUT = 6,     /* device: a look-back wait ran past opts.wait_limit_s */
@@ -113,7 +113,7 @@ typedef enum scan_op {
 typedef struct scan_opts {
   int32_t variant;       /* scan_variant; 0 = AUTO */
   int32_t chunk;         /* scalar/log: elements of T per block row, one of 128, 256, 512,
-                            1024; affine: time steps per block, one of 16, 32, 64; 0 = planner */
+                            1024; affine: time steps per block, one of 64, 128, 256; 0 = planner */
   int32_t rows_per_cta;  /* scalar/log: rows (channels) per block, 1..16; 0 = planner */
   int32_t test_stall;    /* test hook: 1 makes one look-back wait on a summary that is
                             never published, so the wait limit expires (SCAN_ERR_TIMEOUT) */
@@ -208,8 +208,8 @@ scan_status scan_log_fwd(const float* log_a, const float* log_x,
 /* Block-matrix forward ([TSK] One associative-scan family, matrix_affine_scan;
  * Kernel design): H_t = A_t H_{t-1} + B_t per (b, n) lane, H_{-1} = h0.
  * A: [B,T,N,k,k], Bm and H: [B,T,N,k,v], h0: nullable [B,N,k,v]; row-major
- * matrices; fp32. Supported (k, v): k = v = 4 and k = 1 with v = 1;
- * others return SCAN_ERR_UNSUPPORTED. */
+ * matrices; fp32, 16-byte aligned (else SCAN_ERR_ALIGNMENT). Supported
+ * (k, v): (4, 4) and (2, 2); others return SCAN_ERR_UNSUPPORTED. */
 scan_status affine_scan_fwd(const float* A, const float* Bm, const float* h0,
                             float* H, int64_t B, int64_t T, int64_t N,
                             int32_t k, int32_t v, const scan_opts* opts,

@@ -55,13 +55,23 @@ def test_status_strings_and_version():
 
 def test_workspace_sizes():
     import associative_affine_scan_gb300 as scan
+    lookback = {"variant": scan.SCAN_VARIANT_LOOKBACK}
     # look-back: header + 16 bytes per (branch, row, chunk of 512)
-    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096) == 256 + 12288 * 8 * 16
-    assert scan.scan_workspace_bytes(scan.SCAN_OP_BIDIR_FWD, 1, 2048, 1000) == \
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096, opts=lookback) == \
+        256 + 12288 * 8 * 16
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_BIDIR_FWD, 1, 2048, 1000, opts=lookback) == \
         256 + 2 * 2048 * 2 * 16
-    # stationary needs only the header
+    # stationary needs only the header; rows that fill the GPU choose it
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096,
                                      opts={"variant": scan.SCAN_VARIANT_STATIONARY}) == 256
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096) == 256
+    # few rows (here 64) take the look-back
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 64, 100000) == \
+        256 + 64 * ((100000 + 511) // 512) * 16
+    # affine k=v=4: one 52-float record per (lane, chunk of 128 steps)
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_FWD, 8, 256, 4096, 4, 4) == \
+        256 + 8 * 256 * 32 * 52 * 4
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_FWD, 8, 256, 4096, 3, 4) == 0
     # rejected arguments size to 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, -1, 4, 4) == 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 100}) == 0

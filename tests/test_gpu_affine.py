@@ -1,0 +1,151 @@
+"""GPU parity of the block-matrix affine scan against the fp64 oracle.
+
+H_t = A_t H_{t-1} + B_t and its backward ("Triton scan kernels": One
+associative-scan family; Autograd integration and the reversed-scan backward),
+through the C ABI. The products do not commute, so any order mistake shows up
+against the oracle.
+
+Tolerance, fp32: max |got - ref| / max(1, |ref|) <= 1e-5 for H and dB. dA_t =
+G_t H_{t-1}^T and dh0 = A_0^T G_0 are k-term contractions whose fp32 rounding
+error is bounded by the sum of the magnitudes of their terms, not by the
+result (cancellation), so their error is normalised by
+max(1, |ref|, sum_j |G_ij| |H_lj|) (resp. sum_l |A_li| |G_lj|), with the term
+magnitudes taken from the oracle's own values.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from associative_affine_scan_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+DEV = torch.device("cuda", 0)
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def rel_err(got, ref, scale=None):
+    got = got.detach().double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.maximum(1.0, np.abs(ref))
+    if scale is not None:
+        den = np.maximum(den, scale)
+    return 0.0 if got.size == 0 else float(np.max(np.abs(got - ref) / den))
+
+
+def contraction_scales(A, h0, ref_H, ref_dB):
+    """sum_j |G_ij| |H_{t-1,lj}| for dA and sum_l |A_0,li| |G_0,lj| for dh0."""
+    A = np.asarray(A.double() if isinstance(A, torch.Tensor) else A, dtype=np.float64)
+    G = np.abs(ref_dB)
+    prev = np.empty_like(ref_H)
+    prev[:, 1:] = ref_H[:, :-1]
+    prev[:, 0] = 0.0 if h0 is None else np.asarray(h0.double())
+    dA_scale = np.einsum("btnij,btnlj->btnil", G, np.abs(prev))
+    dh0_scale = np.einsum("bnli,bnlj->bnij", np.abs(A[:, 0]), G[:, 0])
+    return dA_scale, dh0_scale
+
+
+def run_and_check(lib, w, opts=None):
+    A, Bm, dH = w.A.to(DEV), w.Bm.to(DEV), w.dH.to(DEV)
+    h0 = w.h0.to(DEV) if w.h0 is not None else None
+    H = lib.affine_scan_fwd(A, Bm, h0, opts=opts)
+    dA, dB, dh0 = lib.affine_scan_bwd(A, H, dH, h0, opts=opts)
+    torch.cuda.synchronize()
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    ref_H = oracle.affine_fwd(w.A, w.Bm, w.h0)
+    ref_dA, ref_dB, ref_dh0 = oracle.affine_bwd(w.A, w.Bm, w.dH, w.h0)
+    sA, s0 = contraction_scales(w.A, w.h0, ref_H, ref_dB)
+    errs = {"H": rel_err(H, ref_H), "dA": rel_err(dA, ref_dA, sA), "dB": rel_err(dB, ref_dB),
+            "dh0": rel_err(dh0, ref_dh0, s0)}
+    assert max(errs.values()) <= TOL, errs
+
+
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 200, 1000])
+@pytest.mark.parametrize("N", [1, 37, 70])
+def test_affine_4x4_shapes(lib, T, N):
+    for h0 in (True, False):
+        w = workloads.affine(2, T, N, 4, 4, seed=T * 100 + N, h0=h0)
+        run_and_check(lib, w)
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_affine_chunk_sizes(lib, chunk):
+    w = workloads.affine(1, 777, 33, 4, 4, seed=chunk, h0=True)
+    run_and_check(lib, w, {"chunk": chunk})
+
+
+def test_affine_2x2(lib):
+    w = workloads.affine(3, 513, 40, 2, 2, seed=5, h0=True)
+    run_and_check(lib, w)
+
+
+def test_affine_golden_worked_example_bit_exact(lib):
+    with open(os.path.join(HERE, "golden", "affine_2x2_dyadic.json")) as f:
+        g = json.load(f)
+    A, Bm, h0, dH = (torch.tensor(g[k], dtype=torch.float32, device=DEV)
+                     for k in ("A", "Bm", "h0", "dH"))
+    H = lib.affine_scan_fwd(A, Bm, h0)
+    dA, dB, dh0 = lib.affine_scan_bwd(A, H, dH, h0)
+    assert H.cpu().tolist() == g["H"]
+    assert dB.cpu().tolist() == g["dB"]
+    assert dA.cpu().tolist() == g["dA"]
+    assert dh0.cpu().tolist() == g["dh0"]
+
+
+def test_affine_identity_is_cumsum_exactly(lib):
+    T, N = 300, 32
+    A = torch.eye(4).expand(1, T, N, 4, 4).contiguous().to(DEV)
+    Bm = torch.randint(-3, 4, (1, T, N, 4, 4)).float().to(DEV)
+    H = lib.affine_scan_fwd(A, Bm)
+    assert torch.equal(H, torch.cumsum(Bm, dim=1))
+
+
+def test_affine_rejects_unsupported_and_misaligned(lib):
+    A = torch.zeros(1, 4, 2, 3, 3, device=DEV)
+    Bm = torch.zeros(1, 4, 2, 3, 3, device=DEV)
+    with pytest.raises(lib.ScanError) as e:
+        lib.affine_scan_fwd(A, Bm)
+    assert e.value.status == lib.SCAN_ERR_UNSUPPORTED
+    buf = torch.zeros(1 + 2 * 4 * 16, device=DEV)
+    A = buf[1:].view(1, 4, 2, 4, 4)
+    with pytest.raises(lib.ScanError) as e:
+        lib.affine_scan_fwd(A, torch.zeros(1, 4, 2, 4, 4, device=DEV))
+    assert e.value.status == lib.SCAN_ERR_ALIGNMENT
+
+
+def test_affine_wait_limit_reports_timeout(lib):
+    w = workloads.affine(1, 600, 32, 4, 4, seed=9, h0=True)
+    A, Bm, h0 = w.A.to(DEV), w.Bm.to(DEV), w.h0.to(DEV)
+    lib.scan_get_device_status(DEV)
+    lib.affine_scan_fwd(A, Bm, h0, opts={"chunk": 128, "test_stall": 1, "wait_limit_s": 1e-3})
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_ERR_TIMEOUT
+    H = lib.affine_scan_fwd(A, Bm, h0, opts={"chunk": 128})
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    assert rel_err(H, oracle.affine_fwd(w.A, w.Bm, w.h0)) <= TOL
+
+
+def test_full_affine_4x4_sampled_lanes(lib):
+    w = workloads.affine_4x4(seed=0)
+    A, Bm, dH = w.A.to(DEV), w.Bm.to(DEV), w.dH.to(DEV)
+    H = lib.affine_scan_fwd(A, Bm)
+    dA, dB, dh0 = lib.affine_scan_bwd(A, H, dH)
+    torch.cuda.synchronize()
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    g = np.random.default_rng(4)
+    B, T, N = w.A.shape[:3]
+    lanes = [(0, 0), (B - 1, N - 1)] + [(int(g.integers(B)), int(g.integers(N))) for _ in range(10)]
+    for b, n in lanes:
+        sl = (slice(b, b + 1), slice(None), slice(n, n + 1))
+        ref_H = oracle.affine_fwd(w.A[sl], w.Bm[sl])
+        ref_dA, ref_dB, ref_dh0 = oracle.affine_bwd(w.A[sl], w.Bm[sl], w.dH[sl])
+        sA, s0 = contraction_scales(w.A[sl], None, ref_H, ref_dB)
+        assert rel_err(H[sl], ref_H) <= TOL, (b, n)
+        assert rel_err(dA[sl], ref_dA, sA) <= TOL, (b, n)
+        assert rel_err(dB[sl], ref_dB) <= TOL, (b, n)
+        assert rel_err(dh0[b:b + 1, n:n + 1], ref_dh0, s0) <= TOL, (b, n)

@@ -42,6 +42,7 @@ from ._binding import (  # noqa: F401
     scan_bidir_fwd,
     scan_bwd,
     scan_fwd,
+    scan_fwd_noalloc,
     scan_get_device_status,
     scan_log_fwd,
     scan_status_string,

@@ -47,7 +47,7 @@ SCAN_OP_AFFINE_BWD = 6
 EXPORTED = (
     "scan_status_string", "scan_version", "scan_workspace_bytes", "scan_workspace_init",
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
-    "scan_log_fwd", "affine_scan_fwd", "affine_scan_bwd",
+    "scan_log_fwd", "affine_scan_fwd", "affine_scan_bwd", "scan_fwd_noalloc",
 )
 
 
@@ -97,6 +97,8 @@ _SIGS = {
                         ctypes.c_int),
     "affine_scan_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _opt,
                          _vp, _sz, _vp], ctypes.c_int),
+    "scan_fwd_noalloc": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, ctypes.c_int, _i32,
+                          _vp], ctypes.c_int),
 }
 
 _lock = threading.Lock()
@@ -439,3 +441,27 @@ def affine_scan_bwd(A, H, dH, h0=None, *, out=None, opts=None, stream=None):
                                _ptr(dh0), B, T, N, k, v, _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "affine_scan_bwd")
     return dA, dB, dh0
+
+
+def scan_fwd_noalloc(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None, stream=None):
+    """scan_fwd for callers that cannot allocate device memory.
+
+    The scan's scratch is a fixed array inside libscan (no workspace, no
+    allocation by the library). Only `out` is allocated here when not given;
+    a caller that cannot allocate passes its own `out`. Overlapping calls on
+    one GPU share that scratch and must be serialised; the first call on a
+    device should come before any stream capture.
+    """
+    _need(a, "a")
+    dev = a.device
+    dt = _dtype_code(a)
+    B, C, T, n = _scalar_dims(a, cu_seqlens)
+    _need(x, "x", dtype=a.dtype, shape=a.shape, device=dev)
+    _need(h0, "h0", dtype=torch.float32, shape=(n, C) if cu_seqlens is not None else (B, C),
+          device=dev)
+    h = out if out is not None else torch.empty(a.shape, dtype=torch.float32, device=dev)
+    _need(h, "out", dtype=torch.float32, shape=a.shape, device=dev)
+    st = lib().scan_fwd_noalloc(_ptr(a), _ptr(x), _ptr(h0), _ptr(cu_seqlens), n, _ptr(h), B, C, T,
+                                dt, int(bool(reverse)), _stream(stream, dev))
+    _check(st, "scan_fwd_noalloc")
+    return h

@@ -226,6 +226,37 @@ scan_status affine_scan_bwd(const float* A, const float* H, const float* dH,
                             int32_t v, const scan_opts* opts, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
+/* Bytes of the library's own scratch used by scan_fwd_noalloc (16 MiB). */
+#define SCAN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* scan_fwd without a caller-provided workspace and without any allocation.
+ * No counterpart in the source pages: it exists for callers that cannot
+ * allocate device memory -- code running inside a memory-capped or
+ * pre-partitioned arena, real-time paths that forbid allocation after
+ * start-up, plugin hosts that hand over only the tensors they own. The
+ * caller still passes a, x, h0, cu_seqlens and h exactly as for scan_fwd
+ * (same layouts and meaning); the look-back chunk summaries go to a fixed
+ * scratch array of SCAN_NOALLOC_SCRATCH_BYTES compiled into the library,
+ * which every GPU that loads the library keeps until the process exits.
+ *   - Limit: the call needs 256 + 16 * rows * chunks bytes (rows = B*C, or C
+ *     when packed; chunks = ceil((T + 3) / 512) for T > 256). Larger problems
+ *     return SCAN_ERR_WORKSPACE and compute nothing; use scan_fwd for them.
+ *   - The first call on each device sets the scratch up (looks up its device
+ *     address and zeroes its 256-byte header, synchronously); make that first
+ *     call before any stream capture on that device.
+ *   - Every call on a device shares the same scratch and leaves its contents
+ *     behind; the kernel resets what the next call needs. Calls whose kernels
+ *     overlap on the GPU (different streams, or threads) race on it and give
+ *     undefined results: serialise them.
+ *   - Device-side findings (a malformed cu_seqlens, an expired wait) are kept
+ *     in that scratch and cannot be read back; host-side checks return their
+ *     status as usual. Never calls cudaMalloc, cudaFree or any allocating
+ *     routine. */
+scan_status scan_fwd_noalloc(const void* a, const void* x, const float* h0,
+                             const int32_t* cu_seqlens, int32_t n_seqs, float* h,
+                             int64_t B, int64_t C, int64_t T, scan_dtype dt,
+                             int32_t reverse, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

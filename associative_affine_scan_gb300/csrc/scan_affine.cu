@@ -31,8 +31,7 @@
 namespace scan {
 namespace {
 
-constexpr int kSub = 4;     // sub-chunks (warps) per block
-constexpr int kLanes = 32;  // state-block lanes per block
+constexpr int kSub = 4;  // sub-chunks (warps) per block
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
@@ -114,51 +113,6 @@ __device__ __forceinline__ void mul(const float (&M)[K * K], const float (&X)[K 
     }
 }
 
-// Y = M^T X
-template <int K, int W>
-__device__ __forceinline__ void mul_t(const float (&M)[K * K], const float (&X)[K * W],
-                                      float (&Y)[K * W]) {
-#pragma unroll
-  for (int i = 0; i < K; ++i)
-#pragma unroll
-    for (int j = 0; j < W; ++j) {
-      float acc = M[i] * X[j];
-#pragma unroll
-      for (int l = 1; l < K; ++l) acc = fmaf(M[l * K + i], X[l * W + j], acc);
-      Y[i * W + j] = acc;
-    }
-}
-
-// Y = M X + D
-template <int K, int W>
-__device__ __forceinline__ void mul_add(const float (&M)[K * K], const float (&X)[K * W],
-                                        const float (&D)[K * W], float (&Y)[K * W]) {
-#pragma unroll
-  for (int i = 0; i < K; ++i)
-#pragma unroll
-    for (int j = 0; j < W; ++j) {
-      float acc = D[i * W + j];
-#pragma unroll
-      for (int l = 0; l < K; ++l) acc = fmaf(M[i * K + l], X[l * W + j], acc);
-      Y[i * W + j] = acc;
-    }
-}
-
-// Y = M^T X + D
-template <int K, int W>
-__device__ __forceinline__ void mul_t_add(const float (&M)[K * K], const float (&X)[K * W],
-                                          const float (&D)[K * W], float (&Y)[K * W]) {
-#pragma unroll
-  for (int i = 0; i < K; ++i)
-#pragma unroll
-    for (int j = 0; j < W; ++j) {
-      float acc = D[i * W + j];
-#pragma unroll
-      for (int l = 0; l < K; ++l) acc = fmaf(M[l * K + i], X[l * W + j], acc);
-      Y[i * W + j] = acc;
-    }
-}
-
 template <int N>
 __device__ __forceinline__ void copy(const float (&s)[N], float (&d)[N]) {
 #pragma unroll
@@ -176,16 +130,62 @@ struct RecLayout {
   static constexpr int kFloats = ((kFlags + 2) + 3) & ~3;
 };
 
-// Carry-in of chunk k of one lane: walk back over the lane's earlier chunks,
-// composing their summaries (later ones applied last) until one publishes
-// its inclusive state. Bounded by p.wait_limit_ns.
+// Column j of a block (k x v, row-major): c[i] = X[i][j].
 template <int K, int V>
-__device__ void lookback(const AffineParams& p, const float* lane_recs, int k, uint32_t epoch,
-                         bool stalled, unsigned ticket, int64_t lane_id, float (&carry)[K * V]) {
+__device__ __forceinline__ void load_col(const float* X, int j, float (&c)[K], bool keep) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) c[i] = keep ? __ldg(X + i * V + j) : __ldcs(X + i * V + j);
+}
+
+template <int K, int V>
+__device__ __forceinline__ void store_col(float* X, int j, const float (&c)[K]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) __stcs(X + i * V + j, c[i]);
+}
+
+template <int K, int V>
+__device__ __forceinline__ void store_col_cg(float* X, int j, const float (&c)[K]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) __stcg(X + i * V + j, c[i]);
+}
+
+// y = M x + d (M k x k row-major, x, d k-vectors); y must not alias x
+template <int K>
+__device__ __forceinline__ void mv_add(const float (&M)[K * K], const float (&x)[K],
+                                       const float (&d)[K], float (&y)[K]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    float acc = d[i];
+#pragma unroll
+    for (int l = 0; l < K; ++l) acc = fmaf(M[i * K + l], x[l], acc);
+    y[i] = acc;
+  }
+}
+
+// y = M^T x + d
+template <int K>
+__device__ __forceinline__ void mtv_add(const float (&M)[K * K], const float (&x)[K],
+                                        const float (&d)[K], float (&y)[K]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    float acc = d[i];
+#pragma unroll
+    for (int l = 0; l < K; ++l) acc = fmaf(M[l * K + i], x[l], acc);
+    y[i] = acc;
+  }
+}
+
+// Carry-in column j of chunk k of one lane: walk back over the lane's earlier
+// chunks, composing their summaries (later ones applied last) until one has
+// published its inclusive state. Bounded by p.wait_limit_ns.
+template <int K, int V>
+__device__ void lookback_col(const AffineParams& p, const float* lane_recs, int k,
+                             uint32_t epoch, bool stalled, unsigned ticket, int64_t lane_id,
+                             int j, float (&carry)[K]) {
   using RL = RecLayout<K, V>;
   uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
   if (stalled) tag_agg = tag_inc = 0xffffffffu;
-  float Pacc[K * K], Qacc[K * V];
+  float Pacc[K * K], Qacc[K];
   set_identity<K>(Pacc);
   fill(Qacc, 0.f);
   int pos = k - 1;
@@ -195,17 +195,18 @@ __device__ void lookback(const AffineParams& p, const float* lane_recs, int k, u
     const float* r = lane_recs + (int64_t)pos * RL::kFloats;
     const unsigned* flags = reinterpret_cast<const unsigned*>(r + RL::kFlags);
     if (ld_acquire_u32(flags + 1) == tag_inc) {
-      float Hc[K * V], tmp[K * V];
-      ldv_cg(r + RL::kH, Hc);
-      mul_add<K, V>(Pacc, Hc, Qacc, tmp);
-      copy(tmp, carry);
+      float Hc[K];
+#pragma unroll
+      for (int i = 0; i < K; ++i) Hc[i] = __ldcg(r + RL::kH + i * V + j);
+      mv_add<K>(Pacc, Hc, Qacc, carry);
       return;
     }
     if (ld_acquire_u32(flags) == tag_agg) {
-      float Pp[K * K], Qp[K * V], tq[K * V], tp[K * K];
+      float Pp[K * K], Qp[K], tq[K], tp[K * K];
       ldv_cg(r + RL::kP, Pp);
-      ldv_cg(r + RL::kQ, Qp);
-      mul_add<K, V>(Pacc, Qp, Qacc, tq);  // earlier chunk applied first
+#pragma unroll
+      for (int i = 0; i < K; ++i) Qp[i] = __ldcg(r + RL::kQ + i * V + j);
+      mv_add<K>(Pacc, Qp, Qacc, tq);  // the earlier chunk is applied first
       mul<K, K>(Pacc, Pp, tp);
       copy(tq, Qacc);
       copy(tp, Pacc);
@@ -229,12 +230,36 @@ __device__ void lookback(const AffineParams& p, const float* lane_recs, int k, u
   copy(Qacc, carry);
 }
 
+// D holds this thread's rank-1 part G[:, j] H[:, j]^T of dA (k x k). After the
+// exchange over the V threads of the lane (xor partners), slot row 0 of D is
+// row j of dA summed over all columns. Indices stay compile-time; the thread's
+// column bits only select which half it keeps.
+template <int K, int V>
+__device__ __forceinline__ void reduce_scatter_rows(float (&D)[K * K], int j) {
+#pragma unroll
+  for (int m = 1; m < V; m <<= 1) {
+    const bool hi = (j & m) != 0;
+#pragma unroll
+    for (int i = 0; i < K; i += 2 * m) {
+#pragma unroll
+      for (int l = 0; l < K; ++l) {
+        const float lo_v = D[i * K + l], hi_v = D[(i + m) * K + l];
+        const float send = hi ? lo_v : hi_v;
+        const float keep = hi ? hi_v : lo_v;
+        D[i * K + l] = keep + __shfl_xor_sync(kFull, send, m);
+      }
+    }
+  }
+}
+
 template <int K, int V, int LS, int MODE>
 __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ AffineParams p) {
-  constexpr int KK = K * K, KV = K * V;
+  static_assert(K == V, "one thread per column of P and Q needs k == v");
+  constexpr int KK = K * K, KV = K * V, NL = 32 / V;
   using RL = RecLayout<K, V>;
-  __shared__ float s_sum[kSub][kLanes][KK + KV];
-  __shared__ float s_in[kSub][kLanes][KV];
+  __shared__ float s_P[kSub][NL][KK];
+  __shared__ float s_Q[kSub][NL][KV];
+  __shared__ float s_in[kSub][NL][KV];
   __shared__ unsigned s_ticket, s_epoch;
 
   if (threadIdx.x == 0) {
@@ -246,13 +271,14 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
   const unsigned ticket = s_ticket;
   const uint32_t epoch = s_epoch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ln = lane / V, j = lane % V;  // lane in block, column
 
   if ((int64_t)ticket < p.ntiles) {
     const int k = (int)(ticket / (unsigned)p.G);
     const int g = (int)(ticket % (unsigned)p.G);
-    const int64_t groups_n = (p.N + kLanes - 1) / kLanes;
+    const int64_t groups_n = (p.N + NL - 1) / NL;
     const int64_t b = g / groups_n;
-    const int64_t n = (g % groups_n) * kLanes + lane;
+    const int64_t n = (g % groups_n) * NL + ln;
     const bool active = n < p.N;
     const int m = (MODE == MODE_FWD) ? k : (p.M - 1 - k);
     const int64_t T = p.T;
@@ -262,164 +288,197 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
     const int64_t NN = p.N;
     auto blk = [&](int64_t t) -> int64_t { return (b * T + t) * NN + n; };
 
-    // ---- pass 1: sub-chunk summary ----
-    float P[KK], Q[KV];
-    set_identity<K>(P);
-    fill(Q, 0.f);
+    // ---- pass 1: column j of the sub-chunk summary (P, Q) ----
+    float Pc[K], Qc[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      Pc[i] = (i == j) ? 1.f : 0.f;
+      Qc[i] = 0.f;
+    }
     if (active && t_lo < t_hi) {
       if (MODE == MODE_FWD) {
-        float An[KK], Bn[KV];
+        float An[KK], Bn[K];
         ldv(p.A + blk(t_lo) * KK, An, true);
-        ldv(p.Bm + blk(t_lo) * KV, Bn, true);
+        load_col<K, V>(p.Bm + blk(t_lo) * KV, j, Bn, true);
         for (int64_t t = t_lo; t < t_hi; ++t) {
-          float Ac[KK], Bc[KV], tq[KV], tp[KK];
+          float Ac[KK], Bc[K], tq[K], tp[K];
           copy(An, Ac);
           copy(Bn, Bc);
           if (t + 1 < t_hi) {
             ldv(p.A + blk(t + 1) * KK, An, true);
-            ldv(p.Bm + blk(t + 1) * KV, Bn, true);
+            load_col<K, V>(p.Bm + blk(t + 1) * KV, j, Bn, true);
           }
-          mul_add<K, V>(Ac, Q, Bc, tq);
-          mul<K, K>(Ac, P, tp);
-          copy(tq, Q);
-          copy(tp, P);
+          mv_add<K>(Ac, Qc, Bc, tq);
+          float z[K];
+          fill(z, 0.f);
+          mv_add<K>(Ac, Pc, z, tp);
+          copy(tq, Qc);
+          copy(tp, Pc);
         }
       } else {
         // G_t = A_{t+1}^T G_{t+1} + dH_t, walking t downwards
-        float An[KK], Dn[KV];
+        float An[KK], Dn[K];
         {
           const int64_t t = t_hi - 1;
           if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, An, true);
           else fill(An, 0.f);
-          ldv(p.dH + blk(t) * KV, Dn, true);
+          load_col<K, V>(p.dH + blk(t) * KV, j, Dn, true);
         }
         for (int64_t t = t_hi - 1; t >= t_lo; --t) {
-          float Ac[KK], Dc[KV], tq[KV], tp[KK];
+          float Ac[KK], Dc[K], tq[K], tp[K];
           copy(An, Ac);
           copy(Dn, Dc);
           if (t - 1 >= t_lo) {
             ldv(p.A + blk(t) * KK, An, true);
-            ldv(p.dH + blk(t - 1) * KV, Dn, true);
+            load_col<K, V>(p.dH + blk(t - 1) * KV, j, Dn, true);
           }
-          mul_t_add<K, V>(Ac, Q, Dc, tq);
-          mul_t<K, K>(Ac, P, tp);
-          copy(tq, Q);
-          copy(tp, P);
+          mtv_add<K>(Ac, Qc, Dc, tq);
+          float z[K];
+          fill(z, 0.f);
+          mtv_add<K>(Ac, Pc, z, tp);
+          copy(tq, Qc);
+          copy(tp, Pc);
         }
       }
     }
 #pragma unroll
-    for (int i = 0; i < KK; ++i) s_sum[warp][lane][i] = P[i];
-#pragma unroll
-    for (int i = 0; i < KV; ++i) s_sum[warp][lane][KK + i] = Q[i];
+    for (int i = 0; i < K; ++i) {
+      s_P[warp][ln][i * K + j] = Pc[i];
+      s_Q[warp][ln][i * V + j] = Qc[i];
+    }
     __syncthreads();
 
-    // ---- chunk summary, look-back, carry-ins (warp 0, one thread per lane) ----
-    if (warp == 0 && active) {
-      float Pt[KK], Qt[KV];
-      set_identity<K>(Pt);
-      fill(Qt, 0.f);
-#pragma unroll
-      for (int q = 0; q < kSub; ++q) {
-        const int s = (MODE == MODE_FWD) ? q : kSub - 1 - q;
-        float Ps[KK], Qs[KV], tq[KV], tp[KK];
-#pragma unroll
-        for (int i = 0; i < KK; ++i) Ps[i] = s_sum[s][lane][i];
-#pragma unroll
-        for (int i = 0; i < KV; ++i) Qs[i] = s_sum[s][lane][KK + i];
-        mul_add<K, V>(Ps, Qt, Qs, tq);  // sub-chunk s applied after the earlier ones
-        mul<K, K>(Ps, Pt, tp);
-        copy(tq, Qt);
-        copy(tp, Pt);
-      }
+    // ---- chunk summary, look-back, carry-ins (warp 0: 8 lanes x 4 columns) ----
+    if (warp == 0) {
       float* lane_recs = p.recs + lane_id * (int64_t)p.M * RL::kFloats;
       float* rec = lane_recs + (int64_t)k * RL::kFloats;
       unsigned* flags = reinterpret_cast<unsigned*>(rec + RL::kFlags);
       const uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
-      float carry[KV];
-      if (k == 0) {
-        if (MODE == MODE_FWD && p.h0) ldv(p.h0 + lane_id * KV, carry, false);
-        else fill(carry, 0.f);
-      } else {
-        stv_cg(rec + RL::kP, Pt);
-        stv_cg(rec + RL::kQ, Qt);
-        __threadfence();
-        st_release_u32(flags, tag_agg);
+      float carry[K];
+      fill(carry, 0.f);
+      if (active) {
+        if (k == 0) {
+          if (MODE == MODE_FWD && p.h0) load_col<K, V>(p.h0 + lane_id * KV, j, carry, false);
+        } else {
+          // column j of the chunk summary, sub-chunks in scan order
+          float Pt[K], Qt[K];
+#pragma unroll
+          for (int i = 0; i < K; ++i) {
+            Pt[i] = (i == j) ? 1.f : 0.f;
+            Qt[i] = 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < kSub; ++q) {
+            const int s = (MODE == MODE_FWD) ? q : kSub - 1 - q;
+            float Ps[KK], Qs[K], tq[K], tp[K], z[K];
+#pragma unroll
+            for (int i = 0; i < KK; ++i) Ps[i] = s_P[s][ln][i];
+#pragma unroll
+            for (int i = 0; i < K; ++i) Qs[i] = s_Q[s][ln][i * V + j];
+            fill(z, 0.f);
+            mv_add<K>(Ps, Qt, Qs, tq);
+            mv_add<K>(Ps, Pt, z, tp);
+            copy(tq, Qt);
+            copy(tp, Pt);
+          }
+#pragma unroll
+          for (int i = 0; i < K; ++i) {
+            __stcg(rec + RL::kP + i * K + j, Pt[i]);
+            __stcg(rec + RL::kQ + i * V + j, Qt[i]);
+          }
+          __threadfence();
+        }
+      }
+      __syncwarp();
+      if (active && k > 0) {
+        if (j == 0) st_release_u32(flags, tag_agg);
         const bool stalled = p.test_stall && lane_id == 0 && k == 1;
-        lookback<K, V>(p, lane_recs, k, epoch, stalled, ticket, lane_id, carry);
+        lookback_col<K, V>(p, lane_recs, k, epoch, stalled, ticket, lane_id, j, carry);
       }
-      {
-        float Hout[KV];
-        mul_add<K, V>(Pt, carry, Qt, Hout);
-        stv_cg(rec + RL::kH, Hout);
+      if (active) {
+        // carry-in of every sub-chunk, and the chunk's inclusive state
+#pragma unroll
+        for (int q = 0; q < kSub; ++q) {
+          const int s = (MODE == MODE_FWD) ? q : kSub - 1 - q;
+#pragma unroll
+          for (int i = 0; i < K; ++i) s_in[s][ln][i * V + j] = carry[i];
+          float Ps[KK], Qs[K], tq[K];
+#pragma unroll
+          for (int i = 0; i < KK; ++i) Ps[i] = s_P[s][ln][i];
+#pragma unroll
+          for (int i = 0; i < K; ++i) Qs[i] = s_Q[s][ln][i * V + j];
+          mv_add<K>(Ps, carry, Qs, tq);
+          copy(tq, carry);
+        }
+        store_col_cg<K, V>(rec + RL::kH, j, carry);
         __threadfence();
-        st_release_u32(flags + 1, tag_inc);
       }
-#pragma unroll
-      for (int q = 0; q < kSub; ++q) {
-        const int s = (MODE == MODE_FWD) ? q : kSub - 1 - q;
-#pragma unroll
-        for (int i = 0; i < KV; ++i) s_in[s][lane][i] = carry[i];
-        float Ps[KK], Qs[KV], tq[KV];
-#pragma unroll
-        for (int i = 0; i < KK; ++i) Ps[i] = s_sum[s][lane][i];
-#pragma unroll
-        for (int i = 0; i < KV; ++i) Qs[i] = s_sum[s][lane][KK + i];
-        mul_add<K, V>(Ps, carry, Qs, tq);
-        copy(tq, carry);
-      }
+      __syncwarp();
+      if (active && j == 0) st_release_u32(flags + 1, tag_inc);
     }
     __syncthreads();
 
     // ---- pass 3: replay the sub-chunk from its carry-in ----
-    if (active && t_lo < t_hi) {
-      float c[KV];
+    float c[K];
 #pragma unroll
-      for (int i = 0; i < KV; ++i) c[i] = s_in[warp][lane][i];
-      if (MODE == MODE_FWD) {
-        float An[KK], Bn[KV];
+    for (int i = 0; i < K; ++i) c[i] = s_in[warp][ln][i * V + j];
+    const bool work = active && t_lo < t_hi;
+    if (MODE == MODE_FWD) {
+      if (work) {
+        float An[KK], Bn[K];
         ldv(p.A + blk(t_lo) * KK, An, false);
-        ldv(p.Bm + blk(t_lo) * KV, Bn, false);
+        load_col<K, V>(p.Bm + blk(t_lo) * KV, j, Bn, false);
         for (int64_t t = t_lo; t < t_hi; ++t) {
-          float Ac[KK], Bc[KV], h[KV];
+          float Ac[KK], Bc[K], h[K];
           copy(An, Ac);
           copy(Bn, Bc);
           if (t + 1 < t_hi) {
             ldv(p.A + blk(t + 1) * KK, An, false);
-            ldv(p.Bm + blk(t + 1) * KV, Bn, false);
+            load_col<K, V>(p.Bm + blk(t + 1) * KV, j, Bn, false);
           }
-          mul_add<K, V>(Ac, c, Bc, h);
-          stv(p.out_H + blk(t) * KV, h);
+          mv_add<K>(Ac, c, Bc, h);
+          store_col<K, V>(p.out_H + blk(t) * KV, j, h);
           copy(h, c);
         }
-      } else {
-        for (int64_t t = t_hi - 1; t >= t_lo; --t) {
-          float An[KK], Dn[KV], Hp[KV], gnew[KV], dA[KK];
+      }
+    } else {
+      // every thread of the warp runs the same number of steps so the row
+      // exchange of dA stays warp-uniform; idle threads compute on zeros
+      const int64_t w_lo = (int64_t)m * (kSub * LS) + (int64_t)warp * LS;
+      const int64_t w_hi = w_lo + LS < T ? w_lo + LS : T;
+      for (int64_t t = w_hi - 1; t >= w_lo; --t) {
+        float An[KK], Dn[K], Hp[K], gn[K], D[KK];
+        if (work) {
           if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, An, false);
           else fill(An, 0.f);
-          ldv(p.dH + blk(t) * KV, Dn, false);
-          if (t >= 1) ldv(p.H + blk(t - 1) * KV, Hp, false);
-          else if (p.h0) ldv(p.h0 + lane_id * KV, Hp, false);
+          load_col<K, V>(p.dH + blk(t) * KV, j, Dn, false);
+          if (t >= 1) load_col<K, V>(p.H + blk(t - 1) * KV, j, Hp, false);
+          else if (p.h0) load_col<K, V>(p.h0 + lane_id * KV, j, Hp, false);
           else fill(Hp, 0.f);
-          mul_t_add<K, V>(An, c, Dn, gnew);
-          copy(gnew, c);
-          stv(p.dB + blk(t) * KV, c);
-          // dA_t = G_t H_{t-1}^T
+        } else {
+          fill(An, 0.f);
+          fill(Dn, 0.f);
+          fill(Hp, 0.f);
+        }
+        mtv_add<K>(An, c, Dn, gn);
+        copy(gn, c);
+        // dA_t = G_t H_{t-1}^T: this column's rank-1 part, summed across the lane
 #pragma unroll
-          for (int i = 0; i < K; ++i)
+        for (int i = 0; i < K; ++i)
 #pragma unroll
-            for (int l = 0; l < K; ++l) {
-              float acc = c[i * V] * Hp[l * V];
+          for (int l = 0; l < K; ++l) D[i * K + l] = c[i] * Hp[l];
+        reduce_scatter_rows<K, V>(D, j);
+        if (work) {
+          store_col<K, V>(p.dB + blk(t) * KV, j, c);
+          float* row = p.dA + blk(t) * KK + j * K;
 #pragma unroll
-              for (int j = 1; j < V; ++j) acc = fmaf(c[i * V + j], Hp[l * V + j], acc);
-              dA[i * K + l] = acc;
-            }
-          stv(p.dA + blk(t) * KK, dA);
+          for (int l = 0; l < K; ++l) __stcs(row + l, D[l]);
           if (t == 0 && p.dh0) {
-            float A0[KK], d0[KV];
+            float A0[KK], d0[K], z[K];
             ldv(p.A + blk(0) * KK, A0, false);
-            mul_t<K, V>(A0, c, d0);
-            stv(p.dh0 + lane_id * KV, d0);
+            fill(z, 0.f);
+            mtv_add<K>(A0, c, z, d0);
+            store_col<K, V>(p.dh0 + lane_id * KV, j, d0);
           }
         }
       }
@@ -469,7 +528,7 @@ int affine_record_floats(int k, int v) {
 }
 
 int affine_sub_chunks() { return kSub; }
-int affine_lanes_per_block() { return kLanes; }
+int affine_lanes_per_block(int v) { return 32 / v; }
 
 cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
   return launch_affine<MODE_FWD>(p, pl, s);

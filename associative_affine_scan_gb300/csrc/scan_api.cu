@@ -91,8 +91,8 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   return SCAN_OK;
 }
 
-// Per-shape plan for the block-matrix form: a block covers 32 lanes and one
-// chunk of Lc steps (4 sub-chunks of Lc / 4).
+// Per-shape plan for the block-matrix form: a block covers 32 / v lanes (one
+// thread per column) and one chunk of Lc steps (4 sub-chunks of Lc / 4).
 scan_status plan_affine(int64_t B, int64_t T, int64_t N, int k, int v, const scan_opts& o,
                         AffinePlan* pl) {
   if (B < 0 || T < 0 || N < 0) return SCAN_ERR_INVALID_ARG;
@@ -100,7 +100,7 @@ scan_status plan_affine(int64_t B, int64_t T, int64_t N, int k, int v, const sca
   if (rec == 0) return SCAN_ERR_UNSUPPORTED;
   int Lc = o.chunk ? o.chunk : 128;
   if (Lc != 64 && Lc != 128 && Lc != 256) return SCAN_ERR_INVALID_ARG;
-  const int64_t lanes = affine_lanes_per_block();
+  const int64_t lanes = affine_lanes_per_block(v);
   const int64_t M = T > 0 ? (T + Lc - 1) / Lc : 0;
   const int64_t G = B * ((N + lanes - 1) / lanes);
   if (M * G > kMaxGrid) return SCAN_ERR_UNSUPPORTED;

@@ -108,7 +108,7 @@ struct AffinePlan {
 // Floats per (lane, chunk) record for block shape (k, v); 0 if unsupported.
 int affine_record_floats(int k, int v);
 int affine_sub_chunks();
-int affine_lanes_per_block();
+int affine_lanes_per_block(int v);
 
 cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);
 cudaError_t launch_affine_bwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);

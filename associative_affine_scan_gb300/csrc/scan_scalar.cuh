@@ -474,14 +474,23 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
 
   if (!active) return;
 
-  // packed sequences: the sequence holding each group's first step
+  // packed sequences: the sequence holding each group's first step (one
+  // search per lane, then forward steps), and whether the group's 4 steps
+  // are interior: no sequence starts or ends on them, so they need no
+  // per-step boundary test
   int gseg[J];
+  bool inner[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) {
+    const int64_t t = tl + 128 * j;
     gseg[j] = 0;
     if (VARLEN) {
-      const int64_t t = tl + 128 * j;
-      gseg[j] = seg_find(win, t < 0 ? 0 : (t < T ? t : T - 1));
+      const int64_t tc = t < 0 ? 0 : (t < T ? t : T - 1);
+      gseg[j] = (j == 0) ? seg_find(win, tc) : seg_advance(win, gseg[j - 1], tc);
+      inner[j] = t >= 0 && t + 4 <= T && (int64_t)win.cu[gseg[j]] != t &&
+                 (int64_t)win.cu[gseg[j] + 1] > t + 4;
+    } else {
+      inner[j] = false;  // dense rows test t == 0 and t == T - 1 directly
     }
   }
   // Boundary facts of step tt (valid, in group j): does a sequence start or
@@ -492,7 +501,11 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
   };
   auto bound = [&](int j, int64_t tt) -> Bound {
     Bound b;
-    if (VARLEN) {
+    if (VARLEN && inner[j]) {
+      b.start = false;
+      b.end = false;
+      b.h0row = row;
+    } else if (VARLEN) {
       const int s = seg_advance(win, gseg[j], tt);
       b.start = (int64_t)win.cu[s] == tt;
       b.end = (int64_t)win.cu[s + 1] == tt + 1;

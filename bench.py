@@ -170,33 +170,44 @@ def run_ours(args, world, rank, local):
     dh0 = torch.empty(B, C, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step():
-        scan.scan_fwd(a, x, h0, out=h)
-        scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
+    # The two C-ABI calls are captured once into CUDA graphs on a dedicated
+    # stream and replayed, so the host-side marshalling of the binding does
+    # not leave the GPU idle inside the timed events (each replay launches the
+    # same single kernel the direct call launches).
+    gs = torch.cuda.Stream(dev)
+    gs.wait_stream(stream)
+    with torch.cuda.stream(gs):
+        for _ in range(args.warmup):
+            flush.zero_()
+            scan.scan_fwd(a, x, h0, out=h)
+            scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
     torch.cuda.synchronize()
-    if scan.scan_get_device_status(dev) != scan.SCAN_OK:
+    if scan.scan_get_device_status(dev, gs) != scan.SCAN_OK:
         raise RuntimeError("device status not OK after warm-up")
+    g_fwd, g_bwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fwd, stream=gs):
+        scan.scan_fwd(a, x, h0, out=h)
+    with torch.cuda.graph(g_bwd, stream=gs):
+        scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
+    torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()  # L2 flush between timed steps, outside the event pair
-            ev[i][0].record(stream)
-            scan.scan_fwd(a, x, h0, out=h)
-            ev[i][1].record(stream)
-            scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
-            ev[i][2].record(stream)
+        with torch.cuda.stream(gs):
+            for i in range(args.steps):
+                flush.zero_()  # L2 flush between timed steps, outside the event pair
+                ev[i][0].record(gs)
+                g_fwd.replay()
+                ev[i][1].record(gs)
+                g_bwd.replay()
+                ev[i][2].record(gs)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     barrier(world)
-    status = scan.scan_get_device_status(dev)
+    status = scan.scan_get_device_status(dev, gs)
     if status != scan.SCAN_OK:
         raise RuntimeError(f"device status {scan.scan_status_string(status)}")
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]

@@ -6,11 +6,12 @@ through the C ABI. The products do not commute, so any order mistake shows up
 against the oracle.
 
 Tolerance, fp32: max |got - ref| / max(1, |ref|) <= 1e-5 for H and dB. dA_t =
-G_t H_{t-1}^T and dh0 = A_0^T G_0 are k-term contractions whose fp32 rounding
-error is bounded by the sum of the magnitudes of their terms, not by the
-result (cancellation), so their error is normalised by
-max(1, |ref|, sum_j |G_ij| |H_lj|) (resp. sum_l |A_li| |G_lj|), with the term
-magnitudes taken from the oracle's own values.
+G_t H_{t-1}^T and dh0 = A_0^T G_0 are k-term contractions of those fp32
+results, so their error is bounded by the magnitudes of their terms, not by
+the result (cancellation): if G and H each meet e in the max(1, |.|) metric,
+dA_il is within 2e sum_j max(1, |G_ij|) max(1, |H_lj|). Their error is
+normalised by that term scale (resp. sum_l |A_li| max(1, |G_lj|) for dh0),
+computed from the oracle's own values.
 """
 
 import json
@@ -40,13 +41,13 @@ def rel_err(got, ref, scale=None):
 
 
 def contraction_scales(A, h0, ref_H, ref_dB):
-    """sum_j |G_ij| |H_{t-1,lj}| for dA and sum_l |A_0,li| |G_0,lj| for dh0."""
+    """Term scales of the dA and dh0 contractions (see the module docstring)."""
     A = np.asarray(A.double() if isinstance(A, torch.Tensor) else A, dtype=np.float64)
-    G = np.abs(ref_dB)
+    G = np.maximum(1.0, np.abs(ref_dB))
     prev = np.empty_like(ref_H)
     prev[:, 1:] = ref_H[:, :-1]
     prev[:, 0] = 0.0 if h0 is None else np.asarray(h0.double())
-    dA_scale = np.einsum("btnij,btnlj->btnil", G, np.abs(prev))
+    dA_scale = np.einsum("btnij,btnlj->btnil", G, np.maximum(1.0, np.abs(prev)))
     dh0_scale = np.einsum("bnli,bnlj->bnij", np.abs(A[:, 0]), G[:, 0])
     return dA_scale, dh0_scale
 

@@ -32,6 +32,7 @@ from ._binding import (  # noqa: F401
     SCAN_OP_LOG_FWD,
     SCAN_VARIANT_AUTO,
     SCAN_VARIANT_LOOKBACK,
+    SCAN_VARIANT_STREAM,
     SCAN_VARIANT_STATIONARY,
     ScanError,
     ScanOpts,

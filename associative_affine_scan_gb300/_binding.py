@@ -35,6 +35,7 @@ SCAN_BF16 = 1
 SCAN_VARIANT_AUTO = 0
 SCAN_VARIANT_STATIONARY = 1
 SCAN_VARIANT_LOOKBACK = 2
+SCAN_VARIANT_STREAM = 3
 
 SCAN_OP_FWD = 0
 SCAN_OP_BWD = 1
@@ -67,6 +68,7 @@ class ScanOpts(ctypes.Structure):
         ("test_stall", ctypes.c_int32),
         ("wait_limit_s", ctypes.c_double),
         ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
+        ("segments", ctypes.c_int32),
     ]
 
 

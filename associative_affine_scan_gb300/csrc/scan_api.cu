@@ -14,6 +14,7 @@ namespace {
 
 constexpr int64_t kMaxGrid = 0x7fffffffLL;
 constexpr int64_t kStationaryMinRows = 152 * 16;
+constexpr int64_t kStationaryWaves = 4;
 constexpr int kCuSmemEntries = 4096;  // packed offsets staged in shared memory
 
 __global__ void fill_zero_kernel(float* p, int64_t n) {
@@ -42,7 +43,6 @@ int chunk_to_j(int chunk) {
     case 128: return 1;
     case 256: return 2;
     case 512: return 4;
-    case 1024: return 8;
     default: return 0;
   }
 }
@@ -63,12 +63,13 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   if (R < 0 || R > 8) return SCAN_ERR_INVALID_ARG;
   if (R == 0) R = rows < 4 ? (int)(rows > 0 ? rows : 1) : 4;
   const int64_t L = 128LL * J;
-  // the vectorised path shifts each row by up to 3 elements
-  const int64_t span = T + ((T % 4) ? 3 : 0);
+  // the vectorised paths shift each row by up to 3 elements (7 for staged
+  // bf16 rows)
+  const int64_t span = T + ((T % 8) ? 7 : 0);
   const int64_t M = T > 0 ? (span + L - 1) / L : 0;
   const int64_t G = (rows + R - 1) / R;
   int variant = o.variant;
-  if (variant < 0 || variant > 2) return SCAN_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 3) return SCAN_ERR_INVALID_ARG;
   // Stationary blocks walk T in order with the carry in registers and no
   // inter-block traffic; that needs enough rows to occupy every SM (one warp
   // per row, about 16 resident warps per SM on 152 SMs). Fewer rows split T
@@ -78,14 +79,33 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   const int64_t tiles = M * G * nbr;
   if (M > kMaxGrid || G > kMaxGrid || tiles > kMaxGrid || rows * M * nbr > (1LL << 40))
     return SCAN_ERR_UNSUPPORTED;
+  // Stationary rows are cut into segments when the row groups alone give
+  // fewer than about four waves of blocks (152 SMs x 16 warps), so that no
+  // long-running block is left alone in a last partial wave.
+  int64_t nseg = 1, cps = M;
+  if ((variant == VAR_STATIONARY || variant == VAR_STREAM) && M > 0) {
+    if (o.segments < 0) return SCAN_ERR_INVALID_ARG;
+    const int64_t blocks = G * nbr;
+    const int64_t target = kStationaryWaves * 152 * 16 / R;
+    nseg = o.segments ? o.segments : (blocks >= target ? 1 : (target + blocks - 1) / blocks);
+    if (nseg > M) nseg = M;
+    cps = (M + nseg - 1) / nseg;
+    nseg = (M + cps - 1) / cps;
+    if (nseg * G * nbr > kMaxGrid) return SCAN_ERR_UNSUPPORTED;
+  }
   pl->variant = variant;
   pl->J = J;
   pl->R = R;
   pl->M = (int)M;
   pl->G = (int)G;
+  pl->nseg = (int)nseg;
+  pl->cps = (int)cps;
   pl->vec = true;
-  pl->ws_bytes = kWsHeaderBytes +
-                 (variant == VAR_LOOKBACK ? (size_t)(nbr * rows * M) * 16u : (size_t)0);
+  size_t recs = 0;
+  if (variant == VAR_LOOKBACK) recs = (size_t)(nbr * rows * M);
+  if ((variant == VAR_STATIONARY || variant == VAR_STREAM) && nseg > 1)
+    recs = (size_t)(nbr * rows * nseg);
+  pl->ws_bytes = kWsHeaderBytes + recs * 16u;
   (void)varlen;
   pl->smem = 0;
   return SCAN_OK;
@@ -137,7 +157,8 @@ scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t 
   if (st != SCAN_OK) return st;
   if (!ws) return SCAN_ERR_WORKSPACE;
   if (ws_bytes < pl->ws_bytes || !aligned(ws, 16)) return SCAN_ERR_WORKSPACE;
-  if (cu) pl->smem = 4u * (size_t)(n_seqs + 1 <= kCuSmemEntries ? n_seqs + 1 : kCuSmemEntries);
+  // packed offsets are staged in shared memory when they fit
+  if (cu) pl->smem = n_seqs + 1 <= kCuSmemEntries ? 4u * (size_t)(n_seqs + 1) : 0u;
   std::memset(p, 0, sizeof(*p));
   p->cu = cu;
   p->n_seqs = cu ? n_seqs : 1;
@@ -147,13 +168,31 @@ scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t 
   p->M = pl->M;
   p->G = pl->G;
   p->R = pl->R;
-  p->ntiles = (int64_t)pl->M * pl->G * nbr;
+  p->nseg = pl->nseg;
+  p->cps = pl->cps;
+  p->ntiles = (pl->variant == VAR_LOOKBACK ? (int64_t)pl->M : (int64_t)pl->nseg) * pl->G * nbr;
   p->hdr = static_cast<WsHeader*>(ws);
   p->recs = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(ws) +
                                                   kWsHeaderBytes);
   p->wait_limit_ns = wait_ns(o);
   p->test_stall = o.test_stall;
   return SCAN_OK;
+}
+
+// The stream variant copies whole 16-byte blocks into shared memory: it needs
+// 16-byte aligned tensors and a ring that fits in shared memory; otherwise
+// the same stationary scheme runs with register loads.
+void finish_plan(ScalarPlan* pl, int mode, size_t elt_a, bool all16) {
+  if (pl->variant != VAR_STREAM) return;
+  const int stages = stream_stages(pl->J);
+  const size_t ring = round_up((size_t)pl->R * stages * 8, 128) +
+                      (size_t)pl->R * stages * stream_stage_bytes(mode, pl->J, (int)elt_a);
+  const size_t total = round_up(pl->smem, 128) + ring;
+  if (!pl->vec || !all16 || total > 227 * 1024) {
+    pl->variant = VAR_STATIONARY;
+    return;
+  }
+  pl->smem = total;
 }
 
 scan_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA; }
@@ -250,6 +289,7 @@ scan_status scan_fwd(const void* a, const void* x, const float* h0, const int32_
   if (p.rows * T == 0) return SCAN_OK;
   if (!a || !x || !h) return SCAN_ERR_INVALID_ARG;
   pl.vec = aligned(a, 4 * elt(dt)) && aligned(x, 4 * elt(dt)) && aligned(h, 16);
+  finish_plan(&pl, MODE_FWD, elt(dt), aligned(a, 16) && aligned(x, 16));
   p.br[0].a = a;
   p.br[0].x = x;
   p.br[0].h0 = h0;
@@ -274,6 +314,7 @@ scan_status scan_bwd(const void* a, const float* h, const float* dh, const float
   if (!a || !h || !dh || !da || !dx) return SCAN_ERR_INVALID_ARG;
   pl.vec = aligned(a, 4 * elt(dt)) && aligned(da, 4 * elt(dt)) && aligned(dx, 4 * elt(dt)) &&
            aligned(h, 16) && aligned(dh, 16);
+  finish_plan(&pl, MODE_BWD, elt(dt), aligned(a, 16));
   p.br[0].a = a;
   p.br[0].h = h;
   p.br[0].dh = dh;
@@ -301,6 +342,8 @@ scan_status scan_bidir_fwd(const void* af, const void* xf, const void* ar, const
   const size_t va = 4 * elt(dt);
   pl.vec = aligned(af, va) && aligned(xf, va) && aligned(ar, va) && aligned(xr, va) &&
            aligned(hf, 16) && aligned(hr, 16);
+  finish_plan(&pl, MODE_FWD, elt(dt),
+              aligned(af, 16) && aligned(xf, 16) && aligned(ar, 16) && aligned(xr, 16));
   p.br[0].a = af;
   p.br[0].x = xf;
   p.br[0].h0 = h0f;
@@ -338,6 +381,7 @@ scan_status scan_bidir_bwd(const void* af, const float* hf, const float* dhf, co
   pl.vec = aligned(af, va) && aligned(ar, va) && aligned(daf, va) && aligned(dxf, va) &&
            aligned(dar, va) && aligned(dxr, va) && aligned(hf, 16) && aligned(dhf, 16) &&
            aligned(hr, 16) && aligned(dhr, 16);
+  finish_plan(&pl, MODE_BWD, elt(dt), aligned(af, 16) && aligned(ar, 16));
   p.br[0].a = af;
   p.br[0].h = hf;
   p.br[0].dh = dhf;
@@ -370,6 +414,7 @@ scan_status scan_log_fwd(const float* log_a, const float* log_x, const float* lo
   if (p.rows * T == 0) return SCAN_OK;
   if (!log_a || !log_x || !h) return SCAN_ERR_INVALID_ARG;
   pl.vec = aligned(log_a, 16) && aligned(log_x, 16) && aligned(h, 16);
+  finish_plan(&pl, MODE_FWD, 4, true);
   p.br[0].a = log_a;
   p.br[0].x = log_x;
   p.br[0].h0 = log_h0;

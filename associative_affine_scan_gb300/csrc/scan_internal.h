@@ -10,7 +10,22 @@
 namespace scan {
 
 enum Mode { MODE_FWD = 0, MODE_BWD = 1 };
-enum Variant { VAR_STATIONARY = 1, VAR_LOOKBACK = 2 };
+// Carry schemes. The first three are public (scan_variant); SEGMENTED is the
+// stationary scheme with rows cut into segments, compiled separately so the
+// plain stationary kernel keeps its register budget.
+enum Variant { VAR_STATIONARY = 1, VAR_LOOKBACK = 2, VAR_STREAM = 3, VAR_SEGMENTED = 4 };
+
+// Stream variant: each warp runs a ring of shared-memory stages, one chunk of
+// its row per stage, filled by bulk async copies; smaller chunks get more
+// stages so that a warp keeps about the same bytes in flight. A backward
+// stage also holds 8 steps on each side of the chunk (the shifted operands).
+__host__ __device__ constexpr int stream_stages(int J) { return J >= 4 ? 3 : (J == 2 ? 4 : 8); }
+__host__ __device__ constexpr int stream_pad(int mode) { return mode == MODE_BWD ? 8 : 0; }
+__host__ __device__ constexpr size_t stream_stage_bytes(int mode, int J, int elt_a) {
+  return mode == MODE_FWD ? (size_t)(128 * J) * 2 * (size_t)elt_a
+                          : (size_t)(128 * J + 2 * stream_pad(mode)) * ((size_t)elt_a + 8);
+}
+__host__ __device__ constexpr size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace header, at offset 0 of every workspace. The look-back kernels take
 // a tile ticket from `ticket_epoch` (low 32 bits) and read the launch epoch
@@ -50,7 +65,9 @@ struct ScalarParams {
   int M;              // chunks per row along T
   int G;              // row groups (blocks along rows)
   int R;              // rows (warps) per block
-  int64_t ntiles;     // M * G * nbr
+  int64_t ntiles;     // look-back: M * G * nbr; segmented stationary: nseg * G * nbr
+  int nseg;           // stationary: segments per row (1 = one block walks the whole row)
+  int cps;            // stationary: chunks per segment
   unsigned long long* recs;  // look-back records: [nbr][rows][M] x 16 bytes
   WsHeader* hdr;
   unsigned long long wait_limit_ns;
@@ -63,6 +80,8 @@ struct ScalarPlan {
   int R;
   int M;
   int G;
+  int nseg;     // stationary: segments per row
+  int cps;      // stationary: chunks per segment
   bool vec;     // vectorised loads/stores
   size_t ws_bytes;
   size_t smem;

@@ -93,6 +93,8 @@ extern "C" scan_status scan_fwd_noalloc(const void* a, const void* x, const floa
   pl.M = (int)M;
   pl.G = (int)G;
   pl.vec = aligned(a, va) && aligned(x, va) && aligned(h, 16);
+  pl.nseg = 1;
+  pl.cps = (int)M;
   pl.ws_bytes = need;
   pl.smem = cu_seqlens ? 4u * (size_t)(n_seqs + 1 <= 4096 ? n_seqs + 1 : 4096) : 0;
 
@@ -112,6 +114,8 @@ extern "C" scan_status scan_fwd_noalloc(const void* a, const void* x, const floa
   p.G = (int)G;
   p.R = R;
   p.ntiles = tiles;
+  p.nseg = 1;
+  p.cps = (int)M;
   p.hdr = static_cast<WsHeader*>(scratch);
   p.recs = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(scratch) +
                                                   kWsHeaderBytes);

@@ -118,6 +118,49 @@ struct IO<__nv_bfloat16> {
   }
 };
 
+// Reads of a shared-memory stage; i is the step index relative to the stage.
+template <typename TA>
+struct SIO;
+
+template <>
+struct SIO<float> {
+  static __device__ __forceinline__ void ld4(const unsigned char* base, int64_t i, float v[4]) {
+    const float4 q = *reinterpret_cast<const float4*>(base + i * 4);
+    v[0] = q.x;
+    v[1] = q.y;
+    v[2] = q.z;
+    v[3] = q.w;
+  }
+  static __device__ __forceinline__ float ld1(const unsigned char* base, int64_t i) {
+    return *reinterpret_cast<const float*>(base + i * 4);
+  }
+};
+
+template <>
+struct SIO<__nv_bfloat16> {
+  static __device__ __forceinline__ void ld4(const unsigned char* base, int64_t i, float v[4]) {
+    const uint2 q = *reinterpret_cast<const uint2*>(base + i * 2);
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xffff0000u);
+  }
+  static __device__ __forceinline__ float ld1(const unsigned char* base, int64_t i) {
+    const unsigned short u = *reinterpret_cast<const unsigned short*>(base + i * 2);
+    return __uint_as_float(((unsigned)u) << 16);
+  }
+};
+
+// One chunk's inputs as copied into a shared-memory stage: row-relative step
+// e0 sits at offset 0 of each tensor; steps [c_lo, c_hi) were copied.
+struct StageView {
+  const unsigned char* a;
+  const unsigned char* x;
+  const unsigned char* h;
+  const unsigned char* dh;
+  int64_t e0, c_lo, c_hi;
+};
+
 // ---------------------------------------------------------------------------
 // the two monoids
 // ---------------------------------------------------------------------------
@@ -263,6 +306,24 @@ __device__ __forceinline__ int seg_advance(const SegWin& w, int s, int64_t t) {
   return s;
 }
 
+// The sequence holding t, starting from a nearby guess s (the one that held
+// the previous chunk's steps): a few steps either way, else a full search.
+__device__ __forceinline__ int seg_near(const SegWin& w, int s, int64_t t) {
+  if (s < 0 || s >= w.n) return seg_find(w, t);
+#pragma unroll 1
+  for (int it = 0; it < 8; ++it) {
+    if ((int64_t)w.cu[s] > t) {
+      if (s == 0) return 0;
+      --s;
+    } else if (s + 1 < w.n && (int64_t)w.cu[s + 1] <= t) {
+      ++s;
+    } else {
+      return s;
+    }
+  }
+  return seg_find(w, t);
+}
+
 // Checks 0 = cu[0] <= ... <= cu[n] = T and writes dh0 = 0 for empty sequences.
 // Called by every thread of one block.
 template <int MODE>
@@ -398,9 +459,14 @@ __device__ __forceinline__ float prev_in_memory(const float (&V)[J][4], int j, f
 
 // S is the scan direction: +1 walks t upwards, -1 downwards. A forward call
 // scans in the recurrence's direction; a backward call scans against it.
-template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S>
+// SMEM: the chunk's inputs are read from a shared-memory stage (sv) where it
+// holds them, else from global memory. seg_hint (packed sequences): the
+// sequence that held the previous chunk's steps for this warp, -1 if none;
+// updated for the next chunk.
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S, bool SMEM = false>
 __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int k, bool stationary,
-                                      uint32_t epoch, unsigned ticket, const SegWin& win, float& carry) {
+                                      uint32_t epoch, unsigned ticket, const SegWin& win, float& carry,
+                                      const StageView* sv = nullptr, int* seg_hint = nullptr) {
   using E = typename Op::E;
   constexpr int L = 128 * J;
   const BranchArgs& br = p.br[brn];
@@ -410,8 +476,10 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
   const int64_t T = p.T;
   const int m = (S > 0) ? k : (p.M - 1 - k);
   // rows are cut so that every 4-step group starts on a 4-element boundary of
-  // memory (16 bytes fp32, 8 bytes bf16) whatever T is
-  const int shift = VEC ? (int)((row * T) & 3) : 0;
+  // memory (16 bytes fp32, 8 bytes bf16), or for staged bf16 on an 8-element
+  // (16-byte) boundary, whatever T is
+  constexpr int kAlign = (SMEM && sizeof(TA) == 2) ? 8 : 4;
+  const int shift = VEC ? (int)((row * T) & (kAlign - 1)) : 0;
   const int64_t t0 = (int64_t)m * L - shift;
   const int64_t roff = row * T;
   const int64_t tl = t0 + 4 * lane;
@@ -425,7 +493,10 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int64_t t = tl + 128 * j;
-        if (VEC && t >= 0 && t + 4 <= T) {
+        if (SMEM && t >= sv->c_lo && t + 4 <= sv->c_hi && t >= 0 && t + 4 <= T) {
+          SIO<TA>::ld4(sv->a, t - sv->e0, A[j]);
+          SIO<TA>::ld4(sv->x, t - sv->e0, X[j]);
+        } else if (VEC && t >= 0 && t + 4 <= T) {
           IO<TA>::ld4(a + t, A[j]);
           IO<TA>::ld4(x + t, X[j]);
         } else {
@@ -444,7 +515,11 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int64_t t = tl + 128 * j;
-        if (VEC && t >= 0 && t + 4 <= T) {
+        if (SMEM && t >= sv->c_lo && t + 4 <= sv->c_hi && t >= 0 && t + 4 <= T) {
+          SIO<TA>::ld4(sv->a, t - sv->e0, A[j]);
+          SIO<float>::ld4(sv->h, t - sv->e0, H[j]);
+          SIO<float>::ld4(sv->dh, t - sv->e0, X[j]);
+        } else if (VEC && t >= 0 && t + 4 <= T) {
           IO<TA>::ld4(a + t, A[j]);
           IO<float>::ld4(h + t, H[j]);
           IO<float>::ld4(dh + t, X[j]);
@@ -464,8 +539,12 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
       if (lane == 0) {
         const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
         const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
-        if (pa >= 0 && pa < T) halo_a = IO<TA>::ld1(a + pa);
-        if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(h + ph);
+        if (pa >= 0 && pa < T)
+          halo_a = (SMEM && pa >= sv->c_lo && pa < sv->c_hi) ? SIO<TA>::ld1(sv->a, pa - sv->e0)
+                                                               : IO<TA>::ld1(a + pa);
+        if (ph >= 0 && ph < T)
+          halo_h = (SMEM && ph >= sv->c_lo && ph < sv->c_hi) ? SIO<float>::ld1(sv->h, ph - sv->e0)
+                                                               : IO<float>::ld1(h + ph);
       }
       halo_a = __shfl_sync(kFull, halo_a, 0);
       halo_h = __shfl_sync(kFull, halo_h, 0);
@@ -486,13 +565,17 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
     gseg[j] = 0;
     if (VARLEN) {
       const int64_t tc = t < 0 ? 0 : (t < T ? t : T - 1);
-      gseg[j] = (j == 0) ? seg_find(win, tc) : seg_advance(win, gseg[j - 1], tc);
+      if (j == 0)
+        gseg[j] = seg_hint ? seg_near(win, *seg_hint, tc) : seg_find(win, tc);
+      else
+        gseg[j] = seg_advance(win, gseg[j - 1], tc);
       inner[j] = t >= 0 && t + 4 <= T && (int64_t)win.cu[gseg[j]] != t &&
                  (int64_t)win.cu[gseg[j] + 1] > t + 4;
     } else {
       inner[j] = false;  // dense rows test t == 0 and t == T - 1 directly
     }
   }
+  if (VARLEN && seg_hint) *seg_hint = (S > 0) ? gseg[J - 1] : gseg[0];
   // Boundary facts of step tt (valid, in group j): does a sequence start or
   // end there, and which row of h0/dh0 belongs to its sequence.
   struct Bound {
@@ -683,11 +766,172 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
 }
 
 // ---------------------------------------------------------------------------
+// bulk async copies into shared memory (TMA) and their mbarriers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 state;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 state, [%0], %1;\n}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared; addresses 16-byte aligned, bytes % 16 == 0
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes,
+                                              unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of `bar`; false once limit_ns has passed.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity,
+                                          unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t_begin = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t_begin > limit_ns) return false;
+  return true;
+}
+
+// One warp streams chunks [k0, k1) of its row through a ring of
+// stream_stages(J) shared-memory stages: lane 0 keeps that many
+// chunks in flight as bulk copies (one per tensor, the chunk's contiguous
+// run of the row), the warp scans chunk k from its stage while the next ones
+// arrive, with the carry in registers. Steps a stage does not hold (the last
+// few bytes of a tensor) are read from global memory by the chunk body.
+template <class Op, int MODE, bool VARLEN, int J, typename TA, int S>
+__device__ __forceinline__ void stream_chunks(const ScalarParams& p, int brn, int g, int k0, int k1,
+                              const SegWin& win, float& carry, unsigned char* region) {
+  constexpr int L = 128 * J;
+  constexpr int PAD = stream_pad(MODE);
+  constexpr int LE = L + 2 * PAD;
+  constexpr int kAlign = sizeof(TA) == 2 ? 8 : 4;
+  constexpr int e_a = (int)sizeof(TA);
+  constexpr int e_1 = MODE == MODE_FWD ? (int)sizeof(TA) : 4;
+  constexpr int e_2 = 4;
+  constexpr size_t SB = stream_stage_bytes(MODE, J, (int)sizeof(TA));
+  constexpr int kStages = stream_stages(J);
+  constexpr size_t o_1 = (size_t)LE * e_a;
+  constexpr size_t o_2 = o_1 + (size_t)LE * e_1;
+  const BranchArgs& br = p.br[brn];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)g * p.R + warp;
+  if (row >= p.rows) return;
+  const int64_t T = p.T, roff = row * T, total = p.rows * T;
+  const int shift = (int)((row * T) & (kAlign - 1));
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(region) + warp * kStages;
+  unsigned char* stages = region + round_up((size_t)p.R * kStages * 8, 128) +
+                          (size_t)warp * kStages * SB;
+  const unsigned char* g_a = static_cast<const unsigned char*>(br.a);
+  const unsigned char* g_1 = MODE == MODE_FWD ? static_cast<const unsigned char*>(br.x)
+                                              : reinterpret_cast<const unsigned char*>(br.h);
+  const unsigned char* g_2 = reinterpret_cast<const unsigned char*>(br.dh);
+  // whole 16-byte blocks of every tensor end at this element (the coarsest
+  // granularity, 16 / smallest element size, is a multiple of the others)
+  const int64_t end_all = total - total % (16 / (e_a < e_1 ? e_a : e_1));
+
+  // row-relative steps held by the stage of chunk k
+  auto range = [&](int k, int64_t& e0, int64_t& lo, int64_t& hi) {
+    const int m = (S > 0) ? k : (p.M - 1 - k);
+    const int64_t t0 = (int64_t)m * L - shift;
+    e0 = t0 - PAD;
+    lo = e0 < -roff ? -roff : e0;
+    hi = t0 + L + PAD;
+    if (hi > end_all - roff) hi = end_all - roff;
+  };
+  auto issue = [&](int k, int s) {  // lane 0
+    int64_t e0, lo, hi;
+    range(k, e0, lo, hi);
+    const unsigned n = hi > lo ? (unsigned)(hi - lo) : 0u;
+    const unsigned bytes = n * (unsigned)(e_a + e_1 + (MODE == MODE_BWD ? e_2 : 0));
+    mbar_expect_tx(&bars[s], bytes);
+    if (n) {
+      unsigned char* st = stages + (size_t)s * SB;
+      const int64_t off = lo - e0;
+      bulk_copy_g2s(st + off * e_a, g_a + (roff + lo) * e_a, n * e_a, &bars[s]);
+      bulk_copy_g2s(st + o_1 + off * e_1, g_1 + (roff + lo) * e_1, n * e_1, &bars[s]);
+      if (MODE == MODE_BWD)
+        bulk_copy_g2s(st + o_2 + off * e_2, g_2 + (roff + lo) * e_2, n * e_2, &bars[s]);
+    }
+  };
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int n = k1 - k0;
+  int hint = -1;
+  if (lane == 0)
+    for (int s = 0; s < kStages && s < n; ++s) issue(k0 + s, s);
+  for (int i = 0; i < n; ++i) {
+    const int s = i % kStages;
+    const bool ok = __all_sync(kFull, mbar_wait(&bars[s], (unsigned)((i / kStages) & 1),
+                                                p.wait_limit_ns));
+    if (!ok) {
+      // a copy never landed: record it, give the copies still in flight a
+      // bounded chance to finish, and stop this row
+      if (lane == 0) {
+        set_status(p.hdr, kStatusTimeout);
+        for (int j = i; j < n && j < i + kStages; ++j)
+          mbar_wait(&bars[j % kStages], (unsigned)((j / kStages) & 1), p.wait_limit_ns);
+      }
+      __syncwarp();
+      return;
+    }
+    StageView sv;
+    sv.a = stages + (size_t)s * SB;
+    sv.x = sv.a + o_1;
+    sv.h = sv.a + o_1;
+    sv.dh = sv.a + o_2;
+    range(k0 + i, sv.e0, sv.c_lo, sv.c_hi);
+    chunk<Op, MODE, VARLEN, true, J, TA, S, true>(p, brn, g, k0 + i, true, 0u, 0u, win, carry, &sv,
+                                                  &hint);
+    __syncwarp();
+    if (i + kStages < n && lane == 0) {
+      fence_proxy_async_smem();  // this warp's reads of the stage precede the refill
+      issue(k0 + i + kStages, s);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
 
 template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
-__global__ void __launch_bounds__(256) scalar_scan_kernel(const __grid_constant__ ScalarParams p) {
+__device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
   extern __shared__ __align__(16) unsigned char smem[];
   SegWin win;
   win.cu = p.cu;
@@ -738,31 +982,129 @@ __global__ void __launch_bounds__(256) scalar_scan_kernel(const __grid_constant_
         __threadfence();
       }
     }
-  } else {
+  } else if (VARIANT == VAR_STATIONARY) {
     const int g = blockIdx.x / p.nbr;
     const int brn = blockIdx.x % p.nbr;
     if (VARLEN && blockIdx.x == 0) check_segments<MODE>(p);
     float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
     const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
+    int hint = -1;
     for (int k = 0; k < p.M; ++k) {
       if (S > 0)
-        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, true, 0u, 0u, win, carry);
+        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr, &hint);
       else
-        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, true, 0u, 0u, win, carry);
+        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr, &hint);
+    }
+  } else {
+    // VAR_SEGMENTED and VAR_STREAM: stationary carry over [k0, k1). With
+    // nseg > 1 a row is cut into nseg segments of cps chunks, taken in ticket
+    // order (segment index major): a block waits once for the end state of
+    // its rows' previous segments (published G * nbr tickets earlier, so
+    // normally already there), walks its segment and publishes its end state.
+    __shared__ unsigned s_ticket, s_epoch;
+    const bool segmented = p.nseg > 1;
+    int g = 0, brn = 0, seg = 0;
+    unsigned ticket = 0;
+    uint32_t epoch = 0;
+    bool have = true;
+    if (segmented) {
+      if (threadIdx.x == 0) {
+        const unsigned long long te = atomicAdd(&p.hdr->ticket_epoch, 1ull);
+        s_ticket = (unsigned)te;
+        s_epoch = (unsigned)(te >> 32);
+      }
+      __syncthreads();
+      ticket = s_ticket;
+      epoch = s_epoch;
+      have = (int64_t)ticket < p.ntiles;
+      const int per_s = p.G * p.nbr;
+      seg = (int)(ticket / (unsigned)per_s);
+      const int rem = (int)(ticket % (unsigned)per_s);
+      g = rem / p.nbr;
+      brn = rem % p.nbr;
+    } else {
+      g = blockIdx.x / p.nbr;
+      brn = blockIdx.x % p.nbr;
+    }
+    if (have) {
+      if (VARLEN && (segmented ? ticket == 0 : blockIdx.x == 0)) check_segments<MODE>(p);
+      const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
+      const int64_t row = (int64_t)g * p.R + warp;
+      const bool active = row < p.rows;
+      unsigned long long* recs_row = p.recs + ((int64_t)brn * p.rows + row) * (int64_t)p.nseg * 2;
+      float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
+      if (segmented && seg > 0 && active)
+        carry = lookback<Op>(p, recs_row, seg, epoch, lane, ticket, brn, row);
+      const int k0 = seg * p.cps;
+      const int k1 = k0 + p.cps < p.M ? k0 + p.cps : p.M;
+      if (VARIANT == VAR_STREAM) {
+        const size_t cu_bytes = VARLEN ? 4 * (size_t)(p.n_seqs + 1 <= kCuSmem ? p.n_seqs + 1 : 0) : 0;
+        unsigned char* region = smem + round_up(cu_bytes, 128);
+        if (S > 0)
+          stream_chunks<Op, MODE, VARLEN, J, TA, 1>(p, brn, g, k0, k1, win, carry, region);
+        else
+          stream_chunks<Op, MODE, VARLEN, J, TA, -1>(p, brn, g, k0, k1, win, carry, region);
+      } else {
+        int hint = -1;
+        for (int k = k0; k < k1; ++k) {
+          if (S > 0)
+            chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr,
+                                                   &hint);
+          else
+            chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr,
+                                                    &hint);
+        }
+      }
+      if (segmented && active && lane == 0)
+        st_relaxed(recs_row + 2 * (int64_t)seg + 1, pack_rec((epoch << 2) | 2u, carry));
+    } else if (threadIdx.x == 0) {
+      set_status(p.hdr, kStatusWorkspace);
+    }
+    if (segmented) {
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned d = atomicAdd(&p.hdr->done, 1u);
+        if (d == gridDim.x - 1) {
+          p.hdr->done = 0u;
+          atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
+          __threadfence();
+        }
+      }
     }
   }
+}
+
+// The register-carry kernels keep ptxas's default register budget for 256-
+// thread blocks; the stream kernel, whose occupancy shared memory bounds
+// anyway, may use the full register file so it does not spill.
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
+__global__ void __launch_bounds__(256) scalar_scan_kernel(const __grid_constant__ ScalarParams p) {
+  scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
+}
+
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
+__global__ void __launch_bounds__(256, 1)
+    scalar_stream_kernel(const __grid_constant__ ScalarParams p) {
+  scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
 }
 
 // Host-side dispatch over the compile-time choices.
 template <class Op, int MODE, typename TA, int VARIANT, bool VARLEN, bool VEC, int J>
 cudaError_t launch_one(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
-  auto kern = scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+  auto kern = [] {
+    if constexpr (VARIANT == VAR_STREAM)
+      return scalar_stream_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+    else
+      return scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+  }();
   if (pl.smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pl.smem);
     if (e != cudaSuccess) return e;
   }
-  const int64_t grid = (VARIANT == VAR_LOOKBACK) ? p.ntiles : (int64_t)p.G * p.nbr;
+  const bool ticketed = VARIANT == VAR_LOOKBACK || p.nseg > 1;
+  const int64_t grid = ticketed ? p.ntiles : (int64_t)p.G * p.nbr;
   if (grid <= 0) return cudaSuccess;
   kern<<<(unsigned)grid, 32 * p.R, pl.smem, s>>>(p);
   return cudaGetLastError();
@@ -774,26 +1116,36 @@ cudaError_t launch_pick_j(const ScalarParams& p, const ScalarPlan& pl, cudaStrea
     case 1: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 1>(p, pl, s);
     case 2: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 2>(p, pl, s);
     case 4: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 4>(p, pl, s);
-    case 8: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 8>(p, pl, s);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class Op, int MODE, typename TA, int VARIANT>
+cudaError_t launch_layouts(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
+  const bool varlen = p.cu != nullptr;
+  if constexpr (VARIANT == VAR_STREAM) {  // bulk copies need the vectorised layout
+    if (!pl.vec) return cudaErrorInvalidValue;
+    return varlen ? launch_pick_j<Op, MODE, TA, VARIANT, true, true>(p, pl, s)
+                  : launch_pick_j<Op, MODE, TA, VARIANT, false, true>(p, pl, s);
+  } else {
+    if (varlen)
+      return pl.vec ? launch_pick_j<Op, MODE, TA, VARIANT, true, true>(p, pl, s)
+                    : launch_pick_j<Op, MODE, TA, VARIANT, true, false>(p, pl, s);
+    return pl.vec ? launch_pick_j<Op, MODE, TA, VARIANT, false, true>(p, pl, s)
+                  : launch_pick_j<Op, MODE, TA, VARIANT, false, false>(p, pl, s);
   }
 }
 
 template <class Op, int MODE, typename TA>
 cudaError_t launch_scalar(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
-  const bool varlen = p.cu != nullptr;
-  if (pl.variant == VAR_LOOKBACK) {
-    if (varlen)
-      return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, true, true>(p, pl, s)
-                    : launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, true, false>(p, pl, s);
-    return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, false, true>(p, pl, s)
-                  : launch_pick_j<Op, MODE, TA, VAR_LOOKBACK, false, false>(p, pl, s);
+  switch (pl.variant) {
+    case VAR_LOOKBACK: return launch_layouts<Op, MODE, TA, VAR_LOOKBACK>(p, pl, s);
+    case VAR_STREAM: return launch_layouts<Op, MODE, TA, VAR_STREAM>(p, pl, s);
+    case VAR_STATIONARY:
+      return p.nseg > 1 ? launch_layouts<Op, MODE, TA, VAR_SEGMENTED>(p, pl, s)
+                        : launch_layouts<Op, MODE, TA, VAR_STATIONARY>(p, pl, s);
+    default: return cudaErrorInvalidValue;
   }
-  if (varlen)
-    return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_STATIONARY, true, true>(p, pl, s)
-                  : launch_pick_j<Op, MODE, TA, VAR_STATIONARY, true, false>(p, pl, s);
-  return pl.vec ? launch_pick_j<Op, MODE, TA, VAR_STATIONARY, false, true>(p, pl, s)
-                : launch_pick_j<Op, MODE, TA, VAR_STATIONARY, false, false>(p, pl, s);
 }
 
 }  // namespace scan

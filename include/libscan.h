@@ -87,16 +87,22 @@ typedef enum scan_dtype {
   SCAN_BF16 = 1
 } scan_dtype;
 
-/* How T is split across thread blocks. STATIONARY: one block walks the whole
- * row group in order with the running state in registers ([TSK] Kernel design;
- * [RGA] state-stationary serial path). LOOKBACK: T is cut into chunks handled
- * by independent blocks; each block publishes its chunk summary (P, Q)
- * ([RGA] Exact real chunk algebra) and reads its predecessors' summaries
- * (decoupled look-back). AUTO picks per shape. */
+/* How T is split across thread blocks. STATIONARY: a block walks a row
+ * group in order with the running state in registers ([TSK] Kernel design;
+ * [RGA] state-stationary serial path); long rows may be cut into a few
+ * segments, each block waiting once for the end state of the previous
+ * segment. LOOKBACK: T is cut into chunks handled by independent blocks; each
+ * block publishes its chunk summary (P, Q) ([RGA] Exact real chunk algebra)
+ * and reads its predecessors' summaries (decoupled look-back). STREAM: the
+ * stationary scheme with each warp's chunks streamed into a ring of shared-
+ * memory stages by bulk asynchronous copies (TMA), several chunks in flight
+ * per warp; needs 16-byte aligned tensors (else it runs as STATIONARY). AUTO
+ * picks per shape. */
 typedef enum scan_variant {
   SCAN_VARIANT_AUTO = 0,
   SCAN_VARIANT_STATIONARY = 1,
-  SCAN_VARIANT_LOOKBACK = 2
+  SCAN_VARIANT_LOOKBACK = 2,
+  SCAN_VARIANT_STREAM = 3
 } scan_variant;
 
 typedef enum scan_op {
@@ -112,13 +118,14 @@ typedef enum scan_op {
 /* Optional tuning and test controls; pass NULL for the defaults (all zero). */
 typedef struct scan_opts {
   int32_t variant;       /* scan_variant; 0 = AUTO */
-  int32_t chunk;         /* scalar/log: elements of T per block row, one of 128, 256, 512,
-                            1024; affine: time steps per block, one of 64, 128, 256; 0 = planner */
+  int32_t chunk;         /* scalar/log: elements of T per block row, one of 128, 256, 512;
+                            affine: time steps per block, one of 64, 128, 256; 0 = planner */
   int32_t rows_per_cta;  /* scalar/log: rows (channels) per block, 1..16; 0 = planner */
   int32_t test_stall;    /* test hook: 1 makes one look-back wait on a summary that is
                             never published, so the wait limit expires (SCAN_ERR_TIMEOUT) */
   double wait_limit_s;   /* bound on every look-back wait; <= 0 means 1.0 second */
   const int32_t* cu_seqlens_host; /* optional host copy of cu_seqlens, validated before launch */
+  int32_t segments;      /* stationary: segments each row is cut into (>= 1); 0 = planner */
 } scan_opts;
 
 /* Human-readable name of a status code (static string, never NULL). */

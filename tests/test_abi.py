@@ -65,6 +65,14 @@ def test_workspace_sizes():
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096,
                                      opts={"variant": scan.SCAN_VARIANT_STATIONARY}) == 256
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096) == 256
+    # forced stationary with too few row groups for four waves: rows are cut
+    # into segments that hand their end state on through the workspace
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 2048, 100000,
+                                     opts={"variant": scan.SCAN_VARIANT_STATIONARY}) == \
+        256 + 2048 * 5 * 16
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 2048, 100000,
+                                     opts={"variant": scan.SCAN_VARIANT_STATIONARY,
+                                           "segments": 1}) == 256
     # few rows (here 64) take the look-back
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 64, 100000) == \
         256 + 64 * ((100000 + 511) // 512) * 16
@@ -75,6 +83,8 @@ def test_workspace_sizes():
     # rejected arguments size to 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, -1, 4, 4) == 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 100}) == 0
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 1024}) == 0
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"variant": 4}) == 0
 
 
 def _raw(name):

@@ -40,7 +40,10 @@ def cuda(*ts):
 
 def variants(scan):
     return [("lookback", {"variant": scan.SCAN_VARIANT_LOOKBACK}),
-            ("stationary", {"variant": scan.SCAN_VARIANT_STATIONARY})]
+            ("stationary", {"variant": scan.SCAN_VARIANT_STATIONARY, "segments": 1}),
+            ("segmented", {"variant": scan.SCAN_VARIANT_STATIONARY, "segments": 3}),
+            ("stream", {"variant": scan.SCAN_VARIANT_STREAM, "segments": 1}),
+            ("stream_segmented", {"variant": scan.SCAN_VARIANT_STREAM, "segments": 2})]
 
 
 def check_fwd_bwd(scan, a, x, dh, h0=None, cu=None, reverse=False, opts=None, tol_h=TOL32,
@@ -73,7 +76,7 @@ def test_dense_fp32_shapes(lib, T, reverse):
         check_fwd_bwd(lib, w.a, w.x, w.dh, w.h0, None, reverse, opts)
 
 
-@pytest.mark.parametrize("chunk", [128, 256, 512, 1024])
+@pytest.mark.parametrize("chunk", [128, 256, 512])
 @pytest.mark.parametrize("rows_per_cta", [1, 3, 8])
 def test_dense_chunk_and_rows(lib, chunk, rows_per_cta):
     w = workloads.scalar_dense(3, 7, 3001, seed=chunk + rows_per_cta, h0=True)

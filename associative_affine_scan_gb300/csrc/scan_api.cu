@@ -52,12 +52,23 @@ int chunk_to_j(int chunk) {
 scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const scan_opts& o,
                         ScalarPlan* pl) {
   if (rows < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
+  int variant = o.variant;
+  if (variant < 0 || variant > 3) return SCAN_ERR_INVALID_ARG;
+  // Stationary blocks walk T in order with the carry in registers and no
+  // inter-block traffic; that needs enough rows to occupy every SM (one warp
+  // per row, about 16 resident warps per SM on 152 SMs). Fewer rows split T
+  // across blocks and use the look-back.
+  if (variant == SCAN_VARIANT_AUTO)
+    variant = rows * nbr >= kStationaryMinRows ? VAR_STATIONARY : VAR_LOOKBACK;
+  // Chunks of 256 steps (runs of 8 per lane) keep the register-carry kernels'
+  // loads at 8 cache lines per warp instruction; the look-back prefers 512
+  // (fewer published summaries per row).
   int J;
   if (o.chunk) {
     J = chunk_to_j(o.chunk);
     if (!J) return SCAN_ERR_INVALID_ARG;
   } else {
-    J = T <= 128 ? 1 : (T <= 256 ? 2 : 4);
+    J = T <= 128 ? 1 : ((T <= 256 || variant != VAR_LOOKBACK) ? 2 : 4);
   }
   int R = o.rows_per_cta;
   if (R < 0 || R > 8) return SCAN_ERR_INVALID_ARG;
@@ -68,14 +79,6 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   const int64_t span = T + ((T % 8) ? 7 : 0);
   const int64_t M = T > 0 ? (span + L - 1) / L : 0;
   const int64_t G = (rows + R - 1) / R;
-  int variant = o.variant;
-  if (variant < 0 || variant > 3) return SCAN_ERR_INVALID_ARG;
-  // Stationary blocks walk T in order with the carry in registers and no
-  // inter-block traffic; that needs enough rows to occupy every SM (one warp
-  // per row, about 16 resident warps per SM on 152 SMs). Fewer rows split T
-  // across blocks and use the look-back.
-  if (variant == SCAN_VARIANT_AUTO)
-    variant = rows * nbr >= kStationaryMinRows ? VAR_STATIONARY : VAR_LOOKBACK;
   const int64_t tiles = M * G * nbr;
   if (M > kMaxGrid || G > kMaxGrid || tiles > kMaxGrid || rows * M * nbr > (1LL << 40))
     return SCAN_ERR_UNSUPPORTED;

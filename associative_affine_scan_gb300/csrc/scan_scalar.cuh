@@ -10,18 +10,19 @@
 //
 // Work decomposition (one thread block = R rows x one chunk of L = 128 J
 // time steps; one warp per row):
-//   * each lane holds 4 consecutive steps per 128-step block, loaded with one
-//     128-bit (fp32) or 64-bit (bf16) coalesced access per block;
-//   * lane-serial composition of its 4 steps, a warp-shuffle inclusive scan of
-//     the lanes' (P, Q) pairs and a serial carry across the J blocks give every
-//     step its chunk-local map (P_t, Q_t) in fp32 registers;
+//   * each lane owns a run of V = 4 J consecutive steps, loaded as J aligned
+//     4-step groups (128-bit fp32 / 64-bit bf16 accesses);
+//   * a lane-serial pass composes the run's map (P, Q), a warp-shuffle
+//     inclusive scan of the 32 run maps gives each run its chunk-local
+//     prefix, and a second lane-serial pass runs the recurrence itself over
+//     the run from its carry-in, all in fp32 registers;
 //   * the chunk's carry-in comes either from the registers of the same block
 //     (STATIONARY: the block walks its row group's chunks in order) or from a
 //     decoupled look-back over the published summaries of earlier chunks
 //     (LOOKBACK: chunks are independent blocks taken in ticket order, chunk
 //     index major, so earlier chunks always belong to running or finished
 //     blocks);
-//   * h_t = P_t h_in + Q_t is stored with 128-bit streaming stores.
+//   * outputs are written with vector streaming stores.
 //
 // Packed sequences (cu_seqlens) never cut the tiling: the first step of every
 // sequence (in scan direction) becomes the constant map (0, a h0 + x), which
@@ -181,6 +182,13 @@ struct LinOp {
     return {e2.p * e1.p, fmaf(e2.p, e1.q, e2.q)};
   }
   static __device__ __forceinline__ float initial_carry() { return 0.f; }
+  // one step of the recurrence on the carried state, the state a sequence's
+  // first step produces, and the state as output
+  static __device__ __forceinline__ float step(float h, float a, float x) { return fmaf(a, h, x); }
+  static __device__ __forceinline__ float first(float a, float x, const float* h0, int64_t i) {
+    return fmaf(a, h0 ? h0[i] : 0.f, x);
+  }
+  static __device__ __forceinline__ float out(float h) { return h; }
   static __device__ __forceinline__ float value(const E& e, float c) { return fmaf(e.p, c, e.q); }
   static __device__ __forceinline__ float carry_after(const E& e, float c) { return fmaf(e.p, c, e.q); }
   static __device__ __forceinline__ bool is_const(const E& e) { return e.p == 0.f; }
@@ -241,6 +249,13 @@ struct LogOp {
     return r;
   }
   static __device__ __forceinline__ float initial_carry() { return -CUDART_INF_F; }
+  static __device__ __forceinline__ float step(float l, float la, float lx) {
+    return log_add_exp(l + la, lx);
+  }
+  static __device__ __forceinline__ float first(float la, float lx, const float* lh0, int64_t i) {
+    return lh0 ? log_add_exp(lh0[i] + la, lx) : lx;
+  }
+  static __device__ __forceinline__ float out(float l) { return __expf(l); }
   // linear-space output exp(l_t) for the carry-in log state c
   static __device__ __forceinline__ float value(const E& e, float c) {
     return __expf(c + e.a) + e.s * __expf(e.m);
@@ -433,35 +448,21 @@ __device__ float lookback(const ScalarParams& p, const unsigned long long* recs_
 }
 
 // ---------------------------------------------------------------------------
-// neighbours across lanes (backward needs a_{t+-1} and h_{t-+1})
-// ---------------------------------------------------------------------------
-
-// value at memory position (group start + 4): the next lane's first element,
-// the next block's lane 0, or the halo after the chunk
-template <int J>
-__device__ __forceinline__ float next_in_memory(const float (&V)[J][4], int j, float halo, int lane) {
-  float v = __shfl_down_sync(kFull, V[j][0], 1);
-  const float vb = (j + 1 < J) ? __shfl_sync(kFull, V[j + 1 < J ? j + 1 : j][0], 0) : halo;
-  return lane == 31 ? vb : v;
-}
-
-// value at memory position (group start - 1)
-template <int J>
-__device__ __forceinline__ float prev_in_memory(const float (&V)[J][4], int j, float halo, int lane) {
-  float v = __shfl_up_sync(kFull, V[j][3], 1);
-  const float vb = (j > 0) ? __shfl_sync(kFull, V[j > 0 ? j - 1 : 0][3], 31) : halo;
-  return lane == 0 ? vb : v;
-}
-
-// ---------------------------------------------------------------------------
 // one chunk of one row group
 // ---------------------------------------------------------------------------
 
+// Each lane owns a run of V = 4 J consecutive steps of the chunk (lane l:
+// steps t0 + V l ... t0 + V l + V - 1), read as J aligned 4-step groups.
+// The chunk costs one lane-serial pass to compose the run's map, one warp
+// scan over the 32 run maps, and one lane-serial pass that runs the
+// recurrence itself from the run's carry-in: about three arithmetic
+// instructions per step plus V-amortised shuffles.
+//
 // S is the scan direction: +1 walks t upwards, -1 downwards. A forward call
 // scans in the recurrence's direction; a backward call scans against it.
 // SMEM: the chunk's inputs are read from a shared-memory stage (sv) where it
 // holds them, else from global memory. seg_hint (packed sequences): the
-// sequence that held the previous chunk's steps for this warp, -1 if none;
+// sequence that held this lane's run in the previous chunk, -1 if none;
 // updated for the next chunk.
 template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S, bool SMEM = false>
 __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int k, bool stationary,
@@ -469,10 +470,12 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
                                       const StageView* sv = nullptr, int* seg_hint = nullptr) {
   using E = typename Op::E;
   constexpr int L = 128 * J;
+  constexpr int V = 4 * J;
+  constexpr bool BWD = MODE == MODE_BWD;
   const BranchArgs& br = p.br[brn];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)g * p.R + warp;
-  const bool active = row < p.rows;
+  if (row >= p.rows) return;  // the whole warp leaves together
   const int64_t T = p.T;
   const int m = (S > 0) ? k : (p.M - 1 - k);
   // rows are cut so that every 4-step group starts on a 4-element boundary of
@@ -482,114 +485,115 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
   const int shift = VEC ? (int)((row * T) & (kAlign - 1)) : 0;
   const int64_t t0 = (int64_t)m * L - shift;
   const int64_t roff = row * T;
-  const int64_t tl = t0 + 4 * lane;
+  const int64_t tr = t0 + (int64_t)V * lane;  // first step of this lane's run
 
-  float A[J][4], X[J][4], H[J][4];
-  float halo_a = 0.f, halo_h = 0.f;
-  if (active) {
-    const TA* a = static_cast<const TA*>(br.a) + roff;
-    if (MODE == MODE_FWD) {
-      const TA* x = static_cast<const TA*>(br.x) + roff;
+  // ---- loads: A = gates, X = inputs (forward) or dh (backward), H = states ----
+  float A[V], X[V], H[BWD ? V : 1];
+  const TA* a = static_cast<const TA*>(br.a) + roff;
+  const void* xsrc = BWD ? static_cast<const void*>(br.dh) : br.x;
+  const unsigned char* sx = SMEM ? (BWD ? sv->dh : sv->x) : nullptr;
 #pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int64_t t = tl + 128 * j;
-        if (SMEM && t >= sv->c_lo && t + 4 <= sv->c_hi && t >= 0 && t + 4 <= T) {
-          SIO<TA>::ld4(sv->a, t - sv->e0, A[j]);
-          SIO<TA>::ld4(sv->x, t - sv->e0, X[j]);
-        } else if (VEC && t >= 0 && t + 4 <= T) {
-          IO<TA>::ld4(a + t, A[j]);
-          IO<TA>::ld4(x + t, X[j]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int64_t tt = t + e;
-            const bool v = tt >= 0 && tt < T;
-            A[j][e] = v ? IO<TA>::ld1(a + tt) : 0.f;
-            X[j][e] = v ? IO<TA>::ld1(x + tt) : 0.f;
-          }
-        }
+  for (int i = 0; i < J; ++i) {
+    const int64_t t = tr + 4 * i;
+    float* ai = A + 4 * i;
+    float* xi = X + 4 * i;
+    float* hi = H + (BWD ? 4 * i : 0);
+    if (SMEM && t >= sv->c_lo && t + 4 <= sv->c_hi && t >= 0 && t + 4 <= T) {
+      SIO<TA>::ld4(sv->a, t - sv->e0, ai);
+      if (BWD) {
+        SIO<float>::ld4(sx, t - sv->e0, xi);
+        SIO<float>::ld4(sv->h, t - sv->e0, hi);
+      } else {
+        SIO<TA>::ld4(sx, t - sv->e0, xi);
+      }
+    } else if (VEC && t >= 0 && t + 4 <= T) {
+      IO<TA>::ld4(a + t, ai);
+      if (BWD) {
+        IO<float>::ld4(static_cast<const float*>(xsrc) + roff + t, xi);
+        IO<float>::ld4(br.h + roff + t, hi);
+      } else {
+        IO<TA>::ld4(static_cast<const TA*>(xsrc) + roff + t, xi);
       }
     } else {
-      const float* h = br.h + roff;
-      const float* dh = br.dh + roff;
 #pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int64_t t = tl + 128 * j;
-        if (SMEM && t >= sv->c_lo && t + 4 <= sv->c_hi && t >= 0 && t + 4 <= T) {
-          SIO<TA>::ld4(sv->a, t - sv->e0, A[j]);
-          SIO<float>::ld4(sv->h, t - sv->e0, H[j]);
-          SIO<float>::ld4(sv->dh, t - sv->e0, X[j]);
-        } else if (VEC && t >= 0 && t + 4 <= T) {
-          IO<TA>::ld4(a + t, A[j]);
-          IO<float>::ld4(h + t, H[j]);
-          IO<float>::ld4(dh + t, X[j]);
+      for (int e = 0; e < 4; ++e) {
+        const int64_t tt = t + e;
+        const bool v = tt >= 0 && tt < T;
+        ai[e] = v ? IO<TA>::ld1(a + tt) : 0.f;
+        if (BWD) {
+          xi[e] = v ? IO<float>::ld1(static_cast<const float*>(xsrc) + roff + tt) : 0.f;
+          hi[e] = v ? IO<float>::ld1(br.h + roff + tt) : 0.f;
         } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int64_t tt = t + e;
-            const bool v = tt >= 0 && tt < T;
-            A[j][e] = v ? IO<TA>::ld1(a + tt) : 0.f;
-            H[j][e] = v ? IO<float>::ld1(h + tt) : 0.f;
-            X[j][e] = v ? IO<float>::ld1(dh + tt) : 0.f;
-          }
+          xi[e] = v ? IO<TA>::ld1(static_cast<const TA*>(xsrc) + roff + tt) : 0.f;
         }
       }
-      // halos: the gate one step after (S = -1) or before (S = +1) the chunk,
-      // the state one step before (S = -1) or after (S = +1)
-      if (lane == 0) {
-        const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
-        const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
-        if (pa >= 0 && pa < T)
-          halo_a = (SMEM && pa >= sv->c_lo && pa < sv->c_hi) ? SIO<TA>::ld1(sv->a, pa - sv->e0)
-                                                               : IO<TA>::ld1(a + pa);
-        if (ph >= 0 && ph < T)
-          halo_h = (SMEM && ph >= sv->c_lo && ph < sv->c_hi) ? SIO<float>::ld1(sv->h, ph - sv->e0)
-                                                               : IO<float>::ld1(h + ph);
-      }
-      halo_a = __shfl_sync(kFull, halo_a, 0);
-      halo_h = __shfl_sync(kFull, halo_h, 0);
     }
   }
 
-  if (!active) return;
-
-  // packed sequences: the sequence holding each group's first step (one
-  // search per lane, then forward steps), and whether the group's 4 steps
-  // are interior: no sequence starts or ends on them, so they need no
-  // per-step boundary test
-  int gseg[J];
-  bool inner[J];
-#pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int64_t t = tl + 128 * j;
-    gseg[j] = 0;
-    if (VARLEN) {
-      const int64_t tc = t < 0 ? 0 : (t < T ? t : T - 1);
-      if (j == 0)
-        gseg[j] = seg_hint ? seg_near(win, *seg_hint, tc) : seg_find(win, tc);
-      else
-        gseg[j] = seg_advance(win, gseg[j - 1], tc);
-      inner[j] = t >= 0 && t + 4 <= T && (int64_t)win.cu[gseg[j]] != t &&
-                 (int64_t)win.cu[gseg[j] + 1] > t + 4;
+  // backward neighbours across runs: the gate one step past the run's far
+  // end in scan order (a_{t+1} for S = -1, a_{t-1} for S = +1) and the
+  // state one step past its near end (h_{t-1}, resp. h_{t+1}); the lanes at
+  // the chunk's edges take them from memory (the halos)
+  float a_nb = 0.f, h_nb = 0.f;
+  if (BWD) {
+    float halo_a = 0.f, halo_h = 0.f;
+    if (lane == 0) {
+      const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
+      const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
+      if (pa >= 0 && pa < T)
+        halo_a = (SMEM && pa >= sv->c_lo && pa < sv->c_hi) ? SIO<TA>::ld1(sv->a, pa - sv->e0)
+                                                             : IO<TA>::ld1(a + pa);
+      if (ph >= 0 && ph < T)
+        halo_h = (SMEM && ph >= sv->c_lo && ph < sv->c_hi) ? SIO<float>::ld1(sv->h, ph - sv->e0)
+                                                             : IO<float>::ld1(br.h + roff + ph);
+    }
+    halo_a = __shfl_sync(kFull, halo_a, 0);
+    halo_h = __shfl_sync(kFull, halo_h, 0);
+    if (S < 0) {
+      const float an = __shfl_down_sync(kFull, A[0], 1);
+      const float hp = __shfl_up_sync(kFull, H[V - 1], 1);
+      a_nb = lane == 31 ? halo_a : an;
+      h_nb = lane == 0 ? halo_h : hp;
     } else {
-      inner[j] = false;  // dense rows test t == 0 and t == T - 1 directly
+      const float ap = __shfl_up_sync(kFull, A[V - 1], 1);
+      const float hn = __shfl_down_sync(kFull, H[0], 1);
+      a_nb = lane == 0 ? halo_a : ap;
+      h_nb = lane == 31 ? halo_h : hn;
     }
   }
-  if (VARLEN && seg_hint) *seg_hint = (S > 0) ? gseg[J - 1] : gseg[0];
-  // Boundary facts of step tt (valid, in group j): does a sequence start or
+  // backward: the shifted gate of element e (before sequence cuts), and the
+  // neighbouring state that multiplies dx into da
+  auto gate_of = [&](int e) -> float {
+    if (S < 0) return e + 1 < V ? A[e + 1 < V ? e + 1 : e] : a_nb;
+    return e > 0 ? A[e > 0 ? e - 1 : 0] : a_nb;
+  };
+  auto hn_of = [&](int e) -> float {
+    if (S < 0) return e > 0 ? H[BWD ? (e > 0 ? e - 1 : 0) : 0] : h_nb;
+    return e + 1 < V ? H[BWD ? (e + 1 < V ? e + 1 : e) : 0] : h_nb;
+  };
+
+  // ---- is the run plain: every step valid, no sequence starts or ends in it ----
+  int s_run = 0;
+  bool plain;
+  if (VARLEN) {
+    const int64_t tc = tr < 0 ? 0 : (tr < T ? tr : T - 1);
+    s_run = seg_hint ? seg_near(win, *seg_hint, tc) : seg_find(win, tc);
+    if (seg_hint) *seg_hint = s_run;
+    plain = tr >= 0 && tr + V <= T && (int64_t)win.cu[s_run] != tr &&
+            (int64_t)win.cu[s_run + 1] > tr + V;
+  } else {
+    plain = tr > 0 && tr + V < T;
+  }
+  // Boundary facts of a valid step tt of the run: does a sequence start or
   // end there, and which row of h0/dh0 belongs to its sequence.
   struct Bound {
     bool start, end;
     int64_t h0row;
   };
-  auto bound = [&](int j, int64_t tt) -> Bound {
+  auto bound = [&](int64_t tt) -> Bound {
     Bound b;
-    if (VARLEN && inner[j]) {
-      b.start = false;
-      b.end = false;
-      b.h0row = row;
-    } else if (VARLEN) {
-      const int s = seg_advance(win, gseg[j], tt);
+    if (VARLEN) {
+      const int s = seg_advance(win, s_run, tt);
       b.start = (int64_t)win.cu[s] == tt;
       b.end = (int64_t)win.cu[s + 1] == tt + 1;
       b.h0row = (int64_t)s * p.rows + row;
@@ -601,83 +605,44 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
     return b;
   };
 
-  // ---- elements ----
-  E el[J][4];
-  float HN[J];  // backward: cross-lane neighbour state of each group's edge step
+  // ---- pass 1: the run's map, composed in scan order ----
+  E run = Op::identity();
+  if (plain) {
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int64_t t = tl + 128 * j;
-    if (MODE == MODE_FWD) {
+    for (int ii = 0; ii < V; ++ii) {
+      const int e = (S > 0) ? ii : V - 1 - ii;
+      run = Op::compose(run, Op::make(BWD ? gate_of(e) : A[e], X[e]));
+    }
+  } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int64_t tt = t + e;
-        E v = Op::identity();
-        if (tt >= 0 && tt < T) {
-          v = Op::make(A[j][e], X[j][e]);
-          const Bound bd = bound(j, tt);
-          if ((S > 0) ? bd.start : bd.end) v = Op::make_first(A[j][e], X[j][e], br.h0, bd.h0row);
-        }
-        el[j][e] = v;
+    for (int ii = 0; ii < V; ++ii) {
+      const int e = (S > 0) ? ii : V - 1 - ii;
+      const int64_t tt = tr + e;
+      if (tt < 0 || tt >= T) continue;  // outside the row: the identity
+      const Bound bd = bound(tt);
+      E v;
+      if (!BWD) {
+        v = ((S > 0) ? bd.start : bd.end) ? Op::make_first(A[e], X[e], br.h0, bd.h0row)
+                                          : Op::make(A[e], X[e]);
+      } else {
+        // the shifted gate is 0 past the end of the sequence (scan-first step)
+        v = Op::make(((S < 0) ? bd.end : bd.start) ? 0.f : gate_of(e), X[e]);
       }
-    } else {
-      float gate[4];
-      if (S < 0) {  // causal recurrence: gate a_{t+1}, state h_{t-1}
-        gate[0] = A[j][1];
-        gate[1] = A[j][2];
-        gate[2] = A[j][3];
-        gate[3] = next_in_memory<J>(A, j, halo_a, lane);
-        HN[j] = prev_in_memory<J>(H, j, halo_h, lane);
-      } else {  // reverse recurrence: gate a_{t-1}, state h_{t+1}
-        gate[0] = prev_in_memory<J>(A, j, halo_a, lane);
-        gate[1] = A[j][0];
-        gate[2] = A[j][1];
-        gate[3] = A[j][2];
-        HN[j] = next_in_memory<J>(H, j, halo_h, lane);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int64_t tt = t + e;
-        E v = Op::identity();
-        if (tt >= 0 && tt < T) {
-          // the shifted gate is 0 past the end of the sequence (scan-first step)
-          const Bound bd = bound(j, tt);
-          const bool cut = (S < 0) ? bd.end : bd.start;
-          v = Op::make(cut ? 0.f : gate[e], X[j][e]);
-        }
-        el[j][e] = v;
-      }
+      run = Op::compose(run, v);
     }
   }
 
-  // ---- chunk-local inclusive scan in scan order ----
-  E blk = Op::identity();
+  // ---- warp scan of the run maps: exclusive prefix and chunk total ----
+  E inc = run;
 #pragma unroll
-  for (int jj = 0; jj < J; ++jj) {
-    const int j = (S > 0) ? jj : (J - 1 - jj);
-    E lane_tot;
-    if (S > 0) {
-#pragma unroll
-      for (int e = 1; e < 4; ++e) el[j][e] = Op::compose(el[j][e - 1], el[j][e]);
-      lane_tot = el[j][3];
-    } else {
-#pragma unroll
-      for (int e = 2; e >= 0; --e) el[j][e] = Op::compose(el[j][e + 1], el[j][e]);
-      lane_tot = el[j][0];
-    }
-    E inc = lane_tot;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const E o = (S > 0) ? Op::shfl_up(inc, off) : Op::shfl_down(inc, off);
-      const bool has = (S > 0) ? (lane >= off) : (lane + off < 32);
-      if (has) inc = Op::compose(o, inc);
-    }
-    E ex = (S > 0) ? Op::shfl_up(inc, 1) : Op::shfl_down(inc, 1);
-    if (lane == ((S > 0) ? 0 : 31)) ex = Op::identity();
-    const E pre = Op::compose(blk, ex);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) el[j][e] = Op::compose(pre, el[j][e]);
-    blk = Op::compose(blk, Op::shfl(inc, (S > 0) ? 31 : 0));
+  for (int off = 1; off < 32; off <<= 1) {
+    const E o = (S > 0) ? Op::shfl_up(inc, off) : Op::shfl_down(inc, off);
+    const bool has = (S > 0) ? (lane >= off) : (lane + off < 32);
+    if (has) inc = Op::compose(o, inc);
   }
+  E ex = (S > 0) ? Op::shfl_up(inc, 1) : Op::shfl_down(inc, 1);
+  if (lane == ((S > 0) ? 0 : 31)) ex = Op::identity();
+  const E blk = Op::shfl(inc, (S > 0) ? 31 : 0);
 
   // ---- carry-in ----
   float c;
@@ -708,56 +673,77 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
     }
   }
 
-  // ---- outputs ----
-  if (MODE == MODE_FWD) {
+  // ---- pass 2: the recurrence over the run from its carry-in; X[e] becomes
+  // the output (h_t forward, the adjoint g_t = dL/dx_t backward) ----
+  float st = Op::carry_after(ex, c);
+  if (plain) {
+#pragma unroll
+    for (int ii = 0; ii < V; ++ii) {
+      const int e = (S > 0) ? ii : V - 1 - ii;
+      st = Op::step(st, BWD ? gate_of(e) : A[e], X[e]);
+      X[e] = Op::out(st);
+    }
+  } else {
+#pragma unroll
+    for (int ii = 0; ii < V; ++ii) {
+      const int e = (S > 0) ? ii : V - 1 - ii;
+      const int64_t tt = tr + e;
+      if (tt < 0 || tt >= T) continue;
+      const Bound bd = bound(tt);
+      if (!BWD) {
+        st = ((S > 0) ? bd.start : bd.end) ? Op::first(A[e], X[e], br.h0, bd.h0row)
+                                           : Op::step(st, A[e], X[e]);
+      } else {
+        st = Op::step(st, ((S < 0) ? bd.end : bd.start) ? 0.f : gate_of(e), X[e]);
+      }
+      X[e] = Op::out(st);
+    }
+  }
+
+  // ---- stores ----
+  if (!BWD) {
     float* h = br.out_h + roff;
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int64_t t = tl + 128 * j;
-      float v[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = Op::value(el[j][e], c);
+    for (int i = 0; i < J; ++i) {
+      const int64_t t = tr + 4 * i;
       if (VEC && t >= 0 && t + 4 <= T) {
-        IO<float>::st4(h + t, v);
+        IO<float>::st4(h + t, X + 4 * i);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (t + e >= 0 && t + e < T) IO<float>::st1(h + t + e, v[e]);
+          if (t + e >= 0 && t + e < T) IO<float>::st1(h + t + e, X[4 * i + e]);
       }
     }
   } else {
     TA* dx = static_cast<TA*>(br.dx) + roff;
     TA* da = static_cast<TA*>(br.da) + roff;
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int64_t t = tl + 128 * j;
-      float gx[4], ga[4];
+    for (int i = 0; i < J; ++i) {
+      const int64_t t = tr + 4 * i;
+      float ga[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
+        const int idx = 4 * i + e;
+        float hn = hn_of(idx);
         const int64_t tt = t + e;
-        const float gv = Op::value(el[j][e], c);
-        float hn;
-        if (S < 0) hn = (e > 0) ? H[j][e - 1] : HN[j];
-        else hn = (e < 3) ? H[j][e + 1] : HN[j];
-        if (tt >= 0 && tt < T) {
+        if (!plain && tt >= 0 && tt < T) {
           // the step that starts the forward recurrence reads h0 and feeds dh0
-          const Bound bd = bound(j, tt);
+          const Bound bd = bound(tt);
           if ((S < 0) ? bd.start : bd.end) {
             hn = br.h0 ? br.h0[bd.h0row] : 0.f;
-            if (br.dh0) br.dh0[bd.h0row] = A[j][e] * gv;
+            if (br.dh0) br.dh0[bd.h0row] = A[idx] * X[idx];
           }
         }
-        gx[e] = gv;
-        ga[e] = gv * hn;
+        ga[e] = X[idx] * hn;
       }
       if (VEC && t >= 0 && t + 4 <= T) {
-        IO<TA>::st4(dx + t, gx);
+        IO<TA>::st4(dx + t, X + 4 * i);
         IO<TA>::st4(da + t, ga);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           if (t + e >= 0 && t + e < T) {
-            IO<TA>::st1(dx + t + e, gx[e]);
+            IO<TA>::st1(dx + t + e, X[4 * i + e]);
             IO<TA>::st1(da + t + e, ga[e]);
           }
       }

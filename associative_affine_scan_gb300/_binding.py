@@ -69,6 +69,7 @@ class ScanOpts(ctypes.Structure):
         ("wait_limit_s", ctypes.c_double),
         ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
         ("segments", ctypes.c_int32),
+        ("stages", ctypes.c_int32),
     ]
 
 

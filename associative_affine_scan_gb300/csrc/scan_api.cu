@@ -16,6 +16,7 @@ constexpr int64_t kMaxGrid = 0x7fffffffLL;
 constexpr int64_t kStationaryMinRows = 152 * 16;
 constexpr int64_t kStationaryWaves = 4;
 constexpr int kCuSmemEntries = 4096;  // packed offsets staged in shared memory
+constexpr bool kStreamOutTiles = true;  // stream: interior outputs leave by tensor stores
 
 __global__ void fill_zero_kernel(float* p, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -49,8 +50,11 @@ int chunk_to_j(int chunk) {
 
 // Per-shape plan for the scalar and log forms. rows = B*C (dense) or C (packed);
 // nbr = number of branches launched together.
-scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const scan_opts& o,
-                        ScalarPlan* pl) {
+// wide: the call prefers chunks of 512 steps -- dense fp32 rows of the linear
+// form (whose register-carry kernels use the interleaved, fully coalesced
+// layout) and log-space rows (bound by arithmetic, which longer runs cut).
+scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, bool wide,
+                        const scan_opts& o, ScalarPlan* pl) {
   if (rows < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
   int variant = o.variant;
   if (variant < 0 || variant > 3) return SCAN_ERR_INVALID_ARG;
@@ -60,15 +64,18 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   // across blocks and use the look-back.
   if (variant == SCAN_VARIANT_AUTO)
     variant = rows * nbr >= kStationaryMinRows ? VAR_STATIONARY : VAR_LOOKBACK;
-  // Chunks of 256 steps (runs of 8 per lane) keep the register-carry kernels'
-  // loads at 8 cache lines per warp instruction; the look-back prefers 512
-  // (fewer published summaries per row).
+  // Lane runs of 8 steps (chunks of 256) keep the register-carry kernels'
+  // loads at 8 cache lines per warp instruction; wide calls, the stream
+  // variant's tiles and the look-back (fewer published summaries per row)
+  // take chunks of 512.
   int J;
   if (o.chunk) {
     J = chunk_to_j(o.chunk);
     if (!J) return SCAN_ERR_INVALID_ARG;
+  } else if (T <= 256) {
+    J = T <= 128 ? 1 : 2;
   } else {
-    J = T <= 128 ? 1 : ((T <= 256 || variant != VAR_LOOKBACK) ? 2 : 4);
+    J = (wide || variant == VAR_LOOKBACK || variant == VAR_STREAM) ? 4 : 2;
   }
   int R = o.rows_per_cta;
   if (R < 0 || R > 8) return SCAN_ERR_INVALID_ARG;
@@ -86,7 +93,7 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   // fewer than about four waves of blocks (152 SMs x 16 warps), so that no
   // long-running block is left alone in a last partial wave.
   int64_t nseg = 1, cps = M;
-  if ((variant == VAR_STATIONARY || variant == VAR_STREAM) && M > 0) {
+  if (variant == VAR_STATIONARY && M > 0) {
     if (o.segments < 0) return SCAN_ERR_INVALID_ARG;
     const int64_t blocks = G * nbr;
     const int64_t target = kStationaryWaves * 152 * 16 / R;
@@ -106,8 +113,9 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, const sca
   pl->vec = true;
   size_t recs = 0;
   if (variant == VAR_LOOKBACK) recs = (size_t)(nbr * rows * M);
-  if ((variant == VAR_STATIONARY || variant == VAR_STREAM) && nseg > 1)
-    recs = (size_t)(nbr * rows * nseg);
+  if (variant == VAR_STATIONARY && nseg > 1) recs = (size_t)(nbr * rows * nseg);
+  if (o.stages < 0 || o.stages == 1 || o.stages > kMaxStages) return SCAN_ERR_INVALID_ARG;
+  pl->ns = o.stages;
   pl->ws_bytes = kWsHeaderBytes + recs * 16u;
   (void)varlen;
   pl->smem = 0;
@@ -145,8 +153,8 @@ scan_status check_host_cu(const int32_t* cu, int32_t n, int64_t T) {
 // Shared front end of the scalar/log entry points: shape checks, plan,
 // workspace check, base parameters.
 scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t n_seqs, int nbr,
-                    const scan_opts& o, void* ws, size_t ws_bytes, ScalarParams* p,
-                    ScalarPlan* pl) {
+                    bool wide, const scan_opts& o, void* ws, size_t ws_bytes,
+                    ScalarParams* p, ScalarPlan* pl) {
   if (B < 0 || C < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
   if (cu) {
     if (B != 1 || n_seqs < 1 || T > 0x7fffffffLL) return SCAN_ERR_INVALID_ARG;
@@ -156,7 +164,7 @@ scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t 
     }
   }
   const int64_t rows = B * C;
-  scan_status st = plan_scalar(rows, T, nbr, cu != nullptr, o, pl);
+  scan_status st = plan_scalar(rows, T, nbr, cu != nullptr, wide, o, pl);
   if (st != SCAN_OK) return st;
   if (!ws) return SCAN_ERR_WORKSPACE;
   if (ws_bytes < pl->ws_bytes || !aligned(ws, 16)) return SCAN_ERR_WORKSPACE;
@@ -182,20 +190,54 @@ scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t 
   return SCAN_OK;
 }
 
-// The stream variant copies whole 16-byte blocks into shared memory: it needs
-// 16-byte aligned tensors and a ring that fits in shared memory; otherwise
-// the same stationary scheme runs with register loads.
-void finish_plan(ScalarPlan* pl, int mode, size_t elt_a, bool all16) {
+// Workspace of a scalar/log call: the larger of the two layouts' plans, so
+// one size serves every dtype and form of the call.
+size_t ws_scalar(int64_t rows, int64_t T, int nbr, const scan_opts& o) {
+  ScalarPlan a, b;
+  if (plan_scalar(rows, T, nbr, false, false, o, &a) != SCAN_OK) return 0;
+  if (plan_scalar(rows, T, nbr, false, true, o, &b) != SCAN_OK) return 0;
+  return a.ws_bytes > b.ws_bytes ? a.ws_bytes : b.ws_bytes;
+}
+
+// The stream variant reads and writes every tensor through tensor maps: all
+// of them 16-byte aligned, at least one 128-byte row (64 elements) long, and
+// a ring that fits in shared memory; otherwise the same rows run STATIONARY.
+// Its chunks start on a 128-byte row of the flat tensor, so a row is shifted
+// by up to E - 1 elements (E = 128 / element size of a) and M is recounted;
+// without segments it needs only the workspace header.
+void finish_plan(ScalarPlan* pl, ScalarParams* p, int mode, int elt_a, bool all16,
+                 int rows_per_cta) {
   if (pl->variant != VAR_STREAM) return;
-  const int stages = stream_stages(pl->J);
-  const size_t ring = round_up((size_t)pl->R * stages * 8, 128) +
-                      (size_t)pl->R * stages * stream_stage_bytes(mode, pl->J, (int)elt_a);
-  const size_t total = round_up(pl->smem, 128) + ring;
-  if (!pl->vec || !all16 || total > 227 * 1024) {
+  const int E = tma_row_elems(elt_a);
+  const int64_t n = p->rows * p->T;
+  auto fallback = [&] {
     pl->variant = VAR_STATIONARY;
-    return;
+    pl->nseg = p->nseg = 1;
+    pl->cps = p->cps = pl->M;
+  };
+  if (!pl->vec || !all16 || n < E) return fallback();
+  if (rows_per_cta == 0) {
+    pl->R = p->R = 1;
+    pl->G = p->G = (int)((p->rows + pl->R - 1) / pl->R);
   }
-  pl->smem = total;
+  const int64_t L = 128LL * pl->J;
+  const int64_t span = p->T + ((p->T % E) ? E - 1 : 0);
+  pl->M = p->M = (int)((span + L - 1) / L);
+  // the stage is refilled as soon as it is in registers, so a few stages
+  // cover the copies' latency
+  const int ns = pl->ns ? pl->ns : 3;
+  pl->tma_out = kStreamOutTiles;
+  const size_t cu = round_up(pl->smem, 128);
+  auto total = [&](int k) {
+    return cu + tma_bar_bytes(pl->R) + 1024 +
+           (size_t)pl->R * tma_warp_bytes(mode, pl->J, elt_a, k, pl->tma_out);
+  };
+  if (total(ns) > 227 * 1024) return fallback();
+  pl->ns = p->ns = ns;
+  p->tma_out = pl->tma_out ? 1 : 0;
+  pl->nseg = p->nseg = 1;
+  pl->cps = p->cps = pl->M;
+  pl->smem = total(ns);
 }
 
 scan_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA; }
@@ -241,15 +283,14 @@ size_t scan_workspace_bytes(scan_op op, int64_t B, int64_t C, int64_t T, int32_t
                             const scan_opts* opts) {
   const scan_opts o = defaults(opts);
   if (B < 0 || C < 0 || T < 0) return 0;
-  ScalarPlan pl;
   switch (op) {
     case SCAN_OP_FWD:
     case SCAN_OP_BWD:
     case SCAN_OP_LOG_FWD:
-      return plan_scalar(B * C, T, 1, false, o, &pl) == SCAN_OK ? pl.ws_bytes : 0;
+      return ws_scalar(B * C, T, 1, o);
     case SCAN_OP_BIDIR_FWD:
     case SCAN_OP_BIDIR_BWD:
-      return plan_scalar(B * C, T, 2, false, o, &pl) == SCAN_OK ? pl.ws_bytes : 0;
+      return ws_scalar(B * C, T, 2, o);
     case SCAN_OP_AFFINE_FWD:
     case SCAN_OP_AFFINE_BWD: {
       AffinePlan ap;
@@ -287,12 +328,14 @@ scan_status scan_fwd(const void* a, const void* x, const float* h0, const int32_
   const scan_opts o = defaults(opts);
   ScalarParams p;
   ScalarPlan pl;
-  scan_status st = prepare(B, C, T, cu, n_seqs, 1, o, ws, ws_bytes, &p, &pl);
+  scan_status st =
+      prepare(B, C, T, cu, n_seqs, 1, !cu && dt == SCAN_F32, o, ws, ws_bytes, &p, &pl);
   if (st != SCAN_OK) return st;
   if (p.rows * T == 0) return SCAN_OK;
   if (!a || !x || !h) return SCAN_ERR_INVALID_ARG;
   pl.vec = aligned(a, 4 * elt(dt)) && aligned(x, 4 * elt(dt)) && aligned(h, 16);
-  finish_plan(&pl, MODE_FWD, elt(dt), aligned(a, 16) && aligned(x, 16));
+  finish_plan(&pl, &p, MODE_FWD, (int)elt(dt), aligned(a, 16) && aligned(x, 16) && aligned(h, 16),
+              o.rows_per_cta);
   p.br[0].a = a;
   p.br[0].x = x;
   p.br[0].h0 = h0;
@@ -310,14 +353,18 @@ scan_status scan_bwd(const void* a, const float* h, const float* dh, const float
   const scan_opts o = defaults(opts);
   ScalarParams p;
   ScalarPlan pl;
-  scan_status st = prepare(B, C, T, cu, n_seqs, 1, o, ws, ws_bytes, &p, &pl);
+  scan_status st =
+      prepare(B, C, T, cu, n_seqs, 1, !cu && dt == SCAN_F32, o, ws, ws_bytes, &p, &pl);
   if (st != SCAN_OK) return st;
   const int64_t n_h0 = cu ? (int64_t)n_seqs * C : B * C;
   if (p.rows * T == 0) return zero_dh0(dh0, n_h0, stream);
   if (!a || !h || !dh || !da || !dx) return SCAN_ERR_INVALID_ARG;
   pl.vec = aligned(a, 4 * elt(dt)) && aligned(da, 4 * elt(dt)) && aligned(dx, 4 * elt(dt)) &&
            aligned(h, 16) && aligned(dh, 16);
-  finish_plan(&pl, MODE_BWD, elt(dt), aligned(a, 16));
+  finish_plan(&pl, &p, MODE_BWD, (int)elt(dt),
+              aligned(a, 16) && aligned(h, 16) && aligned(dh, 16) && aligned(da, 16) &&
+                  aligned(dx, 16),
+              o.rows_per_cta);
   p.br[0].a = a;
   p.br[0].h = h;
   p.br[0].dh = dh;
@@ -338,15 +385,18 @@ scan_status scan_bidir_fwd(const void* af, const void* xf, const void* ar, const
   const scan_opts o = defaults(opts);
   ScalarParams p;
   ScalarPlan pl;
-  scan_status st = prepare(B, C, T, cu, n_seqs, 2, o, ws, ws_bytes, &p, &pl);
+  scan_status st =
+      prepare(B, C, T, cu, n_seqs, 2, !cu && dt == SCAN_F32, o, ws, ws_bytes, &p, &pl);
   if (st != SCAN_OK) return st;
   if (p.rows * T == 0) return SCAN_OK;
   if (!af || !xf || !ar || !xr || !hf || !hr) return SCAN_ERR_INVALID_ARG;
   const size_t va = 4 * elt(dt);
   pl.vec = aligned(af, va) && aligned(xf, va) && aligned(ar, va) && aligned(xr, va) &&
            aligned(hf, 16) && aligned(hr, 16);
-  finish_plan(&pl, MODE_FWD, elt(dt),
-              aligned(af, 16) && aligned(xf, 16) && aligned(ar, 16) && aligned(xr, 16));
+  finish_plan(&pl, &p, MODE_FWD, (int)elt(dt),
+              aligned(af, 16) && aligned(xf, 16) && aligned(ar, 16) && aligned(xr, 16) &&
+                  aligned(hf, 16) && aligned(hr, 16),
+              o.rows_per_cta);
   p.br[0].a = af;
   p.br[0].x = xf;
   p.br[0].h0 = h0f;
@@ -371,7 +421,8 @@ scan_status scan_bidir_bwd(const void* af, const float* hf, const float* dhf, co
   const scan_opts o = defaults(opts);
   ScalarParams p;
   ScalarPlan pl;
-  scan_status st = prepare(B, C, T, cu, n_seqs, 2, o, ws, ws_bytes, &p, &pl);
+  scan_status st =
+      prepare(B, C, T, cu, n_seqs, 2, !cu && dt == SCAN_F32, o, ws, ws_bytes, &p, &pl);
   if (st != SCAN_OK) return st;
   const int64_t n_h0 = cu ? (int64_t)n_seqs * C : B * C;
   if (p.rows * T == 0) {
@@ -384,7 +435,11 @@ scan_status scan_bidir_bwd(const void* af, const float* hf, const float* dhf, co
   pl.vec = aligned(af, va) && aligned(ar, va) && aligned(daf, va) && aligned(dxf, va) &&
            aligned(dar, va) && aligned(dxr, va) && aligned(hf, 16) && aligned(dhf, 16) &&
            aligned(hr, 16) && aligned(dhr, 16);
-  finish_plan(&pl, MODE_BWD, elt(dt), aligned(af, 16) && aligned(ar, 16));
+  finish_plan(&pl, &p, MODE_BWD, (int)elt(dt),
+              aligned(af, 16) && aligned(ar, 16) && aligned(hf, 16) && aligned(dhf, 16) &&
+                  aligned(hr, 16) && aligned(dhr, 16) && aligned(daf, 16) && aligned(dxf, 16) &&
+                  aligned(dar, 16) && aligned(dxr, 16),
+              o.rows_per_cta);
   p.br[0].a = af;
   p.br[0].h = hf;
   p.br[0].dh = dhf;
@@ -412,12 +467,13 @@ scan_status scan_log_fwd(const float* log_a, const float* log_x, const float* lo
   const scan_opts o = defaults(opts);
   ScalarParams p;
   ScalarPlan pl;
-  scan_status st = prepare(B, C, T, cu, n_seqs, 1, o, ws, ws_bytes, &p, &pl);
+  scan_status st = prepare(B, C, T, cu, n_seqs, 1, true, o, ws, ws_bytes, &p, &pl);
   if (st != SCAN_OK) return st;
   if (p.rows * T == 0) return SCAN_OK;
   if (!log_a || !log_x || !h) return SCAN_ERR_INVALID_ARG;
   pl.vec = aligned(log_a, 16) && aligned(log_x, 16) && aligned(h, 16);
-  finish_plan(&pl, MODE_FWD, 4, true);
+  finish_plan(&pl, &p, MODE_FWD, 4, aligned(log_a, 16) && aligned(log_x, 16) && aligned(h, 16),
+              o.rows_per_cta);
   p.br[0].a = log_a;
   p.br[0].x = log_x;
   p.br[0].h0 = log_h0;

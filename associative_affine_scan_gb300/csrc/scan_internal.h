@@ -4,6 +4,7 @@
 // agree on these layouts; nothing here is part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,17 +16,38 @@ enum Mode { MODE_FWD = 0, MODE_BWD = 1 };
 // plain stationary kernel keeps its register budget.
 enum Variant { VAR_STATIONARY = 1, VAR_LOOKBACK = 2, VAR_STREAM = 3, VAR_SEGMENTED = 4 };
 
-// Stream variant: each warp runs a ring of shared-memory stages, one chunk of
-// its row per stage, filled by bulk async copies; smaller chunks get more
-// stages so that a warp keeps about the same bytes in flight. A backward
-// stage also holds 8 steps on each side of the chunk (the shifted operands).
-__host__ __device__ constexpr int stream_stages(int J) { return J >= 4 ? 3 : (J == 2 ? 4 : 8); }
-__host__ __device__ constexpr int stream_pad(int mode) { return mode == MODE_BWD ? 8 : 0; }
-__host__ __device__ constexpr size_t stream_stage_bytes(int mode, int J, int elt_a) {
-  return mode == MODE_FWD ? (size_t)(128 * J) * 2 * (size_t)elt_a
-                          : (size_t)(128 * J + 2 * stream_pad(mode)) * ((size_t)elt_a + 8);
-}
 __host__ __device__ constexpr size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Stream variant: each warp walks whole rows through a ring of shared-memory
+// stages, one chunk per stage, each input tile brought in by one 2-D tensor
+// copy (TMA) with the 128-byte swizzle; outputs of interior chunks leave
+// through swizzled tiles and tensor stores. A tensor is viewed as a flat
+// [n / E, E] array of 128-byte rows (E = 128 / element size), so every tile
+// starts on a 128-byte row: a chunk's first step is aligned to E elements of
+// the flat tensor. Tiles are padded to 1024 bytes, the span of the swizzle.
+constexpr int kMaxStages = 16;
+__host__ __device__ constexpr int tma_row_elems(int elt) { return 128 / elt; }
+__host__ __device__ constexpr size_t tma_tile_bytes(int J, int elt) {
+  return (size_t)((128 * J * elt + 1023) / 1024 * 1024);
+}
+// input tiles of one stage: forward a, x; backward a, h, dh
+__host__ __device__ constexpr size_t tma_stage_bytes(int mode, int J, int elt_a) {
+  return mode == MODE_FWD ? 2 * tma_tile_bytes(J, elt_a)
+                          : tma_tile_bytes(J, elt_a) + 2 * tma_tile_bytes(J, 4);
+}
+// output tiles of one buffer: forward h; backward dx, da
+__host__ __device__ constexpr size_t tma_out_bytes(int mode, int J, int elt_a) {
+  return mode == MODE_FWD ? tma_tile_bytes(J, 4) : 2 * tma_tile_bytes(J, elt_a);
+}
+// Dynamic shared memory of a stream block: packed offsets, mbarriers, 1 KB of
+// alignment slack, then per warp ns stages and (with output tiles) two
+// output buffers.
+__host__ __device__ constexpr size_t tma_bar_bytes(int R) { return (size_t)R * kMaxStages * 8; }
+__host__ __device__ constexpr size_t tma_warp_bytes(int mode, int J, int elt_a, int ns,
+                                                    bool out_tiles) {
+  return (size_t)ns * tma_stage_bytes(mode, J, elt_a) +
+         (out_tiles ? 2 * tma_out_bytes(mode, J, elt_a) : 0);
+}
 
 // Workspace header, at offset 0 of every workspace. The look-back kernels take
 // a tile ticket from `ticket_epoch` (low 32 bits) and read the launch epoch
@@ -68,6 +90,10 @@ struct ScalarParams {
   int64_t ntiles;     // look-back: M * G * nbr; segmented stationary: nseg * G * nbr
   int nseg;           // stationary: segments per row (1 = one block walks the whole row)
   int cps;            // stationary: chunks per segment
+  int ns;             // stream: stages per warp
+  int rpw;            // stream: rows (branch-major) per warp
+  int tma_out;        // stream: interior chunks leave through tiles and tensor stores
+  int64_t tile_hi;    // stream: flat elements [0, tile_hi) of every input are reachable by tiles
   unsigned long long* recs;  // look-back records: [nbr][rows][M] x 16 bytes
   WsHeader* hdr;
   unsigned long long wait_limit_ns;
@@ -83,9 +109,22 @@ struct ScalarPlan {
   int nseg;     // stationary: segments per row
   int cps;      // stationary: chunks per segment
   bool vec;     // vectorised loads/stores
+  int ns;       // stream: stages per warp
+  bool tma_out; // stream: outputs through tiles and tensor stores
   size_t ws_bytes;
   size_t smem;
 };
+
+// Stream variant: the tensor maps of a launch, per branch (kernel parameter).
+struct TmaMaps {
+  CUtensorMap in[2][3];   // forward: a, x; backward: a, h, dh
+  CUtensorMap out[2][2];  // forward: h; backward: dx, da
+};
+
+// Encodes the flat [n / E, E] view of a tensor of n elements of elt bytes, with
+// tiles of 128 J elements and the 128-byte swizzle. False if the driver entry
+// point is missing or refuses the map.
+bool encode_tile_map(CUtensorMap* m, const void* ptr, int elt, int64_t n, int J);
 
 // Launchers (one translation unit per mode/dtype family).
 cudaError_t launch_scalar_fwd_f32(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);

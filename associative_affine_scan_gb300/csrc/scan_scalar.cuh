@@ -37,6 +37,9 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <cstring>
+#include <type_traits>
+
 #include "scan_internal.h"
 
 namespace scan {
@@ -119,47 +122,52 @@ struct IO<__nv_bfloat16> {
   }
 };
 
-// Reads of a shared-memory stage; i is the step index relative to the stage.
+// 128-byte swizzle of a tile written by a 2-D tensor copy: the 16-byte unit
+// index inside each 128-byte row is XORed with the row index mod 8 (tiles
+// start on 1024-byte boundaries, the span of the pattern).
+__device__ __forceinline__ uint32_t swz128(uint32_t b) { return b ^ ((b >> 3) & 0x70u); }
+
+// Four consecutive elements at element offset o (a multiple of 4) of a
+// swizzled tile.
 template <typename TA>
-struct SIO;
+struct TIO;
 
 template <>
-struct SIO<float> {
-  static __device__ __forceinline__ void ld4(const unsigned char* base, int64_t i, float v[4]) {
-    const float4 q = *reinterpret_cast<const float4*>(base + i * 4);
+struct TIO<float> {
+  static __device__ __forceinline__ void ld4(const unsigned char* tile, uint32_t o, float v[4]) {
+    const float4 q = *reinterpret_cast<const float4*>(tile + swz128(o * 4u));
     v[0] = q.x;
     v[1] = q.y;
     v[2] = q.z;
     v[3] = q.w;
   }
-  static __device__ __forceinline__ float ld1(const unsigned char* base, int64_t i) {
-    return *reinterpret_cast<const float*>(base + i * 4);
+  static __device__ __forceinline__ void st4(unsigned char* tile, uint32_t o, const float v[4]) {
+    *reinterpret_cast<float4*>(tile + swz128(o * 4u)) = make_float4(v[0], v[1], v[2], v[3]);
   }
 };
 
 template <>
-struct SIO<__nv_bfloat16> {
-  static __device__ __forceinline__ void ld4(const unsigned char* base, int64_t i, float v[4]) {
-    const uint2 q = *reinterpret_cast<const uint2*>(base + i * 2);
+struct TIO<__nv_bfloat16> {
+  static __device__ __forceinline__ void ld4(const unsigned char* tile, uint32_t o, float v[4]) {
+    const uint2 q = *reinterpret_cast<const uint2*>(tile + swz128(o * 2u));
     v[0] = __uint_as_float(q.x << 16);
     v[1] = __uint_as_float(q.x & 0xffff0000u);
     v[2] = __uint_as_float(q.y << 16);
     v[3] = __uint_as_float(q.y & 0xffff0000u);
   }
-  static __device__ __forceinline__ float ld1(const unsigned char* base, int64_t i) {
-    const unsigned short u = *reinterpret_cast<const unsigned short*>(base + i * 2);
-    return __uint_as_float(((unsigned)u) << 16);
+  static __device__ __forceinline__ void st4(unsigned char* tile, uint32_t o, const float v[4]) {
+    *reinterpret_cast<uint2*>(tile + swz128(o * 2u)) =
+        make_uint2(IO<__nv_bfloat16>::pack2(v[0], v[1]), IO<__nv_bfloat16>::pack2(v[2], v[3]));
   }
 };
 
-// One chunk's inputs as copied into a shared-memory stage: row-relative step
-// e0 sits at offset 0 of each tensor; steps [c_lo, c_hi) were copied.
+// One chunk's tiles in shared memory (stream variant).
 struct StageView {
-  const unsigned char* a;
-  const unsigned char* x;
-  const unsigned char* h;
-  const unsigned char* dh;
-  int64_t e0, c_lo, c_hi;
+  const unsigned char* in[3];  // swizzled input tiles: a, then x (forward) or h, dh (backward)
+  unsigned char* out[2];       // swizzled output tiles: h (forward) or dx, da (backward);
+                               // null: outputs go straight to global memory
+  int64_t e0;                  // row-relative step at tile offset 0
+  int64_t c_hi;                // the tiles hold steps [e0, c_hi)
 };
 
 // ---------------------------------------------------------------------------
@@ -448,6 +456,262 @@ __device__ float lookback(const ScalarParams& p, const unsigned long long* recs_
 }
 
 // ---------------------------------------------------------------------------
+// chunk carry-in: register carry or decoupled look-back
+// ---------------------------------------------------------------------------
+
+// The carry entering chunk k of a row, given the chunk's own map blk.
+// Stationary: the running carry, advanced past the chunk. Look-back: the
+// chunk publishes its summary (or, for the first chunk or a constant map, its
+// inclusive state) before it looks back, then its inclusive state.
+template <class Op>
+__device__ __forceinline__ float chunk_carry_in(const ScalarParams& p, int brn, int64_t row, int k,
+                                                bool stationary, uint32_t epoch, unsigned ticket,
+                                                const typename Op::E& blk, float& carry) {
+  const int lane = threadIdx.x & 31;
+  float c;
+  if (stationary) {
+    c = carry;
+    carry = Op::carry_after(blk, c);
+    return c;
+  }
+  unsigned long long* recs_row = p.recs + ((int64_t)brn * p.rows + row) * (int64_t)p.M * 2;
+  unsigned long long* rec = recs_row + 2 * (int64_t)k;
+  const uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
+  if (k == 0) {
+    c = Op::initial_carry();
+    if (lane == 0) st_relaxed(rec + 1, pack_rec(tag_inc, Op::carry_after(blk, c)));
+    return c;
+  }
+  const bool cst = Op::is_const(blk);
+  if (lane == 0) {
+    if (cst) {
+      st_relaxed(rec + 1, pack_rec(tag_inc, Op::const_carry(blk)));
+    } else {
+      float u, w;
+      Op::to_agg(blk, u, w);
+      st_relaxed(rec, pack_rec(tag_agg, u));
+      st_relaxed(rec + 1, pack_rec(tag_agg, w));
+    }
+  }
+  c = lookback<Op>(p, recs_row, k, epoch, lane, ticket, brn, row);
+  if (!cst && lane == 0) st_relaxed(rec + 1, pack_rec(tag_inc, Op::carry_after(blk, c)));
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// one chunk, interleaved layout (dense fp32 rows)
+// ---------------------------------------------------------------------------
+
+// value at memory position (group start + 4): the next lane's first element,
+// the next block's lane 0, or the halo after the chunk
+template <int J>
+__device__ __forceinline__ float next_in_memory(const float (&V)[J][4], int j, float halo, int lane) {
+  const float v = __shfl_down_sync(kFull, V[j][0], 1);
+  const float vb = (j + 1 < J) ? __shfl_sync(kFull, V[j + 1 < J ? j + 1 : j][0], 0) : halo;
+  return lane == 31 ? vb : v;
+}
+
+// value at memory position (group start - 1)
+template <int J>
+__device__ __forceinline__ float prev_in_memory(const float (&V)[J][4], int j, float halo, int lane) {
+  const float v = __shfl_up_sync(kFull, V[j][3], 1);
+  const float vb = (j > 0) ? __shfl_sync(kFull, V[j > 0 ? j - 1 : 0][3], 31) : halo;
+  return lane == 0 ? vb : v;
+}
+
+// Lane l holds the 4-step groups at t0 + 128 j + 4 l (j < J): every warp
+// load and store is one fully coalesced 512-byte access, at the price of a
+// warp scan per 128-step block (the scan order runs across the lanes, then
+// across the blocks). Chosen where memory-pipe wavefronts, not arithmetic,
+// bound the kernel: dense fp32 rows of the linear form.
+template <class Op, int MODE, bool VEC, int J, typename TA, int S>
+__device__ __forceinline__ void chunk_groups(const ScalarParams& p, int brn, int64_t row, int k,
+                                             bool stationary, uint32_t epoch, unsigned ticket,
+                                             float& carry) {
+  using E = typename Op::E;
+  constexpr int L = 128 * J;
+  constexpr bool BWD = MODE == MODE_BWD;
+  const BranchArgs& br = p.br[brn];
+  const int lane = threadIdx.x & 31;
+  if (row >= p.rows) return;  // the whole warp leaves together
+  const int64_t T = p.T;
+  const int m = (S > 0) ? k : (p.M - 1 - k);
+  const int shift = VEC ? (int)((row * T) & 3) : 0;
+  const int64_t t0 = (int64_t)m * L - shift;
+  const int64_t roff = row * T;
+  const int64_t tl = t0 + 4 * lane;
+
+  float A[J][4], X[J][4], H[J][4];  // H: backward only
+  const TA* a = static_cast<const TA*>(br.a) + roff;
+  const TA* x = BWD ? nullptr : static_cast<const TA*>(br.x) + roff;
+  const float* h = br.h + roff;
+  const float* dh = br.dh + roff;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int64_t t = tl + 128 * j;
+    if (VEC && t >= 0 && t + 4 <= T) {
+      IO<TA>::ld4(a + t, A[j]);
+      if (BWD) {
+        IO<float>::ld4(h + t, H[j]);
+        IO<float>::ld4(dh + t, X[j]);
+      } else {
+        IO<TA>::ld4(x + t, X[j]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t tt = t + e;
+        const bool v = tt >= 0 && tt < T;
+        A[j][e] = v ? IO<TA>::ld1(a + tt) : 0.f;
+        if (BWD) {
+          H[j][e] = v ? IO<float>::ld1(h + tt) : 0.f;
+          X[j][e] = v ? IO<float>::ld1(dh + tt) : 0.f;
+        } else {
+          X[j][e] = v ? IO<TA>::ld1(x + tt) : 0.f;
+        }
+      }
+    }
+  }
+  // backward halos: the gate one step after (S = -1) or before (S = +1) the
+  // chunk, the state one step before (S = -1) or after (S = +1)
+  float halo_a = 0.f, halo_h = 0.f;
+  if (BWD) {
+    if (lane == 0) {
+      const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
+      const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
+      if (pa >= 0 && pa < T) halo_a = IO<TA>::ld1(a + pa);
+      if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(h + ph);
+    }
+    halo_a = __shfl_sync(kFull, halo_a, 0);
+    halo_h = __shfl_sync(kFull, halo_h, 0);
+  }
+
+  // ---- elements (dense rows: the recurrence starts at t = 0 or T - 1) ----
+  E el[J][4];
+  float HN[J];  // backward: cross-lane neighbour state of each group's edge step
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int64_t t = tl + 128 * j;
+    float gate[4] = {0.f, 0.f, 0.f, 0.f};
+    if (BWD) {
+      if (S < 0) {  // causal recurrence: gate a_{t+1}, state h_{t-1}
+        gate[0] = A[j][1];
+        gate[1] = A[j][2];
+        gate[2] = A[j][3];
+        gate[3] = next_in_memory<J>(A, j, halo_a, lane);
+        HN[j] = prev_in_memory<J>(H, j, halo_h, lane);
+      } else {  // reverse recurrence: gate a_{t-1}, state h_{t+1}
+        gate[0] = prev_in_memory<J>(A, j, halo_a, lane);
+        gate[1] = A[j][0];
+        gate[2] = A[j][1];
+        gate[3] = A[j][2];
+        HN[j] = next_in_memory<J>(H, j, halo_h, lane);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t tt = t + e;
+      E v = Op::identity();
+      if (tt >= 0 && tt < T) {
+        if (!BWD) {
+          v = ((S > 0) ? tt == 0 : tt == T - 1) ? Op::make_first(A[j][e], X[j][e], br.h0, row)
+                                                : Op::make(A[j][e], X[j][e]);
+        } else {
+          // the shifted gate is 0 past the end of the row (scan-first step)
+          v = Op::make(((S < 0) ? tt == T - 1 : tt == 0) ? 0.f : gate[e], X[j][e]);
+        }
+      }
+      el[j][e] = v;
+    }
+  }
+
+  // ---- chunk-local inclusive scan in scan order ----
+  E blk = Op::identity();
+#pragma unroll
+  for (int jj = 0; jj < J; ++jj) {
+    const int j = (S > 0) ? jj : (J - 1 - jj);
+    E lane_tot;
+    if (S > 0) {
+#pragma unroll
+      for (int e = 1; e < 4; ++e) el[j][e] = Op::compose(el[j][e - 1], el[j][e]);
+      lane_tot = el[j][3];
+    } else {
+#pragma unroll
+      for (int e = 2; e >= 0; --e) el[j][e] = Op::compose(el[j][e + 1], el[j][e]);
+      lane_tot = el[j][0];
+    }
+    E inc = lane_tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const E o = (S > 0) ? Op::shfl_up(inc, off) : Op::shfl_down(inc, off);
+      const bool has = (S > 0) ? (lane >= off) : (lane + off < 32);
+      if (has) inc = Op::compose(o, inc);
+    }
+    E ex = (S > 0) ? Op::shfl_up(inc, 1) : Op::shfl_down(inc, 1);
+    if (lane == ((S > 0) ? 0 : 31)) ex = Op::identity();
+    const E pre = Op::compose(blk, ex);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) el[j][e] = Op::compose(pre, el[j][e]);
+    blk = Op::compose(blk, Op::shfl(inc, (S > 0) ? 31 : 0));
+  }
+
+  const float c = chunk_carry_in<Op>(p, brn, row, k, stationary, epoch, ticket, blk, carry);
+
+  // ---- outputs ----
+  if (!BWD) {
+    float* hout = br.out_h + roff;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int64_t t = tl + 128 * j;
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = Op::value(el[j][e], c);
+      if (VEC && t >= 0 && t + 4 <= T) {
+        IO<float>::st4(hout + t, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (t + e >= 0 && t + e < T) IO<float>::st1(hout + t + e, v[e]);
+      }
+    }
+  } else {
+    TA* dx = static_cast<TA*>(br.dx) + roff;
+    TA* da = static_cast<TA*>(br.da) + roff;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int64_t t = tl + 128 * j;
+      float gx[4], ga[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t tt = t + e;
+        const float gv = Op::value(el[j][e], c);
+        float hn;
+        if (S < 0) hn = (e > 0) ? H[j][e > 0 ? e - 1 : 0] : HN[j];
+        else hn = (e < 3) ? H[j][e < 3 ? e + 1 : 3] : HN[j];
+        // the step that starts the forward recurrence reads h0 and feeds dh0
+        if ((S < 0) ? tt == 0 : tt == T - 1) {
+          hn = br.h0 ? br.h0[row] : 0.f;
+          if (br.dh0) br.dh0[row] = A[j][e] * gv;
+        }
+        gx[e] = gv;
+        ga[e] = gv * hn;
+      }
+      if (VEC && t >= 0 && t + 4 <= T) {
+        IO<TA>::st4(dx + t, gx);
+        IO<TA>::st4(da + t, ga);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (t + e >= 0 && t + e < T) {
+            IO<TA>::st1(dx + t + e, gx[e]);
+            IO<TA>::st1(da + t + e, ga[e]);
+          }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // one chunk of one row group
 // ---------------------------------------------------------------------------
 
@@ -460,28 +724,40 @@ __device__ float lookback(const ScalarParams& p, const unsigned long long* recs_
 //
 // S is the scan direction: +1 walks t upwards, -1 downwards. A forward call
 // scans in the recurrence's direction; a backward call scans against it.
-// SMEM: the chunk's inputs are read from a shared-memory stage (sv) where it
-// holds them, else from global memory. seg_hint (packed sequences): the
-// sequence that held this lane's run in the previous chunk, -1 if none;
-// updated for the next chunk.
-template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S, bool SMEM = false>
-__device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int k, bool stationary,
-                                      uint32_t epoch, unsigned ticket, const SegWin& win, float& carry,
-                                      const StageView* sv = nullptr, int* seg_hint = nullptr) {
+// SMEM: the chunk's inputs are read from the swizzled tiles of sv where they
+// hold them (else from global memory), and its outputs go to sv's output
+// tiles when it has them. seg_hint (packed sequences): the sequence that held
+// this lane's run in the previous chunk, -1 if none; updated for the next
+// chunk. release() is called by every lane once the chunk's inputs are in
+// registers (the stream variant refills the stage there).
+struct NoRelease {
+  __device__ __forceinline__ void operator()() const {}
+};
+
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S, bool SMEM = false,
+          class Release = NoRelease>
+__device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t row, int k,
+                                      bool stationary, uint32_t epoch, unsigned ticket,
+                                      const SegWin& win, float& carry,
+                                      const StageView* sv = nullptr, int* seg_hint = nullptr,
+                                      const Release& release = Release()) {
+  if constexpr (!VARLEN && !SMEM && std::is_same<Op, LinOp>::value && sizeof(TA) == 4) {
+    chunk_groups<Op, MODE, VEC, J, TA, S>(p, brn, row, k, stationary, epoch, ticket, carry);
+    return;
+  }
   using E = typename Op::E;
   constexpr int L = 128 * J;
   constexpr int V = 4 * J;
   constexpr bool BWD = MODE == MODE_BWD;
   const BranchArgs& br = p.br[brn];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)g * p.R + warp;
+  const int lane = threadIdx.x & 31;
   if (row >= p.rows) return;  // the whole warp leaves together
   const int64_t T = p.T;
   const int m = (S > 0) ? k : (p.M - 1 - k);
   // rows are cut so that every 4-step group starts on a 4-element boundary of
-  // memory (16 bytes fp32, 8 bytes bf16), or for staged bf16 on an 8-element
-  // (16-byte) boundary, whatever T is
-  constexpr int kAlign = (SMEM && sizeof(TA) == 2) ? 8 : 4;
+  // memory (16 bytes fp32, 8 bytes bf16), or for tensor-copied tiles on a
+  // 128-byte row of the flat tensor, whatever T is
+  constexpr int kAlign = SMEM ? tma_row_elems((int)sizeof(TA)) : 4;
   const int shift = VEC ? (int)((row * T) & (kAlign - 1)) : 0;
   const int64_t t0 = (int64_t)m * L - shift;
   const int64_t roff = row * T;
@@ -491,20 +767,20 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
   float A[V], X[V], H[BWD ? V : 1];
   const TA* a = static_cast<const TA*>(br.a) + roff;
   const void* xsrc = BWD ? static_cast<const void*>(br.dh) : br.x;
-  const unsigned char* sx = SMEM ? (BWD ? sv->dh : sv->x) : nullptr;
 #pragma unroll
   for (int i = 0; i < J; ++i) {
     const int64_t t = tr + 4 * i;
     float* ai = A + 4 * i;
     float* xi = X + 4 * i;
     float* hi = H + (BWD ? 4 * i : 0);
-    if (SMEM && t >= sv->c_lo && t + 4 <= sv->c_hi && t >= 0 && t + 4 <= T) {
-      SIO<TA>::ld4(sv->a, t - sv->e0, ai);
+    if (SMEM && t + 4 <= sv->c_hi) {
+      const uint32_t o = (uint32_t)(t - sv->e0);
+      TIO<TA>::ld4(sv->in[0], o, ai);
       if (BWD) {
-        SIO<float>::ld4(sx, t - sv->e0, xi);
-        SIO<float>::ld4(sv->h, t - sv->e0, hi);
+        TIO<float>::ld4(sv->in[1], o, hi);
+        TIO<float>::ld4(sv->in[2], o, xi);
       } else {
-        SIO<TA>::ld4(sx, t - sv->e0, xi);
+        TIO<TA>::ld4(sv->in[1], o, xi);
       }
     } else if (VEC && t >= 0 && t + 4 <= T) {
       IO<TA>::ld4(a + t, ai);
@@ -540,12 +816,8 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
     if (lane == 0) {
       const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
       const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
-      if (pa >= 0 && pa < T)
-        halo_a = (SMEM && pa >= sv->c_lo && pa < sv->c_hi) ? SIO<TA>::ld1(sv->a, pa - sv->e0)
-                                                             : IO<TA>::ld1(a + pa);
-      if (ph >= 0 && ph < T)
-        halo_h = (SMEM && ph >= sv->c_lo && ph < sv->c_hi) ? SIO<float>::ld1(sv->h, ph - sv->e0)
-                                                             : IO<float>::ld1(br.h + roff + ph);
+      if (pa >= 0 && pa < T) halo_a = IO<TA>::ld1(a + pa);
+      if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(br.h + roff + ph);
     }
     halo_a = __shfl_sync(kFull, halo_a, 0);
     halo_h = __shfl_sync(kFull, halo_h, 0);
@@ -561,6 +833,7 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
       h_nb = lane == 31 ? halo_h : hn;
     }
   }
+  release();
   // backward: the shifted gate of element e (before sequence cuts), and the
   // neighbouring state that multiplies dx into da
   auto gate_of = [&](int e) -> float {
@@ -644,34 +917,7 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
   if (lane == ((S > 0) ? 0 : 31)) ex = Op::identity();
   const E blk = Op::shfl(inc, (S > 0) ? 31 : 0);
 
-  // ---- carry-in ----
-  float c;
-  if (stationary) {
-    c = carry;
-    carry = Op::carry_after(blk, c);
-  } else {
-    unsigned long long* recs_row = p.recs + ((int64_t)brn * p.rows + row) * (int64_t)p.M * 2;
-    unsigned long long* rec = recs_row + 2 * (int64_t)k;
-    const uint32_t tag_agg = (epoch << 2) | 1u, tag_inc = (epoch << 2) | 2u;
-    if (k == 0) {
-      c = Op::initial_carry();
-      if (lane == 0) st_relaxed(rec + 1, pack_rec(tag_inc, Op::carry_after(blk, c)));
-    } else {
-      const bool cst = Op::is_const(blk);
-      if (lane == 0) {
-        if (cst) {
-          st_relaxed(rec + 1, pack_rec(tag_inc, Op::const_carry(blk)));
-        } else {
-          float u, w;
-          Op::to_agg(blk, u, w);
-          st_relaxed(rec, pack_rec(tag_agg, u));
-          st_relaxed(rec + 1, pack_rec(tag_agg, w));
-        }
-      }
-      c = lookback<Op>(p, recs_row, k, epoch, lane, ticket, brn, row);
-      if (!cst && lane == 0) st_relaxed(rec + 1, pack_rec(tag_inc, Op::carry_after(blk, c)));
-    }
-  }
+  const float c = chunk_carry_in<Op>(p, brn, row, k, stationary, epoch, ticket, blk, carry);
 
   // ---- pass 2: the recurrence over the run from its carry-in; X[e] becomes
   // the output (h_t forward, the adjoint g_t = dL/dx_t backward) ----
@@ -701,12 +947,15 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
   }
 
   // ---- stores ----
+  const bool staged_out = SMEM && sv->out[0] != nullptr;  // the whole chunk lies inside the row
   if (!BWD) {
     float* h = br.out_h + roff;
 #pragma unroll
     for (int i = 0; i < J; ++i) {
       const int64_t t = tr + 4 * i;
-      if (VEC && t >= 0 && t + 4 <= T) {
+      if (staged_out) {
+        TIO<float>::st4(sv->out[0], (uint32_t)(t - sv->e0), X + 4 * i);
+      } else if (VEC && t >= 0 && t + 4 <= T) {
         IO<float>::st4(h + t, X + 4 * i);
       } else {
 #pragma unroll
@@ -736,7 +985,10 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
         }
         ga[e] = X[idx] * hn;
       }
-      if (VEC && t >= 0 && t + 4 <= T) {
+      if (staged_out) {
+        TIO<TA>::st4(sv->out[0], (uint32_t)(t - sv->e0), X + 4 * i);
+        TIO<TA>::st4(sv->out[1], (uint32_t)(t - sv->e0), ga);
+      } else if (VEC && t >= 0 && t + 4 <= T) {
         IO<TA>::st4(dx + t, X + 4 * i);
         IO<TA>::st4(da + t, ga);
       } else {
@@ -749,10 +1001,12 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int g, int
       }
     }
   }
+  // this lane's tile writes become visible to the tensor store issued next
+  if (staged_out) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
-// bulk async copies into shared memory (TMA) and their mbarriers
+// tensor copies (TMA) between global and shared memory, and their mbarriers
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
@@ -779,15 +1033,34 @@ __device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned
       : "memory");
 }
 
-// 1-D bulk copy global -> shared; addresses 16-byte aligned, bytes % 16 == 0
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes,
-                                              unsigned long long* bar) {
+// Tile (x, y) of a 2-D tensor map into shared memory; completes on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            unsigned long long* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Shared-memory tile to tile (x, y) of a 2-D tensor map, in the current bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// All but the newest N bulk groups have finished reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// All bulk groups have completed their global writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity) {
   unsigned ok;
@@ -810,115 +1083,191 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned pari
   return true;
 }
 
-// One warp streams chunks [k0, k1) of its row through a ring of
-// stream_stages(J) shared-memory stages: lane 0 keeps that many
-// chunks in flight as bulk copies (one per tensor, the chunk's contiguous
-// run of the row), the warp scans chunk k from its stage while the next ones
-// arrive, with the carry in registers. Steps a stage does not hold (the last
-// few bytes of a tensor) are read from global memory by the chunk body.
-template <class Op, int MODE, bool VARLEN, int J, typename TA, int S>
-__device__ __forceinline__ void stream_chunks(const ScalarParams& p, int brn, int g, int k0, int k1,
-                              const SegWin& win, float& carry, unsigned char* region) {
+// The stream variant. Warp w of the grid takes rows [w rpw, (w + 1) rpw) of
+// the branch-major row list (branch b, row r -> b rows + r) and walks their
+// chunks in scan order as one sequence of items, with the carry in registers
+// (reset at each row). Lane 0 keeps ns items in flight: each stage of the
+// warp's ring receives one item's input tiles by 2-D tensor copies that
+// complete on the stage's mbarrier. The warp reads a stage into registers
+// and refills it at once with the item ns ahead, so the ring covers only
+// the copies' latency and the next rows' first chunks are already arriving
+// while a row ends. With out_tiles, a chunk that lies wholly inside its row
+// writes its outputs to one of two swizzled output buffers that lane 0 sends
+// out with tensor stores (one bulk group per item); other chunks store
+// straight from registers.
+template <class Op, int MODE, bool VARLEN, int J, typename TA>
+__device__ __forceinline__ void stream_rows(const ScalarParams& p, const TmaMaps& maps,
+                                            const SegWin& win, unsigned long long* bars,
+                                            unsigned char* region) {
   constexpr int L = 128 * J;
-  constexpr int PAD = stream_pad(MODE);
-  constexpr int LE = L + 2 * PAD;
-  constexpr int kAlign = sizeof(TA) == 2 ? 8 : 4;
-  constexpr int e_a = (int)sizeof(TA);
-  constexpr int e_1 = MODE == MODE_FWD ? (int)sizeof(TA) : 4;
-  constexpr int e_2 = 4;
-  constexpr size_t SB = stream_stage_bytes(MODE, J, (int)sizeof(TA));
-  constexpr int kStages = stream_stages(J);
-  constexpr size_t o_1 = (size_t)LE * e_a;
-  constexpr size_t o_2 = o_1 + (size_t)LE * e_1;
-  const BranchArgs& br = p.br[brn];
+  constexpr bool BWD = MODE == MODE_BWD;
+  constexpr int EA = (int)sizeof(TA);
+  constexpr int E = tma_row_elems(EA);  // flat alignment of a chunk's first step
+  constexpr int E1 = tma_row_elems(BWD ? 4 : EA);
+  constexpr int EO = tma_row_elems(BWD ? EA : 4);
+  constexpr uint32_t kTileA = (uint32_t)tma_tile_bytes(J, EA);
+  constexpr uint32_t kTile1 = (uint32_t)tma_tile_bytes(J, BWD ? 4 : EA);
+  constexpr uint32_t kStage = (uint32_t)tma_stage_bytes(MODE, J, EA);
+  constexpr uint32_t kOut0 = (uint32_t)tma_tile_bytes(J, BWD ? EA : 4);
+  constexpr uint32_t kOut = (uint32_t)tma_out_bytes(MODE, J, EA);
+  // bytes one item's copies deliver (whole boxes, zero-filled past the end)
+  constexpr uint32_t kTx = (uint32_t)L * (BWD ? (uint32_t)EA + 8u : 2u * (uint32_t)EA);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)g * p.R + warp;
-  if (row >= p.rows) return;
-  const int64_t T = p.T, roff = row * T, total = p.rows * T;
-  const int shift = (int)((row * T) & (kAlign - 1));
-  unsigned long long* bars = reinterpret_cast<unsigned long long*>(region) + warp * kStages;
-  unsigned char* stages = region + round_up((size_t)p.R * kStages * 8, 128) +
-                          (size_t)warp * kStages * SB;
-  const unsigned char* g_a = static_cast<const unsigned char*>(br.a);
-  const unsigned char* g_1 = MODE == MODE_FWD ? static_cast<const unsigned char*>(br.x)
-                                              : reinterpret_cast<const unsigned char*>(br.h);
-  const unsigned char* g_2 = reinterpret_cast<const unsigned char*>(br.dh);
-  // whole 16-byte blocks of every tensor end at this element (the coarsest
-  // granularity, 16 / smallest element size, is a multiple of the others)
-  const int64_t end_all = total - total % (16 / (e_a < e_1 ? e_a : e_1));
+  const int ns = p.ns;
+  const bool out_tiles = p.tma_out != 0;
+  bars += warp * kMaxStages;
+  unsigned char* stages = region + (size_t)warp * tma_warp_bytes(MODE, J, EA, ns, out_tiles);
+  unsigned char* outs = stages + (size_t)ns * kStage;
 
-  // row-relative steps held by the stage of chunk k
-  auto range = [&](int k, int64_t& e0, int64_t& lo, int64_t& hi) {
-    const int m = (S > 0) ? k : (p.M - 1 - k);
-    const int64_t t0 = (int64_t)m * L - shift;
-    e0 = t0 - PAD;
-    lo = e0 < -roff ? -roff : e0;
-    hi = t0 + L + PAD;
-    if (hi > end_all - roff) hi = end_all - roff;
+  const int64_t nq = (int64_t)p.nbr * p.rows;
+  const int64_t gw = (int64_t)blockIdx.x * p.R + warp;
+  const int64_t q0 = gw * p.rpw;
+  const int64_t q1 = q0 + p.rpw < nq ? q0 + p.rpw : nq;
+  if (q0 >= q1) return;
+  const int64_t T = p.T;
+  const int M = p.M;
+
+  // a position in the warp's item sequence, advanced one chunk at a time
+  struct Cursor {
+    int brn, S, k;
+    int64_t row, roff, t0;
   };
-  auto issue = [&](int k, int s) {  // lane 0
-    int64_t e0, lo, hi;
-    range(k, e0, lo, hi);
-    const unsigned n = hi > lo ? (unsigned)(hi - lo) : 0u;
-    const unsigned bytes = n * (unsigned)(e_a + e_1 + (MODE == MODE_BWD ? e_2 : 0));
-    mbar_expect_tx(&bars[s], bytes);
-    if (n) {
-      unsigned char* st = stages + (size_t)s * SB;
-      const int64_t off = lo - e0;
-      bulk_copy_g2s(st + off * e_a, g_a + (roff + lo) * e_a, n * e_a, &bars[s]);
-      bulk_copy_g2s(st + o_1 + off * e_1, g_1 + (roff + lo) * e_1, n * e_1, &bars[s]);
-      if (MODE == MODE_BWD)
-        bulk_copy_g2s(st + o_2 + off * e_2, g_2 + (roff + lo) * e_2, n * e_2, &bars[s]);
+  auto settle = [&](Cursor& c) {  // derived fields for (brn, row, k)
+    c.S = BWD ? -p.br[c.brn].dir : p.br[c.brn].dir;
+    c.roff = c.row * T;
+    const int m = c.S > 0 ? c.k : M - 1 - c.k;
+    c.t0 = (int64_t)m * L - (int64_t)(c.roff & (E - 1));
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.k == M) {
+      c.k = 0;
+      if (++c.row == p.rows) {
+        c.row = 0;
+        ++c.brn;
+      }
     }
+    settle(c);
+  };
+  Cursor cur;
+  cur.brn = (int)(q0 / p.rows);
+  cur.row = q0 % p.rows;
+  cur.k = 0;
+  settle(cur);
+  Cursor nxt = cur;  // next item to issue
+  int64_t left = (q1 - q0) * (int64_t)M;  // items not yet issued
+  const int64_t n = left;
+
+  auto issue = [&](int s) {  // lane 0: nxt into stage s
+    const int64_t f = nxt.roff + nxt.t0;  // flat first element, a multiple of E
+    unsigned char* st = stages + (size_t)s * kStage;
+    mbar_expect_tx(&bars[s], kTx);
+    tma_load_2d(st, &maps.in[nxt.brn][0], 0, (int)(f / E), &bars[s]);
+    tma_load_2d(st + kTileA, &maps.in[nxt.brn][1], 0, (int)(f / E1), &bars[s]);
+    if (BWD) tma_load_2d(st + kTileA + kTile1, &maps.in[nxt.brn][2], 0, (int)(f / 32), &bars[s]);
   };
 
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < ns; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
+  for (int s = 0; s < ns && left > 0; ++s) {
+    if (lane == 0) issue(s);
+    advance(nxt);
+    --left;
+  }
   __syncwarp();
-  const int n = k1 - k0;
+
+  float carry = 0.f;
   int hint = -1;
-  if (lane == 0)
-    for (int s = 0; s < kStages && s < n; ++s) issue(k0 + s, s);
-  for (int i = 0; i < n; ++i) {
-    const int s = i % kStages;
-    const bool ok = __all_sync(kFull, mbar_wait(&bars[s], (unsigned)((i / kStages) & 1),
-                                                p.wait_limit_ns));
+  int s = 0;
+  unsigned phase = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const bool ok = __all_sync(kFull, mbar_wait(&bars[s], phase, p.wait_limit_ns));
     if (!ok) {
       // a copy never landed: record it, give the copies still in flight a
-      // bounded chance to finish, and stop this row
+      // bounded chance to finish, and stop this warp
       if (lane == 0) {
         set_status(p.hdr, kStatusTimeout);
-        for (int j = i; j < n && j < i + kStages; ++j)
-          mbar_wait(&bars[j % kStages], (unsigned)((j / kStages) & 1), p.wait_limit_ns);
+        int s2 = s;
+        unsigned ph2 = phase;
+        for (int64_t j = i + 1; j < n && j < i + ns; ++j) {
+          if (++s2 == ns) {
+            s2 = 0;
+            ph2 ^= 1u;
+          }
+          mbar_wait(&bars[s2], ph2, p.wait_limit_ns);
+        }
       }
-      __syncwarp();
-      return;
+      break;
     }
+    if (cur.k == 0) {
+      carry = BWD ? 0.f : Op::initial_carry();
+      hint = -1;
+    }
+    const bool staged = out_tiles && cur.t0 >= 0 && cur.t0 + L <= T;
+    unsigned char* ob = outs + (size_t)(i & 1) * kOut;
     StageView sv;
-    sv.a = stages + (size_t)s * SB;
-    sv.x = sv.a + o_1;
-    sv.h = sv.a + o_1;
-    sv.dh = sv.a + o_2;
-    range(k0 + i, sv.e0, sv.c_lo, sv.c_hi);
-    chunk<Op, MODE, VARLEN, true, J, TA, S, true>(p, brn, g, k0 + i, true, 0u, 0u, win, carry, &sv,
-                                                  &hint);
-    __syncwarp();
-    if (i + kStages < n && lane == 0) {
-      fence_proxy_async_smem();  // this warp's reads of the stage precede the refill
-      issue(k0 + i + kStages, s);
+    const unsigned char* st = stages + (size_t)s * kStage;
+    sv.in[0] = st;
+    sv.in[1] = st + kTileA;
+    sv.in[2] = st + kTileA + kTile1;
+    sv.out[0] = staged ? ob : nullptr;
+    sv.out[1] = staged ? ob + kOut0 : nullptr;
+    sv.e0 = cur.t0;
+    sv.c_hi = p.tile_hi - cur.roff;
+    if (sv.c_hi > cur.t0 + L) sv.c_hi = cur.t0 + L;
+    if (staged) {
+      // the tensor store that last read this buffer (two items back) is done
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+    }
+    // refill this stage as soon as its tiles are in registers
+    const bool refill = left > 0;
+    auto release = [&] {
+      __syncwarp();
+      if (refill && lane == 0) {
+        fence_proxy_async_smem();  // the warp's reads of the stage precede the refill
+        issue(s);
+      }
+    };
+    if (cur.S > 0)
+      chunk<Op, MODE, VARLEN, true, J, TA, 1, true>(p, cur.brn, cur.row, cur.k, true, 0u, 0u, win,
+                                                    carry, &sv, &hint, release);
+    else
+      chunk<Op, MODE, VARLEN, true, J, TA, -1, true>(p, cur.brn, cur.row, cur.k, true, 0u, 0u, win,
+                                                     carry, &sv, &hint, release);
+    if (refill) {
+      advance(nxt);
+      --left;
+    }
+    if (out_tiles) {
+      __syncwarp();
+      if (lane == 0) {
+        if (staged) {
+          const int64_t f = cur.roff + cur.t0;
+          tma_store_2d(&maps.out[cur.brn][0], 0, (int)(f / EO), ob);
+          if (BWD) tma_store_2d(&maps.out[cur.brn][1], 0, (int)(f / E), ob + kOut0);
+        }
+        bulk_commit();  // one group per item, possibly empty
+      }
+    }
+    advance(cur);
+    if (++s == ns) {
+      s = 0;
+      phase ^= 1u;
     }
   }
+  if (out_tiles && lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
 
-template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
-__device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
-  extern __shared__ __align__(16) unsigned char smem[];
+// Packed offsets: staged once per block in shared memory when they fit.
+template <bool VARLEN>
+__device__ __forceinline__ SegWin stage_offsets(const ScalarParams& p, unsigned char* smem) {
   SegWin win;
   win.cu = p.cu;
   win.n = p.n_seqs;
@@ -928,9 +1277,14 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
     __syncthreads();
     win.cu = s_cu;
   }
+  return win;
+}
+
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
+__device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const SegWin win = stage_offsets<VARLEN>(p, smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  (void)warp;
-  (void)lane;
 
   if (VARIANT == VAR_LOOKBACK) {
     __shared__ unsigned s_ticket, s_epoch;
@@ -948,13 +1302,14 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
       const int rem = (int)(ticket % (unsigned)per_k);
       const int g = rem / p.nbr;
       const int brn = rem % p.nbr;
+      const int64_t row = (int64_t)g * p.R + warp;
       if (VARLEN && ticket == 0) check_segments<MODE>(p);
       float carry = 0.f;
       const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
       if (S > 0)
-        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, false, epoch, ticket, win, carry);
+        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, row, k, false, epoch, ticket, win, carry);
       else
-        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, false, epoch, ticket, win, carry);
+        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, row, k, false, epoch, ticket, win, carry);
     } else if (threadIdx.x == 0) {
       set_status(p.hdr, kStatusWorkspace);
     }
@@ -971,145 +1326,184 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
   } else if (VARIANT == VAR_STATIONARY) {
     const int g = blockIdx.x / p.nbr;
     const int brn = blockIdx.x % p.nbr;
+    const int64_t row = (int64_t)g * p.R + warp;
     if (VARLEN && blockIdx.x == 0) check_segments<MODE>(p);
     float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
     const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
     int hint = -1;
     for (int k = 0; k < p.M; ++k) {
       if (S > 0)
-        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr, &hint);
+        chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
+                                               &hint);
       else
-        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr, &hint);
+        chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
+                                                &hint);
     }
   } else {
-    // VAR_SEGMENTED and VAR_STREAM: stationary carry over [k0, k1). With
-    // nseg > 1 a row is cut into nseg segments of cps chunks, taken in ticket
-    // order (segment index major): a block waits once for the end state of
-    // its rows' previous segments (published G * nbr tickets earlier, so
-    // normally already there), walks its segment and publishes its end state.
+    // VAR_SEGMENTED: a row is cut into nseg segments of cps chunks, taken in
+    // ticket order (segment index major): a block waits once for the end
+    // state of its rows' previous segments (published G * nbr tickets
+    // earlier), walks its segment with the carry in registers and publishes
+    // its end state.
     __shared__ unsigned s_ticket, s_epoch;
-    const bool segmented = p.nseg > 1;
-    int g = 0, brn = 0, seg = 0;
-    unsigned ticket = 0;
-    uint32_t epoch = 0;
-    bool have = true;
-    if (segmented) {
-      if (threadIdx.x == 0) {
-        const unsigned long long te = atomicAdd(&p.hdr->ticket_epoch, 1ull);
-        s_ticket = (unsigned)te;
-        s_epoch = (unsigned)(te >> 32);
-      }
-      __syncthreads();
-      ticket = s_ticket;
-      epoch = s_epoch;
-      have = (int64_t)ticket < p.ntiles;
-      const int per_s = p.G * p.nbr;
-      seg = (int)(ticket / (unsigned)per_s);
-      const int rem = (int)(ticket % (unsigned)per_s);
-      g = rem / p.nbr;
-      brn = rem % p.nbr;
-    } else {
-      g = blockIdx.x / p.nbr;
-      brn = blockIdx.x % p.nbr;
+    if (threadIdx.x == 0) {
+      const unsigned long long te = atomicAdd(&p.hdr->ticket_epoch, 1ull);
+      s_ticket = (unsigned)te;
+      s_epoch = (unsigned)(te >> 32);
     }
-    if (have) {
-      if (VARLEN && (segmented ? ticket == 0 : blockIdx.x == 0)) check_segments<MODE>(p);
+    __syncthreads();
+    const unsigned ticket = s_ticket;
+    const uint32_t epoch = s_epoch;
+    if ((int64_t)ticket < p.ntiles) {
+      const int per_s = p.G * p.nbr;
+      const int seg = (int)(ticket / (unsigned)per_s);
+      const int rem = (int)(ticket % (unsigned)per_s);
+      const int g = rem / p.nbr;
+      const int brn = rem % p.nbr;
+      if (VARLEN && ticket == 0) check_segments<MODE>(p);
       const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
       const int64_t row = (int64_t)g * p.R + warp;
       const bool active = row < p.rows;
       unsigned long long* recs_row = p.recs + ((int64_t)brn * p.rows + row) * (int64_t)p.nseg * 2;
       float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
-      if (segmented && seg > 0 && active)
-        carry = lookback<Op>(p, recs_row, seg, epoch, lane, ticket, brn, row);
+      if (seg > 0 && active) carry = lookback<Op>(p, recs_row, seg, epoch, lane, ticket, brn, row);
       const int k0 = seg * p.cps;
       const int k1 = k0 + p.cps < p.M ? k0 + p.cps : p.M;
-      if (VARIANT == VAR_STREAM) {
-        const size_t cu_bytes = VARLEN ? 4 * (size_t)(p.n_seqs + 1 <= kCuSmem ? p.n_seqs + 1 : 0) : 0;
-        unsigned char* region = smem + round_up(cu_bytes, 128);
+      int hint = -1;
+      for (int k = k0; k < k1; ++k) {
         if (S > 0)
-          stream_chunks<Op, MODE, VARLEN, J, TA, 1>(p, brn, g, k0, k1, win, carry, region);
+          chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
+                                                 &hint);
         else
-          stream_chunks<Op, MODE, VARLEN, J, TA, -1>(p, brn, g, k0, k1, win, carry, region);
-      } else {
-        int hint = -1;
-        for (int k = k0; k < k1; ++k) {
-          if (S > 0)
-            chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr,
-                                                   &hint);
-          else
-            chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, g, k, true, 0u, 0u, win, carry, nullptr,
-                                                    &hint);
-        }
+          chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
+                                                  &hint);
       }
-      if (segmented && active && lane == 0)
+      if (active && lane == 0)
         st_relaxed(recs_row + 2 * (int64_t)seg + 1, pack_rec((epoch << 2) | 2u, carry));
     } else if (threadIdx.x == 0) {
       set_status(p.hdr, kStatusWorkspace);
     }
-    if (segmented) {
-      __syncthreads();
-      if (threadIdx.x == 0) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned d = atomicAdd(&p.hdr->done, 1u);
+      if (d == gridDim.x - 1) {
+        p.hdr->done = 0u;
+        atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
         __threadfence();
-        const unsigned d = atomicAdd(&p.hdr->done, 1u);
-        if (d == gridDim.x - 1) {
-          p.hdr->done = 0u;
-          atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
-          __threadfence();
-        }
       }
     }
   }
 }
 
 // The register-carry kernels keep ptxas's default register budget for 256-
-// thread blocks; the stream kernel, whose occupancy shared memory bounds
-// anyway, may use the full register file so it does not spill.
+// thread blocks.
 template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
 __global__ void __launch_bounds__(256) scalar_scan_kernel(const __grid_constant__ ScalarParams p) {
   scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
 }
 
-template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
+// The stream kernel: persistent warps, occupancy bounded by shared memory.
+template <class Op, int MODE, bool VARLEN, int J, typename TA>
 __global__ void __launch_bounds__(256, 1)
-    scalar_stream_kernel(const __grid_constant__ ScalarParams p) {
-  scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
+    scalar_stream_kernel(const __grid_constant__ ScalarParams p, const __grid_constant__ TmaMaps maps) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const SegWin win = stage_offsets<VARLEN>(p, smem);
+  if (VARLEN && blockIdx.x == 0) check_segments<MODE>(p);
+  const size_t cu_bytes = VARLEN ? 4 * (size_t)(p.n_seqs + 1 <= kCuSmem ? p.n_seqs + 1 : 0) : 0;
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + round_up(cu_bytes, 128));
+  const uint32_t base = smem_u32(smem);
+  const size_t after = round_up(cu_bytes, 128) + tma_bar_bytes(p.R);
+  const size_t pad = (size_t)((1024u - ((base + (uint32_t)after) & 1023u)) & 1023u);
+  stream_rows<Op, MODE, VARLEN, J, TA>(p, maps, win, bars, smem + after + pad);
 }
 
 // Host-side dispatch over the compile-time choices.
 template <class Op, int MODE, typename TA, int VARIANT, bool VARLEN, bool VEC, int J>
 cudaError_t launch_one(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
-  auto kern = [] {
-    if constexpr (VARIANT == VAR_STREAM)
-      return scalar_stream_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
-    else
-      return scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
-  }();
+  auto kern = scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
   if (pl.smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pl.smem);
     if (e != cudaSuccess) return e;
   }
-  const bool ticketed = VARIANT == VAR_LOOKBACK || p.nseg > 1;
+  const bool ticketed = VARIANT == VAR_LOOKBACK || VARIANT == VAR_SEGMENTED;
   const int64_t grid = ticketed ? p.ntiles : (int64_t)p.G * p.nbr;
   if (grid <= 0) return cudaSuccess;
   kern<<<(unsigned)grid, 32 * p.R, pl.smem, s>>>(p);
   return cudaGetLastError();
 }
 
+// Stream variant: tensor maps for every input and output of each branch, and
+// a persistent grid sized by occupancy, rows dealt out evenly to its warps.
+template <class Op, int MODE, typename TA, bool VARLEN, int J>
+cudaError_t launch_stream(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
+  constexpr int EA = (int)sizeof(TA);
+  auto kern = scalar_stream_kernel<Op, MODE, VARLEN, J, TA>;
+  const int64_t n = p.rows * p.T;
+  TmaMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  bool ok = true;
+  for (int b = 0; b < p.nbr; ++b) {
+    const BranchArgs& br = p.br[b];
+    ok = ok && encode_tile_map(&maps.in[b][0], br.a, EA, n, J);
+    if (MODE == MODE_FWD) {
+      ok = ok && encode_tile_map(&maps.in[b][1], br.x, EA, n, J) &&
+           encode_tile_map(&maps.out[b][0], br.out_h, 4, n, J);
+    } else {
+      ok = ok && encode_tile_map(&maps.in[b][1], br.h, 4, n, J) &&
+           encode_tile_map(&maps.in[b][2], br.dh, 4, n, J) &&
+           encode_tile_map(&maps.out[b][0], br.dx, EA, n, J) &&
+           encode_tile_map(&maps.out[b][1], br.da, EA, n, J);
+    }
+  }
+  if (!ok) return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * p.R, pl.smem)) !=
+      cudaSuccess)
+    return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  ScalarParams q = p;
+  const int64_t nq = (int64_t)p.nbr * p.rows;
+  const int64_t warps = (int64_t)per_sm * p.R * sms;
+  q.rpw = (int)((nq + warps - 1) / warps);
+  const int64_t used = (nq + q.rpw - 1) / q.rpw;
+  const int64_t grid = (used + p.R - 1) / p.R;
+  constexpr int E = tma_row_elems(EA);
+  q.tile_hi = n / E * E;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, 32 * p.R, pl.smem, s>>>(q, maps);
+  return cudaGetLastError();
+}
+
 template <class Op, int MODE, typename TA, int VARIANT, bool VARLEN, bool VEC>
 cudaError_t launch_pick_j(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
-  switch (pl.J) {
-    case 1: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 1>(p, pl, s);
-    case 2: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 2>(p, pl, s);
-    case 4: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 4>(p, pl, s);
-    default: return cudaErrorInvalidValue;
+  if constexpr (VARIANT == VAR_STREAM) {
+    switch (pl.J) {
+      case 1: return launch_stream<Op, MODE, TA, VARLEN, 1>(p, pl, s);
+      case 2: return launch_stream<Op, MODE, TA, VARLEN, 2>(p, pl, s);
+      case 4: return launch_stream<Op, MODE, TA, VARLEN, 4>(p, pl, s);
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    switch (pl.J) {
+      case 1: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 1>(p, pl, s);
+      case 2: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 2>(p, pl, s);
+      case 4: return launch_one<Op, MODE, TA, VARIANT, VARLEN, VEC, 4>(p, pl, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
 }
 
 template <class Op, int MODE, typename TA, int VARIANT>
 cudaError_t launch_layouts(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
   const bool varlen = p.cu != nullptr;
-  if constexpr (VARIANT == VAR_STREAM) {  // bulk copies need the vectorised layout
+  if constexpr (VARIANT == VAR_STREAM) {  // tensor copies need the vectorised layout
     if (!pl.vec) return cudaErrorInvalidValue;
     return varlen ? launch_pick_j<Op, MODE, TA, VARIANT, true, true>(p, pl, s)
                   : launch_pick_j<Op, MODE, TA, VARIANT, false, true>(p, pl, s);

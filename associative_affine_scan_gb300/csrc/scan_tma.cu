@@ -1,0 +1,50 @@
+// scan_tma.cu -- host side of the stream variant: tensor maps for 2-D tensor
+// copies (TMA) of the flat [n / E, E] view of a scan tensor.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "scan_internal.h"
+
+namespace scan {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// The encoder lives in the driver; the runtime hands out its entry point, so
+// the library needs no link-time dependency on libcuda.
+void load_encoder() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && fn)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+}  // namespace
+
+bool encode_tile_map(CUtensorMap* m, const void* ptr, int elt, int64_t n, int J) {
+  std::call_once(g_encode_once, load_encoder);
+  if (!g_encode || !ptr || (elt != 2 && elt != 4) || (J != 1 && J != 2 && J != 4)) return false;
+  if (reinterpret_cast<uintptr_t>(ptr) % 16) return false;
+  const int E = tma_row_elems(elt);
+  const int64_t rows = n / E;
+  if (rows < 1 || rows > (1LL << 32)) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {(cuuint32_t)E, (cuuint32_t)(128 * J / E)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      elt == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace scan

@@ -93,11 +93,13 @@ typedef enum scan_dtype {
  * segments, each block waiting once for the end state of the previous
  * segment. LOOKBACK: T is cut into chunks handled by independent blocks; each
  * block publishes its chunk summary (P, Q) ([RGA] Exact real chunk algebra)
- * and reads its predecessors' summaries (decoupled look-back). STREAM: the
- * stationary scheme with each warp's chunks streamed into a ring of shared-
- * memory stages by bulk asynchronous copies (TMA), several chunks in flight
- * per warp; needs 16-byte aligned tensors (else it runs as STATIONARY). AUTO
- * picks per shape. */
+ * and reads its predecessors' summaries (decoupled look-back). STREAM: a
+ * persistent grid sized by occupancy; each warp walks a contiguous share of
+ * whole rows with the running state in registers, its chunks arriving in a
+ * ring of shared-memory stages by 2-D tensor copies (TMA) several chunks
+ * ahead, and leaving through tensor stores; needs every tensor 16-byte
+ * aligned and at least 64 elements (else it runs as STATIONARY). AUTO picks
+ * per shape. */
 typedef enum scan_variant {
   SCAN_VARIANT_AUTO = 0,
   SCAN_VARIANT_STATIONARY = 1,
@@ -126,6 +128,7 @@ typedef struct scan_opts {
   double wait_limit_s;   /* bound on every look-back wait; <= 0 means 1.0 second */
   const int32_t* cu_seqlens_host; /* optional host copy of cu_seqlens, validated before launch */
   int32_t segments;      /* stationary: segments each row is cut into (>= 1); 0 = planner */
+  int32_t stages;        /* stream: chunks in flight per warp, 2..16; 0 = planner */
 } scan_opts;
 
 /* Human-readable name of a status code (static string, never NULL). */

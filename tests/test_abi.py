@@ -85,6 +85,14 @@ def test_workspace_sizes():
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 100}) == 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 1024}) == 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"variant": 4}) == 0
+    # the stream variant walks whole rows per warp: the header is all it needs
+    stream = {"variant": scan.SCAN_VARIANT_STREAM}
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_BIDIR_FWD, 1, 2048, 275479, opts=stream) == 256
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 2048, 100000,
+                                     opts=dict(stream, segments=4)) == 256
+    for bad in (1, 17, -2):
+        assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4,
+                                         opts=dict(stream, stages=bad)) == 0
 
 
 def _raw(name):

@@ -42,8 +42,8 @@ def variants(scan):
     return [("lookback", {"variant": scan.SCAN_VARIANT_LOOKBACK}),
             ("stationary", {"variant": scan.SCAN_VARIANT_STATIONARY, "segments": 1}),
             ("segmented", {"variant": scan.SCAN_VARIANT_STATIONARY, "segments": 3}),
-            ("stream", {"variant": scan.SCAN_VARIANT_STREAM, "segments": 1}),
-            ("stream_segmented", {"variant": scan.SCAN_VARIANT_STREAM, "segments": 2})]
+            ("stream", {"variant": scan.SCAN_VARIANT_STREAM}),
+            ("stream_two_stages", {"variant": scan.SCAN_VARIANT_STREAM, "stages": 2})]
 
 
 def check_fwd_bwd(scan, a, x, dh, h0=None, cu=None, reverse=False, opts=None, tol_h=TOL32,
@@ -369,8 +369,24 @@ def test_log_packed_with_resets(lib):
 # ---------------------------------------------------------------------------
 
 def test_full_dense_4k(lib):
+    """Every output of the 8 x 1536 x 4096 workload, with the planner's choice
+    and with each register-carry and stream scheme (the stream grid deals
+    several rows to each warp at this size)."""
     w = workloads.dense_4k(seed=0)
-    check_fwd_bwd(lib, w.a, w.x, w.dh, w.h0, None, False)
+    ref_h = oracle.scan_fwd(w.a, w.x, w.h0)
+    ref_da, ref_dx, ref_dh0 = oracle.scan_bwd(w.a, w.x, w.dh, w.h0)
+    ga, gx, gdh, gh0 = cuda(w.a, w.x, w.dh, w.h0)
+    for opts in (None, {"variant": lib.SCAN_VARIANT_STATIONARY},
+                 {"variant": lib.SCAN_VARIANT_STREAM},
+                 {"variant": lib.SCAN_VARIANT_STREAM, "chunk": 256}):
+        h = lib.scan_fwd(ga, gx, gh0, opts=opts)
+        da, dx, dh0 = lib.scan_bwd(ga, h, gdh, gh0, opts=opts)
+        torch.cuda.synchronize()
+        assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+        errs = (rel_err(h, ref_h), rel_err(da, ref_da), rel_err(dx, ref_dx),
+                rel_err(dh0, ref_dh0))
+        assert max(errs) <= TOL32, (opts, errs)
+        del h, da, dx, dh0
 
 
 def sample_rows(n_rows, k, seed):
@@ -399,12 +415,15 @@ def test_full_dense_64k_sampled_rows(lib):
         assert rel_err(dh0.view(-1)[r:r + 1], ref_dh0[0]) <= TOL32, r
 
 
-def test_full_packed_bidir_sampled_channels(lib):
+@pytest.mark.parametrize("variant", ["planner", "stream"])
+def test_full_packed_bidir_sampled_channels(lib, variant):
     w = workloads.packed_bidir(seed=0)
     g = cuda(w.af, w.xf, w.ar, w.xr, w.cu_seqlens, w.dhf, w.dhr)
     af, xf, ar, xr, cu, dhf, dhr = g
-    hf, hr = lib.scan_bidir_fwd(af, xf, ar, xr, None, None, cu)
-    daf, dxf, dh0f, dar, dxr, dh0r = lib.scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, None, None, cu)
+    opts = {"variant": lib.SCAN_VARIANT_STREAM} if variant == "stream" else None
+    hf, hr = lib.scan_bidir_fwd(af, xf, ar, xr, None, None, cu, opts=opts)
+    daf, dxf, dh0f, dar, dxr, dh0r = lib.scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, None, None, cu,
+                                                        opts=opts)
     torch.cuda.synchronize()
     assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
     for c in sample_rows(w.af.shape[0], 12, 2):

@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     SCAN_OP_BIDIR_FWD,
     SCAN_OP_BWD,
     SCAN_OP_FWD,
+    SCAN_OP_LOG_BWD,
     SCAN_OP_LOG_FWD,
     SCAN_VARIANT_AUTO,
     SCAN_VARIANT_LOOKBACK,
@@ -46,6 +47,7 @@ from ._binding import (  # noqa: F401
     scan_fwd_noalloc,
     scan_get_device_status,
     scan_log_fwd,
+    scan_log_bwd,
     scan_status_string,
     scan_version,
     scan_workspace_bytes,

@@ -44,11 +44,12 @@ SCAN_OP_BIDIR_BWD = 3
 SCAN_OP_LOG_FWD = 4
 SCAN_OP_AFFINE_FWD = 5
 SCAN_OP_AFFINE_BWD = 6
+SCAN_OP_LOG_BWD = 7
 
 EXPORTED = (
     "scan_status_string", "scan_version", "scan_workspace_bytes", "scan_workspace_init",
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
-    "scan_log_fwd", "affine_scan_fwd", "affine_scan_bwd", "scan_fwd_noalloc",
+    "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "scan_fwd_noalloc",
 )
 
 
@@ -96,6 +97,8 @@ _SIGS = {
                        ctypes.c_int),
     "scan_log_fwd": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, _i32, _opt, _vp, _sz,
                       _vp], ctypes.c_int),
+    "scan_log_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32,
+                      _opt, _vp, _sz, _vp], ctypes.c_int),
     "affine_scan_fwd": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _opt, _vp, _sz, _vp],
                         ctypes.c_int),
     "affine_scan_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _opt,
@@ -396,6 +399,36 @@ def scan_log_fwd(log_a, log_x, log_h0=None, cu_seqlens=None, reverse=False, *, o
                             B, C, T, int(bool(reverse)), _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "scan_log_fwd")
     return h
+
+
+def scan_log_bwd(log_a, log_x, h, dh, log_h0=None, cu_seqlens=None, reverse=False, *, out=None,
+                 opts=None, stream=None, need_dh0=True):
+    """Backward of L = sum dh * h for h = scan_log_fwd(log_a, log_x, log_h0, ...).
+
+    Returns (dlog_a, dlog_x, dlog_h0), all fp32."""
+    _need(log_a, "log_a", dtype=torch.float32)
+    dev = log_a.device
+    B, C, T, n = _scalar_dims(log_a, cu_seqlens)
+    for t, name in ((log_x, "log_x"), (h, "h"), (dh, "dh")):
+        _need(t, name, dtype=torch.float32, shape=log_a.shape, device=dev)
+    h0_shape = (n, C) if cu_seqlens is not None else (B, C)
+    _need(log_h0, "log_h0", dtype=torch.float32, shape=h0_shape, device=dev)
+    if out is not None:
+        dla, dlx, dlh0 = out
+    else:
+        dla = torch.empty_like(log_a)
+        dlx = torch.empty_like(log_a)
+        dlh0 = torch.empty(h0_shape, dtype=torch.float32, device=dev) if need_dh0 else None
+    _need(dla, "dlog_a", dtype=torch.float32, shape=log_a.shape, device=dev)
+    _need(dlx, "dlog_x", dtype=torch.float32, shape=log_a.shape, device=dev)
+    _need(dlh0, "dlog_h0", dtype=torch.float32, shape=h0_shape, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_LOG_BWD, B, C, T, 0, 0, opts, dev, s)
+    st = lib().scan_log_bwd(_ptr(log_a), _ptr(log_x), _ptr(h), _ptr(dh), _ptr(log_h0),
+                            _ptr(cu_seqlens), n, _ptr(dla), _ptr(dlx), _ptr(dlh0), B, C, T,
+                            int(bool(reverse)), _optref(o), _ptr(ws), ws.numel(), s)
+    _check(st, "scan_log_bwd")
+    return dla, dlx, dlh0
 
 
 def _affine_dims(A, Bm):

@@ -287,6 +287,7 @@ size_t scan_workspace_bytes(scan_op op, int64_t B, int64_t C, int64_t T, int32_t
     case SCAN_OP_FWD:
     case SCAN_OP_BWD:
     case SCAN_OP_LOG_FWD:
+    case SCAN_OP_LOG_BWD:
       return ws_scalar(B * C, T, 1, o);
     case SCAN_OP_BIDIR_FWD:
     case SCAN_OP_BIDIR_BWD:
@@ -480,6 +481,34 @@ scan_status scan_log_fwd(const float* log_a, const float* log_x, const float* lo
   p.br[0].out_h = h;
   p.br[0].dir = reverse ? -1 : 1;
   return from_cuda(launch_log_fwd(p, pl, stream));
+}
+
+scan_status scan_log_bwd(const float* log_a, const float* log_x, const float* h, const float* dh,
+                         const float* log_h0, const int32_t* cu, int32_t n_seqs, float* dlog_a,
+                         float* dlog_x, float* dlog_h0, int64_t B, int64_t C, int64_t T,
+                         int32_t reverse, const scan_opts* opts, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+  scan_opts o = defaults(opts);
+  if (o.variant == SCAN_VARIANT_STREAM) o.variant = SCAN_VARIANT_STATIONARY;
+  ScalarParams p;
+  ScalarPlan pl;
+  scan_status st = prepare(B, C, T, cu, n_seqs, 1, false, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  const int64_t n_h0 = cu ? (int64_t)n_seqs * C : B * C;
+  if (p.rows * T == 0) return zero_dh0(dlog_h0, n_h0, stream);
+  if (!log_a || !log_x || !h || !dh || !dlog_a || !dlog_x) return SCAN_ERR_INVALID_ARG;
+  pl.vec = aligned(log_a, 16) && aligned(log_x, 16) && aligned(h, 16) && aligned(dh, 16) &&
+           aligned(dlog_a, 16) && aligned(dlog_x, 16);
+  p.br[0].a = log_a;
+  p.br[0].x = log_x;
+  p.br[0].h = h;
+  p.br[0].dh = dh;
+  p.br[0].h0 = log_h0;
+  p.br[0].da = dlog_a;
+  p.br[0].dx = dlog_x;
+  p.br[0].dh0 = dlog_h0;
+  p.br[0].dir = reverse ? -1 : 1;
+  return from_cuda(launch_log_bwd(p, pl, stream));
 }
 
 }  // extern "C"

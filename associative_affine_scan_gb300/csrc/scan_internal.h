@@ -10,7 +10,9 @@
 
 namespace scan {
 
-enum Mode { MODE_FWD = 0, MODE_BWD = 1 };
+// MODE_LOGBWD: the backward of the log-space form, run as the linear adjoint
+// on a = exp(log a) with the log-space chain rule applied to its outputs.
+enum Mode { MODE_FWD = 0, MODE_BWD = 1, MODE_LOGBWD = 2 };
 // Carry schemes. The first three are public (scan_variant); SEGMENTED is the
 // stationary scheme with rows cut into segments, compiled separately so the
 // plain stationary kernel keeps its register budget.
@@ -66,10 +68,11 @@ constexpr size_t kWsHeaderBytes = 256;  // records start here
 // One branch of a scalar scan launch.
 struct BranchArgs {
   const void* a;     // gate a (dtype dt); forward and backward
-  const void* x;     // forward: x (dtype dt)
+  const void* x;     // forward: x (dtype dt); log-space backward: log x
   const float* h;    // backward: forward output h
   const float* dh;   // backward: upstream gradient
-  const float* h0;   // nullable initial state ([B,C] dense, [n_seqs,C] packed)
+  const float* h0;   // nullable initial state ([B,C] dense, [n_seqs,C] packed); log h0 in
+                     // the log-space backward
   float* out_h;      // forward output
   void* dx;          // backward outputs (dtype dt)
   void* da;
@@ -132,6 +135,7 @@ cudaError_t launch_scalar_fwd_bf16(const ScalarParams& p, const ScalarPlan& pl, 
 cudaError_t launch_scalar_bwd_f32(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
 cudaError_t launch_scalar_bwd_bf16(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
 cudaError_t launch_log_fwd(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
+cudaError_t launch_log_bwd(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
 
 // Block-matrix affine scan.
 struct AffineParams {

@@ -360,7 +360,7 @@ __device__ inline void check_segments(const ScalarParams& p) {
     if (i < n && (int64_t)p.cu[i + 1] < c) bad = 1;
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.hdr, kStatusSeqlens);
-  if (MODE == MODE_BWD) {
+  if (MODE != MODE_FWD) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     for (int b = 0; b < p.nbr; ++b) {
       float* dh0 = p.br[b].dh0;
@@ -741,14 +741,16 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
                                       const SegWin& win, float& carry,
                                       const StageView* sv = nullptr, int* seg_hint = nullptr,
                                       const Release& release = Release()) {
-  if constexpr (!VARLEN && !SMEM && std::is_same<Op, LinOp>::value && sizeof(TA) == 4) {
+  if constexpr (!VARLEN && !SMEM && MODE != MODE_LOGBWD && std::is_same<Op, LinOp>::value &&
+                sizeof(TA) == 4) {
     chunk_groups<Op, MODE, VEC, J, TA, S>(p, brn, row, k, stationary, epoch, ticket, carry);
     return;
   }
   using E = typename Op::E;
   constexpr int L = 128 * J;
   constexpr int V = 4 * J;
-  constexpr bool BWD = MODE == MODE_BWD;
+  constexpr bool BWD = MODE != MODE_FWD;
+  constexpr bool LOGIN = MODE == MODE_LOGBWD;  // backward of the log-space form
   const BranchArgs& br = p.br[brn];
   const int lane = threadIdx.x & 31;
   if (row >= p.rows) return;  // the whole warp leaves together
@@ -763,8 +765,9 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
   const int64_t roff = row * T;
   const int64_t tr = t0 + (int64_t)V * lane;  // first step of this lane's run
 
-  // ---- loads: A = gates, X = inputs (forward) or dh (backward), H = states ----
-  float A[V], X[V], H[BWD ? V : 1];
+  // ---- loads: A = gates, X = inputs (forward) or dh (backward), H = states,
+  // LX = log x (log-space backward) ----
+  float A[V], X[V], H[BWD ? V : 1], LX[LOGIN ? V : 1];
   const TA* a = static_cast<const TA*>(br.a) + roff;
   const void* xsrc = BWD ? static_cast<const void*>(br.dh) : br.x;
 #pragma unroll
@@ -787,6 +790,8 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
       if (BWD) {
         IO<float>::ld4(static_cast<const float*>(xsrc) + roff + t, xi);
         IO<float>::ld4(br.h + roff + t, hi);
+        if (LOGIN)
+          IO<float>::ld4(static_cast<const float*>(br.x) + roff + t, LX + (LOGIN ? 4 * i : 0));
       } else {
         IO<TA>::ld4(static_cast<const TA*>(xsrc) + roff + t, xi);
       }
@@ -799,6 +804,9 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
         if (BWD) {
           xi[e] = v ? IO<float>::ld1(static_cast<const float*>(xsrc) + roff + tt) : 0.f;
           hi[e] = v ? IO<float>::ld1(br.h + roff + tt) : 0.f;
+          if (LOGIN)
+            LX[LOGIN ? 4 * i + e : 0] =
+                v ? IO<float>::ld1(static_cast<const float*>(br.x) + roff + tt) : 0.f;
         } else {
           xi[e] = v ? IO<TA>::ld1(static_cast<const TA*>(xsrc) + roff + tt) : 0.f;
         }
@@ -812,11 +820,16 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
   // the chunk's edges take them from memory (the halos)
   float a_nb = 0.f, h_nb = 0.f;
   if (BWD) {
+    // log-space backward: the linear adjoint runs on the gates a = exp(log a)
+    if (LOGIN) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) A[e] = __expf(A[e]);
+    }
     float halo_a = 0.f, halo_h = 0.f;
     if (lane == 0) {
       const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
       const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
-      if (pa >= 0 && pa < T) halo_a = IO<TA>::ld1(a + pa);
+      if (pa >= 0 && pa < T) halo_a = LOGIN ? __expf(IO<TA>::ld1(a + pa)) : IO<TA>::ld1(a + pa);
       if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(br.h + roff + ph);
     }
     halo_a = __shfl_sync(kFull, halo_a, 0);
@@ -969,7 +982,9 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
 #pragma unroll
     for (int i = 0; i < J; ++i) {
       const int64_t t = tr + 4 * i;
-      float ga[4];
+      // dx_t = g_t, da_t = g_t h_{t-1}; log-space: d log x_t = g_t x_t and
+      // d log a_t = g_t a_t h_{t-1}
+      float gx[4], ga[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int idx = 4 * i + e;
@@ -977,25 +992,27 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
         const int64_t tt = t + e;
         if (!plain && tt >= 0 && tt < T) {
           // the step that starts the forward recurrence reads h0 and feeds dh0
+          // (log space: d log h0 = a_0 g_0 h0)
           const Bound bd = bound(tt);
           if ((S < 0) ? bd.start : bd.end) {
-            hn = br.h0 ? br.h0[bd.h0row] : 0.f;
-            if (br.dh0) br.dh0[bd.h0row] = A[idx] * X[idx];
+            hn = br.h0 ? (LOGIN ? __expf(br.h0[bd.h0row]) : br.h0[bd.h0row]) : 0.f;
+            if (br.dh0) br.dh0[bd.h0row] = A[idx] * X[idx] * (LOGIN ? hn : 1.f);
           }
         }
-        ga[e] = X[idx] * hn;
+        ga[e] = X[idx] * hn * (LOGIN ? A[idx] : 1.f);
+        gx[e] = LOGIN ? X[idx] * __expf(LX[LOGIN ? idx : 0]) : X[idx];
       }
       if (staged_out) {
-        TIO<TA>::st4(sv->out[0], (uint32_t)(t - sv->e0), X + 4 * i);
+        TIO<TA>::st4(sv->out[0], (uint32_t)(t - sv->e0), gx);
         TIO<TA>::st4(sv->out[1], (uint32_t)(t - sv->e0), ga);
       } else if (VEC && t >= 0 && t + 4 <= T) {
-        IO<TA>::st4(dx + t, X + 4 * i);
+        IO<TA>::st4(dx + t, gx);
         IO<TA>::st4(da + t, ga);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           if (t + e >= 0 && t + e < T) {
-            IO<TA>::st1(dx + t + e, X[4 * i + e]);
+            IO<TA>::st1(dx + t + e, gx[e]);
             IO<TA>::st1(da + t + e, ga[e]);
           }
       }
@@ -1504,9 +1521,13 @@ template <class Op, int MODE, typename TA, int VARIANT>
 cudaError_t launch_layouts(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
   const bool varlen = p.cu != nullptr;
   if constexpr (VARIANT == VAR_STREAM) {  // tensor copies need the vectorised layout
-    if (!pl.vec) return cudaErrorInvalidValue;
-    return varlen ? launch_pick_j<Op, MODE, TA, VARIANT, true, true>(p, pl, s)
-                  : launch_pick_j<Op, MODE, TA, VARIANT, false, true>(p, pl, s);
+    if constexpr (MODE == MODE_LOGBWD) {
+      return cudaErrorInvalidValue;  // planned as stationary
+    } else {
+      if (!pl.vec) return cudaErrorInvalidValue;
+      return varlen ? launch_pick_j<Op, MODE, TA, VARIANT, true, true>(p, pl, s)
+                    : launch_pick_j<Op, MODE, TA, VARIANT, false, true>(p, pl, s);
+    }
   } else {
     if (varlen)
       return pl.vec ? launch_pick_j<Op, MODE, TA, VARIANT, true, true>(p, pl, s)

@@ -114,7 +114,8 @@ typedef enum scan_op {
   SCAN_OP_BIDIR_BWD = 3,
   SCAN_OP_LOG_FWD = 4,
   SCAN_OP_AFFINE_FWD = 5,
-  SCAN_OP_AFFINE_BWD = 6
+  SCAN_OP_AFFINE_BWD = 6,
+  SCAN_OP_LOG_BWD = 7
 } scan_op;
 
 /* Optional tuning and test controls; pass NULL for the defaults (all zero). */
@@ -214,6 +215,24 @@ scan_status scan_log_fwd(const float* log_a, const float* log_x,
                          int64_t T, int32_t reverse, const scan_opts* opts,
                          void* workspace, size_t workspace_bytes,
                          cudaStream_t stream);
+
+/* Log-space backward of L = sum_t dh_t h_t with h = scan_log_fwd(...). The
+ * adjoint is the linear one on a = exp(log_a), x = exp(log_x)
+ * ([TSK] One associative-scan family; the chain rule through exp):
+ *   g_t = dh_t + a_{t+1} g_{t+1} (a_{t+1} = 0 past a sequence end),
+ *   dlog_x_t = g_t x_t, dlog_a_t = g_t a_t h_{t-1} (h_{-1} = exp(log_h0)),
+ *   dlog_h0 = a_0 g_0 exp(log_h0) per row or sequence (0 without log_h0).
+ * reverse mirrors the shifts as scan_bwd does. Inputs: log_a, log_x as given
+ * to scan_log_fwd, h its output, dh fp32; all outputs fp32 in the same
+ * layouts; dlog_h0 nullable. Runs STATIONARY or LOOKBACK (a STREAM request
+ * runs STATIONARY). */
+scan_status scan_log_bwd(const float* log_a, const float* log_x, const float* h,
+                         const float* dh, const float* log_h0,
+                         const int32_t* cu_seqlens, int32_t n_seqs,
+                         float* dlog_a, float* dlog_x, float* dlog_h0, int64_t B,
+                         int64_t C, int64_t T, int32_t reverse,
+                         const scan_opts* opts, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
 
 /* Block-matrix forward ([TSK] One associative-scan family, matrix_affine_scan;
  * Kernel design): H_t = A_t H_{t-1} + B_t per (b, n) lane, H_{-1} = h0.

@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for fn in ("scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd", "scan_log_fwd",
-               "affine_scan_fwd", "affine_scan_bwd", "scan_workspace_bytes",
+               "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "scan_workspace_bytes",
                "scan_workspace_init", "scan_get_device_status", "scan_status_string"):
         assert fn in names
 
@@ -85,6 +85,10 @@ def test_workspace_sizes():
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 100}) == 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 1024}) == 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"variant": 4}) == 0
+    # the log-space backward plans like the other scalar calls
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_LOG_BWD, 1, 64, 100000) == \
+        256 + 64 * ((100000 + 511) // 512) * 16
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_LOG_BWD, 8, 1536, 4096) == 256
     # the stream variant walks whole rows per warp: the header is all it needs
     stream = {"variant": scan.SCAN_VARIANT_STREAM}
     assert scan.scan_workspace_bytes(scan.SCAN_OP_BIDIR_FWD, 1, 2048, 275479, opts=stream) == 256

@@ -364,6 +364,36 @@ def test_log_packed_with_resets(lib):
             assert rel_err(h, ref) <= TOL32
 
 
+def check_log_bwd(scan, la, lx, dh, lh0=None, cu=None, reverse=False, opts=None):
+    """Log-space forward on the GPU, then its backward, against the oracle."""
+    ga, gx, gdh, gh0, gcu = cuda(la, lx, dh, lh0, cu)
+    h = scan.scan_log_fwd(ga, gx, gh0, gcu, reverse, opts=opts)
+    dla, dlx, dlh0 = scan.scan_log_bwd(ga, gx, h, gdh, gh0, gcu, reverse, opts=opts)
+    torch.cuda.synchronize()
+    assert scan.scan_get_device_status(DEV) == scan.SCAN_OK
+    ref = oracle.scan_log_bwd(la, lx, dh, lh0, cu, reverse)
+    errs = (rel_err(dla, ref[0]), rel_err(dlx, ref[1]), rel_err(dlh0, ref[2]))
+    assert max(errs) <= TOL32, errs
+
+
+@pytest.mark.parametrize("T", [1, 5, 128, 129, 777, 4096])
+@pytest.mark.parametrize("reverse", [False, True])
+def test_log_bwd_dense(lib, T, reverse):
+    w = workloads.log_dense(2, 3, T, seed=T + 1, h0=True)
+    for _, opts in variants(lib):
+        for h0 in (w.log_h0, None):
+            check_log_bwd(lib, w.log_a, w.log_x, w.dh, h0, None, reverse, opts)
+
+
+def test_log_bwd_packed_with_resets(lib):
+    a, x, dh, h0, cu = random_packed(3, PACKED_LENS[0], seed=23, p_reset=0.02)
+    la = torch.log(a)  # exact zeros become -inf
+    lh0 = torch.log(h0.abs() + 0.5)
+    for _, opts in variants(lib):
+        for rev in (False, True):
+            check_log_bwd(lib, la, x, dh, lh0, cu, rev, opts)
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads in the benchmark's launch configuration
 # ---------------------------------------------------------------------------
@@ -447,6 +477,13 @@ def test_full_log_4k_sampled_rows(lib):
     torch.cuda.synchronize()
     h2 = h.view(B * C, T)
     la, lx = w.log_a.view(B * C, T), w.log_x.view(B * C, T)
+    dla, dlx, _ = lib.scan_log_bwd(ga, gx, h, w.dh.to(DEV))
+    torch.cuda.synchronize()
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    dla2, dlx2, dh2 = dla.view(B * C, T), dlx.view(B * C, T), w.dh.view(B * C, T)
     for r in sample_rows(B * C, 32, 3):
         ref = oracle.scan_log_fwd(la[r][None, None], lx[r][None, None])
         assert rel_err(h2[r], ref[0, 0]) <= TOL32, r
+        rg = oracle.scan_log_bwd(la[r][None, None], lx[r][None, None], dh2[r][None, None])
+        assert rel_err(dla2[r], rg[0][0, 0]) <= TOL32, r
+        assert rel_err(dlx2[r], rg[1][0, 0]) <= TOL32, r

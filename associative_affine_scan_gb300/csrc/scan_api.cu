@@ -14,7 +14,6 @@ namespace {
 
 constexpr int64_t kMaxGrid = 0x7fffffffLL;
 constexpr int64_t kStationaryMinRows = 152 * 16;
-constexpr int64_t kStationaryWaves = 4;
 constexpr int kCuSmemEntries = 4096;  // packed offsets staged in shared memory
 constexpr bool kStreamOutTiles = true;  // stream: interior outputs leave by tensor stores
 
@@ -89,15 +88,14 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, bool wide
   const int64_t tiles = M * G * nbr;
   if (M > kMaxGrid || G > kMaxGrid || tiles > kMaxGrid || rows * M * nbr > (1LL << 40))
     return SCAN_ERR_UNSUPPORTED;
-  // Stationary rows are cut into segments when the row groups alone give
-  // fewer than about four waves of blocks (152 SMs x 16 warps), so that no
-  // long-running block is left alone in a last partial wave.
+  // Stationary rows are cut into segments only on request: a segment cannot
+  // start before the end state of the one before it is known, so segments
+  // add resident warps that mostly wait (measured slower on every shape the
+  // planner sends to STATIONARY).
   int64_t nseg = 1, cps = M;
   if (variant == VAR_STATIONARY && M > 0) {
     if (o.segments < 0) return SCAN_ERR_INVALID_ARG;
-    const int64_t blocks = G * nbr;
-    const int64_t target = kStationaryWaves * 152 * 16 / R;
-    nseg = o.segments ? o.segments : (blocks >= target ? 1 : (target + blocks - 1) / blocks);
+    nseg = o.segments ? o.segments : 1;
     if (nseg > M) nseg = M;
     cps = (M + nseg - 1) / nseg;
     nseg = (M + cps - 1) / cps;

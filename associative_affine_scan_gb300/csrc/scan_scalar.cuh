@@ -80,15 +80,21 @@ __device__ __forceinline__ void set_status(WsHeader* hdr, unsigned code) {
 template <typename TA>
 struct IO;
 
+// Raw: the packed form of 4 consecutive elements as one vector load returns
+// it, unpacked to fp32 only when used (loads issued ahead of their use).
 template <>
 struct IO<float> {
-  static __device__ __forceinline__ void ld4(const float* p, float v[4]) {
-    const float4 q = __ldcs(reinterpret_cast<const float4*>(p));
+  using Raw = float4;
+  static __device__ __forceinline__ Raw ldraw(const float* p) {
+    return __ldcs(reinterpret_cast<const float4*>(p));
+  }
+  static __device__ __forceinline__ void unpack(const Raw& q, float v[4]) {
     v[0] = q.x;
     v[1] = q.y;
     v[2] = q.z;
     v[3] = q.w;
   }
+  static __device__ __forceinline__ void ld4(const float* p, float v[4]) { unpack(ldraw(p), v); }
   static __device__ __forceinline__ float ld1(const float* p) { return __ldcs(p); }
   static __device__ __forceinline__ void st4(float* p, const float v[4]) {
     __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
@@ -98,12 +104,18 @@ struct IO<float> {
 
 template <>
 struct IO<__nv_bfloat16> {
-  static __device__ __forceinline__ void ld4(const __nv_bfloat16* p, float v[4]) {
-    const uint2 q = __ldcs(reinterpret_cast<const uint2*>(p));
+  using Raw = uint2;
+  static __device__ __forceinline__ Raw ldraw(const __nv_bfloat16* p) {
+    return __ldcs(reinterpret_cast<const uint2*>(p));
+  }
+  static __device__ __forceinline__ void unpack(const Raw& q, float v[4]) {
     v[0] = __uint_as_float(q.x << 16);
     v[1] = __uint_as_float(q.x & 0xffff0000u);
     v[2] = __uint_as_float(q.y << 16);
     v[3] = __uint_as_float(q.y & 0xffff0000u);
+  }
+  static __device__ __forceinline__ void ld4(const __nv_bfloat16* p, float v[4]) {
+    unpack(ldraw(p), v);
   }
   static __device__ __forceinline__ float ld1(const __nv_bfloat16* p) {
     const unsigned short u = __ldcs(reinterpret_cast<const unsigned short*>(p));
@@ -734,13 +746,40 @@ struct NoRelease {
   __device__ __forceinline__ void operator()() const {}
 };
 
+// The register-carry loop's loads one chunk ahead: a lane's vector loads of
+// the next chunk of its row (raw, the aligned in-row 4-step groups only) and
+// the backward halos, issued before the current chunk is computed so that
+// each warp keeps two chunks of loads in flight.
+template <int J, typename TA, int MODE>
+struct RunAhead {
+  static constexpr bool BWD = MODE != MODE_FWD;
+  static constexpr bool LOGIN = MODE == MODE_LOGBWD;
+  using XT = typename std::conditional<BWD, float, TA>::type;
+  typename IO<TA>::Raw a[J];
+  typename IO<XT>::Raw x[J];  // x forward, dh backward
+  float4 h[BWD ? J : 1];
+  float4 lx[LOGIN ? J : 1];
+  float halo_a, halo_h;
+  bool full;  // holds the chunk this call is about to scan
+};
+
+// Look-ahead pays where a launch's warps are all resident at once and each
+// keeps too few bytes in flight: the packed bf16 forward (one wave of
+// row-warps, 2-byte inputs, 8 more registers). Elsewhere, the packed
+// backward included, its registers cost more occupancy than it gains.
+template <int MODE, bool VARLEN, typename TA>
+__host__ __device__ constexpr bool uses_ahead() {
+  return MODE == MODE_FWD && VARLEN && sizeof(TA) == 2;
+}
+
 template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int S, bool SMEM = false,
           class Release = NoRelease>
 __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t row, int k,
                                       bool stationary, uint32_t epoch, unsigned ticket,
                                       const SegWin& win, float& carry,
                                       const StageView* sv = nullptr, int* seg_hint = nullptr,
-                                      const Release& release = Release()) {
+                                      const Release& release = Release(),
+                                      RunAhead<J, TA, MODE>* ahead = nullptr, bool next = false) {
   if constexpr (!VARLEN && !SMEM && MODE != MODE_LOGBWD && std::is_same<Op, LinOp>::value &&
                 sizeof(TA) == 4) {
     chunk_groups<Op, MODE, VEC, J, TA, S>(p, brn, row, k, stationary, epoch, ticket, carry);
@@ -770,6 +809,7 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
   float A[V], X[V], H[BWD ? V : 1], LX[LOGIN ? V : 1];
   const TA* a = static_cast<const TA*>(br.a) + roff;
   const void* xsrc = BWD ? static_cast<const void*>(br.dh) : br.x;
+  using XT = typename RunAhead<J, TA, MODE>::XT;  // element type of xsrc
 #pragma unroll
   for (int i = 0; i < J; ++i) {
     const int64_t t = tr + 4 * i;
@@ -785,6 +825,11 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
       } else {
         TIO<TA>::ld4(sv->in[1], o, xi);
       }
+    } else if (VEC && t >= 0 && t + 4 <= T && ahead && ahead->full) {
+      IO<TA>::unpack(ahead->a[i], ai);
+      IO<XT>::unpack(ahead->x[i], xi);
+      if (BWD) IO<float>::unpack(ahead->h[BWD ? i : 0], hi);
+      if (LOGIN) IO<float>::unpack(ahead->lx[LOGIN ? i : 0], LX + (LOGIN ? 4 * i : 0));
     } else if (VEC && t >= 0 && t + 4 <= T) {
       IO<TA>::ld4(a + t, ai);
       if (BWD) {
@@ -814,6 +859,41 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
     }
   }
 
+  // this chunk's halos if they came with the look-ahead; then the loads of
+  // the next chunk of the row (scan order), before this one is scanned
+  const bool had = ahead && ahead->full;
+  const float had_ha = had ? ahead->halo_a : 0.f, had_hh = had ? ahead->halo_h : 0.f;
+  if (ahead) {
+    ahead->full = next;
+    if (next) {
+      const int mn = (S > 0) ? k + 1 : (p.M - 2 - k);
+      const int64_t t0n = (int64_t)mn * L - shift;
+      const int64_t trn = t0n + (int64_t)V * lane;
+#pragma unroll
+      for (int i = 0; i < J; ++i) {
+        const int64_t t = trn + 4 * i;
+        if (VEC && t >= 0 && t + 4 <= T) {
+          ahead->a[i] = IO<TA>::ldraw(a + t);
+          ahead->x[i] = IO<XT>::ldraw(static_cast<const XT*>(xsrc) + roff + t);
+          if (BWD) ahead->h[BWD ? i : 0] = IO<float>::ldraw(br.h + roff + t);
+          if (LOGIN)
+            ahead->lx[LOGIN ? i : 0] = IO<float>::ldraw(static_cast<const float*>(br.x) + roff + t);
+        }
+      }
+      if (BWD) {
+        // raw gate halo (log space: log a, -inf outside the row)
+        ahead->halo_a = LOGIN ? -CUDART_INF_F : 0.f;
+        ahead->halo_h = 0.f;
+        if (lane == 0) {
+          const int64_t pa = (S < 0) ? t0n + L : t0n - 1;
+          const int64_t ph = (S < 0) ? t0n - 1 : t0n + L;
+          if (pa >= 0 && pa < T) ahead->halo_a = IO<TA>::ld1(a + pa);
+          if (ph >= 0 && ph < T) ahead->halo_h = IO<float>::ld1(br.h + roff + ph);
+        }
+      }
+    }
+  }
+
   // backward neighbours across runs: the gate one step past the run's far
   // end in scan order (a_{t+1} for S = -1, a_{t-1} for S = +1) and the
   // state one step past its near end (h_{t-1}, resp. h_{t+1}); the lanes at
@@ -826,7 +906,10 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
       for (int e = 0; e < V; ++e) A[e] = __expf(A[e]);
     }
     float halo_a = 0.f, halo_h = 0.f;
-    if (lane == 0) {
+    if (had) {
+      halo_a = LOGIN ? __expf(had_ha) : had_ha;
+      halo_h = had_hh;
+    } else if (lane == 0) {
       const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
       const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
       if (pa >= 0 && pa < T) halo_a = LOGIN ? __expf(IO<TA>::ld1(a + pa)) : IO<TA>::ld1(a + pa);
@@ -1348,13 +1431,17 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
     float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
     const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
     int hint = -1;
+    RunAhead<J, TA, MODE> ahead;
+    ahead.full = false;
+    RunAhead<J, TA, MODE>* ap = uses_ahead<MODE, VARLEN, TA>() ? &ahead : nullptr;
     for (int k = 0; k < p.M; ++k) {
+      const bool next = k + 1 < p.M;
       if (S > 0)
         chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
-                                               &hint);
+                                               &hint, NoRelease(), ap, next);
       else
         chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
-                                                &hint);
+                                                &hint, NoRelease(), ap, next);
     }
   } else {
     // VAR_SEGMENTED: a row is cut into nseg segments of cps chunks, taken in
@@ -1387,13 +1474,17 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
       const int k0 = seg * p.cps;
       const int k1 = k0 + p.cps < p.M ? k0 + p.cps : p.M;
       int hint = -1;
+      RunAhead<J, TA, MODE> ahead;
+      ahead.full = false;
+      RunAhead<J, TA, MODE>* ap = uses_ahead<MODE, VARLEN, TA>() ? &ahead : nullptr;
       for (int k = k0; k < k1; ++k) {
+        const bool next = k + 1 < k1;
         if (S > 0)
           chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
-                                                 &hint);
+                                                 &hint, NoRelease(), ap, next);
         else
           chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
-                                                  &hint);
+                                                  &hint, NoRelease(), ap, next);
       }
       if (active && lane == 0)
         st_relaxed(recs_row + 2 * (int64_t)seg + 1, pack_rec((epoch << 2) | 2u, carry));

@@ -65,11 +65,13 @@ def test_workspace_sizes():
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096,
                                      opts={"variant": scan.SCAN_VARIANT_STATIONARY}) == 256
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 8, 1536, 4096) == 256
-    # forced stationary with too few row groups for four waves: rows are cut
-    # into segments that hand their end state on through the workspace
+    # stationary rows cut into segments on request hand their end state on
+    # through the workspace; unsegmented stationary needs only the header
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 2048, 100000,
-                                     opts={"variant": scan.SCAN_VARIANT_STATIONARY}) == \
-        256 + 2048 * 5 * 16
+                                     opts={"variant": scan.SCAN_VARIANT_STATIONARY,
+                                           "segments": 5}) == 256 + 2048 * 5 * 16
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 2048, 100000,
+                                     opts={"variant": scan.SCAN_VARIANT_STATIONARY}) == 256
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 2048, 100000,
                                      opts={"variant": scan.SCAN_VARIANT_STATIONARY,
                                            "segments": 1}) == 256

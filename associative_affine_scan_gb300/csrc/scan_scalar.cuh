@@ -748,8 +748,10 @@ struct NoRelease {
 
 // The register-carry loop's loads one chunk ahead: a lane's vector loads of
 // the next chunk of its row (raw, the aligned in-row 4-step groups only) and
-// the backward halos, issued before the current chunk is computed so that
-// each warp keeps two chunks of loads in flight.
+// the backward gate halo, issued before the current chunk is computed so that
+// each warp keeps two chunks of loads in flight. The backward's states h are
+// not among them: they are first used after the scan, so their loads,
+// issued at the chunk's start, already overlap it.
 template <int J, typename TA, int MODE>
 struct RunAhead {
   static constexpr bool BWD = MODE != MODE_FWD;
@@ -757,16 +759,16 @@ struct RunAhead {
   using XT = typename std::conditional<BWD, float, TA>::type;
   typename IO<TA>::Raw a[J];
   typename IO<XT>::Raw x[J];  // x forward, dh backward
-  float4 h[BWD ? J : 1];
   float4 lx[LOGIN ? J : 1];
-  float halo_a, halo_h;
-  bool full;  // holds the chunk this call is about to scan
+  float halo_a;  // backward: the gate halo
+  bool full;     // holds the chunk this call is about to scan
 };
 
 // Look-ahead pays where a launch's warps are all resident at once and each
 // keeps too few bytes in flight: the packed bf16 forward (one wave of
-// row-warps, 2-byte inputs, 8 more registers). Elsewhere, the packed
-// backward included, its registers cost more occupancy than it gains.
+// row-warps, 2-byte inputs, 8 more registers at 256-step chunks). Elsewhere
+// its registers cost more occupancy than it gains; the packed backward,
+// which already moves 14 bytes per step, measured slower with it.
 template <int MODE, bool VARLEN, typename TA>
 __host__ __device__ constexpr bool uses_ahead() {
   return MODE == MODE_FWD && VARLEN && sizeof(TA) == 2;
@@ -828,7 +830,7 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
     } else if (VEC && t >= 0 && t + 4 <= T && ahead && ahead->full) {
       IO<TA>::unpack(ahead->a[i], ai);
       IO<XT>::unpack(ahead->x[i], xi);
-      if (BWD) IO<float>::unpack(ahead->h[BWD ? i : 0], hi);
+      if (BWD) IO<float>::ld4(br.h + roff + t, hi);
       if (LOGIN) IO<float>::unpack(ahead->lx[LOGIN ? i : 0], LX + (LOGIN ? 4 * i : 0));
     } else if (VEC && t >= 0 && t + 4 <= T) {
       IO<TA>::ld4(a + t, ai);
@@ -862,7 +864,7 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
   // this chunk's halos if they came with the look-ahead; then the loads of
   // the next chunk of the row (scan order), before this one is scanned
   const bool had = ahead && ahead->full;
-  const float had_ha = had ? ahead->halo_a : 0.f, had_hh = had ? ahead->halo_h : 0.f;
+  const float had_ha = had ? ahead->halo_a : 0.f;
   if (ahead) {
     ahead->full = next;
     if (next) {
@@ -875,7 +877,6 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
         if (VEC && t >= 0 && t + 4 <= T) {
           ahead->a[i] = IO<TA>::ldraw(a + t);
           ahead->x[i] = IO<XT>::ldraw(static_cast<const XT*>(xsrc) + roff + t);
-          if (BWD) ahead->h[BWD ? i : 0] = IO<float>::ldraw(br.h + roff + t);
           if (LOGIN)
             ahead->lx[LOGIN ? i : 0] = IO<float>::ldraw(static_cast<const float*>(br.x) + roff + t);
         }
@@ -883,12 +884,9 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
       if (BWD) {
         // raw gate halo (log space: log a, -inf outside the row)
         ahead->halo_a = LOGIN ? -CUDART_INF_F : 0.f;
-        ahead->halo_h = 0.f;
         if (lane == 0) {
           const int64_t pa = (S < 0) ? t0n + L : t0n - 1;
-          const int64_t ph = (S < 0) ? t0n - 1 : t0n + L;
           if (pa >= 0 && pa < T) ahead->halo_a = IO<TA>::ld1(a + pa);
-          if (ph >= 0 && ph < T) ahead->halo_h = IO<float>::ld1(br.h + roff + ph);
         }
       }
     }
@@ -898,36 +896,27 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
   // end in scan order (a_{t+1} for S = -1, a_{t-1} for S = +1) and the
   // state one step past its near end (h_{t-1}, resp. h_{t+1}); the lanes at
   // the chunk's edges take them from memory (the halos)
-  float a_nb = 0.f, h_nb = 0.f;
+  float a_nb = 0.f, halo_h = 0.f;
   if (BWD) {
     // log-space backward: the linear adjoint runs on the gates a = exp(log a)
     if (LOGIN) {
 #pragma unroll
       for (int e = 0; e < V; ++e) A[e] = __expf(A[e]);
     }
-    float halo_a = 0.f, halo_h = 0.f;
-    if (had) {
-      halo_a = LOGIN ? __expf(had_ha) : had_ha;
-      halo_h = had_hh;
-    } else if (lane == 0) {
+    float halo_a = 0.f;
+    if (lane == 0) {
       const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
       const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
-      if (pa >= 0 && pa < T) halo_a = LOGIN ? __expf(IO<TA>::ld1(a + pa)) : IO<TA>::ld1(a + pa);
-      if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(br.h + roff + ph);
+      if (had) {
+        halo_a = LOGIN ? __expf(had_ha) : had_ha;
+      } else if (pa >= 0 && pa < T) {
+        halo_a = LOGIN ? __expf(IO<TA>::ld1(a + pa)) : IO<TA>::ld1(a + pa);
+      }
+      if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(br.h + roff + ph);  // used after the scan
     }
     halo_a = __shfl_sync(kFull, halo_a, 0);
-    halo_h = __shfl_sync(kFull, halo_h, 0);
-    if (S < 0) {
-      const float an = __shfl_down_sync(kFull, A[0], 1);
-      const float hp = __shfl_up_sync(kFull, H[V - 1], 1);
-      a_nb = lane == 31 ? halo_a : an;
-      h_nb = lane == 0 ? halo_h : hp;
-    } else {
-      const float ap = __shfl_up_sync(kFull, A[V - 1], 1);
-      const float hn = __shfl_down_sync(kFull, H[0], 1);
-      a_nb = lane == 0 ? halo_a : ap;
-      h_nb = lane == 31 ? halo_h : hn;
-    }
+    const float an = (S < 0) ? __shfl_down_sync(kFull, A[0], 1) : __shfl_up_sync(kFull, A[V - 1], 1);
+    a_nb = lane == ((S < 0) ? 31 : 0) ? halo_a : an;
   }
   release();
   // backward: the shifted gate of element e (before sequence cuts), and the
@@ -935,10 +924,6 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
   auto gate_of = [&](int e) -> float {
     if (S < 0) return e + 1 < V ? A[e + 1 < V ? e + 1 : e] : a_nb;
     return e > 0 ? A[e > 0 ? e - 1 : 0] : a_nb;
-  };
-  auto hn_of = [&](int e) -> float {
-    if (S < 0) return e > 0 ? H[BWD ? (e > 0 ? e - 1 : 0) : 0] : h_nb;
-    return e + 1 < V ? H[BWD ? (e + 1 < V ? e + 1 : e) : 0] : h_nb;
   };
 
   // ---- is the run plain: every step valid, no sequence starts or ends in it ----
@@ -1062,6 +1047,15 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
   } else {
     TA* dx = static_cast<TA*>(br.dx) + roff;
     TA* da = static_cast<TA*>(br.da) + roff;
+    // the state one step past the run's near end (h_{t-1} for S = -1,
+    // h_{t+1} for S = +1), from the neighbour lane or the halo
+    halo_h = __shfl_sync(kFull, halo_h, 0);
+    const float hx = (S < 0) ? __shfl_up_sync(kFull, H[V - 1], 1) : __shfl_down_sync(kFull, H[0], 1);
+    const float h_nb = lane == ((S < 0) ? 0 : 31) ? halo_h : hx;
+    auto hn_of = [&](int e) -> float {
+      if (S < 0) return e > 0 ? H[e > 0 ? e - 1 : 0] : h_nb;
+      return e + 1 < V ? H[e + 1 < V ? e + 1 : e] : h_nb;
+    };
 #pragma unroll
     for (int i = 0; i < J; ++i) {
       const int64_t t = tr + 4 * i;

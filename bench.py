@@ -40,9 +40,9 @@ BWD_BYTES = 20
 # kernel-level Fwd+Bwd table, seqlen 4096: 0.602 ms on an H100 (fp32 inferred)
 PAGES_FWD_BWD_MS = {"dense_4k": 0.602, "dense_64k": 9.212}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward
-# kernel on this workload, from the ncu capture summarised in profiles/
-# (None until a capture of the current kernel exists)
-BWD_TRAFFIC_BYTES = None
+# kernel on dense_4k (604.28 + 357.60 MB), from a full ncu capture of the
+# current kernel; None for a workload without a capture
+BWD_TRAFFIC_BYTES = {"dense_4k": 961879552}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -282,16 +282,31 @@ def time_calls(fn, steps, warmup, flush, stream):
     return total / steps
 
 
-def measure_rows(args, dev, scan):
-    """Per-row throughput of the other forms (packed bidirectional, affine, log)."""
+ROWS = ("packed_bidir", "log_4k", "affine_4x4")
+
+
+def measure_rows(args, dev, scan, names=ROWS, small=False):
+    """Per-row throughput of the other forms (packed bidirectional, affine, log).
+
+    small: the packed row with 12 sequences instead of 64 (same 2 x 2048 rows,
+    2.5 GB on the device), the size used for full ncu captures."""
     from associative_affine_scan_gb300 import workloads
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    steps, warm = max(3, min(args.steps, 10)), 3
+    steps, warm = max(1, min(args.steps, 10)), 3
     out = {}
     peak, _ = measured_peaks()
+    if "packed_bidir" in names:
+        out["packed_bidir"] = _row_packed(scan, workloads, dev, steps, warm, flush, stream, small)
+    if "log_4k" in names:
+        out["log_4k"] = _row_log(scan, workloads, dev, steps, warm, flush, stream, peak)
+    if "affine_4x4" in names:
+        out["affine_4x4"] = _row_affine(scan, workloads, dev, steps, warm, flush, stream)
+    return out
 
-    w = workloads.packed_bidir(seed=0)
+
+def _row_packed(scan, workloads, dev, steps, warm, flush, stream, small):
+    w = workloads.packed_bidir(seed=0, n_seqs=12 if small else 64)
     af, xf, ar, xr, cu, dhf, dhr = (t.to(dev) for t in (w.af, w.xf, w.ar, w.xr, w.cu_seqlens,
                                                          w.dhf, w.dhr))
     hf, hr = scan.scan_bidir_fwd(af, xf, ar, xr, None, None, cu)
@@ -301,11 +316,12 @@ def measure_rows(args, dev, scan):
     g = scan.scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, None, None, cu)
     b_ms = time_calls(lambda: scan.scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, None, None, cu, out=g),
                       steps, warm, flush, stream)
-    out["packed_bidir"] = {"elems": n, "fwd_ms": f_ms, "bwd_ms": b_ms,
-                           "fwd_gbs": n * 8 / f_ms / 1e6, "bwd_gbs": n * 14 / b_ms / 1e6,
-                           "fwd_bwd_elem_per_s": n / (f_ms + b_ms) * 1e3}
-    del af, xf, ar, xr, dhf, dhr, hf, hr, g
+    return {"elems": n, "sum_len": int(w.cu_seqlens[-1]), "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_gbs": n * 8 / f_ms / 1e6, "bwd_gbs": n * 14 / b_ms / 1e6,
+            "fwd_bwd_elem_per_s": n / (f_ms + b_ms) * 1e3}
 
+
+def _row_log(scan, workloads, dev, steps, warm, flush, stream, peak):
     # log space: fwd reads log a, log x and writes h (12 B/elem); bwd reads
     # log a, log x, h, dh and writes d log a, d log x (24 B/elem)
     w = workloads.log_4k(seed=0)
@@ -316,12 +332,12 @@ def measure_rows(args, dev, scan):
     gl = scan.scan_log_bwd(la, lx, hl, ldh)
     lb_ms = time_calls(lambda: scan.scan_log_bwd(la, lx, hl, ldh, out=gl), steps, warm, flush,
                        stream)
-    out["log_4k"] = {"elems": n, "fwd_ms": l_ms, "bwd_ms": lb_ms,
-                     "fwd_gbs": n * 12 / l_ms / 1e6, "bwd_gbs": n * 24 / lb_ms / 1e6,
-                     "fwd_frac": n * 12 / l_ms / 1e6 / peak,
-                     "bwd_frac": n * 24 / lb_ms / 1e6 / peak}
-    del la, lx, ldh, hl, gl
+    return {"elems": n, "fwd_ms": l_ms, "bwd_ms": lb_ms,
+            "fwd_gbs": n * 12 / l_ms / 1e6, "bwd_gbs": n * 24 / lb_ms / 1e6,
+            "fwd_frac": n * 12 / l_ms / 1e6 / peak, "bwd_frac": n * 24 / lb_ms / 1e6 / peak}
 
+
+def _row_affine(scan, workloads, dev, steps, warm, flush, stream):
     try:
         w = workloads.affine_4x4(seed=0)
         A, Bm, dH = w.A.to(dev), w.Bm.to(dev), w.dH.to(dev)
@@ -331,11 +347,10 @@ def measure_rows(args, dev, scan):
         g = scan.affine_scan_bwd(A, H, dH)
         b_ms = time_calls(lambda: scan.affine_scan_bwd(A, H, dH, out=g), steps, warm, flush,
                           stream)
-        out["affine_4x4"] = {"blocks": nb, "fwd_ms": f_ms, "bwd_ms": b_ms,
-                             "fwd_gbs": nb * 192 / f_ms / 1e6, "bwd_gbs": nb * 320 / b_ms / 1e6}
+        return {"blocks": nb, "fwd_ms": f_ms, "bwd_ms": b_ms,
+                "fwd_gbs": nb * 192 / f_ms / 1e6, "bwd_gbs": nb * 320 / b_ms / 1e6}
     except Exception as e:  # reported, not fatal: the other rows still print
-        out["affine_4x4"] = {"error": str(e)}
-    return out
+        return {"error": str(e)}
 
 
 def oracle_fwd_bwd(w, rows):
@@ -406,10 +421,27 @@ def main():
     ap.add_argument("--all-rows", action="store_true",
                     help="also time the packed bidirectional, log and affine forms")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--row", choices=ROWS,
+                    help="time only this form (fwd and bwd, --steps timed calls each) and print "
+                         "its figures; the command the ncu captures of that form use")
+    ap.add_argument("--small", action="store_true",
+                    help="with --row packed_bidir: 12 sequences instead of 64 (ncu capture size)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
+
+    if args.row:
+        import associative_affine_scan_gb300 as scan
+        if not os.path.exists(scan.LIB_PATH):
+            import __graft_entry__
+            __graft_entry__.build()
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        rows = measure_rows(args, dev, scan, names=(args.row,), small=args.small)
+        if rank == 0:
+            print(json.dumps({"row": args.row, "small": args.small, **rows[args.row]}), flush=True)
+        return
 
     if args.impl == "reference":
         line = run_reference(args, world, rank)
@@ -444,7 +476,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "scalar_scan_kernel (backward)",
                      "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
                      "peak_source": peak_kind,
-                     "traffic": BWD_TRAFFIC_BYTES},
+                     "traffic": BWD_TRAFFIC_BYTES.get(args.workload)},
         "e2e": {"value": n_total / (r["e2e_ms"] * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": r["bytes_in"], "d2h_bytes_per_step": r["bytes_out"]},
         "gpu_launches": 2 * args.steps,

@@ -33,6 +33,12 @@ namespace {
 
 constexpr int kSub = 4;  // sub-chunks (warps) per block
 
+// Steps per load batch: a thread issues the loads of PB consecutive steps
+// before composing the first of them (k = v = 4: batches of 2 measured faster
+// than 4, whose 128 registers halve the resident warps; one step at a time
+// was slower still).
+constexpr int affine_batch(int k) { return k <= 2 ? 8 : 2; }
+
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -255,6 +261,8 @@ __device__ __forceinline__ void reduce_scatter_rows(float (&D)[K * K], int j) {
 template <int K, int V, int LS, int MODE>
 __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ AffineParams p) {
   static_assert(K == V, "one thread per column of P and Q needs k == v");
+  constexpr int PB = affine_batch(K);  // steps whose loads are in flight together
+  static_assert(LS % PB == 0, "sub-chunks are whole batches");
   constexpr int KK = K * K, KV = K * V, NL = 32 / V;
   using RL = RecLayout<K, V>;
   __shared__ float s_P[kSub][NL][KK];
@@ -295,49 +303,53 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
       Pc[i] = (i == j) ? 1.f : 0.f;
       Qc[i] = 0.f;
     }
+    // The steps are taken in batches of PB: a batch's loads are all issued
+    // before its first step is composed, so a thread keeps PB steps of
+    // inputs in flight instead of one.
     if (active && t_lo < t_hi) {
       if (MODE == MODE_FWD) {
-        float An[KK], Bn[K];
-        ldv(p.A + blk(t_lo) * KK, An, true);
-        load_col<K, V>(p.Bm + blk(t_lo) * KV, j, Bn, true);
-        for (int64_t t = t_lo; t < t_hi; ++t) {
-          float Ac[KK], Bc[K], tq[K], tp[K];
-          copy(An, Ac);
-          copy(Bn, Bc);
-          if (t + 1 < t_hi) {
-            ldv(p.A + blk(t + 1) * KK, An, true);
-            load_col<K, V>(p.Bm + blk(t + 1) * KV, j, Bn, true);
-          }
-          mv_add<K>(Ac, Qc, Bc, tq);
-          float z[K];
-          fill(z, 0.f);
-          mv_add<K>(Ac, Pc, z, tp);
-          copy(tq, Qc);
-          copy(tp, Pc);
+        for (int64_t t0 = t_lo; t0 < t_hi; t0 += PB) {
+          float Ab[PB][KK], Bb[PB][K];
+#pragma unroll
+          for (int q = 0; q < PB; ++q)
+            if (t0 + q < t_hi) {
+              ldv(p.A + blk(t0 + q) * KK, Ab[q], true);
+              load_col<K, V>(p.Bm + blk(t0 + q) * KV, j, Bb[q], true);
+            }
+#pragma unroll
+          for (int q = 0; q < PB; ++q)
+            if (t0 + q < t_hi) {
+              float tq[K], tp[K], z[K];
+              fill(z, 0.f);
+              mv_add<K>(Ab[q], Qc, Bb[q], tq);
+              mv_add<K>(Ab[q], Pc, z, tp);
+              copy(tq, Qc);
+              copy(tp, Pc);
+            }
         }
       } else {
         // G_t = A_{t+1}^T G_{t+1} + dH_t, walking t downwards
-        float An[KK], Dn[K];
-        {
-          const int64_t t = t_hi - 1;
-          if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, An, true);
-          else fill(An, 0.f);
-          load_col<K, V>(p.dH + blk(t) * KV, j, Dn, true);
-        }
-        for (int64_t t = t_hi - 1; t >= t_lo; --t) {
-          float Ac[KK], Dc[K], tq[K], tp[K];
-          copy(An, Ac);
-          copy(Dn, Dc);
-          if (t - 1 >= t_lo) {
-            ldv(p.A + blk(t) * KK, An, true);
-            load_col<K, V>(p.dH + blk(t - 1) * KV, j, Dn, true);
+        for (int64_t t0 = t_hi - 1; t0 >= t_lo; t0 -= PB) {
+          float Ab[PB][KK], Db[PB][K];
+#pragma unroll
+          for (int q = 0; q < PB; ++q) {
+            const int64_t t = t0 - q;
+            if (t >= t_lo) {
+              if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, Ab[q], true);
+              else fill(Ab[q], 0.f);
+              load_col<K, V>(p.dH + blk(t) * KV, j, Db[q], true);
+            }
           }
-          mtv_add<K>(Ac, Qc, Dc, tq);
-          float z[K];
-          fill(z, 0.f);
-          mtv_add<K>(Ac, Pc, z, tp);
-          copy(tq, Qc);
-          copy(tp, Pc);
+#pragma unroll
+          for (int q = 0; q < PB; ++q)
+            if (t0 - q >= t_lo) {
+              float tq[K], tp[K], z[K];
+              fill(z, 0.f);
+              mtv_add<K>(Ab[q], Qc, Db[q], tq);
+              mtv_add<K>(Ab[q], Pc, z, tp);
+              copy(tq, Qc);
+              copy(tp, Pc);
+            }
         }
       }
     }
@@ -425,20 +437,22 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
     const bool work = active && t_lo < t_hi;
     if (MODE == MODE_FWD) {
       if (work) {
-        float An[KK], Bn[K];
-        ldv(p.A + blk(t_lo) * KK, An, false);
-        load_col<K, V>(p.Bm + blk(t_lo) * KV, j, Bn, false);
-        for (int64_t t = t_lo; t < t_hi; ++t) {
-          float Ac[KK], Bc[K], h[K];
-          copy(An, Ac);
-          copy(Bn, Bc);
-          if (t + 1 < t_hi) {
-            ldv(p.A + blk(t + 1) * KK, An, false);
-            load_col<K, V>(p.Bm + blk(t + 1) * KV, j, Bn, false);
-          }
-          mv_add<K>(Ac, c, Bc, h);
-          store_col<K, V>(p.out_H + blk(t) * KV, j, h);
-          copy(h, c);
+        for (int64_t t0 = t_lo; t0 < t_hi; t0 += PB) {
+          float Ab[PB][KK], Bb[PB][K];
+#pragma unroll
+          for (int q = 0; q < PB; ++q)
+            if (t0 + q < t_hi) {
+              ldv(p.A + blk(t0 + q) * KK, Ab[q], false);
+              load_col<K, V>(p.Bm + blk(t0 + q) * KV, j, Bb[q], false);
+            }
+#pragma unroll
+          for (int q = 0; q < PB; ++q)
+            if (t0 + q < t_hi) {
+              float h[K];
+              mv_add<K>(Ab[q], c, Bb[q], h);
+              store_col<K, V>(p.out_H + blk(t0 + q) * KV, j, h);
+              copy(h, c);
+            }
         }
       }
     } else {
@@ -446,39 +460,49 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
       // exchange of dA stays warp-uniform; idle threads compute on zeros
       const int64_t w_lo = (int64_t)m * (kSub * LS) + (int64_t)warp * LS;
       const int64_t w_hi = w_lo + LS < T ? w_lo + LS : T;
-      for (int64_t t = w_hi - 1; t >= w_lo; --t) {
-        float An[KK], Dn[K], Hp[K], gn[K], D[KK];
-        if (work) {
-          if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, An, false);
-          else fill(An, 0.f);
-          load_col<K, V>(p.dH + blk(t) * KV, j, Dn, false);
-          if (t >= 1) load_col<K, V>(p.H + blk(t - 1) * KV, j, Hp, false);
-          else if (p.h0) load_col<K, V>(p.h0 + lane_id * KV, j, Hp, false);
-          else fill(Hp, 0.f);
-        } else {
-          fill(An, 0.f);
-          fill(Dn, 0.f);
-          fill(Hp, 0.f);
+      for (int64_t t0 = w_hi - 1; t0 >= w_lo; t0 -= PB) {
+        float Ab[PB][KK], Db[PB][K], Hb[PB][K];
+#pragma unroll
+        for (int q = 0; q < PB; ++q) {
+          const int64_t t = t0 - q;
+          if (work && t >= w_lo) {
+            if (t + 1 < T) ldv(p.A + blk(t + 1) * KK, Ab[q], false);
+            else fill(Ab[q], 0.f);
+            load_col<K, V>(p.dH + blk(t) * KV, j, Db[q], false);
+            if (t >= 1) load_col<K, V>(p.H + blk(t - 1) * KV, j, Hb[q], false);
+            else if (p.h0) load_col<K, V>(p.h0 + lane_id * KV, j, Hb[q], false);
+            else fill(Hb[q], 0.f);
+          } else {
+            fill(Ab[q], 0.f);
+            fill(Db[q], 0.f);
+            fill(Hb[q], 0.f);
+          }
         }
-        mtv_add<K>(An, c, Dn, gn);
-        copy(gn, c);
-        // dA_t = G_t H_{t-1}^T: this column's rank-1 part, summed across the lane
 #pragma unroll
-        for (int i = 0; i < K; ++i)
+        for (int q = 0; q < PB; ++q) {
+          const int64_t t = t0 - q;
+          if (t < w_lo) break;  // warp-uniform: w_lo and t0 are the same for every thread
+          float gn[K], D[KK];
+          mtv_add<K>(Ab[q], c, Db[q], gn);
+          copy(gn, c);
+          // dA_t = G_t H_{t-1}^T: this column's rank-1 part, summed across the lane
 #pragma unroll
-          for (int l = 0; l < K; ++l) D[i * K + l] = c[i] * Hp[l];
-        reduce_scatter_rows<K, V>(D, j);
-        if (work) {
-          store_col<K, V>(p.dB + blk(t) * KV, j, c);
-          float* row = p.dA + blk(t) * KK + j * K;
+          for (int i = 0; i < K; ++i)
 #pragma unroll
-          for (int l = 0; l < K; ++l) __stcs(row + l, D[l]);
-          if (t == 0 && p.dh0) {
-            float A0[KK], d0[K], z[K];
-            ldv(p.A + blk(0) * KK, A0, false);
-            fill(z, 0.f);
-            mtv_add<K>(A0, c, z, d0);
-            store_col<K, V>(p.dh0 + lane_id * KV, j, d0);
+            for (int l = 0; l < K; ++l) D[i * K + l] = c[i] * Hb[q][l];
+          reduce_scatter_rows<K, V>(D, j);
+          if (work) {
+            store_col<K, V>(p.dB + blk(t) * KV, j, c);
+            float* row = p.dA + blk(t) * KK + j * K;
+#pragma unroll
+            for (int l = 0; l < K; ++l) __stcs(row + l, D[l]);
+            if (t == 0 && p.dh0) {
+              float A0[KK], d0[K], z[K];
+              ldv(p.A + blk(0) * KK, A0, false);
+              fill(z, 0.f);
+              mtv_add<K>(A0, c, z, d0);
+              store_col<K, V>(p.dh0 + lane_id * KV, j, d0);
+            }
           }
         }
       }

@@ -78,9 +78,9 @@ def test_workspace_sizes():
     # few rows (here 64) take the look-back
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 64, 100000) == \
         256 + 64 * ((100000 + 511) // 512) * 16
-    # affine k=v=4: one 52-float record per (lane, chunk of 128 steps)
+    # affine k=v=4: one 52-float record per (lane, chunk of 64 steps)
     assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_FWD, 8, 256, 4096, 4, 4) == \
-        256 + 8 * 256 * 32 * 52 * 4
+        256 + 8 * 256 * 64 * 52 * 4
     assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_FWD, 8, 256, 4096, 3, 4) == 0
     # rejected arguments size to 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, -1, 4, 4) == 0

@@ -536,23 +536,38 @@ cudaError_t launch_kv(const AffineParams& p, const AffinePlan& pl, cudaStream_t 
   return cudaGetLastError();
 }
 
+// (4, 4) and (2, 2) run the register kernel above; every other shape of the
+// envelope runs the column-thread kernel with streamed A (scan_affine_generic.cuh).
 template <int MODE>
 cudaError_t launch_affine(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
   if (p.k == 4 && p.v == 4) return launch_kv<4, 4, MODE>(p, pl, s);
   if (p.k == 2 && p.v == 2) return launch_kv<2, 2, MODE>(p, pl, s);
-  return cudaErrorInvalidValue;
+  switch (p.k) {
+    case 1: return launch_affine_generic_k1(p, MODE, s);
+    case 2: return launch_affine_generic_k2(p, MODE, s);
+    case 4: return launch_affine_generic_k4(p, MODE, s);
+    case 8: return launch_affine_generic_k8(p, MODE, s);
+    case 16:
+      return MODE == MODE_FWD ? launch_affine_generic_k16_fwd(p, s)
+                              : launch_affine_generic_k16_bwd(p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
+namespace {
+bool envelope(int x) { return x == 1 || x == 2 || x == 4 || x == 8 || x == 16; }
+}  // namespace
+
 int affine_record_floats(int k, int v) {
-  if (k == 4 && v == 4) return RecLayout<4, 4>::kFloats;
-  if (k == 2 && v == 2) return RecLayout<2, 2>::kFloats;
-  return 0;
+  if (!envelope(k) || !envelope(v)) return 0;
+  // P (k x k), Q (k x v), inclusive state (k x v), two flags, padded to 16 bytes
+  return ((k * k + 2 * k * v + 2) + 3) & ~3;
 }
 
 int affine_sub_chunks() { return kSub; }
-int affine_lanes_per_block(int v) { return 32 / v; }
+int affine_lanes_per_block(int k, int v) { return 32 / (k > v ? k : v); }
 
 cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
   return launch_affine<MODE_FWD>(p, pl, s);

@@ -128,7 +128,7 @@ scan_status plan_affine(int64_t B, int64_t T, int64_t N, int k, int v, const sca
   if (rec == 0) return SCAN_ERR_UNSUPPORTED;
   int Lc = o.chunk ? o.chunk : 64;
   if (Lc != 64 && Lc != 128 && Lc != 256) return SCAN_ERR_INVALID_ARG;
-  const int64_t lanes = affine_lanes_per_block(v);
+  const int64_t lanes = affine_lanes_per_block(k, v);
   const int64_t M = T > 0 ? (T + Lc - 1) / Lc : 0;
   const int64_t G = B * ((N + lanes - 1) / lanes);
   if (M * G > kMaxGrid) return SCAN_ERR_UNSUPPORTED;

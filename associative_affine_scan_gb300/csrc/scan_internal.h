@@ -167,10 +167,21 @@ struct AffinePlan {
   size_t ws_bytes;
 };
 
-// Floats per (lane, chunk) record for block shape (k, v); 0 if unsupported.
+// Floats per (lane, chunk) record for block shape (k, v); 0 if unsupported
+// (k, v in {1, 2, 4, 8, 16} are supported).
 int affine_record_floats(int k, int v);
 int affine_sub_chunks();
-int affine_lanes_per_block(int v);
+// state blocks (lanes) per warp: 32 / max(k, v) column threads
+int affine_lanes_per_block(int k, int v);
+
+// Kernels for the shapes the register kernel does not cover, one launcher
+// per k (mode: MODE_FWD or MODE_BWD).
+cudaError_t launch_affine_generic_k1(const AffineParams& p, int mode, cudaStream_t s);
+cudaError_t launch_affine_generic_k2(const AffineParams& p, int mode, cudaStream_t s);
+cudaError_t launch_affine_generic_k4(const AffineParams& p, int mode, cudaStream_t s);
+cudaError_t launch_affine_generic_k8(const AffineParams& p, int mode, cudaStream_t s);
+cudaError_t launch_affine_generic_k16_fwd(const AffineParams& p, cudaStream_t s);
+cudaError_t launch_affine_generic_k16_bwd(const AffineParams& p, cudaStream_t s);
 
 cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);
 cudaError_t launch_affine_bwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);

@@ -265,20 +265,31 @@ def run_ours(args, world, rank, local):
 
 
 def time_calls(fn, steps, warmup, flush, stream):
-    for _ in range(warmup):
-        flush.zero_()
+    """Mean device time of fn (a few C-ABI calls): warm up, capture fn once into a
+    CUDA graph on a dedicated stream, then time `steps` replays with CUDA events on
+    that stream, the L2 flushed before each (outside the event pair)."""
+    gs = torch.cuda.Stream(flush.device)
+    gs.wait_stream(stream)
+    with torch.cuda.stream(gs):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
         fn()
     torch.cuda.synchronize()
     total = 0.0
-    for _ in range(steps):
-        flush.zero_()
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        fn()
-        e.record(stream)
-        torch.cuda.synchronize()
-        total += s.elapsed_time(e)
+    with torch.cuda.stream(gs):
+        for _ in range(steps):
+            flush.zero_()
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(gs)
+            graph.replay()
+            e.record(gs)
+            torch.cuda.synchronize()
+            total += s.elapsed_time(e)
     return total / steps
 
 

@@ -238,7 +238,9 @@ scan_status scan_log_bwd(const float* log_a, const float* log_x, const float* h,
  * Kernel design): H_t = A_t H_{t-1} + B_t per (b, n) lane, H_{-1} = h0.
  * A: [B,T,N,k,k], Bm and H: [B,T,N,k,v], h0: nullable [B,N,k,v]; row-major
  * matrices; fp32, 16-byte aligned (else SCAN_ERR_ALIGNMENT). Supported
- * (k, v): (4, 4) and (2, 2); others return SCAN_ERR_UNSUPPORTED. */
+ * (k, v): k and v each in {1, 2, 4, 8, 16} ([TSK] Conformance envelope);
+ * others return SCAN_ERR_UNSUPPORTED. (4, 4) and (2, 2) run a kernel that
+ * keeps whole blocks in registers, every other shape one that streams A. */
 scan_status affine_scan_fwd(const float* A, const float* Bm, const float* h0,
                             float* H, int64_t B, int64_t T, int64_t N,
                             int32_t k, int32_t v, const scan_opts* opts,

@@ -82,6 +82,11 @@ def test_workspace_sizes():
     assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_FWD, 8, 256, 4096, 4, 4) == \
         256 + 8 * 256 * 64 * 52 * 4
     assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_FWD, 8, 256, 4096, 3, 4) == 0
+    # the rest of the envelope: k = 16, v = 1 records hold P (256), Q (16),
+    # the inclusive state (16) and 2 flags, padded to 292 floats
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_BWD, 8, 256, 4096, 16, 1) == \
+        256 + 8 * 256 * 64 * 292 * 4
+    assert scan.scan_workspace_bytes(scan.SCAN_OP_AFFINE_FWD, 1, 4, 64, 32, 1) == 0
     # rejected arguments size to 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, -1, 4, 4) == 0
     assert scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4, 4, opts={"chunk": 100}) == 0

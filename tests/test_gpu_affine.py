@@ -86,6 +86,38 @@ def test_affine_2x2(lib):
     run_and_check(lib, w)
 
 
+ENVELOPE = [(k, v) for k in (1, 2, 4, 8, 16) for v in (1, 2, 4, 8, 16)]
+
+
+@pytest.mark.parametrize("k,v", ENVELOPE)
+def test_affine_envelope(lib, k, v):
+    """Every block shape of the envelope, forward and backward, over several
+    chunks (T = 131 at 64-step chunks) and a partial group of lanes (N = 5)."""
+    w = workloads.affine(2, 131, 5, k, v, seed=17 * k + v, h0=True)
+    run_and_check(lib, w)
+
+
+@pytest.mark.parametrize("k,v", [(1, 16), (16, 1), (8, 2)])
+def test_affine_envelope_longer_chunks_and_no_h0(lib, k, v):
+    w = workloads.affine(1, 700, 9, k, v, seed=k + 100 * v, h0=False)
+    run_and_check(lib, w, {"chunk": 256})
+
+
+def test_affine_k1_is_the_scalar_scan(lib):
+    """k = v = 1 is h_t = a_t h_{t-1} + x_t: the same values as the scalar
+    forward on the same inputs (one lane per channel)."""
+    B, T, N = 2, 300, 7
+    g = torch.Generator().manual_seed(3)
+    a = torch.rand((B, T, N), generator=g)
+    x = torch.randn((B, T, N), generator=g)
+    H = lib.affine_scan_fwd(a.view(B, T, N, 1, 1).to(DEV), x.view(B, T, N, 1, 1).to(DEV))
+    h = lib.scan_fwd(a.permute(0, 2, 1).contiguous().to(DEV), x.permute(0, 2, 1).contiguous().to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.scan_fwd(a.permute(0, 2, 1).contiguous(), x.permute(0, 2, 1).contiguous())
+    assert rel_err(H.view(B, T, N).permute(0, 2, 1), ref) <= TOL
+    assert rel_err(h, ref) <= TOL
+
+
 def test_affine_golden_worked_example_bit_exact(lib):
     with open(os.path.join(HERE, "golden", "affine_2x2_dyadic.json")) as f:
         g = json.load(f)

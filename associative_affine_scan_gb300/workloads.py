@@ -125,6 +125,21 @@ def scalar_dense(B: int, C: int, T: int, seed: int = 0, *, gate: str = "uniform"
     return ScalarWorkload(name, a.to(dtype), x.to(dtype), dh, h0t)
 
 
+def dense_beyond_int32(device, seed: int = 0) -> ScalarWorkload:
+    """B=1, C=8200, T=262144 fp32 (2,149,580,800 elements, past 2^31): the
+    dense recipe of dense_4k (a~U(0,1), x~N(0,1), h0~N(0,1), dh~N(0,1)),
+    generated on `device` from a seeded generator of that device (34 GB of
+    fp32 inputs; rows 8192.. start beyond element 2^31)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    shape = (1, 8200, 262144)
+    a = torch.rand(shape, generator=g, device=device)
+    x = torch.randn(shape, generator=g, device=device)
+    h0t = torch.randn((1, 8200), generator=g, device=device)
+    dh = torch.randn(shape, generator=g, device=device)
+    return ScalarWorkload("dense_beyond_int32", a, x, dh, h0t)
+
+
 def single_sequence(seed: int = 0) -> ScalarWorkload:
     g = _gen(seed)
     C, T = 4, 128

@@ -446,6 +446,34 @@ def test_full_dense_64k_sampled_rows(lib):
 
 
 @pytest.mark.parametrize("variant", ["planner", "stream"])
+def test_beyond_int32_elements_sampled_rows(lib, variant):
+    """2^31 + 2,097,152 elements: every offset past element 2^31 needs 64-bit
+    indexing. Rows on both sides of the boundary against the oracle."""
+    if torch.cuda.get_device_properties(DEV).total_memory < (64 << 30):
+        pytest.skip("needs about 52 GB of device memory")
+    w = workloads.dense_beyond_int32(DEV, seed=0)
+    B, C, T = w.a.shape
+    assert B * C * T > 2 ** 31
+    opts = {"variant": lib.SCAN_VARIANT_STREAM} if variant == "stream" else None
+    h = lib.scan_fwd(w.a, w.x, w.h0, opts=opts)
+    da, dx, dh0 = lib.scan_bwd(w.a, h, w.dh, w.h0, opts=opts)
+    torch.cuda.synchronize()
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    first_past = 2 ** 31 // T  # 8192: the first row that starts past element 2^31
+    for r in (0, 1, first_past - 1, first_past, C - 2, C - 1):
+        ra, rx, rdh = (t[0, r][None, None].cpu() for t in (w.a, w.x, w.dh))
+        rh0 = w.h0[:, r:r + 1].cpu()
+        ref_h = oracle.scan_fwd(ra, rx, rh0)
+        ref_da, ref_dx, ref_dh0 = oracle.scan_bwd(ra, rx, rdh, rh0)
+        assert rel_err(h[0, r], ref_h[0, 0]) <= TOL32, r
+        assert rel_err(da[0, r], ref_da[0, 0]) <= TOL32, r
+        assert rel_err(dx[0, r], ref_dx[0, 0]) <= TOL32, r
+        assert rel_err(dh0[:, r], ref_dh0[:, 0]) <= TOL32, r
+    del h, da, dx, dh0, w
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", ["planner", "stream"])
 def test_full_packed_bidir_sampled_channels(lib, variant):
     w = workloads.packed_bidir(seed=0)
     g = cuda(w.af, w.xf, w.ar, w.xr, w.cu_seqlens, w.dhf, w.dhr)

@@ -38,6 +38,8 @@ from ._binding import (  # noqa: F401
     ScanError,
     ScanOpts,
     affine_scan_bwd,
+    affine_prefix_fwd,
+    affine_prefix_bwd,
     affine_scan_fwd,
     lib,
     scan_bidir_bwd,

@@ -49,7 +49,8 @@ SCAN_OP_LOG_BWD = 7
 EXPORTED = (
     "scan_status_string", "scan_version", "scan_workspace_bytes", "scan_workspace_init",
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
-    "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "scan_fwd_noalloc",
+    "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "affine_prefix_fwd",
+    "affine_prefix_bwd", "scan_fwd_noalloc",
 )
 
 
@@ -103,6 +104,9 @@ _SIGS = {
                         ctypes.c_int),
     "affine_scan_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _opt,
                          _vp, _sz, _vp], ctypes.c_int),
+    "affine_prefix_fwd": ([_vp, _vp, _i64, _i64, _i64, _i32, _opt, _vp, _sz, _vp], ctypes.c_int),
+    "affine_prefix_bwd": ([_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i32, _opt, _vp, _sz, _vp],
+                          ctypes.c_int),
     "scan_fwd_noalloc": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, ctypes.c_int, _i32,
                           _vp], ctypes.c_int),
 }
@@ -477,6 +481,44 @@ def affine_scan_bwd(A, H, dH, h0=None, *, out=None, opts=None, stream=None):
                                _ptr(dh0), B, T, N, k, v, _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "affine_scan_bwd")
     return dA, dB, dh0
+
+
+def affine_prefix_fwd(A, *, out=None, opts=None, stream=None):
+    """Abar_t = A_t A_{t-1} ... A_0 per lane. Returns Abar [B,T,N,k,k] (fp32)."""
+    _need(A, "A", dtype=torch.float32)
+    if A.dim() != 5 or A.shape[3] != A.shape[4]:
+        raise ValueError("affine_prefix_fwd expects A [B,T,N,k,k]")
+    dev = A.device
+    B, T, N, k, _ = A.shape
+    Abar = out if out is not None else torch.empty_like(A)
+    _need(Abar, "out", dtype=torch.float32, shape=A.shape, device=dev)
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_AFFINE_FWD, B, N, T, k, k, opts, dev, s)
+    st = lib().affine_prefix_fwd(_ptr(A), _ptr(Abar), B, T, N, k, _optref(o), _ptr(ws),
+                                 ws.numel(), s)
+    _check(st, "affine_prefix_fwd")
+    return Abar
+
+
+def affine_prefix_bwd(A, Abar, dAbar, dA=None, *, accumulate=False, opts=None, stream=None):
+    """Backward of L = sum <dAbar_t, Abar_t>: returns dA, written (or, with
+    accumulate=True, added into the given dA)."""
+    _need(A, "A", dtype=torch.float32)
+    dev = A.device
+    for t, name in ((Abar, "Abar"), (dAbar, "dAbar")):
+        _need(t, name, dtype=torch.float32, shape=A.shape, device=dev)
+    if dA is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs the dA to add into")
+        dA = torch.empty_like(A)
+    _need(dA, "dA", dtype=torch.float32, shape=A.shape, device=dev)
+    B, T, N, k, _ = A.shape
+    s = _stream(stream, dev)
+    ws, nb, o = workspace_for(SCAN_OP_AFFINE_BWD, B, N, T, k, k, opts, dev, s)
+    st = lib().affine_prefix_bwd(_ptr(A), _ptr(Abar), _ptr(dAbar), _ptr(dA), int(bool(accumulate)),
+                                 B, T, N, k, _optref(o), _ptr(ws), ws.numel(), s)
+    _check(st, "affine_prefix_bwd")
+    return dA
 
 
 def scan_fwd_noalloc(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None, stream=None):

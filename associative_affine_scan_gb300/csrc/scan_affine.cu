@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
   const uint32_t epoch = s_epoch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ln = lane / V, j = lane % V;  // lane in block, column
+  const bool zero_b = (p.flags & AFF_ZERO_B) != 0, eye_h0 = (p.flags & AFF_EYE_H0) != 0;
+  const bool acc_da = (p.flags & AFF_ACC_DA) != 0;
 
   if ((int64_t)ticket < p.ntiles) {
     const int k = (int)(ticket / (unsigned)p.G);
@@ -314,7 +316,8 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
           for (int q = 0; q < PB; ++q)
             if (t0 + q < t_hi) {
               ldv(p.A + blk(t0 + q) * KK, Ab[q], true);
-              load_col<K, V>(p.Bm + blk(t0 + q) * KV, j, Bb[q], true);
+              if (zero_b) fill(Bb[q], 0.f);
+              else load_col<K, V>(p.Bm + blk(t0 + q) * KV, j, Bb[q], true);
             }
 #pragma unroll
           for (int q = 0; q < PB; ++q)
@@ -370,7 +373,12 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
       fill(carry, 0.f);
       if (active) {
         if (k == 0) {
-          if (MODE == MODE_FWD && p.h0) load_col<K, V>(p.h0 + lane_id * KV, j, carry, false);
+          if (MODE == MODE_FWD && eye_h0) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) carry[i] = (i == j) ? 1.f : 0.f;
+          } else if (MODE == MODE_FWD && p.h0) {
+            load_col<K, V>(p.h0 + lane_id * KV, j, carry, false);
+          }
         } else {
           // column j of the chunk summary, sub-chunks in scan order
           float Pt[K], Qt[K];
@@ -443,7 +451,8 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
           for (int q = 0; q < PB; ++q)
             if (t0 + q < t_hi) {
               ldv(p.A + blk(t0 + q) * KK, Ab[q], false);
-              load_col<K, V>(p.Bm + blk(t0 + q) * KV, j, Bb[q], false);
+              if (zero_b) fill(Bb[q], 0.f);
+              else load_col<K, V>(p.Bm + blk(t0 + q) * KV, j, Bb[q], false);
             }
 #pragma unroll
           for (int q = 0; q < PB; ++q)
@@ -470,7 +479,10 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
             else fill(Ab[q], 0.f);
             load_col<K, V>(p.dH + blk(t) * KV, j, Db[q], false);
             if (t >= 1) load_col<K, V>(p.H + blk(t - 1) * KV, j, Hb[q], false);
-            else if (p.h0) load_col<K, V>(p.h0 + lane_id * KV, j, Hb[q], false);
+            else if (eye_h0) {
+#pragma unroll
+              for (int i = 0; i < K; ++i) Hb[q][i] = (i == j) ? 1.f : 0.f;
+            } else if (p.h0) load_col<K, V>(p.h0 + lane_id * KV, j, Hb[q], false);
             else fill(Hb[q], 0.f);
           } else {
             fill(Ab[q], 0.f);
@@ -492,10 +504,15 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
             for (int l = 0; l < K; ++l) D[i * K + l] = c[i] * Hb[q][l];
           reduce_scatter_rows<K, V>(D, j);
           if (work) {
-            store_col<K, V>(p.dB + blk(t) * KV, j, c);
+            if (p.dB) store_col<K, V>(p.dB + blk(t) * KV, j, c);
             float* row = p.dA + blk(t) * KK + j * K;
+            if (acc_da) {
 #pragma unroll
-            for (int l = 0; l < K; ++l) __stcs(row + l, D[l]);
+              for (int l = 0; l < K; ++l) row[l] += D[l];
+            } else {
+#pragma unroll
+              for (int l = 0; l < K; ++l) __stcs(row + l, D[l]);
+            }
             if (t == 0 && p.dh0) {
               float A0[KK], d0[K], z[K];
               ldv(p.A + blk(0) * KK, A0, false);

@@ -270,6 +270,8 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
   const uint32_t epoch = s_epoch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ln = lane / C, c = lane % C;  // lane (state block) in the warp, column
+  const bool zero_b = (p.flags & AFF_ZERO_B) != 0, eye_h0 = (p.flags & AFF_EYE_H0) != 0;
+  const bool acc_da = (p.flags & AFF_ACC_DA) != 0;
   const int LS = p.Lc / kSub;
 
   if ((int64_t)ticket < p.ntiles) {
@@ -299,7 +301,12 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
       if (MODE == MODE_FWD) {
         for (int64_t t = t_lo; t < t_hi; ++t) {
           float d[K];
-          ld_col<K, V>(p.Bm + blk(t) * KV, c, d);
+          if (zero_b) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) d[i] = 0.f;
+          } else {
+            ld_col<K, V>(p.Bm + blk(t) * KV, c, d);
+          }
           step_fwd<K>(p.A + blk(t) * KK, Pc, Qc, d);
         }
       } else {
@@ -339,7 +346,12 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
       for (int i = 0; i < K; ++i) carry[i] = 0.f;
       if (active) {
         if (k == 0) {
-          if (MODE == MODE_FWD && p.h0) ld_col<K, V>(p.h0 + lane_id * KV, c, carry);
+          if (MODE == MODE_FWD && eye_h0) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) carry[i] = (i == c && c < V) ? 1.f : 0.f;
+          } else if (MODE == MODE_FWD && p.h0) {
+            ld_col<K, V>(p.h0 + lane_id * KV, c, carry);
+          }
         } else {
           // column c of the chunk summary, sub-chunks in scan order
           float Pt[K], Qt[K];
@@ -411,7 +423,12 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
       if (work && c < V) {
         for (int64_t t = t_lo; t < t_hi; ++t) {
           float d[K];
-          ld_col<K, V>(p.Bm + blk(t) * KV, c, d);
+          if (zero_b) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) d[i] = 0.f;
+          } else {
+            ld_col<K, V>(p.Bm + blk(t) * KV, c, d);
+          }
           col_fwd<K>(p.A + blk(t) * KK, h, d);
           st_col<K, V>(p.out_H + blk(t) * KV, c, h);
         }
@@ -432,9 +449,12 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
 #pragma unroll
             for (int i = 0; i < K; ++i) h[i] = d[i];
           }
-          st_col<K, V>(p.dB + blk(t) * KV, c, h);
+          if (p.dB) st_col<K, V>(p.dB + blk(t) * KV, c, h);
           if (t >= 1) ld_col<K, V>(p.H + blk(t - 1) * KV, c, hp);
-          else if (p.h0) ld_col<K, V>(p.h0 + lane_id * KV, c, hp);
+          else if (eye_h0) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) hp[i] = (i == c) ? 1.f : 0.f;
+          } else if (p.h0) ld_col<K, V>(p.h0 + lane_id * KV, c, hp);
           if (t == 0 && p.dh0) {
             float d0[K], z[K];
 #pragma unroll
@@ -464,8 +484,13 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
             row[l] = acc;
           }
           float* dst = p.dA + blk(t) * KK + c * K;
+          if (acc_da) {
 #pragma unroll
-          for (int l = 0; l < K; ++l) __stcs(dst + l, row[l]);
+            for (int l = 0; l < K; ++l) dst[l] += row[l];
+          } else {
+#pragma unroll
+            for (int l = 0; l < K; ++l) __stcs(dst + l, row[l]);
+          }
         }
         __syncwarp();
       }

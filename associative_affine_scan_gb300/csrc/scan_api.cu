@@ -583,4 +583,42 @@ scan_status affine_scan_bwd(const float* A, const float* H, const float* dH, con
   return from_cuda(launch_affine_bwd(p, pl, stream));
 }
 
+scan_status affine_prefix_fwd(const float* A, float* Abar, int64_t B, int64_t T, int64_t N,
+                              int32_t k, const scan_opts* opts, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+  const scan_opts o = defaults(opts);
+  AffineParams p;
+  AffinePlan pl;
+  scan_status st = prepare_affine(B, T, N, k, k, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  if (B * T * N == 0) return SCAN_OK;
+  if (!A || !Abar) return SCAN_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(Abar, 16)) return SCAN_ERR_ALIGNMENT;
+  p.A = A;
+  p.out_H = Abar;
+  p.flags = AFF_ZERO_B | AFF_EYE_H0;
+  return from_cuda(launch_affine_fwd(p, pl, stream));
+}
+
+scan_status affine_prefix_bwd(const float* A, const float* Abar, const float* dAbar, float* dA,
+                              int32_t accumulate, int64_t B, int64_t T, int64_t N, int32_t k,
+                              const scan_opts* opts, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+  const scan_opts o = defaults(opts);
+  AffineParams p;
+  AffinePlan pl;
+  scan_status st = prepare_affine(B, T, N, k, k, o, ws, ws_bytes, &p, &pl);
+  if (st != SCAN_OK) return st;
+  if (B * T * N == 0) return SCAN_OK;
+  if (!A || !Abar || !dAbar || !dA) return SCAN_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(Abar, 16) || !aligned(dAbar, 16) || !aligned(dA, 16))
+    return SCAN_ERR_ALIGNMENT;
+  p.A = A;
+  p.H = Abar;
+  p.dH = dAbar;
+  p.dA = dA;
+  p.flags = AFF_EYE_H0 | (accumulate ? AFF_ACC_DA : 0);
+  return from_cuda(launch_affine_bwd(p, pl, stream));
+}
+
 }  // extern "C"

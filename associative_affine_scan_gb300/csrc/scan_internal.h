@@ -143,13 +143,14 @@ struct AffineParams {
   const float* Bm;
   const float* H;    // backward: forward output
   const float* dH;   // backward
-  const float* h0;
+  const float* h0;   // nullable; see flags
   float* out_H;      // forward output
   float* dA;
   float* dB;
   float* dh0;
   int64_t B, T, N;
   int k, v;
+  int flags;         // AFF_* below
   int Lc;            // time steps per chunk
   int M;             // chunks along T
   int G;             // lane groups = B * ceil(N / 32)
@@ -159,6 +160,13 @@ struct AffineParams {
   unsigned long long wait_limit_ns;
   int test_stall;
 };
+
+// AffineParams.flags. The coefficient prefix Abar_t = A_t ... A_0 is the same
+// scan with v = k, no injection and the identity as initial state; its
+// gradient adds into the dA of the state's backward.
+constexpr int AFF_ZERO_B = 1;   // Bm is absent: B_t = 0
+constexpr int AFF_EYE_H0 = 2;   // h0 = I (k = v); h0 pointer unused
+constexpr int AFF_ACC_DA = 4;   // backward adds into dA instead of writing it
 
 struct AffinePlan {
   int Lc;

@@ -257,6 +257,27 @@ scan_status affine_scan_bwd(const float* A, const float* H, const float* dH,
                             int32_t v, const scan_opts* opts, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
+/* Coefficient prefix of the block scan ([TSK] One associative-scan family:
+ * matrix_affine_scan composes the pairs (A, B) and returns the composed
+ * coefficient as well): Abar_t = A_t A_{t-1} ... A_0 per (b, n) lane, i.e. the
+ * block scan with v = k, B_t = 0 and h0 = I. A, Abar: [B,T,N,k,k] fp32,
+ * 16-byte aligned; k in {1, 2, 4, 8, 16}; workspace as affine_scan_fwd with
+ * v = k. */
+scan_status affine_prefix_fwd(const float* A, float* Abar, int64_t B, int64_t T,
+                              int64_t N, int32_t k, const scan_opts* opts,
+                              void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/* Backward of L = sum_t <dAbar_t, Abar_t>: G_t = dAbar_t + A_{t+1}^T G_{t+1},
+ * dA_t = G_t Abar_{t-1}^T (Abar_{-1} = I). Abar is affine_prefix_fwd's output.
+ * accumulate != 0 adds into dA (so a dA already written by affine_scan_bwd
+ * receives both gradient terms); otherwise dA is overwritten. */
+scan_status affine_prefix_bwd(const float* A, const float* Abar,
+                              const float* dAbar, float* dA, int32_t accumulate,
+                              int64_t B, int64_t T, int64_t N, int32_t k,
+                              const scan_opts* opts, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of the library's own scratch used by scan_fwd_noalloc (16 MiB). */
 #define SCAN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -118,6 +118,51 @@ def test_affine_k1_is_the_scalar_scan(lib):
     assert rel_err(h, ref) <= TOL
 
 
+def prefix_reference(A, dAbar):
+    """The coefficient prefix is the block scan with v = k, B = 0, h0 = I."""
+    B, T, N, k, _ = A.shape
+    zeros = torch.zeros_like(A)
+    eye = torch.eye(k).expand(B, N, k, k).contiguous()
+    ref = oracle.affine_fwd(A, zeros, eye)
+    ref_dA = oracle.affine_bwd(A, zeros, dAbar, eye)[0]
+    # term scale of dA_t = G_t Abar_{t-1}^T (module docstring)
+    G = np.maximum(1.0, np.abs(oracle.affine_bwd(A, zeros, dAbar, eye)[1]))
+    prev = np.empty_like(ref)
+    prev[:, 1:] = ref[:, :-1]
+    prev[:, 0] = np.asarray(eye.double())
+    scale = np.einsum("btnij,btnlj->btnil", G, np.maximum(1.0, np.abs(prev)))
+    return ref, ref_dA, scale
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 8, 16])
+def test_affine_prefix(lib, k):
+    w = workloads.affine(2, 150, 5, k, k, seed=31 + k)
+    dAbar = w.dH
+    Abar = lib.affine_prefix_fwd(w.A.to(DEV))
+    dA = lib.affine_prefix_bwd(w.A.to(DEV), Abar, dAbar.to(DEV))
+    torch.cuda.synchronize()
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    ref, ref_dA, scale = prefix_reference(w.A, dAbar)
+    assert rel_err(Abar, ref) <= TOL
+    assert rel_err(dA, ref_dA, scale) <= TOL
+
+
+def test_affine_prefix_gradient_accumulates(lib):
+    """accumulate=True adds the prefix's dA term to the state's dA. (The two
+    prefix backward runs compared here may differ by rounding: the look-back
+    composes whichever earlier records are already published.)"""
+    w = workloads.affine(1, 200, 9, 4, 4, seed=77, h0=True)
+    A, Bm, dH, h0 = w.A.to(DEV), w.Bm.to(DEV), w.dH.to(DEV), w.h0.to(DEV)
+    H = lib.affine_scan_fwd(A, Bm, h0)
+    dA_state, _, _ = lib.affine_scan_bwd(A, H, dH, h0)
+    Abar = lib.affine_prefix_fwd(A)
+    dAbar = torch.randn(A.shape, generator=torch.Generator().manual_seed(5)).to(DEV)
+    dA_prefix = lib.affine_prefix_bwd(A, Abar, dAbar)
+    both = lib.affine_prefix_bwd(A, Abar, dAbar, dA_state.clone(), accumulate=True)
+    torch.cuda.synchronize()
+    assert rel_err(both, (dA_state + dA_prefix).double().cpu().numpy()) <= TOL
+
+
 def test_affine_golden_worked_example_bit_exact(lib):
     with open(os.path.join(HERE, "golden", "affine_2x2_dyadic.json")) as f:
         g = json.load(f)

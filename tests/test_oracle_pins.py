@@ -459,3 +459,19 @@ def test_compose_identity_and_order():
     assert oracle.compose((3.0, 1.0), (0.5, 2.0)) == (1.5, 2.5)
     # a reset (P = 0) erases the earlier summary
     assert oracle.compose((0.7, -4.0), (0.0, 3.0)) == (0.0, 3.0)
+
+
+def test_affine_coefficient_prefix_is_the_product_of_gates():
+    """Abar_t = A_t ... A_0 ("Triton scan kernels", One associative-scan family:
+    the composed coefficient) equals the block scan with B = 0 and h0 = I;
+    checked against explicit numpy products, later factors on the left."""
+    g = np.random.default_rng(4)
+    B, T, N, k = 1, 6, 2, 3
+    A = g.standard_normal((B, T, N, k, k)) * 0.7
+    eye = np.broadcast_to(np.eye(k), (B, N, k, k)).copy()
+    got = oracle.affine_fwd(A, np.zeros_like(A), eye)
+    for n in range(N):
+        P = np.eye(k)
+        for t in range(T):
+            P = A[0, t, n] @ P
+            assert np.allclose(got[0, t, n], P, rtol=1e-13, atol=1e-13)

@@ -19,6 +19,9 @@ What each routine follows (page titles and sections of the source pages):
   backward (reverse scan with A_{t+1}^T).
 * ``chunk_summary`` / ``compose``: "Our RG-LRU GPU audit", Exact real chunk
   algebra.
+* ``gdn_fwd`` / ``gdn_bwd``: "Operations & Triton Kernels" (HyMo), The chunked
+  GDN algorithm (write h_t = alpha_t h_{t-1} + b_t v_t^T, read o_t = c_t . h_t)
+  and Mathematical Derivation of the Reverse-Time Backward Pass.
 """
 
 from __future__ import annotations
@@ -72,6 +75,9 @@ def _load():
                 "oracle_affine_fwd": [_dp, _dp, _dp, _dp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int],
                 "oracle_affine_bwd": [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
                                       ctypes.c_int, ctypes.c_int],
+                "oracle_gdn_fwd": [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64, _i64],
+                "oracle_gdn_bwd": [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                   _i64, _i64, _i64, _i64, _i64],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -198,6 +204,39 @@ def affine_bwd(A, Bm, dH, h0=None):
     if rc:
         raise ValueError("oracle_affine_bwd: malformed arguments")
     return dA, dB, dh0
+
+
+def gdn_fwd(alpha, b, v, c, h0=None):
+    """o_t = h_t^T c_t with h_t = alpha_t h_{t-1} + b_t v_t^T ("Operations & Triton
+    Kernels" (HyMo), The chunked GDN algorithm). alpha [B,H,T]; b, c [B,H,T,S];
+    v [B,H,T,D]; h0 [B,H,S,D] or None. Returns o [B,H,T,D]."""
+    alpha, b, v, c, h0 = _f64(alpha), _f64(b), _f64(v), _f64(c), _f64(h0)
+    B, H, T, S = b.shape
+    D = v.shape[-1]
+    o = np.empty((B, H, T, D), dtype=np.float64)
+    rc = _load().oracle_gdn_fwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(o),
+                                B, H, T, S, D)
+    if rc:
+        raise ValueError("oracle_gdn_fwd: malformed arguments")
+    return o
+
+
+def gdn_bwd(alpha, b, v, c, dout, h0=None):
+    """Gradients of L = sum <dout_t, o_t>: (dalpha, db, dv, dc, dh0) (the same
+    page, Mathematical Derivation of the Reverse-Time Backward Pass)."""
+    alpha, b, v, c, dout, h0 = _f64(alpha), _f64(b), _f64(v), _f64(c), _f64(dout), _f64(h0)
+    B, H, T, S = b.shape
+    D = v.shape[-1]
+    da = np.empty_like(alpha)
+    db = np.empty_like(b)
+    dv = np.empty_like(v)
+    dc = np.empty_like(c)
+    dh0 = np.empty((B, H, S, D), dtype=np.float64)
+    rc = _load().oracle_gdn_bwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(dout),
+                                _ptr(da), _ptr(db), _ptr(dv), _ptr(dc), _ptr(dh0), B, H, T, S, D)
+    if rc:
+        raise ValueError("oracle_gdn_bwd: malformed arguments")
+    return da, db, dv, dc, dh0
 
 
 def chunk_summary(a, x):

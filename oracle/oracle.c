@@ -379,3 +379,98 @@ void oracle_compose(double P1, double Q1, double P2, double Q2, double* P,
   *P = P2 * P1;
   *Q = P2 * Q1 + Q2;
 }
+
+/* "Operations & Triton Kernels" (HyMo), The chunked GDN algorithm: the write
+ * h_t = alpha_t h_{t-1} + b_t (outer) v_t and the read o_t = c_t . h_t, one
+ * step after the other for every (batch, head). */
+int oracle_gdn_fwd(const double* alpha, const double* b, const double* v,
+                   const double* c, const double* h0, double* o, int64_t B,
+                   int64_t H, int64_t T, int64_t S, int64_t D) {
+  if (!alpha || !b || !v || !c || !o || B < 0 || H < 0 || T < 0 || S < 1 || D < 1)
+    return -1;
+  double* h = (double*)malloc(sizeof(double) * (size_t)(S * D));
+  if (!h) return -1;
+  for (int64_t bh = 0; bh < B * H; ++bh) {
+    for (int64_t i = 0; i < S * D; ++i) h[i] = h0 ? h0[bh * S * D + i] : 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+      const int64_t st = bh * T + t;
+      const double al = alpha[st];
+      for (int64_t s = 0; s < S; ++s)
+        for (int64_t d = 0; d < D; ++d)
+          h[s * D + d] = al * h[s * D + d] + b[st * S + s] * v[st * D + d];
+      for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t s = 0; s < S; ++s) acc += c[st * S + s] * h[s * D + d];
+        o[st * D + d] = acc;
+      }
+    }
+  }
+  free(h);
+  return 0;
+}
+
+/* The same page, Mathematical Derivation of the Reverse-Time Backward Pass,
+ * with alpha itself as the gate input (its dalpha is the page's decay-gate
+ * gradient before the chain rule into the gate's parameters). The forward
+ * states are kept (this is the oracle: O(T S D) memory is fine). */
+int oracle_gdn_bwd(const double* alpha, const double* b, const double* v,
+                   const double* c, const double* h0, const double* dout,
+                   double* dalpha, double* db, double* dv, double* dc,
+                   double* dh0, int64_t B, int64_t H, int64_t T, int64_t S,
+                   int64_t D) {
+  if (!alpha || !b || !v || !c || !dout || !dalpha || !db || !dv || !dc || B < 0 ||
+      H < 0 || T < 0 || S < 1 || D < 1)
+    return -1;
+  const int64_t SD = S * D;
+  double* hs = (double*)malloc(sizeof(double) * (size_t)((T + 1) * SD));
+  double* dh = (double*)malloc(sizeof(double) * (size_t)SD);
+  if (!hs || !dh) {
+    free(hs);
+    free(dh);
+    return -1;
+  }
+  for (int64_t bh = 0; bh < B * H; ++bh) {
+    /* hs[0] = h_{-1}, hs[t + 1] = h_t */
+    for (int64_t i = 0; i < SD; ++i) hs[i] = h0 ? h0[bh * SD + i] : 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+      const int64_t st = bh * T + t;
+      for (int64_t s = 0; s < S; ++s)
+        for (int64_t d = 0; d < D; ++d)
+          hs[(t + 1) * SD + s * D + d] =
+              alpha[st] * hs[t * SD + s * D + d] + b[st * S + s] * v[st * D + d];
+    }
+    for (int64_t i = 0; i < SD; ++i) dh[i] = 0.0;
+    for (int64_t t = T - 1; t >= 0; --t) {
+      const int64_t st = bh * T + t;
+      const double* ht = hs + (t + 1) * SD;
+      const double* hp = hs + t * SD;
+      /* dh_t = c_t do_t^T + alpha_{t+1} dh_{t+1} */
+      const double an = (t + 1 < T) ? alpha[st + 1] : 0.0;
+      for (int64_t s = 0; s < S; ++s)
+        for (int64_t d = 0; d < D; ++d)
+          dh[s * D + d] = c[st * S + s] * dout[st * D + d] + an * dh[s * D + d];
+      for (int64_t s = 0; s < S; ++s) {
+        double acc_c = 0.0, acc_b = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+          acc_c += ht[s * D + d] * dout[st * D + d];
+          acc_b += dh[s * D + d] * v[st * D + d];
+        }
+        dc[st * S + s] = acc_c;
+        db[st * S + s] = acc_b;
+      }
+      for (int64_t d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t s = 0; s < S; ++s) acc += b[st * S + s] * dh[s * D + d];
+        dv[st * D + d] = acc;
+      }
+      double acc_a = 0.0;
+      for (int64_t i = 0; i < SD; ++i) acc_a += dh[i] * hp[i];
+      dalpha[st] = acc_a;
+    }
+    if (dh0)
+      for (int64_t i = 0; i < SD; ++i) dh0[bh * SD + i] = (T > 0 ? alpha[bh * T] : 0.0) * dh[i];
+  }
+  free(hs);
+  free(dh);
+  return 0;
+}

@@ -80,6 +80,26 @@ int oracle_affine_bwd(const double* A, const double* Bm, const double* h0,
                       const double* dH, double* dA, double* dB, double* dh0,
                       int64_t B, int64_t T, int64_t N, int k, int v);
 
+/* Scalar-gated outer-product state ("Operations & Triton Kernels" (HyMo),
+ * The chunked GDN algorithm): per (batch, head)
+ *   h_t = alpha_t h_{t-1} + b_t v_t^T   (S x D), h_{-1} = h0 (or 0)
+ *   o_t = h_t^T c_t                      (D)
+ * Layouts: alpha [B,H,T]; b, c [B,H,T,S]; v, o [B,H,T,D]; h0 [B,H,S,D]. */
+int oracle_gdn_fwd(const double* alpha, const double* b, const double* v,
+                   const double* c, const double* h0, double* o, int64_t B,
+                   int64_t H, int64_t T, int64_t S, int64_t D);
+
+/* Its backward for L = sum_t <do_t, o_t> (the same page, Mathematical
+ * Derivation of the Reverse-Time Backward Pass), with alpha as the gate
+ * input: dh_t = c_t do_t^T + alpha_{t+1} dh_{t+1}; dc_t = h_t do_t;
+ * dv_t = dh_t^T b_t; db_t = dh_t v_t; dalpha_t = sum(dh_t * h_{t-1});
+ * dh0 = alpha_0 dh_0. States from its own fp64 forward. */
+int oracle_gdn_bwd(const double* alpha, const double* b, const double* v,
+                   const double* c, const double* h0, const double* dout,
+                   double* dalpha, double* db, double* dv, double* dc,
+                   double* dh0, int64_t B, int64_t H, int64_t T, int64_t S,
+                   int64_t D);
+
 /* Chunk summary of n consecutive scalar steps, built left to right
  * (P <- a_t P, Q <- a_t Q + x_t from P = 1, Q = 0). */
 void oracle_chunk_summary(const double* a, const double* x, int64_t n,

@@ -475,3 +475,83 @@ def test_affine_coefficient_prefix_is_the_product_of_gates():
         for t in range(T):
             P = A[0, t, n] @ P
             assert np.allclose(got[0, t, n], P, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# scalar-gated outer-product state ("Operations & Triton Kernels" (HyMo))
+# ---------------------------------------------------------------------------
+
+def _gdn_inputs(g, B, H, T, S, D, dyadic=False):
+    if dyadic:
+        al = g.choice([0.0, 0.5, 1.0, 0.25], size=(B, H, T))
+        b = g.integers(-3, 4, size=(B, H, T, S)).astype(np.float64)
+        v = g.integers(-3, 4, size=(B, H, T, D)).astype(np.float64)
+        c = g.integers(-3, 4, size=(B, H, T, S)).astype(np.float64)
+        h0 = g.integers(-3, 4, size=(B, H, S, D)).astype(np.float64)
+    else:
+        al = g.random((B, H, T))
+        b, c = g.standard_normal((B, H, T, S)), g.standard_normal((B, H, T, S))
+        v, h0 = g.standard_normal((B, H, T, D)), g.standard_normal((B, H, S, D))
+    return al, b, v, c, h0
+
+
+def test_gdn_forward_exact_closed_form():
+    """h_t = (prod_{r<=t} alpha_r) h0 + sum_{u<=t} (prod_{u<r<=t} alpha_r) b_u v_u^T and
+    o_t = h_t^T c_t, in exact rational arithmetic (dyadic inputs: every fp64
+    partial result is exact, so the oracle must match bit for bit)."""
+    g = np.random.default_rng(11)
+    B, H, T, S, D = 1, 2, 5, 3, 2
+    al, b, v, c, h0 = _gdn_inputs(g, B, H, T, S, D, dyadic=True)
+    got = oracle.gdn_fwd(al, b, v, c, h0)
+    F = Fraction
+    for hh in range(H):
+        for t in range(T):
+            for d in range(D):
+                o = F(0)
+                for s_ in range(S):
+                    prod = F(1)
+                    for r in range(t + 1):
+                        prod *= F(al[0, hh, r])
+                    h = prod * F(h0[0, hh, s_, d])
+                    for u in range(t + 1):
+                        w = F(1)
+                        for r in range(u + 1, t + 1):
+                            w *= F(al[0, hh, r])
+                        h += w * F(b[0, hh, u, s_]) * F(v[0, hh, u, d])
+                    o += F(c[0, hh, t, s_]) * h
+                assert got[0, hh, t, d] == float(o)
+
+
+def test_gdn_with_one_by_one_state_is_the_scalar_scan():
+    """S = D = 1: h_t = alpha_t h_{t-1} + b_t v_t, o_t = c_t h_t."""
+    g = np.random.default_rng(12)
+    al, b, v, c, h0 = _gdn_inputs(g, 2, 3, 40, 1, 1)
+    got = oracle.gdn_fwd(al, b, v, c, h0)
+    h = oracle.scan_fwd(torch.tensor(al), torch.tensor(b[..., 0] * v[..., 0]),
+                        torch.tensor(h0[..., 0, 0]))
+    assert np.allclose(got[..., 0], c[..., 0] * np.asarray(h), rtol=1e-14, atol=1e-14)
+
+
+def test_gdn_backward_central_differences():
+    """L = sum <do, o> is linear in b, v, c and h0 separately (central differences
+    are exact up to rounding) and polynomial in alpha (O(eps^2))."""
+    g = np.random.default_rng(13)
+    B, H, T, S, D = 1, 2, 6, 3, 2
+    al, b, v, c, h0 = _gdn_inputs(g, B, H, T, S, D)
+    do = g.standard_normal((B, H, T, D))
+    dal, db, dv, dc, dh0 = oracle.gdn_bwd(al, b, v, c, do, h0)
+
+    def loss(al_, b_, v_, c_, h0_):
+        return float((oracle.gdn_fwd(al_, b_, v_, c_, h0_) * do).sum())
+
+    args = [al, b, v, c, h0]
+    for which, grad, eps, tol in ((0, dal, 1e-5, 1e-8), (1, db, 1e-3, 1e-9), (2, dv, 1e-3, 1e-9),
+                                  (3, dc, 1e-3, 1e-9), (4, dh0, 1e-3, 1e-9)):
+        x = args[which]
+        for idx in np.ndindex(x.shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            fd = (loss(*plus) - loss(*minus)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= tol * max(1.0, abs(fd)), (which, idx, fd, grad[idx])

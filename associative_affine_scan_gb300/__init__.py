@@ -40,6 +40,9 @@ from ._binding import (  # noqa: F401
     affine_scan_bwd,
     affine_prefix_fwd,
     affine_prefix_bwd,
+    gdn_checkpoint_bytes,
+    gdn_fwd,
+    gdn_bwd,
     affine_scan_fwd,
     lib,
     scan_bidir_bwd,

@@ -50,7 +50,7 @@ EXPORTED = (
     "scan_status_string", "scan_version", "scan_workspace_bytes", "scan_workspace_init",
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
     "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "affine_prefix_fwd",
-    "affine_prefix_bwd", "scan_fwd_noalloc",
+    "affine_prefix_bwd", "gdn_checkpoint_bytes", "gdn_fwd", "gdn_bwd", "scan_fwd_noalloc",
 )
 
 
@@ -105,6 +105,11 @@ _SIGS = {
     "affine_scan_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _opt,
                          _vp, _sz, _vp], ctypes.c_int),
     "affine_prefix_fwd": ([_vp, _vp, _i64, _i64, _i64, _i32, _opt, _vp, _sz, _vp], ctypes.c_int),
+    "gdn_checkpoint_bytes": ([_i64, _i64, _i64, _i64, _i64], ctypes.c_size_t),
+    "gdn_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp],
+                ctypes.c_int),
+    "gdn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                 _i64, _vp], ctypes.c_int),
     "affine_prefix_bwd": ([_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i32, _opt, _vp, _sz, _vp],
                           ctypes.c_int),
     "scan_fwd_noalloc": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, ctypes.c_int, _i32,
@@ -519,6 +524,61 @@ def affine_prefix_bwd(A, Abar, dAbar, dA=None, *, accumulate=False, opts=None, s
                                  B, T, N, k, _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "affine_prefix_bwd")
     return dA
+
+
+def gdn_checkpoint_bytes(B, H, T, S, D) -> int:
+    return int(lib().gdn_checkpoint_bytes(B, H, T, S, D))
+
+
+def _gdn_dims(alpha, b, v, c):
+    _need(alpha, "alpha", dtype=torch.float32)
+    if alpha.dim() != 3 or b.dim() != 4 or v.dim() != 4:
+        raise ValueError("gdn expects alpha [B,H,T], b, c [B,H,T,S], v [B,H,T,D]")
+    B, H, T = alpha.shape
+    S, D = b.shape[-1], v.shape[-1]
+    dev = alpha.device
+    _need(b, "b", dtype=torch.float32, shape=(B, H, T, S), device=dev)
+    _need(c, "c", dtype=torch.float32, shape=(B, H, T, S), device=dev)
+    _need(v, "v", dtype=torch.float32, shape=(B, H, T, D), device=dev)
+    return B, H, T, S, D
+
+
+def gdn_fwd(alpha, b, v, c, h0=None, *, checkpoints=True, out=None, stream=None):
+    """o_t = h_t^T c_t with h_t = alpha_t h_{t-1} + b_t v_t^T. Returns (o, ckpt),
+    ckpt being the backward's checkpoint buffer (None with checkpoints=False)."""
+    B, H, T, S, D = _gdn_dims(alpha, b, v, c)
+    dev = alpha.device
+    _need(h0, "h0", dtype=torch.float32, shape=(B, H, S, D), device=dev)
+    o = out if out is not None else torch.empty((B, H, T, D), dtype=torch.float32, device=dev)
+    _need(o, "out", dtype=torch.float32, shape=(B, H, T, D), device=dev)
+    ckpt = None
+    if checkpoints:
+        n = gdn_checkpoint_bytes(B, H, T, S, D) // 4
+        ckpt = torch.empty(max(n, 1), dtype=torch.float32, device=dev)
+    s = _stream(stream, dev)
+    st = lib().gdn_fwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(o), _ptr(ckpt),
+                       B, H, T, S, D, s)
+    _check(st, "gdn_fwd")
+    return o, ckpt
+
+
+def gdn_bwd(alpha, b, v, c, ckpt, dout, *, need_dh0=True, out=None, stream=None):
+    """Backward of L = sum <dout_t, o_t>: returns (dalpha, db, dv, dc, dh0)."""
+    B, H, T, S, D = _gdn_dims(alpha, b, v, c)
+    dev = alpha.device
+    _need(dout, "dout", dtype=torch.float32, shape=(B, H, T, D), device=dev)
+    if ckpt is None:
+        raise ValueError("gdn_bwd needs the forward's checkpoint buffer")
+    if out is not None:
+        dal, db, dv, dc, dh0 = out
+    else:
+        dal, db, dv, dc = (torch.empty_like(t) for t in (alpha, b, v, c))
+        dh0 = torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if need_dh0 else None
+    s = _stream(stream, dev)
+    st = lib().gdn_bwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(ckpt), _ptr(dout), _ptr(dal),
+                       _ptr(db), _ptr(dv), _ptr(dc), _ptr(dh0), B, H, T, S, D, s)
+    _check(st, "gdn_bwd")
+    return dal, db, dv, dc, dh0
 
 
 def scan_fwd_noalloc(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None, stream=None):

@@ -217,6 +217,43 @@ def affine_4x4(seed: int = 0, scale: int = 1) -> AffineWorkload:
     return affine(8, 4096 // scale, 256, 4, 4, seed, name="affine_4x4")
 
 
+@dataclass
+class GdnWorkload:
+    name: str
+    alpha: torch.Tensor  # [B,H,T]
+    b: torch.Tensor      # [B,H,T,S]
+    v: torch.Tensor      # [B,H,T,D]
+    c: torch.Tensor      # [B,H,T,S]
+    dout: torch.Tensor   # [B,H,T,D]
+    h0: Optional[torch.Tensor] = None  # [B,H,S,D]
+
+    @property
+    def n_steps(self) -> int:
+        return self.alpha.numel()
+
+
+def gdn(B: int, H: int, T: int, S: int, D: int, seed: int = 0, *, h0: bool = False,
+        name: str = "gdn") -> GdnWorkload:
+    """Scalar-gated outer-product state inputs: gates alpha = sigmoid(z),
+    z~N(3,1) (decays near 1), keys b, c ~ N(0,1)/sqrt(S), values v ~ N(0,1),
+    upstream gradient dout ~ N(0,1), optional h0 ~ N(0,1); fp32, drawn in
+    that order from one CPU generator."""
+    g = _gen(seed)
+    alpha = torch.sigmoid(torch.randn((B, H, T), generator=g) + 3.0)
+    b = torch.randn((B, H, T, S), generator=g) / S ** 0.5
+    v = torch.randn((B, H, T, D), generator=g)
+    c = torch.randn((B, H, T, S), generator=g) / S ** 0.5
+    dout = torch.randn((B, H, T, D), generator=g)
+    h0t = torch.randn((B, H, S, D), generator=g) if h0 else None
+    return GdnWorkload(name, alpha, b, v, c, dout, h0t)
+
+
+def gdn_4k(seed: int = 0) -> GdnWorkload:
+    """8 batches x 32 heads x 4096 steps, (S, D) = (32, 32): the state shape
+    and chunked T of the GDN page's worked setting."""
+    return gdn(8, 32, 4096, 32, 32, seed, name="gdn_4k")
+
+
 def log_dense(B: int, C: int, T: int, seed: int = 0, *, h0: bool = False,
               name: str = "log") -> LogWorkload:
     g = _gen(seed)

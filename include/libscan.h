@@ -22,6 +22,8 @@
  *          scan_bidirectional_branched, cu_seqlens), how it works (chunked
  *          scan, no cross-document leakage, backward by a reverse scan on
  *          shifted gates with d_gates = shifted_states * d_tokens).
+ *   [GDN]  "Operations & Triton Kernels" (HyMo): The chunked GDN algorithm;
+ *          Mathematical Derivation of the Reverse-Time Backward Pass.
  *   [RGA]  "Our RG-LRU GPU audit": Strengthened fused path (resets, nonzero
  *          initial state and its gradient, partial final chunks), Exact real
  *          chunk algebra (h_out = P h_in + Q).
@@ -277,6 +279,36 @@ scan_status affine_prefix_bwd(const float* A, const float* Abar,
                               int64_t B, int64_t T, int64_t N, int32_t k,
                               const scan_opts* opts, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
+
+/* Scalar-gated outer-product state ([GDN] The chunked GDN algorithm), per
+ * (batch, head):  h_t = alpha_t h_{t-1} + b_t v_t^T (S x D),  h_{-1} = h0,
+ *                 o_t = h_t^T c_t (a D-vector).
+ * Layouts (fp32, T-major within a head): alpha [B,H,T]; b, c [B,H,T,S];
+ * v, o [B,H,T,D]; h0 nullable [B,H,S,D] (0 when NULL). S, D in {16, 32}
+ * (else SCAN_ERR_UNSUPPORTED); b, c, v, o, h0, ckpt 16-byte aligned (else
+ * SCAN_ERR_ALIGNMENT). ckpt (nullable): gdn_checkpoint_bytes() bytes, filled
+ * with the state before every 64th step, [B,H,ceil(T/64),S,D]; the backward
+ * starts from it. No workspace; asynchronous on `stream`. */
+size_t gdn_checkpoint_bytes(int64_t B, int64_t H, int64_t T, int64_t S,
+                            int64_t D);
+scan_status gdn_fwd(const float* alpha, const float* b, const float* v,
+                    const float* c, const float* h0, float* o, float* ckpt,
+                    int64_t B, int64_t H, int64_t T, int64_t S, int64_t D,
+                    cudaStream_t stream);
+
+/* Its backward for L = sum_t <dout_t, o_t> ([GDN] Mathematical Derivation of
+ * the Reverse-Time Backward Pass, with alpha itself as the gate input):
+ *   dh_t = c_t dout_t^T + alpha_{t+1} dh_{t+1},   dc_t = h_t dout_t,
+ *   dv_t = dh_t^T b_t,  db_t = dh_t v_t,  dalpha_t = <dh_t, h_{t-1}>,
+ *   dh0 = alpha_0 dh_0 (nullable).
+ * ckpt is the forward's checkpoint buffer (for the same inputs and h0); the
+ * states in between are recomputed, none is stored. Outputs in the layouts of
+ * the corresponding inputs. */
+scan_status gdn_bwd(const float* alpha, const float* b, const float* v,
+                    const float* c, const float* ckpt, const float* dout,
+                    float* dalpha, float* db, float* dv, float* dc, float* dh0,
+                    int64_t B, int64_t H, int64_t T, int64_t S, int64_t D,
+                    cudaStream_t stream);
 
 /* Bytes of the library's own scratch used by scan_fwd_noalloc (16 MiB). */
 #define SCAN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

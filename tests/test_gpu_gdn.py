@@ -1,0 +1,104 @@
+"""GPU parity of the scalar-gated outer-product state against the fp64 oracle.
+
+h_t = alpha_t h_{t-1} + b_t v_t^T, o_t = h_t^T c_t per (batch, head), and the
+reverse-time backward ("Operations & Triton Kernels" (HyMo): The chunked GDN
+algorithm; Mathematical Derivation of the Reverse-Time Backward Pass), through
+the C ABI.
+
+Tolerance, fp32: o, dv, db, dc and dh0 are sums over S or D products of fp32
+values, dalpha a sum over S * D; each error is normalised by the sum of the
+absolute values of its terms, which the oracle computes by running on
+|alpha|, |b|, |v|, |c|, |h0|, |dout| (every term becomes its absolute value),
+and must stay within 1e-5 of it (or of max(1, |ref|), whichever is larger).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from associative_affine_scan_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+DEV = torch.device("cuda", 0)
+
+
+def err(got, ref, scale):
+    got = got.detach().double().cpu().numpy()
+    den = np.maximum(np.maximum(1.0, np.abs(ref)), scale)
+    return 0.0 if got.size == 0 else float(np.max(np.abs(got - ref) / den))
+
+
+def check(lib, w):
+    alpha, b, v, c, dout = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout))
+    h0 = w.h0.to(DEV) if w.h0 is not None else None
+    o, ck = lib.gdn_fwd(alpha, b, v, c, h0)
+    g = lib.gdn_bwd(alpha, b, v, c, ck, dout)
+    torch.cuda.synchronize()
+    ref_o = oracle.gdn_fwd(w.alpha, w.b, w.v, w.c, w.h0)
+    ref_g = oracle.gdn_bwd(w.alpha, w.b, w.v, w.c, w.dout, w.h0)
+    ab = lambda t: None if t is None else t.abs()
+    sc_o = oracle.gdn_fwd(ab(w.alpha), ab(w.b), ab(w.v), ab(w.c), ab(w.h0))
+    sc_g = oracle.gdn_bwd(ab(w.alpha), ab(w.b), ab(w.v), ab(w.c), ab(w.dout), ab(w.h0))
+    errs = {"o": err(o, ref_o, sc_o)}
+    for name, got, ref, sc in zip(("dalpha", "db", "dv", "dc", "dh0"), g, ref_g, sc_g):
+        errs[name] = err(got, ref, sc)
+    assert max(errs.values()) <= TOL, errs
+
+
+@pytest.mark.parametrize("S,D", [(16, 16), (16, 32), (32, 16), (32, 32)])
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 63, 64, 65, 130, 257])
+def test_gdn_shapes(lib, S, D, T):
+    for h0 in (True, False):
+        w = workloads.gdn(2, 3, T, S, D, seed=T * 7 + S + D + h0, h0=h0)
+        check(lib, w)
+
+
+def test_gdn_with_one_by_one_state_matches_the_scalar_scan(lib):
+    """Identity through the reduction: with b_t = e_0, c_t = e_0 and v_t = x_t e_0,
+    o_t[0] is the scalar scan h_t = alpha_t h_{t-1} + x_t."""
+    B, H, T, S, D = 1, 4, 300, 16, 16
+    g = torch.Generator().manual_seed(8)
+    alpha = torch.rand((B, H, T), generator=g)
+    x = torch.randn((B, H, T), generator=g)
+    b = torch.zeros(B, H, T, S)
+    b[..., 0] = 1.0
+    c = b.clone()
+    v = torch.zeros(B, H, T, D)
+    v[..., 0] = x
+    o, _ = lib.gdn_fwd(alpha.to(DEV), b.to(DEV), v.to(DEV), c.to(DEV), checkpoints=False)
+    torch.cuda.synchronize()
+    ref = oracle.scan_fwd(alpha.view(1, B * H, T), x.view(1, B * H, T))
+    assert np.allclose(o[..., 0].cpu().double().numpy().reshape(1, B * H, T), ref,
+                       rtol=1e-5, atol=1e-6)
+
+
+def test_gdn_rejects_unsupported_shapes(lib):
+    a = torch.rand(1, 1, 8, device=DEV)
+    b = torch.zeros(1, 1, 8, 8, device=DEV)
+    with pytest.raises(lib.ScanError) as e:
+        lib.gdn_fwd(a, b, b, b)
+    assert e.value.status == lib.SCAN_ERR_UNSUPPORTED
+
+
+def test_gdn_4k_sampled_heads(lib):
+    """The bench workload (8 x 32 heads x 4096 steps, 32 x 32 state), every
+    output of 6 sampled heads against the oracle."""
+    w = workloads.gdn_4k(seed=0)
+    alpha, b, v, c, dout = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout))
+    o, ck = lib.gdn_fwd(alpha, b, v, c)
+    dal, db, dv, dc, dh0 = lib.gdn_bwd(alpha, b, v, c, ck, dout)
+    torch.cuda.synchronize()
+    for bb, hh in ((0, 0), (0, 31), (3, 7), (5, 20), (7, 0), (7, 31)):
+        sl = lambda t: t[bb:bb + 1, hh:hh + 1]
+        ins = [sl(t) for t in (w.alpha, w.b, w.v, w.c)]
+        ref_o = oracle.gdn_fwd(*ins)
+        ref_g = oracle.gdn_bwd(*ins, sl(w.dout))
+        absin = [t.abs() for t in ins]
+        sc_o = oracle.gdn_fwd(*absin)
+        sc_g = oracle.gdn_bwd(*absin, sl(w.dout).abs())
+        assert err(sl(o), ref_o, sc_o) <= TOL, (bb, hh)
+        for got, ref, sc in zip((sl(dal), sl(db), sl(dv), sl(dc), sl(dh0)), ref_g, sc_g):
+            assert err(got, ref, sc) <= TOL, (bb, hh)

@@ -545,15 +545,21 @@ def _gdn_dims(alpha, b, v, c):
 
 def gdn_fwd(alpha, b, v, c, h0=None, *, checkpoints=True, out=None, stream=None):
     """o_t = h_t^T c_t with h_t = alpha_t h_{t-1} + b_t v_t^T. Returns (o, ckpt),
-    ckpt being the backward's checkpoint buffer (None with checkpoints=False)."""
+    ckpt being the backward's checkpoint buffer: allocated (checkpoints=True),
+    the given fp32 tensor of gdn_checkpoint_bytes() bytes, or None (False)."""
     B, H, T, S, D = _gdn_dims(alpha, b, v, c)
     dev = alpha.device
     _need(h0, "h0", dtype=torch.float32, shape=(B, H, S, D), device=dev)
     o = out if out is not None else torch.empty((B, H, T, D), dtype=torch.float32, device=dev)
     _need(o, "out", dtype=torch.float32, shape=(B, H, T, D), device=dev)
     ckpt = None
-    if checkpoints:
-        n = gdn_checkpoint_bytes(B, H, T, S, D) // 4
+    n = gdn_checkpoint_bytes(B, H, T, S, D) // 4
+    if isinstance(checkpoints, torch.Tensor):
+        ckpt = checkpoints
+        _need(ckpt, "checkpoints", dtype=torch.float32, device=dev)
+        if ckpt.numel() < n or not ckpt.is_contiguous():
+            raise ValueError(f"checkpoints: needs {n} contiguous floats")
+    elif checkpoints:
         ckpt = torch.empty(max(n, 1), dtype=torch.float32, device=dev)
     s = _stream(stream, dev)
     st = lib().gdn_fwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(o), _ptr(ckpt),

@@ -293,7 +293,7 @@ def time_calls(fn, steps, warmup, flush, stream):
     return total / steps
 
 
-ROWS = ("packed_bidir", "log_4k", "affine_4x4")
+ROWS = ("packed_bidir", "log_4k", "affine_4x4", "gdn_4k")
 
 
 def measure_rows(args, dev, scan, names=ROWS, small=False):
@@ -313,7 +313,30 @@ def measure_rows(args, dev, scan, names=ROWS, small=False):
         out["log_4k"] = _row_log(scan, workloads, dev, steps, warm, flush, stream, peak)
     if "affine_4x4" in names:
         out["affine_4x4"] = _row_affine(scan, workloads, dev, steps, warm, flush, stream)
+    if "gdn_4k" in names:
+        out["gdn_4k"] = _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak)
     return out
+
+
+def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
+    # per (head, step), S = D = 32: fwd reads alpha, b, c (S), v (D) and writes
+    # o (D) plus a 4 KB checkpoint every 64 steps; bwd reads alpha, b, c, v,
+    # dout and the checkpoints and writes dalpha, db, dc, dv
+    w = workloads.gdn_4k(seed=0)
+    alpha, b, v, c, dout = (t.to(dev) for t in (w.alpha, w.b, w.v, w.c, w.dout))
+    S, D = b.shape[-1], v.shape[-1]
+    o, ck = scan.gdn_fwd(alpha, b, v, c)
+    n = alpha.numel()
+    f_bytes = n * (4 + 8 * S + 8 * D) + ck.numel() * 4
+    b_bytes = n * (8 + 16 * S + 16 * D) + ck.numel() * 4
+    f_ms = time_calls(lambda: scan.gdn_fwd(alpha, b, v, c, checkpoints=ck, out=o), steps, warm,
+                      flush, stream)
+    g = scan.gdn_bwd(alpha, b, v, c, ck, dout)
+    b_ms = time_calls(lambda: scan.gdn_bwd(alpha, b, v, c, ck, dout, out=g), steps, warm, flush,
+                      stream)
+    return {"head_steps": n, "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_gbs": f_bytes / f_ms / 1e6, "bwd_gbs": b_bytes / b_ms / 1e6,
+            "fwd_frac": f_bytes / f_ms / 1e6 / peak, "bwd_frac": b_bytes / b_ms / 1e6 / peak}
 
 
 def _row_packed(scan, workloads, dev, steps, warm, flush, stream, small):

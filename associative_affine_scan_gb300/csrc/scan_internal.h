@@ -61,6 +61,10 @@ struct alignas(64) WsHeader {
   unsigned int done;
   unsigned int status;
   unsigned int info[4];  // where a wait expired: tile ticket, branch, row, scan index
+  // two-branch stationary launches: row-group tickets per branch, and the
+  // count of finished blocks (the last one resets all three)
+  unsigned int branch_ticket[2];
+  unsigned int branch_done;
 };
 
 constexpr size_t kWsHeaderBytes = 256;  // records start here

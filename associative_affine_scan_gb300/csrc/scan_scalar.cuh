@@ -1418,8 +1418,31 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
       }
     }
   } else if (VARIANT == VAR_STATIONARY) {
-    const int g = blockIdx.x / p.nbr;
-    const int brn = blockIdx.x % p.nbr;
+    // Two branches scan in opposite directions, each through its own copy of
+    // the chunk code, and SM pairs (smid 2i, 2i + 1) running both keep twice
+    // the code hot. A block takes a row group of the branch matching its SM
+    // pair's parity (the other branch once that one is used up: 2 G blocks
+    // always find 2 G groups), so an SM pair mostly runs one direction
+    // (measured: packed bidirectional backward 3.75 -> 3.31 ms; keying on the
+    // SM's own parity instead gained nothing).
+    __shared__ int s_g, s_brn;
+    if (p.nbr == 2) {
+      if (threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        int b = (int)((smid >> 1) & 1u);
+        unsigned tk = atomicAdd(&p.hdr->branch_ticket[b], 1u);
+        if (tk >= (unsigned)p.G) {
+          b ^= 1;
+          tk = atomicAdd(&p.hdr->branch_ticket[b], 1u);
+        }
+        s_g = (int)tk;
+        s_brn = b;
+      }
+      __syncthreads();
+    }
+    const int g = p.nbr == 2 ? s_g : blockIdx.x / p.nbr;
+    const int brn = p.nbr == 2 ? s_brn : blockIdx.x % p.nbr;
     const int64_t row = (int64_t)g * p.R + warp;
     if (VARLEN && blockIdx.x == 0) check_segments<MODE>(p);
     float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
@@ -1436,6 +1459,18 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
       else
         chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
                                                 &hint, NoRelease(), ap, next);
+    }
+    if (p.nbr == 2) {
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const unsigned d = atomicAdd(&p.hdr->branch_done, 1u);
+        if (d == gridDim.x - 1) {  // every block has taken its ticket and finished
+          p.hdr->branch_ticket[0] = 0u;
+          p.hdr->branch_ticket[1] = 0u;
+          p.hdr->branch_done = 0u;
+          __threadfence();
+        }
+      }
     }
   } else {
     // VAR_SEGMENTED: a row is cut into nseg segments of cps chunks, taken in

@@ -209,6 +209,9 @@ struct LinOp {
     return fmaf(a, h0 ? h0[i] : 0.f, x);
   }
   static __device__ __forceinline__ float out(float h) { return h; }
+  // the carried state of the second lane pass is h itself
+  using PState = float;
+  static __device__ __forceinline__ PState enter(const E& ex, float c) { return fmaf(ex.p, c, ex.q); }
   static __device__ __forceinline__ float value(const E& e, float c) { return fmaf(e.p, c, e.q); }
   static __device__ __forceinline__ float carry_after(const E& e, float c) { return fmaf(e.p, c, e.q); }
   static __device__ __forceinline__ bool is_const(const E& e) { return e.p == 0.f; }
@@ -269,13 +272,30 @@ struct LogOp {
     return r;
   }
   static __device__ __forceinline__ float initial_carry() { return -CUDART_INF_F; }
-  static __device__ __forceinline__ float step(float l, float la, float lx) {
-    return log_add_exp(l + la, lx);
+  // The second lane pass carries l_t as a max-shifted pair: l = m + log(s),
+  // s >= 1 (or m = -inf). A step folds in exp(log a + l) and exp(log x) with
+  // one exponential, the output exp(l) = s exp(m) costs one more; no
+  // logarithm is taken along the run.
+  struct PState {
+    float m, s;
+  };
+  static __device__ __forceinline__ PState enter(const E& ex, float c) {
+    const E e = compose(from_inc(c), ex);
+    return {e.m, e.s};
   }
-  static __device__ __forceinline__ float first(float la, float lx, const float* lh0, int64_t i) {
-    return lh0 ? log_add_exp(lh0[i] + la, lx) : lx;
+  static __device__ __forceinline__ PState step(const PState& st, float la, float lx) {
+    const float u = st.m + la;  // the carried mass, shifted
+    const float d = u - lx;     // NaN only when both are -inf
+    float ex = __expf(-fabsf(d));
+    if (d != d) ex = 0.f;
+    const bool up = u > lx;
+    return {up ? u : lx, up ? st.s + ex : fmaf(st.s, ex, 1.f)};
   }
-  static __device__ __forceinline__ float out(float l) { return __expf(l); }
+  static __device__ __forceinline__ PState first(float la, float lx, const float* lh0, int64_t i) {
+    const E e = make_first(la, lx, lh0, i);
+    return {e.m, e.s};
+  }
+  static __device__ __forceinline__ float out(const PState& st) { return st.s * __expf(st.m); }
   // linear-space output exp(l_t) for the carry-in log state c
   static __device__ __forceinline__ float value(const E& e, float c) {
     return __expf(c + e.a) + e.s * __expf(e.m);
@@ -1002,7 +1022,7 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
 
   // ---- pass 2: the recurrence over the run from its carry-in; X[e] becomes
   // the output (h_t forward, the adjoint g_t = dL/dx_t backward) ----
-  float st = Op::carry_after(ex, c);
+  typename Op::PState st = Op::enter(ex, c);
   if (plain) {
 #pragma unroll
     for (int ii = 0; ii < V; ++ii) {

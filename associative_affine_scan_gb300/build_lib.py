@@ -17,6 +17,12 @@ LIB = os.path.join(HERE, "libscan.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
+# Per-unit extras. The log-space forward spends most of its issue slots on
+# exponentials of the max-shifted log-sum-exp; with subnormals flushed to zero
+# __expf needs no rescaling around the special-function unit (a subnormal
+# exponential only ever adds to a sum of at least one, or is an output below
+# 1e-38). Measured 10 % faster on the 8 x 1536 x 4096 log forward.
+UNIT_FLAGS = {"scan_log_fwd.cu": ["-ftz=true"]}
 
 
 def nvcc() -> str:
@@ -51,13 +57,13 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     for src in srcs:
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        if _stale(obj, [src] + hdrs):
+        if _stale(obj, [src, os.path.abspath(__file__)] + hdrs):
             todo.append((src, obj))
 
     def compile_one(item):
         src, obj = item
         tmp = obj + f".tmp{os.getpid()}"
-        cmd = [cc, *ARCH, *FLAGS, "-c", src, "-o", tmp]
+        cmd = [cc, *ARCH, *FLAGS, *UNIT_FLAGS.get(os.path.basename(src), []), "-c", src, "-o", tmp]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

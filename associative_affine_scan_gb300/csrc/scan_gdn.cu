@@ -32,7 +32,6 @@ namespace {
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kStage = 32;  // forward: steps per staged block
 constexpr int kCoarse = 64;  // checkpoint interval
-constexpr int kFine = 8;     // backward: states recomputed at a time
 
 struct GdnParams {
   const float* alpha;  // [B,H,T]
@@ -48,6 +47,8 @@ struct GdnParams {
   float* dv;
   float* dc;
   float* dh0;          // nullable
+  float* wsS;          // backward workspace: [B,H,NC,S,D] chunk adjoints
+  float* wsG;          // [B,H,NC] gate product of each chunk
   int64_t BH, T;
   int64_t NC;
 };
@@ -180,212 +181,601 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
   }
 }
 
-// Sum of RS per-lane values over the CW column lanes of a warp (lane bits
-// below CW), scattered by recursive halving: afterwards lane j (j = lane % CW
-// < RS) holds the total of value j.
-template <int RS, int CW>
-__device__ __forceinline__ float reduce_scatter_cols(float (&x)[RS], int lane) {
-#pragma unroll
-  for (int m = RS / 2; m >= 1; m >>= 1) {
-    const bool hi = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < m; ++i) {
-      const float send = hi ? x[i] : x[i + m];
-      const float keep = hi ? x[i + m] : x[i];
-      x[i] = keep + __shfl_xor_sync(kFullMask, send, m);
-    }
-  }
-  float v = x[0];
-#pragma unroll
-  for (int m = RS; m < CW; m <<= 1) v += __shfl_xor_sync(kFullMask, v, m);  // remaining column bits
-  return v;
-}
+// ---------------------------------------------------------------------------
+// Backward, chunked over T ("Operations & Triton Kernels" (HyMo), The chunked
+// GDN algorithm, applied to the reverse-time pass). Within a chunk of n <= 64
+// steps starting from H_in (the checkpoint) and with G_out, the adjoint of the
+// state after the chunk (gradients from later chunks only):
+//   Gamma_t = alpha_0 .. alpha_t,  D[t][tau] = alpha_{tau+1} .. alpha_t (tau <= t)
+//   dh_t   = sum_{t' >= t} D[t'][t] c_t' dout_t'^T + D[n-1][t] G_out
+//   G_in   = sum_t Gamma_t c_t dout_t^T + Gamma_{n-1} G_out      (adjoint of H_in)
+// and, with CB[t][tau] = c_t.b_tau, DoV[t][tau] = dout_t.v_tau, P = D o CB,
+// dS = D o DoV (elementwise, zero above the diagonal), w_tau = D[n-1][tau]:
+//   db_tau = sum_t dS[t][tau] c_t + w_tau G_out v_tau
+//   dv_tau = sum_t P[t][tau] dout_t + w_tau G_out^T b_tau
+//   dc_t   = sum_tau dS[t][tau] b_tau + Gamma_t H_in dout_t
+//   dalpha_r = <dh_r, h_{r-1}>
+//            = sum_{t >= r} D[t][r] (Gamma_{r-1} z_t + Y[t][r])
+//              + w_r (Gamma_{r-1} <G_out, H_in> + y_r),
+//   z_t = c_t^T H_in dout_t, Y[t][r] = sum_{tau < r} D[r-1][tau] CB[t][tau] DoV[t][tau],
+//   y_r = sum_{tau < r} D[r-1][tau] b_tau^T G_out v_tau
+// (all products of gates, no division, so a gate of 0 is exact). Three
+// launches: (1) per chunk, V = sum_t Gamma_t c_t dout_t^T and Gamma_{n-1};
+// (2) per head, G_in = V + Gamma_{n-1} G_out from the last chunk to the first,
+// leaving each chunk's G_out in the workspace and dh0 = G_in of chunk 0;
+// (3) per chunk, the gradients above as small GEMMs in shared memory.
+// ---------------------------------------------------------------------------
 
-// Shared memory of the backward, in floats: a 64-step block's inputs, the
-// state before each 8-step piece (per thread), and two buffers of per-warp
-// partial sums for the 8 steps of a piece.
-template <int S, int D, int CW_>
-struct BwdSmem {
-  using LY = Layout<S, D, CW_>;
-  static constexpr int RED = 2 * S + LY::RG;  // db, dc, and dalpha per row group
-  static constexpr int b = 0;
-  static constexpr int c = b + kCoarse * S;
-  static constexpr int v = c + kCoarse * S;
-  static constexpr int dout = v + kCoarse * D;
-  static constexpr int al = dout + kCoarse * D;        // kCoarse + 4
-  static constexpr int fine = al + kCoarse + 4;        // [kCoarse / kFine][RS][NT]
-  static constexpr int red = fine + (kCoarse / kFine) * S * D;  // [2][kFine][NW][RED]
-  static constexpr int total = red + 2 * kFine * LY::NW * RED;
+constexpr int kL = kCoarse;  // steps per chunk (the checkpoint interval)
+
+template <int S, int D>
+struct AdjLayout {
+  static constexpr int NT = (S / 2) * (D / 4);  // a thread owns 2 x 4 entries of V
 };
 
-template <int S, int D, int CW_>
-__global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_bwd_kernel(const GdnParams p) {
-  using LY = Layout<S, D, CW_>;
-  using SM = BwdSmem<S, D, CW_>;
-  constexpr int CW = LY::CW, RG = LY::RG, RS = LY::RS, NW = LY::NW, NT = LY::NT;
-  constexpr int RED = SM::RED;
-  extern __shared__ __align__(16) float sm[];
-  float* s_b = sm + SM::b;
-  float* s_c = sm + SM::c;
-  float* s_v = sm + SM::v;
-  float* s_do = sm + SM::dout;
-  float* s_al = sm + SM::al;  // alpha of the block's steps and of the step after it
-  float* s_fine = sm + SM::fine;
-  float* s_red = sm + SM::red;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = lane % CW, d = warp * CW + j, g = lane / CW, s0 = g * RS;
-  const int64_t bh = blockIdx.x;
-  if (bh >= p.BH) return;
-  const int64_t T = p.T;
+// Product scan of 64 values held two per lane (v0 = element 2 l, v1 = element
+// 2 l + 1): returns the product of the elements before the lane's pair and
+// sets incl to the product through it.
+__device__ __forceinline__ float prefix_prod64(float v0, float v1, int lane, float& incl) {
+  float x = v0 * v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFullMask, x, o);
+    if (lane >= o) x *= y;
+  }
+  float e = __shfl_up_sync(kFullMask, x, 1);
+  if (lane == 0) e = 1.f;
+  incl = x;
+  return e;
+}
 
-  float dh[RS];
+template <int S, int D>
+__global__ void __launch_bounds__(AdjLayout<S, D>::NT) gdn_bwd_adj_kernel(const GdnParams p) {
+  constexpr int NT = AdjLayout<S, D>::NT;
+  __shared__ __align__(16) float s_c[kL * S];
+  __shared__ __align__(16) float s_do[kL * D];
+  __shared__ float s_g[kL];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t blk = blockIdx.x, bh = blk / p.NC, k = blk - bh * p.NC;
+  const int64_t T = p.T, r0 = bh * T + k * kL;
+  const int n = (int)(T - k * kL < kL ? T - k * kL : kL);
+  stage_block(s_c, p.c + r0 * S, n * S, tid, NT);
+  stage_block(s_do, p.dout + r0 * D, n * D, tid, NT);
+  cp_async_commit();
+  if (tid < 32) {  // Gamma_t within the chunk (gates past its end count as 1)
+    const float a0 = 2 * lane < n ? __ldg(p.alpha + r0 + 2 * lane) : 1.f;
+    const float a1 = 2 * lane + 1 < n ? __ldg(p.alpha + r0 + 2 * lane + 1) : 1.f;
+    float incl;
+    const float e = prefix_prod64(a0, a1, lane, incl);
+    s_g[2 * lane] = e * a0;
+    s_g[2 * lane + 1] = incl;
+    if (lane == 31) p.wsG[blk] = incl;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  const int si = tid / (D / 4), dj = tid - si * (D / 4);
+  float acc[2][4] = {};
+  for (int t = 0; t < n; ++t) {
+    const float g = s_g[t];
+    const float2 cq = *reinterpret_cast<const float2*>(s_c + t * S + 2 * si);
+    const float4 dq = *reinterpret_cast<const float4*>(s_do + t * D + 4 * dj);
+    const float c0 = cq.x * g, c1 = cq.y * g;
+    acc[0][0] = fmaf(c0, dq.x, acc[0][0]);
+    acc[0][1] = fmaf(c0, dq.y, acc[0][1]);
+    acc[0][2] = fmaf(c0, dq.z, acc[0][2]);
+    acc[0][3] = fmaf(c0, dq.w, acc[0][3]);
+    acc[1][0] = fmaf(c1, dq.x, acc[1][0]);
+    acc[1][1] = fmaf(c1, dq.y, acc[1][1]);
+    acc[1][2] = fmaf(c1, dq.z, acc[1][2]);
+    acc[1][3] = fmaf(c1, dq.w, acc[1][3]);
+  }
+  float* V = p.wsS + blk * S * D;
 #pragma unroll
-  for (int i = 0; i < RS; ++i) dh[i] = 0.f;
-  int buf = 0;  // which s_red buffer the current piece writes
+  for (int i = 0; i < 2; ++i)
+    *reinterpret_cast<float4*>(V + (2 * si + i) * D + 4 * dj) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+}
 
-  for (int64_t J = p.NC - 1; J >= 0; --J) {
-    const int64_t t0 = J * kCoarse;
-    const int rows = (int)(T - t0 < kCoarse ? T - t0 : kCoarse);
-    __syncthreads();  // the previous block's readers are done with the inputs
-    stage_block(s_b, p.b + (bh * T + t0) * S, rows * S, tid, NT);
-    stage_block(s_c, p.c + (bh * T + t0) * S, rows * S, tid, NT);
-    stage_block(s_v, p.v + (bh * T + t0) * D, rows * D, tid, NT);
-    stage_block(s_do, p.dout + (bh * T + t0) * D, rows * D, tid, NT);
-    cp_async_commit();
-    for (int i = tid; i <= rows; i += NT) {
-      const int64_t t = t0 + i;
-      s_al[i] = t < T ? __ldg(p.alpha + bh * T + t) : 0.f;  // alpha_{T} = 0 past the end
+// One thread per 4 entries of a head's S x D adjoint, walking the chunks from
+// the last; the loads of the next 8 chunks are in flight while the current 8
+// are chained.
+template <int S, int D>
+__global__ void __launch_bounds__(S * D / 4) gdn_bwd_carry_kernel(const GdnParams p) {
+  constexpr int Q = S * D / 4, G8 = 8;
+  const int tid = threadIdx.x;
+  const int64_t bh = blockIdx.x, NC = p.NC;
+  float4* ws = reinterpret_cast<float4*>(p.wsS + bh * NC * S * D) + tid;
+  const float* gam = p.wsG + bh * NC;
+  float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 V[G8], Vn[G8];
+  float g[G8], gn[G8];
+#pragma unroll
+  for (int j = 0; j < G8; ++j)
+    if (NC - 1 - j >= 0) {
+      V[j] = __ldcg(ws + (NC - 1 - j) * Q);
+      g[j] = __ldcg(gam + NC - 1 - j);
     }
-    float h[RS];
+  for (int64_t kb = NC - 1; kb >= 0; kb -= G8) {
 #pragma unroll
-    for (int i = 0; i < RS; ++i) h[i] = p.ckpt[(bh * p.NC + J) * S * D + (s0 + i) * D + d];
-    cp_async_wait<0>();
-    __syncthreads();
-    // ---- the state before each 8-step piece (each thread its own entries) ----
-    const int npiece = (rows + kFine - 1) / kFine;
-    const int last_start = (npiece - 1) * kFine;
-    for (int r = 0;; ++r) {
-      if (r % kFine == 0) {
-#pragma unroll
-        for (int i = 0; i < RS; ++i) s_fine[((r / kFine) * RS + i) * NT + tid] = h[i];
+    for (int j = 0; j < G8; ++j)
+      if (kb - G8 - j >= 0) {
+        Vn[j] = __ldcg(ws + (kb - G8 - j) * Q);
+        gn[j] = __ldcg(gam + kb - G8 - j);
       }
-      if (r == last_start) break;
-      const float al = s_al[r];
-      const float vd = s_v[r * D + d];
-      float bb[RS];
-      ld_row<RS>(s_b + r * S + s0, bb);
 #pragma unroll
-      for (int i = 0; i < RS; ++i) h[i] = fmaf(al, h[i], bb[i] * vd);
-    }
-    // ---- pieces from the last: states in registers, adjoint backwards ----
-    for (int f = npiece - 1; f >= 0; --f) {
-      const int r0 = f * kFine;
-      const int nr = rows - r0 < kFine ? rows - r0 : kFine;
-      float hs[kFine + 1][RS];  // hs[q] = state before step r0 + q
-#pragma unroll
-      for (int i = 0; i < RS; ++i) hs[0][i] = s_fine[(f * RS + i) * NT + tid];
-#pragma unroll
-      for (int q = 0; q < kFine; ++q) {
-        if (q < nr) {
-          const int r = r0 + q;
-          const float al = s_al[r];
-          const float vd = s_v[r * D + d];
-          float bb[RS];
-          ld_row<RS>(s_b + r * S + s0, bb);
-#pragma unroll
-          for (int i = 0; i < RS; ++i) hs[q + 1][i] = fmaf(al, hs[q][i], bb[i] * vd);
-        }
+    for (int j = 0; j < G8; ++j)
+      if (kb - j >= 0) {
+        ws[(kb - j) * Q] = G;  // adjoint of the state after chunk kb - j
+        G = make_float4(fmaf(g[j], G.x, V[j].x), fmaf(g[j], G.y, V[j].y), fmaf(g[j], G.z, V[j].z),
+                        fmaf(g[j], G.w, V[j].w));
       }
-      float* red = s_red + buf * (kFine * NW * RED);
 #pragma unroll
-      for (int q = kFine - 1; q >= 0; --q) {
-        if (q < nr) {
-          const int r = r0 + q;
-          const int64_t t = t0 + r;
-          const float an = s_al[r + 1];  // alpha_{t+1}; 0 past the end
-          const float dod = s_do[r * D + d];
-          const float vd = s_v[r * D + d];
-          float bb[RS], cc[RS], xb[RS], xc[RS];
-          ld_row<RS>(s_b + r * S + s0, bb);
-          ld_row<RS>(s_c + r * S + s0, cc);
-          float dvp = 0.f, dal = 0.f;
-#pragma unroll
-          for (int i = 0; i < RS; ++i) {
-            dh[i] = fmaf(an, dh[i], cc[i] * dod);  // dh_t = c_t do_t^T + alpha_{t+1} dh_{t+1}
-            dvp = fmaf(bb[i], dh[i], dvp);         // dv_t[d] = sum_s b_t[s] dh_t[s][d]
-            dal = fmaf(dh[i], hs[q][i], dal);      // dalpha_t = <dh_t, h_{t-1}>
-            xb[i] = dh[i] * vd;                    // db_t[s] = sum_d dh_t[s][d] v_t[d]
-            xc[i] = hs[q + 1][i] * dod;            // dc_t[s] = sum_d h_t[s][d] do_t[d]
-          }
-#pragma unroll
-          for (int m = CW; m < 32; m <<= 1) dvp += __shfl_xor_sync(kFullMask, dvp, m);
-          if (g == 0) __stcs(p.dv + (bh * T + t) * D + d, dvp);
-#pragma unroll
-          for (int m = 1; m < CW; m <<= 1) dal += __shfl_xor_sync(kFullMask, dal, m);
-          const float wb = reduce_scatter_cols<RS, CW>(xb, lane);
-          const float wc = reduce_scatter_cols<RS, CW>(xc, lane);
-          float* rq = red + (q * NW + warp) * RED;
-          if (j < RS) {
-            rq[s0 + j] = wb;
-            rq[S + s0 + j] = wc;
-          }
-          if (j == 0) rq[2 * S + g] = dal;
-        }
-      }
-      __syncthreads();
-      // sums over the warps (and row groups, for dalpha) of the piece's steps
-      for (int k = tid; k < nr * (2 * S + 1); k += NT) {
-        const int q = k / (2 * S + 1), e = k - q * (2 * S + 1);
-        const float* rq = red + q * NW * RED;
-        const int64_t t = t0 + r0 + q;
-        float acc = 0.f;
-        if (e < 2 * S) {
-#pragma unroll
-          for (int w = 0; w < NW; ++w) acc += rq[w * RED + e];
-          if (e < S) __stcs(p.db + (bh * T + t) * S + e, acc);
-          else __stcs(p.dc + (bh * T + t) * S + (e - S), acc);
-        } else {
-#pragma unroll
-          for (int w = 0; w < NW; ++w)
-#pragma unroll
-            for (int gg = 0; gg < RG; ++gg) acc += rq[w * RED + 2 * S + gg];
-          __stcs(p.dalpha + bh * T + t, acc);
-        }
-      }
-      buf ^= 1;  // the next piece writes the other buffer; this one's readers
-                 // finish before the barrier that ends the next piece
+    for (int j = 0; j < G8; ++j) {
+      V[j] = Vn[j];
+      g[j] = gn[j];
     }
   }
-  // dh0 = alpha_0 dh_0
-  if (p.dh0 && T > 0) {
-    const float a0 = __ldg(p.alpha + bh * T);
+  if (p.dh0) reinterpret_cast<float4*>(p.dh0 + bh * S * D)[tid] = G;
+}
+
+// Shared memory of the chunk-gradient kernel, in floats. Rows are padded by 4
+// floats (16-byte aligned, conflict-free 16-byte reads of consecutive rows).
+template <int S, int D>
+struct ChunkSmem {
+  static constexpr int SP = S + 4, DP = D + 4, LP = kL + 4;
+  static constexpr int b = 0;                  // [kL][SP]
+  static constexpr int c = b + kL * SP;        // [kL][SP]
+  static constexpr int dout = c + kL * SP;     // [kL][DP]
+  static constexpr int r1 = dout + kL * DP;    // v, H_in^T, G_out, G_out^T; later dS^T
+  static constexpr int v = r1;                 // [kL][DP]
+  static constexpr int hinT = v + kL * DP;     // [D][SP]
+  static constexpr int gout = hinT + D * SP;   // [S][DP]
+  static constexpr int goutT = gout + S * DP;  // [D][SP]
+  static constexpr int dsT = r1;               // [kL][LP]
+  static constexpr int r1_end = goutT + D * SP > r1 + kL * LP ? goutT + D * SP : r1 + kL * LP;
+  static constexpr int cb = r1_end;            // [kL][LP]: CB, then P
+  static constexpr int dov = cb + kL * LP;     // [kL][LP]: DoV, then dS
+  static constexpr int y = dov + kL * LP;      // [kL][LP]
+  static constexpr int al = y + kL * LP;       // kL + 4 gates (1 past the chunk's end)
+  static constexpr int gam = al + kL + 4;      // Gamma_t
+  static constexpr int gm1 = gam + kL;         // Gamma_{t-1}
+  static constexpr int wdec = gm1 + kL;        // D[n-1][t]
+  static constexpr int z = wdec + kL;
+  static constexpr int w = z + kL;
+  static constexpr int yv = w + kL;            // kL + 4
+  static constexpr int red = yv + kL + 4;      // per-warp partial sums
+  static constexpr int qf = red + 12;          // [4][kL]: gate products of each row quarter
+  static constexpr int qa = qf + 4 * kL;       // [4][kL]: dalpha partial sums of each quarter
+  static constexpr int total = qa + 4 * kL;
+};
+
+__device__ __forceinline__ float f4(const float4& q, int i) {
+  return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
+}
+
+// N (1 or 2) consecutive floats of shared memory
+template <int N>
+__device__ __forceinline__ void ld_n(const float* p, float (&x)[N]) {
+  if constexpr (N == 2) {
+    const float2 q = *reinterpret_cast<const float2*>(p);
+    x[0] = q.x;
+    x[1] = q.y;
+  } else {
+    x[0] = p[0];
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void st_n(float* p, const float (&x)[N]) {
+  if constexpr (N == 2) {
+    __stcs(reinterpret_cast<float2*>(p), make_float2(x[0], x[1]));
+  } else {
+    __stcs(p, x[0]);
+  }
+}
+
+template <int S, int D>
+__global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p) {
+  using SM = ChunkSmem<S, D>;
+  constexpr int SP = SM::SP, DP = SM::DP, LP = SM::LP, NT = 256;
+  constexpr int TNS = S / 16, TND = D / 16;  // output columns per thread
+  extern __shared__ __align__(16) float sm[];
+  float* sb = sm + SM::b;
+  float* sc = sm + SM::c;
+  float* sdo = sm + SM::dout;
+  float* sv = sm + SM::v;
+  float* shT = sm + SM::hinT;
+  float* sg = sm + SM::gout;
+  float* sgT = sm + SM::goutT;
+  float* sdsT = sm + SM::dsT;
+  float* scb = sm + SM::cb;
+  float* sdv = sm + SM::dov;
+  float* sy = sm + SM::y;
+  float* sal = sm + SM::al;
+  float* sgam = sm + SM::gam;
+  float* sgm1 = sm + SM::gm1;
+  float* swd = sm + SM::wdec;
+  float* sz = sm + SM::z;
+  float* sw = sm + SM::w;
+  float* syv = sm + SM::yv;
+  float* sred = sm + SM::red;
+  float* sqf = sm + SM::qf;
+  float* sqa = sm + SM::qa;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t blk = blockIdx.x, bh = blk / p.NC, k = blk - bh * p.NC;
+  const int64_t T = p.T, r0 = bh * T + k * kL;
+  const int n = (int)(T - k * kL < kL ? T - k * kL : kL);
+
+  // ---- inputs of the chunk (rows past n zeroed), H_in^T, G_out, G_out^T ----
+  for (int i = tid; i < n * (S / 4); i += NT) {
+    const int t = i / (S / 4), q = 4 * (i - t * (S / 4));
+    cp_async16(sb + t * SP + q, p.b + (r0 + t) * S + q);
+    cp_async16(sc + t * SP + q, p.c + (r0 + t) * S + q);
+  }
+  for (int i = tid; i < n * (D / 4); i += NT) {
+    const int t = i / (D / 4), q = 4 * (i - t * (D / 4));
+    cp_async16(sv + t * DP + q, p.v + (r0 + t) * D + q);
+    cp_async16(sdo + t * DP + q, p.dout + (r0 + t) * D + q);
+  }
+  cp_async_commit();
+  for (int i = n * SP + tid; i < kL * SP; i += NT) {
+    sb[i] = 0.f;
+    sc[i] = 0.f;
+  }
+  for (int i = n * DP + tid; i < kL * DP; i += NT) {
+    sv[i] = 0.f;
+    sdo[i] = 0.f;
+  }
+  for (int i = tid; i < kL + 4; i += NT) sal[i] = i < n ? __ldg(p.alpha + r0 + i) : 1.f;
+  float win = 0.f;
+  {
+    const float* hin = p.ckpt + blk * S * D;
+    const float* gout = p.wsS + blk * S * D;
+    for (int e = tid; e < S * D; e += NT) {
+      const int s = e / D, d = e - s * D;
+      const float h = __ldg(hin + e), g = __ldcg(gout + e);
+      shT[d * SP + s] = h;
+      sg[s * DP + d] = g;
+      sgT[d * SP + s] = g;
+      win = fmaf(h, g, win);
+    }
+  }
 #pragma unroll
-    for (int i = 0; i < RS; ++i) p.dh0[(bh * S + s0 + i) * D + d] = a0 * dh[i];
+  for (int o = 16; o >= 1; o >>= 1) win += __shfl_xor_sync(kFullMask, win, o);
+  if (lane == 0) sred[warp] = win;
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- gate products: Gamma_t, Gamma_{t-1} (warp 0); D[n-1][t] (warp 1) ----
+  if (warp == 0) {
+    const float a0 = sal[2 * lane], a1 = sal[2 * lane + 1];
+    float incl;
+    const float e = prefix_prod64(a0, a1, lane, incl);
+    sgam[2 * lane] = e * a0;
+    sgam[2 * lane + 1] = incl;
+    sgm1[2 * lane] = e;
+    sgm1[2 * lane + 1] = e * a0;
+  } else if (warp == 1) {
+    const float a0 = sal[2 * lane], a1 = sal[2 * lane + 1];
+    float x = a0 * a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(kFullMask, x, o);
+      if (lane + o < 32) x *= y;
+    }
+    float e = __shfl_down_sync(kFullMask, x, 1);
+    if (lane == 31) e = 1.f;
+    swd[2 * lane + 1] = e;
+    swd[2 * lane] = a1 * e;
+  }
+
+  // ---- HDo = dout H_in^T, Gv = v G_out^T, Gb = b G_out, kept in registers:
+  // thread rows 4 ri .. 4 ri + 3, columns TN cj .. TN cj + TN - 1 ----
+  const int ri = tid >> 4, cj = tid & 15;
+  float hdo[4][TNS], gv[4][TNS], gb[4][TND];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int j = 0; j < TNS; ++j) hdo[i][j] = gv[i][j] = 0.f;
+#pragma unroll
+    for (int j = 0; j < TND; ++j) gb[i][j] = 0.f;
+  }
+#pragma unroll 2
+  for (int d = 0; d < D; d += 4) {
+    float4 ad[4], av[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ad[i] = *reinterpret_cast<const float4*>(sdo + (4 * ri + i) * DP + d);
+      av[i] = *reinterpret_cast<const float4*>(sv + (4 * ri + i) * DP + d);
+    }
+#pragma unroll
+    for (int dd = 0; dd < 4; ++dd) {
+      float bh_[TNS], bg_[TNS];
+      ld_n<TNS>(shT + (d + dd) * SP + TNS * cj, bh_);
+      ld_n<TNS>(sgT + (d + dd) * SP + TNS * cj, bg_);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < TNS; ++j) {
+          hdo[i][j] = fmaf(f4(ad[i], dd), bh_[j], hdo[i][j]);
+          gv[i][j] = fmaf(f4(av[i], dd), bg_[j], gv[i][j]);
+        }
+    }
+  }
+#pragma unroll 2
+  for (int s = 0; s < S; s += 4) {
+    float4 ab[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ab[i] = *reinterpret_cast<const float4*>(sb + (4 * ri + i) * SP + s);
+#pragma unroll
+    for (int ss = 0; ss < 4; ++ss) {
+      float g_[TND];
+      ld_n<TND>(sg + (s + ss) * DP + TND * cj, g_);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < TND; ++j) gb[i][j] = fmaf(f4(ab[i], ss), g_[j], gb[i][j]);
+    }
+  }
+  // z_t = c_t . HDo_t and w_tau = b_tau . Gv_tau, summed over a row's 16 column threads
+  {
+    float zp[4], wp[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float cr[TNS], br[TNS];
+      ld_n<TNS>(sc + (4 * ri + i) * SP + TNS * cj, cr);
+      ld_n<TNS>(sb + (4 * ri + i) * SP + TNS * cj, br);
+      zp[i] = wp[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) {
+        zp[i] = fmaf(cr[j], hdo[i][j], zp[i]);
+        wp[i] = fmaf(br[j], gv[i][j], wp[i]);
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        zp[i] += __shfl_xor_sync(kFullMask, zp[i], o);
+        wp[i] += __shfl_xor_sync(kFullMask, wp[i], o);
+      }
+    }
+    if (cj == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sz[4 * ri + i] = zp[i];
+        sw[4 * ri + i] = wp[i];
+      }
+    }
+  }
+
+  // ---- CB = c b^T and DoV = dout v^T (64 x 64); a warp takes a 16 x 32
+  // block, skipped when the block lies entirely above the diagonal ----
+  {
+    const int bi = warp >> 1, bj = warp & 1;
+    if (32 * bj <= 16 * bi + 15) {
+      const int li = lane >> 3, lj = lane & 7;
+      float acb[4][4], adv[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acb[i][j] = adv[i][j] = 0.f;
+#pragma unroll 2
+      for (int s = 0; s < S; s += 4) {
+        float4 a[4], q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          a[i] = *reinterpret_cast<const float4*>(sc + (16 * bi + li + 4 * i) * SP + s);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          q[j] = *reinterpret_cast<const float4*>(sb + (32 * bj + lj + 8 * j) * SP + s);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            acb[i][j] = fmaf(a[i].x, q[j].x,
+                             fmaf(a[i].y, q[j].y, fmaf(a[i].z, q[j].z, fmaf(a[i].w, q[j].w, acb[i][j]))));
+      }
+#pragma unroll 2
+      for (int d = 0; d < D; d += 4) {
+        float4 a[4], q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          a[i] = *reinterpret_cast<const float4*>(sdo + (16 * bi + li + 4 * i) * DP + d);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          q[j] = *reinterpret_cast<const float4*>(sv + (32 * bj + lj + 8 * j) * DP + d);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            adv[i][j] = fmaf(a[i].x, q[j].x,
+                             fmaf(a[i].y, q[j].y, fmaf(a[i].z, q[j].z, fmaf(a[i].w, q[j].w, adv[i][j]))));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int o = (16 * bi + li + 4 * i) * LP + 32 * bj + lj + 8 * j;
+          scb[o] = acb[i][j];
+          sdv[o] = adv[i][j];
+        }
+    }
+  }
+  __syncthreads();
+
+  // ---- Y[t][r] (row t: an affine scan over r with gates alpha_r) and y_r;
+  // a warp scans 4 rows at a time (independent shuffle chains) ----
+  {
+    const float a0 = sal[2 * lane], a1 = sal[2 * lane + 1];
+    for (int rb = warp; rb <= kL; rb += 4 * (NT / 32)) {
+      float A[4], X[4], x0[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = rb + u * (NT / 32);
+        float y0 = 0.f, y1 = 0.f;
+        if (row < kL) {
+          if (2 * lane <= row) y0 = scb[row * LP + 2 * lane] * sdv[row * LP + 2 * lane];
+          if (2 * lane + 1 <= row) y1 = scb[row * LP + 2 * lane + 1] * sdv[row * LP + 2 * lane + 1];
+        } else if (row == kL) {
+          y0 = sw[2 * lane];
+          y1 = sw[2 * lane + 1];
+        }
+        x0[u] = y0;
+        A[u] = a0 * a1;
+        X[u] = fmaf(a1, y0, y1);
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float Ap = __shfl_up_sync(kFullMask, A[u], o), Xp = __shfl_up_sync(kFullMask, X[u], o);
+          if (lane >= o) {
+            X[u] = fmaf(A[u], Xp, X[u]);
+            A[u] *= Ap;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = rb + u * (NT / 32);
+        float e = __shfl_up_sync(kFullMask, X[u], 1);
+        if (lane == 0) e = 0.f;
+        if (row <= kL) {
+          float* dst = row < kL ? sy + row * LP : syv;
+          dst[2 * lane] = e;
+          dst[2 * lane + 1] = fmaf(a0, e, x0[u]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- down each column tau: D[t][tau] for t >= tau; P and dS in place, dS^T
+  // (zero below its diagonal), dalpha_tau. Warp w takes columns
+  // 32 (w & 1) .. + 31 over the row quarter 16 (w >> 1) .. + 15: first the
+  // quarter's product of the gates that enter D (rows t > tau), exchanged
+  // through shared memory, then the walk from the product of the earlier
+  // quarters. ----
+  {
+    const int tau = 32 * (warp & 1) + lane, q = warp >> 1, tq = 16 * q;
+    float f = 1.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (tq + i > tau) f *= sal[tq + i];
+    sqf[q * kL + tau] = f;
+    __syncthreads();
+    float dec = 1.f;
+    for (int i = 0; i < q; ++i) dec *= sqf[i * kL + tau];
+    const float gm = sgm1[tau];
+    float acc = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int t = tq + i;
+      float* pc = scb + t * LP + tau;
+      float* pd = sdv + t * LP + tau;
+      if (t < tau) {
+        *pc = 0.f;
+        *pd = 0.f;
+        sdsT[tau * LP + t] = 0.f;
+      } else {
+        if (t > tau) dec *= sal[t];
+        const float ds = dec * *pd;
+        *pc = dec * *pc;
+        *pd = ds;
+        sdsT[tau * LP + t] = ds;
+        acc = fmaf(dec, fmaf(gm, sz[t], sy[t * LP + tau]), acc);
+      }
+    }
+    sqa[q * kL + tau] = acc;
+  }
+  __syncthreads();
+  if (tid < kL) {
+    const int tau = tid;
+    float wtot = 0.f;
+#pragma unroll
+    for (int i = 0; i < NT / 32; ++i) wtot += sred[i];
+    const float acc = (sqa[tau] + sqa[kL + tau]) + (sqa[2 * kL + tau] + sqa[3 * kL + tau]);
+    if (tau < n) p.dalpha[r0 + tau] = fmaf(swd[tau], fmaf(sgm1[tau], wtot, syv[tau]), acc);
+  }
+
+  // ---- db = dS^T c + w o Gv, dv = P^T dout + w o Gb, dc = dS b + Gamma o HDo ----
+  {
+    float adb[4][TNS], adv[4][TND], adc[4][TNS];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float wd = swd[4 * ri + i], g = sgam[4 * ri + i];
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) {
+        adb[i][j] = wd * gv[i][j];
+        adc[i][j] = g * hdo[i][j];
+      }
+#pragma unroll
+      for (int j = 0; j < TND; ++j) adv[i][j] = wd * gb[i][j];
+    }
+    // the warp's rows are 8 w .. 8 w + 7; dS[t][tau] and P[t][tau] vanish for t < tau
+#pragma unroll 2
+    for (int t = 8 * warp; t < n; ++t) {
+      const float4 ds = *reinterpret_cast<const float4*>(sdv + t * LP + 4 * ri);
+      const float4 pp = *reinterpret_cast<const float4*>(scb + t * LP + 4 * ri);
+      float cr[TNS], dr[TND];
+      ld_n<TNS>(sc + t * SP + TNS * cj, cr);
+      ld_n<TND>(sdo + t * DP + TND * cj, dr);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < TNS; ++j) adb[i][j] = fmaf(f4(ds, i), cr[j], adb[i][j]);
+#pragma unroll
+        for (int j = 0; j < TND; ++j) adv[i][j] = fmaf(f4(pp, i), dr[j], adv[i][j]);
+      }
+    }
+    // dS^T[tau][t] vanishes for tau > t
+    const int thi = 8 * warp + 8 < n ? 8 * warp + 8 : n;
+#pragma unroll 2
+    for (int tau = 0; tau < thi; ++tau) {
+      const float4 a = *reinterpret_cast<const float4*>(sdsT + tau * LP + 4 * ri);
+      float br[TNS];
+      ld_n<TNS>(sb + tau * SP + TNS * cj, br);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < TNS; ++j) adc[i][j] = fmaf(f4(a, i), br[j], adc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = 4 * ri + i;
+      if (m < n) {
+        st_n<TNS>(p.db + (r0 + m) * S + TNS * cj, adb[i]);
+        st_n<TNS>(p.dc + (r0 + m) * S + TNS * cj, adc[i]);
+        st_n<TND>(p.dv + (r0 + m) * D + TND * cj, adv[i]);
+      }
+    }
   }
 }
 
 template <int S, int D, int CW>
-cudaError_t launch(const GdnParams& p, bool fwd, cudaStream_t s) {
-  if (p.BH <= 0 || p.T <= 0) return cudaSuccess;
-  using LY = Layout<S, D, CW>;
-  if (fwd) {
-    gdn_fwd_kernel<S, D, CW><<<(unsigned)p.BH, LY::NT, 0, s>>>(p);
-    return cudaGetLastError();
-  }
-  const size_t smem = sizeof(float) * (size_t)BwdSmem<S, D, CW>::total;
-  cudaError_t e = cudaFuncSetAttribute(gdn_bwd_kernel<S, D, CW>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  gdn_bwd_kernel<S, D, CW><<<(unsigned)p.BH, LY::NT, smem, s>>>(p);
+cudaError_t launch_fwd(const GdnParams& p, cudaStream_t s) {
+  gdn_fwd_kernel<S, D, CW><<<(unsigned)p.BH, Layout<S, D, CW>::NT, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-// Eight columns per warp (four row groups): measured faster than four columns
-// per warp (eight row groups), whose extra warps cost more in per-lane loads
-// and shuffles than they recover in latency hiding.
+template <int S, int D>
+cudaError_t launch_bwd(const GdnParams& p, cudaStream_t s) {
+  const unsigned nblk = (unsigned)(p.BH * p.NC);
+  gdn_bwd_adj_kernel<S, D><<<nblk, AdjLayout<S, D>::NT, 0, s>>>(p);
+  gdn_bwd_carry_kernel<S, D><<<(unsigned)p.BH, S * D / 4, 0, s>>>(p);
+  const size_t smem = sizeof(float) * (size_t)ChunkSmem<S, D>::total;
+  cudaError_t e = cudaFuncSetAttribute(gdn_bwd_chunk_kernel<S, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  gdn_bwd_chunk_kernel<S, D><<<nblk, 256, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Forward: eight columns per warp (four row groups), measured faster than four
+// columns per warp (eight row groups), whose extra warps cost more in per-lane
+// loads and shuffles than they recover in latency hiding.
 template <int S, int D>
 cudaError_t launch(const GdnParams& p, bool fwd, cudaStream_t s) {
-  return launch<S, D, 8>(p, fwd, s);
+  if (p.BH <= 0 || p.T <= 0) return cudaSuccess;
+  return fwd ? launch_fwd<S, D, 8>(p, s) : launch_bwd<S, D>(p, s);
 }
 
 cudaError_t dispatch(const GdnParams& p, int S, int D, bool fwd, cudaStream_t s) {
@@ -409,6 +799,12 @@ extern "C" {
 size_t gdn_checkpoint_bytes(int64_t B, int64_t H, int64_t T, int64_t S, int64_t D) {
   if (B < 0 || H < 0 || T < 0 || !shape_ok(S, D)) return 0;
   return sizeof(float) * (size_t)(B * H) * (size_t)((T + kCoarse - 1) / kCoarse) * (size_t)(S * D);
+}
+
+size_t gdn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t T, int64_t S, int64_t D) {
+  if (B < 0 || H < 0 || T < 0 || !shape_ok(S, D)) return 0;
+  const size_t chunks = (size_t)(B * H) * (size_t)((T + kL - 1) / kL);
+  return sizeof(float) * (chunks * (size_t)(S * D) + round_up(chunks, 4));
 }
 
 scan_status gdn_fwd(const float* alpha, const float* b, const float* v, const float* c,
@@ -438,7 +834,7 @@ scan_status gdn_fwd(const float* alpha, const float* b, const float* v, const fl
 scan_status gdn_bwd(const float* alpha, const float* b, const float* v, const float* c,
                     const float* ckpt, const float* dout, float* dalpha, float* db, float* dv,
                     float* dc, float* dh0, int64_t B, int64_t H, int64_t T, int64_t S,
-                    int64_t D, cudaStream_t stream) {
+                    int64_t D, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || H < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
   if (!shape_ok(S, D)) return SCAN_ERR_UNSUPPORTED;
   if (B * H == 0) return SCAN_OK;
@@ -453,7 +849,10 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v, const fl
   if (!al16(b) || !al16(v) || !al16(c) || !al16(ckpt) || !al16(dout) || !al16(db) ||
       !al16(dv) || !al16(dc) || !al16(dh0))
     return SCAN_ERR_ALIGNMENT;
-  if (B * H > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
+  const int64_t NC = (T + kL - 1) / kL;
+  if (B * H * NC > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
+  if (!workspace || !al16(workspace) || workspace_bytes < gdn_bwd_workspace_bytes(B, H, T, S, D))
+    return SCAN_ERR_WORKSPACE;
   GdnParams p{};
   p.alpha = alpha;
   p.b = b;
@@ -466,9 +865,11 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v, const fl
   p.dv = dv;
   p.dc = dc;
   p.dh0 = dh0;
+  p.wsS = static_cast<float*>(workspace);
+  p.wsG = p.wsS + (size_t)(B * H * NC) * (size_t)(S * D);
   p.BH = B * H;
   p.T = T;
-  p.NC = (T + kCoarse - 1) / kCoarse;
+  p.NC = NC;
   return dispatch(p, (int)S, (int)D, false, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
 }
 

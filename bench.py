@@ -331,9 +331,11 @@ def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
     b_bytes = n * (8 + 16 * S + 16 * D) + ck.numel() * 4
     f_ms = time_calls(lambda: scan.gdn_fwd(alpha, b, v, c, checkpoints=ck, out=o), steps, warm,
                       flush, stream)
-    g = scan.gdn_bwd(alpha, b, v, c, ck, dout)
-    b_ms = time_calls(lambda: scan.gdn_bwd(alpha, b, v, c, ck, dout, out=g), steps, warm, flush,
-                      stream)
+    ws = torch.empty(scan.gdn_bwd_workspace_bytes(*alpha.shape, S, D), dtype=torch.uint8,
+                     device=dev)
+    g = scan.gdn_bwd(alpha, b, v, c, ck, dout, workspace=ws)
+    b_ms = time_calls(lambda: scan.gdn_bwd(alpha, b, v, c, ck, dout, out=g, workspace=ws), steps,
+                      warm, flush, stream)
     return {"head_steps": n, "fwd_ms": f_ms, "bwd_ms": b_ms,
             "fwd_gbs": f_bytes / f_ms / 1e6, "bwd_gbs": b_bytes / b_ms / 1e6,
             "fwd_frac": f_bytes / f_ms / 1e6 / peak, "bwd_frac": b_bytes / b_ms / 1e6 / peak}

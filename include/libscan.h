@@ -301,13 +301,20 @@ scan_status gdn_fwd(const float* alpha, const float* b, const float* v,
  *   dh_t = c_t dout_t^T + alpha_{t+1} dh_{t+1},   dc_t = h_t dout_t,
  *   dv_t = dh_t^T b_t,  db_t = dh_t v_t,  dalpha_t = <dh_t, h_{t-1}>,
  *   dh0 = alpha_0 dh_0 (nullable).
- * ckpt is the forward's checkpoint buffer (for the same inputs and h0); the
- * states in between are recomputed, none is stored. Outputs in the layouts of
- * the corresponding inputs. */
+ * Computed chunk by chunk over T ([GDN] The chunked GDN algorithm): within a
+ * 64-step chunk the products above become small matrix products; only the
+ * adjoint of the state between chunks runs serially. ckpt is the forward's
+ * checkpoint buffer (for the same inputs and h0); no state is stored besides
+ * it. workspace: gdn_bwd_workspace_bytes() bytes of device memory, 16-byte
+ * aligned, owned by the caller (else SCAN_ERR_WORKSPACE); it holds no state
+ * between calls. Outputs in the layouts of the corresponding inputs. */
+size_t gdn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t T, int64_t S,
+                               int64_t D);
 scan_status gdn_bwd(const float* alpha, const float* b, const float* v,
                     const float* c, const float* ckpt, const float* dout,
                     float* dalpha, float* db, float* dv, float* dc, float* dh0,
                     int64_t B, int64_t H, int64_t T, int64_t S, int64_t D,
+                    void* workspace, size_t workspace_bytes,
                     cudaStream_t stream);
 
 /* Bytes of the library's own scratch used by scan_fwd_noalloc (16 MiB). */

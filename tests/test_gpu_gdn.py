@@ -102,3 +102,33 @@ def test_gdn_4k_sampled_heads(lib):
         assert err(sl(o), ref_o, sc_o) <= TOL, (bb, hh)
         for got, ref, sc in zip((sl(dal), sl(db), sl(dv), sl(dc), sl(dh0)), ref_g, sc_g):
             assert err(got, ref, sc) <= TOL, (bb, hh)
+
+
+@pytest.mark.parametrize("T", [64, 200])
+def test_gdn_gate_zero_resets(lib, T):
+    """alpha_t = 0 erases the state (h_t = b_t v_t^T). Zero gates at a chunk's
+    first and last steps and inside it; the backward's per-chunk gate
+    products are formed without division, so dalpha stays exact there."""
+    w = workloads.gdn(2, 2, T, 32, 32, seed=11 + T, h0=True)
+    for t in (0, 1, 31, 63, 64, 127, 128, 199):
+        if t < T:
+            w.alpha[:, :, t] = 0.0
+    w.alpha[1, 1, :] = 0.0  # every step a reset
+    check(lib, w)
+
+
+def test_gdn_bwd_rejects_a_short_workspace(lib):
+    w = workloads.gdn(1, 2, 130, 16, 16, seed=3, h0=False)
+    alpha, b, v, c, dout = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout))
+    _, ck = lib.gdn_fwd(alpha, b, v, c)
+    need = lib.gdn_bwd_workspace_bytes(1, 2, 130, 16, 16)
+    assert need == 4 * (2 * 3 * 16 * 16 + 8)
+    with pytest.raises(ValueError):
+        lib.gdn_bwd(alpha, b, v, c, ck, dout,
+                    workspace=torch.empty(need - 16, dtype=torch.uint8, device=DEV))
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    got = lib.gdn_bwd(alpha, b, v, c, ck, dout, workspace=ws)
+    ref = lib.gdn_bwd(alpha, b, v, c, ck, dout)
+    torch.cuda.synchronize()
+    for x, y in zip(got, ref):
+        assert torch.equal(x, y)

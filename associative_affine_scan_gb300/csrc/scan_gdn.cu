@@ -326,10 +326,10 @@ struct ChunkSmem {
   static constexpr int b = 0;                  // [kL][SP]
   static constexpr int c = b + kL * SP;        // [kL][SP]
   static constexpr int dout = c + kL * SP;     // [kL][DP]
-  static constexpr int r1 = dout + kL * DP;    // v, H_in^T, G_out, G_out^T; later dS^T
+  static constexpr int r1 = dout + kL * DP;    // v, H_in, G_out, G_out^T; later dS^T
   static constexpr int v = r1;                 // [kL][DP]
-  static constexpr int hinT = v + kL * DP;     // [D][SP]
-  static constexpr int gout = hinT + D * SP;   // [S][DP]
+  static constexpr int hin = v + kL * DP;      // [S][DP]
+  static constexpr int gout = hin + S * DP;    // [S][DP]
   static constexpr int goutT = gout + S * DP;  // [D][SP]
   static constexpr int dsT = r1;               // [kL][LP]
   static constexpr int r1_end = goutT + D * SP > r1 + kL * LP ? goutT + D * SP : r1 + kL * LP;
@@ -353,25 +353,52 @@ __device__ __forceinline__ float f4(const float4& q, int i) {
   return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
 }
 
-// N (1 or 2) consecutive floats of shared memory
-template <int N>
-__device__ __forceinline__ void ld_n(const float* p, float (&x)[N]) {
-  if constexpr (N == 2) {
-    const float2 q = *reinterpret_cast<const float2*>(p);
-    x[0] = q.x;
-    x[1] = q.y;
-  } else {
-    x[0] = p[0];
-  }
+// Two fp32 fused multiply-adds in one packed instruction (sm_100 and later):
+// {a.x b.x + c.x, a.y b.y + c.y}, each rounded once, as fmaf would.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long A, B, C, R;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
+  return r;
 }
 
-template <int N>
-__device__ __forceinline__ void st_n(float* p, const float (&x)[N]) {
-  if constexpr (N == 2) {
-    __stcs(reinterpret_cast<float2*>(p), make_float2(x[0], x[1]));
-  } else {
-    __stcs(p, x[0]);
+// acc += the dot product of two 4-vectors, as two interleaved partial sums
+__device__ __forceinline__ float2 dot4x2(const float4& a, const float4& b, float2 acc) {
+  acc = ffma2(make_float2(a.x, a.y), make_float2(b.x, b.y), acc);
+  return ffma2(make_float2(a.z, a.w), make_float2(b.z, b.w), acc);
+}
+
+// Block of a 64 x 64 product C[m][n] = sum_k A[m][k] B[n][k] (both operands
+// row-major with K consecutive, row strides ap and bp): rows m0 + li + 4 i,
+// columns n0 + lj + 8 j, written to out (row stride LP).
+template <int K, int LP>
+__device__ __forceinline__ void gemm_nt_block(const float* A, int ap, const float* B, int bp,
+                                              int m0, int n0, int li, int lj, float* out) {
+  float2 acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
+#pragma unroll 2
+  for (int kk = 0; kk < K; kk += 4) {
+    float4 a[4], q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(A + (m0 + li + 4 * i) * ap + kk);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const float4*>(B + (n0 + lj + 8 * j) * bp + kk);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = dot4x2(a[i], q[j], acc[i][j]);
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[(m0 + li + 4 * i) * LP + n0 + lj + 8 * j] = acc[i][j].x + acc[i][j].y;
 }
 
 template <int S, int D>
@@ -384,7 +411,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
   float* sc = sm + SM::c;
   float* sdo = sm + SM::dout;
   float* sv = sm + SM::v;
-  float* shT = sm + SM::hinT;
+  float* sh = sm + SM::hin;
   float* sg = sm + SM::gout;
   float* sgT = sm + SM::goutT;
   float* sdsT = sm + SM::dsT;
@@ -434,7 +461,7 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
     for (int e = tid; e < S * D; e += NT) {
       const int s = e / D, d = e - s * D;
       const float h = __ldg(hin + e), g = __ldcg(gout + e);
-      shT[d * SP + s] = h;
+      sh[s * DP + d] = h;
       sg[s * DP + d] = g;
       sgT[d * SP + s] = g;
       win = fmaf(h, g, win);
@@ -470,51 +497,60 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
   }
 
   // ---- HDo = dout H_in^T, Gv = v G_out^T, Gb = b G_out, kept in registers:
-  // thread rows 4 ri .. 4 ri + 3, columns TN cj .. TN cj + TN - 1 ----
+  // thread rows 4 ri .. 4 ri + 3, columns cj + 16 j (j < TN) ----
   const int ri = tid >> 4, cj = tid & 15;
   float hdo[4][TNS], gv[4][TNS], gb[4][TND];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int j = 0; j < TNS; ++j) hdo[i][j] = gv[i][j] = 0.f;
-#pragma unroll
-    for (int j = 0; j < TND; ++j) gb[i][j] = 0.f;
-  }
-#pragma unroll 2
-  for (int d = 0; d < D; d += 4) {
-    float4 ad[4], av[4];
+  {
+    float2 ah[4][TNS], ag[4][TNS], ab[4][TND];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      ad[i] = *reinterpret_cast<const float4*>(sdo + (4 * ri + i) * DP + d);
-      av[i] = *reinterpret_cast<const float4*>(sv + (4 * ri + i) * DP + d);
-    }
 #pragma unroll
-    for (int dd = 0; dd < 4; ++dd) {
-      float bh_[TNS], bg_[TNS];
-      ld_n<TNS>(shT + (d + dd) * SP + TNS * cj, bh_);
-      ld_n<TNS>(sgT + (d + dd) * SP + TNS * cj, bg_);
+      for (int j = 0; j < TNS; ++j) ah[i][j] = ag[i][j] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < TND; ++j) ab[i][j] = make_float2(0.f, 0.f);
+    }
+#pragma unroll 2
+    for (int d = 0; d < D; d += 4) {  // HDo[t][s] = sum_d dout[t][d] H_in[s][d]; Gv likewise
+      float4 ad[4], av[4], qh[TNS], qg[TNS];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ad[i] = *reinterpret_cast<const float4*>(sdo + (4 * ri + i) * DP + d);
+        av[i] = *reinterpret_cast<const float4*>(sv + (4 * ri + i) * DP + d);
+      }
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) {
+        qh[j] = *reinterpret_cast<const float4*>(sh + (cj + 16 * j) * DP + d);
+        qg[j] = *reinterpret_cast<const float4*>(sg + (cj + 16 * j) * DP + d);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < TNS; ++j) {
-          hdo[i][j] = fmaf(f4(ad[i], dd), bh_[j], hdo[i][j]);
-          gv[i][j] = fmaf(f4(av[i], dd), bg_[j], gv[i][j]);
+          ah[i][j] = dot4x2(ad[i], qh[j], ah[i][j]);
+          ag[i][j] = dot4x2(av[i], qg[j], ag[i][j]);
         }
     }
-  }
 #pragma unroll 2
-  for (int s = 0; s < S; s += 4) {
-    float4 ab[4];
+    for (int s0 = 0; s0 < S; s0 += 4) {  // Gb[tau][d] = sum_s b[tau][s] G_out^T[d][s]
+      float4 a[4], q[TND];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ab[i] = *reinterpret_cast<const float4*>(sb + (4 * ri + i) * SP + s);
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(sb + (4 * ri + i) * SP + s0);
 #pragma unroll
-    for (int ss = 0; ss < 4; ++ss) {
-      float g_[TND];
-      ld_n<TND>(sg + (s + ss) * DP + TND * cj, g_);
+      for (int j = 0; j < TND; ++j) q[j] = *reinterpret_cast<const float4*>(sgT + (cj + 16 * j) * SP + s0);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < TND; ++j) gb[i][j] = fmaf(f4(ab[i], ss), g_[j], gb[i][j]);
+        for (int j = 0; j < TND; ++j) ab[i][j] = dot4x2(a[i], q[j], ab[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) {
+        hdo[i][j] = ah[i][j].x + ah[i][j].y;
+        gv[i][j] = ag[i][j].x + ag[i][j].y;
+      }
+#pragma unroll
+      for (int j = 0; j < TND; ++j) gb[i][j] = ab[i][j].x + ab[i][j].y;
     }
   }
   // z_t = c_t . HDo_t and w_tau = b_tau . Gv_tau, summed over a row's 16 column threads
@@ -522,14 +558,11 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
     float zp[4], wp[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float cr[TNS], br[TNS];
-      ld_n<TNS>(sc + (4 * ri + i) * SP + TNS * cj, cr);
-      ld_n<TNS>(sb + (4 * ri + i) * SP + TNS * cj, br);
       zp[i] = wp[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < TNS; ++j) {
-        zp[i] = fmaf(cr[j], hdo[i][j], zp[i]);
-        wp[i] = fmaf(br[j], gv[i][j], wp[i]);
+        zp[i] = fmaf(sc[(4 * ri + i) * SP + cj + 16 * j], hdo[i][j], zp[i]);
+        wp[i] = fmaf(sb[(4 * ri + i) * SP + cj + 16 * j], gv[i][j], wp[i]);
       }
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) {
@@ -551,53 +584,19 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
   {
     const int bi = warp >> 1, bj = warp & 1;
     if (32 * bj <= 16 * bi + 15) {
-      const int li = lane >> 3, lj = lane & 7;
-      float acb[4][4], adv[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acb[i][j] = adv[i][j] = 0.f;
-#pragma unroll 2
-      for (int s = 0; s < S; s += 4) {
-        float4 a[4], q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          a[i] = *reinterpret_cast<const float4*>(sc + (16 * bi + li + 4 * i) * SP + s);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          q[j] = *reinterpret_cast<const float4*>(sb + (32 * bj + lj + 8 * j) * SP + s);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            acb[i][j] = fmaf(a[i].x, q[j].x,
-                             fmaf(a[i].y, q[j].y, fmaf(a[i].z, q[j].z, fmaf(a[i].w, q[j].w, acb[i][j]))));
-      }
-#pragma unroll 2
-      for (int d = 0; d < D; d += 4) {
-        float4 a[4], q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          a[i] = *reinterpret_cast<const float4*>(sdo + (16 * bi + li + 4 * i) * DP + d);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          q[j] = *reinterpret_cast<const float4*>(sv + (32 * bj + lj + 8 * j) * DP + d);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            adv[i][j] = fmaf(a[i].x, q[j].x,
-                             fmaf(a[i].y, q[j].y, fmaf(a[i].z, q[j].z, fmaf(a[i].w, q[j].w, adv[i][j]))));
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int o = (16 * bi + li + 4 * i) * LP + 32 * bj + lj + 8 * j;
-          scb[o] = acb[i][j];
-          sdv[o] = adv[i][j];
-        }
+      gemm_nt_block<S, LP>(sc, SP, sb, SP, 16 * bi, 32 * bj, lane >> 3, lane & 7, scb);
+      gemm_nt_block<D, LP>(sdo, DP, sv, DP, 16 * bi, 32 * bj, lane >> 3, lane & 7, sdv);
     }
+  }
+  // the column walk below splits rows into quarters; here each (column, quarter)
+  // forms the product of the quarter's gates that enter D (rows t > tau)
+  {
+    const int tau = 32 * (warp & 1) + lane, tq = 16 * (warp >> 1);
+    float f = 1.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (tq + i > tau) f *= sal[tq + i];
+    sqf[(warp >> 1) * kL + tau] = f;
   }
   __syncthreads();
 
@@ -650,18 +649,10 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
 
   // ---- down each column tau: D[t][tau] for t >= tau; P and dS in place, dS^T
   // (zero below its diagonal), dalpha_tau. Warp w takes columns
-  // 32 (w & 1) .. + 31 over the row quarter 16 (w >> 1) .. + 15: first the
-  // quarter's product of the gates that enter D (rows t > tau), exchanged
-  // through shared memory, then the walk from the product of the earlier
-  // quarters. ----
+  // 32 (w & 1) .. + 31 over the row quarter 16 (w >> 1) .. + 15, starting from
+  // the product of the earlier quarters' gates. ----
   {
     const int tau = 32 * (warp & 1) + lane, q = warp >> 1, tq = 16 * q;
-    float f = 1.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (tq + i > tau) f *= sal[tq + i];
-    sqf[q * kL + tau] = f;
-    __syncthreads();
     float dec = 1.f;
     for (int i = 0; i < q; ++i) dec *= sqf[i * kL + tau];
     const float gm = sgm1[tau];
@@ -716,8 +707,10 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
       const float4 ds = *reinterpret_cast<const float4*>(sdv + t * LP + 4 * ri);
       const float4 pp = *reinterpret_cast<const float4*>(scb + t * LP + 4 * ri);
       float cr[TNS], dr[TND];
-      ld_n<TNS>(sc + t * SP + TNS * cj, cr);
-      ld_n<TND>(sdo + t * DP + TND * cj, dr);
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) cr[j] = sc[t * SP + cj + 16 * j];
+#pragma unroll
+      for (int j = 0; j < TND; ++j) dr[j] = sdo[t * DP + cj + 16 * j];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -732,7 +725,8 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
     for (int tau = 0; tau < thi; ++tau) {
       const float4 a = *reinterpret_cast<const float4*>(sdsT + tau * LP + 4 * ri);
       float br[TNS];
-      ld_n<TNS>(sb + tau * SP + TNS * cj, br);
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) br[j] = sb[tau * SP + cj + 16 * j];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -742,9 +736,13 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
     for (int i = 0; i < 4; ++i) {
       const int m = 4 * ri + i;
       if (m < n) {
-        st_n<TNS>(p.db + (r0 + m) * S + TNS * cj, adb[i]);
-        st_n<TNS>(p.dc + (r0 + m) * S + TNS * cj, adc[i]);
-        st_n<TND>(p.dv + (r0 + m) * D + TND * cj, adv[i]);
+#pragma unroll
+        for (int j = 0; j < TNS; ++j) {
+          __stcs(p.db + (r0 + m) * S + cj + 16 * j, adb[i][j]);
+          __stcs(p.dc + (r0 + m) * S + cj + 16 * j, adc[i][j]);
+        }
+#pragma unroll
+        for (int j = 0; j < TND; ++j) __stcs(p.dv + (r0 + m) * D + cj + 16 * j, adv[i][j]);
       }
     }
   }

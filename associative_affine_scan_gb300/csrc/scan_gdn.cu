@@ -63,6 +63,30 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Two fp32 fused multiply-adds in one packed instruction (sm_100 and later):
+// {a.x b.x + c.x, a.y b.y + c.y}, each rounded once, as fmaf would.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long A, B, C, R;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
+  return r;
+}
+
+// {a.x b.x, a.y b.y} in one packed instruction, each rounded once
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long A, B, R;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(R) : "l"(A), "l"(B));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
+  return r;
+}
+
 // Thread layout of a head's block: warp w owns columns CW w .. CW w + CW - 1
 // of h; lane l holds column CW w + (l % CW) and the RS = S / RG rows of row
 // group g = l / CW (RG = 32 / CW row groups). Columns evolve independently,
@@ -75,7 +99,7 @@ struct Layout {
   static constexpr int RS = S / RG;    // rows per lane
   static constexpr int NW = D / CW;    // warps per head
   static constexpr int NT = 32 * NW;   // threads per block
-  static_assert(RS >= 1 && RS <= CW && NW >= 1, "layout");
+  static_assert(RS >= 2 && RS % 2 == 0 && RS <= CW && NW >= 1, "layout");
 };
 
 // Asynchronous 16-byte copies of n floats (n % 4 == 0) by the block's threads.
@@ -152,27 +176,32 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
     const int st = blk & 1;
     const int64_t t0 = (int64_t)blk * kStage;
     const int rows = (int)(T - t0 < kStage ? T - t0 : kStage);
+    if (p.ckpt && (t0 % kCoarse) == 0) {  // stages start on 32-step boundaries
+      float* ck = p.ckpt + (bh * p.NC + t0 / kCoarse) * S * D;
+#pragma unroll
+      for (int i = 0; i < RS; ++i) ck[(s0 + i) * D + d] = h[i];
+    }
 #pragma unroll 4
     for (int r = 0; r < rows; ++r) {
       const int64_t t = t0 + r;
-      if (p.ckpt && (t % kCoarse) == 0) {
-        float* ck = p.ckpt + (bh * p.NC + t / kCoarse) * S * D;
-#pragma unroll
-        for (int i = 0; i < RS; ++i) ck[(s0 + i) * D + d] = h[i];
-      }
       const float al = s_al[st][r];
       const float vd = s_v[st][r * D + d];
       float bb[RS], cc[RS];
       ld_row<RS>(s_b[st] + r * S + s0, bb);
       ld_row<RS>(s_c[st] + r * S + s0, cc);
-      float acc0 = 0.f, acc1 = 0.f;
+      // h = alpha h + b v (the product rounded, then one fused step) and the
+      // read-out's two interleaved partial sums, two rows per instruction
+      const float2 al2 = make_float2(al, al), vd2 = make_float2(vd, vd);
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < RS; ++i) {
-        h[i] = fmaf(al, h[i], bb[i] * vd);
-        if (i & 1) acc1 = fmaf(cc[i], h[i], acc1);
-        else acc0 = fmaf(cc[i], h[i], acc0);
+      for (int i = 0; i < RS; i += 2) {
+        const float2 bv = fmul2(make_float2(bb[i], bb[i + 1]), vd2);
+        const float2 hp = ffma2(al2, make_float2(h[i], h[i + 1]), bv);
+        h[i] = hp.x;
+        h[i + 1] = hp.y;
+        acc = ffma2(make_float2(cc[i], cc[i + 1]), hp, acc);
       }
-      float o = acc0 + acc1;
+      float o = acc.x + acc.y;
 #pragma unroll
       for (int m = CW; m < 32; m <<= 1) o += __shfl_xor_sync(kFullMask, o, m);
       if (g == 0) __stcs(p.o + (bh * T + t) * D + d, o);
@@ -351,19 +380,6 @@ struct ChunkSmem {
 
 __device__ __forceinline__ float f4(const float4& q, int i) {
   return i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
-}
-
-// Two fp32 fused multiply-adds in one packed instruction (sm_100 and later):
-// {a.x b.x + c.x, a.y b.y + c.y}, each rounded once, as fmaf would.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long A, B, C, R;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R) : "l"(A), "l"(B), "l"(C));
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(R));
-  return r;
 }
 
 // acc += the dot product of two 4-vectors, as two interleaved partial sums

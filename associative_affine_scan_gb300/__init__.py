@@ -42,7 +42,7 @@ from ._binding import (  # noqa: F401
     affine_prefix_bwd,
     gdn_checkpoint_bytes,
     gdn_fwd,
-    gdn_bwd_workspace_bytes,
+    gdn_workspace_bytes,
     gdn_bwd,
     affine_scan_fwd,
     lib,

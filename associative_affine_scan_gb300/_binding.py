@@ -50,7 +50,7 @@ EXPORTED = (
     "scan_status_string", "scan_version", "scan_workspace_bytes", "scan_workspace_init",
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
     "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "affine_prefix_fwd",
-    "affine_prefix_bwd", "gdn_checkpoint_bytes", "gdn_fwd", "gdn_bwd_workspace_bytes", "gdn_bwd",
+    "affine_prefix_bwd", "gdn_checkpoint_bytes", "gdn_fwd", "gdn_workspace_bytes", "gdn_bwd",
     "scan_fwd_noalloc",
 )
 
@@ -107,9 +107,9 @@ _SIGS = {
                          _vp, _sz, _vp], ctypes.c_int),
     "affine_prefix_fwd": ([_vp, _vp, _i64, _i64, _i64, _i32, _opt, _vp, _sz, _vp], ctypes.c_int),
     "gdn_checkpoint_bytes": ([_i64, _i64, _i64, _i64, _i64], ctypes.c_size_t),
-    "gdn_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp],
-                ctypes.c_int),
-    "gdn_bwd_workspace_bytes": ([_i64, _i64, _i64, _i64, _i64], ctypes.c_size_t),
+    "gdn_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _sz,
+                 _vp], ctypes.c_int),
+    "gdn_workspace_bytes": ([_i64, _i64, _i64, _i64, _i64], ctypes.c_size_t),
     "gdn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                  _i64, _vp, _sz, _vp], ctypes.c_int),
     "affine_prefix_bwd": ([_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i32, _opt, _vp, _sz, _vp],
@@ -545,10 +545,13 @@ def _gdn_dims(alpha, b, v, c):
     return B, H, T, S, D
 
 
-def gdn_fwd(alpha, b, v, c, h0=None, *, checkpoints=True, out=None, stream=None):
+def gdn_fwd(alpha, b, v, c, h0=None, *, checkpoints=True, out=None, workspace=None,
+            stream=None):
     """o_t = h_t^T c_t with h_t = alpha_t h_{t-1} + b_t v_t^T. Returns (o, ckpt),
     ckpt being the backward's checkpoint buffer: allocated (checkpoints=True),
-    the given fp32 tensor of gdn_checkpoint_bytes() bytes, or None (False)."""
+    the given fp32 tensor of gdn_checkpoint_bytes() bytes, or None (False).
+    workspace: a device tensor of at least gdn_workspace_bytes() bytes
+    (allocated here when None)."""
     B, H, T, S, D = _gdn_dims(alpha, b, v, c)
     dev = alpha.device
     _need(h0, "h0", dtype=torch.float32, shape=(B, H, S, D), device=dev)
@@ -563,22 +566,33 @@ def gdn_fwd(alpha, b, v, c, h0=None, *, checkpoints=True, out=None, stream=None)
             raise ValueError(f"checkpoints: needs {n} contiguous floats")
     elif checkpoints:
         ckpt = torch.empty(max(n, 1), dtype=torch.float32, device=dev)
+    workspace = _gdn_workspace(workspace, B, H, T, S, D, dev, "gdn_fwd")
     s = _stream(stream, dev)
     st = lib().gdn_fwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(o), _ptr(ckpt),
-                       B, H, T, S, D, s)
+                       B, H, T, S, D, _ptr(workspace),
+                       workspace.numel() * workspace.element_size(), s)
     _check(st, "gdn_fwd")
     return o, ckpt
 
 
-def gdn_bwd_workspace_bytes(B, H, T, S, D) -> int:
-    return int(lib().gdn_bwd_workspace_bytes(B, H, T, S, D))
+def gdn_workspace_bytes(B, H, T, S, D) -> int:
+    return int(lib().gdn_workspace_bytes(B, H, T, S, D))
+
+
+def _gdn_workspace(workspace, B, H, T, S, D, dev, name):
+    nws = gdn_workspace_bytes(B, H, T, S, D)
+    if workspace is None:
+        return torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    if not workspace.is_contiguous() or workspace.numel() * workspace.element_size() < nws:
+        raise ValueError(f"{name} workspace must be a contiguous tensor of >= {nws} bytes")
+    return workspace
 
 
 def gdn_bwd(alpha, b, v, c, ckpt, dout, *, need_dh0=True, out=None, workspace=None,
             stream=None):
     """Backward of L = sum <dout_t, o_t>: returns (dalpha, db, dv, dc, dh0).
 
-    workspace: a device tensor of at least gdn_bwd_workspace_bytes() bytes
+    workspace: a device tensor of at least gdn_workspace_bytes() bytes
     (allocated here when None)."""
     B, H, T, S, D = _gdn_dims(alpha, b, v, c)
     dev = alpha.device
@@ -590,11 +604,7 @@ def gdn_bwd(alpha, b, v, c, ckpt, dout, *, need_dh0=True, out=None, workspace=No
     else:
         dal, db, dv, dc = (torch.empty_like(t) for t in (alpha, b, v, c))
         dh0 = torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if need_dh0 else None
-    nws = gdn_bwd_workspace_bytes(B, H, T, S, D)
-    if workspace is None:
-        workspace = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
-    if not workspace.is_contiguous() or workspace.numel() * workspace.element_size() < nws:
-        raise ValueError(f"gdn_bwd workspace must be a contiguous tensor of >= {nws} bytes")
+    workspace = _gdn_workspace(workspace, B, H, T, S, D, dev, "gdn_bwd")
     s = _stream(stream, dev)
     st = lib().gdn_bwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(ckpt), _ptr(dout), _ptr(dal),
                        _ptr(db), _ptr(dv), _ptr(dc), _ptr(dh0), B, H, T, S, D, _ptr(workspace),

@@ -5,20 +5,13 @@
 //   o_t = h_t^T c_t                         (D-vector)
 // and its reverse-time backward with the states recomputed from checkpoints.
 //
-// Work decomposition: one block per (batch, head) walks T with the state in
-// registers, split by columns over D / CW warps (columns of h evolve
-// independently); a lane holds S / RG rows of one column. The per-step inputs
-// (b_t, c_t, v_t, alpha_t) are staged in shared memory by asynchronous 16-byte
-// copies, 32 steps per stage, two stages in flight. The forward stores the
-// state before every 64th step (the checkpoints the backward starts from). The
-// backward walks those 64-step blocks from the end: it stages the block's
-// inputs, recomputes the block's states forward keeping the one before every
-// 8th step, and then, for each 8-step piece from the last, recomputes its
-// states into registers and runs the adjoint over them:
-// dh_t = c_t do_t^T + alpha_{t+1} dh_{t+1}, dv_t = dh_t^T b_t (a column's
-// rows summed by shuffles), db_t = dh_t v_t and dc_t = h_t do_t (a
-// reduce-scatter of shuffles over the warp's columns, then a sum over warps in
-// shared memory once per piece), dalpha_t = <dh_t, h_{t-1}>.
+// Work decomposition: both directions are cut into 64-step chunks (the
+// checkpoint interval) that run in parallel; only the S x D state between
+// chunks (forward) or its adjoint (backward) is carried serially, by a short
+// kernel per head (see the section on the chunked form below). Within a chunk
+// the forward walks the steps with the state in registers, a block of D / 8
+// warps per chunk, each warp 8 state columns x 4 row groups; the backward
+// forms the chunk's gradients as small matrix products in shared memory.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -133,54 +126,202 @@ __device__ __forceinline__ void ld_row(const float* src, float (&x)[N]) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Both directions run chunked over T in 64-step chunks (the checkpoint
+// interval). Per chunk of n steps with gates alpha_0 .. alpha_{n-1}:
+//   forward:  H_out = Gamma H_in + U,   U = sum_tau w_tau b_tau v_tau^T,
+//             w_tau = alpha_{tau+1} .. alpha_{n-1},  Gamma = alpha_0 .. alpha_{n-1};
+//   backward: G_in = Gamma G_out + V,   V = sum_t Gamma_t c_t dout_t^T,
+//             Gamma_t = alpha_0 .. alpha_t
+// (the page's chunked GDN algorithm: a chunk's effect on the state is one
+// scale and one rank-n update). A first launch forms U (or V) and Gamma for
+// every chunk in parallel; a second walks each head's chunks in order with
+// the S x D state (or adjoint) in registers, leaving in the workspace the
+// state before (adjoint after) each chunk; a third runs every chunk in
+// parallel from it.
+// ---------------------------------------------------------------------------
+
+constexpr int kL = kCoarse;  // steps per chunk (the checkpoint interval)
+
+template <int S, int D>
+struct SumLayout {
+  static constexpr int NT = (S / 2) * (D / 4);  // a thread owns 2 x 4 entries of the sum
+};
+
+// Product scans of 64 values held two per lane (v0 = element 2 l, v1 =
+// element 2 l + 1). prefix: returns the product of the elements before the
+// lane's pair and sets incl to the product through it. suffix: returns the
+// product of the elements after the pair and sets total to the product of all.
+__device__ __forceinline__ float prefix_prod64(float v0, float v1, int lane, float& incl) {
+  float x = v0 * v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFullMask, x, o);
+    if (lane >= o) x *= y;
+  }
+  float e = __shfl_up_sync(kFullMask, x, 1);
+  if (lane == 0) e = 1.f;
+  incl = x;
+  return e;
+}
+
+__device__ __forceinline__ float suffix_prod64(float v0, float v1, int lane, float& total) {
+  float x = v0 * v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_down_sync(kFullMask, x, o);
+    if (lane + o < 32) x *= y;
+  }
+  float e = __shfl_down_sync(kFullMask, x, 1);
+  if (lane == 31) e = 1.f;
+  total = __shfl_sync(kFullMask, x, 0);
+  return e;
+}
+
+// U (FWD: sum_tau w_tau b_tau v_tau^T) or V (sum_t Gamma_t c_t dout_t^T) of
+// one chunk into the workspace, with the chunk's gate product.
+template <int S, int D, bool FWD>
+__global__ void __launch_bounds__(SumLayout<S, D>::NT) gdn_chunk_sum_kernel(const GdnParams p) {
+  constexpr int NT = SumLayout<S, D>::NT;
+  __shared__ __align__(16) float s_x[kL * S];
+  __shared__ __align__(16) float s_y[kL * D];
+  __shared__ float s_g[kL];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t blk = blockIdx.x, bh = blk / p.NC, k = blk - bh * p.NC;
+  const int64_t T = p.T, r0 = bh * T + k * kL;
+  const int n = (int)(T - k * kL < kL ? T - k * kL : kL);
+  stage_block(s_x, (FWD ? p.b : p.c) + r0 * S, n * S, tid, NT);
+  stage_block(s_y, (FWD ? p.v : p.dout) + r0 * D, n * D, tid, NT);
+  cp_async_commit();
+  if (tid < 32) {  // gates past the chunk's end count as 1
+    const float a0 = 2 * lane < n ? __ldg(p.alpha + r0 + 2 * lane) : 1.f;
+    const float a1 = 2 * lane + 1 < n ? __ldg(p.alpha + r0 + 2 * lane + 1) : 1.f;
+    float all;
+    if constexpr (FWD) {
+      const float e = suffix_prod64(a0, a1, lane, all);
+      s_g[2 * lane + 1] = e;
+      s_g[2 * lane] = a1 * e;
+    } else {
+      const float e = prefix_prod64(a0, a1, lane, all);
+      s_g[2 * lane] = e * a0;
+      s_g[2 * lane + 1] = all;
+      all = __shfl_sync(kFullMask, all, 31);
+    }
+    if (lane == 0) p.wsG[blk] = all;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  const int si = tid / (D / 4), dj = tid - si * (D / 4);
+  float acc[2][4] = {};
+  for (int t = 0; t < n; ++t) {
+    const float g = s_g[t];
+    const float2 xq = *reinterpret_cast<const float2*>(s_x + t * S + 2 * si);
+    const float4 yq = *reinterpret_cast<const float4*>(s_y + t * D + 4 * dj);
+    const float x0 = xq.x * g, x1 = xq.y * g;
+    acc[0][0] = fmaf(x0, yq.x, acc[0][0]);
+    acc[0][1] = fmaf(x0, yq.y, acc[0][1]);
+    acc[0][2] = fmaf(x0, yq.z, acc[0][2]);
+    acc[0][3] = fmaf(x0, yq.w, acc[0][3]);
+    acc[1][0] = fmaf(x1, yq.x, acc[1][0]);
+    acc[1][1] = fmaf(x1, yq.y, acc[1][1]);
+    acc[1][2] = fmaf(x1, yq.z, acc[1][2]);
+    acc[1][3] = fmaf(x1, yq.w, acc[1][3]);
+  }
+  float* out = p.wsS + blk * S * D;
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    *reinterpret_cast<float4*>(out + (2 * si + i) * D + 4 * dj) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+}
+
+// One thread per 4 entries of a head's S x D state (FWD, chunks in order from
+// h0; also written to the checkpoints) or adjoint (chunks from the last, from
+// 0; dh0 at the end). The loads of the next 8 chunks are in flight while the
+// current 8 are chained.
+template <int S, int D, bool FWD>
+__global__ void __launch_bounds__(S * D / 4) gdn_carry_kernel(const GdnParams p) {
+  constexpr int Q = S * D / 4, G8 = 8;
+  const int tid = threadIdx.x;
+  const int64_t bh = blockIdx.x, NC = p.NC;
+  float4* ws = reinterpret_cast<float4*>(p.wsS + bh * NC * S * D) + tid;
+  float4* ck = p.ckpt ? reinterpret_cast<float4*>(p.ckpt + bh * NC * S * D) + tid : nullptr;
+  const float* gam = p.wsG + bh * NC;
+  auto chunk = [&](int64_t i) { return FWD ? i : NC - 1 - i; };
+  float4 H = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (FWD && p.h0) H = reinterpret_cast<const float4*>(p.h0 + bh * S * D)[tid];
+  float4 U[G8], Un[G8];
+  float g[G8], gn[G8];
+#pragma unroll
+  for (int j = 0; j < G8; ++j)
+    if (j < NC) {
+      U[j] = __ldcg(ws + chunk(j) * Q);
+      g[j] = __ldcg(gam + chunk(j));
+    }
+  for (int64_t i0 = 0; i0 < NC; i0 += G8) {
+#pragma unroll
+    for (int j = 0; j < G8; ++j)
+      if (i0 + G8 + j < NC) {
+        Un[j] = __ldcg(ws + chunk(i0 + G8 + j) * Q);
+        gn[j] = __ldcg(gam + chunk(i0 + G8 + j));
+      }
+#pragma unroll
+    for (int j = 0; j < G8; ++j)
+      if (i0 + j < NC) {
+        const int64_t c = chunk(i0 + j);
+        ws[c * Q] = H;  // state before (adjoint after) chunk c
+        if (FWD && ck) ck[c * Q] = H;
+        H = make_float4(fmaf(g[j], H.x, U[j].x), fmaf(g[j], H.y, U[j].y), fmaf(g[j], H.z, U[j].z),
+                        fmaf(g[j], H.w, U[j].w));
+      }
+#pragma unroll
+    for (int j = 0; j < G8; ++j) {
+      U[j] = Un[j];
+      g[j] = gn[j];
+    }
+  }
+  if (!FWD && p.dh0) reinterpret_cast<float4*>(p.dh0 + bh * S * D)[tid] = H;
+}
+
+// One 64-step chunk per block, from the state before it (in the workspace).
 template <int S, int D, int CW_>
 __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const GdnParams p) {
   using LY = Layout<S, D, CW_>;
   constexpr int CW = LY::CW, RS = LY::RS, NT = LY::NT;
+  static_assert(kL == 2 * kStage, "two stages per chunk");
   __shared__ __align__(16) float s_b[2][kStage * S];
   __shared__ __align__(16) float s_c[2][kStage * S];
   __shared__ __align__(16) float s_v[2][kStage * D];
   __shared__ float s_al[2][kStage];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = warp * CW + lane % CW, g = lane / CW, s0 = g * RS;
-  const int64_t bh = blockIdx.x;
-  if (bh >= p.BH) return;
-  const int64_t T = p.T;
-  float h[RS];
-#pragma unroll
-  for (int i = 0; i < RS; ++i) h[i] = p.h0 ? p.h0[(bh * S + s0 + i) * D + d] : 0.f;
-
+  const int64_t blk = blockIdx.x, bh = blk / p.NC, k = blk - bh * p.NC;
+  const int64_t T = p.T, tc = k * kL;
+  const int n = (int)(T - tc < kL ? T - tc : kL);
+  const int nst = (n + kStage - 1) / kStage;
   const float* gb = p.b + bh * T * S;
   const float* gc = p.c + bh * T * S;
   const float* gv = p.v + bh * T * D;
-  const int nblk = (int)((T + kStage - 1) / kStage);
-  auto issue = [&](int blk) {
-    const int64_t t0 = (int64_t)blk * kStage;
+  for (int st = 0; st < nst; ++st) {
+    const int64_t t0 = tc + st * kStage;
     const int rows = (int)(T - t0 < kStage ? T - t0 : kStage);
-    const int st = blk & 1;
     stage_block(s_b[st], gb + t0 * S, rows * S, tid, NT);
     stage_block(s_c[st], gc + t0 * S, rows * S, tid, NT);
     stage_block(s_v[st], gv + t0 * D, rows * D, tid, NT);
     cp_async_commit();
     if (tid < rows) s_al[st][tid] = __ldg(p.alpha + bh * T + t0 + tid);
-  };
-  issue(0);
-  for (int blk = 0; blk < nblk; ++blk) {
-    if (blk + 1 < nblk) {
-      issue(blk + 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const int st = blk & 1;
-    const int64_t t0 = (int64_t)blk * kStage;
-    const int rows = (int)(T - t0 < kStage ? T - t0 : kStage);
-    if (p.ckpt && (t0 % kCoarse) == 0) {  // stages start on 32-step boundaries
-      float* ck = p.ckpt + (bh * p.NC + t0 / kCoarse) * S * D;
+  }
+  float h[RS];
+  {
+    const float* hin = p.wsS + blk * S * D;
 #pragma unroll
-      for (int i = 0; i < RS; ++i) ck[(s0 + i) * D + d] = h[i];
-    }
+    for (int i = 0; i < RS; ++i) h[i] = __ldcg(hin + (s0 + i) * D + d);
+  }
+  for (int st = 0; st < nst; ++st) {
+    if (st + 1 < nst) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncthreads();
+    const int64_t t0 = tc + st * kStage;
+    const int rows = (int)(T - t0 < kStage ? T - t0 : kStage);
 #pragma unroll 4
     for (int r = 0; r < rows; ++r) {
       const int64_t t = t0 + r;
@@ -206,7 +347,6 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
       for (int m = CW; m < 32; m <<= 1) o += __shfl_xor_sync(kFullMask, o, m);
       if (g == 0) __stcs(p.o + (bh * T + t) * D + d, o);
     }
-    __syncthreads();  // the stage is refilled two blocks later
   }
 }
 
@@ -234,118 +374,6 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
 // leaving each chunk's G_out in the workspace and dh0 = G_in of chunk 0;
 // (3) per chunk, the gradients above as small GEMMs in shared memory.
 // ---------------------------------------------------------------------------
-
-constexpr int kL = kCoarse;  // steps per chunk (the checkpoint interval)
-
-template <int S, int D>
-struct AdjLayout {
-  static constexpr int NT = (S / 2) * (D / 4);  // a thread owns 2 x 4 entries of V
-};
-
-// Product scan of 64 values held two per lane (v0 = element 2 l, v1 = element
-// 2 l + 1): returns the product of the elements before the lane's pair and
-// sets incl to the product through it.
-__device__ __forceinline__ float prefix_prod64(float v0, float v1, int lane, float& incl) {
-  float x = v0 * v1;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(kFullMask, x, o);
-    if (lane >= o) x *= y;
-  }
-  float e = __shfl_up_sync(kFullMask, x, 1);
-  if (lane == 0) e = 1.f;
-  incl = x;
-  return e;
-}
-
-template <int S, int D>
-__global__ void __launch_bounds__(AdjLayout<S, D>::NT) gdn_bwd_adj_kernel(const GdnParams p) {
-  constexpr int NT = AdjLayout<S, D>::NT;
-  __shared__ __align__(16) float s_c[kL * S];
-  __shared__ __align__(16) float s_do[kL * D];
-  __shared__ float s_g[kL];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int64_t blk = blockIdx.x, bh = blk / p.NC, k = blk - bh * p.NC;
-  const int64_t T = p.T, r0 = bh * T + k * kL;
-  const int n = (int)(T - k * kL < kL ? T - k * kL : kL);
-  stage_block(s_c, p.c + r0 * S, n * S, tid, NT);
-  stage_block(s_do, p.dout + r0 * D, n * D, tid, NT);
-  cp_async_commit();
-  if (tid < 32) {  // Gamma_t within the chunk (gates past its end count as 1)
-    const float a0 = 2 * lane < n ? __ldg(p.alpha + r0 + 2 * lane) : 1.f;
-    const float a1 = 2 * lane + 1 < n ? __ldg(p.alpha + r0 + 2 * lane + 1) : 1.f;
-    float incl;
-    const float e = prefix_prod64(a0, a1, lane, incl);
-    s_g[2 * lane] = e * a0;
-    s_g[2 * lane + 1] = incl;
-    if (lane == 31) p.wsG[blk] = incl;
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-  const int si = tid / (D / 4), dj = tid - si * (D / 4);
-  float acc[2][4] = {};
-  for (int t = 0; t < n; ++t) {
-    const float g = s_g[t];
-    const float2 cq = *reinterpret_cast<const float2*>(s_c + t * S + 2 * si);
-    const float4 dq = *reinterpret_cast<const float4*>(s_do + t * D + 4 * dj);
-    const float c0 = cq.x * g, c1 = cq.y * g;
-    acc[0][0] = fmaf(c0, dq.x, acc[0][0]);
-    acc[0][1] = fmaf(c0, dq.y, acc[0][1]);
-    acc[0][2] = fmaf(c0, dq.z, acc[0][2]);
-    acc[0][3] = fmaf(c0, dq.w, acc[0][3]);
-    acc[1][0] = fmaf(c1, dq.x, acc[1][0]);
-    acc[1][1] = fmaf(c1, dq.y, acc[1][1]);
-    acc[1][2] = fmaf(c1, dq.z, acc[1][2]);
-    acc[1][3] = fmaf(c1, dq.w, acc[1][3]);
-  }
-  float* V = p.wsS + blk * S * D;
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-    *reinterpret_cast<float4*>(V + (2 * si + i) * D + 4 * dj) =
-        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-}
-
-// One thread per 4 entries of a head's S x D adjoint, walking the chunks from
-// the last; the loads of the next 8 chunks are in flight while the current 8
-// are chained.
-template <int S, int D>
-__global__ void __launch_bounds__(S * D / 4) gdn_bwd_carry_kernel(const GdnParams p) {
-  constexpr int Q = S * D / 4, G8 = 8;
-  const int tid = threadIdx.x;
-  const int64_t bh = blockIdx.x, NC = p.NC;
-  float4* ws = reinterpret_cast<float4*>(p.wsS + bh * NC * S * D) + tid;
-  const float* gam = p.wsG + bh * NC;
-  float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 V[G8], Vn[G8];
-  float g[G8], gn[G8];
-#pragma unroll
-  for (int j = 0; j < G8; ++j)
-    if (NC - 1 - j >= 0) {
-      V[j] = __ldcg(ws + (NC - 1 - j) * Q);
-      g[j] = __ldcg(gam + NC - 1 - j);
-    }
-  for (int64_t kb = NC - 1; kb >= 0; kb -= G8) {
-#pragma unroll
-    for (int j = 0; j < G8; ++j)
-      if (kb - G8 - j >= 0) {
-        Vn[j] = __ldcg(ws + (kb - G8 - j) * Q);
-        gn[j] = __ldcg(gam + kb - G8 - j);
-      }
-#pragma unroll
-    for (int j = 0; j < G8; ++j)
-      if (kb - j >= 0) {
-        ws[(kb - j) * Q] = G;  // adjoint of the state after chunk kb - j
-        G = make_float4(fmaf(g[j], G.x, V[j].x), fmaf(g[j], G.y, V[j].y), fmaf(g[j], G.z, V[j].z),
-                        fmaf(g[j], G.w, V[j].w));
-      }
-#pragma unroll
-    for (int j = 0; j < G8; ++j) {
-      V[j] = Vn[j];
-      g[j] = gn[j];
-    }
-  }
-  if (p.dh0) reinterpret_cast<float4*>(p.dh0 + bh * S * D)[tid] = G;
-}
 
 // Shared memory of the chunk-gradient kernel, in floats. Rows are padded by 4
 // floats (16-byte aligned, conflict-free 16-byte reads of consecutive rows).
@@ -766,15 +794,18 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
 
 template <int S, int D, int CW>
 cudaError_t launch_fwd(const GdnParams& p, cudaStream_t s) {
-  gdn_fwd_kernel<S, D, CW><<<(unsigned)p.BH, Layout<S, D, CW>::NT, 0, s>>>(p);
+  const unsigned nblk = (unsigned)(p.BH * p.NC);
+  gdn_chunk_sum_kernel<S, D, true><<<nblk, SumLayout<S, D>::NT, 0, s>>>(p);
+  gdn_carry_kernel<S, D, true><<<(unsigned)p.BH, S * D / 4, 0, s>>>(p);
+  gdn_fwd_kernel<S, D, CW><<<nblk, Layout<S, D, CW>::NT, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 template <int S, int D>
 cudaError_t launch_bwd(const GdnParams& p, cudaStream_t s) {
   const unsigned nblk = (unsigned)(p.BH * p.NC);
-  gdn_bwd_adj_kernel<S, D><<<nblk, AdjLayout<S, D>::NT, 0, s>>>(p);
-  gdn_bwd_carry_kernel<S, D><<<(unsigned)p.BH, S * D / 4, 0, s>>>(p);
+  gdn_chunk_sum_kernel<S, D, false><<<nblk, SumLayout<S, D>::NT, 0, s>>>(p);
+  gdn_carry_kernel<S, D, false><<<(unsigned)p.BH, S * D / 4, 0, s>>>(p);
   const size_t smem = sizeof(float) * (size_t)ChunkSmem<S, D>::total;
   cudaError_t e = cudaFuncSetAttribute(gdn_bwd_chunk_kernel<S, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -815,7 +846,7 @@ size_t gdn_checkpoint_bytes(int64_t B, int64_t H, int64_t T, int64_t S, int64_t 
   return sizeof(float) * (size_t)(B * H) * (size_t)((T + kCoarse - 1) / kCoarse) * (size_t)(S * D);
 }
 
-size_t gdn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t T, int64_t S, int64_t D) {
+size_t gdn_workspace_bytes(int64_t B, int64_t H, int64_t T, int64_t S, int64_t D) {
   if (B < 0 || H < 0 || T < 0 || !shape_ok(S, D)) return 0;
   const size_t chunks = (size_t)(B * H) * (size_t)((T + kL - 1) / kL);
   return sizeof(float) * (chunks * (size_t)(S * D) + round_up(chunks, 4));
@@ -823,14 +854,18 @@ size_t gdn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t T, int64_t S, int64
 
 scan_status gdn_fwd(const float* alpha, const float* b, const float* v, const float* c,
                     const float* h0, float* o, float* ckpt, int64_t B, int64_t H, int64_t T,
-                    int64_t S, int64_t D, cudaStream_t stream) {
+                    int64_t S, int64_t D, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
   if (B < 0 || H < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
   if (!shape_ok(S, D)) return SCAN_ERR_UNSUPPORTED;
   if (B * H * T == 0) return SCAN_OK;
   if (!alpha || !b || !v || !c || !o) return SCAN_ERR_INVALID_ARG;
   if (!al16(b) || !al16(v) || !al16(c) || !al16(h0) || !al16(o) || !al16(ckpt))
     return SCAN_ERR_ALIGNMENT;
-  if (B * H > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
+  const int64_t NC = (T + kL - 1) / kL;
+  if (B * H * NC > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
+  if (!workspace || !al16(workspace) || workspace_bytes < gdn_workspace_bytes(B, H, T, S, D))
+    return SCAN_ERR_WORKSPACE;
   GdnParams p{};
   p.alpha = alpha;
   p.b = b;
@@ -839,9 +874,11 @@ scan_status gdn_fwd(const float* alpha, const float* b, const float* v, const fl
   p.h0 = h0;
   p.o = o;
   p.ckpt = ckpt;
+  p.wsS = static_cast<float*>(workspace);
+  p.wsG = p.wsS + (size_t)(B * H * NC) * (size_t)(S * D);
   p.BH = B * H;
   p.T = T;
-  p.NC = (T + kCoarse - 1) / kCoarse;
+  p.NC = NC;
   return dispatch(p, (int)S, (int)D, true, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
 }
 
@@ -865,7 +902,7 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v, const fl
     return SCAN_ERR_ALIGNMENT;
   const int64_t NC = (T + kL - 1) / kL;
   if (B * H * NC > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
-  if (!workspace || !al16(workspace) || workspace_bytes < gdn_bwd_workspace_bytes(B, H, T, S, D))
+  if (!workspace || !al16(workspace) || workspace_bytes < gdn_workspace_bytes(B, H, T, S, D))
     return SCAN_ERR_WORKSPACE;
   GdnParams p{};
   p.alpha = alpha;

@@ -325,14 +325,13 @@ def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
     w = workloads.gdn_4k(seed=0)
     alpha, b, v, c, dout = (t.to(dev) for t in (w.alpha, w.b, w.v, w.c, w.dout))
     S, D = b.shape[-1], v.shape[-1]
-    o, ck = scan.gdn_fwd(alpha, b, v, c)
+    ws = torch.empty(scan.gdn_workspace_bytes(*alpha.shape, S, D), dtype=torch.uint8, device=dev)
+    o, ck = scan.gdn_fwd(alpha, b, v, c, workspace=ws)
     n = alpha.numel()
     f_bytes = n * (4 + 8 * S + 8 * D) + ck.numel() * 4
     b_bytes = n * (8 + 16 * S + 16 * D) + ck.numel() * 4
-    f_ms = time_calls(lambda: scan.gdn_fwd(alpha, b, v, c, checkpoints=ck, out=o), steps, warm,
-                      flush, stream)
-    ws = torch.empty(scan.gdn_bwd_workspace_bytes(*alpha.shape, S, D), dtype=torch.uint8,
-                     device=dev)
+    f_ms = time_calls(lambda: scan.gdn_fwd(alpha, b, v, c, checkpoints=ck, out=o, workspace=ws),
+                      steps, warm, flush, stream)
     g = scan.gdn_bwd(alpha, b, v, c, ck, dout, workspace=ws)
     b_ms = time_calls(lambda: scan.gdn_bwd(alpha, b, v, c, ck, dout, out=g, workspace=ws), steps,
                       warm, flush, stream)

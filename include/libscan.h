@@ -288,12 +288,19 @@ scan_status affine_prefix_bwd(const float* A, const float* Abar,
  * (else SCAN_ERR_UNSUPPORTED); b, c, v, o, h0, ckpt 16-byte aligned (else
  * SCAN_ERR_ALIGNMENT). ckpt (nullable): gdn_checkpoint_bytes() bytes, filled
  * with the state before every 64th step, [B,H,ceil(T/64),S,D]; the backward
- * starts from it. No workspace; asynchronous on `stream`. */
+ * starts from it. Computed in 64-step chunks run in parallel, from the state
+ * between chunks carried by a short serial pass per head.
+ * workspace: gdn_workspace_bytes() bytes of device memory, 16-byte aligned,
+ * owned by the caller (else SCAN_ERR_WORKSPACE); no state is kept in it
+ * between calls. Asynchronous on `stream`. */
 size_t gdn_checkpoint_bytes(int64_t B, int64_t H, int64_t T, int64_t S,
                             int64_t D);
+size_t gdn_workspace_bytes(int64_t B, int64_t H, int64_t T, int64_t S,
+                           int64_t D);
 scan_status gdn_fwd(const float* alpha, const float* b, const float* v,
                     const float* c, const float* h0, float* o, float* ckpt,
                     int64_t B, int64_t H, int64_t T, int64_t S, int64_t D,
+                    void* workspace, size_t workspace_bytes,
                     cudaStream_t stream);
 
 /* Its backward for L = sum_t <dout_t, o_t> ([GDN] Mathematical Derivation of
@@ -305,11 +312,8 @@ scan_status gdn_fwd(const float* alpha, const float* b, const float* v,
  * 64-step chunk the products above become small matrix products; only the
  * adjoint of the state between chunks runs serially. ckpt is the forward's
  * checkpoint buffer (for the same inputs and h0); no state is stored besides
- * it. workspace: gdn_bwd_workspace_bytes() bytes of device memory, 16-byte
- * aligned, owned by the caller (else SCAN_ERR_WORKSPACE); it holds no state
- * between calls. Outputs in the layouts of the corresponding inputs. */
-size_t gdn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t T, int64_t S,
-                               int64_t D);
+ * it. workspace: as for gdn_fwd. Outputs in the layouts of the corresponding
+ * inputs. */
 scan_status gdn_bwd(const float* alpha, const float* b, const float* v,
                     const float* c, const float* ckpt, const float* dout,
                     float* dalpha, float* db, float* dv, float* dc, float* dh0,

@@ -121,7 +121,7 @@ def test_gdn_bwd_rejects_a_short_workspace(lib):
     w = workloads.gdn(1, 2, 130, 16, 16, seed=3, h0=False)
     alpha, b, v, c, dout = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout))
     _, ck = lib.gdn_fwd(alpha, b, v, c)
-    need = lib.gdn_bwd_workspace_bytes(1, 2, 130, 16, 16)
+    need = lib.gdn_workspace_bytes(1, 2, 130, 16, 16)
     assert need == 4 * (2 * 3 * 16 * 16 + 8)
     with pytest.raises(ValueError):
         lib.gdn_bwd(alpha, b, v, c, ck, dout,
@@ -132,3 +132,18 @@ def test_gdn_bwd_rejects_a_short_workspace(lib):
     torch.cuda.synchronize()
     for x, y in zip(got, ref):
         assert torch.equal(x, y)
+
+
+def test_gdn_fwd_rejects_a_short_workspace(lib):
+    w = workloads.gdn(1, 2, 70, 32, 16, seed=4, h0=True)
+    alpha, b, v, c = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c))
+    h0 = w.h0.to(DEV)
+    need = lib.gdn_workspace_bytes(1, 2, 70, 32, 16)
+    with pytest.raises(ValueError):
+        lib.gdn_fwd(alpha, b, v, c, h0, workspace=torch.empty(need - 16, dtype=torch.uint8,
+                                                             device=DEV))
+    o1, k1 = lib.gdn_fwd(alpha, b, v, c, h0, workspace=torch.empty(need, dtype=torch.uint8,
+                                                                   device=DEV))
+    o2, k2 = lib.gdn_fwd(alpha, b, v, c, h0)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(k1, k2)

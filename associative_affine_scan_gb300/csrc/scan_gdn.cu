@@ -23,7 +23,7 @@ namespace scan {
 namespace {
 
 constexpr unsigned kFullMask = 0xffffffffu;
-constexpr int kStage = 32;  // forward: steps per staged block
+constexpr int kStage = 16;  // steps per stage of the two-slot input rings
 constexpr int kCoarse = 64;  // checkpoint interval
 
 struct GdnParams {
@@ -185,16 +185,24 @@ __device__ __forceinline__ float suffix_prod64(float v0, float v1, int lane, flo
 template <int S, int D, bool FWD>
 __global__ void __launch_bounds__(32) gdn_chunk_sum_kernel(const GdnParams p) {
   constexpr int TM = SumLayout<S, D>::TM, TN = SumLayout<S, D>::TN;
-  __shared__ __align__(16) float s_x[kL * S];
-  __shared__ __align__(16) float s_y[kL * D];
+  __shared__ __align__(16) float s_x[2][kStage * S];
+  __shared__ __align__(16) float s_y[2][kStage * D];
   __shared__ float s_g[kL];
   const int lane = threadIdx.x;
   const int64_t blk = blockIdx.x, bh = blk / p.NC, k = blk - bh * p.NC;
   const int64_t T = p.T, r0 = bh * T + k * kL;
   const int n = (int)(T - k * kL < kL ? T - k * kL : kL);
-  stage_block(s_x, (FWD ? p.b : p.c) + r0 * S, n * S, lane, 32);
-  stage_block(s_y, (FWD ? p.v : p.dout) + r0 * D, n * D, lane, 32);
-  cp_async_commit();
+  const int nst = (n + kStage - 1) / kStage;
+  const float* gx = (FWD ? p.b : p.c) + r0 * S;
+  const float* gy = (FWD ? p.v : p.dout) + r0 * D;
+  auto issue = [&](int st) {  // stage st into slot st & 1
+    const int rows = n - st * kStage < kStage ? n - st * kStage : kStage;
+    stage_block(s_x[st & 1], gx + st * kStage * S, rows * S, lane, 32);
+    stage_block(s_y[st & 1], gy + st * kStage * D, rows * D, lane, 32);
+    cp_async_commit();
+  };
+  issue(0);
+  if (nst > 1) issue(1);
   {  // gates past the chunk's end count as 1
     const float a0 = 2 * lane < n ? __ldg(p.alpha + r0 + 2 * lane) : 1.f;
     const float a1 = 2 * lane + 1 < n ? __ldg(p.alpha + r0 + 2 * lane + 1) : 1.f;
@@ -211,41 +219,49 @@ __global__ void __launch_bounds__(32) gdn_chunk_sum_kernel(const GdnParams p) {
     }
     if (lane == 0) p.wsG[blk] = all;
   }
-  cp_async_wait<0>();
-  __syncwarp();
   const int si = lane >> 2, dj = lane & 3;
   float2 acc[TM][TN / 2];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
     for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+  for (int stg = 0; stg < nst; ++stg) {
+    if (stg + 1 < nst) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncwarp();
+    const float* sx = s_x[stg & 1];
+    const float* sy = s_y[stg & 1];
+    const int rows = n - stg * kStage < kStage ? n - stg * kStage : kStage;
 #pragma unroll 2
-  for (int t = 0; t < n; ++t) {
-    const float g = s_g[t];
-    const float2 g2 = make_float2(g, g);
-    float x[TM];
-    if constexpr (TM == 4) {
-      const float4 q = *reinterpret_cast<const float4*>(s_x + t * S + 4 * si);
-      x[0] = q.x;
-      x[1] = q.y;
-      x[2] = q.z;
-      x[3] = q.w;
-    } else {
-      const float2 q = *reinterpret_cast<const float2*>(s_x + t * S + 2 * si);
-      x[0] = q.x;
-      x[1] = q.y;
+    for (int r = 0; r < rows; ++r) {
+      const float g = s_g[stg * kStage + r];
+      const float2 g2 = make_float2(g, g);
+      float x[TM];
+      if constexpr (TM == 4) {
+        const float4 q = *reinterpret_cast<const float4*>(sx + r * S + 4 * si);
+        x[0] = q.x;
+        x[1] = q.y;
+        x[2] = q.z;
+        x[3] = q.w;
+      } else {
+        const float2 q = *reinterpret_cast<const float2*>(sx + r * S + 2 * si);
+        x[0] = q.x;
+        x[1] = q.y;
+      }
+      float2 y[TN / 2];
+#pragma unroll
+      for (int j = 0; j < TN / 4; ++j) {
+        const float4 q = *reinterpret_cast<const float4*>(sy + r * D + TN * dj + 4 * j);
+        y[2 * j] = fmul2(make_float2(q.x, q.y), g2);
+        y[2 * j + 1] = fmul2(make_float2(q.z, q.w), g2);
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = ffma2(make_float2(x[i], x[i]), y[j], acc[i][j]);
     }
-    float2 y[TN / 2];
-#pragma unroll
-    for (int j = 0; j < TN / 4; ++j) {
-      const float4 q = *reinterpret_cast<const float4*>(s_y + t * D + TN * dj + 4 * j);
-      y[2 * j] = fmul2(make_float2(q.x, q.y), g2);
-      y[2 * j + 1] = fmul2(make_float2(q.z, q.w), g2);
-    }
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-      for (int j = 0; j < TN / 2; ++j) acc[i][j] = ffma2(make_float2(x[i], x[i]), y[j], acc[i][j]);
+    __syncwarp();  // slot stg & 1 is read; refill it with stage stg + 2
+    if (stg + 2 < nst) issue(stg + 2);
   }
   float* out = p.wsS + blk * S * D;
 #pragma unroll
@@ -290,8 +306,10 @@ __global__ void __launch_bounds__(S * D / 4) gdn_carry_kernel(const GdnParams p)
     for (int j = 0; j < G8; ++j)
       if (i0 + j < NC) {
         const int64_t c = chunk(i0 + j);
-        ws[c * Q] = H;  // state before (adjoint after) chunk c
+        // state before (adjoint after) chunk c; the forward keeps it in the
+        // checkpoints when the caller asked for them, else in the workspace
         if (FWD && ck) ck[c * Q] = H;
+        else ws[c * Q] = H;
         H = make_float4(fmaf(g[j], H.x, U[j].x), fmaf(g[j], H.y, U[j].y), fmaf(g[j], H.z, U[j].z),
                         fmaf(g[j], H.w, U[j].w));
       }
@@ -309,7 +327,7 @@ template <int S, int D, int CW_>
 __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const GdnParams p) {
   using LY = Layout<S, D, CW_>;
   constexpr int CW = LY::CW, RS = LY::RS, NT = LY::NT;
-  static_assert(kL == 2 * kStage, "two stages per chunk");
+  static_assert(kL % kStage == 0, "whole stages per chunk");
   __shared__ __align__(16) float s_b[2][kStage * S];
   __shared__ __align__(16) float s_c[2][kStage * S];
   __shared__ __align__(16) float s_v[2][kStage * D];
@@ -323,27 +341,32 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
   const float* gb = p.b + bh * T * S;
   const float* gc = p.c + bh * T * S;
   const float* gv = p.v + bh * T * D;
-  for (int st = 0; st < nst; ++st) {
+  // stage st of the chunk into slot st & 1 (a ring of two)
+  auto issue = [&](int st) {
     const int64_t t0 = tc + st * kStage;
-    const int rows = (int)(T - t0 < kStage ? T - t0 : kStage);
-    stage_block(s_b[st], gb + t0 * S, rows * S, tid, NT);
-    stage_block(s_c[st], gc + t0 * S, rows * S, tid, NT);
-    stage_block(s_v[st], gv + t0 * D, rows * D, tid, NT);
+    const int rows = n - st * kStage < kStage ? n - st * kStage : kStage;
+    const int q = st & 1;
+    stage_block(s_b[q], gb + t0 * S, rows * S, tid, NT);
+    stage_block(s_c[q], gc + t0 * S, rows * S, tid, NT);
+    stage_block(s_v[q], gv + t0 * D, rows * D, tid, NT);
     cp_async_commit();
-    if (tid < rows) s_al[st][tid] = __ldg(p.alpha + bh * T + t0 + tid);
-  }
+    if (tid < rows) s_al[q][tid] = __ldg(p.alpha + bh * T + t0 + tid);
+  };
+  issue(0);
+  if (nst > 1) issue(1);
   float h[RS];
   {
-    const float* hin = p.wsS + blk * S * D;
+    const float* hin = (p.ckpt ? p.ckpt : p.wsS) + blk * S * D;  // where the carry left it
 #pragma unroll
     for (int i = 0; i < RS; ++i) h[i] = __ldcg(hin + (s0 + i) * D + d);
   }
-  for (int st = 0; st < nst; ++st) {
-    if (st + 1 < nst) cp_async_wait<1>();
+  for (int stg = 0; stg < nst; ++stg) {
+    if (stg + 1 < nst) cp_async_wait<1>();
     else cp_async_wait<0>();
     __syncthreads();
-    const int64_t t0 = tc + st * kStage;
-    const int rows = (int)(T - t0 < kStage ? T - t0 : kStage);
+    const int st = stg & 1;
+    const int64_t t0 = tc + stg * kStage;
+    const int rows = n - stg * kStage < kStage ? n - stg * kStage : kStage;
 #pragma unroll 4
     for (int r = 0; r < rows; ++r) {
       const int64_t t = t0 + r;
@@ -369,6 +392,8 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
       for (int m = CW; m < 32; m <<= 1) o += __shfl_xor_sync(kFullMask, o, m);
       if (g == 0) __stcs(p.o + (bh * T + t) * D + d, o);
     }
+    __syncthreads();  // slot st is read; refill it with stage stg + 2
+    if (stg + 2 < nst) issue(stg + 2);
   }
 }
 

@@ -51,6 +51,7 @@ from ._binding import (  # noqa: F401
     scan_bwd,
     scan_fwd,
     scan_fwd_noalloc,
+    scan_step_host,
     scan_get_device_status,
     scan_log_fwd,
     scan_log_bwd,

@@ -51,7 +51,7 @@ EXPORTED = (
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
     "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "affine_prefix_fwd",
     "affine_prefix_bwd", "gdn_checkpoint_bytes", "gdn_fwd", "gdn_workspace_bytes", "gdn_bwd",
-    "scan_fwd_noalloc",
+    "scan_fwd_noalloc", "scan_step_host",
 )
 
 
@@ -74,6 +74,14 @@ class ScanOpts(ctypes.Structure):
         ("segments", ctypes.c_int32),
         ("stages", ctypes.c_int32),
     ]
+
+
+class HostIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("a", "x", "h0", "dh", "h", "da", "dx", "dh0")]
+
+
+class DeviceIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("a", "x", "h0", "dh", "h", "da", "dx", "dh0")]
 
 
 _vp = ctypes.c_void_p
@@ -110,6 +118,8 @@ _SIGS = {
     "gdn_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _sz,
                  _vp], ctypes.c_int),
     "gdn_workspace_bytes": ([_i64, _i64, _i64, _i64, _i64], ctypes.c_size_t),
+    "scan_step_host": ([ctypes.POINTER(HostIO), ctypes.POINTER(DeviceIO), _i64, _i64, _i64,
+                        ctypes.c_int, _i32, _opt, _vp, _sz, _vp], ctypes.c_int),
     "gdn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                  _i64, _vp, _sz, _vp], ctypes.c_int),
     "affine_prefix_bwd": ([_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i32, _opt, _vp, _sz, _vp],
@@ -334,6 +344,53 @@ def scan_bwd(a, h, dh, h0=None, cu_seqlens=None, reverse=False, *, out=None, opt
                         _ptr(ws), ws.numel(), s)
     _check(st, "scan_bwd")
     return da, dx, dh0
+
+
+def scan_step_host(a, x, dh, h0=None, *, out, device, pieces=0, opts=None, stream=None):
+    """scan_fwd then scan_bwd on dense rows held in host memory, pipelined over
+    row pieces (copies overlap the scans). a, x, dh, h0: host tensors (pinned
+    for overlap); out = (h, da, dx, dh0) host tensors for the results (dh0 None
+    when h0 is None); device = (a, x, h0, dh, h, da, dx, dh0) device buffers of
+    the same shapes on the device that runs the step. Returns out."""
+    if a.dim() != 3:
+        raise ValueError("scan_step_host takes dense [B, C, T] rows")
+    B, C, T = a.shape
+    dt = _dtype_code(a)
+    h, da, dx, dh0 = out
+    d_a, d_x, d_h0, d_dh, d_h, d_da, d_dx, d_dh0 = device
+    for name, t in (("a", a), ("x", x), ("dh", dh), ("h", h), ("da", da), ("dx", dx)):
+        if t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, C, T):
+            raise ValueError(f"scan_step_host: host tensor {name} must be contiguous [B, C, T]")
+    for name, t in (("h0", h0), ("dh0", dh0)):
+        if t is not None and (t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, C)):
+            raise ValueError(f"scan_step_host: host tensor {name} must be contiguous [B, C]")
+    dev = d_a.device
+    for name, t, like in (("a", d_a, a), ("x", d_x, x), ("dh", d_dh, dh), ("h", d_h, h),
+                          ("da", d_da, da), ("dx", d_dx, dx), ("h0", d_h0, h0),
+                          ("dh0", d_dh0, dh0)):
+        if like is None:
+            continue
+        _need(t, "device " + name, dtype=like.dtype, shape=like.shape, device=dev)
+    if x.dtype != a.dtype or da.dtype != a.dtype or dx.dtype != a.dtype:
+        raise ValueError("scan_step_host: a, x, da, dx share one dtype")
+    p = lambda t: None if t is None else t.data_ptr()
+    hio = HostIO(p(a), p(x), p(h0), p(dh), p(h), p(da), p(dx), p(dh0))
+    dio = DeviceIO(p(d_a), p(d_x), p(d_h0) if h0 is not None else None, p(d_dh), p(d_h), p(d_da),
+                   p(d_dx), p(d_dh0) if dh0 is not None else None)
+    s = _stream(stream, dev)
+    np_ = pieces if pieces else min(8, B * C)
+    rows = -(-(B * C) // max(np_, 1))
+    o = ScanOpts()  # a copy: the caller's options are not modified
+    src = _opts(opts)
+    if src is not None:
+        ctypes.memmove(ctypes.byref(o), ctypes.byref(src), ctypes.sizeof(ScanOpts))
+    if o.variant == SCAN_VARIANT_AUTO:
+        o.variant = SCAN_VARIANT_STATIONARY
+    ws, nb, _ = workspace_for(SCAN_OP_BWD, 1, rows, T, 0, 0, o, dev, s)
+    st = lib().scan_step_host(ctypes.byref(hio), ctypes.byref(dio), B, C, T, dt, int(pieces),
+                              _optref(o), _ptr(ws), ws.numel(), s)
+    _check(st, "scan_step_host")
+    return out
 
 
 def scan_bidir_fwd(af, xf, ar, xr, h0f=None, h0r=None, cu_seqlens=None, *, out=None, opts=None,

@@ -6,8 +6,10 @@ scan on the dense [B=8, C=1536, T=4096] fp32 workload (synthetic, seeded).
 
 Prints one JSON line (rank 0). `value` is whole-job scan elements/s of the
 fwd+bwd step with inputs resident in HBM (CUDA events on the launching stream,
-L2 flushed between steps); `e2e` is the same metric through the same C ABI
-calls with pinned host buffers, host<->device copies inside the timed region.
+L2 flushed between steps); `e2e` is the same metric through the C ABI's
+host-buffer step (scan_step_host: pinned host inputs and results, the copies
+pipelined with the scans over row pieces), host<->device copies inside the
+timed region.
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 Under torchrun (N > 1) every rank scans its own copy of the workload (weak
 scaling, no collective on the data path); the step time is the max over ranks.
@@ -228,18 +230,11 @@ def run_ours(args, world, rank, local):
     bytes_in = sum(t.numel() * t.element_size() for t in (ha, hx, hdh) + ((hh0,) if hh0 is not None else ()))
     bytes_out = sum(t.numel() * t.element_size() for t in (out_h, out_da, out_dx, out_dh0))
 
+    # one library call per step: the library pipelines the copies in, the two
+    # scans and the copies out over row pieces
     def e2e_step():
-        a.copy_(ha, non_blocking=True)
-        x.copy_(hx, non_blocking=True)
-        dh.copy_(hdh, non_blocking=True)
-        if hh0 is not None:
-            h0.copy_(hh0, non_blocking=True)
-        scan.scan_fwd(a, x, h0, out=h)
-        scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0))
-        out_h.copy_(h, non_blocking=True)
-        out_da.copy_(da, non_blocking=True)
-        out_dx.copy_(dx, non_blocking=True)
-        out_dh0.copy_(dh0, non_blocking=True)
+        scan.scan_step_host(ha, hx, hdh, hh0, out=(out_h, out_da, out_dx, out_dh0),
+                            device=(a, x, h0, dh, h, da, dx, dh0))
 
     e2e_steps = max(3, min(args.steps, 10))
     for _ in range(2):

@@ -321,6 +321,58 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v,
                     void* workspace, size_t workspace_bytes,
                     cudaStream_t stream);
 
+/* One training step of dense rows (scan_fwd then scan_bwd, reverse = 0) whose
+ * inputs and results are in host memory ([AST] the scan and its reversed-scan
+ * backward; the rows of [B,C,T] are independent, so cutting between rows is
+ * exact). The B*C rows are cut into `pieces` pieces (0: 8; at most 64): each
+ * piece's inputs are copied to the device buffers on one internal stream, the
+ * piece is scanned forward and backward on `stream`, and its results are copied
+ * back on a second internal stream, so the copies of neighbouring pieces run
+ * under the scans and both copy directions run together. Results equal those
+ * of scan_fwd and scan_bwd on the whole problem with the same variant, bit for
+ * bit when T is a multiple of 4; otherwise a piece's rows start at another
+ * 4-element memory phase, which moves the kernels' run boundaries and so the
+ * rounding (within the forms' usual tolerance).
+ * host: a, x (dt), dh [B,C,T] and h0 [B,C] (nullable) in; h [B,C,T] fp32, da,
+ *       dx (dt) and dh0 [B,C] (nullable, with h0 and the device's h0/dh0 on
+ *       the same footing) out. Page-locked host memory is needed for the
+ *       copies to overlap (pageable memory works, without overlap).
+ * dev:  device buffers of the same shapes, owned by the caller; their
+ *       contents are overwritten.
+ * Host and device pointers must all be given except h0/dh0 (else
+ * SCAN_ERR_INVALID_ARG). opts: as for scan_fwd, except that the variant
+ * defaults to SCAN_VARIANT_STATIONARY (a piece has fewer rows than the GPU has
+ * warp slots). workspace: scan_workspace_bytes(SCAN_OP_BWD, 1, C', T, ...) for
+ * the largest piece of C' = ceil(B*C / pieces) rows, shared by the pieces'
+ * scans (they run in order on `stream`). Asynchronous: on return the whole step
+ * is queued and `stream` waits for its last copy; calls on one device are
+ * serialised on the host. */
+typedef struct {
+  const void* a;
+  const void* x;
+  const float* h0;
+  const float* dh;
+  float* h;
+  void* da;
+  void* dx;
+  float* dh0;
+} scan_host_io;
+typedef struct {
+  void* a;
+  void* x;
+  float* h0;
+  float* dh;
+  float* h;
+  void* da;
+  void* dx;
+  float* dh0;
+} scan_device_io;
+scan_status scan_step_host(const scan_host_io* host, const scan_device_io* dev,
+                           int64_t B, int64_t C, int64_t T, scan_dtype dt,
+                           int32_t pieces, const scan_opts* opts,
+                           void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
 /* Bytes of the library's own scratch used by scan_fwd_noalloc (16 MiB). */
 #define SCAN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -152,3 +152,29 @@ def test_affine_envelope_rejected_on_host():
     ws = ctypes.c_void_p(0x100000)
     assert f(fake, fake, None, fake, 1, 8, 4, 3, 4, None, ws, 1 << 20, None) == \
         scan.SCAN_ERR_UNSUPPORTED
+
+
+def test_step_host_argument_checks_need_no_gpu():
+    """scan_step_host rejects malformed calls before touching the GPU."""
+    import associative_affine_scan_gb300 as scan
+    from associative_affine_scan_gb300._binding import DeviceIO, HostIO
+    f = _raw("scan_step_host")
+    fk = 0x1000
+    full = dict(a=fk, x=fk, h0=None, dh=fk, h=fk, da=fk, dx=fk, dh0=None)
+    hio, dio = HostIO(**full), DeviceIO(**full)
+    ws = ctypes.c_void_p(0x100000)
+    call = lambda h, d, B=1, C=4, T=64, dt=0, pieces=0: f(
+        ctypes.byref(h) if h is not None else None, ctypes.byref(d) if d is not None else None,
+        B, C, T, dt, pieces, None, ws, 4096, None)
+    assert call(None, dio) == scan.SCAN_ERR_INVALID_ARG
+    assert call(hio, None) == scan.SCAN_ERR_INVALID_ARG
+    assert call(hio, dio, dt=7) == scan.SCAN_ERR_INVALID_ARG
+    assert call(hio, dio, C=-1) == scan.SCAN_ERR_INVALID_ARG
+    assert call(hio, dio, pieces=65) == scan.SCAN_ERR_INVALID_ARG
+    # h0 on one side only
+    assert call(HostIO(**dict(full, h0=fk)), dio) == scan.SCAN_ERR_INVALID_ARG
+    assert call(hio, DeviceIO(**dict(full, dh0=fk))) == scan.SCAN_ERR_INVALID_ARG
+    # a missing result buffer
+    assert call(HostIO(**dict(full, dx=None)), dio) == scan.SCAN_ERR_INVALID_ARG
+    # empty problem: nothing to copy or launch
+    assert call(HostIO(), DeviceIO(), C=0) == scan.SCAN_OK

@@ -3,7 +3,7 @@
 // Reverse-Time Backward Pass):
 //   h_t = alpha_t h_{t-1} + b_t v_t^T      (S x D state per (batch, head))
 //   o_t = h_t^T c_t                         (D-vector)
-// and its reverse-time backward with the states recomputed from checkpoints.
+// and its reverse-time backward, started from the forward's checkpoints.
 //
 // Work decomposition: both directions are cut into 64-step chunks (the
 // checkpoint interval) that run in parallel; only the S x D state between
@@ -40,7 +40,8 @@ struct GdnParams {
   float* dv;
   float* dc;
   float* dh0;          // nullable
-  float* wsS;          // backward workspace: [B,H,NC,S,D] chunk adjoints
+  float* wsS;          // workspace [B,H,NC,S,D]: each chunk's state (adjoint) sum,
+                       // then the state before (adjoint after) the chunk
   float* wsG;          // [B,H,NC] gate product of each chunk
   int64_t BH, T;
   int64_t NC;
@@ -90,7 +91,7 @@ struct Layout {
   static constexpr int CW = CW_;       // columns per warp
   static constexpr int RG = 32 / CW;   // row groups
   static constexpr int RS = S / RG;    // rows per lane
-  static constexpr int NW = D / CW;    // warps per head
+  static constexpr int NW = D / CW;    // warps per chunk
   static constexpr int NT = 32 * NW;   // threads per block
   static_assert(RS >= 2 && RS % 2 == 0 && RS <= CW && NW >= 1, "layout");
 };

@@ -5,8 +5,8 @@
 //   o_t = h_t^T c_t                         (D-vector)
 // and its reverse-time backward, started from the forward's checkpoints.
 //
-// Work decomposition: both directions are cut into 64-step chunks (the
-// checkpoint interval) that run in parallel; only the S x D state between
+// Work decomposition: both directions are cut into chunks (64 steps forward,
+// 32 backward: the checkpoint interval) that run in parallel; only the S x D state between
 // chunks (forward) or its adjoint (backward) is carried serially, by a short
 // kernel per head (see the section on the chunked form below). Within a chunk
 // the forward walks the steps with the state in registers, one warp per chunk
@@ -24,7 +24,7 @@ namespace {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kStage = 16;  // steps per stage of the two-slot input rings
-constexpr int kCoarse = 64;  // checkpoint interval
+constexpr int kCoarse = 32;  // checkpoint interval
 
 struct GdnParams {
   const float* alpha;  // [B,H,T]
@@ -33,7 +33,7 @@ struct GdnParams {
   const float* c;      // [B,H,T,S]
   const float* h0;     // [B,H,S,D] nullable
   float* o;            // forward output [B,H,T,D]
-  float* ckpt;         // [B,H,NC,S,D], NC = ceil(T / 64): state before step 64 j
+  float* ckpt;         // [B,H,NCK,S,D], NCK = ceil(T / 32): state before step 32 j
   const float* dout;   // backward
   float* dalpha;
   float* db;
@@ -44,7 +44,8 @@ struct GdnParams {
                        // then the state before (adjoint after) the chunk
   float* wsG;          // [B,H,NC] gate product of each chunk
   int64_t BH, T;
-  int64_t NC;
+  int64_t NC;   // chunks per head of this direction's launches
+  int64_t NCK;  // checkpoints per head
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -128,8 +129,10 @@ __device__ __forceinline__ void ld_row(const float* src, float (&x)[N]) {
 }
 
 // ---------------------------------------------------------------------------
-// Both directions run chunked over T in 64-step chunks (the checkpoint
-// interval). Per chunk of n steps with gates alpha_0 .. alpha_{n-1}:
+// Both directions run chunked over T: the forward in 64-step chunks, the
+// backward in 32-step chunks (the checkpoint interval; its chunk products grow
+// with the square of the chunk length, and at 32 steps four blocks share an
+// SM). Per chunk of n steps with gates alpha_0 .. alpha_{n-1}:
 //   forward:  H_out = Gamma H_in + U,   U = sum_tau w_tau b_tau v_tau^T,
 //             w_tau = alpha_{tau+1} .. alpha_{n-1},  Gamma = alpha_0 .. alpha_{n-1};
 //   backward: G_in = Gamma G_out + V,   V = sum_t Gamma_t c_t dout_t^T,
@@ -142,7 +145,10 @@ __device__ __forceinline__ void ld_row(const float* src, float (&x)[N]) {
 // parallel from it.
 // ---------------------------------------------------------------------------
 
-constexpr int kL = kCoarse;  // steps per chunk (the checkpoint interval)
+constexpr int kL = kCoarse;  // steps per backward chunk (the checkpoint interval)
+constexpr int kLF = 64;      // steps per forward chunk (a whole number of checkpoint intervals)
+constexpr int kRatio = kLF / kL;  // checkpoints per forward chunk
+static_assert(kLF % kL == 0 && kLF <= 64, "forward chunk");
 
 // The chunk sums run one warp per chunk; a lane owns TM x TN entries of the
 // S x D sum (TM = S / 8 rows, TN = D / 4 columns).
@@ -151,34 +157,54 @@ struct SumLayout {
   static constexpr int TM = S / 8, TN = D / 4;
 };
 
-// Product scans of 64 values held two per lane (v0 = element 2 l, v1 =
-// element 2 l + 1). prefix: returns the product of the elements before the
-// lane's pair and sets incl to the product through it. suffix: returns the
-// product of the elements after the pair and sets total to the product of all.
-__device__ __forceinline__ float prefix_prod64(float v0, float v1, int lane, float& incl) {
-  float x = v0 * v1;
+constexpr int kEPL = kL / 32;  // gates per lane in the backward's scans over a chunk
+static_assert(kL % 32 == 0 && kL <= 64, "chunk length");
+
+// Product scans over a chunk's 32 EPL gates, lane l holding elements
+// EPL l .. EPL l + EPL - 1 in v. prefix_prods: pi[i] = the product of the
+// elements up to and including the lane's i-th, pe[i] = up to and excluding
+// it; returns the product of all. suffix_prods: q[i] = the product of the
+// elements after the lane's i-th; returns the product of all.
+template <int EPL>
+__device__ __forceinline__ float prefix_prods(const float (&v)[EPL], float (&pi)[EPL],
+                                              float (&pe)[EPL], int lane) {
+  float x = 1.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) x *= v[i];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y = __shfl_up_sync(kFullMask, x, o);
     if (lane >= o) x *= y;
   }
-  float e = __shfl_up_sync(kFullMask, x, 1);
-  if (lane == 0) e = 1.f;
-  incl = x;
-  return e;
+  float run = __shfl_up_sync(kFullMask, x, 1);
+  if (lane == 0) run = 1.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    pe[i] = run;
+    run *= v[i];
+    pi[i] = run;
+  }
+  return __shfl_sync(kFullMask, x, 31);
 }
 
-__device__ __forceinline__ float suffix_prod64(float v0, float v1, int lane, float& total) {
-  float x = v0 * v1;
+template <int EPL>
+__device__ __forceinline__ float suffix_prods(const float (&v)[EPL], float (&q)[EPL], int lane) {
+  float x = 1.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) x *= v[i];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y = __shfl_down_sync(kFullMask, x, o);
     if (lane + o < 32) x *= y;
   }
-  float e = __shfl_down_sync(kFullMask, x, 1);
-  if (lane == 31) e = 1.f;
-  total = __shfl_sync(kFullMask, x, 0);
-  return e;
+  float run = __shfl_down_sync(kFullMask, x, 1);
+  if (lane == 31) run = 1.f;
+#pragma unroll
+  for (int i = EPL - 1; i >= 0; --i) {
+    q[i] = run;
+    run *= v[i];
+  }
+  return __shfl_sync(kFullMask, x, 0);
 }
 
 // U (FWD: sum_tau w_tau b_tau v_tau^T) or V (sum_t Gamma_t c_t dout_t^T) of
@@ -186,6 +212,8 @@ __device__ __forceinline__ float suffix_prod64(float v0, float v1, int lane, flo
 template <int S, int D, bool FWD>
 __global__ void __launch_bounds__(32) gdn_chunk_sum_kernel(const GdnParams p) {
   constexpr int TM = SumLayout<S, D>::TM, TN = SumLayout<S, D>::TN;
+  constexpr int kL = FWD ? kLF : ::scan::kL;  // this direction's chunk
+  constexpr int kEPL = kL / 32;
   __shared__ __align__(16) float s_x[2][kStage * S];
   __shared__ __align__(16) float s_y[2][kStage * D];
   __shared__ float s_g[kL];
@@ -205,19 +233,16 @@ __global__ void __launch_bounds__(32) gdn_chunk_sum_kernel(const GdnParams p) {
   issue(0);
   if (nst > 1) issue(1);
   {  // gates past the chunk's end count as 1
-    const float a0 = 2 * lane < n ? __ldg(p.alpha + r0 + 2 * lane) : 1.f;
-    const float a1 = 2 * lane + 1 < n ? __ldg(p.alpha + r0 + 2 * lane + 1) : 1.f;
-    float all;
-    if constexpr (FWD) {
-      const float e = suffix_prod64(a0, a1, lane, all);
-      s_g[2 * lane + 1] = e;
-      s_g[2 * lane] = a1 * e;
-    } else {
-      const float e = prefix_prod64(a0, a1, lane, all);
-      s_g[2 * lane] = e * a0;
-      s_g[2 * lane + 1] = all;
-      all = __shfl_sync(kFullMask, all, 31);
+    float av[kEPL], g[kEPL], ge[kEPL], all;
+#pragma unroll
+    for (int i = 0; i < kEPL; ++i) {
+      const int t = kEPL * lane + i;
+      av[i] = t < n ? __ldg(p.alpha + r0 + t) : 1.f;
     }
+    if constexpr (FWD) all = suffix_prods(av, g, lane);
+    else all = prefix_prods(av, g, ge, lane);
+#pragma unroll
+    for (int i = 0; i < kEPL; ++i) s_g[kEPL * lane + i] = g[i];
     if (lane == 0) p.wsG[blk] = all;
   }
   const int si = lane >> 2, dj = lane & 3;
@@ -283,7 +308,7 @@ __global__ void __launch_bounds__(S * D / 4) gdn_carry_kernel(const GdnParams p)
   const int tid = threadIdx.x;
   const int64_t bh = blockIdx.x, NC = p.NC;
   float4* ws = reinterpret_cast<float4*>(p.wsS + bh * NC * S * D) + tid;
-  float4* ck = p.ckpt ? reinterpret_cast<float4*>(p.ckpt + bh * NC * S * D) + tid : nullptr;
+  float4* ck = p.ckpt ? reinterpret_cast<float4*>(p.ckpt + bh * p.NCK * S * D) + tid : nullptr;
   const float* gam = p.wsG + bh * NC;
   auto chunk = [&](int64_t i) { return FWD ? i : NC - 1 - i; };
   float4 H = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -309,7 +334,7 @@ __global__ void __launch_bounds__(S * D / 4) gdn_carry_kernel(const GdnParams p)
         const int64_t c = chunk(i0 + j);
         // state before (adjoint after) chunk c; the forward keeps it in the
         // checkpoints when the caller asked for them, else in the workspace
-        if (FWD && ck) ck[c * Q] = H;
+        if (FWD && ck) ck[c * kRatio * Q] = H;
         else ws[c * Q] = H;
         H = make_float4(fmaf(g[j], H.x, U[j].x), fmaf(g[j], H.y, U[j].y), fmaf(g[j], H.z, U[j].z),
                         fmaf(g[j], H.w, U[j].w));
@@ -323,12 +348,14 @@ __global__ void __launch_bounds__(S * D / 4) gdn_carry_kernel(const GdnParams p)
   if (!FWD && p.dh0) reinterpret_cast<float4*>(p.dh0 + bh * S * D)[tid] = H;
 }
 
-// One 64-step chunk per block, from the state before it (in the workspace).
+// One 64-step chunk per block, from the state before it (the carry left it in
+// the checkpoints, or the workspace when there are none); the walk writes the
+// checkpoint in the middle of the chunk.
 template <int S, int D, int CW_>
 __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const GdnParams p) {
   using LY = Layout<S, D, CW_>;
   constexpr int CW = LY::CW, RS = LY::RS, NT = LY::NT;
-  static_assert(kL % kStage == 0, "whole stages per chunk");
+  static_assert(kLF % kStage == 0 && kL % kStage == 0, "whole stages per chunk");
   __shared__ __align__(16) float s_b[2][kStage * S];
   __shared__ __align__(16) float s_c[2][kStage * S];
   __shared__ __align__(16) float s_v[2][kStage * D];
@@ -336,9 +363,10 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = warp * CW + lane % CW, g = lane / CW, s0 = g * RS;
   const int64_t blk = blockIdx.x, bh = blk / p.NC, k = blk - bh * p.NC;
-  const int64_t T = p.T, tc = k * kL;
-  const int n = (int)(T - tc < kL ? T - tc : kL);
+  const int64_t T = p.T, tc = k * kLF;
+  const int n = (int)(T - tc < kLF ? T - tc : kLF);
   const int nst = (n + kStage - 1) / kStage;
+  float* ckb = p.ckpt ? p.ckpt + (bh * p.NCK + k * kRatio) * S * D : nullptr;  // this chunk's
   const float* gb = p.b + bh * T * S;
   const float* gc = p.c + bh * T * S;
   const float* gv = p.v + bh * T * D;
@@ -357,7 +385,7 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
   if (nst > 1) issue(1);
   float h[RS];
   {
-    const float* hin = (p.ckpt ? p.ckpt : p.wsS) + blk * S * D;  // where the carry left it
+    const float* hin = ckb ? ckb : p.wsS + blk * S * D;  // where the carry left it
 #pragma unroll
     for (int i = 0; i < RS; ++i) h[i] = __ldcg(hin + (s0 + i) * D + d);
   }
@@ -368,6 +396,12 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
     const int st = stg & 1;
     const int64_t t0 = tc + stg * kStage;
     const int rows = n - stg * kStage < kStage ? n - stg * kStage : kStage;
+    // the checkpoints inside the chunk (the carry wrote the one at its start)
+    if (ckb && stg > 0 && (stg * kStage) % kL == 0) {
+      float* cq = ckb + (stg * kStage / kL) * S * D;
+#pragma unroll
+      for (int i = 0; i < RS; ++i) cq[(s0 + i) * D + d] = h[i];
+    }
 #pragma unroll 4
     for (int r = 0; r < rows; ++r) {
       const int64_t t = t0 + r;
@@ -400,7 +434,7 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
 
 // ---------------------------------------------------------------------------
 // Backward, chunked over T ("Operations & Triton Kernels" (HyMo), The chunked
-// GDN algorithm, applied to the reverse-time pass). Within a chunk of n <= 64
+// GDN algorithm, applied to the reverse-time pass). Within a chunk of n <= 32
 // steps starting from H_in (the checkpoint) and with G_out, the adjoint of the
 // state after the chunk (gradients from later chunks only):
 //   Gamma_t = alpha_0 .. alpha_t,  D[t][tau] = alpha_{tau+1} .. alpha_t (tau <= t)
@@ -464,39 +498,44 @@ __device__ __forceinline__ float2 dot4x2(const float4& a, const float4& b, float
   return ffma2(make_float2(a.z, a.w), make_float2(b.z, b.w), acc);
 }
 
-// Block of a 64 x 64 product C[m][n] = sum_k A[m][k] B[n][k] (both operands
-// row-major with K consecutive, row strides ap and bp): rows m0 + li + 4 i,
-// columns n0 + lj + 8 j, written to out (row stride LP).
-template <int K, int LP>
+// A warp's block of a kL x kL product C[m][n] = sum_k A[m][k] B[n][k] (both
+// operands row-major with K consecutive, row strides ap and bp): rows
+// m0 + li + 4 i (i < 4), columns n0 + lj + 8 j (j < NJ), written to out (row
+// stride LP).
+template <int K, int LP, int NJ>
 __device__ __forceinline__ void gemm_nt_block(const float* A, int ap, const float* B, int bp,
                                               int m0, int n0, int li, int lj, float* out) {
-  float2 acc[4][4];
+  float2 acc[4][NJ];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
+    for (int j = 0; j < NJ; ++j) acc[i][j] = make_float2(0.f, 0.f);
 #pragma unroll 2
   for (int kk = 0; kk < K; kk += 4) {
-    float4 a[4], q[4];
+    float4 a[4], q[NJ];
 #pragma unroll
     for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(A + (m0 + li + 4 * i) * ap + kk);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const float4*>(B + (n0 + lj + 8 * j) * bp + kk);
+    for (int j = 0; j < NJ; ++j) q[j] = *reinterpret_cast<const float4*>(B + (n0 + lj + 8 * j) * bp + kk);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = dot4x2(a[i], q[j], acc[i][j]);
+      for (int j = 0; j < NJ; ++j) acc[i][j] = dot4x2(a[i], q[j], acc[i][j]);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) out[(m0 + li + 4 * i) * LP + n0 + lj + 8 * j] = acc[i][j].x + acc[i][j].y;
+    for (int j = 0; j < NJ; ++j) out[(m0 + li + 4 * i) * LP + n0 + lj + 8 * j] = acc[i][j].x + acc[i][j].y;
 }
 
+// Threads of the chunk-gradient kernel: 4 per step of the chunk (16 column
+// threads x 4 rows per row tile; kL columns x 4 row quarters in the walk).
+constexpr int kBwdThreads = 4 * kL;
+
 template <int S, int D>
-__global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 128 / kL) gdn_bwd_chunk_kernel(const GdnParams p) {
   using SM = ChunkSmem<S, D>;
-  constexpr int SP = SM::SP, DP = SM::DP, LP = SM::LP, NT = 256;
+  constexpr int SP = SM::SP, DP = SM::DP, LP = SM::LP, NT = kBwdThreads;
   constexpr int TNS = S / 16, TND = D / 16;  // output columns per thread
   extern __shared__ __align__(16) float sm[];
   float* sb = sm + SM::b;
@@ -566,26 +605,22 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
   __syncthreads();
 
   // ---- gate products: Gamma_t, Gamma_{t-1} (warp 0); D[n-1][t] (warp 1) ----
-  if (warp == 0) {
-    const float a0 = sal[2 * lane], a1 = sal[2 * lane + 1];
-    float incl;
-    const float e = prefix_prod64(a0, a1, lane, incl);
-    sgam[2 * lane] = e * a0;
-    sgam[2 * lane + 1] = incl;
-    sgm1[2 * lane] = e;
-    sgm1[2 * lane + 1] = e * a0;
-  } else if (warp == 1) {
-    const float a0 = sal[2 * lane], a1 = sal[2 * lane + 1];
-    float x = a0 * a1;
+  if (warp < 2) {
+    float av[kEPL], g[kEPL], ge[kEPL];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_down_sync(kFullMask, x, o);
-      if (lane + o < 32) x *= y;
+    for (int i = 0; i < kEPL; ++i) av[i] = sal[kEPL * lane + i];
+    if (warp == 0) {
+      prefix_prods(av, g, ge, lane);
+#pragma unroll
+      for (int i = 0; i < kEPL; ++i) {
+        sgam[kEPL * lane + i] = g[i];
+        sgm1[kEPL * lane + i] = ge[i];
+      }
+    } else {
+      suffix_prods(av, g, lane);
+#pragma unroll
+      for (int i = 0; i < kEPL; ++i) swd[kEPL * lane + i] = g[i];
     }
-    float e = __shfl_down_sync(kFullMask, x, 1);
-    if (lane == 31) e = 1.f;
-    swd[2 * lane + 1] = e;
-    swd[2 * lane] = a1 * e;
   }
 
   // ---- HDo = dout H_in^T, Gv = v G_out^T, Gb = b G_out, kept in registers:
@@ -671,47 +706,59 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
     }
   }
 
-  // ---- CB = c b^T and DoV = dout v^T (64 x 64); a warp takes a 16 x 32
-  // block, skipped when the block lies entirely above the diagonal ----
+  // ---- CB = c b^T and DoV = dout v^T (kL x kL); warp w takes the 16-row,
+  // kL/2-column block (w / 2, w % 2), skipped when it lies entirely above the
+  // diagonal ----
   {
+    constexpr int HW = kL / 2;
     const int bi = warp >> 1, bj = warp & 1;
-    if (32 * bj <= 16 * bi + 15) {
-      gemm_nt_block<S, LP>(sc, SP, sb, SP, 16 * bi, 32 * bj, lane >> 3, lane & 7, scb);
-      gemm_nt_block<D, LP>(sdo, DP, sv, DP, 16 * bi, 32 * bj, lane >> 3, lane & 7, sdv);
+    if (HW * bj <= 16 * bi + 15) {
+      gemm_nt_block<S, LP, HW / 8>(sc, SP, sb, SP, 16 * bi, HW * bj, lane >> 3, lane & 7, scb);
+      gemm_nt_block<D, LP, HW / 8>(sdo, DP, sv, DP, 16 * bi, HW * bj, lane >> 3, lane & 7, sdv);
     }
   }
   // the column walk below splits rows into quarters; here each (column, quarter)
   // forms the product of the quarter's gates that enter D (rows t > tau)
+  constexpr int kQ = kL / 4;      // rows per quarter
+  constexpr int kColW = kL / 32;  // warps per quarter (32 columns each)
   {
-    const int tau = 32 * (warp & 1) + lane, tq = 16 * (warp >> 1);
+    const int tau = 32 * (warp % kColW) + lane, q = warp / kColW, tq = kQ * q;
     float f = 1.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kQ; ++i)
       if (tq + i > tau) f *= sal[tq + i];
-    sqf[(warp >> 1) * kL + tau] = f;
+    sqf[q * kL + tau] = f;
   }
   __syncthreads();
 
   // ---- Y[t][r] (row t: an affine scan over r with gates alpha_r) and y_r;
-  // a warp scans 4 rows at a time (independent shuffle chains) ----
+  // lane l holds r = kEPL l .. kEPL l + kEPL - 1; a warp scans 4 rows at a time
+  // (independent shuffle chains) ----
   {
-    const float a0 = sal[2 * lane], a1 = sal[2 * lane + 1];
-    for (int rb = warp; rb <= kL; rb += 4 * (NT / 32)) {
-      float A[4], X[4], x0[4];
+    float ar[kEPL];
+#pragma unroll
+    for (int e = 0; e < kEPL; ++e) ar[e] = sal[kEPL * lane + e];
+    constexpr int NWp = NT / 32;
+    for (int rb = warp; rb <= kL; rb += 4 * NWp) {
+      float A[4], X[4], xs[4][kEPL];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int row = rb + u * (NT / 32);
-        float y0 = 0.f, y1 = 0.f;
-        if (row < kL) {
-          if (2 * lane <= row) y0 = scb[row * LP + 2 * lane] * sdv[row * LP + 2 * lane];
-          if (2 * lane + 1 <= row) y1 = scb[row * LP + 2 * lane + 1] * sdv[row * LP + 2 * lane + 1];
-        } else if (row == kL) {
-          y0 = sw[2 * lane];
-          y1 = sw[2 * lane + 1];
+        const int row = rb + u * NWp;
+        A[u] = 1.f;
+        X[u] = 0.f;
+#pragma unroll
+        for (int e = 0; e < kEPL; ++e) {
+          const int r = kEPL * lane + e;
+          float xv = 0.f;
+          if (row < kL) {
+            if (r <= row) xv = scb[row * LP + r] * sdv[row * LP + r];
+          } else if (row == kL) {
+            xv = sw[r];
+          }
+          xs[u][e] = xv;
+          X[u] = fmaf(ar[e], X[u], xv);  // the lane's run composed: state after it from 0
+          A[u] *= ar[e];
         }
-        x0[u] = y0;
-        A[u] = a0 * a1;
-        X[u] = fmaf(a1, y0, y1);
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -726,13 +773,16 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int row = rb + u * (NT / 32);
-        float e = __shfl_up_sync(kFullMask, X[u], 1);
-        if (lane == 0) e = 0.f;
+        const int row = rb + u * NWp;
+        float st = __shfl_up_sync(kFullMask, X[u], 1);
+        if (lane == 0) st = 0.f;
         if (row <= kL) {
           float* dst = row < kL ? sy + row * LP : syv;
-          dst[2 * lane] = e;
-          dst[2 * lane + 1] = fmaf(a0, e, x0[u]);
+#pragma unroll
+          for (int e = 0; e < kEPL; ++e) {
+            dst[kEPL * lane + e] = st;  // the state before element r
+            st = fmaf(ar[e], st, xs[u][e]);
+          }
         }
       }
     }
@@ -740,17 +790,16 @@ __global__ void __launch_bounds__(256, 2) gdn_bwd_chunk_kernel(const GdnParams p
   __syncthreads();
 
   // ---- down each column tau: D[t][tau] for t >= tau; P and dS in place, dS^T
-  // (zero below its diagonal), dalpha_tau. Warp w takes columns
-  // 32 (w & 1) .. + 31 over the row quarter 16 (w >> 1) .. + 15, starting from
-  // the product of the earlier quarters' gates. ----
+  // (zero below its diagonal), dalpha_tau. Warp w takes 32 columns over one
+  // row quarter, starting from the product of the earlier quarters' gates. ----
   {
-    const int tau = 32 * (warp & 1) + lane, q = warp >> 1, tq = 16 * q;
+    const int tau = 32 * (warp % kColW) + lane, q = warp / kColW, tq = kQ * q;
     float dec = 1.f;
     for (int i = 0; i < q; ++i) dec *= sqf[i * kL + tau];
     const float gm = sgm1[tau];
     float acc = 0.f;
 #pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kQ; ++i) {
       const int t = tq + i;
       float* pc = scb + t * LP + tau;
       float* pd = sdv + t * LP + tau;
@@ -858,7 +907,7 @@ cudaError_t launch_bwd(const GdnParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(gdn_bwd_chunk_kernel<S, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  gdn_bwd_chunk_kernel<S, D><<<nblk, 256, smem, s>>>(p);
+  gdn_bwd_chunk_kernel<S, D><<<nblk, kBwdThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -928,7 +977,8 @@ scan_status gdn_fwd(const float* alpha, const float* b, const float* v, const fl
   p.wsG = p.wsS + (size_t)(B * H * NC) * (size_t)(S * D);
   p.BH = B * H;
   p.T = T;
-  p.NC = NC;
+  p.NC = (T + kLF - 1) / kLF;  // the forward's chunks (the workspace holds NC >= these)
+  p.NCK = NC;
   return dispatch(p, (int)S, (int)D, true, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
 }
 
@@ -971,6 +1021,7 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v, const fl
   p.BH = B * H;
   p.T = T;
   p.NC = NC;
+  p.NCK = NC;
   return dispatch(p, (int)S, (int)D, false, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
 }
 

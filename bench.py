@@ -315,7 +315,7 @@ def measure_rows(args, dev, scan, names=ROWS, small=False):
 
 def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
     # per (head, step), S = D = 32: fwd reads alpha, b, c (S), v (D) and writes
-    # o (D) plus a 4 KB checkpoint every 64 steps; bwd reads alpha, b, c, v,
+    # o (D) plus a 4 KB checkpoint every 32 steps; bwd reads alpha, b, c, v,
     # dout and the checkpoints and writes dalpha, db, dc, dv
     w = workloads.gdn_4k(seed=0)
     alpha, b, v, c, dout = (t.to(dev) for t in (w.alpha, w.b, w.v, w.c, w.dout))

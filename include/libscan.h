@@ -287,7 +287,7 @@ scan_status affine_prefix_bwd(const float* A, const float* Abar,
  * v, o [B,H,T,D]; h0 nullable [B,H,S,D] (0 when NULL). S, D in {16, 32}
  * (else SCAN_ERR_UNSUPPORTED); b, c, v, o, h0, ckpt 16-byte aligned (else
  * SCAN_ERR_ALIGNMENT). ckpt (nullable): gdn_checkpoint_bytes() bytes, filled
- * with the state before every 64th step, [B,H,ceil(T/64),S,D]; the backward
+ * with the state before every 32nd step, [B,H,ceil(T/32),S,D]; the backward
  * starts from it. Computed in 64-step chunks run in parallel, from the state
  * between chunks carried by a short serial pass per head.
  * workspace: gdn_workspace_bytes() bytes of device memory, 16-byte aligned,
@@ -309,7 +309,7 @@ scan_status gdn_fwd(const float* alpha, const float* b, const float* v,
  *   dv_t = dh_t^T b_t,  db_t = dh_t v_t,  dalpha_t = <dh_t, h_{t-1}>,
  *   dh0 = alpha_0 dh_0 (nullable).
  * Computed chunk by chunk over T ([GDN] The chunked GDN algorithm): within a
- * 64-step chunk the products above become small matrix products; only the
+ * 32-step chunk the products above become small matrix products; only the
  * adjoint of the state between chunks runs serially. ckpt is the forward's
  * checkpoint buffer (for the same inputs and h0); no state is stored besides
  * it. workspace: as for gdn_fwd. Outputs in the layouts of the corresponding

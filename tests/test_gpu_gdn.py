@@ -110,7 +110,7 @@ def test_gdn_gate_zero_resets(lib, T):
     first and last steps and inside it; the backward's per-chunk gate
     products are formed without division, so dalpha stays exact there."""
     w = workloads.gdn(2, 2, T, 32, 32, seed=11 + T, h0=True)
-    for t in (0, 1, 31, 63, 64, 127, 128, 199):
+    for t in (0, 1, 31, 32, 63, 64, 95, 96, 127, 128, 199):
         if t < T:
             w.alpha[:, :, t] = 0.0
     w.alpha[1, 1, :] = 0.0  # every step a reset
@@ -122,7 +122,8 @@ def test_gdn_bwd_rejects_a_short_workspace(lib):
     alpha, b, v, c, dout = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout))
     _, ck = lib.gdn_fwd(alpha, b, v, c)
     need = lib.gdn_workspace_bytes(1, 2, 130, 16, 16)
-    assert need == 4 * (2 * 3 * 16 * 16 + 8)
+    # one 16 x 16 matrix and one gate product per 32-step chunk: 2 heads x 5 chunks
+    assert need == 4 * (2 * 5 * 16 * 16 + 12)
     with pytest.raises(ValueError):
         lib.gdn_bwd(alpha, b, v, c, ck, dout,
                     workspace=torch.empty(need - 16, dtype=torch.uint8, device=DEV))

@@ -465,17 +465,17 @@ struct ChunkSmem {
   static constexpr int b = 0;                  // [kL][SP]
   static constexpr int c = b + kL * SP;        // [kL][SP]
   static constexpr int dout = c + kL * SP;     // [kL][DP]
-  static constexpr int r1 = dout + kL * DP;    // v, H_in, G_out, G_out^T; later dS^T
+  static constexpr int r1 = dout + kL * DP;    // v, H_in, G_out, G_out^T; then Y; then dS^T
   static constexpr int v = r1;                 // [kL][DP]
   static constexpr int hin = v + kL * DP;      // [S][DP]
   static constexpr int gout = hin + S * DP;    // [S][DP]
   static constexpr int goutT = gout + S * DP;  // [D][SP]
   static constexpr int dsT = r1;               // [kL][LP]
+  static constexpr int y = r1;                 // [kL][LP]
   static constexpr int r1_end = goutT + D * SP > r1 + kL * LP ? goutT + D * SP : r1 + kL * LP;
   static constexpr int cb = r1_end;            // [kL][LP]: CB, then P
   static constexpr int dov = cb + kL * LP;     // [kL][LP]: DoV, then dS
-  static constexpr int y = dov + kL * LP;      // [kL][LP]
-  static constexpr int al = y + kL * LP;       // kL + 4 gates (1 past the chunk's end)
+  static constexpr int al = dov + kL * LP;     // kL + 4 gates (1 past the chunk's end)
   static constexpr int gam = al + kL + 4;      // Gamma_t
   static constexpr int gm1 = gam + kL;         // Gamma_{t-1}
   static constexpr int wdec = gm1 + kL;        // D[n-1][t]
@@ -533,7 +533,7 @@ __device__ __forceinline__ void gemm_nt_block(const float* A, int ap, const floa
 constexpr int kBwdThreads = 4 * kL;
 
 template <int S, int D>
-__global__ void __launch_bounds__(kBwdThreads, 128 / kL) gdn_bwd_chunk_kernel(const GdnParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(const GdnParams p) {
   using SM = ChunkSmem<S, D>;
   constexpr int SP = SM::SP, DP = SM::DP, LP = SM::LP, NT = kBwdThreads;
   constexpr int TNS = S / 16, TND = D / 16;  // output columns per thread
@@ -797,8 +797,8 @@ __global__ void __launch_bounds__(kBwdThreads, 128 / kL) gdn_bwd_chunk_kernel(co
     float dec = 1.f;
     for (int i = 0; i < q; ++i) dec *= sqf[i * kL + tau];
     const float gm = sgm1[tau];
-    float acc = 0.f;
-#pragma unroll 4
+    float acc = 0.f, dst[kQ];
+#pragma unroll
     for (int i = 0; i < kQ; ++i) {
       const int t = tq + i;
       float* pc = scb + t * LP + tau;
@@ -806,17 +806,20 @@ __global__ void __launch_bounds__(kBwdThreads, 128 / kL) gdn_bwd_chunk_kernel(co
       if (t < tau) {
         *pc = 0.f;
         *pd = 0.f;
-        sdsT[tau * LP + t] = 0.f;
+        dst[i] = 0.f;
       } else {
         if (t > tau) dec *= sal[t];
         const float ds = dec * *pd;
         *pc = dec * *pc;
         *pd = ds;
-        sdsT[tau * LP + t] = ds;
+        dst[i] = ds;
         acc = fmaf(dec, fmaf(gm, sz[t], sy[t * LP + tau]), acc);
       }
     }
     sqa[q * kL + tau] = acc;
+    __syncthreads();  // every read of Y is done: dS^T takes its place
+#pragma unroll
+    for (int i = 0; i < kQ; ++i) sdsT[tau * LP + tq + i] = dst[i];
   }
   __syncthreads();
   if (tid < kL) {

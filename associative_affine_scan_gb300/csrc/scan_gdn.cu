@@ -564,7 +564,8 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
   const int64_t T = p.T, r0 = bh * T + k * kL;
   const int n = (int)(T - k * kL < kL ? T - k * kL : kL);
 
-  // ---- inputs of the chunk (rows past n zeroed), H_in^T, G_out, G_out^T ----
+  // ---- inputs of the chunk (rows past n zeroed), H_in and G_out, all by
+  // asynchronous copies; then G_out^T and <G_out, H_in> from shared memory ----
   for (int i = tid; i < n * (S / 4); i += NT) {
     const int t = i / (S / 4), q = 4 * (i - t * (S / 4));
     cp_async16(sb + t * SP + q, p.b + (r0 + t) * S + q);
@@ -574,6 +575,15 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
     const int t = i / (D / 4), q = 4 * (i - t * (D / 4));
     cp_async16(sv + t * DP + q, p.v + (r0 + t) * D + q);
     cp_async16(sdo + t * DP + q, p.dout + (r0 + t) * D + q);
+  }
+  {
+    const float* hin = p.ckpt + blk * S * D;
+    const float* gout = p.wsS + blk * S * D;
+    for (int i = tid; i < S * (D / 4); i += NT) {
+      const int s_ = i / (D / 4), q = 4 * (i - s_ * (D / 4));
+      cp_async16(sh + s_ * DP + q, hin + s_ * D + q);
+      cp_async16(sg + s_ * DP + q, gout + s_ * D + q);
+    }
   }
   cp_async_commit();
   for (int i = n * SP + tid; i < kL * SP; i += NT) {
@@ -585,23 +595,20 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
     sdo[i] = 0.f;
   }
   for (int i = tid; i < kL + 4; i += NT) sal[i] = i < n ? __ldg(p.alpha + r0 + i) : 1.f;
-  float win = 0.f;
-  {
-    const float* hin = p.ckpt + blk * S * D;
-    const float* gout = p.wsS + blk * S * D;
-    for (int e = tid; e < S * D; e += NT) {
-      const int s = e / D, d = e - s * D;
-      const float h = __ldg(hin + e), g = __ldcg(gout + e);
-      sh[s * DP + d] = h;
-      sg[s * DP + d] = g;
-      sgT[d * SP + s] = g;
-      win = fmaf(h, g, win);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) win += __shfl_xor_sync(kFullMask, win, o);
-  if (lane == 0) sred[warp] = win;
   cp_async_wait<0>();
+  __syncthreads();
+  {
+    float win = 0.f;
+    for (int e = tid; e < S * D; e += NT) {
+      const int s_ = e / D, d = e - s_ * D;
+      const float g = sg[s_ * DP + d];
+      sgT[d * SP + s_] = g;
+      win = fmaf(sh[s_ * DP + d], g, win);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) win += __shfl_xor_sync(kFullMask, win, o);
+    if (lane == 0) sred[warp] = win;
+  }
   __syncthreads();
 
   // ---- gate products: Gamma_t, Gamma_{t-1} (warp 0); D[n-1][t] (warp 1) ----

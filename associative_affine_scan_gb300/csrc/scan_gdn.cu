@@ -565,7 +565,11 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
   const int n = (int)(T - k * kL < kL ? T - k * kL : kL);
 
   // ---- inputs of the chunk (rows past n zeroed), H_in and G_out, all by
-  // asynchronous copies; then G_out^T and <G_out, H_in> from shared memory ----
+  // asynchronous copies; then G_out^T and <G_out, H_in> from shared memory.
+  // The gates are loaded first and stored last, so their latency passes
+  // under the copies' issue. ----
+  static_assert(NT >= kL + 4, "one gate per thread");
+  const float gate = tid < n ? __ldg(p.alpha + r0 + tid) : 1.f;  // 1 past the chunk's end
   for (int i = tid; i < n * (S / 4); i += NT) {
     const int t = i / (S / 4), q = 4 * (i - t * (S / 4));
     cp_async16(sb + t * SP + q, p.b + (r0 + t) * S + q);
@@ -594,7 +598,7 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
     sv[i] = 0.f;
     sdo[i] = 0.f;
   }
-  for (int i = tid; i < kL + 4; i += NT) sal[i] = i < n ? __ldg(p.alpha + r0 + i) : 1.f;
+  if (tid < kL + 4) sal[tid] = gate;
   cp_async_wait<0>();
   __syncthreads();
   {

@@ -370,6 +370,25 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
   const float* gb = p.b + bh * T * S;
   const float* gc = p.c + bh * T * S;
   const float* gv = p.v + bh * T * D;
+  // The chunk's gates, kLF / 32 per lane, are loaded first and written to a
+  // stage's slot only after its copies and the state's loads are under way
+  // (a load stored straight into shared memory would hold the warp there).
+  static_assert(NT == 32 && kStage <= 32 && 32 % kStage == 0, "one warp per chunk");
+  constexpr int GPL = kLF / 32;
+  float gates[GPL];
+#pragma unroll
+  for (int i = 0; i < GPL; ++i) {
+    const int t = 32 * i + lane;
+    gates[i] = t < n ? __ldg(p.alpha + bh * T + tc + t) : 0.f;
+  }
+  auto put_gates = [&](int st) {  // stage st's kStage gates into slot st & 1
+    const int e0 = st * kStage, j = lane - (e0 & 31);
+    float gv_ = gates[0];
+#pragma unroll
+    for (int i = 1; i < GPL; ++i)
+      if ((e0 >> 5) == i) gv_ = gates[i];
+    if (j >= 0 && j < kStage && e0 + j < n) s_al[st & 1][j] = gv_;
+  };
   // stage st of the chunk into slot st & 1 (a ring of two)
   auto issue = [&](int st) {
     const int64_t t0 = tc + st * kStage;
@@ -379,7 +398,6 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
     stage_block(s_c[q], gc + t0 * S, rows * S, tid, NT);
     stage_block(s_v[q], gv + t0 * D, rows * D, tid, NT);
     cp_async_commit();
-    if (tid < rows) s_al[q][tid] = __ldg(p.alpha + bh * T + t0 + tid);
   };
   issue(0);
   if (nst > 1) issue(1);
@@ -389,6 +407,8 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
 #pragma unroll
     for (int i = 0; i < RS; ++i) h[i] = __ldcg(hin + (s0 + i) * D + d);
   }
+  put_gates(0);
+  if (nst > 1) put_gates(1);
   for (int stg = 0; stg < nst; ++stg) {
     if (stg + 1 < nst) cp_async_wait<1>();
     else cp_async_wait<0>();
@@ -428,7 +448,10 @@ __global__ void __launch_bounds__(Layout<S, D, CW_>::NT) gdn_fwd_kernel(const Gd
       if (g == 0) __stcs(p.o + (bh * T + t) * D + d, o);
     }
     __syncthreads();  // slot st is read; refill it with stage stg + 2
-    if (stg + 2 < nst) issue(stg + 2);
+    if (stg + 2 < nst) {
+      issue(stg + 2);
+      put_gates(stg + 2);
+    }
   }
 }
 

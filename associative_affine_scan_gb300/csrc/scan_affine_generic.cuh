@@ -290,6 +290,10 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
     auto blk = [&](int64_t t) -> int64_t { return (b * T + t) * NN + (active ? n : 0); };
     const int lns = ln < NL ? ln : 0;  // shared-memory slot (threads past NL lanes idle)
 
+    // two steps per loop trip let the next step's loads rise above this one's
+    // arithmetic: faster for k = 2 and k = 16 (forward 7-20 %), slower for
+    // k = 1 and k = 8 (5-20 %), measured over the envelope
+    constexpr int kStepUnroll = (K == 2 || K == 16) ? 2 : 1;
     // ---- pass 1: column c of the sub-chunk summary (P, Q) ----
     float Pc[K], Qc[K];
 #pragma unroll
@@ -299,6 +303,7 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
     }
     if (active && t_lo < t_hi) {
       if (MODE == MODE_FWD) {
+        #pragma unroll kStepUnroll
         for (int64_t t = t_lo; t < t_hi; ++t) {
           float d[K];
           if (zero_b) {
@@ -311,6 +316,7 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
         }
       } else {
         // G_t = A_{t+1}^T G_{t+1} + dH_t, walking t downwards
+        #pragma unroll kStepUnroll
         for (int64_t t = t_hi - 1; t >= t_lo; --t) {
           float d[K];
           ld_col<K, V>(p.dH + blk(t) * KV, c, d);
@@ -421,6 +427,7 @@ __global__ void __launch_bounds__(128) generic_kernel(const __grid_constant__ Af
     const bool work = active && t_lo < t_hi;
     if (MODE == MODE_FWD) {
       if (work && c < V) {
+        #pragma unroll kStepUnroll
         for (int64_t t = t_lo; t < t_hi; ++t) {
           float d[K];
           if (zero_b) {

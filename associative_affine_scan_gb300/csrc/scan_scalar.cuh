@@ -1560,6 +1560,22 @@ __global__ void __launch_bounds__(256) scalar_scan_kernel(const __grid_constant_
   scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
 }
 
+// The dense log-space forward waits on memory with a third of the warp slots
+// filled at its default 76 registers; held to 64 (four 256-thread blocks per
+// SM) it runs 5 % faster on the 8 x 1536 x 4096 rows. (Stating a minimum of
+// one block for the other kernels changes their budget too, so they keep the
+// form above.)
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
+__global__ void __launch_bounds__(256, 4)
+    scalar_scan_kernel_r64(const __grid_constant__ ScalarParams p) {
+  scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
+}
+
+template <class Op, int MODE, bool VARLEN>
+constexpr bool uses_r64() {
+  return std::is_same<Op, LogOp>::value && MODE == MODE_FWD && !VARLEN;
+}
+
 // The stream kernel: persistent warps, occupancy bounded by shared memory.
 template <class Op, int MODE, bool VARLEN, int J, typename TA>
 __global__ void __launch_bounds__(256, 1)
@@ -1578,7 +1594,12 @@ __global__ void __launch_bounds__(256, 1)
 // Host-side dispatch over the compile-time choices.
 template <class Op, int MODE, typename TA, int VARIANT, bool VARLEN, bool VEC, int J>
 cudaError_t launch_one(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
-  auto kern = scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+  auto kern = [] {  // only the chosen kernel is instantiated
+    if constexpr (uses_r64<Op, MODE, VARLEN>())
+      return scalar_scan_kernel_r64<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+    else
+      return scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+  }();
   if (pl.smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pl.smem);

@@ -48,8 +48,11 @@ def check(lib, w):
     assert max(errs.values()) <= TOL, errs
 
 
+# T covers the backward's 32-step chunks (31, 32, 33), the forward's 64-step
+# chunks (63, 64, 65) and the checkpoint a forward chunk writes in its middle
+# (96, 97), with ragged tails.
 @pytest.mark.parametrize("S,D", [(16, 16), (16, 32), (32, 16), (32, 32)])
-@pytest.mark.parametrize("T", [1, 5, 16, 17, 63, 64, 65, 130, 257])
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 31, 32, 33, 63, 64, 65, 96, 97, 130, 257])
 def test_gdn_shapes(lib, S, D, T):
     for h0 in (True, False):
         w = workloads.gdn(2, 3, T, S, D, seed=T * 7 + S + D + h0, h0=h0)

@@ -42,9 +42,9 @@ BWD_BYTES = 20
 # kernel-level Fwd+Bwd table, seqlen 4096: 0.602 ms on an H100 (fp32 inferred)
 PAGES_FWD_BWD_MS = {"dense_4k": 0.602, "dense_64k": 9.212}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward
-# kernel on dense_4k (604.28 + 357.60 MB), from a full ncu capture of the
-# current kernel; None for a workload without a capture
-BWD_TRAFFIC_BYTES = {"dense_4k": 961879552}
+# kernel on dense_4k (604.20 + 360.27 MB), from a full ncu capture of the
+# current kernel and launch shape; None for a workload without a capture
+BWD_TRAFFIC_BYTES = {"dense_4k": 964472576}
 L2_FLUSH_BYTES = 256 << 20
 
 

@@ -52,10 +52,15 @@ int chunk_to_j(int chunk) {
 // wide: rows that prefer chunks of 512 steps on the register-carry kernels:
 // dense fp32 rows of the linear form (interleaved, fully coalesced layout) and
 // dense rows of the log form.
-// short_runs: stationary rows that prefer chunks of 256 steps even when wide
-// (the dense fp32 backward: 0.1695 vs 0.1725 ms on 8 x 1536 x 4096 rows).
+// short_runs: stationary rows that prefer chunks of 256 steps even when wide:
+// dense fp32 rows of the linear form, whose kernels at that length are held
+// to 72 registers (28 row-warps per SM). On 8 x 1536 rows the backward ran
+// 0.1651 ms at T = 4096 and 2.516 ms at T = 65536 (chunks of 512 at the
+// default budget: 0.1725 and 2.572), the forward 0.1015 / 1.464 ms (0.1014 /
+// 1.480).
 // r_default: rows per block when the caller leaves it to the planner (dense
-// fp32 rows: 2, forward 0.1012 vs 0.1020 ms, backward as above).
+// fp32 rows: 2; forward 0.1012 vs 0.1020 ms and backward 0.1694 vs 0.1711 ms
+// at 4 rows, at T = 4096).
 scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, bool wide,
                         const scan_opts& o, ScalarPlan* pl, bool short_runs = false,
                         int r_default = 4) {
@@ -335,7 +340,7 @@ scan_status scan_fwd(const void* a, const void* x, const float* h0, const int32_
   ScalarParams p;
   ScalarPlan pl;
   const bool dense32 = !cu && dt == SCAN_F32;
-  scan_status st = prepare(B, C, T, cu, n_seqs, 1, dense32, o, ws, ws_bytes, &p, &pl, false,
+  scan_status st = prepare(B, C, T, cu, n_seqs, 1, dense32, o, ws, ws_bytes, &p, &pl, dense32,
                            dense32 ? 2 : 4);
   if (st != SCAN_OK) return st;
   if (p.rows * T == 0) return SCAN_OK;

@@ -1576,6 +1576,25 @@ constexpr bool uses_r64() {
   return std::is_same<Op, LogOp>::value && MODE == MODE_FWD && !VARLEN;
 }
 
+// Dense fp32 rows of the linear form, stationary, in chunks of up to 256
+// steps: at the default budget (80 registers) 24 row-warps fit an SM, and
+// the 12,288 rows of the 8 x 1536 workload take 3.4 waves whose last one
+// leaves HBM short of loads in flight. Held to 72 registers (no spills at
+// these chunk lengths) 28 fit, 2.9 waves: backward 0.1696 -> 0.1654 ms at
+// T = 4096 and 2.562 -> 2.516 ms at T = 65536; forward in chunks of 256
+// 1.516 -> 1.464 ms at T = 65536, equal at 4096. (At 64 registers the
+// T = 4096 rows lost again; chunks of 512 spill under either cap.)
+template <class Op, int MODE, bool VARLEN, bool VEC, int J, typename TA, int VARIANT>
+__global__ void __maxnreg__(72) scalar_scan_kernel_r72(const __grid_constant__ ScalarParams p) {
+  scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
+}
+
+template <class Op, bool VARLEN, int J, typename TA, int VARIANT>
+constexpr bool uses_r72() {
+  return std::is_same<Op, LinOp>::value && !VARLEN && J <= 2 && std::is_same<TA, float>::value &&
+         VARIANT == VAR_STATIONARY;
+}
+
 // The stream kernel: persistent warps, occupancy bounded by shared memory.
 template <class Op, int MODE, bool VARLEN, int J, typename TA>
 __global__ void __launch_bounds__(256, 1)
@@ -1597,6 +1616,8 @@ cudaError_t launch_one(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t
   auto kern = [] {  // only the chosen kernel is instantiated
     if constexpr (uses_r64<Op, MODE, VARLEN>())
       return scalar_scan_kernel_r64<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
+    else if constexpr (uses_r72<Op, VARLEN, J, TA, VARIANT>())
+      return scalar_scan_kernel_r72<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
     else
       return scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
   }();

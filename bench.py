@@ -42,9 +42,9 @@ BWD_BYTES = 20
 # kernel-level Fwd+Bwd table, seqlen 4096: 0.602 ms on an H100 (fp32 inferred)
 PAGES_FWD_BWD_MS = {"dense_4k": 0.602, "dense_64k": 9.212}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward
-# kernel on dense_4k (604.20 + 360.27 MB), from a full ncu capture of the
+# kernel on dense_4k (604.34 + 358.28 MB), from a full ncu capture of the
 # current kernel and launch shape; None for a workload without a capture
-BWD_TRAFFIC_BYTES = {"dense_4k": 964472576}
+BWD_TRAFFIC_BYTES = {"dense_4k": 962622976}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -544,7 +544,7 @@ def main():
                 "frac": fwd_gbs / peak},
         "bwd": {"ms": r["bwd_ms"], "elem_per_s": r["n"] / (r["bwd_ms"] * 1e-3), "gbs": bwd_gbs,
                 "frac": bwd_gbs / peak},
-        "roofline": {"bound": "hbm", "kernel": "scalar_scan_kernel (backward)",
+        "roofline": {"bound": "hbm", "kernel": "scalar_scan_kernel_r72 (backward)",
                      "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
                      "peak_source": peak_kind,
                      "traffic": BWD_TRAFFIC_BYTES.get(args.workload)},

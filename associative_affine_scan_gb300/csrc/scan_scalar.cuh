@@ -1589,10 +1589,12 @@ __global__ void __maxnreg__(72) scalar_scan_kernel_r72(const __grid_constant__ S
   scalar_scan_body<Op, MODE, VARLEN, VEC, J, TA, VARIANT>(p);
 }
 
-template <class Op, bool VARLEN, int J, typename TA, int VARIANT>
+// (Not the log-space backward, which runs the linear form's recurrence: its
+// vectorised kernel already uses 72 registers at the default budget.)
+template <class Op, int MODE, bool VARLEN, int J, typename TA, int VARIANT>
 constexpr bool uses_r72() {
-  return std::is_same<Op, LinOp>::value && !VARLEN && J <= 2 && std::is_same<TA, float>::value &&
-         VARIANT == VAR_STATIONARY;
+  return std::is_same<Op, LinOp>::value && MODE != MODE_LOGBWD && !VARLEN && J <= 2 &&
+         std::is_same<TA, float>::value && VARIANT == VAR_STATIONARY;
 }
 
 // The stream kernel: persistent warps, occupancy bounded by shared memory.
@@ -1616,7 +1618,7 @@ cudaError_t launch_one(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t
   auto kern = [] {  // only the chosen kernel is instantiated
     if constexpr (uses_r64<Op, MODE, VARLEN>())
       return scalar_scan_kernel_r64<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
-    else if constexpr (uses_r72<Op, VARLEN, J, TA, VARIANT>())
+    else if constexpr (uses_r72<Op, MODE, VARLEN, J, TA, VARIANT>())
       return scalar_scan_kernel_r72<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
     else
       return scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;

@@ -50,7 +50,8 @@ int chunk_to_j(int chunk) {
 // Per-shape plan for the scalar and log forms. rows = B*C (dense) or C (packed);
 // nbr = number of branches launched together.
 // wide: rows that prefer chunks of 512 steps on the register-carry kernels:
-// dense fp32 rows of the linear form (interleaved, fully coalesced layout) and
+// dense rows of the linear form's forward (fp32: the interleaved, fully
+// coalesced layout; bf16: lane runs of 16 steps), dense fp32 backward rows and
 // dense rows of the log form.
 // short_runs: stationary rows that prefer chunks of 256 steps even when wide:
 // dense fp32 rows of the linear form, whose kernels at that length are held
@@ -339,9 +340,11 @@ scan_status scan_fwd(const void* a, const void* x, const float* h0, const int32_
   const scan_opts o = defaults(opts);
   ScalarParams p;
   ScalarPlan pl;
+  // dense bf16 rows: lane runs of 16 steps, one row per block (8 x 1536 x
+  // 4096: 0.0900 vs 0.0996 ms at runs of 8 and 4 rows per block)
   const bool dense32 = !cu && dt == SCAN_F32;
-  scan_status st = prepare(B, C, T, cu, n_seqs, 1, dense32, o, ws, ws_bytes, &p, &pl, dense32,
-                           dense32 ? 2 : 4);
+  scan_status st = prepare(B, C, T, cu, n_seqs, 1, !cu, o, ws, ws_bytes, &p, &pl, dense32,
+                           dense32 ? 2 : (cu ? 4 : 1));
   if (st != SCAN_OK) return st;
   if (p.rows * T == 0) return SCAN_OK;
   if (!a || !x || !h) return SCAN_ERR_INVALID_ARG;
@@ -365,9 +368,11 @@ scan_status scan_bwd(const void* a, const float* h, const float* dh, const float
   const scan_opts o = defaults(opts);
   ScalarParams p;
   ScalarPlan pl;
+  // dense bf16 rows keep runs of 8 (16: 0.163 vs 0.137 ms on 8 x 1536 x
+  // 4096), two rows per block (4: 0.1382 ms)
   const bool dense32 = !cu && dt == SCAN_F32;
   scan_status st = prepare(B, C, T, cu, n_seqs, 1, dense32, o, ws, ws_bytes, &p, &pl, dense32,
-                           dense32 ? 2 : 4);
+                           cu ? 4 : 2);
   if (st != SCAN_OK) return st;
   const int64_t n_h0 = cu ? (int64_t)n_seqs * C : B * C;
   if (p.rows * T == 0) return zero_dh0(dh0, n_h0, stream);

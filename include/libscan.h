@@ -125,7 +125,8 @@ typedef struct scan_opts {
   int32_t variant;       /* scan_variant; 0 = AUTO */
   int32_t chunk;         /* scalar/log: elements of T per block row, one of 128, 256, 512;
                             affine: time steps per block, one of 64, 128, 256; 0 = planner */
-  int32_t rows_per_cta;  /* scalar/log: rows (channels) per block, 1..16; 0 = planner */
+  int32_t rows_per_cta;  /* scalar/log: rows (channels) per block, 1..8 (blocks of 32 x
+                            rows_per_cta threads); 0 = planner */
   int32_t test_stall;    /* test hook: 1 makes one look-back wait on a summary that is
                             never published, so the wait limit expires (SCAN_ERR_TIMEOUT) */
   double wait_limit_s;   /* bound on every look-back wait; <= 0 means 1.0 second */

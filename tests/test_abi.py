@@ -138,9 +138,10 @@ def test_host_side_checks_need_no_gpu():
              None) == scan.SCAN_ERR_INVALID_ARG
     # bad option values
     opts = scan.ScanOpts()
-    opts.rows_per_cta = 99
-    assert f(fake, fake, None, None, 0, fake, 1, 4, 64, 0, 0, ctypes.byref(opts), ws, 1 << 20,
-             None) == scan.SCAN_ERR_INVALID_ARG
+    for r in (99, 9, -1):  # rows per block: 1..8, 0 = planner
+        opts.rows_per_cta = r
+        assert f(fake, fake, None, None, 0, fake, 1, 4, 64, 0, 0, ctypes.byref(opts), ws, 1 << 20,
+                 None) == scan.SCAN_ERR_INVALID_ARG
     # empty problem: nothing to launch, OK
     assert f(None, None, None, None, 0, None, 1, 0, 64, 0, 0, None, ws, 4096, None) == scan.SCAN_OK
 

@@ -244,6 +244,13 @@ class _Workspaces:
             buf = self._buf.get(key)
             if buf is None or buf.numel() < nbytes:
                 size = max(nbytes, 4096)
+                # The caching allocator orders a block's reuse by torch's current
+                # stream only, while the library uses the buffer on `stream`:
+                # wait for the device before a smaller buffer is given back (a
+                # kernel on `stream` may still read it) and before a new block,
+                # which may still be in use by work queued on another stream,
+                # is zeroed on `stream`. Buffers only grow, so this is rare.
+                torch.cuda.synchronize(device)
                 buf = torch.empty(size, dtype=torch.uint8, device=device)
                 _check(lib().scan_workspace_init(_ptr(buf), size, stream), "scan_workspace_init")
                 self._buf[key] = buf
@@ -623,17 +630,32 @@ def gdn_fwd(alpha, b, v, c, h0=None, *, checkpoints=True, out=None, workspace=No
             raise ValueError(f"checkpoints: needs {n} contiguous floats")
     elif checkpoints:
         ckpt = torch.empty(max(n, 1), dtype=torch.float32, device=dev)
+    own_ws = workspace is None
     workspace = _gdn_workspace(workspace, B, H, T, S, D, dev, "gdn_fwd")
     s = _stream(stream, dev)
     st = lib().gdn_fwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(o), _ptr(ckpt),
                        B, H, T, S, D, _ptr(workspace),
                        workspace.numel() * workspace.element_size(), s)
     _check(st, "gdn_fwd")
+    if own_ws:
+        _release_after(workspace, s, dev)
     return o, ckpt
 
 
 def gdn_workspace_bytes(B, H, T, S, D) -> int:
     return int(lib().gdn_workspace_bytes(B, H, T, S, D))
+
+
+def _release_after(t, s, dev):
+    """A scratch tensor allocated here and used by work queued on stream `s`:
+    when `s` is not torch's current stream, tell the caching allocator not to
+    reuse its memory before that work is done (it orders reuse by the
+    allocation stream only)."""
+    h = s.value or 0  # ctypes gives None for the null stream
+    if h == torch.cuda.current_stream(dev).cuda_stream:
+        return
+    ds = torch.cuda.default_stream(dev)
+    t.record_stream(ds if h == ds.cuda_stream else torch.cuda.ExternalStream(h, device=dev))
 
 
 def _gdn_workspace(workspace, B, H, T, S, D, dev, name):
@@ -661,12 +683,15 @@ def gdn_bwd(alpha, b, v, c, ckpt, dout, *, need_dh0=True, out=None, workspace=No
     else:
         dal, db, dv, dc = (torch.empty_like(t) for t in (alpha, b, v, c))
         dh0 = torch.empty((B, H, S, D), dtype=torch.float32, device=dev) if need_dh0 else None
+    own_ws = workspace is None
     workspace = _gdn_workspace(workspace, B, H, T, S, D, dev, "gdn_bwd")
     s = _stream(stream, dev)
     st = lib().gdn_bwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(ckpt), _ptr(dout), _ptr(dal),
                        _ptr(db), _ptr(dv), _ptr(dc), _ptr(dh0), B, H, T, S, D, _ptr(workspace),
                        workspace.numel() * workspace.element_size(), s)
     _check(st, "gdn_bwd")
+    if own_ws:
+        _release_after(workspace, s, dev)
     return dal, db, dv, dc, dh0
 
 

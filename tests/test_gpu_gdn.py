@@ -151,3 +151,22 @@ def test_gdn_fwd_rejects_a_short_workspace(lib):
     o2, k2 = lib.gdn_fwd(alpha, b, v, c, h0)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(k1, k2)
+
+
+def test_gdn_on_a_side_stream(lib):
+    """A caller's own stream: the same results bit for bit as on the current
+    stream, with the scratch workspace the binding allocates kept alive until
+    the side stream's kernels are done."""
+    w = workloads.gdn(2, 4, 300, 32, 32, seed=11, h0=True)
+    alpha, b, v, c, dout, h0 = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout, w.h0))
+    o_ref, ck_ref = lib.gdn_fwd(alpha, b, v, c, h0)
+    g_ref = lib.gdn_bwd(alpha, b, v, c, ck_ref, dout)
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    for _ in range(3):  # later calls reuse memory the allocator got back
+        o, ck = lib.gdn_fwd(alpha, b, v, c, h0, stream=side)
+        g = lib.gdn_bwd(alpha, b, v, c, ck, dout, stream=side)
+    side.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(ck, ck_ref)
+    for got, ref in zip(g, g_ref):
+        assert torch.equal(got, ref)

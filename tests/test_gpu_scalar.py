@@ -94,6 +94,31 @@ def test_dense_bf16(lib, T):
             check_fwd_bwd(lib, w.a, w.x, w.dh, w.h0, None, rev, opts)
 
 
+def test_dense_on_a_side_stream(lib):
+    """A caller's own stream gets its own cached workspace and the results of
+    the current stream: bit for bit when stationary; within the fp32 bound
+    through the look-back, whose carry may be composed from predecessors'
+    summaries in another order from run to run."""
+    w = workloads.scalar_dense(2, 5, 3000, seed=21, h0=True)
+    a, x, dh, h0 = cuda(w.a, w.x, w.dh, w.h0)
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    for variant in (lib.SCAN_VARIANT_STATIONARY, lib.SCAN_VARIANT_LOOKBACK):
+        opts = {"variant": variant}
+        h_ref = lib.scan_fwd(a, x, h0, opts=opts)
+        g_ref = lib.scan_bwd(a, h_ref, dh, h0, opts=opts)
+        for _ in range(2):
+            h = lib.scan_fwd(a, x, h0, opts=opts, stream=side)
+            g = lib.scan_bwd(a, h, dh, h0, opts=opts, stream=side)
+        side.synchronize()
+        for got, ref in zip((h,) + tuple(g), (h_ref,) + tuple(g_ref)):
+            if variant == lib.SCAN_VARIANT_STATIONARY:
+                assert torch.equal(got, ref)
+            else:
+                assert rel_err(got, ref.double().cpu().numpy()) <= TOL32
+    assert lib.scan_get_device_status(DEV, stream=side) == lib.SCAN_OK
+
+
 def test_dense_no_h0_and_gates_near_one(lib):
     w = workloads.scalar_dense(2, 4, 4100, seed=3, gate="sigmoid2", h0=False)
     check_fwd_bwd(lib, w.a, w.x, w.dh, None, None, False)

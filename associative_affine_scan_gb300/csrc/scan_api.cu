@@ -264,6 +264,17 @@ size_t elt(scan_dtype dt) { return dt == SCAN_BF16 ? 2 : 4; }
 }  // namespace
 
 namespace scan {
+scan_status scalar_plan_status(int64_t rows, int64_t T, int nbr, const scan_opts* opts) {
+  const scan_opts o = defaults(opts);
+  for (int w = 0; w < 2; ++w)
+    for (int sr = 0; sr < 2; ++sr) {
+      ScalarPlan pl;
+      const scan_status st = plan_scalar(rows, T, nbr, false, w != 0, o, &pl, sr != 0);
+      if (st != SCAN_OK) return st;
+    }
+  return SCAN_OK;
+}
+
 cudaError_t launch_fill_zero(float* p, int64_t n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "../../include/libscan.h"
+#include "scan_internal.h"
 
 namespace scan {
 namespace {
@@ -79,6 +80,15 @@ extern "C" scan_status scan_step_host(const scan_host_io* host, const scan_devic
   if (o.variant == SCAN_VARIANT_AUTO) o.variant = SCAN_VARIANT_STATIONARY;
   const int np = (int)(pieces == 0 ? (rows < 8 ? rows : 8) : (pieces < rows ? pieces : rows));
   const int64_t esz = dt == SCAN_F32 ? 4 : 2;
+  // The plans of the largest piece are checked before anything is queued, so
+  // a call rejected for its options or its workspace leaves nothing in flight
+  // (a smaller piece needs no more workspace than the largest).
+  const int64_t big = (rows + np - 1) / np;
+  const scan_status ps = scalar_plan_status(big, T, 1, &o);
+  if (ps != SCAN_OK) return ps;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SCAN_ERR_WORKSPACE;
+  for (scan_op op : {SCAN_OP_FWD, SCAN_OP_BWD})
+    if (workspace_bytes < scan_workspace_bytes(op, 1, big, T, 0, 0, &o)) return SCAN_ERR_WORKSPACE;
 
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return SCAN_ERR_CUDA;
@@ -88,6 +98,13 @@ extern "C" scan_status scan_step_host(const scan_host_io* host, const scan_devic
   if (!pp.ready && make_pipe(pp) != cudaSuccess) return SCAN_ERR_CUDA;
 
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // on a failure after the first copy was queued, the caller's stream still
+  // waits for the copies in flight (best effort) before the status returns
+  auto fail = [&](scan_status st) {
+    if (ok(cudaEventRecord(pp.end, pp.in))) cudaStreamWaitEvent(stream, pp.end, 0);
+    if (ok(cudaEventRecord(pp.end, pp.out))) cudaStreamWaitEvent(stream, pp.end, 0);
+    return st;
+  };
   // the copies start after the work already queued on the caller's stream
   if (!ok(cudaEventRecord(pp.start, stream)) || !ok(cudaStreamWaitEvent(pp.in, pp.start, 0)) ||
       !ok(cudaStreamWaitEvent(pp.out, pp.start, 0)))
@@ -102,31 +119,31 @@ extern "C" scan_status scan_step_host(const scan_host_io* host, const scan_devic
     if (!ok(cudaMemcpyAsync(byte(dev->a, lo), cbyte(host->a, lo), nb, h2d, pp.in)) ||
         !ok(cudaMemcpyAsync(byte(dev->x, lo), cbyte(host->x, lo), nb, h2d, pp.in)) ||
         !ok(cudaMemcpyAsync(byte(dev->dh, lo4), cbyte(host->dh, lo4), nb4, h2d, pp.in)))
-      return SCAN_ERR_CUDA;
+      return fail(SCAN_ERR_CUDA);
     if (host->h0 && !ok(cudaMemcpyAsync(dev->h0 + r0, host->h0 + r0, n * 4, h2d, pp.in)))
-      return SCAN_ERR_CUDA;
-    if (!ok(cudaEventRecord(pp.in_done[i], pp.in))) return SCAN_ERR_CUDA;
+      return fail(SCAN_ERR_CUDA);
+    if (!ok(cudaEventRecord(pp.in_done[i], pp.in))) return fail(SCAN_ERR_CUDA);
     // ---- scans (the caller's stream) ----
-    if (!ok(cudaStreamWaitEvent(stream, pp.in_done[i], 0))) return SCAN_ERR_CUDA;
+    if (!ok(cudaStreamWaitEvent(stream, pp.in_done[i], 0))) return fail(SCAN_ERR_CUDA);
     scan_status st = scan_fwd(cbyte(dev->a, lo), cbyte(dev->x, lo), dev->h0 ? dev->h0 + r0 : nullptr,
                               nullptr, 0, reinterpret_cast<float*>(byte(dev->h, lo4)), 1, n, T, dt,
                               0, &o, workspace, workspace_bytes, stream);
-    if (st != SCAN_OK) return st;
+    if (st != SCAN_OK) return fail(st);
     st = scan_bwd(cbyte(dev->a, lo), reinterpret_cast<const float*>(cbyte(dev->h, lo4)),
                   reinterpret_cast<const float*>(cbyte(dev->dh, lo4)),
                   dev->h0 ? dev->h0 + r0 : nullptr, nullptr, 0, byte(dev->da, lo),
                   byte(dev->dx, lo), dev->dh0 ? dev->dh0 + r0 : nullptr, 1, n, T, dt, 0, &o,
                   workspace, workspace_bytes, stream);
-    if (st != SCAN_OK) return st;
-    if (!ok(cudaEventRecord(pp.scanned[i], stream))) return SCAN_ERR_CUDA;
+    if (st != SCAN_OK) return fail(st);
+    if (!ok(cudaEventRecord(pp.scanned[i], stream))) return fail(SCAN_ERR_CUDA);
     // ---- out ----
-    if (!ok(cudaStreamWaitEvent(pp.out, pp.scanned[i], 0))) return SCAN_ERR_CUDA;
+    if (!ok(cudaStreamWaitEvent(pp.out, pp.scanned[i], 0))) return fail(SCAN_ERR_CUDA);
     if (!ok(cudaMemcpyAsync(byte(host->h, lo4), cbyte(dev->h, lo4), nb4, d2h, pp.out)) ||
         !ok(cudaMemcpyAsync(byte(host->da, lo), cbyte(dev->da, lo), nb, d2h, pp.out)) ||
         !ok(cudaMemcpyAsync(byte(host->dx, lo), cbyte(dev->dx, lo), nb, d2h, pp.out)))
-      return SCAN_ERR_CUDA;
+      return fail(SCAN_ERR_CUDA);
     if (host->dh0 && !ok(cudaMemcpyAsync(host->dh0 + r0, dev->dh0 + r0, n * 4, d2h, pp.out)))
-      return SCAN_ERR_CUDA;
+      return fail(SCAN_ERR_CUDA);
   }
   // the caller's stream continues after the last copy out
   if (!ok(cudaEventRecord(pp.end, pp.out)) || !ok(cudaStreamWaitEvent(stream, pp.end, 0)))

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/libscan.h"
+
 namespace scan {
 
 // MODE_LOGBWD: the backward of the log-space form, run as the linear adjoint
@@ -200,5 +202,10 @@ cudaError_t launch_affine_bwd(const AffineParams& p, const AffinePlan& pl, cudaS
 
 // Writes zeros to n floats (empty-input edge cases).
 cudaError_t launch_fill_zero(float* p, int64_t n, cudaStream_t s);
+
+// Status the planner gives dense rows of the scalar form with these options
+// (every layout it may pick), without launching anything: SCAN_OK,
+// SCAN_ERR_INVALID_ARG or SCAN_ERR_UNSUPPORTED.
+scan_status scalar_plan_status(int64_t rows, int64_t T, int nbr, const scan_opts* opts);
 
 }  // namespace scan

@@ -345,9 +345,13 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v,
  * defaults to SCAN_VARIANT_STATIONARY (a piece has fewer rows than the GPU has
  * warp slots). workspace: scan_workspace_bytes(SCAN_OP_BWD, 1, C', T, ...) for
  * the largest piece of C' = ceil(B*C / pieces) rows, shared by the pieces'
- * scans (they run in order on `stream`). Asynchronous: on return the whole step
- * is queued and `stream` waits for its last copy; calls on one device are
- * serialised on the host. */
+ * scans (they run in order on `stream`). The options and shape of the
+ * largest piece (SCAN_ERR_INVALID_ARG / SCAN_ERR_UNSUPPORTED) and the
+ * workspace (missing, not 16-byte aligned or too small: SCAN_ERR_WORKSPACE)
+ * are checked before anything is queued; a CUDA error after that returns
+ * SCAN_ERR_CUDA with `stream` made to wait for the copies already queued.
+ * Asynchronous: on return the whole step is queued and `stream` waits for its
+ * last copy; calls on one device are serialised on the host. */
 typedef struct {
   const void* a;
   const void* x;

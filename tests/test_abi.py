@@ -164,9 +164,9 @@ def test_step_host_argument_checks_need_no_gpu():
     full = dict(a=fk, x=fk, h0=None, dh=fk, h=fk, da=fk, dx=fk, dh0=None)
     hio, dio = HostIO(**full), DeviceIO(**full)
     ws = ctypes.c_void_p(0x100000)
-    call = lambda h, d, B=1, C=4, T=64, dt=0, pieces=0: f(
+    call = lambda h, d, B=1, C=4, T=64, dt=0, pieces=0, opts=None, w=ws, nw=4096: f(
         ctypes.byref(h) if h is not None else None, ctypes.byref(d) if d is not None else None,
-        B, C, T, dt, pieces, None, ws, 4096, None)
+        B, C, T, dt, pieces, ctypes.byref(opts) if opts is not None else None, w, nw, None)
     assert call(None, dio) == scan.SCAN_ERR_INVALID_ARG
     assert call(hio, None) == scan.SCAN_ERR_INVALID_ARG
     assert call(hio, dio, dt=7) == scan.SCAN_ERR_INVALID_ARG
@@ -177,5 +177,27 @@ def test_step_host_argument_checks_need_no_gpu():
     assert call(hio, DeviceIO(**dict(full, dh0=fk))) == scan.SCAN_ERR_INVALID_ARG
     # a missing result buffer
     assert call(HostIO(**dict(full, dx=None)), dio) == scan.SCAN_ERR_INVALID_ARG
+    # options and workspace are checked before the first copy is queued
+    bad = scan.ScanOpts()
+    bad.rows_per_cta = 99
+    assert call(hio, dio, opts=bad) == scan.SCAN_ERR_INVALID_ARG
+    bad = scan.ScanOpts()
+    bad.chunk = 300
+    assert call(hio, dio, opts=bad) == scan.SCAN_ERR_INVALID_ARG
+    assert call(hio, dio, w=None) == scan.SCAN_ERR_WORKSPACE
+    assert call(hio, dio, w=ctypes.c_void_p(0x100008)) == scan.SCAN_ERR_WORKSPACE
+    lb = scan.ScanOpts()
+    lb.variant = scan.SCAN_VARIANT_LOOKBACK  # per-chunk summaries: more than a header
+    need = scan.scan_workspace_bytes(scan.SCAN_OP_FWD, 1, 4096, 4096, opts=lb)
+    assert need > 4096
+    assert call(hio, dio, C=8192, T=4096, pieces=2, opts=lb, nw=need - 16) == \
+        scan.SCAN_ERR_WORKSPACE
     # empty problem: nothing to copy or launch
     assert call(HostIO(), DeviceIO(), C=0) == scan.SCAN_OK
+    # valid calls pass those checks and reach the device: without a GPU the
+    # first CUDA call fails (never run where a GPU would take the fake pointers)
+    import torch
+    if not torch.cuda.is_available():
+        for opts in (None, lb):
+            assert call(hio, dio, C=12288, T=4096, pieces=8, opts=opts, nw=1 << 30) == \
+                scan.SCAN_ERR_CUDA

@@ -314,9 +314,10 @@ def measure_rows(args, dev, scan, names=ROWS, small=False):
 
 
 def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
-    # per (head, step), S = D = 32: fwd reads alpha, b, c (S), v (D) and writes
-    # o (D) plus a 4 KB checkpoint every 32 steps; bwd reads alpha, b, c, v,
-    # dout and the checkpoints and writes dalpha, db, dc, dv
+    # per (head, step): fwd reads alpha, b, c (S each), v (D) and writes o (D)
+    # plus an S x D checkpoint every 32 steps; bwd reads alpha, b, c, v, dout
+    # and the checkpoints and writes dalpha, db, dc (S side: 16 S bytes) and
+    # dv (D side: v, dout, dv, 12 D bytes)
     w = workloads.gdn_4k(seed=0)
     alpha, b, v, c, dout = (t.to(dev) for t in (w.alpha, w.b, w.v, w.c, w.dout))
     S, D = b.shape[-1], v.shape[-1]
@@ -324,7 +325,7 @@ def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
     o, ck = scan.gdn_fwd(alpha, b, v, c, workspace=ws)
     n = alpha.numel()
     f_bytes = n * (4 + 8 * S + 8 * D) + ck.numel() * 4
-    b_bytes = n * (8 + 16 * S + 16 * D) + ck.numel() * 4
+    b_bytes = n * (8 + 16 * S + 12 * D) + ck.numel() * 4
     f_ms = time_calls(lambda: scan.gdn_fwd(alpha, b, v, c, checkpoints=ck, out=o, workspace=ws),
                       steps, warm, flush, stream)
     g = scan.gdn_bwd(alpha, b, v, c, ck, dout, workspace=ws)

@@ -11,7 +11,9 @@ results, so their error is bounded by the magnitudes of their terms, not by
 the result (cancellation): if G and H each meet e in the max(1, |.|) metric,
 dA_il is within 2e sum_j max(1, |G_ij|) max(1, |H_lj|). Their error is
 normalised by that term scale (resp. sum_l |A_li| max(1, |G_lj|) for dh0),
-computed from the oracle's own values.
+computed from the oracle's own values. Beside that gate, the plain metric
+max |got - ref| / max(1, |ref|) of dA and dh0 is computed, printed and held to
+1e-3, the gate "Triton scan kernels" (Conformance) puts on affine gradients.
 """
 
 import json
@@ -22,11 +24,13 @@ import pytest
 import torch
 
 import oracle
+from _sweep import max_rel, sweep
 from associative_affine_scan_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
+TOL_GRAD_PLAIN = 1e-3
 DEV = torch.device("cuda", 0)
 HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -64,7 +68,11 @@ def run_and_check(lib, w, opts=None):
     sA, s0 = contraction_scales(w.A, w.h0, ref_H, ref_dB)
     errs = {"H": rel_err(H, ref_H), "dA": rel_err(dA, ref_dA, sA), "dB": rel_err(dB, ref_dB),
             "dh0": rel_err(dh0, ref_dh0, s0)}
+    plain = {"dA": rel_err(dA, ref_dA), "dh0": rel_err(dh0, ref_dh0)}
+    print("affine", tuple(w.A.shape), "plain-metric gradient error", plain)
     assert max(errs.values()) <= TOL, errs
+    assert max(plain.values()) <= TOL_GRAD_PLAIN, plain
+    return plain
 
 
 @pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 200, 1000])
@@ -208,22 +216,40 @@ def test_affine_wait_limit_reports_timeout(lib):
     assert rel_err(H, oracle.affine_fwd(w.A, w.Bm, w.h0)) <= TOL
 
 
-def test_full_affine_4x4_sampled_lanes(lib):
+def test_full_affine_4x4_all_lanes(lib):
+    """Every output of the 8 x 4096 x 256 block workload (k = v = 4) against the
+    oracle, in batches of 32 lanes: H and dB within 1e-5 of max(1, |ref|), dA
+    and dh0 within 1e-5 of their term scale and within 1e-3 in the plain
+    metric (both printed)."""
     w = workloads.affine_4x4(seed=0)
     A, Bm, dH = w.A.to(DEV), w.Bm.to(DEV), w.dH.to(DEV)
     H = lib.affine_scan_fwd(A, Bm)
     dA, dB, dh0 = lib.affine_scan_bwd(A, H, dH)
     torch.cuda.synchronize()
     assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
-    g = np.random.default_rng(4)
+    del A, Bm, dH
     B, T, N = w.A.shape[:3]
-    lanes = [(0, 0), (B - 1, N - 1)] + [(int(g.integers(B)), int(g.integers(N))) for _ in range(10)]
-    for b, n in lanes:
-        sl = (slice(b, b + 1), slice(None), slice(n, n + 1))
-        ref_H = oracle.affine_fwd(w.A[sl], w.Bm[sl])
-        ref_dA, ref_dB, ref_dh0 = oracle.affine_bwd(w.A[sl], w.Bm[sl], w.dH[sl])
-        sA, s0 = contraction_scales(w.A[sl], None, ref_H, ref_dB)
-        assert rel_err(H[sl], ref_H) <= TOL, (b, n)
-        assert rel_err(dA[sl], ref_dA, sA) <= TOL, (b, n)
-        assert rel_err(dB[sl], ref_dB) <= TOL, (b, n)
-        assert rel_err(dh0[b:b + 1, n:n + 1], ref_dh0, s0) <= TOL, (b, n)
+    lanes = 32
+    groups = (N + lanes - 1) // lanes
+
+    def check(i0, i1):
+        e = {}
+        for i in range(i0, i1):
+            b, n0 = i // groups, (i % groups) * lanes
+            sl = (slice(b, b + 1), slice(None), slice(n0, min(N, n0 + lanes)))
+            ref_H = oracle.affine_fwd(w.A[sl], w.Bm[sl])
+            ref_dA, ref_dB, ref_dh0 = oracle.affine_bwd(w.A[sl], w.Bm[sl], w.dH[sl])
+            sA, s0 = contraction_scales(w.A[sl], None, ref_H, ref_dB)
+            got_dh0 = dh0[b:b + 1, sl[2]]
+            for k, v in (("H", max_rel(H[sl], ref_H)), ("dB", max_rel(dB[sl], ref_dB)),
+                         ("dA", max_rel(dA[sl], ref_dA, sA)), ("dh0", max_rel(got_dh0, ref_dh0, s0)),
+                         ("dA_plain", max_rel(dA[sl], ref_dA)),
+                         ("dh0_plain", max_rel(got_dh0, ref_dh0))):
+                e[k] = max(e.get(k, 0.0), v)
+        return e
+
+    errs = sweep(B * groups, 1, check)
+    print("affine_4x4 all lanes", errs)
+    assert errs["items"] == B * groups
+    assert max(errs[k] for k in ("H", "dB", "dA", "dh0")) <= TOL, errs
+    assert max(errs["dA_plain"], errs["dh0_plain"]) <= TOL_GRAD_PLAIN, errs

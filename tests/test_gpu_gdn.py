@@ -10,6 +10,9 @@ values, dalpha a sum over S * D; each error is normalised by the sum of the
 absolute values of its terms, which the oracle computes by running on
 |alpha|, |b|, |v|, |c|, |h0|, |dout| (every term becomes its absolute value),
 and must stay within 1e-5 of it (or of max(1, |ref|), whichever is larger).
+The plain metric max |got - ref| / max(1, |ref|) of every gradient is
+computed beside it, printed, and held to 1e-3 (the gate "Triton scan kernels",
+Conformance, puts on gradients of the affine scan).
 """
 
 import numpy as np
@@ -17,18 +20,25 @@ import pytest
 import torch
 
 import oracle
+from _sweep import sweep
 from associative_affine_scan_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
+TOL_GRAD_PLAIN = 1e-3
 DEV = torch.device("cuda", 0)
 
 
-def err(got, ref, scale):
+def err(got, ref, scale=None):
     got = got.detach().double().cpu().numpy()
-    den = np.maximum(np.maximum(1.0, np.abs(ref)), scale)
+    den = np.maximum(1.0, np.abs(ref))
+    if scale is not None:
+        den = np.maximum(den, scale)
     return 0.0 if got.size == 0 else float(np.max(np.abs(got - ref) / den))
+
+
+GRADS = ("dalpha", "db", "dv", "dc", "dh0")
 
 
 def check(lib, w):
@@ -43,9 +53,13 @@ def check(lib, w):
     sc_o = oracle.gdn_fwd(ab(w.alpha), ab(w.b), ab(w.v), ab(w.c), ab(w.h0))
     sc_g = oracle.gdn_bwd(ab(w.alpha), ab(w.b), ab(w.v), ab(w.c), ab(w.dout), ab(w.h0))
     errs = {"o": err(o, ref_o, sc_o)}
-    for name, got, ref, sc in zip(("dalpha", "db", "dv", "dc", "dh0"), g, ref_g, sc_g):
+    plain = {}
+    for name, got, ref, sc in zip(GRADS, g, ref_g, sc_g):
         errs[name] = err(got, ref, sc)
+        plain[name] = err(got, ref)
+    print("gdn", tuple(w.b.shape), "plain-metric gradient error", plain)
     assert max(errs.values()) <= TOL, errs
+    assert max(plain.values()) <= TOL_GRAD_PLAIN, plain
 
 
 # T covers the backward's 32-step chunks (31, 32, 33), the forward's 64-step
@@ -86,25 +100,42 @@ def test_gdn_rejects_unsupported_shapes(lib):
     assert e.value.status == lib.SCAN_ERR_UNSUPPORTED
 
 
-def test_gdn_4k_sampled_heads(lib):
-    """The bench workload (8 x 32 heads x 4096 steps, 32 x 32 state), every
-    output of 6 sampled heads against the oracle."""
+def test_gdn_4k_all_heads(lib):
+    """Every output of the bench workload (8 x 32 heads x 4096 steps, 32 x 32
+    state) against the oracle, head by head on the host cores: within 1e-5 of
+    the term scale, and the gradients within 1e-3 in the plain metric."""
     w = workloads.gdn_4k(seed=0)
     alpha, b, v, c, dout = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout))
     o, ck = lib.gdn_fwd(alpha, b, v, c)
-    dal, db, dv, dc, dh0 = lib.gdn_bwd(alpha, b, v, c, ck, dout)
+    outs = lib.gdn_bwd(alpha, b, v, c, ck, dout)
     torch.cuda.synchronize()
-    for bb, hh in ((0, 0), (0, 31), (3, 7), (5, 20), (7, 0), (7, 31)):
-        sl = lambda t: t[bb:bb + 1, hh:hh + 1]
-        ins = [sl(t) for t in (w.alpha, w.b, w.v, w.c)]
-        ref_o = oracle.gdn_fwd(*ins)
-        ref_g = oracle.gdn_bwd(*ins, sl(w.dout))
-        absin = [t.abs() for t in ins]
-        sc_o = oracle.gdn_fwd(*absin)
-        sc_g = oracle.gdn_bwd(*absin, sl(w.dout).abs())
-        assert err(sl(o), ref_o, sc_o) <= TOL, (bb, hh)
-        for got, ref, sc in zip((sl(dal), sl(db), sl(dv), sl(dc), sl(dh0)), ref_g, sc_g):
-            assert err(got, ref, sc) <= TOL, (bb, hh)
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    B, H = w.alpha.shape[:2]
+
+    def check(i0, i1):
+        e = {}
+        for i in range(i0, i1):
+            bb, hh = divmod(i, H)
+            sl = lambda t: t[bb:bb + 1, hh:hh + 1]
+            ins = [sl(t) for t in (w.alpha, w.b, w.v, w.c)]
+            ref_o = oracle.gdn_fwd(*ins)
+            ref_g = oracle.gdn_bwd(*ins, sl(w.dout))
+            absin = [t.abs() for t in ins]
+            sc_o = oracle.gdn_fwd(*absin)
+            sc_g = oracle.gdn_bwd(*absin, sl(w.dout).abs())
+            vals = [("o", err(sl(o), ref_o, sc_o))]
+            for name, got, ref, sc in zip(GRADS, outs, ref_g, sc_g):
+                vals.append((name, err(sl(got), ref, sc)))
+                vals.append((name + "_plain", err(sl(got), ref)))
+            for k, val in vals:
+                e[k] = max(e.get(k, 0.0), val)
+        return e
+
+    errs = sweep(B * H, 4, check)
+    print("gdn_4k all heads", errs)
+    assert errs["items"] == B * H
+    assert max(errs[k] for k in ("o",) + GRADS) <= TOL, errs
+    assert max(errs[k + "_plain"] for k in GRADS) <= TOL_GRAD_PLAIN, errs
 
 
 @pytest.mark.parametrize("T", [64, 200])

@@ -14,7 +14,6 @@ namespace {
 
 constexpr int64_t kMaxGrid = 0x7fffffffLL;
 constexpr int64_t kStationaryMinRows = 152 * 16;
-constexpr int kCuSmemEntries = 4096;  // packed offsets staged in shared memory
 constexpr bool kStreamOutTiles = true;  // stream: interior outputs leave by tensor stores
 
 __global__ void fill_zero_kernel(float* p, int64_t n) {
@@ -196,6 +195,7 @@ scan_status prepare(int64_t B, int64_t C, int64_t T, const int32_t* cu, int32_t 
   p->hdr = static_cast<WsHeader*>(ws);
   p->recs = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(ws) +
                                                   kWsHeaderBytes);
+  p->rec_bytes = pl->ws_bytes - kWsHeaderBytes;
   p->wait_limit_ns = wait_ns(o);
   p->test_stall = o.test_stall;
   return SCAN_OK;
@@ -563,6 +563,7 @@ scan_status prepare_affine(int64_t B, int64_t T, int64_t N, int32_t k, int32_t v
   p->ntiles = (int64_t)pl->M * pl->G;
   p->hdr = static_cast<WsHeader*>(ws);
   p->recs = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeaderBytes);
+  p->rec_bytes = pl->ws_bytes - kWsHeaderBytes;
   p->wait_limit_ns = wait_ns(o);
   p->test_stall = o.test_stall;
   return SCAN_OK;

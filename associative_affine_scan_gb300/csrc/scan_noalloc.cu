@@ -35,6 +35,10 @@ std::atomic<void*> g_scratch_ptr[kMaxDevices];
 // Device address of g_noalloc_scratch on the current device. In host code the
 // symbol's name is only a host-side stand-in, so the address must come from
 // cudaGetSymbolAddress, called once per device with that device current.
+// Nothing is written here: a __device__ array without an initialiser is
+// zero-filled when the module is loaded, so the header (tile ticket, epoch,
+// completion counter, status word) starts at 0 with no copy or memset that
+// could race with a kernel already queued on another stream.
 scan_status scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SCAN_ERR_CUDA;
@@ -45,13 +49,26 @@ scan_status scratch_on_current_device(void** out) {
     p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
     if (!p) {
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SCAN_ERR_CUDA;
-      // the tile ticket, completion counter and status word must start at 0
-      if (cudaMemset(p, 0, kWsHeaderBytes) != cudaSuccess) return SCAN_ERR_CUDA;
       g_scratch_ptr[dev].store(p, std::memory_order_release);
     }
   }
   *out = p;
   return SCAN_OK;
+}
+
+// The scratch is per device and the launch goes to the current device: the
+// tensors must live there (a pointer of another device is refused).
+bool on_current_device(const void* ptr) {
+  int dev = 0;
+  cudaPointerAttributes at;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged
+             ? at.device == dev
+             : false;
 }
 
 }  // namespace
@@ -79,6 +96,8 @@ extern "C" scan_status scan_fwd_noalloc(const void* a, const void* x, const floa
   const size_t need = kWsHeaderBytes + (size_t)(rows * M) * 16u;
   if (need > kScratchBytes) return SCAN_ERR_WORKSPACE;  // beyond the fixed scratch
 
+  if (!on_current_device(a) || !on_current_device(x) || !on_current_device(h))
+    return SCAN_ERR_INVALID_ARG;
   void* scratch = nullptr;
   scan_status st = scratch_on_current_device(&scratch);
   if (st != SCAN_OK) return st;
@@ -96,7 +115,8 @@ extern "C" scan_status scan_fwd_noalloc(const void* a, const void* x, const floa
   pl.nseg = 1;
   pl.cps = (int)M;
   pl.ws_bytes = need;
-  pl.smem = cu_seqlens ? 4u * (size_t)(n_seqs + 1 <= 4096 ? n_seqs + 1 : 4096) : 0;
+  // as for scan_fwd: offsets staged in shared memory only when they all fit
+  pl.smem = cu_seqlens && n_seqs + 1 <= kCuSmemEntries ? 4u * (size_t)(n_seqs + 1) : 0;
 
   ScalarParams p;
   std::memset(&p, 0, sizeof(p));
@@ -119,6 +139,7 @@ extern "C" scan_status scan_fwd_noalloc(const void* a, const void* x, const floa
   p.hdr = static_cast<WsHeader*>(scratch);
   p.recs = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(scratch) +
                                                   kWsHeaderBytes);
+  p.rec_bytes = need - kWsHeaderBytes;
   p.wait_limit_ns = 1000000000ULL;
   const cudaError_t e = dt == SCAN_F32 ? launch_scalar_fwd_f32(p, pl, stream)
                                        : launch_scalar_fwd_bf16(p, pl, stream);

@@ -532,11 +532,7 @@ __global__ void __launch_bounds__(128) affine_kernel(const __grid_constant__ Aff
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned d = atomicAdd(&p.hdr->done, 1u);
-    if (d == gridDim.x - 1) {
-      p.hdr->done = 0u;
-      atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
-      __threadfence();
-    }
+    if (d == gridDim.x - 1) finish_lookback_launch(p.hdr, p.recs, p.rec_bytes, epoch);
   }
 }
 

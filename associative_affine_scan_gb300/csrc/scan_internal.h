@@ -67,9 +67,47 @@ struct alignas(64) WsHeader {
   // count of finished blocks (the last one resets all three)
   unsigned int branch_ticket[2];
   unsigned int branch_done;
+  // the most record bytes any launch has used on this workspace since the
+  // records were last cleared (see finish_lookback_launch)
+  unsigned long long rec_bytes;
 };
+static_assert(sizeof(WsHeader) <= 256, "the header fits its 256 bytes");
 
 constexpr size_t kWsHeaderBytes = 256;  // records start here
+
+#ifdef __CUDACC__
+// End of a launch that took tile tickets, run by thread 0 of the block that
+// finished last (every other block has counted itself done after its work):
+// clear the completion count, reset the ticket and advance the epoch.
+// Record tags carry only the epoch's low 30 bits (tag = epoch * 4 + kind), so
+// on one workspace a tag comes back every 2^30 launches. A record that no
+// launch rewrote in between would then pass for a current one; so before the
+// epoch whose tag bits wrap to zero, every record byte any launch has used
+// since the last clear is zeroed (a zero word carries tag 0, which no record
+// kind uses). This costs one pass over the records per 2^30 launches.
+__device__ __forceinline__ void finish_lookback_launch(WsHeader* hdr, void* recs,
+                                                       unsigned long long rec_bytes,
+                                                       uint32_t epoch) {
+  hdr->done = 0u;
+  if (rec_bytes > hdr->rec_bytes) hdr->rec_bytes = rec_bytes;
+  const uint32_t next = epoch + 1u;
+  if ((next & 0x3fffffffu) == 0u) {
+    const unsigned long long n = hdr->rec_bytes / 4;  // records are whole floats
+    uint4* w16 = static_cast<uint4*>(recs);           // 16-byte aligned (after the header)
+    const unsigned long long n16 = n / 4;
+    for (unsigned long long i = 0; i < n16; ++i) w16[i] = make_uint4(0u, 0u, 0u, 0u);
+    unsigned int* w4 = static_cast<unsigned int*>(recs);
+    for (unsigned long long i = n16 * 4; i < n; ++i) w4[i] = 0u;
+    hdr->rec_bytes = 0ull;
+    __threadfence();
+  }
+  atomicExch(&hdr->ticket_epoch, ((unsigned long long)next) << 32);
+  __threadfence();
+}
+#endif
+// Packed offsets are staged in shared memory when n_seqs + 1 entries fit in
+// this many; otherwise the kernels read cu_seqlens from global memory.
+constexpr int kCuSmemEntries = 4096;
 
 // One branch of a scalar scan launch.
 struct BranchArgs {
@@ -104,6 +142,7 @@ struct ScalarParams {
   int tma_out;        // stream: interior chunks leave through tiles and tensor stores
   int64_t tile_hi;    // stream: flat elements [0, tile_hi) of every input are reachable by tiles
   unsigned long long* recs;  // look-back records: [nbr][rows][M] x 16 bytes
+  unsigned long long rec_bytes;  // bytes of records this launch may use
   WsHeader* hdr;
   unsigned long long wait_limit_ns;
   int test_stall;
@@ -134,6 +173,7 @@ struct TmaMaps {
 // tiles of 128 J elements and the 128-byte swizzle. False if the driver entry
 // point is missing or refuses the map.
 bool encode_tile_map(CUtensorMap* m, const void* ptr, int elt, int64_t n, int J);
+bool encode_rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int box_rows);
 
 // Launchers (one translation unit per mode/dtype family).
 cudaError_t launch_scalar_fwd_f32(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
@@ -162,6 +202,7 @@ struct AffineParams {
   int G;             // lane groups = B * ceil(N / 32)
   int64_t ntiles;
   float* recs;       // look-back records: [B*N][M] x record floats
+  unsigned long long rec_bytes;  // bytes of records this launch may use
   WsHeader* hdr;
   unsigned long long wait_limit_ns;
   int test_stall;

@@ -1431,11 +1431,7 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
     if (threadIdx.x == 0) {
       __threadfence();
       const unsigned d = atomicAdd(&p.hdr->done, 1u);
-      if (d == gridDim.x - 1) {
-        p.hdr->done = 0u;
-        atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
-        __threadfence();
-      }
+      if (d == gridDim.x - 1) finish_lookback_launch(p.hdr, p.recs, p.rec_bytes, epoch);
     }
   } else if (VARIANT == VAR_STATIONARY) {
     // Two branches scan in opposite directions, each through its own copy of
@@ -1544,11 +1540,7 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
     if (threadIdx.x == 0) {
       __threadfence();
       const unsigned d = atomicAdd(&p.hdr->done, 1u);
-      if (d == gridDim.x - 1) {
-        p.hdr->done = 0u;
-        atomicExch(&p.hdr->ticket_epoch, ((unsigned long long)(epoch + 1u)) << 32);
-        __threadfence();
-      }
+      if (d == gridDim.x - 1) finish_lookback_launch(p.hdr, p.recs, p.rec_bytes, epoch);
     }
   }
 }

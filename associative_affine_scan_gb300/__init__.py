@@ -14,6 +14,8 @@ from ._binding import (  # noqa: F401
     EXPORTED,
     LIB_PATH,
     SCAN_BF16,
+    SCAN_COPY_TMA,
+    SCAN_COPY_VEC,
     SCAN_ERR_ALIGNMENT,
     SCAN_ERR_CUDA,
     SCAN_ERR_INVALID_ARG,
@@ -49,6 +51,7 @@ from ._binding import (  # noqa: F401
     scan_bidir_bwd,
     scan_bidir_fwd,
     scan_bwd,
+    scan_copy,
     scan_fwd,
     scan_fwd_noalloc,
     scan_step_host,

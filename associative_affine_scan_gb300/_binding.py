@@ -46,12 +46,15 @@ SCAN_OP_AFFINE_FWD = 5
 SCAN_OP_AFFINE_BWD = 6
 SCAN_OP_LOG_BWD = 7
 
+SCAN_COPY_VEC = 0
+SCAN_COPY_TMA = 1
+
 EXPORTED = (
     "scan_status_string", "scan_version", "scan_workspace_bytes", "scan_workspace_init",
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
     "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "affine_prefix_fwd",
     "affine_prefix_bwd", "gdn_checkpoint_bytes", "gdn_fwd", "gdn_workspace_bytes", "gdn_bwd",
-    "scan_fwd_noalloc", "scan_step_host",
+    "scan_fwd_noalloc", "scan_step_host", "scan_copy",
 )
 
 
@@ -126,6 +129,7 @@ _SIGS = {
                           ctypes.c_int),
     "scan_fwd_noalloc": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, ctypes.c_int, _i32,
                           _vp], ctypes.c_int),
+    "scan_copy": ([_vp, _vp, _sz, _i32, _vp, _vp], ctypes.c_int),
 }
 
 _lock = threading.Lock()
@@ -153,6 +157,13 @@ def lib() -> ctypes.CDLL:
 
 def status_string(status: int) -> str:
     return lib().scan_status_string(int(status)).decode()
+
+
+def _call(device, name: str, *args):
+    """Call entry point `name` with `device` current: the library launches on
+    the current device, which must be the one holding the tensors."""
+    with torch.cuda.device(device):
+        return getattr(lib(), name)(*args)
 
 
 def _check(status: int, where: str) -> None:
@@ -252,7 +263,8 @@ class _Workspaces:
                 # is zeroed on `stream`. Buffers only grow, so this is rare.
                 torch.cuda.synchronize(device)
                 buf = torch.empty(size, dtype=torch.uint8, device=device)
-                _check(lib().scan_workspace_init(_ptr(buf), size, stream), "scan_workspace_init")
+                _check(_call(device, "scan_workspace_init", _ptr(buf), size, stream),
+                       "scan_workspace_init")
                 self._buf[key] = buf
             return buf
 
@@ -291,8 +303,9 @@ def scan_workspace_bytes(op: int, B: int, C: int, T: int, k: int = 0, v: int = 0
 def scan_workspace_init(workspace: torch.Tensor, stream=None) -> None:
     """Zero a caller-owned workspace (a CUDA uint8 tensor) on `stream`."""
     _need(workspace, "workspace")
-    _check(lib().scan_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
-                                     _stream(stream, workspace.device)), "scan_workspace_init")
+    _check(_call(workspace.device, "scan_workspace_init", _ptr(workspace),
+                 workspace.numel() * workspace.element_size(), _stream(stream, workspace.device)),
+           "scan_workspace_init")
 
 
 def scan_get_device_status(device=None, stream=None) -> int:
@@ -302,7 +315,7 @@ def scan_get_device_status(device=None, stream=None) -> int:
     buf = _ws.current(device, s)
     if buf is None:
         return SCAN_OK
-    return int(lib().scan_get_device_status(_ptr(buf), s))
+    return int(_call(device, "scan_get_device_status", _ptr(buf), s))
 
 
 def scan_fwd(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None, opts=None, stream=None):
@@ -318,7 +331,7 @@ def scan_fwd(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None, opts=No
     _need(h, "out", dtype=torch.float32, shape=a.shape, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_FWD, B, C, T, 0, 0, opts, dev, s)
-    st = lib().scan_fwd(_ptr(a), _ptr(x), _ptr(h0), _ptr(cu_seqlens), n, _ptr(h), B, C, T, dt,
+    st = _call(dev, "scan_fwd", _ptr(a), _ptr(x), _ptr(h0), _ptr(cu_seqlens), n, _ptr(h), B, C, T, dt,
                         int(bool(reverse)), _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "scan_fwd")
     return h
@@ -346,7 +359,7 @@ def scan_bwd(a, h, dh, h0=None, cu_seqlens=None, reverse=False, *, out=None, opt
     _need(dh0, "dh0", dtype=torch.float32, shape=h0_shape, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_BWD, B, C, T, 0, 0, opts, dev, s)
-    st = lib().scan_bwd(_ptr(a), _ptr(h), _ptr(dh), _ptr(h0), _ptr(cu_seqlens), n, _ptr(da),
+    st = _call(dev, "scan_bwd", _ptr(a), _ptr(h), _ptr(dh), _ptr(h0), _ptr(cu_seqlens), n, _ptr(da),
                         _ptr(dx), _ptr(dh0), B, C, T, dt, int(bool(reverse)), _optref(o),
                         _ptr(ws), ws.numel(), s)
     _check(st, "scan_bwd")
@@ -394,7 +407,7 @@ def scan_step_host(a, x, dh, h0=None, *, out, device, pieces=0, opts=None, strea
     if o.variant == SCAN_VARIANT_AUTO:
         o.variant = SCAN_VARIANT_STATIONARY
     ws, nb, _ = workspace_for(SCAN_OP_BWD, 1, rows, T, 0, 0, o, dev, s)
-    st = lib().scan_step_host(ctypes.byref(hio), ctypes.byref(dio), B, C, T, dt, int(pieces),
+    st = _call(dev, "scan_step_host", ctypes.byref(hio), ctypes.byref(dio), B, C, T, dt, int(pieces),
                               _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "scan_step_host")
     return out
@@ -421,7 +434,7 @@ def scan_bidir_fwd(af, xf, ar, xr, h0f=None, h0r=None, cu_seqlens=None, *, out=N
     _need(hr, "hr", dtype=torch.float32, shape=af.shape, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_BIDIR_FWD, B, C, T, 0, 0, opts, dev, s)
-    st = lib().scan_bidir_fwd(_ptr(af), _ptr(xf), _ptr(ar), _ptr(xr), _ptr(h0f), _ptr(h0r),
+    st = _call(dev, "scan_bidir_fwd", _ptr(af), _ptr(xf), _ptr(ar), _ptr(xr), _ptr(h0f), _ptr(h0r),
                               _ptr(cu_seqlens), n, _ptr(hf), _ptr(hr), B, C, T, dt, _optref(o),
                               _ptr(ws), ws.numel(), s)
     _check(st, "scan_bidir_fwd")
@@ -449,7 +462,7 @@ def scan_bidir_bwd(af, hf, dhf, ar, hr, dhr, h0f=None, h0r=None, cu_seqlens=None
         dh0r = torch.empty(h0_shape, dtype=torch.float32, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_BIDIR_BWD, B, C, T, 0, 0, opts, dev, s)
-    st = lib().scan_bidir_bwd(_ptr(af), _ptr(hf), _ptr(dhf), _ptr(h0f), _ptr(ar), _ptr(hr),
+    st = _call(dev, "scan_bidir_bwd", _ptr(af), _ptr(hf), _ptr(dhf), _ptr(h0f), _ptr(ar), _ptr(hr),
                               _ptr(dhr), _ptr(h0r), _ptr(cu_seqlens), n, _ptr(daf), _ptr(dxf),
                               _ptr(dh0f), _ptr(dar), _ptr(dxr), _ptr(dh0r), B, C, T, dt,
                               _optref(o), _ptr(ws), ws.numel(), s)
@@ -470,7 +483,7 @@ def scan_log_fwd(log_a, log_x, log_h0=None, cu_seqlens=None, reverse=False, *, o
     _need(h, "out", dtype=torch.float32, shape=log_a.shape, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_LOG_FWD, B, C, T, 0, 0, opts, dev, s)
-    st = lib().scan_log_fwd(_ptr(log_a), _ptr(log_x), _ptr(log_h0), _ptr(cu_seqlens), n, _ptr(h),
+    st = _call(dev, "scan_log_fwd", _ptr(log_a), _ptr(log_x), _ptr(log_h0), _ptr(cu_seqlens), n, _ptr(h),
                             B, C, T, int(bool(reverse)), _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "scan_log_fwd")
     return h
@@ -499,7 +512,7 @@ def scan_log_bwd(log_a, log_x, h, dh, log_h0=None, cu_seqlens=None, reverse=Fals
     _need(dlh0, "dlog_h0", dtype=torch.float32, shape=h0_shape, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_LOG_BWD, B, C, T, 0, 0, opts, dev, s)
-    st = lib().scan_log_bwd(_ptr(log_a), _ptr(log_x), _ptr(h), _ptr(dh), _ptr(log_h0),
+    st = _call(dev, "scan_log_bwd", _ptr(log_a), _ptr(log_x), _ptr(h), _ptr(dh), _ptr(log_h0),
                             _ptr(cu_seqlens), n, _ptr(dla), _ptr(dlx), _ptr(dlh0), B, C, T,
                             int(bool(reverse)), _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "scan_log_bwd")
@@ -526,7 +539,7 @@ def affine_scan_fwd(A, Bm, h0=None, *, out=None, opts=None, stream=None):
     _need(H, "out", dtype=torch.float32, shape=Bm.shape, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_AFFINE_FWD, B, N, T, k, v, opts, dev, s)
-    st = lib().affine_scan_fwd(_ptr(A), _ptr(Bm), _ptr(h0), _ptr(H), B, T, N, k, v, _optref(o),
+    st = _call(dev, "affine_scan_fwd", _ptr(A), _ptr(Bm), _ptr(h0), _ptr(H), B, T, N, k, v, _optref(o),
                                _ptr(ws), ws.numel(), s)
     _check(st, "affine_scan_fwd")
     return H
@@ -548,7 +561,7 @@ def affine_scan_bwd(A, H, dH, h0=None, *, out=None, opts=None, stream=None):
         dh0 = torch.empty((B, N, k, v), dtype=torch.float32, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_AFFINE_BWD, B, N, T, k, v, opts, dev, s)
-    st = lib().affine_scan_bwd(_ptr(A), _ptr(H), _ptr(dH), _ptr(h0), _ptr(dA), _ptr(dB),
+    st = _call(dev, "affine_scan_bwd", _ptr(A), _ptr(H), _ptr(dH), _ptr(h0), _ptr(dA), _ptr(dB),
                                _ptr(dh0), B, T, N, k, v, _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "affine_scan_bwd")
     return dA, dB, dh0
@@ -565,7 +578,7 @@ def affine_prefix_fwd(A, *, out=None, opts=None, stream=None):
     _need(Abar, "out", dtype=torch.float32, shape=A.shape, device=dev)
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_AFFINE_FWD, B, N, T, k, k, opts, dev, s)
-    st = lib().affine_prefix_fwd(_ptr(A), _ptr(Abar), B, T, N, k, _optref(o), _ptr(ws),
+    st = _call(dev, "affine_prefix_fwd", _ptr(A), _ptr(Abar), B, T, N, k, _optref(o), _ptr(ws),
                                  ws.numel(), s)
     _check(st, "affine_prefix_fwd")
     return Abar
@@ -586,7 +599,7 @@ def affine_prefix_bwd(A, Abar, dAbar, dA=None, *, accumulate=False, opts=None, s
     B, T, N, k, _ = A.shape
     s = _stream(stream, dev)
     ws, nb, o = workspace_for(SCAN_OP_AFFINE_BWD, B, N, T, k, k, opts, dev, s)
-    st = lib().affine_prefix_bwd(_ptr(A), _ptr(Abar), _ptr(dAbar), _ptr(dA), int(bool(accumulate)),
+    st = _call(dev, "affine_prefix_bwd", _ptr(A), _ptr(Abar), _ptr(dAbar), _ptr(dA), int(bool(accumulate)),
                                  B, T, N, k, _optref(o), _ptr(ws), ws.numel(), s)
     _check(st, "affine_prefix_bwd")
     return dA
@@ -633,7 +646,7 @@ def gdn_fwd(alpha, b, v, c, h0=None, *, checkpoints=True, out=None, workspace=No
     own_ws = workspace is None
     workspace = _gdn_workspace(workspace, B, H, T, S, D, dev, "gdn_fwd")
     s = _stream(stream, dev)
-    st = lib().gdn_fwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(o), _ptr(ckpt),
+    st = _call(dev, "gdn_fwd", _ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(h0), _ptr(o), _ptr(ckpt),
                        B, H, T, S, D, _ptr(workspace),
                        workspace.numel() * workspace.element_size(), s)
     _check(st, "gdn_fwd")
@@ -686,7 +699,7 @@ def gdn_bwd(alpha, b, v, c, ckpt, dout, *, need_dh0=True, out=None, workspace=No
     own_ws = workspace is None
     workspace = _gdn_workspace(workspace, B, H, T, S, D, dev, "gdn_bwd")
     s = _stream(stream, dev)
-    st = lib().gdn_bwd(_ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(ckpt), _ptr(dout), _ptr(dal),
+    st = _call(dev, "gdn_bwd", _ptr(alpha), _ptr(b), _ptr(v), _ptr(c), _ptr(ckpt), _ptr(dout), _ptr(dal),
                        _ptr(db), _ptr(dv), _ptr(dc), _ptr(dh0), B, H, T, S, D, _ptr(workspace),
                        workspace.numel() * workspace.element_size(), s)
     _check(st, "gdn_bwd")
@@ -713,7 +726,25 @@ def scan_fwd_noalloc(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None,
           device=dev)
     h = out if out is not None else torch.empty(a.shape, dtype=torch.float32, device=dev)
     _need(h, "out", dtype=torch.float32, shape=a.shape, device=dev)
-    st = lib().scan_fwd_noalloc(_ptr(a), _ptr(x), _ptr(h0), _ptr(cu_seqlens), n, _ptr(h), B, C, T,
+    st = _call(dev, "scan_fwd_noalloc", _ptr(a), _ptr(x), _ptr(h0), _ptr(cu_seqlens), n, _ptr(h), B, C, T,
                                 dt, int(bool(reverse)), _stream(stream, dev))
     _check(st, "scan_fwd_noalloc")
     return h
+
+
+def scan_copy(src, dst, mode=SCAN_COPY_VEC, *, status=None, stream=None):
+    """Copy the bytes of src into dst (same byte size) with one of the
+    library's bandwidth-reference copies (SCAN_COPY_VEC or SCAN_COPY_TMA).
+    status: optional CUDA int32 tensor of one element that a TMA wait which
+    expires sets to SCAN_ERR_TIMEOUT. Returns dst."""
+    _need(src, "src")
+    dev = src.device
+    _need(dst, "dst", device=dev)
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("scan_copy: src and dst differ in size")
+    _need(status, "status", dtype=torch.int32, device=dev)
+    st = _call(dev, "scan_copy", _ptr(src), _ptr(dst), nbytes, int(mode), _ptr(status),
+               _stream(stream, dev))
+    _check(st, "scan_copy")
+    return dst

@@ -47,4 +47,23 @@ bool encode_tile_map(CUtensorMap* m, const void* ptr, int elt, int64_t n, int J)
   return r == CUDA_SUCCESS;
 }
 
+// 128-byte rows of a flat buffer as a [rows, 32] fp32 tensor; the box is
+// box_rows whole rows (at most 256), written to shared memory with the
+// 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int box_rows) {
+  std::call_once(g_encode_once, load_encoder);
+  if (!g_encode || !ptr || rows < 1 || rows > (1LL << 32) || box_rows < 1 || box_rows > 256)
+    return false;
+  if (reinterpret_cast<uintptr_t>(ptr) % 16) return false;
+  const cuuint64_t dims[2] = {32, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace scan

@@ -378,6 +378,29 @@ scan_status scan_step_host(const scan_host_io* host, const scan_device_io* dev,
                            void* workspace, size_t workspace_bytes,
                            cudaStream_t stream);
 
+/* scan_copy modes. */
+typedef enum scan_copy_mode {
+  SCAN_COPY_VEC = 0, /* 128-bit streaming loads and stores, grid-stride */
+  SCAN_COPY_TMA = 1  /* 32 KB 2-D tensor-copy tiles through a shared-memory ring */
+} scan_copy_mode;
+
+/* Copies `bytes` from src to dst on the device: the achievable read + write
+ * bandwidth that the scan kernels' roofline fractions are reported against.
+ * No counterpart in the source pages (they time their kernels alone): it
+ * exists so that the ceiling is measured on the same GPU, launch path and
+ * stream as the kernels it bounds, by copies written the way those kernels
+ * move data (SCAN_COPY_VEC: the register path's 16-byte vector accesses;
+ * SCAN_COPY_TMA: the stream variant's tensor copies).
+ *   src, dst: device pointers, 16-byte aligned, not overlapping.
+ *   bytes: a multiple of 16 (VEC) or of 128 (TMA); 0 does nothing.
+ *   status: nullable device word; a TMA wait that expires (1 s) sets it to
+ *     SCAN_ERR_TIMEOUT (the call itself has already returned).
+ * Returns SCAN_ERR_INVALID_ARG for a bad mode, null pointer or size,
+ * SCAN_ERR_ALIGNMENT for misaligned pointers, SCAN_ERR_CUDA if the launch or
+ * the tensor-map encoding fails. Asynchronous on `stream`; allocates nothing. */
+scan_status scan_copy(const void* src, void* dst, size_t bytes, int32_t mode, uint32_t* status,
+                      cudaStream_t stream);
+
 /* Bytes of the library's own scratch used by scan_fwd_noalloc (16 MiB). */
 #define SCAN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -201,3 +201,15 @@ def test_step_host_argument_checks_need_no_gpu():
         for opts in (None, lb):
             assert call(hio, dio, C=12288, T=4096, pieces=8, opts=opts, nw=1 << 30) == \
                 scan.SCAN_ERR_CUDA
+
+
+def test_copy_rejects_bad_arguments_on_the_host(built):
+    """scan_copy checks mode, pointers and alignment before touching the GPU
+    (the pointers here are placeholders that are never dereferenced)."""
+    import associative_affine_scan_gb300 as scan
+    f = scan.lib().scan_copy
+    assert f(1024, 2048, 4096, 7, None, None) == scan.SCAN_ERR_INVALID_ARG
+    assert f(None, 2048, 4096, scan.SCAN_COPY_VEC, None, None) == scan.SCAN_ERR_INVALID_ARG
+    assert f(1024 + 4, 2048, 4096, scan.SCAN_COPY_VEC, None, None) == scan.SCAN_ERR_ALIGNMENT
+    assert f(1024, 2048 + 8, 4096, scan.SCAN_COPY_TMA, None, None) == scan.SCAN_ERR_ALIGNMENT
+    assert f(1024, 2048, 0, scan.SCAN_COPY_TMA, None, None) == scan.SCAN_OK

@@ -2,14 +2,17 @@
 scan on the dense [B=8, C=1536, T=4096] fp32 workload (synthetic, seeded).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload dense_4k|dense_64k] [--all-rows]
+                    [--workload dense_4k|dense_64k] [--no-rows]
 
 Prints one JSON line (rank 0). `value` is whole-job scan elements/s of the
 fwd+bwd step with inputs resident in HBM (CUDA events on the launching stream,
 L2 flushed between steps); `e2e` is the same metric through the C ABI's
 host-buffer step (scan_step_host: pinned host inputs and results, the copies
 pipelined with the scans over row pieces), host<->device copies inside the
-timed region.
+timed region. `rows` times every other workload the same way (the 64K-step
+dense rows, the packed bidirectional bf16 rows, the 4x4 block form, the log
+space, the outer-product state), fwd and bwd, each against the measured copy
+peak and against the library's own copy kernels (`copy`).
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 Under torchrun (N > 1) every rank scans its own copy of the workload (weak
 scaling, no collective on the data path); the step time is the max over ranks.
@@ -42,10 +45,31 @@ BWD_BYTES = 20
 # kernel-level Fwd+Bwd table, seqlen 4096: 0.602 ms on an H100 (fp32 inferred)
 PAGES_FWD_BWD_MS = {"dense_4k": 0.602, "dense_64k": 9.212}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward
-# kernel on dense_4k (604.34 + 358.28 MB), from a full ncu capture of the
-# current kernel and launch shape; None for a workload without a capture
-BWD_TRAFFIC_BYTES = {"dense_4k": 962622976}
+# kernel on dense_4k, from an ncu capture, with the digest of the sources that
+# build that kernel and choose its launch shape at the time of the capture.
+# When the sources differ from the digest the figure no longer describes the
+# kernel that runs, and the line reports traffic as null.
+BWD_TRAFFIC = {"dense_4k": {"bytes": None, "digest": None}}
+KERNEL_SOURCES = ("scan_scalar.cuh", "scan_internal.h", "scan_scalar_bwd_f32.cu", "scan_api.cu")
 L2_FLUSH_BYTES = 256 << 20
+COPY_BYTES = 1 << 30  # per direction, for the copy-ceiling kernels
+
+
+def kernel_digest() -> str:
+    """sha256 over the sources of the dense scalar kernels and their planner."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "associative_affine_scan_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def bwd_traffic(workload: str):
+    t = BWD_TRAFFIC.get(workload)
+    if not t or t["bytes"] is None or t["digest"] != kernel_digest():
+        return None
+    return t["bytes"]
 
 
 def measured_peaks():
@@ -250,13 +274,16 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
-    extra = {}
-    if args.all_rows:
-        extra = measure_rows(args, dev, scan)
+    extra, copy = {}, None
+    if not args.no_rows:
+        del a, x, dh, h, da, dx, dh0, flush
+        torch.cuda.empty_cache()
+        copy = measure_copy(dev, scan, max(3, min(args.steps, 10)))
+        extra = measure_rows(args, dev, scan, ceiling=copy["ceiling_gbs"])
 
     return dict(n=n, B=B, C=C, T=T, ms=ms, fwd_ms=fwd_avg, bwd_ms=bwd_avg, wall=wall,
                 clocks=clocks, e2e_ms=e2e_ms, bytes_in=bytes_in, bytes_out=bytes_out,
-                w=w, extra=extra)
+                w=w, extra=extra, copy=copy)
 
 
 def time_calls(fn, steps, warmup, flush, stream):
@@ -288,32 +315,91 @@ def time_calls(fn, steps, warmup, flush, stream):
     return total / steps
 
 
-ROWS = ("packed_bidir", "log_4k", "affine_4x4", "gdn_4k")
+ROWS = ("dense_64k", "packed_bidir", "affine_4x4", "log_4k", "gdn_4k")
 
 
-def measure_rows(args, dev, scan, names=ROWS, small=False):
-    """Per-row throughput of the other forms (packed bidirectional, affine, log).
+def measure_rows(args, dev, scan, names=ROWS, small=False, ceiling=None):
+    """Throughput of every other workload, fwd and bwd, each timed alone (graph
+    replays, L2 flushed between them); each workload is freed before the next.
 
     small: the packed row with 12 sequences instead of 64 (same 2 x 2048 rows,
-    2.5 GB on the device), the size used for full ncu captures."""
+    2.5 GB on the device), the size used for full ncu captures.
+    ceiling: the library's copy ceiling in GB/s; each row's GB/s is also given
+    as a fraction of it."""
     from associative_affine_scan_gb300 import workloads
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     steps, warm = max(1, min(args.steps, 10)), 3
     out = {}
     peak, _ = measured_peaks()
-    if "packed_bidir" in names:
-        out["packed_bidir"] = _row_packed(scan, workloads, dev, steps, warm, flush, stream, small)
-    if "log_4k" in names:
-        out["log_4k"] = _row_log(scan, workloads, dev, steps, warm, flush, stream, peak)
-    if "affine_4x4" in names:
-        out["affine_4x4"] = _row_affine(scan, workloads, dev, steps, warm, flush, stream)
-    if "gdn_4k" in names:
-        out["gdn_4k"] = _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak)
+    runners = {
+        "dense_64k": lambda: _row_dense(scan, workloads, dev, steps, warm, flush, stream),
+        "packed_bidir": lambda: _row_packed(scan, workloads, dev, steps, warm, flush, stream,
+                                            small),
+        "affine_4x4": lambda: _row_affine(scan, workloads, dev, steps, warm, flush, stream),
+        "log_4k": lambda: _row_log(scan, workloads, dev, steps, warm, flush, stream),
+        "gdn_4k": lambda: _row_gdn(scan, workloads, dev, steps, warm, flush, stream),
+    }
+    for name in names:
+        try:
+            r = runners[name]()
+        except Exception as e:  # reported, not fatal: the other rows still print
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+            continue
+        finally:
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+        for d in ("fwd", "bwd"):
+            r[d + "_frac"] = r[d + "_gbs"] / peak
+            if ceiling:
+                r[d + "_frac_of_copy_kernel"] = r[d + "_gbs"] / ceiling
+        tot_bytes = r["fwd_gbs"] * r["fwd_ms"] + r["bwd_gbs"] * r["bwd_ms"]
+        r["fwd_bwd_gbs"] = tot_bytes / (r["fwd_ms"] + r["bwd_ms"])
+        r["fwd_bwd_frac"] = r["fwd_bwd_gbs"] / peak
+        out[name] = r
     return out
 
 
-def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
+def _row_dense(scan, workloads, dev, steps, warm, flush, stream):
+    # the 8 x 1536 x 65536 fp32 rows: 12 bytes per element forward, 20 backward
+    w = workloads.dense_64k(seed=0)
+    a, x, dh = w.a.to(dev), w.x.to(dev), w.dh.to(dev)
+    del w
+    h = scan.scan_fwd(a, x)
+    n = a.numel()
+    f_ms = time_calls(lambda: scan.scan_fwd(a, x, out=h), steps, warm, flush, stream)
+    g = scan.scan_bwd(a, h, dh)
+    b_ms = time_calls(lambda: scan.scan_bwd(a, h, dh, out=g), steps, warm, flush, stream)
+    return {"elems": n, "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_gbs": n * FWD_BYTES / f_ms / 1e6, "bwd_gbs": n * BWD_BYTES / b_ms / 1e6,
+            "fwd_bwd_elem_per_s": n / (f_ms + b_ms) * 1e3}
+
+
+def measure_copy(dev, scan, steps):
+    """GB/s (read + write) of the library's two copy kernels over COPY_BYTES,
+    timed like the scan rows."""
+    src = torch.empty(COPY_BYTES // 4, dtype=torch.float32, device=dev).uniform_()
+    dst = torch.empty_like(src)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {"bytes_per_direction": COPY_BYTES}
+    peak, _ = measured_peaks()
+    for name, mode in (("vec", scan.SCAN_COPY_VEC), ("tma", scan.SCAN_COPY_TMA)):
+        ms = time_calls(lambda: scan.scan_copy(src, dst, mode, status=status), steps, 3, flush,
+                        stream)
+        gbs = 2 * COPY_BYTES / ms / 1e6
+        out[name] = {"ms": ms, "gbs": gbs, "frac": gbs / peak}
+    torch.cuda.synchronize()
+    if int(status.item()) != 0 or not torch.equal(src, dst):
+        raise RuntimeError("copy kernels: status or contents wrong")
+    out["ceiling_gbs"] = max(out["vec"]["gbs"], out["tma"]["gbs"])
+    del src, dst
+    torch.cuda.empty_cache()
+    return out
+
+
+def _row_gdn(scan, workloads, dev, steps, warm, flush, stream):
     # per (head, step): fwd reads alpha, b, c (S each), v (D) and writes o (D)
     # plus an S x D checkpoint every 32 steps; bwd reads alpha, b, c, v, dout
     # and the checkpoints and writes dalpha, db, dc (S side: 16 S bytes) and
@@ -332,8 +418,7 @@ def _row_gdn(scan, workloads, dev, steps, warm, flush, stream, peak):
     b_ms = time_calls(lambda: scan.gdn_bwd(alpha, b, v, c, ck, dout, out=g, workspace=ws), steps,
                       warm, flush, stream)
     return {"head_steps": n, "fwd_ms": f_ms, "bwd_ms": b_ms,
-            "fwd_gbs": f_bytes / f_ms / 1e6, "bwd_gbs": b_bytes / b_ms / 1e6,
-            "fwd_frac": f_bytes / f_ms / 1e6 / peak, "bwd_frac": b_bytes / b_ms / 1e6 / peak}
+            "fwd_gbs": f_bytes / f_ms / 1e6, "bwd_gbs": b_bytes / b_ms / 1e6}
 
 
 def _row_packed(scan, workloads, dev, steps, warm, flush, stream, small):
@@ -352,7 +437,7 @@ def _row_packed(scan, workloads, dev, steps, warm, flush, stream, small):
             "fwd_bwd_elem_per_s": n / (f_ms + b_ms) * 1e3}
 
 
-def _row_log(scan, workloads, dev, steps, warm, flush, stream, peak):
+def _row_log(scan, workloads, dev, steps, warm, flush, stream):
     # log space: fwd reads log a, log x and writes h (12 B/elem); bwd reads
     # log a, log x, h, dh and writes d log a, d log x (24 B/elem)
     w = workloads.log_4k(seed=0)
@@ -364,24 +449,21 @@ def _row_log(scan, workloads, dev, steps, warm, flush, stream, peak):
     lb_ms = time_calls(lambda: scan.scan_log_bwd(la, lx, hl, ldh, out=gl), steps, warm, flush,
                        stream)
     return {"elems": n, "fwd_ms": l_ms, "bwd_ms": lb_ms,
-            "fwd_gbs": n * 12 / l_ms / 1e6, "bwd_gbs": n * 24 / lb_ms / 1e6,
-            "fwd_frac": n * 12 / l_ms / 1e6 / peak, "bwd_frac": n * 24 / lb_ms / 1e6 / peak}
+            "fwd_gbs": n * 12 / l_ms / 1e6, "bwd_gbs": n * 24 / lb_ms / 1e6}
 
 
 def _row_affine(scan, workloads, dev, steps, warm, flush, stream):
-    try:
-        w = workloads.affine_4x4(seed=0)
-        A, Bm, dH = w.A.to(dev), w.Bm.to(dev), w.dH.to(dev)
-        H = scan.affine_scan_fwd(A, Bm)
-        nb = w.n_blocks
-        f_ms = time_calls(lambda: scan.affine_scan_fwd(A, Bm, out=H), steps, warm, flush, stream)
-        g = scan.affine_scan_bwd(A, H, dH)
-        b_ms = time_calls(lambda: scan.affine_scan_bwd(A, H, dH, out=g), steps, warm, flush,
-                          stream)
-        return {"blocks": nb, "fwd_ms": f_ms, "bwd_ms": b_ms,
-                "fwd_gbs": nb * 192 / f_ms / 1e6, "bwd_gbs": nb * 320 / b_ms / 1e6}
-    except Exception as e:  # reported, not fatal: the other rows still print
-        return {"error": str(e)}
+    # per (b, t, n) block: fwd reads A, B and writes H (3 x 64 bytes); bwd reads
+    # A, H, dH and writes dA, dB (5 x 64 bytes)
+    w = workloads.affine_4x4(seed=0)
+    A, Bm, dH = w.A.to(dev), w.Bm.to(dev), w.dH.to(dev)
+    H = scan.affine_scan_fwd(A, Bm)
+    nb = w.n_blocks
+    f_ms = time_calls(lambda: scan.affine_scan_fwd(A, Bm, out=H), steps, warm, flush, stream)
+    g = scan.affine_scan_bwd(A, H, dH)
+    b_ms = time_calls(lambda: scan.affine_scan_bwd(A, H, dH, out=g), steps, warm, flush, stream)
+    return {"blocks": nb, "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_gbs": nb * 192 / f_ms / 1e6, "bwd_gbs": nb * 320 / b_ms / 1e6}
 
 
 def oracle_fwd_bwd(w, rows, threads=1):
@@ -490,8 +572,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dense_4k", choices=["dense_4k", "dense_64k"])
-    ap.add_argument("--all-rows", action="store_true",
-                    help="also time the packed bidirectional, log and affine forms")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the other workloads and the copy kernels (the headline step only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--row", choices=ROWS,
                     help="time only this form (fwd and bwd, --steps timed calls each) and print "
@@ -548,7 +630,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "scalar_scan_kernel_r72 (backward)",
                      "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
                      "peak_source": peak_kind,
-                     "traffic": BWD_TRAFFIC_BYTES.get(args.workload)},
+                     "traffic": bwd_traffic(args.workload), "kernel_digest": kernel_digest()},
         "e2e": {"value": n_total / (r["e2e_ms"] * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": r["bytes_in"], "d2h_bytes_per_step": r["bytes_out"]},
         "gpu_launches": 2 * args.steps,
@@ -557,6 +639,9 @@ def main():
         "baseline_context": {"ms": pages_ms, "hardware": "H100 80GB",
                              "source": "associative_scan_triton README, kernel-level Fwd+Bwd"},
     }
+    if r["copy"]:
+        line["copy"] = r["copy"]
+        line["roofline"]["frac_of_copy_kernel"] = bwd_gbs / r["copy"]["ceiling_gbs"]
     if r["extra"]:
         line["rows"] = r["extra"]
     if not args.no_cpu_baseline and world == 1:

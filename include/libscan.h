@@ -416,9 +416,14 @@ scan_status scan_copy(const void* src, void* dst, size_t bytes, int32_t mode, ui
  *   - Limit: the call needs 256 + 16 * rows * chunks bytes (rows = B*C, or C
  *     when packed; chunks = ceil((T + 3) / 512) for T > 256). Larger problems
  *     return SCAN_ERR_WORKSPACE and compute nothing; use scan_fwd for them.
- *   - The first call on each device sets the scratch up (looks up its device
- *     address and zeroes its 256-byte header, synchronously); make that first
- *     call before any stream capture on that device.
+ *   - The first call on each device sets the scratch up: it looks up the
+ *     array's device address (cudaGetSymbolAddress, which may load the
+ *     library's device code) and writes nothing; the array is zero when the
+ *     module loads. Make that first call before any stream capture on that
+ *     device.
+ *   - a, x, h (and h0, cu_seqlens) must be device memory of the current
+ *     device, whose scratch the call uses; other pointers return
+ *     SCAN_ERR_INVALID_ARG.
  *   - Every call on a device shares the same scratch and leaves its contents
  *     behind; the kernel resets what the next call needs. Calls whose kernels
  *     overlap on the GPU (different streams, or threads) race on it and give

@@ -553,6 +553,8 @@ cudaError_t launch_kv(const AffineParams& p, const AffinePlan& pl, cudaStream_t 
 // envelope runs the column-thread kernel with streamed A (scan_affine_generic.cuh).
 template <int MODE>
 cudaError_t launch_affine(const AffineParams& p, const AffinePlan& pl, cudaStream_t s) {
+  // the ring kernels cover the plain scan (no coefficient-prefix flags)
+  if (pl.variant == VAR_STATIONARY && p.flags == 0) return launch_affine_ring(p, MODE, s);
   if (p.k == 4 && p.v == 4) return launch_kv<4, 4, MODE>(p, pl, s);
   if (p.k == 2 && p.v == 2) return launch_kv<2, 2, MODE>(p, pl, s);
   switch (p.k) {

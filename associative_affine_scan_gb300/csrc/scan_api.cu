@@ -131,6 +131,11 @@ scan_status plan_scalar(int64_t rows, int64_t T, int nbr, bool varlen, bool wide
   return SCAN_OK;
 }
 
+// Lane groups of 8 (one warp each) from which the 4 x 4 ring kernel is the
+// default: below about one warp per SM the look-back kernels, which split T
+// into chunks, keep more of the GPU busy.
+constexpr int64_t kAffineRingMinWarps = 152;
+
 // Per-shape plan for the block-matrix form: a block covers 32 / v lanes (one
 // thread per column) and one chunk of Lc steps (4 sub-chunks of Lc / 4).
 scan_status plan_affine(int64_t B, int64_t T, int64_t N, int k, int v, const scan_opts& o,
@@ -147,6 +152,16 @@ scan_status plan_affine(int64_t B, int64_t T, int64_t N, int k, int v, const sca
   pl->Lc = Lc;
   pl->M = (int)M;
   pl->G = (int)G;
+  // 4 x 4 blocks of lane-rich shapes walk T with the state in registers,
+  // fed by a ring of tensor copies (no records, no replay); the rest run the
+  // look-back kernels. The workspace is sized for the look-back whatever the
+  // variant, so one size serves the coefficient prefix (look-back only) and
+  // every option of a shape.
+  const bool ring = affine_ring_fits(B, T, N, k, v);
+  if (o.variant == SCAN_VARIANT_STATIONARY && ring) pl->variant = VAR_STATIONARY;
+  else if (o.variant == SCAN_VARIANT_AUTO && ring && affine_ring_warps(B, N) >= kAffineRingMinWarps)
+    pl->variant = VAR_STATIONARY;
+  else pl->variant = VAR_LOOKBACK;
   pl->ws_bytes = kWsHeaderBytes + (size_t)(B * N * M) * (size_t)rec * sizeof(float);
   return SCAN_OK;
 }

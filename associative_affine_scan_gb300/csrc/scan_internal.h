@@ -174,6 +174,8 @@ struct TmaMaps {
 // point is missing or refuses the map.
 bool encode_tile_map(CUtensorMap* m, const void* ptr, int elt, int64_t n, int J);
 bool encode_rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int box_rows);
+bool encode_blocks_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t N,
+                       int box_steps);
 
 // Launchers (one translation unit per mode/dtype family).
 cudaError_t launch_scalar_fwd_f32(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
@@ -216,6 +218,7 @@ constexpr int AFF_EYE_H0 = 2;   // h0 = I (k = v); h0 pointer unused
 constexpr int AFF_ACC_DA = 4;   // backward adds into dA instead of writing it
 
 struct AffinePlan {
+  int variant;  // VAR_STATIONARY: the ring kernel (4 x 4 blocks); VAR_LOOKBACK otherwise
   int Lc;
   int M;
   int G;
@@ -237,6 +240,12 @@ cudaError_t launch_affine_generic_k4(const AffineParams& p, int mode, cudaStream
 cudaError_t launch_affine_generic_k8(const AffineParams& p, int mode, cudaStream_t s);
 cudaError_t launch_affine_generic_k16_fwd(const AffineParams& p, cudaStream_t s);
 cudaError_t launch_affine_generic_k16_bwd(const AffineParams& p, cudaStream_t s);
+
+// The 4 x 4 state-stationary kernels fed by a ring of tensor copies
+// (scan_affine_ring.cu): shapes they take, warps they launch, launcher.
+bool affine_ring_fits(int64_t B, int64_t T, int64_t N, int k, int v);
+int64_t affine_ring_warps(int64_t B, int64_t N);
+cudaError_t launch_affine_ring(const AffineParams& p, int mode, cudaStream_t s);
 
 cudaError_t launch_affine_fwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);
 cudaError_t launch_affine_bwd(const AffineParams& p, const AffinePlan& pl, cudaStream_t s);

@@ -66,4 +66,24 @@ bool encode_rows_map(CUtensorMap* m, const void* ptr, int64_t rows, int box_rows
   return r == CUDA_SUCCESS;
 }
 
+// A [B, T, N, 4, 4] fp32 tensor as {16 floats, N, T, B}: a box is 8 lanes x
+// box_steps steps of one batch row, written to shared memory with the 64-byte
+// swizzle (16-byte piece q of a 64-byte block lands at q ^ ((address >> 7) & 3)).
+bool encode_blocks_map(CUtensorMap* m, const void* ptr, int64_t B, int64_t T, int64_t N,
+                       int box_steps) {
+  std::call_once(g_encode_once, load_encoder);
+  if (!g_encode || !ptr || B < 1 || T < 1 || N < 1 || box_steps < 1 || box_steps > 256) return false;
+  if (reinterpret_cast<uintptr_t>(ptr) % 16) return false;
+  if (N > (1LL << 32) || T > (1LL << 32) || B > (1LL << 32)) return false;
+  const cuuint64_t dims[4] = {16, (cuuint64_t)N, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {64, (cuuint64_t)N * 64, (cuuint64_t)(N * T) * 64};
+  const cuuint32_t box[4] = {16, 8, (cuuint32_t)box_steps, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace scan

@@ -75,12 +75,26 @@ def run_and_check(lib, w, opts=None):
     return plain
 
 
-@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 200, 1000])
-@pytest.mark.parametrize("N", [1, 37, 70])
-def test_affine_4x4_shapes(lib, T, N):
+AFFINE_VARIANTS = {"planner": None, "stationary": {"variant": 1}, "lookback": {"variant": 2}}
+
+
+@pytest.mark.parametrize("T", [1, 5, 15, 16, 17, 63, 64, 65, 200, 1000])
+@pytest.mark.parametrize("N", [1, 7, 8, 9, 37, 70])
+@pytest.mark.parametrize("variant", list(AFFINE_VARIANTS))
+def test_affine_4x4_shapes(lib, T, N, variant):
+    """4 x 4 blocks under the planner and each variant: STATIONARY runs the
+    ring kernel where it applies (N >= 8, T >= 16: one warp per 8 lanes,
+    stage edges at 16-step multiples) and the look-back kernel elsewhere."""
     for h0 in (True, False):
         w = workloads.affine(2, T, N, 4, 4, seed=T * 100 + N, h0=h0)
-        run_and_check(lib, w)
+        run_and_check(lib, w, AFFINE_VARIANTS[variant])
+
+
+def test_affine_4x4_stationary_many_groups(lib):
+    """The ring kernel with several lane groups per batch row, a partial last
+    group (N = 203) and a ragged last stage (T = 1001)."""
+    w = workloads.affine(3, 1001, 203, 4, 4, seed=5, h0=True)
+    run_and_check(lib, w, {"variant": 1})
 
 
 @pytest.mark.parametrize("chunk", [64, 128, 256])
@@ -203,6 +217,23 @@ def test_affine_rejects_unsupported_and_misaligned(lib):
     with pytest.raises(lib.ScanError) as e:
         lib.affine_scan_fwd(A, torch.zeros(1, 4, 2, 4, 4, device=DEV))
     assert e.value.status == lib.SCAN_ERR_ALIGNMENT
+
+
+def test_affine_ring_wait_limit_reports_timeout(lib):
+    """The ring kernel's first warp waits at its second stage on an mbarrier
+    that nothing completes: the wait expires after 1 ms, the status reads
+    SCAN_ERR_TIMEOUT, and the next call runs normally."""
+    w = workloads.affine(1, 600, 32, 4, 4, seed=19, h0=True)
+    A, Bm, h0, dH = w.A.to(DEV), w.Bm.to(DEV), w.h0.to(DEV), w.dH.to(DEV)
+    lib.scan_get_device_status(DEV)
+    opts = {"variant": lib.SCAN_VARIANT_STATIONARY, "test_stall": 1, "wait_limit_s": 1e-3}
+    H = lib.affine_scan_fwd(A, Bm, h0, opts=opts)
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_ERR_TIMEOUT
+    lib.affine_scan_bwd(A, H, dH, h0, opts=opts)
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_ERR_TIMEOUT
+    H = lib.affine_scan_fwd(A, Bm, h0, opts={"variant": lib.SCAN_VARIANT_STATIONARY})
+    assert lib.scan_get_device_status(DEV) == lib.SCAN_OK
+    assert rel_err(H, oracle.affine_fwd(w.A, w.Bm, w.h0)) <= TOL
 
 
 def test_affine_wait_limit_reports_timeout(lib):

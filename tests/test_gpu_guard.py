@@ -29,6 +29,12 @@ DEV = torch.device("cuda", 0)
 PAD = 1024  # elements of sentinel on each side of every output
 SENTINEL = {torch.float32: (torch.int32, 0x7FC0DEAD), torch.bfloat16: (torch.int16, 0x7FA5)}
 TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
+# Outputs that are contractions of several fp32 results (the block form's dA
+# and dh0, the outer-product state's gradients): two look-back runs compose
+# earlier chunks in different orders, so two calls agree to their term scale,
+# not to 1e-5 of the result; they are held to the 1e-3 gradient gate here (the
+# parity tests check them against the oracle).
+CONTRACTIONS = {"dA", "dh0", "dalpha", "db", "dv", "dc"}
 
 
 class Guarded:
@@ -62,20 +68,22 @@ class Guarded:
         assert not bool(inside.any()), f"{name}: {int(inside.sum())} output words not written"
 
 
-def close(got, ref, name):
+def close(got, ref, name, contraction=False):
     g, r = got.double().to(DEV), ref.double().to(DEV)
     if g.numel() == 0:
         return
     err = float(((g - r).abs() / r.abs().clamp_min(1.0)).max())
-    assert err <= TOL[got.dtype], (name, err)
+    tol = 1e-3 if contraction else TOL[got.dtype]
+    assert err <= tol, (name, err)
 
 
-def check_all(pairs):
-    """pairs: (name, Guarded, reference tensor)."""
+def check_all(pairs, contractions=()):
+    """pairs: (name, Guarded, reference tensor); names in `contractions` are
+    compared at the gradient gate (see CONTRACTIONS)."""
     torch.cuda.synchronize()
     for name, gd, ref in pairs:
         gd.check(name)
-        close(gd.t, ref, name)
+        close(gd.t, ref, name, name in contractions)
 
 
 def variants(lib):
@@ -210,7 +218,7 @@ def run_affine(lib, w, opts=None):
     ref = lib.affine_scan_bwd(A, ref_H, dH, h0, opts=opts)
     outs = tuple(Guarded(t.shape) for t in ref)
     lib.affine_scan_bwd(A, ref_H, dH, h0, out=tuple(g.t for g in outs), opts=opts)
-    check_all([("H", H, ref_H)] + list(zip(("dA", "dB", "dh0"), outs, ref)))
+    check_all([("H", H, ref_H)] + list(zip(("dA", "dB", "dh0"), outs, ref)), CONTRACTIONS)
 
 
 @pytest.mark.parametrize("k", [1, 2, 4, 8, 16])
@@ -237,7 +245,7 @@ def test_guard_affine_prefix(lib, k):
     ref_dA = lib.affine_prefix_bwd(A, ref, dAbar)
     dA = Guarded(A.shape)
     lib.affine_prefix_bwd(A, ref, dAbar, dA.t)
-    check_all([("Abar", Abar, ref), ("dA", dA, ref_dA)])
+    check_all([("Abar", Abar, ref), ("dA", dA, ref_dA)], CONTRACTIONS)
 
 
 @pytest.mark.parametrize("S,D", [(16, 16), (16, 32), (32, 16), (32, 32)])
@@ -253,7 +261,7 @@ def test_guard_gdn(lib, S, D, T):
     outs = tuple(Guarded(t.shape) for t in ref)
     lib.gdn_bwd(alpha, b, v, c, ref_ck, dout, out=tuple(g.t for g in outs))
     check_all([("o", o, ref_o), ("checkpoints", ck, ref_ck[:n_ck])] +
-              list(zip(("dalpha", "db", "dv", "dc", "dh0"), outs, ref)))
+              list(zip(("dalpha", "db", "dv", "dc", "dh0"), outs, ref)), CONTRACTIONS)
 
 
 @pytest.mark.parametrize("T,pieces", [(1000, 3), (1001, 4), (3, 2)])

@@ -798,90 +798,6 @@ __host__ __device__ constexpr bool uses_ahead() {
   return MODE == MODE_FWD && VARLEN && sizeof(TA) == 2;
 }
 
-// The register-carry loop's loads D - 1 chunks ahead through shared memory:
-// each lane copies the aligned in-row 4-step groups of its run of a later
-// chunk (gates and inputs forward, gates and dh backward) into slots of its
-// own with asynchronous copies (8 or 16 bytes, one commit group per chunk)
-// and reads them back when that chunk is scanned. Nothing in flight is held
-// in registers, so each row-warp keeps D - 1 chunks of loads outstanding for
-// D x 32 x J x (a + x group bytes) of shared memory. The backward's gate halo
-// (the gate next to the chunk in scan order) is the edge gate of the chunk
-// scanned just before, carried in a register instead of loaded. Used by the
-// packed bf16 backward, whose 4096 row-warps all sit in one wave with one
-// chunk of loads in flight each and no registers to spare for a register
-// look-ahead (3.318 -> 3.263 ms on the 64-sequence workload). The forward
-// keeps its register look-ahead: with the ring it measured 1.837 -> 1.939 ms
-// (it issues about 37 instructions per lane-step, and the copies and
-// shared-memory reads add to them).
-template <int MODE, bool VARLEN, typename TA, int VARIANT>
-__host__ __device__ constexpr bool uses_staged() {
-  return VARIANT == VAR_STATIONARY && VARLEN && sizeof(TA) == 2 && MODE == MODE_BWD;
-}
-
-template <int J, typename TA, int MODE>
-struct Staged {
-  using XT = typename std::conditional<MODE != MODE_FWD, float, TA>::type;
-  static constexpr int D = MODE == MODE_FWD ? 4 : 3;  // chunks in the ring
-  static constexpr int EA = 4 * (int)sizeof(TA);     // bytes of a 4-step group of a
-  static constexpr int EX = 4 * (int)sizeof(XT);     // of x (forward) or dh (backward)
-  static constexpr int SLOT = 32 * J * (EA + EX);
-  static constexpr int BYTES = D * SLOT;             // per warp
-  unsigned char* base;  // this warp's slots (shared memory)
-  float gate_carry;     // backward: edge gate of the chunk scanned last
-  __device__ __forceinline__ unsigned char* a_at(int kk, int i, int lane) const {
-    return base + (kk % D) * SLOT + (i * 32 + lane) * EA;
-  }
-  __device__ __forceinline__ unsigned char* x_at(int kk, int i, int lane) const {
-    return base + (kk % D) * SLOT + 32 * J * EA + (i * 32 + lane) * EX;
-  }
-};
-
-template <int N>
-__device__ __forceinline__ void cp_async(void* dst, const void* src) {
-  if constexpr (N == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-                 : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "n"(N)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Copies for chunk kk (in scan order; nothing past the row's last chunk) into
-// its slot, as one commit group.
-template <int MODE, int J, typename TA, int S>
-__device__ __forceinline__ void stage_chunk(const ScalarParams& p, const BranchArgs& br,
-                                            const Staged<J, TA, MODE>& st, int64_t roff,
-                                            int shift, int kk, int lane) {
-  using XT = typename Staged<J, TA, MODE>::XT;
-  constexpr int L = 128 * J, V = 4 * J;
-  if (kk < p.M) {
-    const int m = (S > 0) ? kk : (p.M - 1 - kk);
-    const int64_t t0 = (int64_t)m * L - shift;
-    const int64_t tr = t0 + (int64_t)V * lane;
-    const bool inside = t0 >= 0 && t0 + L <= p.T;  // warp-uniform
-    const TA* a = static_cast<const TA*>(br.a) + roff;
-    const XT* x = (MODE != MODE_FWD ? static_cast<const XT*>(static_cast<const void*>(br.dh))
-                                    : static_cast<const XT*>(br.x)) + roff;
-#pragma unroll
-    for (int i = 0; i < J; ++i) {
-      const int64_t t = tr + 4 * i;
-      if (inside || (t >= 0 && t + 4 <= p.T)) {
-        cp_async<Staged<J, TA, MODE>::EA>(st.a_at(kk, i, lane), a + t);
-        cp_async<Staged<J, TA, MODE>::EX>(st.x_at(kk, i, lane), x + t);
-      }
-    }
-  }
-  cp_async_commit();
-}
-
 // INSIDE: every 4-step group of every lane lies inside the row (vector path,
 // not the stream variant's tiles); the per-group bounds checks fold away, and
 // packed rows test once per chunk whether any sequence starts or ends in it.
@@ -891,8 +807,7 @@ __device__ __forceinline__ void chunk_body(const ScalarParams& p, int brn, int64
                                            bool stationary, uint32_t epoch, unsigned ticket,
                                            const SegWin& win, float& carry, const StageView* sv,
                                            int* seg_hint, const Release& release,
-                                           RunAhead<J, TA, MODE>* ahead, bool next,
-                                           Staged<J, TA, MODE>* staged) {
+                                           RunAhead<J, TA, MODE>* ahead, bool next) {
   using E = typename Op::E;
   constexpr int L = 128 * J;
   constexpr int V = 4 * J;
@@ -918,12 +833,6 @@ __device__ __forceinline__ void chunk_body(const ScalarParams& p, int brn, int64
   const TA* a = static_cast<const TA*>(br.a) + roff;
   const void* xsrc = BWD ? static_cast<const void*>(br.dh) : br.x;
   using XT = typename RunAhead<J, TA, MODE>::XT;  // element type of xsrc
-  if (VEC && staged) {
-    // the copies of the chunk D - 1 ahead go to the slot of the one scanned
-    // last (its loads are in registers); then this chunk's copies are done
-    stage_chunk<MODE, J, TA, S>(p, br, *staged, roff, shift, k + Staged<J, TA, MODE>::D - 1, lane);
-    cp_async_wait<Staged<J, TA, MODE>::D - 1>();
-  }
 #pragma unroll
   for (int i = 0; i < J; ++i) {
     const int64_t t = tr + 4 * i;
@@ -931,11 +840,7 @@ __device__ __forceinline__ void chunk_body(const ScalarParams& p, int brn, int64
     float* xi = X + 4 * i;
     float* hi = H + (BWD ? 4 * i : 0);
     const bool g_in = INSIDE || (t >= 0 && t + 4 <= T);  // the group lies in the row
-    if (!SMEM && VEC && staged && g_in) {
-      IO<TA>::unpack(*reinterpret_cast<const typename IO<TA>::Raw*>(staged->a_at(k, i, lane)), ai);
-      IO<XT>::unpack(*reinterpret_cast<const typename IO<XT>::Raw*>(staged->x_at(k, i, lane)), xi);
-      if (BWD) IO<float>::ld4(br.h + roff + t, hi);
-    } else if (SMEM && t + 4 <= sv->c_hi) {
+    if (SMEM && t + 4 <= sv->c_hi) {
       const uint32_t o = (uint32_t)(t - sv->e0);
       TIO<TA>::ld4(sv->in[0], o, ai);
       if (BWD) {
@@ -1025,9 +930,7 @@ __device__ __forceinline__ void chunk_body(const ScalarParams& p, int brn, int64
     if (lane == 0) {
       const int64_t pa = (S < 0) ? t0 + L : t0 - 1;
       const int64_t ph = (S < 0) ? t0 - 1 : t0 + L;
-      if (VEC && staged) {
-        halo_a = staged->gate_carry;
-      } else if (had) {
+      if (had) {
         halo_a = LOGIN ? __expf(had_ha) : had_ha;
       } else if (pa >= 0 && pa < T) {
         halo_a = LOGIN ? __expf(IO<TA>::ld1(a + pa)) : IO<TA>::ld1(a + pa);
@@ -1035,11 +938,6 @@ __device__ __forceinline__ void chunk_body(const ScalarParams& p, int brn, int64
       if (ph >= 0 && ph < T) halo_h = IO<float>::ld1(br.h + roff + ph);  // used after the scan
     }
     halo_a = __shfl_sync(kFull, halo_a, 0);
-    // the next chunk in scan order sits just below (S < 0: its halo is this
-    // chunk's first gate, lane 0's) or just above (S > 0: this chunk's last
-    // gate, lane 31's); 0 outside the row, as loaded
-    if (VEC && staged)
-      staged->gate_carry = (S < 0) ? __shfl_sync(kFull, A[0], 0) : __shfl_sync(kFull, A[V - 1], 31);
     const float an = (S < 0) ? __shfl_down_sync(kFull, A[0], 1) : __shfl_up_sync(kFull, A[V - 1], 1);
     a_nb = lane == ((S < 0) ? 31 : 0) ? halo_a : an;
   }
@@ -1247,8 +1145,7 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
                                       const SegWin& win, float& carry,
                                       const StageView* sv = nullptr, int* seg_hint = nullptr,
                                       const Release& release = Release(),
-                                      RunAhead<J, TA, MODE>* ahead = nullptr, bool next = false,
-                                      Staged<J, TA, MODE>* staged = nullptr) {
+                                      RunAhead<J, TA, MODE>* ahead = nullptr, bool next = false) {
   if constexpr (!VARLEN && !SMEM && MODE != MODE_LOGBWD && std::is_same<Op, LinOp>::value &&
                 sizeof(TA) == 4) {
     chunk_groups<Op, MODE, VEC, J, TA, S>(p, brn, row, k, stationary, epoch, ticket, carry);
@@ -1266,14 +1163,12 @@ __device__ __forceinline__ void chunk(const ScalarParams& p, int brn, int64_t ro
     const int64_t t0 = (int64_t)m * (128 * J) - (int)((row * p.T) & 3);
     if (t0 >= 0 && t0 + 128 * J <= p.T) {
       chunk_body<Op, MODE, VARLEN, VEC, J, TA, S, SMEM, Release, true>(
-          p, brn, row, k, stationary, epoch, ticket, win, carry, sv, seg_hint, release, ahead, next,
-          staged);
+          p, brn, row, k, stationary, epoch, ticket, win, carry, sv, seg_hint, release, ahead, next);
       return;
     }
   }
   chunk_body<Op, MODE, VARLEN, VEC, J, TA, S, SMEM, Release, false>(
-      p, brn, row, k, stationary, epoch, ticket, win, carry, sv, seg_hint, release, ahead, next,
-      staged);
+      p, brn, row, k, stationary, epoch, ticket, win, carry, sv, seg_hint, release, ahead, next);
 }
 
 // ---------------------------------------------------------------------------
@@ -1617,33 +1512,17 @@ __device__ __forceinline__ void scalar_scan_body(const ScalarParams& p) {
     float carry = (MODE == MODE_FWD) ? Op::initial_carry() : 0.f;
     const int S = (MODE == MODE_FWD) ? p.br[brn].dir : -p.br[brn].dir;
     int hint = -1;
-    constexpr bool kStaged = uses_staged<MODE, VARLEN, TA, VARIANT>();
     RunAhead<J, TA, MODE> ahead;
     ahead.full = false;
-    RunAhead<J, TA, MODE>* ap = (uses_ahead<MODE, VARLEN, TA>() && !kStaged) ? &ahead : nullptr;
-    Staged<J, TA, MODE> staged;
-    Staged<J, TA, MODE>* sp = nullptr;
-    if (kStaged && VEC && row < p.rows) {
-      // this warp's slots follow the staged offsets in dynamic shared memory
-      const size_t cu_bytes = VARLEN && p.n_seqs + 1 <= kCuSmem ? 4 * (size_t)(p.n_seqs + 1) : 0;
-      staged.base = smem + round_up(cu_bytes, 16) + (size_t)warp * Staged<J, TA, MODE>::BYTES;
-      staged.gate_carry = 0.f;
-      sp = &staged;
-      const int shift = (int)((row * p.T) & 3);
-      const int64_t roff = row * p.T;
-      for (int kk = 0; kk < Staged<J, TA, MODE>::D - 1; ++kk) {
-        if (S > 0) stage_chunk<MODE, J, TA, 1>(p, p.br[brn], staged, roff, shift, kk, lane);
-        else stage_chunk<MODE, J, TA, -1>(p, p.br[brn], staged, roff, shift, kk, lane);
-      }
-    }
+    RunAhead<J, TA, MODE>* ap = uses_ahead<MODE, VARLEN, TA>() ? &ahead : nullptr;
     for (int k = 0; k < p.M; ++k) {
       const bool next = k + 1 < p.M;
       if (S > 0)
         chunk<Op, MODE, VARLEN, VEC, J, TA, 1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
-                                               &hint, NoRelease(), ap, next, sp);
+                                               &hint, NoRelease(), ap, next);
       else
         chunk<Op, MODE, VARLEN, VEC, J, TA, -1>(p, brn, row, k, true, 0u, 0u, win, carry, nullptr,
-                                                &hint, NoRelease(), ap, next, sp);
+                                                &hint, NoRelease(), ap, next);
     }
     if (p.nbr == 2) {
       __syncthreads();
@@ -1784,9 +1663,7 @@ cudaError_t launch_one(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t
     else
       return scalar_scan_kernel<Op, MODE, VARLEN, VEC, J, TA, VARIANT>;
   }();
-  size_t smem = pl.smem;
-  if constexpr (uses_staged<MODE, VARLEN, TA, VARIANT>())
-    if (VEC) smem = round_up(smem, 16) + (size_t)p.R * Staged<J, TA, MODE>::BYTES;
+  const size_t smem = pl.smem;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);

@@ -13,8 +13,10 @@
 // chunk (256 steps; each lane owns a run of 8 consecutive steps, loaded as two
 // aligned 4-step groups). Per chunk: compose each lane's run map (P, Q), one
 // warp-shuffle scan of the 32 run maps, the recurrence over the run from its
-// carry-in, vector stores. The next chunk's loads are issued before the
-// current one is scanned.
+// carry-in, vector stores. Forward: each lane copies its runs of the next
+// chunks into a per-warp ring in shared memory (cp.async, 3 or 4 chunks deep)
+// before it scans the current one; backward: the next chunk's gates and dh
+// are loaded into registers before the current one is scanned.
 //
 // A warp-uniform cursor into cu_seqlens tells whether any sequence boundary
 // touches the chunk (a sequence starting in it or right after it) or the
@@ -87,10 +89,70 @@ __device__ __forceinline__ void warp_scan(LinOp::E run, int lane, LinOp::E& ex, 
   tot = LinOp::shfl(inc, (S > 0) ? 31 : 0);
 }
 
-template <typename TA>
-struct Ahead {
-  typename IO<TA>::Raw u[2], w[2];  // the next chunk's two tensors, raw
+// Asynchronous 8- or 16-byte copies from global to shared memory, one commit
+// group per chunk.
+template <int N>
+__device__ __forceinline__ void cp_async(void* dst, const void* src) {
+  if constexpr (N == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "n"(N)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A warp's ring of D chunk slots in shared memory: each lane copies its run's
+// two 4-step groups of both tensors into its own entries (U: gates, W: x or
+// dh), D - 1 chunks ahead of the one it scans, and reads them back when that
+// chunk comes (no registers held for loads in flight). Chunks that reach out
+// of the row are loaded directly instead (their slot stays unused).
+template <typename TU, typename TW>
+struct Ring {
+  static constexpr int EU = 4 * (int)sizeof(TU), EW = 4 * (int)sizeof(TW);  // bytes per group
+  static constexpr int SLOT = 32 * 2 * (EU + EW);
+  static constexpr int D = SLOT <= 1536 ? 4 : 3;  // chunks in the ring
+  static constexpr int BYTES = D * SLOT;          // per warp
+  unsigned char* base;
+  __device__ __forceinline__ unsigned char* u(int k, int i, int lane) const {
+    return base + (k % D) * SLOT + (i * 32 + lane) * EU;
+  }
+  __device__ __forceinline__ unsigned char* w(int k, int i, int lane) const {
+    return base + (k % D) * SLOT + 64 * EU + (i * 32 + lane) * EW;
+  }
+  // copies of chunk k (when it lies inside the row; tr its lane's run start)
+  __device__ __forceinline__ void issue(int k, bool inside, int64_t tr, const TU* u0,
+                                        const TW* w0, int lane) const {
+    if (inside) {
+      cp_async<EU>(u(k, 0, lane), u0 + tr);
+      cp_async<EU>(u(k, 1, lane), u0 + tr + 4);
+      cp_async<EW>(w(k, 0, lane), w0 + tr);
+      cp_async<EW>(w(k, 1, lane), w0 + tr + 4);
+    }
+    cp_async_commit();
+  }
+  __device__ __forceinline__ void read(int k, int lane, float (&U)[8], float (&W)[8]) const {
+    IO<TU>::unpack(*reinterpret_cast<const typename IO<TU>::Raw*>(u(k, 0, lane)), U);
+    IO<TU>::unpack(*reinterpret_cast<const typename IO<TU>::Raw*>(u(k, 1, lane)), U + 4);
+    IO<TW>::unpack(*reinterpret_cast<const typename IO<TW>::Raw*>(w(k, 0, lane)), W);
+    IO<TW>::unpack(*reinterpret_cast<const typename IO<TW>::Raw*>(w(k, 1, lane)), W + 4);
+  }
 };
+
+template <typename TA>
+using PackedRing = Ring<TA, TA>;  // forward: gates and x
+
+template <typename TA, int MODE>
+constexpr size_t ring_bytes() {
+  return MODE == MODE_FWD ? (size_t)PackedRing<TA>::BYTES : 0;
+}
 
 // ---------------------------------------------------------------------------
 // forward: h_t = a_t h_{t-S} + x_t, scanned in direction S
@@ -98,46 +160,36 @@ struct Ahead {
 
 template <typename TA, int S>
 __device__ void packed_fwd_row(const ScalarParams& p, const BranchArgs& br, int64_t row,
-                               const SegWin& win, int lane) {
+                               const SegWin& win, int lane, unsigned char* ring_base) {
   const int64_t T = p.T, roff = row * T;
   const int shift = (int)(roff & 3);  // 4-step groups on 4-element boundaries of memory
   const TA* a = static_cast<const TA*>(br.a) + roff;
   const TA* x = static_cast<const TA*>(br.x) + roff;
   float* h = br.out_h + roff;
   const int M = p.M;
+  using R = PackedRing<TA>;
+  const R ring{ring_base};
   auto t0_of = [&](int k) { return (int64_t)((S > 0) ? k : (M - 1 - k)) * kPL - shift; };
   auto inside_at = [&](int64_t t) { return t >= 0 && t + kPL <= T; };
-  Ahead<TA> ah;
-  int64_t t0 = t0_of(0);
-  bool ins = inside_at(t0);
-  if (ins) {
-    const int64_t tr = t0 + kPV * lane;
-    ah.u[0] = IO<TA>::ldraw(a + tr), ah.u[1] = IO<TA>::ldraw(a + tr + 4);
-    ah.w[0] = IO<TA>::ldraw(x + tr), ah.w[1] = IO<TA>::ldraw(x + tr + 4);
-  }
+  auto issue = [&](int k) {
+    const int64_t t0k = k < M ? t0_of(k) : -1;
+    ring.issue(k, k < M && inside_at(t0k), t0k + kPV * lane, a, x, lane);
+  };
+  for (int k = 0; k < R::D - 1; ++k) issue(k);
   float carry = 0.f;
   int cur = (S > 0) ? 0 : win.n;
   for (int k = 0; k < M; ++k) {
+    const int64_t t0 = t0_of(k);
+    const bool ins = inside_at(t0);
     const int64_t tr = t0 + kPV * lane;
+    issue(k + R::D - 1);  // into the slot of chunk k - 1, already read
+    cp_async_wait<R::D - 1>();
     float A[kPV], X[kPV];
     if (ins) {
-      IO<TA>::unpack(ah.u[0], A), IO<TA>::unpack(ah.u[1], A + 4);
-      IO<TA>::unpack(ah.w[0], X), IO<TA>::unpack(ah.w[1], X + 4);
+      ring.read(k, lane, A, X);
     } else {
       load_run(a, tr, T, false, A);
       load_run(x, tr, T, false, X);
-    }
-    // the next chunk's loads, before this one is scanned
-    int64_t t0n = 0;
-    bool insn = false;
-    if (k + 1 < M) {
-      t0n = t0_of(k + 1);
-      insn = inside_at(t0n);
-      if (insn) {
-        const int64_t trn = t0n + kPV * lane;
-        ah.u[0] = IO<TA>::ldraw(a + trn), ah.u[1] = IO<TA>::ldraw(a + trn + 4);
-        ah.w[0] = IO<TA>::ldraw(x + trn), ah.w[1] = IO<TA>::ldraw(x + trn + 4);
-      }
     }
     // boundaries: a sequence starting in [t0, t0 + L] or a chunk reaching out of the row
     cur = cursor_at(win, cur, t0);
@@ -178,8 +230,6 @@ __device__ void packed_fwd_row(const ScalarParams& p, const BranchArgs& br, int6
       X[e] = st;
     }
     store_run(h, tr, T, ins, X);
-    t0 = t0n;
-    ins = insn;
   }
 }
 
@@ -193,6 +243,9 @@ template <typename TA, int D>
 __device__ void packed_bwd_row(const ScalarParams& p, const BranchArgs& br, int64_t row,
                                const SegWin& win, int lane) {
   constexpr int S = -D;
+  // (the next chunk's gates and dh are held in registers: a shared-memory
+  // ring here, 3 or 4 chunks deep with or without the states h, measured
+  // slower, 2.69 -> 2.85 / 3.67 ms on the 64-sequence rows)
   const int64_t T = p.T, roff = row * T;
   const int shift = (int)(roff & 3);
   const TA* a = static_cast<const TA*>(br.a) + roff;
@@ -336,6 +389,12 @@ __device__ void packed_bwd_row(const ScalarParams& p, const BranchArgs& br, int6
 // One warp per (branch, row). Two-branch launches take their row group from a
 // per-branch ticket chosen by the parity of the block's SM pair, as the
 // register-carry kernels do, so an SM pair mostly runs one scan direction.
+// Bytes of the packed offsets staged at the start of dynamic shared memory,
+// rounded up to 16 (the rings follow).
+__host__ __device__ __forceinline__ size_t cu_smem_bytes(const ScalarParams& p) {
+  return round_up(p.n_seqs + 1 <= kCuSmem ? 4 * (size_t)(p.n_seqs + 1) : 0, 16);
+}
+
 // At most 72 registers: 28 row-warps per SM, so the 4096 row-warps of the
 // packed bidirectional workload (2 x 2048 rows) are all resident in one wave;
 // a second wave would double the walk.
@@ -366,9 +425,11 @@ __global__ void __maxnreg__(72) packed_kernel(const __grid_constant__ ScalarPara
   const int64_t row = (int64_t)g * p.R + warp;
   if (row < p.rows) {
     const BranchArgs& br = p.br[brn];
+    // this warp's ring follows the staged offsets in dynamic shared memory
+    unsigned char* ring = smem + cu_smem_bytes(p) + (size_t)warp * ring_bytes<TA, MODE>();
     if (MODE == MODE_FWD) {
-      if (br.dir > 0) packed_fwd_row<TA, 1>(p, br, row, win, lane);
-      else packed_fwd_row<TA, -1>(p, br, row, win, lane);
+      if (br.dir > 0) packed_fwd_row<TA, 1>(p, br, row, win, lane, ring);
+      else packed_fwd_row<TA, -1>(p, br, row, win, lane, ring);
     } else {
       if (br.dir > 0) packed_bwd_row<TA, 1>(p, br, row, win, lane);
       else packed_bwd_row<TA, -1>(p, br, row, win, lane);
@@ -393,7 +454,13 @@ cudaError_t launch_packed_t(const ScalarParams& p, const ScalarPlan& pl, cudaStr
   auto kern = packed_kernel<TA, MODE>;
   const int64_t grid = (int64_t)p.G * p.nbr;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, 32 * p.R, pl.smem, s>>>(p);
+  const size_t smem = cu_smem_bytes(p) + (size_t)p.R * ring_bytes<TA, MODE>();
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)grid, 32 * p.R, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -401,7 +468,7 @@ cudaError_t launch_packed_t(const ScalarParams& p, const ScalarPlan& pl, cudaStr
 
 bool packed_applies(const ScalarParams& p, const ScalarPlan& pl) {
   return p.cu != nullptr && pl.vec && pl.variant == VAR_STATIONARY && p.nseg == 1 && pl.J == 2 &&
-         pl.smem <= 48 * 1024;
+         p.R <= 8;
 }
 
 cudaError_t launch_packed(const ScalarParams& p, const ScalarPlan& pl, int mode, int elt,

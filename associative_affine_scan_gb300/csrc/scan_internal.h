@@ -185,10 +185,11 @@ cudaError_t launch_scalar_bwd_bf16(const ScalarParams& p, const ScalarPlan& pl, 
 cudaError_t launch_log_fwd(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
 cudaError_t launch_log_bwd(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s);
 
-// Packed rows of the linear form (cu_seqlens), stationary, vectorised, chunks
-// of 256 steps: the dedicated kernels of scan_packed.cu (mode MODE_FWD or
-// MODE_BWD, elt = element size of a and x).
-bool packed_applies(const ScalarParams& p, const ScalarPlan& pl);
+// Packed rows of the linear form (cu_seqlens), and dense bf16 rows of its
+// backward, stationary, vectorised, chunks of 256 steps: the dedicated
+// kernels of scan_packed.cu (mode MODE_FWD or MODE_BWD, elt = element size of
+// a and x).
+bool packed_applies(const ScalarParams& p, const ScalarPlan& pl, int mode, int elt);
 cudaError_t launch_packed(const ScalarParams& p, const ScalarPlan& pl, int mode, int elt,
                           cudaStream_t s);
 

@@ -1765,7 +1765,8 @@ cudaError_t launch_layouts(const ScalarParams& p, const ScalarPlan& pl, cudaStre
 template <class Op, int MODE, typename TA>
 cudaError_t launch_scalar(const ScalarParams& p, const ScalarPlan& pl, cudaStream_t s) {
   if constexpr (std::is_same<Op, LinOp>::value && (MODE == MODE_FWD || MODE == MODE_BWD))
-    if (packed_applies(p, pl)) return launch_packed(p, pl, MODE, (int)sizeof(TA), s);
+    if (packed_applies(p, pl, MODE, (int)sizeof(TA)))
+      return launch_packed(p, pl, MODE, (int)sizeof(TA), s);
   switch (pl.variant) {
     case VAR_LOOKBACK: return launch_layouts<Op, MODE, TA, VAR_LOOKBACK>(p, pl, s);
     case VAR_STREAM: return launch_layouts<Op, MODE, TA, VAR_STREAM>(p, pl, s);

@@ -73,6 +73,16 @@ def test_gdn_shapes(lib, S, D, T):
         check(lib, w)
 
 
+@pytest.mark.parametrize("S,D", [(16, 16), (16, 32), (32, 16), (32, 32)])
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 31, 32, 33, 100])
+def test_gdn_many_heads(lib, S, D, T):
+    """160 heads (more than one per SM) at ragged T around the 16- and 32-step
+    edges, with and without h0."""
+    for h0 in (True, False):
+        w = workloads.gdn(8, 20, T, S, D, seed=T * 13 + S + D + h0, h0=h0)
+        check(lib, w)
+
+
 def test_gdn_with_one_by_one_state_matches_the_scalar_scan(lib):
     """Identity through the reduction: with b_t = e_0, c_t = e_0 and v_t = x_t e_0,
     o_t[0] is the scalar scan h_t = alpha_t h_{t-1} + x_t."""

@@ -250,11 +250,13 @@ def test_guard_affine_prefix(lib, k):
 
 @pytest.mark.parametrize("S,D", [(16, 16), (16, 32), (32, 16), (32, 32)])
 @pytest.mark.parametrize("T", [1, 31, 32, 33, 63, 64, 65, 97])
-def test_guard_gdn(lib, S, D, T):
-    w = workloads.gdn(2, 3, T, S, D, seed=T + S + D, h0=True)
+@pytest.mark.parametrize("heads", [(2, 3), (8, 20)])
+def test_guard_gdn(lib, S, D, T, heads):
+    B, H = heads
+    w = workloads.gdn(B, H, T, S, D, seed=T + S + D, h0=True)
     alpha, b, v, c, dout, h0 = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout, w.h0))
     ref_o, ref_ck = lib.gdn_fwd(alpha, b, v, c, h0)
-    n_ck = lib.gdn_checkpoint_bytes(2, 3, T, S, D) // 4
+    n_ck = lib.gdn_checkpoint_bytes(B, H, T, S, D) // 4
     o, ck = Guarded(ref_o.shape), Guarded((n_ck,))
     lib.gdn_fwd(alpha, b, v, c, h0, checkpoints=ck.t, out=o.t)
     ref = lib.gdn_bwd(alpha, b, v, c, ref_ck, dout)

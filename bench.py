@@ -49,7 +49,7 @@ PAGES_FWD_BWD_MS = {"dense_4k": 0.602, "dense_64k": 9.212}
 # build that kernel and choose its launch shape at the time of the capture.
 # When the sources differ from the digest the figure no longer describes the
 # kernel that runs, and the line reports traffic as null.
-BWD_TRAFFIC = {"dense_4k": {"bytes": None, "digest": None}}
+BWD_TRAFFIC = {"dense_4k": {"bytes": 961830912, "digest": "4caca3090d8f5eda"}}
 KERNEL_SOURCES = ("scan_scalar.cuh", "scan_internal.h", "scan_scalar_bwd_f32.cu", "scan_api.cu")
 L2_FLUSH_BYTES = 256 << 20
 COPY_BYTES = 1 << 30  # per direction, for the copy-ceiling kernels

@@ -8,6 +8,7 @@ depends on cu_seqlens and reset indexing.
 """
 
 import json
+import math
 import os
 
 import numpy as np
@@ -437,6 +438,32 @@ def test_log_dense(lib, T, reverse):
             h = lib.scan_log_fwd(ga, gx, gh0, None, reverse, opts=opts)
             torch.cuda.synchronize()
             ref = oracle.scan_log_fwd(w.log_a, w.log_x, h0, None, reverse)
+            assert rel_err(h, ref) <= TOL32
+
+
+@pytest.mark.parametrize("reverse", [False, True])
+def test_log_dense_infinities_and_wide_range(lib, reverse):
+    """Dense rows whose runs hold log a = -inf (resets), log x = -inf (zero
+    inputs), whole stretches with no mass at all, and log x over +-20 (terms
+    that differ by up to e^40 inside one run)."""
+    g = torch.Generator().manual_seed(77)
+    B, C, T = 2, 5, 2048 + 37
+    la = torch.nn.functional.logsigmoid(torch.randn((B, C, T), generator=g))
+    lx = (8.0 * torch.randn((B, C, T), generator=g)).clamp(-20.0, 20.0)
+    la[torch.rand((B, C, T), generator=g) < 0.02] = -math.inf
+    lx[torch.rand((B, C, T), generator=g) < 0.05] = -math.inf
+    la[:, 1, 300:700] = -math.inf  # every run here: no carried mass
+    lx[:, 1, 300:700] = -math.inf  # and none added
+    lx[:, 2, :600] = -math.inf     # rows that start empty
+    lh0 = torch.randn((B, C), generator=g)
+    lh0[0, 2] = -math.inf
+    for _, opts in variants(lib):
+        for h0 in (lh0, None):
+            ga, gx, gh0 = cuda(la, lx, h0)
+            h = lib.scan_log_fwd(ga, gx, gh0, None, reverse, opts=opts)
+            torch.cuda.synchronize()
+            ref = oracle.scan_log_fwd(la, lx, h0, None, reverse)
+            assert torch.isfinite(h).all()
             assert rel_err(h, ref) <= TOL32
 
 

@@ -54,6 +54,7 @@ from ._binding import (  # noqa: F401
     scan_copy,
     scan_fwd,
     scan_fwd_noalloc,
+    scan_noalloc_device_status,
     scan_step_host,
     scan_get_device_status,
     scan_log_fwd,

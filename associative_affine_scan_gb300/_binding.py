@@ -54,7 +54,7 @@ EXPORTED = (
     "scan_get_device_status", "scan_fwd", "scan_bwd", "scan_bidir_fwd", "scan_bidir_bwd",
     "scan_log_fwd", "scan_log_bwd", "affine_scan_fwd", "affine_scan_bwd", "affine_prefix_fwd",
     "affine_prefix_bwd", "gdn_checkpoint_bytes", "gdn_fwd", "gdn_workspace_bytes", "gdn_bwd",
-    "scan_fwd_noalloc", "scan_step_host", "scan_copy",
+    "scan_fwd_noalloc", "scan_noalloc_device_status", "scan_step_host", "scan_copy",
 )
 
 
@@ -129,6 +129,7 @@ _SIGS = {
                           ctypes.c_int),
     "scan_fwd_noalloc": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, ctypes.c_int, _i32,
                           _vp], ctypes.c_int),
+    "scan_noalloc_device_status": ([_vp], ctypes.c_int),
     "scan_copy": ([_vp, _vp, _sz, _i32, _vp, _vp], ctypes.c_int),
 }
 
@@ -730,6 +731,13 @@ def scan_fwd_noalloc(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None,
                                 dt, int(bool(reverse)), _stream(stream, dev))
     _check(st, "scan_fwd_noalloc")
     return h
+
+
+def scan_noalloc_device_status(device=None, stream=None) -> int:
+    """Sticky device status of scan_fwd_noalloc's scratch on `device` (after
+    synchronising `stream`); resets it. Allocates nothing."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return int(_call(device, "scan_noalloc_device_status", _stream(stream, device)))
 
 
 def scan_copy(src, dst, mode=SCAN_COPY_VEC, *, status=None, stream=None):

@@ -145,3 +145,10 @@ extern "C" scan_status scan_fwd_noalloc(const void* a, const void* x, const floa
                                        : launch_scalar_fwd_bf16(p, pl, stream);
   return e == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
 }
+
+extern "C" scan_status scan_noalloc_device_status(cudaStream_t stream) {
+  void* scratch = nullptr;
+  const scan_status st = scratch_on_current_device(&scratch);
+  if (st != SCAN_OK) return st;
+  return scan_get_device_status(scratch, stream);
+}

@@ -429,13 +429,23 @@ scan_status scan_copy(const void* src, void* dst, size_t bytes, int32_t mode, ui
  *     overlap on the GPU (different streams, or threads) race on it and give
  *     undefined results: serialise them.
  *   - Device-side findings (a malformed cu_seqlens, an expired wait) are kept
- *     in that scratch and cannot be read back; host-side checks return their
- *     status as usual. Never calls cudaMalloc, cudaFree or any allocating
- *     routine. */
+ *     in that scratch; scan_noalloc_device_status reads them back. Host-side
+ *     checks return their status as usual. Never calls cudaMalloc, cudaFree
+ *     or any allocating routine. */
 scan_status scan_fwd_noalloc(const void* a, const void* x, const float* h0,
                              const int32_t* cu_seqlens, int32_t n_seqs, float* h,
                              int64_t B, int64_t C, int64_t T, scan_dtype dt,
                              int32_t reverse, cudaStream_t stream);
+
+/* The sticky device status of the current device's scan_fwd_noalloc scratch,
+ * read and cleared: scan_get_device_status (synchronises `stream`, reads the
+ * status word, resets it to 0) applied to the library's own scratch, which
+ * the caller has no pointer to. Returns SCAN_OK, the finding of a call since
+ * the last read (SCAN_ERR_TIMEOUT for an expired look-back wait,
+ * SCAN_ERR_SEQLENS for a malformed device cu_seqlens), or SCAN_ERR_CUDA
+ * when the synchronisation or copies fail. Like scan_fwd_noalloc, it
+ * allocates nothing; the copies are synchronous. */
+scan_status scan_noalloc_device_status(cudaStream_t stream);
 
 #ifdef __cplusplus
 }

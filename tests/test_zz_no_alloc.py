@@ -8,8 +8,8 @@ in a row, because every call reuses the library's fixed scratch array. The
 cases cover short rows (T <= 256: one- and two-block chunks), row counts that
 leave a partial group of 4 rows, no initial state, fp32 and bf16 packed rows,
 more sequences than the shared-memory offset table holds (4096 entries), the
-first call of the file made on a side stream, and guard bands around the
-output. This file is collected last so that a run stopping at the first
+first call of the file made on a side stream, guard bands around the output,
+and the read-back of a finding of the kernel's own checks. This file is collected last so that a run stopping at the first
 failure has run every other test first; it also passes alone in a fresh
 process.
 """
@@ -135,6 +135,28 @@ def test_noalloc_guard_bands(lib, shift):
             torch.cuda.synchronize()
             assert bool((bits[:lo] == SENTINEL).all()) and bool((bits[lo + n:] == SENTINEL).all())
             assert rel_err(out, oracle.scan_fwd(w.a, w.x, w.h0, None, rev)) <= TOL
+
+
+def test_noalloc_device_status_reads_back_and_clears(lib):
+    """A device cu_seqlens that is not non-decreasing (every entry still in
+    [0, T], so every sequence index the kernel forms stays in 0 .. n - 1)
+    returns SCAN_OK from the host checks; the kernel's own check records
+    SCAN_ERR_SEQLENS in the library's scratch, which the accessor reads once
+    and clears. Calls before and after still match the oracle."""
+    a, x, h0, cu = packed(4, [100, 200], seed=31, dtype=torch.float32)
+    check_twice(lib, a, x, h0, cu, False)
+    assert lib.scan_noalloc_device_status(DEV) == lib.SCAN_OK
+    bad = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device=DEV)
+    h0b = torch.zeros(3, 4, device=DEV)
+    lib.scan_fwd_noalloc(a, x, h0b, bad)
+    assert lib.scan_noalloc_device_status(DEV) == lib.SCAN_ERR_SEQLENS
+    assert lib.scan_noalloc_device_status(DEV) == lib.SCAN_OK
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    lib.scan_fwd_noalloc(a, x, h0b, bad, True, stream=side)
+    assert lib.scan_noalloc_device_status(DEV, stream=side) == lib.SCAN_ERR_SEQLENS
+    check_twice(lib, a, x, h0, cu, True)
+    assert lib.scan_noalloc_device_status(DEV) == lib.SCAN_OK
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):

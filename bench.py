@@ -575,9 +575,10 @@ def main():
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the other workloads and the copy kernels (the headline step only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--row", choices=ROWS,
+    ap.add_argument("--row", choices=ROWS + ("copy",),
                     help="time only this form (fwd and bwd, --steps timed calls each) and print "
-                         "its figures; the command the ncu captures of that form use")
+                         "its figures; the command the ncu captures of that form use ('copy': "
+                         "the two copy-ceiling kernels)")
     ap.add_argument("--small", action="store_true",
                     help="with --row packed_bidir: 12 sequences instead of 64 (ncu capture size)")
     args = ap.parse_args()
@@ -592,6 +593,11 @@ def main():
             __graft_entry__.build()
         dev = torch.device("cuda", local)
         torch.cuda.set_device(dev)
+        if args.row == "copy":
+            out = measure_copy(dev, scan, args.steps)
+            if rank == 0:
+                print(json.dumps({"row": "copy", **out}), flush=True)
+            return
         rows = measure_rows(args, dev, scan, names=(args.row,), small=args.small)
         if rank == 0:
             print(json.dumps({"row": args.row, "small": args.small, **rows[args.row]}), flush=True)

@@ -41,7 +41,7 @@ def err(got, ref, scale=None):
 GRADS = ("dalpha", "db", "dv", "dc", "dh0")
 
 
-def check(lib, w):
+def check(lib, w, plain_gate=True):
     alpha, b, v, c, dout = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout))
     h0 = w.h0.to(DEV) if w.h0 is not None else None
     o, ck = lib.gdn_fwd(alpha, b, v, c, h0)
@@ -53,13 +53,14 @@ def check(lib, w):
     sc_o = oracle.gdn_fwd(ab(w.alpha), ab(w.b), ab(w.v), ab(w.c), ab(w.h0))
     sc_g = oracle.gdn_bwd(ab(w.alpha), ab(w.b), ab(w.v), ab(w.c), ab(w.dout), ab(w.h0))
     errs = {"o": err(o, ref_o, sc_o)}
-    plain = {}
+    plain = {"o": err(o, ref_o)}
     for name, got, ref, sc in zip(GRADS, g, ref_g, sc_g):
         errs[name] = err(got, ref, sc)
         plain[name] = err(got, ref)
-    print("gdn", tuple(w.b.shape), "plain-metric gradient error", plain)
+    print("gdn", tuple(w.b.shape), "term-scale error", errs, "plain-metric error", plain)
     assert max(errs.values()) <= TOL, errs
-    assert max(plain.values()) <= TOL_GRAD_PLAIN, plain
+    if plain_gate:
+        assert max(plain[k] for k in GRADS) <= TOL_GRAD_PLAIN, plain
 
 
 # T covers the backward's 32-step chunks (31, 32, 33), the forward's 64-step
@@ -159,6 +160,29 @@ def test_gdn_gate_zero_resets(lib, T):
             w.alpha[:, :, t] = 0.0
     w.alpha[1, 1, :] = 0.0  # every step a reset
     check(lib, w)
+
+
+@pytest.mark.parametrize("S,D", [(32, 32), (32, 16), (16, 16)])
+@pytest.mark.parametrize("T", [64, 130, 257])
+def test_gdn_gate_regimes(lib, S, D, T):
+    """Heads whose gates leave the forward walk's frame range within a chunk
+    and restart it: gates in (0, 0.2) (the product falls below 2^-20 every
+    few steps), gates in (1.1, 1.4) (it rises above 2^20), gates of 1e-8 and 0
+    between ordinary ones, and ordinary gates near 1. Gates above 1 grow the
+    state and its adjoint by up to 1e25 over the sequence, and gradient
+    entries far below their terms come out of cancellation: there the
+    term-scale metric is the gate (the plain metric is printed only)."""
+    w = workloads.gdn(2, 4, T, S, D, seed=5 * T + S + D, h0=True)
+    g = torch.Generator().manual_seed(T + 7)
+    shape = (2, T)
+    w.alpha[:, 0] = 0.2 * torch.rand(shape, generator=g)
+    w.alpha[:, 1] = 1.1 + 0.3 * torch.rand(shape, generator=g)
+    mixed = torch.sigmoid(torch.randn(shape, generator=g) + 3.0)
+    pick = torch.rand(shape, generator=g)
+    mixed[pick < 0.1] = 1e-8
+    mixed[pick > 0.95] = 0.0
+    w.alpha[:, 2] = mixed
+    check(lib, w, plain_gate=False)
 
 
 def test_gdn_bwd_rejects_a_short_workspace(lib):

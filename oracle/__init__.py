@@ -22,6 +22,11 @@ What each routine follows (page titles and sections of the source pages):
 * ``gdn_fwd`` / ``gdn_bwd``: "Operations & Triton Kernels" (HyMo), The chunked
   GDN algorithm (write h_t = alpha_t h_{t-1} + b_t v_t^T, read o_t = c_t . h_t)
   and Mathematical Derivation of the Reverse-Time Backward Pass.
+* ``rglru_fwd`` / ``rglru_bwd``: "Our RG-LRU GPU audit", Strengthened fused
+  path (gate logits, a_param, segment_pos, initial state; the square-root
+  multiplier and write; the clipped square-root backward) and Exact real chunk
+  algebra (a reset is a_t = 0), with the method's own gate formulas, which the
+  pages name but do not print (oracle.h states them).
 """
 
 from __future__ import annotations
@@ -78,6 +83,9 @@ def _load():
                 "oracle_gdn_fwd": [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64, _i64],
                 "oracle_gdn_bwd": [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                                    _i64, _i64, _i64, _i64, _i64],
+                "oracle_rglru_fwd": [_dp, _dp, _dp, _dp, _ip, _dp, _dp, _i64, _i64, _i64],
+                "oracle_rglru_bwd": [_dp, _dp, _dp, _dp, _ip, _dp, _dp, _dp, _dp, _dp, _dp,
+                                     _dp, _i64, _i64, _i64],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -237,6 +245,47 @@ def gdn_bwd(alpha, b, v, c, dout, h0=None):
     if rc:
         raise ValueError("oracle_gdn_bwd: malformed arguments")
     return da, db, dv, dc, dh0
+
+
+def _seg(segment_pos):
+    if segment_pos is None:
+        return None
+    if hasattr(segment_pos, "detach"):
+        segment_pos = segment_pos.detach().cpu().numpy()
+    return np.ascontiguousarray(segment_pos, dtype=np.int32)
+
+
+def rglru_fwd(x, gate_a, gate_x, a_param, segment_pos=None, h0=None):
+    """h_t = a_t h_{t-1} + sqrt(1 - a_t^2) sigmoid(gate_x_t) x_t with
+    a_t = sigmoid(a_param)^(8 sigmoid(gate_a_t)); a reset where segment_pos == 0.
+    x, gate_a, gate_x [B, C, T]; a_param [C]; segment_pos [B, T] or None;
+    h0 [B, C] or None. Returns h [B, C, T]."""
+    x, ga, gx, ap, h0 = _f64(x), _f64(gate_a), _f64(gate_x), _f64(a_param), _f64(h0)
+    seg = _seg(segment_pos)
+    B, C, T = x.shape
+    h = np.empty_like(x)
+    rc = _load().oracle_rglru_fwd(_ptr(x), _ptr(ga), _ptr(gx), _ptr(ap), _ptr(seg, _ip),
+                                  _ptr(h0), _ptr(h), B, C, T)
+    if rc:
+        raise ValueError("oracle_rglru_fwd: malformed arguments")
+    return h
+
+
+def rglru_bwd(x, gate_a, gate_x, a_param, dh, segment_pos=None, h0=None):
+    """Gradients of L = sum dh * h: (dx, dgate_a, dgate_x, da_param, dh0)."""
+    x, ga, gx, ap, dh, h0 = (_f64(x), _f64(gate_a), _f64(gate_x), _f64(a_param), _f64(dh),
+                             _f64(h0))
+    seg = _seg(segment_pos)
+    B, C, T = x.shape
+    dx, dga, dgx = np.empty_like(x), np.empty_like(x), np.empty_like(x)
+    dap = np.empty(C, dtype=np.float64)
+    dh0 = np.empty((B, C), dtype=np.float64)
+    rc = _load().oracle_rglru_bwd(_ptr(x), _ptr(ga), _ptr(gx), _ptr(ap), _ptr(seg, _ip),
+                                  _ptr(h0), _ptr(dh), _ptr(dx), _ptr(dga), _ptr(dgx), _ptr(dap),
+                                  _ptr(dh0), B, C, T)
+    if rc:
+        raise ValueError("oracle_rglru_bwd: malformed arguments")
+    return dx, dga, dgx, dap, dh0
 
 
 def chunk_summary(a, x):

@@ -474,3 +474,105 @@ int oracle_gdn_bwd(const double* alpha, const double* b, const double* v,
   free(dh);
   return 0;
 }
+
+/* "Our RG-LRU GPU audit", Strengthened fused path and Exact real chunk
+ * algebra, with the method's own gate formulas (see oracle.h): the gate
+ * terms of every step, then the scalar recurrence, left to right. */
+#define RG_SCALE 8.0    /* log_a = -RG_SCALE softplus(-a_param) r */
+#define RG_U_MIN 1e-6   /* the square root's derivative is taken at u >= RG_U_MIN */
+
+static double rg_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* log(sigmoid(p)) = -softplus(-p), without overflow for large |p| */
+static double rg_log_sigmoid(double p) { return p < 0.0 ? p - log1p(exp(p)) : -log1p(exp(-p)); }
+
+int oracle_rglru_fwd(const double* x, const double* gate_a, const double* gate_x,
+                     const double* a_param, const int32_t* segment_pos,
+                     const double* h0, double* h, int64_t B, int64_t C, int64_t T) {
+  if (!x || !gate_a || !gate_x || !a_param || !h || B < 0 || C < 0 || T < 0) return -1;
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t c = 0; c < C; ++c) {
+      const double ls = rg_log_sigmoid(a_param[c]);
+      double state = h0 ? h0[b * C + c] : 0.0;
+      for (int64_t t = 0; t < T; ++t) {
+        const int64_t e = (b * C + c) * T + t;
+        const double in_gate = rg_sigmoid(gate_x[e]);
+        double a, write;
+        if (segment_pos && segment_pos[b * T + t] == 0) {
+          a = 0.0;
+          write = in_gate * x[e];
+        } else {
+          const double log_a = RG_SCALE * rg_sigmoid(gate_a[e]) * ls;
+          a = exp(log_a);
+          write = sqrt(-expm1(2.0 * log_a)) * in_gate * x[e];
+        }
+        state = a * state + write;
+        h[e] = state;
+      }
+    }
+  return 0;
+}
+
+int oracle_rglru_bwd(const double* x, const double* gate_a, const double* gate_x,
+                     const double* a_param, const int32_t* segment_pos,
+                     const double* h0, const double* dh, double* dx,
+                     double* dgate_a, double* dgate_x, double* da_param,
+                     double* dh0, int64_t B, int64_t C, int64_t T) {
+  if (!x || !gate_a || !gate_x || !a_param || !dh || !dx || !dgate_a || !dgate_x ||
+      !da_param || B < 0 || C < 0 || T < 0)
+    return -1;
+  double* hs = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  if (!hs) return -1;
+  for (int64_t c = 0; c < C; ++c) {
+    const double ls = rg_log_sigmoid(a_param[c]);
+    double d_ls = 0.0; /* dL / d log(sigmoid(a_param[c])) over every (b, t) */
+    for (int64_t b = 0; b < B; ++b) {
+      const int64_t row = (b * C + c) * T;
+      /* hs[0] = h_{-1}, hs[t + 1] = h_t */
+      hs[0] = h0 ? h0[b * C + c] : 0.0;
+      for (int64_t t = 0; t < T; ++t) {
+        const int64_t e = row + t;
+        const double in_gate = rg_sigmoid(gate_x[e]);
+        const int reset = segment_pos && segment_pos[b * T + t] == 0;
+        const double log_a = reset ? 0.0 : RG_SCALE * rg_sigmoid(gate_a[e]) * ls;
+        const double a = reset ? 0.0 : exp(log_a);
+        const double mult = reset ? 1.0 : sqrt(-expm1(2.0 * log_a));
+        hs[t + 1] = a * hs[t] + mult * (in_gate * x[e]);
+      }
+      double g = 0.0, a_next = 0.0;
+      for (int64_t t = T - 1; t >= 0; --t) {
+        const int64_t e = row + t;
+        g = dh[e] + a_next * g; /* dL/dh_t */
+        const double in_gate = rg_sigmoid(gate_x[e]);
+        double a, d_in;
+        if (segment_pos && segment_pos[b * T + t] == 0) {
+          a = 0.0;
+          dx[e] = g * in_gate;
+          d_in = g * x[e];
+          dgate_a[e] = 0.0;
+        } else {
+          const double r = rg_sigmoid(gate_a[e]);
+          const double log_a = RG_SCALE * r * ls;
+          a = exp(log_a);
+          const double u = -expm1(2.0 * log_a);
+          const double mult = sqrt(u);
+          const double d_mult = g * in_gate * x[e];
+          dx[e] = g * mult * in_gate;
+          d_in = g * mult * x[e];
+          const double dmult_du = 0.5 / sqrt(u > RG_U_MIN ? u : RG_U_MIN);
+          const double d_a = g * hs[t] + d_mult * dmult_du * (-2.0 * a);
+          const double d_log_a = d_a * a;
+          dgate_a[e] = d_log_a * RG_SCALE * ls * r * (1.0 - r);
+          d_ls += d_log_a * RG_SCALE * r;
+        }
+        dgate_x[e] = d_in * in_gate * (1.0 - in_gate);
+        a_next = a;
+      }
+      if (dh0) dh0[b * C + c] = (T > 0 ? a_next : 0.0) * g;
+    }
+    /* d log(sigmoid(p)) / dp = sigmoid(-p) */
+    da_param[c] = d_ls * rg_sigmoid(-a_param[c]);
+  }
+  free(hs);
+  return 0;
+}

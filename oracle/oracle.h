@@ -100,6 +100,35 @@ int oracle_gdn_bwd(const double* alpha, const double* b, const double* v,
                    double* dh0, int64_t B, int64_t H, int64_t T, int64_t S,
                    int64_t D);
 
+/* RG-LRU gate preparation in front of the scalar scan ("Our RG-LRU GPU audit",
+ * Strengthened fused path: recurrent input x, two gate logits, a_param, an
+ * optional segment_pos and initial state; gate activations, log_a, transition
+ * a, square-root multiplier and write; Exact real chunk algebra: a reset is
+ * a_t = 0 with the canonical reset write). The gate formulas are the method's
+ * own; the pages name each of these tensors but do not print them:
+ *   r_t = sigmoid(gate_a_t), i_t = sigmoid(gate_x_t),
+ *   log_a_t = -8 softplus(-a_param[c]) r_t, a_t = exp(log_a_t),
+ *   write_t = sqrt(1 - a_t^2) i_t x_t,
+ *   where segment_pos[b, t] == 0 (a reset): a_t = 0 and write_t = i_t x_t;
+ *   h_t = a_t h_{t-1} + write_t, h_{-1} = h0 (or 0).
+ * Layouts: x, gate_a, gate_x, h [B, C, T]; a_param [C]; segment_pos int32
+ * [B, T] (NULL: no resets); h0 [B, C]. */
+int oracle_rglru_fwd(const double* x, const double* gate_a, const double* gate_x,
+                     const double* a_param, const int32_t* segment_pos,
+                     const double* h0, double* h, int64_t B, int64_t C, int64_t T);
+
+/* Its backward for L = sum_t dh_t h_t: dx, dgate_a, dgate_x (layout of x),
+ * da_param [C] (summed over B and T), dh0 [B, C] (when non-NULL). The
+ * adjoint g_t = dh_t + a_{t+1} g_{t+1} (a_T = 0), then the chain rule through
+ * the gate terms; the square root's derivative d sqrt(u) / du is taken at
+ * max(u, 1e-6) (the clipped square-root backward), u = 1 - a_t^2. States
+ * from its own fp64 forward. */
+int oracle_rglru_bwd(const double* x, const double* gate_a, const double* gate_x,
+                     const double* a_param, const int32_t* segment_pos,
+                     const double* h0, const double* dh, double* dx,
+                     double* dgate_a, double* dgate_x, double* da_param,
+                     double* dh0, int64_t B, int64_t C, int64_t T);
+
 /* Chunk summary of n consecutive scalar steps, built left to right
  * (P <- a_t P, Q <- a_t Q + x_t from P = 1, Q = 0). */
 void oracle_chunk_summary(const double* a, const double* x, int64_t n,

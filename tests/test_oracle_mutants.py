@@ -115,6 +115,37 @@ MUTANTS = [
     ("gdn", "bwd_read_injected_only_at_last_step",
      "dh[s * D + d] = c[st * S + s] * dout[st * D + d] + an * dh[s * D + d];",
      "dh[s * D + d] = an * dh[s * D + d] + (t == T - 1 ? c[st * S + s] * dout[st * D + d] : 0.0);"),
+    # RG-LRU gate preparation
+    ("rglru", "scale_4", "#define RG_SCALE 8.0", "#define RG_SCALE 4.0"),
+    ("rglru", "fwd_log_sigmoid_sign",
+     "const double ls = rg_log_sigmoid(a_param[c]);\n      double state",
+     "const double ls = rg_log_sigmoid(-a_param[c]);\n      double state"),
+    ("rglru", "fwd_no_multiplier",
+     "write = sqrt(-expm1(2.0 * log_a)) * in_gate * x[e];\n        }\n        state = a * state + write;",
+     "write = in_gate * x[e];\n        }\n        state = a * state + write;"),
+    ("rglru", "fwd_reset_keeps_gate", "a = 0.0;\n          write = in_gate * x[e];",
+     "a = exp(RG_SCALE * rg_sigmoid(gate_a[e]) * ls);\n          write = in_gate * x[e];"),
+    ("rglru", "fwd_reset_keeps_multiplier", "write = in_gate * x[e];\n        } else {",
+     "write = sqrt(-expm1(2.0 * RG_SCALE * rg_sigmoid(gate_a[e]) * ls)) * in_gate * x[e];\n"
+     "        } else {"),
+    ("rglru", "fwd_segment_pos_ignores_batch",
+     "if (segment_pos && segment_pos[b * T + t] == 0) {\n          a = 0.0;\n          write",
+     "if (segment_pos && segment_pos[t] == 0) {\n          a = 0.0;\n          write"),
+    ("rglru", "bwd_adjoint_drops_gate", "g = dh[e] + a_next * g; /* dL/dh_t */",
+     "g = dh[e] + g; /* dL/dh_t */"),
+    ("rglru", "bwd_da_uses_h_t", "const double d_a = g * hs[t] + ",
+     "const double d_a = g * hs[t + 1] + "),
+    ("rglru", "bwd_drops_multiplier_term", "d_mult * dmult_du * (-2.0 * a)",
+     "0.0 * dmult_du * (-2.0 * a)"),
+    ("rglru", "bwd_da_param_without_sigmoid", "da_param[c] = d_ls * rg_sigmoid(-a_param[c]);",
+     "da_param[c] = d_ls;"),
+    ("rglru", "bwd_dh0_without_gate", "dh0[b * C + c] = (T > 0 ? a_next : 0.0) * g;",
+     "dh0[b * C + c] = g;"),
+    ("rglru", "bwd_dgate_x_without_sigmoid_derivative",
+     "dgate_x[e] = d_in * in_gate * (1.0 - in_gate);", "dgate_x[e] = d_in;"),
+    ("rglru", "bwd_dgate_a_without_sigmoid_derivative",
+     "dgate_a[e] = d_log_a * RG_SCALE * ls * r * (1.0 - r);",
+     "dgate_a[e] = d_log_a * RG_SCALE * ls * r;"),
 ]
 
 PINS = {
@@ -133,6 +164,9 @@ PINS = {
     "gdn": ["test_gdn_forward_exact_closed_form",
             "test_gdn_with_one_by_one_state_is_the_scalar_scan",
             "test_gdn_backward_central_differences"],
+    "rglru": ["test_rglru_transition_and_multiplier", "test_rglru_frozen_and_open_gates",
+              "test_rglru_is_the_scan_of_its_step_maps", "test_rglru_reset_erases_the_prefix",
+              "test_rglru_backward_central_differences"],
 }
 
 # Runs the named pins against the oracle copy in argv[1] and prints, as JSON,

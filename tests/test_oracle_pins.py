@@ -16,7 +16,12 @@ transposed operand in oracle.c fails at least one of them:
 * the block form against k = 1, diagonal A, A = I (numpy cumsum) and explicit
   numpy matrix products;
 * the chunk algebra of "Our RG-LRU GPU audit" (Exact real chunk algebra)
-  composed in random bracketings.
+  composed in random bracketings;
+* the RG-LRU gate preparation (the same page, Strengthened fused path):
+  the transition against sigmoid(a_param)^(8 r) from a library sigmoid, the
+  multiplier against a^2 + mult^2 = 1, frozen and open gates, the whole
+  sequence against the pinned scalar scan of its one-step maps, reset
+  erasure, and central differences for every gradient.
 """
 
 from fractions import Fraction
@@ -555,3 +560,136 @@ def test_gdn_backward_central_differences():
             minus[which][idx] -= eps
             fd = (loss(*plus) - loss(*minus)) / (2 * eps)
             assert abs(fd - grad[idx]) <= tol * max(1.0, abs(fd)), (which, idx, fd, grad[idx])
+
+
+# ---------------------------------------------------------------------------
+# RG-LRU gate preparation ("Our RG-LRU GPU audit", Strengthened fused path and
+# Exact real chunk algebra; the gate formulas are the method's own)
+# ---------------------------------------------------------------------------
+
+def _expit(z):
+    from scipy.special import expit
+    return expit(z)
+
+
+def _rglru_inputs(g, B, C, T, resets=True):
+    x = g.standard_normal((B, C, T))
+    ga = g.standard_normal((B, C, T))
+    gx = g.standard_normal((B, C, T))
+    ap = 2.0 + g.standard_normal(C)
+    h0 = g.standard_normal((B, C))
+    seg = None
+    if resets:
+        seg = np.tile(np.arange(T, dtype=np.int32), (B, 1)) + 1
+        for b in range(B):
+            for t in g.choice(T, size=max(1, T // 8), replace=False):
+                seg[b, t:] = np.arange(T - t, dtype=np.int32)  # a new segment starts at t
+    return x, ga, gx, ap, seg, h0
+
+
+def _step_maps(x, ga, gx, ap, seg):
+    """a_t and write_t of every step, each read off a one-step call of the
+    oracle: from h0 = 1 with x = 0 (h = a) and from h0 = 0 (h = write)."""
+    B, C, T = x.shape
+    a = np.empty_like(x)
+    w = np.empty_like(x)
+    for b in range(B):
+        for t in range(T):
+            reset = seg is not None and seg[b, t] == 0
+            sp = np.zeros((1, 1), dtype=np.int32) if reset else None
+            col = lambda arr: arr[b, :, t].reshape(1, C, 1)
+            a[b, :, t] = oracle.rglru_fwd(np.zeros((1, C, 1)), col(ga), col(gx), ap, sp,
+                                          np.ones((1, C)))[0, :, 0]
+            w[b, :, t] = oracle.rglru_fwd(col(x), col(ga), col(gx), ap, sp,
+                                          np.zeros((1, C)))[0, :, 0]
+    return a, w
+
+
+def test_rglru_transition_and_multiplier():
+    """a = sigmoid(a_param)^(8 sigmoid(gate_a)) (the same number as
+    exp(-8 softplus(-a_param) r), computed another way), and the multiplier
+    closes a^2 + mult^2 = 1."""
+    g = np.random.default_rng(40)
+    C = 64
+    ga, gx = g.standard_normal((1, C, 1)) * 3, g.standard_normal((1, C, 1)) * 3
+    ap = g.standard_normal(C) * 4
+    a = oracle.rglru_fwd(np.zeros((1, C, 1)), ga, gx, ap, None, np.ones((1, C)))[0, :, 0]
+    want = _expit(ap) ** (8.0 * _expit(ga[0, :, 0]))
+    assert np.allclose(a, want, rtol=1e-12, atol=0)
+    w = oracle.rglru_fwd(np.ones((1, C, 1)), ga, gx, ap, None, np.zeros((1, C)))[0, :, 0]
+    mult = w / _expit(gx[0, :, 0])
+    assert (mult >= 0).all()
+    assert np.allclose(a * a + mult * mult, 1.0, rtol=0, atol=1e-12)
+
+
+def test_rglru_frozen_and_open_gates():
+    """r -> 0 (gate_a = -80): a = 1 and the multiplier vanishes, the state
+    is carried unchanged. a_param -> -inf (-80): a ~ e^-170, the multiplier is
+    1 and h_t = sigmoid(gate_x_t) x_t."""
+    g = np.random.default_rng(41)
+    B, C, T = 2, 3, 50
+    x, ga, gx, ap, _, h0 = _rglru_inputs(g, B, C, T, resets=False)
+    h = oracle.rglru_fwd(x, np.full_like(ga, -80.0), gx, ap, None, h0)
+    assert np.allclose(h, h0[:, :, None], rtol=1e-12, atol=1e-12)
+    gb = np.clip(ga, -1.0, 1.0)
+    h = oracle.rglru_fwd(x, gb, gx, np.full(C, -80.0), None, h0)
+    assert np.allclose(h, _expit(gx) * x, rtol=1e-13, atol=1e-15)
+
+
+def test_rglru_is_the_scan_of_its_step_maps():
+    """The whole sequence equals the scalar scan (pinned above) of the step
+    maps (a_t, write_t) that one-step calls give, resets included: the gates
+    are read per (b, c, t), a_param per channel, segment_pos per (b, t)."""
+    g = np.random.default_rng(42)
+    x, ga, gx, ap, seg, h0 = _rglru_inputs(g, 2, 3, 37)
+    a, w = _step_maps(x, ga, gx, ap, seg)
+    got = oracle.rglru_fwd(x, ga, gx, ap, seg, h0)
+    want = np.asarray(oracle.scan_fwd(torch.tensor(a), torch.tensor(w), torch.tensor(h0)))
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_rglru_reset_erases_the_prefix():
+    """Where segment_pos == 0: h_t = sigmoid(gate_x_t) x_t exactly, whatever
+    came before; inputs before the reset change nothing from it on."""
+    g = np.random.default_rng(43)
+    x, ga, gx, ap, seg, h0 = _rglru_inputs(g, 2, 3, 40)
+    seg[:, 17] = 0
+    h = oracle.rglru_fwd(x, ga, gx, ap, seg, h0)
+    for b in range(2):
+        for t in range(40):
+            if seg[b, t] == 0:
+                assert np.array_equal(h[b, :, t], _expit(gx[b, :, t]) * x[b, :, t])
+    x2, ga2, h02 = x.copy(), ga.copy(), h0 * 3.0
+    x2[:, :, :17] += 1.0
+    ga2[:, :, :17] -= 2.0
+    h2 = oracle.rglru_fwd(x2, ga2, gx, ap, seg, h02)
+    assert np.array_equal(h2[:, :, 17:], h[:, :, 17:])
+
+
+def test_rglru_backward_central_differences():
+    """Every gradient of L = sum dh * h against central differences of the
+    forward (smooth in each input; inputs away from the square root's clip)."""
+    g = np.random.default_rng(44)
+    B, C, T = 2, 2, 9
+    x, ga, gx, ap, seg, h0 = _rglru_inputs(g, B, C, T, resets=False)
+    seg = np.tile(np.arange(T, dtype=np.int32), (B, 1)) + 1
+    seg[0, 4:] = np.arange(T - 4)  # a reset inside row 0 of each channel
+    dh = g.standard_normal((B, C, T))
+    dx, dga, dgx, dap, dh0 = oracle.rglru_bwd(x, ga, gx, ap, dh, seg, h0)
+
+    def loss(*args):
+        return float((oracle.rglru_fwd(args[0], args[1], args[2], args[3], seg, args[4]) * dh).sum())
+
+    args = [x, ga, gx, ap, h0]
+    for which, grad in ((0, dx), (1, dga), (2, dgx), (3, dap), (4, dh0)):
+        arr = args[which]
+        for idx in np.ndindex(arr.shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += 1e-6
+            minus[which][idx] -= 1e-6
+            fd = (loss(*plus) - loss(*minus)) / 2e-6
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (which, idx, fd, grad[idx])
+    # a reset's gate has no effect: its gradient is 0, and dh0 of row 0 sees
+    # the steps before the reset only
+    assert np.all(dga[0, :, 4] == 0.0)

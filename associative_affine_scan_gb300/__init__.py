@@ -48,6 +48,8 @@ from ._binding import (  # noqa: F401
     gdn_bwd,
     affine_scan_fwd,
     lib,
+    rglru_bwd,
+    rglru_fwd,
     scan_bidir_bwd,
     scan_bidir_fwd,
     scan_bwd,

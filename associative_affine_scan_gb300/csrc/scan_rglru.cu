@@ -1,0 +1,407 @@
+// scan_rglru.cu -- RG-LRU gate preparation fused in front of the scalar scan
+// ("Our RG-LRU GPU audit": Strengthened fused path -- the recurrent input, two
+// gate logits, a_param, an optional segment_pos and initial state; the gate
+// activations, log_a, transition, square-root multiplier and write formed in
+// registers and never stored, recomputed by the backward, whose square root
+// derivative is clipped and whose a_param gradient is reduced from partial
+// sums; Exact real chunk algebra -- a reset is a_t = 0 with the canonical
+// write). The gate formulas are the method's own; the pages name the tensors
+// but do not print them:
+//   r_t = sigmoid(gate_a_t), i_t = sigmoid(gate_x_t),
+//   log_a_t = 8 r_t log(sigmoid(a_param[c])), a_t = exp(log_a_t),
+//   write_t = sqrt(1 - a_t^2) i_t x_t; where segment_pos[b, t] == 0 a_t = 0
+//   and write_t = i_t x_t;  h_t = a_t h_{t-1} + write_t, h_{-1} = h0 (or 0).
+//
+// One warp per row (b, c) walks T in 128-step chunks with the state in a
+// register: lane l holds steps 4l .. 4l + 3 of a chunk (one 16-byte vector of
+// each input, so every warp access is one coalesced 512-byte run), composes
+// their maps (P, Q) and a shuffle scan over the lanes gives each lane its
+// carry-in. The next chunk's inputs are loaded before the current one is
+// computed. A block holds the rows of one channel, so the backward sums the
+// a_param gradient over b and t in a fixed order, without a workspace.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/libscan.h"
+#include "scan_internal.h"
+
+namespace scan {
+namespace {
+
+constexpr unsigned kRgFull = 0xffffffffu;
+constexpr float kRgScale = 8.f;    // log_a = kRgScale r log(sigmoid(a_param))
+constexpr float kRgUMin = 1e-6f;   // d sqrt(u) / du is taken at u >= kRgUMin
+constexpr int kRgChunk = 128;      // steps per chunk: 4 per lane
+constexpr int kRgMaxWarps = 8;     // warps (rows of one channel) per block
+
+struct RgParams {
+  const float* x;
+  const float* ga;  // gate_a logits
+  const float* gx;  // gate_x logits
+  const float* ap;  // a_param [C]
+  const int32_t* seg;  // segment_pos [B, T] or null
+  const float* h0;     // [B, C] or null
+  float* h;            // forward output / backward input [B, C, T]
+  const float* dh;
+  float* dx;
+  float* dga;
+  float* dgx;
+  float* dap;  // [C]
+  float* dh0;  // [B, C] or null
+  int64_t B, C, T;
+};
+
+__device__ __forceinline__ float rg_sigmoid(float z) { return 1.f / (1.f + expf(-z)); }
+
+// log(sigmoid(p)) = -softplus(-p), without overflow for large |p|
+__device__ __forceinline__ float rg_log_sigmoid(float p) {
+  return p < 0.f ? p - log1pf(expf(p)) : -log1pf(expf(-p));
+}
+
+// Four consecutive values of a row from step t (zero past T); VEC: t % 4 == 0
+// and the row 16-byte aligned, so a whole group is one vector load.
+template <bool VEC>
+__device__ __forceinline__ void rg_ld(const float* row, int64_t t, int64_t T, float (&v)[4]) {
+  if (VEC && t + 4 <= T) {
+    const float4 q = *reinterpret_cast<const float4*>(row + t);
+    v[0] = q.x;
+    v[1] = q.y;
+    v[2] = q.z;
+    v[3] = q.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = t + j < T ? row[t + j] : 0.f;
+  }
+}
+
+template <bool VEC>
+__device__ __forceinline__ void rg_ld_seg(const int32_t* row, int64_t t, int64_t T, int (&v)[4]) {
+  if (!row) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = 1;
+  } else if (VEC && t + 4 <= T) {
+    const int4 q = *reinterpret_cast<const int4*>(row + t);
+    v[0] = q.x;
+    v[1] = q.y;
+    v[2] = q.z;
+    v[3] = q.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = t + j < T ? row[t + j] : 1;
+  }
+}
+
+template <bool VEC>
+__device__ __forceinline__ void rg_st(float* row, int64_t t, int64_t T, const float (&v)[4]) {
+  if (VEC && t + 4 <= T) {
+    __stcs(reinterpret_cast<float4*>(row + t), make_float4(v[0], v[1], v[2], v[3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (t + j < T) __stcs(row + t + j, v[j]);
+  }
+}
+
+// The gate terms of one step: transition a, the write's factors. A reset
+// (segment_pos == 0) has a = 0 and multiplier 1.
+struct RgStep {
+  float a, u, r, i;  // u = 1 - a^2 (multiplier sqrt(u)); u = 1 at a reset
+};
+
+// a is formed as 1 - d with d = 1 - a = -expm1(log_a) accurate to its own
+// last bit, so that a near 1 (long memories) rounds to the nearest fp32 value
+// without a bias: the state carries a product of thousands of such gates,
+// and exp(log_a) rounded in fp32 came out 0.1 ulp high on average, which
+// 23,000-step memories turned into errors of 1e-5 and more. 1 - a^2 = d (2 - d).
+__device__ __forceinline__ RgStep rg_gates(float ga, float gx, float ls, bool reset) {
+  RgStep s;
+  s.i = rg_sigmoid(gx);
+  s.r = rg_sigmoid(ga);
+  const float d = -expm1f(kRgScale * s.r * ls);
+  s.a = reset ? 0.f : 1.f - d;
+  s.u = reset ? 1.f : d * (2.f - d);
+  return s;
+}
+
+// One chunk's inputs for one lane.
+struct RgIn {
+  float x[4], ga[4], gx[4];
+  int seg[4];
+};
+
+template <bool VEC>
+__device__ __forceinline__ void rg_load(const RgParams& p, int64_t base, const int32_t* seg,
+                                        int64_t t, RgIn& in) {
+  rg_ld<VEC>(p.x + base, t, p.T, in.x);
+  rg_ld<VEC>(p.ga + base, t, p.T, in.ga);
+  rg_ld<VEC>(p.gx + base, t, p.T, in.gx);
+  rg_ld_seg<VEC>(seg, t, p.T, in.seg);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(32 * kRgMaxWarps) rglru_fwd_kernel(const RgParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t c = blockIdx.x, T = p.T;
+  const float ls = rg_log_sigmoid(p.ap[c]);
+  for (int64_t b = warp; b < p.B; b += nw) {
+    const int64_t row = b * p.C + c, base = row * T;
+    const int32_t* seg = p.seg ? p.seg + b * T : nullptr;
+    float carry = p.h0 ? p.h0[row] : 0.f;
+    RgIn in, nx;
+    rg_load<VEC>(p, base, seg, 4 * lane, in);
+    for (int64_t t0 = 0; t0 < T; t0 += kRgChunk) {
+      const int64_t t = t0 + 4 * lane;
+      if (t0 + kRgChunk < T) rg_load<VEC>(p, base, seg, t + kRgChunk, nx);
+      // the lane's four step maps h -> a h + w (identity past T), composed
+      float a[4], w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const RgStep s = rg_gates(in.ga[j], in.gx[j], ls, in.seg[j] == 0);
+        const bool valid = t + j < T;
+        a[j] = valid ? s.a : 1.f;
+        w[j] = valid ? sqrtf(s.u) * s.i * in.x[j] : 0.f;
+      }
+      float P = a[0], Q = w[0];
+#pragma unroll
+      for (int j = 1; j < 4; ++j) {
+        Q = fmaf(a[j], Q, w[j]);
+        P *= a[j];
+      }
+      // inclusive scan over the lanes (time order): (P, Q) after the lane's run
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float Pu = __shfl_up_sync(kRgFull, P, o), Qu = __shfl_up_sync(kRgFull, Q, o);
+        if (lane >= o) {
+          Q = fmaf(P, Qu, Q);
+          P *= Pu;
+        }
+      }
+      float Pe = __shfl_up_sync(kRgFull, P, 1), Qe = __shfl_up_sync(kRgFull, Q, 1);
+      if (lane == 0) {
+        Pe = 1.f;
+        Qe = 0.f;
+      }
+      float st = fmaf(Pe, carry, Qe);  // the state before the lane's first step
+      float out[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        st = fmaf(a[j], st, w[j]);
+        out[j] = st;
+      }
+      rg_st<VEC>(p.h + base, t, T, out);
+      carry = __shfl_sync(kRgFull, st, 31);
+      in = nx;
+    }
+  }
+}
+
+// Backward: the adjoint g_t = dh_t + a_{t+1} g_{t+1} (a_T = 0) from the last
+// chunk to the first (lanes still in time order within a chunk), and per step
+// dx = g m i, d(gate_x) = g m x i (1 - i), and through a:
+//   dL/da = g h_{t-1} + (g i x) (d sqrt(u) / du) (-2 a),  d log_a = a dL/da,
+//   d(gate_a) = d log_a * 8 log(sigmoid(a_param)) r (1 - r),
+//   d log(sigmoid(a_param)) += d log_a * 8 r;
+// a reset step has no gate_a gradient and multiplier 1. h_{t-1} comes from the
+// forward output h (h0 before the first step).
+template <bool VEC>
+__global__ void __launch_bounds__(32 * kRgMaxWarps) rglru_bwd_kernel(const RgParams p) {
+  __shared__ float s_part[kRgMaxWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t c = blockIdx.x, T = p.T;
+  const float ls = rg_log_sigmoid(p.ap[c]);
+  const int64_t nch = (T + kRgChunk - 1) / kRgChunk;
+  float dls = 0.f;  // this lane's share of dL / d log(sigmoid(a_param[c]))
+  for (int64_t b = warp; b < p.B; b += nw) {
+    const int64_t row = b * p.C + c, base = row * T;
+    const int32_t* seg = p.seg ? p.seg + b * T : nullptr;
+    const float init = p.h0 ? p.h0[row] : 0.f;
+    float carry = 0.f;    // g at the first step of the chunk after this one
+    float a_after = 0.f;  // a at that step (0 past the end)
+    RgIn in, nx;
+    float dh[4], hv[4], ndh[4], nhv[4];
+    {
+      const int64_t t = (nch - 1) * kRgChunk + 4 * lane;
+      rg_load<VEC>(p, base, seg, t, in);
+      rg_ld<VEC>(p.dh + base, t, T, dh);
+      rg_ld<VEC>(p.h + base, t, T, hv);
+    }
+    for (int64_t k = nch - 1; k >= 0; --k) {
+      const int64_t t0 = k * kRgChunk, t = t0 + 4 * lane;
+      if (k > 0) {
+        rg_load<VEC>(p, base, seg, t - kRgChunk, nx);
+        rg_ld<VEC>(p.dh + base, t - kRgChunk, T, ndh);
+        rg_ld<VEC>(p.h + base, t - kRgChunk, T, nhv);
+      }
+      // h_{t-1} before the lane's first step
+      float hprev = __shfl_up_sync(kRgFull, hv[3], 1);
+      if (lane == 0) hprev = t0 > 0 ? p.h[base + t0 - 1] : init;
+      RgStep s[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        s[j] = rg_gates(in.ga[j], in.gx[j], ls, in.seg[j] == 0);
+        if (t + j >= T) {
+          s[j].a = 0.f;  // past the end: nothing flows back
+          dh[j] = 0.f;
+        }
+      }
+      // the gate one step later, shifted in from the next lane / chunk
+      const float a_nl = __shfl_down_sync(kRgFull, s[0].a, 1);
+      const float A[4] = {s[1].a, s[2].a, s[3].a, lane == 31 ? a_after : a_nl};
+      // the lane's reverse run: g at its first step = P g_in + Q
+      float P = 1.f, Q = 0.f;
+#pragma unroll
+      for (int j = 3; j >= 0; --j) {
+        Q = fmaf(A[j], Q, dh[j]);
+        P *= A[j];
+      }
+      // inclusive scan over the lanes in reverse (lanes l .. 31)
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float Pd = __shfl_down_sync(kRgFull, P, o), Qd = __shfl_down_sync(kRgFull, Q, o);
+        if (lane + o < 32) {
+          Q = fmaf(P, Qd, Q);
+          P *= Pd;
+        }
+      }
+      float Pe = __shfl_down_sync(kRgFull, P, 1), Qe = __shfl_down_sync(kRgFull, Q, 1);
+      if (lane == 31) {
+        Pe = 1.f;
+        Qe = 0.f;
+      }
+      float g = fmaf(Pe, carry, Qe);  // g at the step after the lane's run
+      float odx[4], oga[4], ogx[4];
+#pragma unroll
+      for (int j = 3; j >= 0; --j) {
+        g = fmaf(A[j], g, dh[j]);
+        const float hp = j > 0 ? hv[j > 0 ? j - 1 : 0] : hprev;
+        const float xv = in.x[j], ig = s[j].i;
+        const bool reset = in.seg[j] == 0;
+        const float mult = reset ? 1.f : sqrtf(s[j].u);
+        odx[j] = g * mult * ig;
+        const float d_in = g * mult * xv;
+        ogx[j] = d_in * ig * (1.f - ig);
+        if (reset || t + j >= T) {
+          oga[j] = 0.f;
+        } else {
+          const float d_mult = g * ig * xv;
+          const float dmdu = 0.5f * rsqrtf(fmaxf(s[j].u, kRgUMin));
+          const float d_a = fmaf(g, hp, d_mult * dmdu * (-2.f * s[j].a));
+          const float dla = d_a * s[j].a;
+          const float r = s[j].r;
+          oga[j] = dla * kRgScale * ls * r * (1.f - r);
+          dls = fmaf(dla * kRgScale, r, dls);
+        }
+      }
+      rg_st<VEC>(p.dx + base, t, T, odx);
+      rg_st<VEC>(p.dga + base, t, T, oga);
+      rg_st<VEC>(p.dgx + base, t, T, ogx);
+      carry = __shfl_sync(kRgFull, g, 0);  // g at step t0
+      a_after = __shfl_sync(kRgFull, s[0].a, 0);
+      if (k > 0) {
+        in = nx;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dh[j] = ndh[j];
+          hv[j] = nhv[j];
+        }
+      }
+    }
+    if (p.dh0 && lane == 0) p.dh0[row] = T > 0 ? a_after * carry : 0.f;  // a_0 g_0
+  }
+  // the a_param gradient: lanes, then warps, in a fixed order
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) dls += __shfl_xor_sync(kRgFull, dls, o);
+  if (lane == 0) s_part[warp] = dls;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float sum = 0.f;
+    for (int w = 0; w < nw; ++w) sum += s_part[w];
+    p.dap[c] = sum * rg_sigmoid(-p.ap[c]);  // d log(sigmoid(p)) / dp = sigmoid(-p)
+  }
+}
+
+bool al16(const void* q) { return q == nullptr || ((uintptr_t)q % 16) == 0; }
+
+cudaError_t rg_launch(const RgParams& p, bool fwd, bool vec, cudaStream_t s) {
+  const int nw = (int)(p.B < kRgMaxWarps ? p.B : kRgMaxWarps);
+  const dim3 grid((unsigned)p.C), block(32u * (unsigned)nw);
+  if (fwd) {
+    if (vec) rglru_fwd_kernel<true><<<grid, block, 0, s>>>(p);
+    else rglru_fwd_kernel<false><<<grid, block, 0, s>>>(p);
+  } else {
+    if (vec) rglru_bwd_kernel<true><<<grid, block, 0, s>>>(p);
+    else rglru_bwd_kernel<false><<<grid, block, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace scan
+
+using namespace scan;
+
+extern "C" {
+
+scan_status rglru_fwd(const float* x, const float* gate_a, const float* gate_x,
+                      const float* a_param, const int32_t* segment_pos, const float* h0, float* h,
+                      int64_t B, int64_t C, int64_t T, cudaStream_t stream) {
+  if (B < 0 || C < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
+  if (C > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
+  if (B * C * T == 0) return SCAN_OK;
+  if (!x || !gate_a || !gate_x || !a_param || !h) return SCAN_ERR_INVALID_ARG;
+  RgParams p{};
+  p.x = x;
+  p.ga = gate_a;
+  p.gx = gate_x;
+  p.ap = a_param;
+  p.seg = segment_pos;
+  p.h0 = h0;
+  p.h = h;
+  p.B = B;
+  p.C = C;
+  p.T = T;
+  const bool vec = T % 4 == 0 && al16(x) && al16(gate_a) && al16(gate_x) && al16(h) &&
+                   al16(segment_pos);
+  return rg_launch(p, true, vec, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
+}
+
+scan_status rglru_bwd(const float* x, const float* gate_a, const float* gate_x,
+                      const float* a_param, const int32_t* segment_pos, const float* h0,
+                      const float* h, const float* dh, float* dx, float* dgate_a, float* dgate_x,
+                      float* da_param, float* dh0, int64_t B, int64_t C, int64_t T,
+                      cudaStream_t stream) {
+  if (B < 0 || C < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
+  if (C > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
+  if (C == 0) return SCAN_OK;
+  if (!da_param || !a_param) return SCAN_ERR_INVALID_ARG;
+  if (B * T == 0) {  // nothing flows back: the parameter and initial-state gradients are 0
+    cudaError_t e = launch_fill_zero(da_param, C, stream);
+    if (e == cudaSuccess && dh0) e = launch_fill_zero(dh0, B * C, stream);
+    return e == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
+  }
+  if (!x || !gate_a || !gate_x || !h || !dh || !dx || !dgate_a || !dgate_x)
+    return SCAN_ERR_INVALID_ARG;
+  RgParams p{};
+  p.x = x;
+  p.ga = gate_a;
+  p.gx = gate_x;
+  p.ap = a_param;
+  p.seg = segment_pos;
+  p.h0 = h0;
+  p.h = const_cast<float*>(h);
+  p.dh = dh;
+  p.dx = dx;
+  p.dga = dgate_a;
+  p.dgx = dgate_x;
+  p.dap = da_param;
+  p.dh0 = dh0;
+  p.B = B;
+  p.C = C;
+  p.T = T;
+  const bool vec = T % 4 == 0 && al16(x) && al16(gate_a) && al16(gate_x) && al16(h) &&
+                   al16(dh) && al16(dx) && al16(dgate_a) && al16(dgate_x) && al16(segment_pos);
+  return rg_launch(p, false, vec, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
+}
+
+}  // extern "C"

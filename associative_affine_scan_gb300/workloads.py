@@ -25,6 +25,11 @@ design: one (b, n) lane per state block, (k, v) blocks):
   B ~ N(0,1), h0 = 0, dH ~ N(0,1)
 * ``log_4k``           [8, 1536, 4096] fp32, log a = logsigmoid(z),
   z ~ N(0,1), log x ~ N(0,1), no initial state, dh ~ N(0,1)
+* ``rglru_4k``         [8, 1536, 4096] fp32 RG-LRU inputs ("Our RG-LRU GPU
+  audit", Strengthened fused path): x, gate_a, gate_x ~ N(0,1), a_param ~
+  U(4.3, 9) per channel (long memories: sigmoid(a_param)^8 from about 0.89 to
+  0.999), segment_pos of documents with lengths ~ U{512..8192} laid end to end
+  from t = 0 in every batch row, no initial state, dh ~ N(0,1)
 
 Every generator takes a ``scale`` that shrinks the sizes for quick tests while
 keeping the distributions.
@@ -266,3 +271,58 @@ def log_dense(B: int, C: int, T: int, seed: int = 0, *, h0: bool = False,
 
 def log_4k(seed: int = 0, scale: int = 1) -> LogWorkload:
     return log_dense(8, 1536 // scale, 4096, seed, name="log_4k")
+
+
+@dataclass
+class RglruWorkload:
+    """Inputs of one RG-LRU problem: x, gate logits [B, C, T], a_param [C],
+    segment_pos int32 [B, T] (or None), h0 [B, C] (or None), dh [B, C, T]."""
+
+    name: str
+    x: torch.Tensor
+    gate_a: torch.Tensor
+    gate_x: torch.Tensor
+    a_param: torch.Tensor
+    dh: torch.Tensor
+    segment_pos: Optional[torch.Tensor] = None
+    h0: Optional[torch.Tensor] = None
+
+    @property
+    def n_elem(self) -> int:
+        return self.x.numel()
+
+
+def document_positions(B: int, T: int, lo: int, hi: int, g: torch.Generator) -> torch.Tensor:
+    """segment_pos [B, T]: per batch row, documents of lengths ~ U{lo..hi} laid
+    end to end from t = 0; the value is the step's position in its document."""
+    pos = torch.empty((B, T), dtype=torch.int32)
+    for b in range(B):
+        t = 0
+        while t < T:
+            n = int(torch.randint(lo, hi + 1, (1,), generator=g))
+            m = min(n, T - t)
+            pos[b, t:t + m] = torch.arange(m, dtype=torch.int32)
+            t += m
+    return pos
+
+
+def rglru(B: int, C: int, T: int, seed: int = 0, *, docs: Optional[tuple] = (512, 8192),
+          h0: bool = False, name: str = "rglru") -> RglruWorkload:
+    """x, gate_a, gate_x ~ N(0,1); a_param ~ U(4.3, 9); segment_pos of documents
+    with lengths ~ U{docs} (None: no resets); dh ~ N(0,1); h0 ~ N(0,1) if asked.
+    Drawn in that order from one generator."""
+    g = _gen(seed)
+    x = torch.randn((B, C, T), generator=g)
+    ga = torch.randn((B, C, T), generator=g)
+    gx = torch.randn((B, C, T), generator=g)
+    ap = 4.3 + 4.7 * torch.rand((C,), generator=g)
+    seg = document_positions(B, T, docs[0], docs[1], g) if docs else None
+    dh = torch.randn((B, C, T), generator=g)
+    h0t = torch.randn((B, C), generator=g) if h0 else None
+    return RglruWorkload(name, x, ga, gx, ap, dh, seg, h0t)
+
+
+def rglru_4k(seed: int = 0) -> RglruWorkload:
+    """8 x 1536 x 4096, the scalar benchmark's dense shape, with documents of
+    the packed benchmark's length mix."""
+    return rglru(8, 1536, 4096, seed, name="rglru_4k")

@@ -322,6 +322,50 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v,
                     void* workspace, size_t workspace_bytes,
                     cudaStream_t stream);
 
+/* RG-LRU gate preparation fused in front of the scalar scan ("Our RG-LRU GPU
+ * audit", Strengthened fused path: the recurrent input, two gate logits,
+ * a_param, optional segment_pos and initial state, with the gate activations,
+ * log_a, transition, square-root multiplier and write formed in registers and
+ * never stored; Exact real chunk algebra: a reset is a_t = 0 with the
+ * canonical write). The gate formulas are the method's own (the pages name
+ * these tensors but do not print them):
+ *   r_t = sigmoid(gate_a_t), i_t = sigmoid(gate_x_t),
+ *   log_a_t = 8 r_t log(sigmoid(a_param[c])), a_t = exp(log_a_t),
+ *   write_t = sqrt(1 - a_t^2) i_t x_t;
+ *   where segment_pos[b, t] == 0 (a reset): a_t = 0, write_t = i_t x_t;
+ *   h_t = a_t h_{t-1} + write_t, h_{-1} = h0 (zero when h0 is NULL).
+ *   x, gate_a, gate_x, h: fp32 [B, C, T] (T contiguous, the scalar scan's
+ *     dense layout); a_param: fp32 [C]; segment_pos: int32 [B, T], shared by
+ *     the channels of a batch row, or NULL (no resets); h0: fp32 [B, C] or
+ *     NULL. All device pointers; any alignment (16-byte aligned rows with
+ *     T % 4 == 0 take the vector path).
+ * Returns SCAN_ERR_INVALID_ARG for negative sizes or a NULL required pointer,
+ * SCAN_ERR_UNSUPPORTED for C > 2^31 - 1, SCAN_ERR_CUDA if the launch fails.
+ * Asynchronous on `stream`; no workspace, no allocation. */
+scan_status rglru_fwd(const float* x, const float* gate_a, const float* gate_x,
+                      const float* a_param, const int32_t* segment_pos, const float* h0,
+                      float* h, int64_t B, int64_t C, int64_t T, cudaStream_t stream);
+
+/* Its backward for L = sum_t dh_t h_t, recomputing the gate terms from the
+ * logits (the same page: backward recomputation of the pointwise terms, the
+ * clipped square-root backward, partial a_param gradients followed by a
+ * reduction): the adjoint g_t = dh_t + a_{t+1} g_{t+1} (a_T = 0), then
+ *   dx_t = g_t m_t i_t, dgate_x_t = g_t m_t x_t i_t (1 - i_t)   (m = sqrt(1 - a^2)),
+ *   dL/da_t = g_t h_{t-1} + g_t i_t x_t (d sqrt(u)/du) (-2 a_t), u = 1 - a_t^2,
+ *     with d sqrt(u)/du taken at max(u, 1e-6) (the clip),
+ *   dgate_a_t = a_t dL/da_t 8 log(sigmoid(a_param)) r_t (1 - r_t),
+ *   da_param[c] = sigmoid(-a_param[c]) sum_{b,t} a_t dL/da_t 8 r_t,
+ *   dh0 = a_0 g_0; a reset step has dgate_a = 0 and m = 1.
+ *   h: the forward's output for the same inputs; dh: fp32 [B, C, T];
+ *   dx, dgate_a, dgate_x: fp32 [B, C, T]; da_param: fp32 [C], written (not
+ *   accumulated), summed over b and t in a fixed order; dh0: [B, C] or NULL.
+ * Errors as for rglru_fwd. Asynchronous on `stream`; no workspace. */
+scan_status rglru_bwd(const float* x, const float* gate_a, const float* gate_x,
+                      const float* a_param, const int32_t* segment_pos, const float* h0,
+                      const float* h, const float* dh, float* dx, float* dgate_a,
+                      float* dgate_x, float* da_param, float* dh0, int64_t B, int64_t C,
+                      int64_t T, cudaStream_t stream);
+
 /* One training step of dense rows (scan_fwd then scan_bwd, reverse = 0) whose
  * inputs and results are in host memory ([AST] the scan and its reversed-scan
  * backward; the rows of [B,C,T] are independent, so cutting between rows is

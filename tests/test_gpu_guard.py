@@ -14,8 +14,9 @@ kernel computes), with several KB on each side. After the call:
 Views start 16-byte aligned (the vector and tensor-copy paths) and, where the
 entry point accepts it, one element off (the scalar paths). Ragged T (1, 3,
 127, 129, 4097), fp32 and bf16, dense and packed, every scalar variant, the
-whole block envelope, the GDN chunk edges and the host-buffer step are covered (the entry
-point without allocation has its guard bands in its own test file).
+whole block envelope, the GDN chunk edges, the RG-LRU forward and backward and the
+host-buffer step are covered (the entry point without allocation has its guard bands in
+its own test file).
 """
 
 import pytest
@@ -264,6 +265,25 @@ def test_guard_gdn(lib, S, D, T, heads):
     lib.gdn_bwd(alpha, b, v, c, ref_ck, dout, out=tuple(g.t for g in outs))
     check_all([("o", o, ref_o), ("checkpoints", ck, ref_ck[:n_ck])] +
               list(zip(("dalpha", "db", "dv", "dc", "dh0"), outs, ref)), CONTRACTIONS)
+
+
+@pytest.mark.parametrize("T", [1, 3, 127, 128, 129, 4097])
+@pytest.mark.parametrize("shift", [0, 1])
+def test_guard_rglru(lib, T, shift):
+    """The RG-LRU forward's h and the backward's dx, dgate_a, dgate_x,
+    da_param and dh0, 16-byte aligned (vector path) and one element off."""
+    w = workloads.rglru(3, 5, T, seed=T + 3, docs=(1, 90), h0=True)
+    x, ga, gx, ap, dh, seg, h0 = (t.to(DEV) for t in (w.x, w.gate_a, w.gate_x, w.a_param, w.dh,
+                                                     w.segment_pos, w.h0))
+    ref_h = lib.rglru_fwd(x, ga, gx, ap, seg, h0)
+    ref = lib.rglru_bwd(x, ga, gx, ap, ref_h, dh, seg, h0)
+    h = Guarded(x.shape, torch.float32, shift)
+    lib.rglru_fwd(x, ga, gx, ap, seg, h0, out=h.t)
+    outs = (Guarded(x.shape, torch.float32, shift), Guarded(x.shape, torch.float32, shift),
+            Guarded(x.shape, torch.float32, shift), Guarded(ap.shape), Guarded(h0.shape))
+    lib.rglru_bwd(x, ga, gx, ap, ref_h, dh, seg, h0, out=tuple(g.t for g in outs))
+    check_all([("h", h, ref_h)] +
+              list(zip(("dx", "dgate_a", "dgate_x", "da_param", "dh0"), outs, ref)))
 
 
 @pytest.mark.parametrize("T,pieces", [(1000, 3), (1001, 4), (3, 2)])

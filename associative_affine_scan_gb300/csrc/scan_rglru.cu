@@ -52,9 +52,32 @@ struct RgParams {
   int64_t B, C, T;
 };
 
-__device__ __forceinline__ float rg_sigmoid(float z) { return 1.f / (1.f + expf(-z)); }
+// Per-step gates use the special-function unit (__expf, an approximate
+// reciprocal): their few-ulp relative errors scale i, r and 1 - a by
+// 1 + O(1e-6), which moves h by about as much, whatever the memory length
+// (a long memory sums 1 / (1 - a) steps, each off by (1 - a) 1e-6 at most).
+__device__ __forceinline__ float rg_sigmoid(float z) {
+  return __fdividef(1.f, 1.f + __expf(-z));
+}
 
-// log(sigmoid(p)) = -softplus(-p), without overflow for large |p|
+// 1 - exp(x) for x <= 0 to a few ulp of itself (x near 0 gives gates near
+// 1): for x > -1/8 the series -x (1 + x/2 (1 + x/3 (1 + x/4 (1 + x/5 (1 +
+// x/6))))) (the first omitted term is below 1e-9 of the sum), else 1 - e^x.
+__device__ __forceinline__ float rg_one_minus_exp(float x) {
+  float q = fmaf(x, 1.f / 6.f, 1.f);
+  q = fmaf(x * 0.2f, q, 1.f);
+  q = fmaf(x * 0.25f, q, 1.f);
+  q = fmaf(x * (1.f / 3.f), q, 1.f);
+  q = fmaf(x * 0.5f, q, 1.f);
+  const float series = -x * q;
+  return x > -0.125f ? series : 1.f - __expf(x);
+}
+
+// sqrt(u) for u >= 0 from the approximate reciprocal square root
+__device__ __forceinline__ float rg_sqrt(float u) { return u > 0.f ? u * rsqrtf(u) : 0.f; }
+
+// log(sigmoid(p)) = -softplus(-p), without overflow for large |p| (once per
+// channel: the library's accurate functions)
 __device__ __forceinline__ float rg_log_sigmoid(float p) {
   return p < 0.f ? p - log1pf(expf(p)) : -log1pf(expf(-p));
 }
@@ -109,16 +132,16 @@ struct RgStep {
   float a, u, r, i;  // u = 1 - a^2 (multiplier sqrt(u)); u = 1 at a reset
 };
 
-// a is formed as 1 - d with d = 1 - a = -expm1(log_a) accurate to its own
-// last bit, so that a near 1 (long memories) rounds to the nearest fp32 value
-// without a bias: the state carries a product of thousands of such gates,
-// and exp(log_a) rounded in fp32 came out 0.1 ulp high on average, which
+// a is formed as 1 - d with d = 1 - a accurate to a few ulp of itself, so
+// that a near 1 (long memories) rounds to the nearest fp32 value without a
+// bias: the state carries a product of thousands of such gates, and
+// exp(log_a) rounded in fp32 came out 0.1 ulp high on average, which
 // 23,000-step memories turned into errors of 1e-5 and more. 1 - a^2 = d (2 - d).
 __device__ __forceinline__ RgStep rg_gates(float ga, float gx, float ls, bool reset) {
   RgStep s;
   s.i = rg_sigmoid(gx);
   s.r = rg_sigmoid(ga);
-  const float d = -expm1f(kRgScale * s.r * ls);
+  const float d = rg_one_minus_exp(kRgScale * s.r * ls);
   s.a = reset ? 0.f : 1.f - d;
   s.u = reset ? 1.f : d * (2.f - d);
   return s;
@@ -160,7 +183,7 @@ __global__ void __launch_bounds__(32 * kRgMaxWarps) rglru_fwd_kernel(const RgPar
         const RgStep s = rg_gates(in.ga[j], in.gx[j], ls, in.seg[j] == 0);
         const bool valid = t + j < T;
         a[j] = valid ? s.a : 1.f;
-        w[j] = valid ? sqrtf(s.u) * s.i * in.x[j] : 0.f;
+        w[j] = valid ? rg_sqrt(s.u) * s.i * in.x[j] : 0.f;
       }
       float P = a[0], Q = w[0];
 #pragma unroll
@@ -277,7 +300,7 @@ __global__ void __launch_bounds__(32 * kRgMaxWarps) rglru_bwd_kernel(const RgPar
         const float hp = j > 0 ? hv[j > 0 ? j - 1 : 0] : hprev;
         const float xv = in.x[j], ig = s[j].i;
         const bool reset = in.seg[j] == 0;
-        const float mult = reset ? 1.f : sqrtf(s[j].u);
+        const float mult = reset ? 1.f : rg_sqrt(s[j].u);
         odx[j] = g * mult * ig;
         const float d_in = g * mult * xv;
         ogx[j] = d_in * ig * (1.f - ig);

@@ -315,7 +315,7 @@ def time_calls(fn, steps, warmup, flush, stream):
     return total / steps
 
 
-ROWS = ("dense_64k", "packed_bidir", "affine_4x4", "log_4k", "gdn_4k")
+ROWS = ("dense_64k", "packed_bidir", "affine_4x4", "log_4k", "gdn_4k", "rglru_4k")
 
 
 def measure_rows(args, dev, scan, names=ROWS, small=False, ceiling=None):
@@ -339,6 +339,7 @@ def measure_rows(args, dev, scan, names=ROWS, small=False, ceiling=None):
         "affine_4x4": lambda: _row_affine(scan, workloads, dev, steps, warm, flush, stream),
         "log_4k": lambda: _row_log(scan, workloads, dev, steps, warm, flush, stream),
         "gdn_4k": lambda: _row_gdn(scan, workloads, dev, steps, warm, flush, stream),
+        "rglru_4k": lambda: _row_rglru(scan, workloads, dev, steps, warm, flush, stream),
     }
     for name in names:
         try:
@@ -450,6 +451,25 @@ def _row_log(scan, workloads, dev, steps, warm, flush, stream):
                        stream)
     return {"elems": n, "fwd_ms": l_ms, "bwd_ms": lb_ms,
             "fwd_gbs": n * 12 / l_ms / 1e6, "bwd_gbs": n * 24 / lb_ms / 1e6}
+
+
+def _row_rglru(scan, workloads, dev, steps, warm, flush, stream):
+    # RG-LRU: fwd reads x, gate_a, gate_x and writes h (16 B/elem); bwd reads
+    # x, gate_a, gate_x, h, dh and writes dx, dgate_a, dgate_x (32 B/elem);
+    # segment_pos (4 B per (b, t), shared by the channels) and a_param are
+    # below 0.1 % and not counted
+    w = workloads.rglru_4k(seed=0)
+    x, ga, gx, ap, dh, seg = (t.to(dev) for t in (w.x, w.gate_a, w.gate_x, w.a_param, w.dh,
+                                                 w.segment_pos))
+    h = scan.rglru_fwd(x, ga, gx, ap, seg)
+    n = x.numel()
+    f_ms = time_calls(lambda: scan.rglru_fwd(x, ga, gx, ap, seg, out=h), steps, warm, flush,
+                      stream)
+    g = scan.rglru_bwd(x, ga, gx, ap, h, dh, seg)
+    b_ms = time_calls(lambda: scan.rglru_bwd(x, ga, gx, ap, h, dh, seg, out=g), steps, warm,
+                      flush, stream)
+    return {"elems": n, "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_gbs": n * 16 / f_ms / 1e6, "bwd_gbs": n * 32 / b_ms / 1e6}
 
 
 def _row_affine(scan, workloads, dev, steps, warm, flush, stream):

@@ -17,12 +17,14 @@ LIB = os.path.join(HERE, "libscan.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
-# Per-unit extras. The log-space forward spends most of its issue slots on
-# exponentials of the max-shifted log-sum-exp; with subnormals flushed to zero
-# __expf needs no rescaling around the special-function unit (a subnormal
-# exponential only ever adds to a sum of at least one, or is an output below
-# 1e-38). Measured 10 % faster on the 8 x 1536 x 4096 log forward.
-UNIT_FLAGS = {"scan_log_fwd.cu": ["-ftz=true"]}
+# Per-unit extras: subnormals flushed to zero, so that the special-function
+# unit's exponentials, reciprocals and square roots need no rescaling around
+# them. The log-space forward spends most of its issue slots on exponentials of
+# the max-shifted log-sum-exp (a subnormal exponential only ever adds to a sum
+# of at least one, or is an output below 1e-38; measured 10 % faster on the
+# 8 x 1536 x 4096 log forward); the RG-LRU kernels on their per-step gates (a
+# flushed gate term is below 1e-38, and outputs are compared with max(1, |h|)).
+UNIT_FLAGS = {"scan_log_fwd.cu": ["-ftz=true"], "scan_rglru.cu": ["-ftz=true"]}
 
 
 def nvcc() -> str:

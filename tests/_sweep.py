@@ -43,6 +43,14 @@ def max_rel(got, ref, scale=None) -> float:
     return float(np.max(np.abs(got - ref) / den))
 
 
+def worst(a: float, b: float) -> float:
+    """The larger of two errors; NaN if either is NaN (Python's max would
+    drop a NaN that is not its first argument)."""
+    if a != a or b != b:
+        return float("nan")
+    return max(a, b)
+
+
 def batches(n: int, size: int):
     return [(i, min(n, i + size)) for i in range(0, n, size)]
 
@@ -57,7 +65,7 @@ def sweep(n: int, size: int, check) -> dict:
     out: dict = {}
     for r in results:
         for k, v in r.items():
-            out[k] = max(out.get(k, 0.0), v)
+            out[k] = worst(out.get(k, 0.0), v)
     out["batches"] = len(parts)
     out["items"] = n
     return out

@@ -20,7 +20,7 @@ import pytest
 import torch
 
 import oracle
-from _sweep import sweep
+from _sweep import sweep, worst
 from associative_affine_scan_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -58,9 +58,9 @@ def check(lib, w, plain_gate=True):
         errs[name] = err(got, ref, sc)
         plain[name] = err(got, ref)
     print("gdn", tuple(w.b.shape), "term-scale error", errs, "plain-metric error", plain)
-    assert max(errs.values()) <= TOL, errs
+    assert all(v <= TOL for v in errs.values()), errs
     if plain_gate:
-        assert max(plain[k] for k in GRADS) <= TOL_GRAD_PLAIN, plain
+        assert all(plain[k] <= TOL_GRAD_PLAIN for k in GRADS), plain
 
 
 # T covers the backward's 32-step chunks (31, 32, 33), the forward's 64-step
@@ -139,14 +139,14 @@ def test_gdn_4k_all_heads(lib):
                 vals.append((name, err(sl(got), ref, sc)))
                 vals.append((name + "_plain", err(sl(got), ref)))
             for k, val in vals:
-                e[k] = max(e.get(k, 0.0), val)
+                e[k] = worst(e.get(k, 0.0), val)
         return e
 
     errs = sweep(B * H, 4, check)
     print("gdn_4k all heads", errs)
     assert errs["items"] == B * H
-    assert max(errs[k] for k in ("o",) + GRADS) <= TOL, errs
-    assert max(errs[k + "_plain"] for k in GRADS) <= TOL_GRAD_PLAIN, errs
+    assert all(errs[k] <= TOL for k in ("o",) + GRADS), errs
+    assert all(errs[k + "_plain"] <= TOL_GRAD_PLAIN for k in GRADS), errs
 
 
 @pytest.mark.parametrize("T", [64, 200])

@@ -18,7 +18,7 @@ import torch
 from scipy.special import expit
 
 import oracle
-from _sweep import as_f64, max_rel, sweep
+from _sweep import as_f64, max_rel, sweep, worst
 from associative_affine_scan_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -34,7 +34,11 @@ def dap_scale(ga, ap, dga_ref, seg):
     ap = as_f64(ap)
     r = expit(ga)
     ls = np.log(expit(ap))[None, :, None]
-    term = np.abs(np.asarray(dga_ref) / (ls * (1.0 - r)))
+    den = ls * (1.0 - r)
+    # where r(1 - r) or log(sigmoid(a_param)) is 0 in fp64 the term cannot be
+    # read back from dgate_a; it counts as 0 (a smaller scale: a stricter gate)
+    safe = np.where(den == 0.0, 1.0, den)
+    term = np.where(den == 0.0, 0.0, np.abs(np.asarray(dga_ref) / safe))
     if seg is not None:
         term = np.where((as_f64(seg) == 0)[:, None, :], 0.0, term)
     return term.sum(axis=(0, 2)) * expit(-ap)
@@ -103,7 +107,7 @@ def test_rglru_shapes(lib, B, C, T, docs):
         w.h0 = h0
         h, g = run(lib, w)
         errs = compare(w, h, g)
-        assert max(errs.values()) <= TOL, errs
+        assert all(v <= TOL for v in errs.values()), errs
 
 
 @pytest.mark.parametrize("shift", [1, 2])
@@ -113,7 +117,7 @@ def test_rglru_unaligned_inputs_take_the_scalar_path(lib, shift):
         w = workloads.rglru(2, 3, T, seed=T + shift, docs=(1, 40), h0=True)
         h, g = run(lib, w, shift=shift)
         errs = compare(w, h, g)
-        assert max(errs.values()) <= TOL, errs
+        assert all(v <= TOL for v in errs.values()), errs
 
 
 def test_rglru_gate_extremes(lib):
@@ -129,7 +133,7 @@ def test_rglru_gate_extremes(lib):
     h, g = run(lib, w)
     errs = compare(w, h, g)
     assert all(np.isfinite(as_f64(t)).all() for t in [h] + g)
-    assert max(errs.values()) <= TOL, errs
+    assert all(v <= TOL for v in errs.values()), errs
 
 
 def test_rglru_full_4k_all_rows(lib):
@@ -154,7 +158,7 @@ def test_rglru_full_4k_all_rows(lib):
             e = errors(sl(h), (sl(dx), sl(dga), sl(dgx), None, dh0[b:b + 1, c0:c0 + per]),
                        ref_h, rg, sc_h, sc_g)
             for k, v in e.items():
-                out[k] = max(out.get(k, 0.0), v)
+                out[k] = worst(out.get(k, 0.0), v)
             out[f"dap_{b}_{c0}"] = rg[3]
             out[f"dsc_{b}_{c0}"] = dap_scale(sl(w.gate_a), ap, rg[1], seg)
         return out
@@ -179,4 +183,4 @@ def test_rglru_full_4k_all_rows(lib):
     errs["da_param"] = max_rel(dap, ref_dap, scale)
     print("rglru_4k all rows", errs)
     assert errs["items"] == B * nb
-    assert max(errs[k] for k in ("h", "dx", "dgate_a", "dgate_x", "dh0", "da_param")) <= TOL, errs
+    assert all(errs[k] <= TOL for k in ("h", "dx", "dgate_a", "dgate_x", "dh0", "da_param")), errs

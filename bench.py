@@ -274,6 +274,20 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
+    # the other carry schemes on the same step (the planner chose stationary)
+    variants = {}
+    if not args.no_rows:
+        for name, var in (("lookback", scan.SCAN_VARIANT_LOOKBACK),
+                          ("stream", scan.SCAN_VARIANT_STREAM)):
+            o = {"variant": var}
+            vf = time_calls(lambda: scan.scan_fwd(a, x, h0, out=h, opts=o), args.steps, 3, flush,
+                            stream)
+            vb = time_calls(lambda: scan.scan_bwd(a, h, dh, h0, out=(da, dx, dh0), opts=o),
+                            args.steps, 3, flush, stream)
+            variants[name] = {"fwd_ms": vf, "bwd_ms": vb, "step_ms": vf + vb}
+        if scan.scan_get_device_status(dev, stream) != scan.SCAN_OK:
+            raise RuntimeError("device status not OK after the variant timings")
+
     extra, copy = {}, None
     if not args.no_rows:
         del a, x, dh, h, da, dx, dh0, flush
@@ -281,9 +295,12 @@ def run_ours(args, world, rank, local):
         copy = measure_copy(dev, scan, max(3, min(args.steps, 10)))
         extra = measure_rows(args, dev, scan, ceiling=copy["ceiling_gbs"])
 
+    spread = {"step_median_ms": float(np.median(step_ms)), "step_min_ms": min(step_ms),
+              "fwd_median_ms": float(np.median(fwd_ms)), "fwd_min_ms": min(fwd_ms),
+              "bwd_median_ms": float(np.median(bwd_ms)), "bwd_min_ms": min(bwd_ms)}
     return dict(n=n, B=B, C=C, T=T, ms=ms, fwd_ms=fwd_avg, bwd_ms=bwd_avg, wall=wall,
                 clocks=clocks, e2e_ms=e2e_ms, bytes_in=bytes_in, bytes_out=bytes_out,
-                w=w, extra=extra, copy=copy)
+                w=w, extra=extra, copy=copy, spread=spread, variants=variants)
 
 
 def time_calls(fn, steps, warmup, flush, stream):
@@ -665,6 +682,11 @@ def main():
         "baseline_context": {"ms": pages_ms, "hardware": "H100 80GB",
                              "source": "associative_scan_triton README, kernel-level Fwd+Bwd"},
     }
+    line["timing_spread"] = r["spread"]  # this rank's median and minimum over the timed steps
+    if r["variants"]:
+        line["variants"] = dict(
+            {"stationary (planner)": {"fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"],
+                                      "step_ms": r["ms"]}}, **r["variants"])
     if r["copy"]:
         line["copy"] = r["copy"]
         line["roofline"]["frac_of_copy_kernel"] = bwd_gbs / r["copy"]["ceiling_gbs"]

@@ -136,6 +136,23 @@ def test_rglru_gate_extremes(lib):
     assert all(v <= TOL for v in errs.values()), errs
 
 
+@pytest.mark.parametrize("T", [256, 300, 515])
+def test_rglru_resets_at_chunk_edges(lib, T):
+    """Resets at the steps either side of the 128-step chunk edges, at the
+    last step, and at t = 0 in one batch row (h0 erased there, dh0 = 0)."""
+    w = workloads.rglru(2, 3, T, seed=T + 9, docs=None, h0=True)
+    seg = torch.arange(1, T + 1, dtype=torch.int32).repeat(2, 1)
+    for t in (1, 127, 128, 129, 255, 256, T - 1):
+        if t < T:
+            seg[0, t] = 0
+    seg[1, 0] = 0
+    w.segment_pos = seg
+    h, g = run(lib, w)
+    errs = compare(w, h, g)
+    assert all(v <= TOL for v in errs.values()), errs
+    assert torch.all(g[4][1] == 0.0)  # dh0 of the row that resets at t = 0
+
+
 def test_rglru_full_4k_all_rows(lib):
     """Every output of the 8 x 1536 x 4096 RG-LRU workload (documents of
     512..8192 steps) against the oracle, channel batches per batch row."""

@@ -131,9 +131,10 @@ _SIGS = {
     "scan_fwd_noalloc": ([_vp, _vp, _vp, _vp, _i32, _vp, _i64, _i64, _i64, ctypes.c_int, _i32,
                           _vp], ctypes.c_int),
     "scan_noalloc_device_status": ([_vp], ctypes.c_int),
-    "rglru_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp], ctypes.c_int),
+    "rglru_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp],
+                  ctypes.c_int),
     "rglru_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
-                   _i64, _vp], ctypes.c_int),
+                   _i64, ctypes.c_int, _vp], ctypes.c_int),
     "scan_copy": ([_vp, _vp, _sz, _i32, _vp, _vp], ctypes.c_int),
 }
 
@@ -738,13 +739,13 @@ def scan_fwd_noalloc(a, x, h0=None, cu_seqlens=None, reverse=False, *, out=None,
 
 
 def _rglru_args(x, gate_a, gate_x, a_param, segment_pos, h0):
-    _need(x, "x", dtype=torch.float32)
+    _need(x, "x")
     if x.dim() != 3:
         raise ValueError("x: expected [B, C, T]")
     dev = x.device
     B, C, T = x.shape
-    _need(gate_a, "gate_a", dtype=torch.float32, shape=x.shape, device=dev)
-    _need(gate_x, "gate_x", dtype=torch.float32, shape=x.shape, device=dev)
+    _need(gate_a, "gate_a", dtype=x.dtype, shape=x.shape, device=dev)
+    _need(gate_x, "gate_x", dtype=x.dtype, shape=x.shape, device=dev)
     _need(a_param, "a_param", dtype=torch.float32, shape=(C,), device=dev)
     _need(segment_pos, "segment_pos", dtype=torch.int32, shape=(B, T), device=dev)
     _need(h0, "h0", dtype=torch.float32, shape=(B, C), device=dev)
@@ -754,13 +755,15 @@ def _rglru_args(x, gate_a, gate_x, a_param, segment_pos, h0):
 def rglru_fwd(x, gate_a, gate_x, a_param, segment_pos=None, h0=None, *, out=None, stream=None):
     """RG-LRU gate preparation and scan: h_t = a_t h_{t-1} + sqrt(1 - a_t^2)
     sigmoid(gate_x_t) x_t, a_t = sigmoid(a_param)^(8 sigmoid(gate_a_t)), a reset
-    where segment_pos == 0. x, gate_a, gate_x [B, C, T]; a_param [C];
-    segment_pos int32 [B, T] or None; h0 [B, C] or None. Returns h [B, C, T]."""
+    where segment_pos == 0. x, gate_a, gate_x [B, C, T] fp32 or bf16; a_param
+    [C]; segment_pos int32 [B, T] or None; h0 [B, C] or None. Returns h
+    [B, C, T] (fp32)."""
     dev, B, C, T = _rglru_args(x, gate_a, gate_x, a_param, segment_pos, h0)
+    dt = _dtype_code(x)
     h = out if out is not None else torch.empty(x.shape, dtype=torch.float32, device=dev)
     _need(h, "out", dtype=torch.float32, shape=x.shape, device=dev)
     st = _call(dev, "rglru_fwd", _ptr(x), _ptr(gate_a), _ptr(gate_x), _ptr(a_param),
-               _ptr(segment_pos), _ptr(h0), _ptr(h), B, C, T, _stream(stream, dev))
+               _ptr(segment_pos), _ptr(h0), _ptr(h), B, C, T, dt, _stream(stream, dev))
     _check(st, "rglru_fwd")
     return h
 
@@ -768,23 +771,25 @@ def rglru_fwd(x, gate_a, gate_x, a_param, segment_pos=None, h0=None, *, out=None
 def rglru_bwd(x, gate_a, gate_x, a_param, h, dh, segment_pos=None, h0=None, *, out=None,
               stream=None, need_dh0=True):
     """Gradients of L = sum dh * h for h = rglru_fwd(...): (dx, dgate_a,
-    dgate_x, da_param, dh0); dh0 is None when need_dh0 is False."""
+    dgate_x, da_param, dh0), the first three in x's dtype; dh0 is None when
+    need_dh0 is False."""
     dev, B, C, T = _rglru_args(x, gate_a, gate_x, a_param, segment_pos, h0)
+    dt = _dtype_code(x)
     _need(h, "h", dtype=torch.float32, shape=x.shape, device=dev)
     _need(dh, "dh", dtype=torch.float32, shape=x.shape, device=dev)
     if out is not None:
         dx, dga, dgx, dap, dh0 = out
     else:
-        dx, dga, dgx = (torch.empty(x.shape, dtype=torch.float32, device=dev) for _ in range(3))
+        dx, dga, dgx = (torch.empty(x.shape, dtype=x.dtype, device=dev) for _ in range(3))
         dap = torch.empty(C, dtype=torch.float32, device=dev)
         dh0 = torch.empty(B, C, dtype=torch.float32, device=dev) if need_dh0 else None
     for t, name in ((dx, "dx"), (dga, "dgate_a"), (dgx, "dgate_x")):
-        _need(t, name, dtype=torch.float32, shape=x.shape, device=dev)
+        _need(t, name, dtype=x.dtype, shape=x.shape, device=dev)
     _need(dap, "da_param", dtype=torch.float32, shape=(C,), device=dev)
     _need(dh0, "dh0", dtype=torch.float32, shape=(B, C), device=dev)
     st = _call(dev, "rglru_bwd", _ptr(x), _ptr(gate_a), _ptr(gate_x), _ptr(a_param),
                _ptr(segment_pos), _ptr(h0), _ptr(h), _ptr(dh), _ptr(dx), _ptr(dga), _ptr(dgx),
-               _ptr(dap), _ptr(dh0), B, C, T, _stream(stream, dev))
+               _ptr(dap), _ptr(dh0), B, C, T, dt, _stream(stream, dev))
     _check(st, "rglru_bwd")
     return dx, dga, dgx, dap, dh0
 

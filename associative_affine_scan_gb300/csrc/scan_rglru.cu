@@ -23,9 +23,11 @@
 // 8 x 1536 x 4096 rows the forward ran 0.1505 -> 0.1432 ms, the backward
 // (without the forward's look-ahead, which held it at 128 registers) 0.307 ->
 // 0.283 ms, a few spilled words included.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "../../include/libscan.h"
 #include "scan_internal.h"
@@ -40,17 +42,17 @@ constexpr int kRgChunk = 128;      // steps per chunk: 4 per lane
 constexpr int kRgMaxWarps = 8;     // warps (rows of one channel) per block
 
 struct RgParams {
-  const float* x;
-  const float* ga;  // gate_a logits
-  const float* gx;  // gate_x logits
+  const void* x;    // input dtype (fp32 or bf16), as ga, gx and the three gradients below
+  const void* ga;   // gate_a logits
+  const void* gx;   // gate_x logits
   const float* ap;  // a_param [C]
   const int32_t* seg;  // segment_pos [B, T] or null
   const float* h0;     // [B, C] or null
   float* h;            // forward output / backward input [B, C, T]
   const float* dh;
-  float* dx;
-  float* dga;
-  float* dgx;
+  void* dx;
+  void* dga;
+  void* dgx;
   float* dap;  // [C]
   float* dh0;  // [B, C] or null
   int64_t B, C, T;
@@ -131,6 +133,45 @@ __device__ __forceinline__ void rg_st(float* row, int64_t t, int64_t T, const fl
   }
 }
 
+// The same for the input dtype TI (fp32 or bf16: 8-byte vectors of 4 bf16,
+// rounded to nearest on store).
+template <typename TI, bool VEC, bool FULL>
+__device__ __forceinline__ void rg_ld_in(const void* base, int64_t off, int64_t t, int64_t T,
+                                         float (&v)[4]) {
+  const TI* row = static_cast<const TI*>(base) + off;
+  if constexpr (std::is_same<TI, float>::value) {
+    rg_ld<VEC, FULL>(row, t, T, v);
+  } else if (VEC && (FULL || t + 4 <= T)) {
+    const uint2 q = *reinterpret_cast<const uint2*>(row + t);
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xffff0000u);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = FULL || t + j < T ? __bfloat162float(row[t + j]) : 0.f;
+  }
+}
+
+template <typename TI, bool VEC, bool FULL>
+__device__ __forceinline__ void rg_st_in(void* base, int64_t off, int64_t t, int64_t T,
+                                         const float (&v)[4]) {
+  TI* row = static_cast<TI*>(base) + off;
+  if constexpr (std::is_same<TI, float>::value) {
+    rg_st<VEC, FULL>(row, t, T, v);
+  } else if (VEC && (FULL || t + 4 <= T)) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+    __stcs(reinterpret_cast<uint2*>(row + t),
+           make_uint2(*reinterpret_cast<const unsigned*>(&lo),
+                      *reinterpret_cast<const unsigned*>(&hi)));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (FULL || t + j < T) row[t + j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
 // The gate terms of one step: transition a, the write's factors. A reset
 // (segment_pos == 0) has a = 0 and multiplier 1.
 struct RgStep {
@@ -161,12 +202,12 @@ struct RgIn {
   float dh[BWD ? 4 : 1], h[BWD ? 4 : 1];
 };
 
-template <bool VEC, bool FULL, bool BWD>
+template <typename TI, bool VEC, bool FULL, bool BWD>
 __device__ __forceinline__ void rg_load(const RgParams& p, int64_t base, const int32_t* seg,
                                         int64_t t, RgIn<BWD>& in) {
-  rg_ld<VEC, FULL>(p.x + base, t, p.T, in.x);
-  rg_ld<VEC, FULL>(p.ga + base, t, p.T, in.ga);
-  rg_ld<VEC, FULL>(p.gx + base, t, p.T, in.gx);
+  rg_ld_in<TI, VEC, FULL>(p.x, base, t, p.T, in.x);
+  rg_ld_in<TI, VEC, FULL>(p.ga, base, t, p.T, in.ga);
+  rg_ld_in<TI, VEC, FULL>(p.gx, base, t, p.T, in.gx);
   rg_ld_seg<VEC, FULL>(seg, t, p.T, in.seg);
   if constexpr (BWD) {
     rg_ld<VEC, FULL>(p.dh + base, t, p.T, in.dh);
@@ -221,7 +262,7 @@ __device__ __forceinline__ void rg_fwd_chunk(const RgParams& p, int64_t base, in
   carry = __shfl_sync(kRgFull, st, 31);
 }
 
-template <bool VEC>
+template <typename TI, bool VEC>
 __global__ void __launch_bounds__(32 * kRgMaxWarps, 4) rglru_fwd_kernel(const RgParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int64_t c = blockIdx.x, T = p.T;
@@ -233,13 +274,13 @@ __global__ void __launch_bounds__(32 * kRgMaxWarps, 4) rglru_fwd_kernel(const Rg
     const int32_t* seg = p.seg ? p.seg + b * T : nullptr;
     float carry = p.h0 ? p.h0[row] : 0.f;
     RgIn<false> in, nx;
-    if (nfull > 0) rg_load<VEC, true>(p, base, seg, 4 * lane, in);
-    else rg_load<VEC, false>(p, base, seg, 4 * lane, in);
+    if (nfull > 0) rg_load<TI, VEC, true>(p, base, seg, 4 * lane, in);
+    else rg_load<TI, VEC, false>(p, base, seg, 4 * lane, in);
     for (int64_t k = 0; k < nfull; ++k) {
       const int64_t t = k * kRgChunk + 4 * lane;
       // the next chunk's loads go out before this one is computed
-      if (k + 1 < nfull) rg_load<VEC, true>(p, base, seg, t + kRgChunk, nx);
-      else if (tail) rg_load<VEC, false>(p, base, seg, t + kRgChunk, nx);
+      if (k + 1 < nfull) rg_load<TI, VEC, true>(p, base, seg, t + kRgChunk, nx);
+      else if (tail) rg_load<TI, VEC, false>(p, base, seg, t + kRgChunk, nx);
       rg_fwd_chunk<VEC, true>(p, base, t, in, ls, lane, carry);
       in = nx;
     }
@@ -257,7 +298,7 @@ __global__ void __launch_bounds__(32 * kRgMaxWarps, 4) rglru_fwd_kernel(const Rg
 // forward output h (h0 before the first step). carry: g at the first step of
 // the chunk after this one, left at g at this chunk's first step; a_after: a
 // at that step (0 past the end), likewise.
-template <bool VEC, bool FULL>
+template <typename TI, bool VEC, bool FULL>
 __device__ __forceinline__ void rg_bwd_chunk(const RgParams& p, int64_t base, int64_t t0,
                                              RgIn<true>& in, float ls, float init, int lane,
                                              float& carry, float& a_after, float& dls) {
@@ -318,14 +359,14 @@ __device__ __forceinline__ void rg_bwd_chunk(const RgParams& p, int64_t base, in
     oga[j] = dla * kRgScale * ls * r * (1.f - r);
     dls = fmaf(dla * kRgScale, r, dls);
   }
-  rg_st<VEC, FULL>(p.dx + base, t, T, odx);
-  rg_st<VEC, FULL>(p.dga + base, t, T, oga);
-  rg_st<VEC, FULL>(p.dgx + base, t, T, ogx);
+  rg_st_in<TI, VEC, FULL>(p.dx, base, t, T, odx);
+  rg_st_in<TI, VEC, FULL>(p.dga, base, t, T, oga);
+  rg_st_in<TI, VEC, FULL>(p.dgx, base, t, T, ogx);
   carry = __shfl_sync(kRgFull, g, 0);  // g at step t0
   a_after = __shfl_sync(kRgFull, s[0].a, 0);
 }
 
-template <bool VEC>
+template <typename TI, bool VEC>
 __global__ void __launch_bounds__(32 * kRgMaxWarps, 4) rglru_bwd_kernel(const RgParams p) {
   __shared__ float s_part[kRgMaxWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -342,13 +383,13 @@ __global__ void __launch_bounds__(32 * kRgMaxWarps, 4) rglru_bwd_kernel(const Rg
     RgIn<true> in;
     if (tail) {  // the partial last chunk first
       const int64_t t0 = nfull * kRgChunk;
-      rg_load<VEC, false>(p, base, seg, t0 + 4 * lane, in);
-      rg_bwd_chunk<VEC, false>(p, base, t0, in, ls, init, lane, carry, a_after, dls);
+      rg_load<TI, VEC, false>(p, base, seg, t0 + 4 * lane, in);
+      rg_bwd_chunk<TI, VEC, false>(p, base, t0, in, ls, init, lane, carry, a_after, dls);
     }
     for (int64_t k = nfull - 1; k >= 0; --k) {
       const int64_t t0 = k * kRgChunk;
-      rg_load<VEC, true>(p, base, seg, t0 + 4 * lane, in);
-      rg_bwd_chunk<VEC, true>(p, base, t0, in, ls, init, lane, carry, a_after, dls);
+      rg_load<TI, VEC, true>(p, base, seg, t0 + 4 * lane, in);
+      rg_bwd_chunk<TI, VEC, true>(p, base, t0, in, ls, init, lane, carry, a_after, dls);
     }
     if (p.dh0 && lane == 0) p.dh0[row] = a_after * carry;  // a_0 g_0 (0 when T == 0)
   }
@@ -364,19 +405,37 @@ __global__ void __launch_bounds__(32 * kRgMaxWarps, 4) rglru_bwd_kernel(const Rg
   }
 }
 
-bool al16(const void* q) { return q == nullptr || ((uintptr_t)q % 16) == 0; }
+bool aligned(const void* q, size_t n) { return q == nullptr || ((uintptr_t)q % n) == 0; }
 
-cudaError_t rg_launch(const RgParams& p, bool fwd, bool vec, cudaStream_t s) {
+template <typename TI>
+cudaError_t rg_launch_t(const RgParams& p, bool fwd, bool vec, cudaStream_t s) {
   const int nw = (int)(p.B < kRgMaxWarps ? p.B : kRgMaxWarps);
   const dim3 grid((unsigned)p.C), block(32u * (unsigned)nw);
   if (fwd) {
-    if (vec) rglru_fwd_kernel<true><<<grid, block, 0, s>>>(p);
-    else rglru_fwd_kernel<false><<<grid, block, 0, s>>>(p);
+    if (vec) rglru_fwd_kernel<TI, true><<<grid, block, 0, s>>>(p);
+    else rglru_fwd_kernel<TI, false><<<grid, block, 0, s>>>(p);
   } else {
-    if (vec) rglru_bwd_kernel<true><<<grid, block, 0, s>>>(p);
-    else rglru_bwd_kernel<false><<<grid, block, 0, s>>>(p);
+    if (vec) rglru_bwd_kernel<TI, true><<<grid, block, 0, s>>>(p);
+    else rglru_bwd_kernel<TI, false><<<grid, block, 0, s>>>(p);
   }
   return cudaGetLastError();
+}
+
+// The vector path: rows of T % 4 == 0 elements from base pointers aligned to
+// one 4-element vector of their type (16 bytes fp32, 8 bytes bf16).
+bool rg_vec(const RgParams& p, scan_dtype dt, bool bwd) {
+  const size_t vi = dt == SCAN_BF16 ? 8 : 16;
+  bool ok = p.T % 4 == 0 && aligned(p.x, vi) && aligned(p.ga, vi) && aligned(p.gx, vi) &&
+            aligned(p.h, 16) && aligned(p.seg, 16);
+  if (bwd) ok = ok && aligned(p.dh, 16) && aligned(p.dx, vi) && aligned(p.dga, vi) &&
+                aligned(p.dgx, vi);
+  return ok;
+}
+
+cudaError_t rg_launch(const RgParams& p, scan_dtype dt, bool fwd, cudaStream_t s) {
+  const bool vec = rg_vec(p, dt, !fwd);
+  return dt == SCAN_BF16 ? rg_launch_t<__nv_bfloat16>(p, fwd, vec, s)
+                         : rg_launch_t<float>(p, fwd, vec, s);
 }
 
 }  // namespace
@@ -386,9 +445,10 @@ using namespace scan;
 
 extern "C" {
 
-scan_status rglru_fwd(const float* x, const float* gate_a, const float* gate_x,
+scan_status rglru_fwd(const void* x, const void* gate_a, const void* gate_x,
                       const float* a_param, const int32_t* segment_pos, const float* h0, float* h,
-                      int64_t B, int64_t C, int64_t T, cudaStream_t stream) {
+                      int64_t B, int64_t C, int64_t T, scan_dtype dt, cudaStream_t stream) {
+  if (dt != SCAN_F32 && dt != SCAN_BF16) return SCAN_ERR_INVALID_ARG;
   if (B < 0 || C < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
   if (C > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
   if (B * C * T == 0) return SCAN_OK;
@@ -404,16 +464,15 @@ scan_status rglru_fwd(const float* x, const float* gate_a, const float* gate_x,
   p.B = B;
   p.C = C;
   p.T = T;
-  const bool vec = T % 4 == 0 && al16(x) && al16(gate_a) && al16(gate_x) && al16(h) &&
-                   al16(segment_pos);
-  return rg_launch(p, true, vec, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
+  return rg_launch(p, dt, true, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
 }
 
-scan_status rglru_bwd(const float* x, const float* gate_a, const float* gate_x,
+scan_status rglru_bwd(const void* x, const void* gate_a, const void* gate_x,
                       const float* a_param, const int32_t* segment_pos, const float* h0,
-                      const float* h, const float* dh, float* dx, float* dgate_a, float* dgate_x,
+                      const float* h, const float* dh, void* dx, void* dgate_a, void* dgate_x,
                       float* da_param, float* dh0, int64_t B, int64_t C, int64_t T,
-                      cudaStream_t stream) {
+                      scan_dtype dt, cudaStream_t stream) {
+  if (dt != SCAN_F32 && dt != SCAN_BF16) return SCAN_ERR_INVALID_ARG;
   if (B < 0 || C < 0 || T < 0) return SCAN_ERR_INVALID_ARG;
   if (C > 0x7fffffffLL) return SCAN_ERR_UNSUPPORTED;
   if (C == 0) return SCAN_OK;
@@ -442,9 +501,7 @@ scan_status rglru_bwd(const float* x, const float* gate_a, const float* gate_x,
   p.B = B;
   p.C = C;
   p.T = T;
-  const bool vec = T % 4 == 0 && al16(x) && al16(gate_a) && al16(gate_x) && al16(h) &&
-                   al16(dh) && al16(dx) && al16(dgate_a) && al16(dgate_x) && al16(segment_pos);
-  return rg_launch(p, false, vec, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
+  return rg_launch(p, dt, false, stream) == cudaSuccess ? SCAN_OK : SCAN_ERR_CUDA;
 }
 
 }  // extern "C"

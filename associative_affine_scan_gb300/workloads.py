@@ -307,14 +307,14 @@ def document_positions(B: int, T: int, lo: int, hi: int, g: torch.Generator) -> 
 
 
 def rglru(B: int, C: int, T: int, seed: int = 0, *, docs: Optional[tuple] = (512, 8192),
-          h0: bool = False, name: str = "rglru") -> RglruWorkload:
-    """x, gate_a, gate_x ~ N(0,1); a_param ~ U(4.3, 9); segment_pos of documents
-    with lengths ~ U{docs} (None: no resets); dh ~ N(0,1); h0 ~ N(0,1) if asked.
-    Drawn in that order from one generator."""
+          h0: bool = False, dtype=torch.float32, name: str = "rglru") -> RglruWorkload:
+    """x, gate_a, gate_x ~ N(0,1) (stored in `dtype`); a_param ~ U(4.3, 9);
+    segment_pos of documents with lengths ~ U{docs} (None: no resets);
+    dh ~ N(0,1); h0 ~ N(0,1) if asked. Drawn in that order from one generator."""
     g = _gen(seed)
-    x = torch.randn((B, C, T), generator=g)
-    ga = torch.randn((B, C, T), generator=g)
-    gx = torch.randn((B, C, T), generator=g)
+    x = torch.randn((B, C, T), generator=g).to(dtype)
+    ga = torch.randn((B, C, T), generator=g).to(dtype)
+    gx = torch.randn((B, C, T), generator=g).to(dtype)
     ap = 4.3 + 4.7 * torch.rand((C,), generator=g)
     seg = document_positions(B, T, docs[0], docs[1], g) if docs else None
     dh = torch.randn((B, C, T), generator=g)

@@ -334,17 +334,21 @@ scan_status gdn_bwd(const float* alpha, const float* b, const float* v,
  *   write_t = sqrt(1 - a_t^2) i_t x_t;
  *   where segment_pos[b, t] == 0 (a reset): a_t = 0, write_t = i_t x_t;
  *   h_t = a_t h_{t-1} + write_t, h_{-1} = h0 (zero when h0 is NULL).
- *   x, gate_a, gate_x, h: fp32 [B, C, T] (T contiguous, the scalar scan's
- *     dense layout); a_param: fp32 [C]; segment_pos: int32 [B, T], shared by
- *     the channels of a batch row, or NULL (no resets); h0: fp32 [B, C] or
- *     NULL. All device pointers; any alignment (16-byte aligned rows with
- *     T % 4 == 0 take the vector path).
- * Returns SCAN_ERR_INVALID_ARG for negative sizes or a NULL required pointer,
+ *   x, gate_a, gate_x: [B, C, T] of dtype dt (SCAN_F32, or SCAN_BF16: the
+ *     page's BF16 boundaries, read into fp32 registers), T contiguous (the
+ *     scalar scan's dense layout); h: fp32 [B, C, T] (the state is carried in
+ *     fp32 either way); a_param: fp32 [C]; segment_pos: int32 [B, T], shared
+ *     by the channels of a batch row, or NULL (no resets); h0: fp32 [B, C] or
+ *     NULL. All device pointers; any alignment (rows of T % 4 == 0 elements
+ *     from pointers aligned to four elements take the vector path).
+ * Returns SCAN_ERR_INVALID_ARG for negative sizes, a bad dtype or a NULL
+ * required pointer,
  * SCAN_ERR_UNSUPPORTED for C > 2^31 - 1, SCAN_ERR_CUDA if the launch fails.
  * Asynchronous on `stream`; no workspace, no allocation. */
-scan_status rglru_fwd(const float* x, const float* gate_a, const float* gate_x,
+scan_status rglru_fwd(const void* x, const void* gate_a, const void* gate_x,
                       const float* a_param, const int32_t* segment_pos, const float* h0,
-                      float* h, int64_t B, int64_t C, int64_t T, cudaStream_t stream);
+                      float* h, int64_t B, int64_t C, int64_t T, scan_dtype dt,
+                      cudaStream_t stream);
 
 /* Its backward for L = sum_t dh_t h_t, recomputing the gate terms from the
  * logits (the same page: backward recomputation of the pointwise terms, the
@@ -357,14 +361,15 @@ scan_status rglru_fwd(const float* x, const float* gate_a, const float* gate_x,
  *   da_param[c] = sigmoid(-a_param[c]) sum_{b,t} a_t dL/da_t 8 r_t,
  *   dh0 = a_0 g_0; a reset step has dgate_a = 0 and m = 1.
  *   h: the forward's output for the same inputs; dh: fp32 [B, C, T];
- *   dx, dgate_a, dgate_x: fp32 [B, C, T]; da_param: fp32 [C], written (not
+ *   dx, dgate_a, dgate_x: [B, C, T] of dtype dt (bf16 rounded to nearest from
+ *   the fp32 results); da_param: fp32 [C], written (not
  *   accumulated), summed over b and t in a fixed order; dh0: [B, C] or NULL.
  * Errors as for rglru_fwd. Asynchronous on `stream`; no workspace. */
-scan_status rglru_bwd(const float* x, const float* gate_a, const float* gate_x,
+scan_status rglru_bwd(const void* x, const void* gate_a, const void* gate_x,
                       const float* a_param, const int32_t* segment_pos, const float* h0,
-                      const float* h, const float* dh, float* dx, float* dgate_a,
-                      float* dgate_x, float* da_param, float* dh0, int64_t B, int64_t C,
-                      int64_t T, cudaStream_t stream);
+                      const float* h, const float* dh, void* dx, void* dgate_a,
+                      void* dgate_x, float* da_param, float* dh0, int64_t B, int64_t C,
+                      int64_t T, scan_dtype dt, cudaStream_t stream);
 
 /* One training step of dense rows (scan_fwd then scan_bwd, reverse = 0) whose
  * inputs and results are in host memory ([AST] the scan and its reversed-scan

@@ -216,22 +216,25 @@ def test_copy_rejects_bad_arguments_on_the_host(built):
 
 
 def test_rglru_rejects_bad_arguments_on_the_host(built):
-    """rglru_fwd / rglru_bwd check sizes and required pointers before any CUDA
-    call (the pointers here are placeholders that are never dereferenced)."""
+    """rglru_fwd / rglru_bwd check sizes, dtype and required pointers before any
+    CUDA call (the pointers here are placeholders that are never dereferenced)."""
     import associative_affine_scan_gb300 as scan
     L = scan.lib()
     p = 4096
+    f32, bf16 = scan.SCAN_F32, scan.SCAN_BF16
     fwd, bwd = L.rglru_fwd, L.rglru_bwd
-    assert fwd(p, p, p, p, None, None, p, -1, 2, 3, None) == scan.SCAN_ERR_INVALID_ARG
-    assert fwd(p, p, p, p, None, None, p, 1, 2, 0, None) == scan.SCAN_OK  # nothing to do
-    assert fwd(None, p, p, p, None, None, p, 1, 2, 3, None) == scan.SCAN_ERR_INVALID_ARG
-    assert fwd(p, p, p, None, None, None, p, 1, 2, 3, None) == scan.SCAN_ERR_INVALID_ARG
-    assert fwd(p, p, p, p, None, None, None, 1, 2, 3, None) == scan.SCAN_ERR_INVALID_ARG
-    assert fwd(p, p, p, p, None, None, p, 1, 1 << 31, 3, None) == scan.SCAN_ERR_UNSUPPORTED
+    assert fwd(p, p, p, p, None, None, p, -1, 2, 3, f32, None) == scan.SCAN_ERR_INVALID_ARG
+    assert fwd(p, p, p, p, None, None, p, 1, 2, 3, 7, None) == scan.SCAN_ERR_INVALID_ARG
+    assert fwd(p, p, p, p, None, None, p, 1, 2, 0, bf16, None) == scan.SCAN_OK  # nothing to do
+    assert fwd(None, p, p, p, None, None, p, 1, 2, 3, f32, None) == scan.SCAN_ERR_INVALID_ARG
+    assert fwd(p, p, p, None, None, None, p, 1, 2, 3, f32, None) == scan.SCAN_ERR_INVALID_ARG
+    assert fwd(p, p, p, p, None, None, None, 1, 2, 3, f32, None) == scan.SCAN_ERR_INVALID_ARG
+    assert fwd(p, p, p, p, None, None, p, 1, 1 << 31, 3, f32, None) == scan.SCAN_ERR_UNSUPPORTED
     args = [p] * 13
-    assert bwd(*args, 1, 2, -3, None) == scan.SCAN_ERR_INVALID_ARG
-    assert bwd(*args, 1, 0, 3, None) == scan.SCAN_OK  # no channels: nothing to write
+    assert bwd(*args, 1, 2, -3, f32, None) == scan.SCAN_ERR_INVALID_ARG
+    assert bwd(*args, 1, 2, 3, 7, None) == scan.SCAN_ERR_INVALID_ARG
+    assert bwd(*args, 1, 0, 3, f32, None) == scan.SCAN_OK  # no channels: nothing to write
     for i in (0, 1, 2, 3, 6, 7, 8, 9, 10, 11):  # the required pointers
         a = list(args)
         a[i] = None
-        assert bwd(*a, 1, 2, 3, None) == scan.SCAN_ERR_INVALID_ARG, i
+        assert bwd(*a, 1, 2, 3, f32, None) == scan.SCAN_ERR_INVALID_ARG, i

@@ -269,18 +269,20 @@ def test_guard_gdn(lib, S, D, T, heads):
 
 @pytest.mark.parametrize("T", [1, 3, 127, 128, 129, 4097])
 @pytest.mark.parametrize("shift", [0, 1])
-def test_guard_rglru(lib, T, shift):
-    """The RG-LRU forward's h and the backward's dx, dgate_a, dgate_x,
-    da_param and dh0, 16-byte aligned (vector path) and one element off."""
-    w = workloads.rglru(3, 5, T, seed=T + 3, docs=(1, 90), h0=True)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_guard_rglru(lib, T, shift, dtype):
+    """The RG-LRU forward's h and the backward's dx, dgate_a, dgate_x (in the
+    input dtype), da_param and dh0, 16-byte aligned (vector path) and one
+    element off."""
+    w = workloads.rglru(3, 5, T, seed=T + 3, docs=(1, 90), h0=True, dtype=dtype)
     x, ga, gx, ap, dh, seg, h0 = (t.to(DEV) for t in (w.x, w.gate_a, w.gate_x, w.a_param, w.dh,
                                                      w.segment_pos, w.h0))
     ref_h = lib.rglru_fwd(x, ga, gx, ap, seg, h0)
     ref = lib.rglru_bwd(x, ga, gx, ap, ref_h, dh, seg, h0)
     h = Guarded(x.shape, torch.float32, shift)
     lib.rglru_fwd(x, ga, gx, ap, seg, h0, out=h.t)
-    outs = (Guarded(x.shape, torch.float32, shift), Guarded(x.shape, torch.float32, shift),
-            Guarded(x.shape, torch.float32, shift), Guarded(ap.shape), Guarded(h0.shape))
+    outs = (Guarded(x.shape, dtype, shift), Guarded(x.shape, dtype, shift),
+            Guarded(x.shape, dtype, shift), Guarded(ap.shape), Guarded(h0.shape))
     lib.rglru_bwd(x, ga, gx, ap, ref_h, dh, seg, h0, out=tuple(g.t for g in outs))
     check_all([("h", h, ref_h)] +
               list(zip(("dx", "dgate_a", "dgate_x", "da_param", "dh0"), outs, ref)))

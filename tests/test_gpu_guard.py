@@ -267,6 +267,24 @@ def test_guard_gdn(lib, S, D, T, heads):
               list(zip(("dalpha", "db", "dv", "dc", "dh0"), outs, ref)), CONTRACTIONS)
 
 
+@pytest.mark.parametrize("T", [1, 64, 65, 300])
+@pytest.mark.parametrize("S,D", [(16, 32), (32, 32)])
+def test_guard_gdn_workspace(lib, T, S, D):
+    """Neither direction writes outside its gdn_workspace_bytes() bytes."""
+    B, H = 2, 3
+    w = workloads.gdn(B, H, T, S, D, seed=T + 8, h0=True)
+    alpha, b, v, c, dout, h0 = (t.to(DEV) for t in (w.alpha, w.b, w.v, w.c, w.dout, w.h0))
+    nb = lib.gdn_workspace_bytes(B, H, T, S, D)
+    assert nb % 16 == 0
+    ws = Guarded((nb // 4,))
+    o, ck = lib.gdn_fwd(alpha, b, v, c, h0, workspace=ws.t.view(torch.uint8))
+    lib.gdn_bwd(alpha, b, v, c, ck, dout, workspace=ws.t.view(torch.uint8))
+    torch.cuda.synchronize()
+    bits = ws.bits
+    assert not bool((bits[:ws.lo] != ws.word).any()), "written below the workspace"
+    assert not bool((bits[ws.lo + ws.n:] != ws.word).any()), "written above the workspace"
+
+
 @pytest.mark.parametrize("T", [1, 3, 127, 128, 129, 4097])
 @pytest.mark.parametrize("shift", [0, 1])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])

@@ -496,7 +496,7 @@ struct ChunkSmem {
   static constexpr int dsT = r1;               // [kL][LP]
   static constexpr int y = r1;                 // [kL][LP]
   static constexpr int r1_end = goutT + D * SP > r1 + kL * LP ? goutT + D * SP : r1 + kL * LP;
-  static constexpr int cb = r1_end;            // [kL][LP]: CB, then P
+  static constexpr int cb = r1_end;            // [kL][LP]: CB, then P^T
   static constexpr int dov = cb + kL * LP;     // [kL][LP]: DoV, then dS
   static constexpr int al = dov + kL * LP;     // kL + 4 gates (1 past the chunk's end)
   static constexpr int gam = al + kL + 4;      // Gamma_t
@@ -570,6 +570,7 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
   float* sgT = sm + SM::goutT;
   float* sdsT = sm + SM::dsT;
   float* scb = sm + SM::cb;
+  float* spT = sm + SM::cb;  // P^T, written over CB once CB is read
   float* sdv = sm + SM::dov;
   float* sy = sm + SM::y;
   float* sal = sm + SM::al;
@@ -823,37 +824,41 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
   }
   __syncthreads();
 
-  // ---- down each column tau: D[t][tau] for t >= tau; P and dS in place, dS^T
-  // (zero below its diagonal), dalpha_tau. Warp w takes 32 columns over one
-  // row quarter, starting from the product of the earlier quarters' gates. ----
+  // ---- down each column tau: D[t][tau] for t >= tau; dS in place, dS^T and
+  // P^T (zero below their diagonals), dalpha_tau. Warp w takes 32 columns over
+  // one row quarter, starting from the product of the earlier quarters' gates. ----
+  static_assert(kQ % 4 == 0, "whole 16-byte pieces of the transposed rows");
   {
     const int tau = 32 * (warp % kColW) + lane, q = warp / kColW, tq = kQ * q;
     float dec = 1.f;
     for (int i = 0; i < q; ++i) dec *= sqf[i * kL + tau];
     const float gm = sgm1[tau];
-    float acc = 0.f, dst[kQ];
+    float acc = 0.f, dst[kQ], pst[kQ];
 #pragma unroll
     for (int i = 0; i < kQ; ++i) {
       const int t = tq + i;
-      float* pc = scb + t * LP + tau;
       float* pd = sdv + t * LP + tau;
       if (t < tau) {
-        *pc = 0.f;
         *pd = 0.f;
-        dst[i] = 0.f;
+        dst[i] = pst[i] = 0.f;
       } else {
         if (t > tau) dec *= sal[t];
         const float ds = dec * *pd;
-        *pc = dec * *pc;
+        pst[i] = dec * scb[t * LP + tau];
         *pd = ds;
         dst[i] = ds;
         acc = fmaf(dec, fmaf(gm, sz[t], sy[t * LP + tau]), acc);
       }
     }
     sqa[q * kL + tau] = acc;
-    __syncthreads();  // every read of Y is done: dS^T takes its place
+    __syncthreads();  // every read of Y and CB is done: dS^T and P^T take their places
 #pragma unroll
-    for (int i = 0; i < kQ; ++i) sdsT[tau * LP + tq + i] = dst[i];
+    for (int i = 0; i < kQ; i += 4) {
+      *reinterpret_cast<float4*>(sdsT + tau * LP + tq + i) =
+          make_float4(dst[i], dst[i + 1], dst[i + 2], dst[i + 3]);
+      *reinterpret_cast<float4*>(spT + tau * LP + tq + i) =
+          make_float4(pst[i], pst[i + 1], pst[i + 2], pst[i + 3]);
+    }
   }
   __syncthreads();
   if (tid < kL) {
@@ -865,62 +870,104 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
     if (tau < n) p.dalpha[r0 + tau] = fmaf(swd[tau], fmaf(sgm1[tau], wtot, syv[tau]), acc);
   }
 
-  // ---- db = dS^T c + w o Gv, dv = P^T dout + w o Gb, dc = dS b + Gamma o HDo ----
+  // ---- db = dS^T c + w o Gv, dv = P^T dout + w o Gb, dc = dS b + Gamma o HDo.
+  // The sums run over t (db, dv) and tau (dc) four at a time, two terms per
+  // packed instruction: the rows of dS^T, P^T and dS give the pairs (16-byte
+  // reads), the columns of c, dout and b two single reads each. ----
   {
-    float adb[4][TNS], adv[4][TND], adc[4][TNS];
+    float2 adb[4][TNS], adv[4][TND];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float wd = swd[4 * ri + i], g = sgam[4 * ri + i];
+      const float wd = swd[4 * ri + i];
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) adb[i][j] = make_float2(wd * gv[i][j], 0.f);
+#pragma unroll
+      for (int j = 0; j < TND; ++j) adv[i][j] = make_float2(wd * gb[i][j], 0.f);
+    }
+    // the warp's rows tau are 8 w .. 8 w + 7, and dS^T[tau][t], P^T[tau][t]
+    // vanish for t < tau; rows past n are zero
+#pragma unroll 1
+    for (int t = 8 * warp; t < n; t += 4) {
+      float4 ds[4], pp[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ds[i] = *reinterpret_cast<const float4*>(sdsT + (4 * ri + i) * LP + t);
+        pp[i] = *reinterpret_cast<const float4*>(spT + (4 * ri + i) * LP + t);
+      }
+      float2 c01[TNS], c23[TNS], d01[TND], d23[TND];
 #pragma unroll
       for (int j = 0; j < TNS; ++j) {
-        adb[i][j] = wd * gv[i][j];
-        adc[i][j] = g * hdo[i][j];
+        const float* q = sc + t * SP + cj + 16 * j;
+        c01[j] = make_float2(q[0], q[SP]);
+        c23[j] = make_float2(q[2 * SP], q[3 * SP]);
       }
 #pragma unroll
-      for (int j = 0; j < TND; ++j) adv[i][j] = wd * gb[i][j];
-    }
-    // the warp's rows are 8 w .. 8 w + 7; dS[t][tau] and P[t][tau] vanish for t < tau
-#pragma unroll 2
-    for (int t = 8 * warp; t < n; ++t) {
-      const float4 ds = *reinterpret_cast<const float4*>(sdv + t * LP + 4 * ri);
-      const float4 pp = *reinterpret_cast<const float4*>(scb + t * LP + 4 * ri);
-      float cr[TNS], dr[TND];
-#pragma unroll
-      for (int j = 0; j < TNS; ++j) cr[j] = sc[t * SP + cj + 16 * j];
-#pragma unroll
-      for (int j = 0; j < TND; ++j) dr[j] = sdo[t * DP + cj + 16 * j];
+      for (int j = 0; j < TND; ++j) {
+        const float* q = sdo + t * DP + cj + 16 * j;
+        d01[j] = make_float2(q[0], q[DP]);
+        d23[j] = make_float2(q[2 * DP], q[3 * DP]);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
 #pragma unroll
-        for (int j = 0; j < TNS; ++j) adb[i][j] = fmaf(f4(ds, i), cr[j], adb[i][j]);
+        for (int j = 0; j < TNS; ++j) {
+          adb[i][j] = ffma2(make_float2(ds[i].x, ds[i].y), c01[j], adb[i][j]);
+          adb[i][j] = ffma2(make_float2(ds[i].z, ds[i].w), c23[j], adb[i][j]);
+        }
 #pragma unroll
-        for (int j = 0; j < TND; ++j) adv[i][j] = fmaf(f4(pp, i), dr[j], adv[i][j]);
+        for (int j = 0; j < TND; ++j) {
+          adv[i][j] = ffma2(make_float2(pp[i].x, pp[i].y), d01[j], adv[i][j]);
+          adv[i][j] = ffma2(make_float2(pp[i].z, pp[i].w), d23[j], adv[i][j]);
+        }
       }
-    }
-    // dS^T[tau][t] vanishes for tau > t
-    const int thi = 8 * warp + 8 < n ? 8 * warp + 8 : n;
-#pragma unroll 2
-    for (int tau = 0; tau < thi; ++tau) {
-      const float4 a = *reinterpret_cast<const float4*>(sdsT + tau * LP + 4 * ri);
-      float br[TNS];
-#pragma unroll
-      for (int j = 0; j < TNS; ++j) br[j] = sb[tau * SP + cj + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < TNS; ++j) adc[i][j] = fmaf(f4(a, i), br[j], adc[i][j]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int m = 4 * ri + i;
       if (m < n) {
 #pragma unroll
-        for (int j = 0; j < TNS; ++j) {
-          __stcs(p.db + (r0 + m) * S + cj + 16 * j, adb[i][j]);
-          __stcs(p.dc + (r0 + m) * S + cj + 16 * j, adc[i][j]);
-        }
+        for (int j = 0; j < TNS; ++j) __stcs(p.db + (r0 + m) * S + cj + 16 * j, adb[i][j].x + adb[i][j].y);
 #pragma unroll
-        for (int j = 0; j < TND; ++j) __stcs(p.dv + (r0 + m) * D + cj + 16 * j, adv[i][j]);
+        for (int j = 0; j < TND; ++j) __stcs(p.dv + (r0 + m) * D + cj + 16 * j, adv[i][j].x + adv[i][j].y);
+      }
+    }
+  }
+  {
+    float2 adc[4][TNS];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float g = sgam[4 * ri + i];
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) adc[i][j] = make_float2(g * hdo[i][j], 0.f);
+    }
+    // dS[t][tau] vanishes for tau > t (the warp's rows t end at 8 w + 7)
+    const int thi = 8 * warp + 8 < n ? 8 * warp + 8 : n;
+#pragma unroll 1
+    for (int tau = 0; tau < thi; tau += 4) {
+      float4 a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(sdv + (4 * ri + i) * LP + tau);
+      float2 b01[TNS], b23[TNS];
+#pragma unroll
+      for (int j = 0; j < TNS; ++j) {
+        const float* q = sb + tau * SP + cj + 16 * j;
+        b01[j] = make_float2(q[0], q[SP]);
+        b23[j] = make_float2(q[2 * SP], q[3 * SP]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < TNS; ++j) {
+          adc[i][j] = ffma2(make_float2(a[i].x, a[i].y), b01[j], adc[i][j]);
+          adc[i][j] = ffma2(make_float2(a[i].z, a[i].w), b23[j], adc[i][j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = 4 * ri + i;
+      if (m < n) {
+#pragma unroll
+        for (int j = 0; j < TNS; ++j) __stcs(p.dc + (r0 + m) * S + cj + 16 * j, adc[i][j].x + adc[i][j].y);
       }
     }
   }

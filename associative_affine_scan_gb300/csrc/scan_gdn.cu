@@ -533,7 +533,7 @@ __device__ __forceinline__ void gemm_nt_block(const float* A, int ap, const floa
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < NJ; ++j) acc[i][j] = make_float2(0.f, 0.f);
-#pragma unroll 2
+#pragma unroll
   for (int kk = 0; kk < K; kk += 4) {
     float4 a[4], q[NJ];
 #pragma unroll
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
 #pragma unroll
       for (int j = 0; j < TND; ++j) ab[i][j] = make_float2(0.f, 0.f);
     }
-#pragma unroll 2
+#pragma unroll
     for (int d = 0; d < D; d += 4) {  // HDo[t][s] = sum_d dout[t][d] H_in[s][d]; Gv likewise
       float4 ad[4], av[4], qh[TNS], qg[TNS];
 #pragma unroll
@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
           ag[i][j] = dot4x2(av[i], qg[j], ag[i][j]);
         }
     }
-#pragma unroll 2
+#pragma unroll
     for (int s0 = 0; s0 < S; s0 += 4) {  // Gb[tau][d] = sum_s b[tau][s] G_out^T[d][s]
       float4 a[4], q[TND];
 #pragma unroll

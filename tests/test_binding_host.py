@@ -23,6 +23,17 @@ def _cpu(*shape, dtype=torch.float32):
     lambda: scan.affine_prefix_fwd(_cpu(1, 8, 2, 4, 4)),
     lambda: scan.gdn_fwd(_cpu(1, 2, 8), _cpu(1, 2, 8, 16), _cpu(1, 2, 8, 16), _cpu(1, 2, 8, 16)),
     lambda: scan.scan_fwd_noalloc(_cpu(1, 2, 8), _cpu(1, 2, 8)),
+    lambda: scan.scan_bidir_bwd(_cpu(2, 8), _cpu(2, 8), _cpu(2, 8), _cpu(2, 8), _cpu(2, 8),
+                                _cpu(2, 8), None, None, torch.tensor([0, 8], dtype=torch.int32)),
+    lambda: scan.scan_log_bwd(_cpu(1, 2, 8), _cpu(1, 2, 8), _cpu(1, 2, 8), _cpu(1, 2, 8)),
+    lambda: scan.affine_scan_bwd(_cpu(1, 8, 2, 4, 4), _cpu(1, 8, 2, 4, 4), _cpu(1, 8, 2, 4, 4)),
+    lambda: scan.affine_prefix_bwd(_cpu(1, 8, 2, 4, 4), _cpu(1, 8, 2, 4, 4), _cpu(1, 8, 2, 4, 4)),
+    lambda: scan.gdn_bwd(_cpu(1, 2, 8), _cpu(1, 2, 8, 16), _cpu(1, 2, 8, 16), _cpu(1, 2, 8, 16),
+                         _cpu(256), _cpu(1, 2, 8, 16)),
+    lambda: scan.rglru_fwd(_cpu(1, 2, 8), _cpu(1, 2, 8), _cpu(1, 2, 8), _cpu(2)),
+    lambda: scan.rglru_bwd(_cpu(1, 2, 8), _cpu(1, 2, 8), _cpu(1, 2, 8), _cpu(2), _cpu(1, 2, 8),
+                           _cpu(1, 2, 8)),
+    lambda: scan.scan_copy(_cpu(1024), _cpu(1024)),
 ])
 def test_cpu_tensors_are_refused(call):
     with pytest.raises(ValueError, match="CUDA tensor"):

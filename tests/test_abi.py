@@ -146,6 +146,57 @@ def test_host_side_checks_need_no_gpu():
     assert f(None, None, None, None, 0, None, 1, 0, 64, 0, 0, None, ws, 4096, None) == scan.SCAN_OK
 
 
+def test_gdn_host_checks_need_no_gpu():
+    """gdn_fwd / gdn_bwd reject malformed calls on the host (no launch, no GPU
+    needed), and the checkpoint and workspace sizes follow their layouts."""
+    import associative_affine_scan_gb300 as scan
+    fwd, bwd = _raw("gdn_fwd"), _raw("gdn_bwd")
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1004)  # not 16-byte aligned
+    ws = ctypes.c_void_p(0x100000)
+    B, H, T, S, D = 2, 3, 130, 32, 16
+    # one S x D state per 32 steps; the workspace holds one S x D matrix per
+    # 32-step chunk and the chunks' gate products (padded to 4 floats)
+    chunks = B * H * ((T + 31) // 32)
+    assert scan.gdn_checkpoint_bytes(B, H, T, S, D) == 4 * chunks * S * D
+    nws = scan.gdn_workspace_bytes(B, H, T, S, D)
+    assert nws == 4 * (chunks * S * D + (chunks + 3) // 4 * 4)
+    for s_, d_ in ((8, 16), (32, 64), (0, 16)):
+        assert scan.gdn_workspace_bytes(B, H, T, s_, d_) == 0
+        assert scan.gdn_checkpoint_bytes(B, H, T, s_, d_) == 0
+    assert scan.gdn_workspace_bytes(-1, H, T, S, D) == 0
+
+    def f(alpha=fake, b=fake, v=fake, c=fake, h0=None, o=fake, ck=fake, dims=(B, H, T, S, D),
+          w=ws, nw=nws):
+        return fwd(alpha, b, v, c, h0, o, ck, *dims, w, nw, None)
+
+    assert f(dims=(B, H, T, 8, 16)) == scan.SCAN_ERR_UNSUPPORTED
+    assert f(dims=(B, -1, T, S, D)) == scan.SCAN_ERR_INVALID_ARG
+    assert f(alpha=None) == scan.SCAN_ERR_INVALID_ARG
+    assert f(o=None) == scan.SCAN_ERR_INVALID_ARG
+    assert f(b=odd) == scan.SCAN_ERR_ALIGNMENT
+    assert f(h0=odd) == scan.SCAN_ERR_ALIGNMENT
+    assert f(w=None) == scan.SCAN_ERR_WORKSPACE
+    assert f(nw=nws - 16) == scan.SCAN_ERR_WORKSPACE
+    assert f(w=odd) == scan.SCAN_ERR_WORKSPACE
+    assert f(alpha=None, b=None, v=None, c=None, o=None, ck=None, dims=(B, H, 0, S, D)) == \
+        scan.SCAN_OK  # empty: nothing to launch
+
+    def g(ck=fake, dout=fake, db=fake, dh0=None, dims=(B, H, T, S, D), w=ws, nw=nws):
+        return bwd(fake, fake, fake, fake, ck, dout, fake, db, fake, fake, dh0, *dims, w, nw, None)
+
+    assert g(dims=(B, H, T, 16, 64)) == scan.SCAN_ERR_UNSUPPORTED
+    assert g(dims=(-1, H, T, S, D)) == scan.SCAN_ERR_INVALID_ARG
+    assert g(ck=None) == scan.SCAN_ERR_INVALID_ARG  # the forward's checkpoints are required
+    assert g(dout=None) == scan.SCAN_ERR_INVALID_ARG
+    assert g(db=odd) == scan.SCAN_ERR_ALIGNMENT
+    assert g(dh0=odd) == scan.SCAN_ERR_ALIGNMENT
+    assert g(w=None) == scan.SCAN_ERR_WORKSPACE
+    assert g(nw=nws - 16) == scan.SCAN_ERR_WORKSPACE
+    assert g(dims=(0, H, T, S, D)) == scan.SCAN_OK  # no heads: nothing to do
+    assert g(dims=(B, H, 0, S, D)) == scan.SCAN_OK  # no steps and no dh0: nothing to write
+
+
 def test_affine_envelope_rejected_on_host():
     import associative_affine_scan_gb300 as scan
     f = _raw("affine_scan_fwd")

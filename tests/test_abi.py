@@ -146,6 +146,80 @@ def test_host_side_checks_need_no_gpu():
     assert f(None, None, None, None, 0, None, 1, 0, 64, 0, 0, None, ws, 4096, None) == scan.SCAN_OK
 
 
+def test_backward_log_bidir_affine_host_checks_need_no_gpu():
+    """The other entry points reject malformed calls on the host too (bad
+    dtype, negative size, missing workspace, a missing required pointer,
+    misaligned block tensors), and an empty problem returns OK without a
+    launch."""
+    import associative_affine_scan_gb300 as scan
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1004)
+    ws = ctypes.c_void_p(0x100000)
+    big = 1 << 30
+    OK, INV, WS, AL = (scan.SCAN_OK, scan.SCAN_ERR_INVALID_ARG, scan.SCAN_ERR_WORKSPACE,
+                       scan.SCAN_ERR_ALIGNMENT)
+
+    # scan_bwd(a, h, dh, h0, cu, n, da, dx, dh0, B, C, T, dt, reverse, opts, ws, nws, stream)
+    bwd = _raw("scan_bwd")
+
+    def b1(a=fake, da=fake, dims=(1, 4, 64), dt=0, w=ws, nw=big):
+        return bwd(a, fake, fake, None, None, 0, da, fake, None, *dims, dt, 0, None, w, nw, None)
+
+    assert b1(dt=5) == INV
+    assert b1(dims=(1, -4, 64)) == INV
+    assert b1(w=None) == WS
+    assert b1(a=None) == INV
+    assert b1(da=None) == INV
+    assert b1(a=None, da=None, dims=(1, 4, 0)) == OK
+
+    # scan_bidir_fwd(af, xf, ar, xr, h0f, h0r, cu, n, hf, hr, B, C, T, dt, opts, ws, nws, stream)
+    bf = _raw("scan_bidir_fwd")
+    assert bf(fake, fake, fake, fake, None, None, None, 0, fake, fake, 1, 4, 64, 9, None, ws,
+              big, None) == INV
+    assert bf(fake, fake, None, fake, None, None, None, 0, fake, fake, 1, 4, 64, 0, None, ws,
+              big, None) == INV
+    assert bf(fake, fake, fake, fake, None, None, None, 0, fake, fake, 1, 4, 64, 0, None, None,
+              0, None) == WS
+    # scan_bidir_bwd(af, hf, dhf, h0f, ar, hr, dhr, h0r, cu, n, daf, dxf, dh0f, dar, dxr, dh0r,
+    #                B, C, T, dt, opts, ws, nws, stream)
+    bb = _raw("scan_bidir_bwd")
+    assert bb(fake, fake, fake, None, fake, fake, fake, None, None, 0, fake, fake, None, None,
+              fake, None, 1, 4, 64, 0, None, ws, big, None) == INV  # dar missing
+    assert bb(None, None, None, None, None, None, None, None, None, 0, None, None, None, None,
+              None, None, 1, 0, 64, 0, None, ws, big, None) == OK
+
+    # scan_log_fwd(la, lx, lh0, cu, n, h, B, C, T, reverse, opts, ws, nws, stream)
+    lf = _raw("scan_log_fwd")
+    assert lf(fake, fake, None, None, 0, None, 1, 4, 64, 0, None, ws, big, None) == INV
+    assert lf(fake, fake, None, None, 0, fake, -1, 4, 64, 0, None, ws, big, None) == INV
+    assert lf(fake, fake, None, None, 0, fake, 1, 4, 4096, 0, None, ws, 16, None) == WS
+    # scan_log_bwd(la, lx, h, dh, lh0, cu, n, dla, dlx, dlh0, B, C, T, reverse, opts, ws, nws, s)
+    lb = _raw("scan_log_bwd")
+    assert lb(fake, fake, fake, fake, None, None, 0, fake, None, None, 1, 4, 64, 0, None, ws,
+              big, None) == INV  # d log x missing
+    assert lb(None, None, None, None, None, None, 0, None, None, None, 1, 4, 0, 0, None, ws,
+              big, None) == OK
+
+    # affine_scan_bwd(A, H, dH, h0, dA, dB, dh0, B, T, N, k, v, opts, ws, nws, stream)
+    ab = _raw("affine_scan_bwd")
+    assert ab(fake, fake, fake, None, fake, fake, None, 1, 64, 4, 4, 3, None, ws, big, None) == \
+        scan.SCAN_ERR_UNSUPPORTED
+    assert ab(fake, fake, fake, None, fake, fake, None, 1, 64, 4, 4, 4, None, None, 0, None) == WS
+    assert ab(fake, fake, None, None, fake, fake, None, 1, 64, 4, 4, 4, None, ws, big, None) == INV
+    assert ab(fake, fake, fake, None, odd, fake, None, 1, 64, 4, 4, 4, None, ws, big, None) == AL
+    # affine_prefix_fwd(A, Abar, B, T, N, k, opts, ws, nws, stream)
+    pf = _raw("affine_prefix_fwd")
+    assert pf(fake, None, 1, 64, 4, 4, None, ws, big, None) == INV
+    assert pf(odd, fake, 1, 64, 4, 4, None, ws, big, None) == AL
+    assert pf(None, None, 1, 0, 4, 4, None, ws, big, None) == OK
+    # affine_prefix_bwd(A, Abar, dAbar, dA, accumulate, B, T, N, k, opts, ws, nws, stream)
+    pb = _raw("affine_prefix_bwd")
+    assert pb(fake, fake, fake, None, 0, 1, 64, 4, 4, None, ws, big, None) == INV
+    assert pb(fake, fake, fake, odd, 1, 1, 64, 4, 4, None, ws, big, None) == AL
+    assert pb(fake, fake, fake, fake, 0, 1, 64, 4, 5, None, ws, big, None) == \
+        scan.SCAN_ERR_UNSUPPORTED
+
+
 def test_gdn_host_checks_need_no_gpu():
     """gdn_fwd / gdn_bwd reject malformed calls on the host (no launch, no GPU
     needed), and the checkpoint and workspace sizes follow their layouts."""

@@ -627,11 +627,24 @@ __global__ void __launch_bounds__(kBwdThreads, 160 / kL) gdn_bwd_chunk_kernel(co
   __syncthreads();
   {
     float win = 0.f;
-    for (int e = tid; e < S * D; e += NT) {
-      const int s_ = e / D, d = e - s_ * D;
-      const float g = sg[s_ * DP + d];
-      sgT[d * SP + s_] = g;
-      win = fmaf(sh[s_ * DP + d], g, win);
+    if constexpr (S == 32 && D == 32 && SP == 36 && DP == 36 && NT == 128) {
+      // by diagonals: lane l takes row l, column (l + k) mod 32, so the reads
+      // (bank 5 l + k) and the transposed writes (bank 5 l + 4 k) are free of
+      // bank conflicts; warp w takes the diagonals k = 8 w .. 8 w + 7
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int s_ = lane, d = (lane + 8 * warp + it) & 31;
+        const float g = sg[s_ * DP + d];
+        sgT[d * SP + s_] = g;
+        win = fmaf(sh[s_ * DP + d], g, win);
+      }
+    } else {
+      for (int e = tid; e < S * D; e += NT) {
+        const int s_ = e / D, d = e - s_ * D;
+        const float g = sg[s_ * DP + d];
+        sgT[d * SP + s_] = g;
+        win = fmaf(sh[s_ * DP + d], g, win);
+      }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) win += __shfl_xor_sync(kFullMask, win, o);

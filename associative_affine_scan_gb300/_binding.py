@@ -197,7 +197,10 @@ def _opts(opts) -> Optional[ScanOpts]:
     if isinstance(opts, ScanOpts):
         return opts
     o = ScanOpts()
+    known = {name for name, _ in ScanOpts._fields_}
     for k, v in dict(opts).items():
+        if k not in known:  # a ctypes structure would keep a misspelt name as a plain attribute
+            raise ValueError(f"unknown scan option {k!r}; options are {sorted(known)}")
         if k == "cu_seqlens_host":
             arr = (ctypes.c_int32 * len(v))(*[int(e) for e in v])
             o._keep = arr  # keep the host copy alive for the call

@@ -50,3 +50,14 @@ def test_missing_library_raises(monkeypatch):
     monkeypatch.setattr(_binding, "LIB_PATH", _binding.LIB_PATH + ".absent")
     with pytest.raises(ImportError, match="missing"):
         _binding.lib()
+
+
+def test_unknown_options_are_refused():
+    """A misspelt option name raises instead of leaving the planner's choice
+    in place; the known names set the structure's fields."""
+    with pytest.raises(ValueError, match="unknown scan option 'chunks'"):
+        _binding._opts({"chunks": 256})
+    o = _binding._opts({"chunk": 256, "rows_per_cta": 2, "variant": scan.SCAN_VARIANT_LOOKBACK,
+                        "wait_limit_s": 0.5, "cu_seqlens_host": [0, 3, 8]})
+    assert (o.chunk, o.rows_per_cta, o.variant, o.wait_limit_s) == (256, 2, scan.SCAN_VARIANT_LOOKBACK, 0.5)
+    assert [o.cu_seqlens_host[i] for i in range(3)] == [0, 3, 8]
